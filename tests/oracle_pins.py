@@ -1,0 +1,274 @@
+"""Pins for the fp64 oracle: checks against what the pages and the mathematics fix.
+
+Each ``pin_*`` takes a loaded oracle library (the real one, or a copy with a
+planted mistake) and raises AssertionError when the oracle disagrees with:
+
+* values worked by hand from the recurrence (``golden/hand_worked.json``);
+* closed forms (final state phi(K)^T V; the geometric sum for a constant gamma;
+  the L = 1 case; one-hot queries and keys; orthonormal keys);
+* library routines for the pieces (torch ELU for phi, numpy logaddexp for
+  softplus, numpy QR for orthonormal keys);
+* equalities the pages check themselves: chunkwise == recurrent for
+  C in {1, 4, 7, L} at L = 13, d = 6 ("Linear / Sparse Attention - minimal
+  runnable implementation", checks [a], [b], [c]); parallel == recurrent ==
+  chunked at n = 300, d = 16, chunk 64, and gated parallel == gated recurrent
+  at n = 200, d = 16, gamma = sigmoid(k.w + 3) ("CS336 lecture 4, code 1:
+  linear attention", demo_two_forms and demo_gating);
+* the resume invariant: running [0, m) then [m, L) from the carried state
+  equals one run over [0, L).
+
+``tests/test_oracle_mutants.py`` plants plausible mistakes in a copy of the
+oracle's C source and checks that at least one pin fails for each.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_worked.json")
+FORMS = ("recurrent", "parallel", "chunk1", "chunk2", "chunk7")
+
+
+def _run(form, lib, *args, **kw):
+    if form == "recurrent":
+        return oracle.recurrent(*args, lib=lib, **kw)
+    if form == "parallel":
+        return oracle.parallel(*args, lib=lib, **kw)
+    return oracle.chunkwise(*args, chunk=int(form[5:]), lib=lib, **kw)
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} != {b.shape}"
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    scale = max(1.0, np.max(np.abs(b)) if b.size else 1.0)
+    assert err <= tol * scale, f"{what}: max |diff| {err:.3e} > {tol:.1e} x {scale:.3g}"
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _elu1(x):
+    """phi via torch's ELU (alpha = 1), a library routine independent of the oracle."""
+    return (torch.nn.functional.elu(torch.as_tensor(x, dtype=torch.float64)) + 1.0).numpy()
+
+
+# --------------------------------------------------------------------------
+def pin_golden(lib):
+    """Hand-worked values (golden/hand_worked.json) for every form."""
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    decays = {
+        "plain_additive": None,
+        "constant_decay_half": [math.log(0.5)],
+        "token_gate_elu1_with_S0": [math.log(0.5), math.log(0.25)],
+        "gate_logits_softplus": [0.0, math.log(3.0)],
+    }
+    for c in cases:
+        q, k, v = (np.array(c[x], dtype=np.float64) for x in ("q", "k", "v"))
+        S0 = None if c["S0"] is None else np.array(c["S0"], dtype=np.float64)
+        dec = decays[c["name"]]
+        for form in FORMS:
+            O, S = _run(form, lib, q, k, v, phi=c["phi"], decay_kind=c["decay_kind"],
+                        decay=None if dec is None else np.array(dec), S0=S0)
+            _close(O, c["O"], 1e-12, f"{c['name']}/{form} O")
+            _close(S, c["S_final"], 1e-12, f"{c['name']}/{form} S_final")
+
+
+def pin_closed_form_additive(lib):
+    """No decay, S0 = 0: S_final = phi(K)^T V, and the last output row is
+    phi(q_{L-1})^T S_final -- the associativity (QK^T)V = Q(K^T V) on the
+    whole sequence."""
+    r = _rng(1)
+    B, H, L, dk, dv = 2, 3, 37, 5, 4
+    q, k, v = r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dv))
+    for phi in ("identity", "elu1"):
+        kf = k if phi == "identity" else _elu1(k)
+        qf = q if phi == "identity" else _elu1(q)
+        S_ref = np.einsum("bhti,bhtj->bhij", kf, v)
+        for form in ("recurrent", "parallel", "chunk7"):
+            O, S = _run(form, lib, q, k, v, phi=phi)
+            _close(S, S_ref, 1e-12, f"additive S_final {phi}/{form}")
+            _close(O[:, :, -1], np.einsum("bhi,bhij->bhj", qf[:, :, -1], S_ref), 1e-12,
+                   f"additive last row {phi}/{form}")
+
+
+def pin_closed_form_constant_decay(lib):
+    """Constant per-head gamma_h (distinct per head):
+    S_final = gamma^L S0 + sum_t gamma^(L-1-t) k_t v_t^T."""
+    r = _rng(2)
+    B, H, L, dk, dv = 2, 4, 29, 3, 5
+    q, k, v = r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dv))
+    S0 = r.normal(size=(B, H, dk, dv))
+    gam = np.array([0.5, 0.9, 0.97, 0.75])
+    w = gam[None, :, None] ** (L - 1 - np.arange(L))[None, None, :]      # [1,H,L]
+    S_ref = (gam ** L)[None, :, None, None] * S0 + np.einsum("ht,bhti,bhtj->bhij", w[0], k, v)
+    for form in ("recurrent", "parallel", "chunk7"):
+        _, S = _run(form, lib, q, k, v, decay_kind="head", decay=np.log(gam), S0=S0)
+        _close(S, S_ref, 1e-12, f"constant-decay S_final/{form}")
+
+
+def pin_single_token(lib):
+    """L = 1: o = alpha phi(q)^T S0 + (phi(q).phi(k)) v, S = alpha S0 + phi(k) v^T."""
+    r = _rng(3)
+    dk, dv = 4, 3
+    q, k, v = r.normal(size=(1, dk)), r.normal(size=(1, dk)), r.normal(size=(1, dv))
+    S0 = r.normal(size=(dk, dv))
+    la = np.array([math.log(0.8)])
+    qf, kf = _elu1(q[0]), _elu1(k[0])
+    o_ref = 0.8 * (qf @ S0) + (qf @ kf) * v[0]
+    S_ref = 0.8 * S0 + np.outer(kf, v[0])
+    for form in FORMS:
+        O, S = _run(form, lib, q, k, v, phi="elu1", decay_kind="token", decay=la, S0=S0)
+        _close(O[0], o_ref, 1e-12, f"L=1 o/{form}")
+        _close(S, S_ref, 1e-12, f"L=1 S/{form}")
+
+
+def pin_one_hot(lib):
+    """One-hot q_t = e_{j_t}, k_t = e_{i_t} (identity phi, per-token decay):
+    o_t = sum over s <= t with i_s == j_t of exp(c_t - c_s) v_s, plus
+    exp(c_t) S0[j_t, :], where c is the running sum of log alpha.  Computed
+    by index selection alone, no dot products."""
+    r = _rng(4)
+    L, d, dv = 23, 4, 3
+    jq, ik = r.integers(0, d, size=L), r.integers(0, d, size=L)
+    q, k = np.eye(d)[jq], np.eye(d)[ik]
+    v = r.normal(size=(L, dv))
+    la = np.log(r.uniform(0.5, 1.0, size=L))
+    S0 = r.normal(size=(d, dv))
+    c = np.cumsum(la)
+    O_ref = np.zeros((L, dv))
+    for t in range(L):
+        O_ref[t] = math.exp(c[t]) * S0[jq[t]]
+        for s in range(t + 1):
+            if ik[s] == jq[t]:
+                O_ref[t] += math.exp(c[t] - c[s]) * v[s]
+    for form in FORMS:
+        O, _ = _run(form, lib, q, k, v, decay_kind="token", decay=la, S0=S0)
+        _close(O, O_ref, 1e-12, f"one-hot/{form}")
+
+
+def pin_orthonormal_keys(lib):
+    """Identity phi, no decay, L = d orthonormal keys (numpy QR): the state
+    maps each key to its value, k_i^T S = v_i^T."""
+    r = _rng(5)
+    d, dv = 6, 4
+    Qm, _ = np.linalg.qr(r.normal(size=(d, d)))
+    K = Qm.T
+    V = r.normal(size=(d, dv))
+    Q = r.normal(size=(d, d))
+    for form in FORMS:
+        _, S = _run(form, lib, Q, K, V)
+        _close(K @ S, V, 1e-12, f"orthonormal keys/{form}")
+
+
+def pin_chunk_invariance(lib):
+    """chunkwise == recurrent for C in {1, 4, 7, L} at L = 13, d = 6, for every
+    phi / decay / S0 combination, plus C = 64 at L = 300 with a ragged tail."""
+    r = _rng(6)
+    B, H, L, d = 1, 2, 13, 6
+    q, k, v = r.normal(size=(B, H, L, d)), r.normal(size=(B, H, L, d)), r.normal(size=(B, H, L, d))
+    S0 = r.normal(size=(B, H, d, d))
+    variants = [("identity", "none", None, None), ("elu1", "none", None, S0),
+                ("identity", "head", np.log([0.9, 0.6]), S0),
+                ("elu1", "token", np.log(r.uniform(0.3, 1.0, size=(B, H, L))), S0),
+                ("identity", "logit", r.normal(size=(B, H, L)) * 3.0, S0)]
+    for phi, kind, dec, s0 in variants:
+        O_ref, S_ref = oracle.recurrent(q, k, v, phi=phi, decay_kind=kind, decay=dec, S0=s0, lib=lib)
+        for C in (1, 4, 7, L):
+            O, S = oracle.chunkwise(q, k, v, C, phi=phi, decay_kind=kind, decay=dec, S0=s0, lib=lib)
+            _close(O, O_ref, 1e-11, f"chunk C={C} {phi}/{kind} O")
+            _close(S, S_ref, 1e-11, f"chunk C={C} {phi}/{kind} S")
+    q, k, v = r.normal(size=(300, 16)), r.normal(size=(300, 16)), r.normal(size=(300, 16))
+    O_ref, S_ref = oracle.recurrent(q, k, v, lib=lib)
+    O, S = oracle.chunkwise(q, k, v, 64, lib=lib)
+    _close(O, O_ref, 1e-11, "chunk 64 ragged O")
+    _close(S, S_ref, 1e-11, "chunk 64 ragged S")
+
+
+def pin_parallel_equals_recurrent(lib):
+    """The page's two demos: parallel == recurrent == chunked (n = 300, d = 16,
+    chunk 64) and gated parallel == gated recurrent (n = 200, d = 16,
+    gamma_t = sigmoid(k_t . w + 3), given here as log gamma_t)."""
+    g = torch.Generator().manual_seed(0)
+    n, d = 300, 16
+    q, k, v = (torch.randn(n, d, generator=g, dtype=torch.float64) for _ in range(3))
+    Op, _ = oracle.parallel(q, k, v, lib=lib)
+    Or, _ = oracle.recurrent(q, k, v, lib=lib)
+    Oc, _ = oracle.chunkwise(q, k, v, 64, lib=lib)
+    _close(Op, Or, 1e-11, "parallel vs recurrent")
+    _close(Oc, Or, 1e-11, "chunked vs recurrent")
+    n = 200
+    q, k, v = (torch.randn(n, d, generator=g, dtype=torch.float64) for _ in range(3))
+    w = torch.randn(d, generator=g, dtype=torch.float64)
+    log_gamma = torch.nn.functional.logsigmoid(k @ w + 3.0)
+    Op, Sp = oracle.parallel(q, k, v, decay_kind="token", decay=log_gamma, lib=lib)
+    Or, Sr = oracle.recurrent(q, k, v, decay_kind="token", decay=log_gamma, lib=lib)
+    _close(Op, Or, 1e-11, "gated parallel vs recurrent O")
+    _close(Sp, Sr, 1e-11, "gated parallel vs recurrent S")
+
+
+def pin_split_invariance(lib):
+    """Resume: run [0, m), then [m, L) from the carried state == one run."""
+    r = _rng(7)
+    B, H, L, dk, dv = 2, 2, 50, 4, 5
+    q, k, v = r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dv))
+    g = r.normal(size=(B, H, L))
+    S0 = r.normal(size=(B, H, dk, dv))
+    for form in ("recurrent", "parallel", "chunk7"):
+        O, S = _run(form, lib, q, k, v, phi="elu1", decay_kind="logit", decay=g, S0=S0)
+        for m in (1, 17, 49):
+            O1, S1 = _run(form, lib, q[:, :, :m], k[:, :, :m], v[:, :, :m], phi="elu1",
+                          decay_kind="logit", decay=g[:, :, :m], S0=S0)
+            O2, S2 = _run(form, lib, q[:, :, m:], k[:, :, m:], v[:, :, m:], phi="elu1",
+                          decay_kind="logit", decay=g[:, :, m:], S0=S1)
+            _close(np.concatenate([O1, O2], axis=2), O, 1e-11, f"split m={m}/{form} O")
+            _close(S2, S, 1e-11, f"split m={m}/{form} S")
+
+
+def pin_library_pieces(lib):
+    """phi = elu + 1 equals torch's ELU + 1 applied beforehand with phi = id;
+    gate logits equal per-token log alpha = -logaddexp(0, g) (numpy); a
+    gamma of exactly 1 equals no decay; L = 0 returns S0 unchanged."""
+    r = _rng(8)
+    B, H, L, dk, dv = 1, 2, 31, 5, 3
+    q, k, v = r.normal(size=(B, H, L, dk)) * 2, r.normal(size=(B, H, L, dk)) * 2, r.normal(size=(B, H, L, dv))
+    g = r.normal(size=(B, H, L)) * 4
+    S0 = r.normal(size=(B, H, dk, dv))
+    for form in ("recurrent", "parallel", "chunk7"):
+        O1, S1 = _run(form, lib, q, k, v, phi="elu1")
+        O2, S2 = _run(form, lib, _elu1(q), _elu1(k), v, phi="identity")
+        _close(O1, O2, 1e-12, f"elu1 vs torch ELU/{form}")
+        _close(S1, S2, 1e-12, f"elu1 vs torch ELU S/{form}")
+        O1, S1 = _run(form, lib, q, k, v, decay_kind="logit", decay=g, S0=S0)
+        O2, S2 = _run(form, lib, q, k, v, decay_kind="token", decay=-np.logaddexp(0.0, g), S0=S0)
+        _close(O1, O2, 1e-12, f"logit vs token/{form}")
+        _close(S1, S2, 1e-12, f"logit vs token S/{form}")
+        O1, S1 = _run(form, lib, q, k, v, decay_kind="head", decay=np.zeros(H), S0=S0)
+        O2, S2 = _run(form, lib, q, k, v, S0=S0)
+        _close(O1, O2, 0.0, f"gamma=1/{form}")
+        _close(S1, S2, 0.0, f"gamma=1 S/{form}")
+        O, S = _run(form, lib, q[:, :, :0], k[:, :, :0], v[:, :, :0], S0=S0)
+        assert O.shape == (B, H, 0, dv)
+        _close(S, S0, 0.0, f"L=0 state/{form}")
+
+
+def pin_state_shape(lib):
+    """The state is [d_k, d_v] whatever L is (page 1, check [c])."""
+    r = _rng(9)
+    for L in (1, 13, 300):
+        q, k, v = r.normal(size=(L, 6)), r.normal(size=(L, 6)), r.normal(size=(L, 4))
+        _, S = oracle.recurrent(q, k, v, lib=lib)
+        assert S.shape == (6, 4), S.shape
+
+
+PINS = [pin_golden, pin_closed_form_additive, pin_closed_form_constant_decay, pin_single_token,
+        pin_one_hot, pin_orthonormal_keys, pin_chunk_invariance, pin_parallel_equals_recurrent,
+        pin_split_invariance, pin_library_pieces, pin_state_shape]
