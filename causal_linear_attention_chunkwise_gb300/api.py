@@ -1,0 +1,159 @@
+"""Python binding of the C ABI, with the same names.  Argument marshalling only:
+tensors become device pointers, torch supplies output memory and the current
+CUDA stream, and every step of the computation runs in the library's kernels.
+
+Host (CPU) tensors are accepted too: they are copied to the current device,
+the same kernels run, and the outputs are copied back (this is the
+end-to-end path the benchmark times with host buffers).
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+
+PHI = {"identity": 0, "elu1": 1}
+DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+DECAY = {"none": 0, "head": 1, "token": 2, "logit": 3}
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_DEVICE_TIMEOUT = range(5)
+
+
+class LAError(RuntimeError):
+    """A non-zero la_status, with the library's message."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"la_status {status}: {message}")
+        self.status = status
+
+
+def _check(status: int):
+    if status != LA_OK:
+        raise LAError(status, _native.load().la_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("expected CUDA tensors")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("expected contiguous tensors")
+
+
+def la_set_feature_map(phi) -> None:
+    """Select phi ("identity" | "elu1" or 0 | 1) for all later calls."""
+    _check(_native.load().la_set_feature_map(PHI.get(phi, phi)))
+
+
+def la_get_feature_map() -> int:
+    return _native.load().la_get_feature_map()
+
+
+def la_chunk_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk=64, dtype=torch.bfloat16) -> int:
+    return int(_native.load().la_chunk_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk,
+                                                           DTYPE[dtype]))
+
+
+def la_chunk_fwd_kernel_count(B, H, L, d_k, d_v, chunk=64, dtype=torch.bfloat16) -> int:
+    return int(_native.load().la_chunk_fwd_kernel_count(B, H, L, d_k, d_v, chunk, DTYPE[dtype]))
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes, device):
+    if nbytes == 0:
+        return None
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def la_chunk_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, O=None,
+                 S_final=None, want_final_state=True, workspace=None, stream=None):
+    """Chunkwise causal linear attention over [B,H,L,d] sequences.
+
+    Returns ``(O, S_final)`` (``S_final`` is None when ``want_final_state`` is
+    false and no buffer is given).  ``decay_kind``: "none" | "head" (decay =
+    fp32 [H] log gamma) | "token" (fp32 [B,H,L] log alpha) | "logit" (fp32
+    [B,H,L] gate logits g).  ``S0``: fp32 [B,H,d_k,d_v] or None.
+    """
+    if not q.is_cuda:
+        return _chunk_fwd_host(q, k, v, chunk, decay_kind, decay, S0, want_final_state)
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or v.dtype != q.dtype or k.dtype != q.dtype:
+        raise ValueError("q, k, v must agree in [B,H,L] and dtype")
+    if O is None:
+        O = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    if S_final is None and want_final_state:
+        S_final = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    _need_cuda(q, k, v, decay, S0, O, S_final)
+    lib = _native.load()
+    ws_need = la_chunk_fwd_workspace_bytes(B, H, L, dk, dv, chunk, q.dtype)
+    if workspace is None:
+        workspace = _workspace(ws_need, q.device)
+    _check(lib.la_chunk_fwd(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, chunk,
+        DECAY[decay_kind], _ptr(decay), _ptr(S0), _ptr(O), _ptr(S_final),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return O, S_final
+
+
+def _chunk_fwd_host(q, k, v, chunk, decay_kind, decay, S0, want_final_state):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    to = lambda t: None if t is None else t.to(dev, non_blocking=True)  # noqa: E731
+    O, Sf = la_chunk_fwd(to(q), to(k), to(v), chunk, decay_kind, to(decay), to(S0),
+                         want_final_state=want_final_state)
+    O_h = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+    O_h.copy_(O, non_blocking=True)
+    Sf_h = None
+    if Sf is not None:
+        Sf_h = torch.empty(Sf.shape, dtype=Sf.dtype, pin_memory=True)
+        Sf_h.copy_(Sf, non_blocking=True)
+    torch.cuda.current_stream().synchronize()
+    return O_h, Sf_h
+
+
+def la_decode_step(q, k, v, S, log_alpha=None, o=None, stream=None):
+    """One decode step: S <- alpha S + phi(k) v^T in place, returns o = phi(q)^T S.
+    q, k [B,H,d_k], v [B,H,d_v], S fp32 [B,H,d_k,d_v], log_alpha fp32 [B,H]."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    _need_cuda(q, k, v, S, log_alpha, o)
+    if S.dtype != torch.float32:
+        raise ValueError("the state S must be fp32")
+    _check(_native.load().la_decode_step(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, dk, dv, _ptr(log_alpha), _ptr(S),
+        _ptr(o), _stream(stream)))
+    return o
+
+
+def la_device_status(stream=None) -> None:
+    """Synchronise and raise LAError if a kernel's bounded wait timed out."""
+    _check(_native.load().la_device_status(_stream(stream)))
+
+
+def la_selftest_wait_timeout(spin_limit: int = 1000, stream=None) -> int:
+    """Run the timeout self-test kernel; returns the status it reports."""
+    lib = _native.load()
+    return lib.la_selftest_wait_timeout(spin_limit, _stream(stream))
+
+
+def la_last_error() -> str:
+    return _native.load().la_last_error().decode()

@@ -1,0 +1,204 @@
+// la_abi.cu -- the extern "C" boundary: argument validation, dispatch to the
+// kernel launchers, the process-wide feature map, error reporting.
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/la_gb300.h"
+#include "la_common.cuh"
+#include "la_internal.h"
+
+namespace la {
+
+__device__ unsigned int g_device_error;
+
+namespace {
+std::atomic<int> g_phi{LA_PHI_IDENTITY};
+thread_local char g_msg[512] = "";
+
+la_status fail(la_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+la_status ok() {
+  g_msg[0] = '\0';
+  return LA_OK;
+}
+
+la_status cuda_fail(cudaError_t e, const char *where) {
+  return fail(LA_ERR_CUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+const char *kernel_name(unsigned int id) {
+  switch (id) {
+    case KID_PREFILL_TC_STATE: return "prefill segment-state kernel";
+    case KID_PREFILL_TC_OUT: return "prefill chunk-output kernel";
+    case KID_SELFTEST: return "wait-timeout self-test kernel";
+    default: return "unknown kernel";
+  }
+}
+}  // namespace
+
+unsigned int *device_error_word() {
+  // The symbol's device address, looked up for the current device on each
+  // call (cheap; avoids caching an address across devices).
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<unsigned int *>(p);
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+la_status la_set_feature_map(int phi) {
+  if (phi != LA_PHI_IDENTITY && phi != LA_PHI_ELU1)
+    return fail(LA_ERR_INVALID_ARG, "la_set_feature_map: unknown feature map %d", phi);
+  g_phi.store(phi);
+  return ok();
+}
+
+int la_get_feature_map(void) { return g_phi.load(); }
+
+size_t la_chunk_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk, int dtype) {
+  PrefillArgs a{};
+  a.dtype = dtype; a.B = B; a.H = H; a.L = L; a.dk = d_k; a.dv = d_v; a.chunk = chunk;
+  if (B <= 0 || H <= 0 || L <= 0) return 0;
+  if (prefill_tc_supported(a)) return prefill_tc_workspace_bytes(B, H, L, d_k);
+  return 0;
+}
+
+int la_chunk_fwd_kernel_count(int B, int H, int L, int d_k, int d_v, int chunk, int dtype) {
+  if (B <= 0 || H <= 0 || L <= 0) return 0;
+  if ((dtype != LA_F32 && dtype != LA_BF16) || !supported_d(d_k) || !supported_d(d_v) ||
+      chunk < 1 || chunk > 64)
+    return 0;
+  PrefillArgs a{};
+  a.dtype = dtype; a.B = B; a.H = H; a.L = L; a.dk = d_k; a.dv = d_v; a.chunk = chunk;
+  if (prefill_tc_supported(a)) return prefill_tc_kernel_count(B, H, L, d_k);
+  return 1;
+}
+
+la_status la_chunk_fwd(const void *q, const void *k, const void *v, int dtype, int B, int H,
+                       int L, int d_k, int d_v, int chunk, int decay_kind, const float *decay,
+                       const float *S0, void *O, float *S_final, void *workspace,
+                       size_t ws_bytes, void *cuda_stream) {
+  if (dtype != LA_F32 && dtype != LA_BF16)
+    return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: unknown dtype %d", dtype);
+  if (B < 0 || H < 0 || L < 0 || d_k <= 0 || d_v <= 0 || chunk <= 0)
+    return fail(LA_ERR_INVALID_ARG,
+                "la_chunk_fwd: bad sizes B=%d H=%d L=%d d_k=%d d_v=%d chunk=%d", B, H, L, d_k,
+                d_v, chunk);
+  if (decay_kind < LA_DECAY_NONE || decay_kind > LA_DECAY_GATE_LOGIT)
+    return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: unknown decay kind %d", decay_kind);
+  if (!supported_d(d_k) || !supported_d(d_v))
+    return fail(LA_ERR_UNSUPPORTED, "la_chunk_fwd: d_k=%d d_v=%d not in {16,32,64,128}", d_k,
+                d_v);
+  if (chunk > 64)
+    return fail(LA_ERR_UNSUPPORTED, "la_chunk_fwd: chunk %d > 64 is not supported", chunk);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  const size_t state_bytes = (size_t)B * H * d_k * d_v * sizeof(float);
+  if ((size_t)B * H == 0) return ok();
+  if (L == 0) {  // nothing to attend to: the final state is the initial one
+    if (!S_final) return ok();
+    if (!aligned16(S_final) || (S0 && !aligned16(S0)))
+      return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: state pointers must be 16-byte aligned");
+    cudaError_t e = S0 ? (S0 == S_final ? cudaSuccess
+                                        : cudaMemcpyAsync(S_final, S0, state_bytes,
+                                                          cudaMemcpyDeviceToDevice, st))
+                       : cudaMemsetAsync(S_final, 0, state_bytes, st);
+    if (e != cudaSuccess) return cuda_fail(e, "la_chunk_fwd (L=0)");
+    return ok();
+  }
+  if (!q || !k || !v || !O)
+    return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: q, k, v and O must be non-null");
+  if (decay_kind != LA_DECAY_NONE && !decay)
+    return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: decay kind %d needs a decay pointer",
+                decay_kind);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(O) ||
+      (S0 && !aligned16(S0)) || (S_final && !aligned16(S_final)))
+    return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: tensors must start on a 16-byte boundary");
+
+  PrefillArgs a{q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(), decay_kind,
+                decay_kind == LA_DECAY_NONE ? nullptr : decay, S0, O, S_final,
+                workspace, ws_bytes, st};
+  if (prefill_tc_supported(a)) {
+    size_t need = prefill_tc_workspace_bytes(B, H, L, d_k);
+    if (need > 0 && (!workspace || ws_bytes < need))
+      return fail(LA_ERR_INVALID_ARG,
+                  "la_chunk_fwd: workspace of %zu bytes needed, %zu given", need,
+                  workspace ? ws_bytes : (size_t)0);
+    if (need > 0 && !aligned16(workspace))
+      return fail(LA_ERR_INVALID_ARG, "la_chunk_fwd: workspace must be 16-byte aligned");
+    const char *why = nullptr;
+    cudaError_t e = launch_prefill_tc(a, &why);
+    if (e != cudaSuccess) return cuda_fail(e, why ? why : "la_chunk_fwd (tcgen05 path)");
+    return ok();
+  }
+  cudaError_t e = launch_prefill_simt(a);
+  if (e != cudaSuccess) return cuda_fail(e, "la_chunk_fwd (SIMT path)");
+  return ok();
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, int dtype, int B, int H,
+                         int d_k, int d_v, const float *log_alpha, float *S, void *o,
+                         void *cuda_stream) {
+  if (dtype != LA_F32 && dtype != LA_BF16)
+    return fail(LA_ERR_INVALID_ARG, "la_decode_step: unknown dtype %d", dtype);
+  if (B < 0 || H < 0 || d_k <= 0 || d_v <= 0)
+    return fail(LA_ERR_INVALID_ARG, "la_decode_step: bad sizes B=%d H=%d d_k=%d d_v=%d", B, H,
+                d_k, d_v);
+  if (!decode_supported(d_k, d_v))
+    return fail(LA_ERR_UNSUPPORTED,
+                "la_decode_step: d_k=%d d_v=%d unsupported (need d_k = d_v in {16,32,64,128})",
+                d_k, d_v);
+  if ((size_t)B * H == 0) return ok();
+  if (!q || !k || !v || !S || !o)
+    return fail(LA_ERR_INVALID_ARG, "la_decode_step: q, k, v, S and o must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) || !aligned16(o))
+    return fail(LA_ERR_INVALID_ARG, "la_decode_step: tensors must start on a 16-byte boundary");
+  DecodeArgs a{q, k, v, dtype, B, H, d_k, d_v, g_phi.load(), log_alpha, S, o,
+               static_cast<cudaStream_t>(cuda_stream)};
+  cudaError_t e = launch_decode(a);
+  if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
+  return ok();
+}
+
+la_status la_device_status(void *cuda_stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  if (e != cudaSuccess) return cuda_fail(e, "la_device_status: stream synchronize");
+  unsigned int word = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "la_device_status: read error word");
+  if (word == 0) return ok();
+  e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e, "la_device_status: clear error word");
+  return fail(LA_ERR_DEVICE_TIMEOUT, "bounded wait timed out in %s (wait site %u)",
+              kernel_name(word & 0xffu), (word >> 8) & 0xffu);
+}
+
+la_status la_selftest_wait_timeout(unsigned int spin_limit, void *cuda_stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = launch_wait_timeout_selftest(spin_limit, st);
+  if (e != cudaSuccess) return cuda_fail(e, "la_selftest_wait_timeout: launch");
+  return la_device_status(cuda_stream);
+}
+
+const char *la_last_error(void) { return g_msg; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// la_internal.h -- launchers shared between the ABI translation unit and the
+// kernel translation units.  Host-only declarations; no device code.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace la {
+
+// Device error word set by kernels whose bounded waits run out.  Codes:
+// bits 0..7 kernel id, bits 8..15 wait site (see la_common.cuh).
+unsigned int *device_error_word();  // device address for the current device
+
+struct PrefillArgs {
+  const void *q, *k, *v;
+  int dtype;  // LA_F32 / LA_BF16
+  int B, H, L, dk, dv, chunk;
+  int phi;
+  int decay_kind;
+  const float *decay;
+  const float *S0;
+  void *O;
+  float *S_final;
+  void *workspace;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+
+struct DecodeArgs {
+  const void *q, *k, *v;
+  int dtype;
+  int B, H, dk, dv;
+  int phi;
+  const float *log_alpha;
+  float *S;
+  void *o;
+  cudaStream_t stream;
+};
+
+// General SIMT prefill (fp32 or bf16, 1 <= chunk <= 64, d <= 128).
+cudaError_t launch_prefill_simt(const PrefillArgs &a);
+
+// Tensor-core (tcgen05) prefill: bf16, chunk 64, dk == dv in {64, 128}.
+bool prefill_tc_supported(const PrefillArgs &a);
+size_t prefill_tc_workspace_bytes(int B, int H, int L, int d);
+int prefill_tc_kernel_count(int B, int H, int L, int d);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why);
+
+// Decode step.
+bool decode_supported(int dk, int dv);
+cudaError_t launch_decode(const DecodeArgs &a);
+
+// Self-test of the bounded-wait timeout path.
+cudaError_t launch_wait_timeout_selftest(unsigned int spin_limit, cudaStream_t s);
+
+}  // namespace la

@@ -1,0 +1,152 @@
+/*
+ * la_gb300.h -- C ABI of the GB300 (sm_103a) causal linear attention library.
+ *
+ * What the library computes.  For every (batch b, head h) sequence of L tokens
+ * with queries q_t, keys k_t (width d_k) and values v_t (width d_v), a matrix
+ * state S in R^{d_k x d_v} evolves as
+ *
+ *     S_t = a_t S_{t-1} + phi(k_t) v_t^T,        o_t = phi(q_t)^T S_t
+ *
+ * (update before read; S_{-1} = S0 or zero).  Sources:
+ *   - "Linear / Sparse Attention - minimal runnable implementation",
+ *     linear_attn_recurrent (the self-inclusive recurrence, S in R^{d_k x d_v})
+ *     and linear_attn_chunkwise (the chunk form the prefill kernels evaluate:
+ *     inter-chunk read Q_c S, intra-chunk ((Q_c K_c^T) .* tril) V_c with the
+ *     diagonal included, then S += K_c^T V_c; a ragged last chunk);
+ *   - "CS336 lecture 4, code 1: linear attention",
+ *     gated_linear_attention_recurrent (S_t = gamma_t S_{t-1} + k_t v_t^T;
+ *     constant gamma is RetNet, input-dependent gamma_t the Mamba-2 gate) and
+ *     gated_linear_attention_parallel (decay factors taken in log space);
+ *   - "Linear / sparse attention tutorial" section 6.2 (the two-part chunk
+ *     computation; gates multiply the state and the in-chunk mask by the
+ *     cumulative decay) and section 8.1 (decode keeps only the fixed-size
+ *     state);
+ *   - "adv13 - Linear Attention / SSM" section 3.2 / 4.2 (phi applied to q
+ *     and k, never to v) and Q1 (phi = elu + 1).
+ *
+ * Conventions for every entry point:
+ *   - Pointers to tensors are DEVICE pointers owned by the caller; the library
+ *     never frees them and never allocates device memory.  Tensors are dense,
+ *     row-major, contiguous, and must start on a 16-byte boundary.
+ *   - Calls are asynchronous on the CUDA stream passed as `cuda_stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).  The return status
+ *     covers argument validation and kernel launch; a device-side timeout of a
+ *     bounded wait is reported by la_device_status().
+ *   - No call aborts, throws or prints.  On any non-zero status the reason is
+ *     available from la_last_error() on the calling thread.
+ */
+#ifndef LA_GB300_H
+#define LA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int la_status;
+
+#define LA_OK                 0  /* success */
+#define LA_ERR_INVALID_ARG    1  /* bad pointer, size, alignment or enum value */
+#define LA_ERR_UNSUPPORTED    2  /* valid request this build has no kernel for */
+#define LA_ERR_CUDA           3  /* a CUDA runtime call or launch failed */
+#define LA_ERR_DEVICE_TIMEOUT 4  /* a kernel's bounded wait ran out (la_device_status) */
+
+/* Feature map phi applied to q and k. */
+#define LA_PHI_IDENTITY 0        /* phi(x) = x ("tutorial" 2.1: RetNet / GLA use phi = id) */
+#define LA_PHI_ELU1     1        /* phi(x) = elu(x) + 1 = x + 1 (x > 0), exp(x) (x <= 0) */
+
+/* Element type of q, k, v and of the outputs O / o.  The state is always fp32. */
+#define LA_F32  0
+#define LA_BF16 1
+
+/* How the per-token decay a_t is given (always in log space, fp32). */
+#define LA_DECAY_NONE       0   /* a_t = 1; decay pointer ignored (may be NULL)    */
+#define LA_DECAY_HEAD       1   /* decay[h] = log gamma_h, shape [H] (RetNet)      */
+#define LA_DECAY_TOKEN      2   /* decay[b,h,t] = log alpha_t, shape [B,H,L]       */
+#define LA_DECAY_GATE_LOGIT 3   /* decay[b,h,t] = g_t, alpha_t = exp(-softplus(g_t)),
+                                   shape [B,H,L] (Mamba-2-style input gate)       */
+
+/* Select phi for all later calls in this process (atomic; default identity).
+ * Returns LA_ERR_INVALID_ARG for an unknown value. */
+la_status la_set_feature_map(int phi);
+
+/* The feature map currently selected. */
+int la_get_feature_map(void);
+
+/* Bytes of device workspace la_chunk_fwd needs for this problem (0 if none).
+ * The workspace holds per-segment partial states when the sequence is split
+ * across CTAs; its contents need no initialisation and are not kept. */
+size_t la_chunk_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk,
+                                    int dtype);
+
+/* Number of kernel launches one la_chunk_fwd call makes for this problem
+ * (host-only query; 0 for an empty problem or an unsupported one). */
+int la_chunk_fwd_kernel_count(int B, int H, int L, int d_k, int d_v, int chunk, int dtype);
+
+/*
+ * Chunkwise-parallel causal linear attention over whole sequences (prefill).
+ *
+ *   q, k      [B,H,L,d_k]  dtype            (read)
+ *   v         [B,H,L,d_v]  dtype            (read)
+ *   dtype     LA_F32 or LA_BF16
+ *   chunk     chunk size C (tokens per chunk); the result does not depend on
+ *             it up to rounding.  The tensor-core path takes C = 64; the
+ *             fp32 / general path takes 1 <= C <= 64.
+ *   decay_kind / decay   see LA_DECAY_*; decay is fp32 device memory.
+ *   S0        [B,H,d_k,d_v] fp32 initial state, or NULL for zero   (read)
+ *   O         [B,H,L,d_v]   dtype, every row written                (write)
+ *   S_final   [B,H,d_k,d_v] fp32 state after the last token, or NULL
+ *             (write; may be the same buffer as S0)
+ *   workspace device scratch of at least la_chunk_fwd_workspace_bytes(...)
+ *             bytes (may be NULL when that is 0); ws_bytes = its size.
+ *
+ * Supported: d_k, d_v in {16, 32, 64, 128}; fp32 inputs run the fp32 SIMT
+ * kernel, bf16 inputs with d_k = d_v in {64, 128} and C = 64 run the tcgen05
+ * tensor-core kernels, other bf16 shapes the SIMT kernel.  L = 0 writes
+ * S_final = S0 (or zero).  Errors: LA_ERR_INVALID_ARG (null or misaligned
+ * pointer, negative size, unknown enum, workspace too small),
+ * LA_ERR_UNSUPPORTED (a d or C outside the list), LA_ERR_CUDA.
+ */
+la_status la_chunk_fwd(const void *q, const void *k, const void *v, int dtype,
+                       int B, int H, int L, int d_k, int d_v, int chunk,
+                       int decay_kind, const float *decay,
+                       const float *S0, void *O, float *S_final,
+                       void *workspace, size_t ws_bytes, void *cuda_stream);
+
+/*
+ * One recurrent decode step for B*H sequences, state updated in place:
+ *
+ *     S <- alpha S + phi(k) v^T ;   o = phi(q)^T S      (update, then read)
+ *
+ *   q, k       [B,H,d_k] dtype   (read)
+ *   v          [B,H,d_v] dtype   (read)
+ *   log_alpha  [B,H] fp32 log of the decay, or NULL for alpha = 1  (read)
+ *   S          [B,H,d_k,d_v] fp32, read and overwritten             (in/out)
+ *   o          [B,H,d_v] dtype                                      (write)
+ *
+ * Supported: d_k = d_v in {16, 32, 64, 128}.  Errors as for la_chunk_fwd.
+ */
+la_status la_decode_step(const void *q, const void *k, const void *v, int dtype,
+                         int B, int H, int d_k, int d_v,
+                         const float *log_alpha, float *S, void *o, void *cuda_stream);
+
+/* Synchronise `cuda_stream`, then report and clear the device error word that
+ * kernels set when a bounded wait runs out: LA_OK, LA_ERR_DEVICE_TIMEOUT (the
+ * message names the kernel and the wait) or LA_ERR_CUDA. */
+la_status la_device_status(void *cuda_stream);
+
+/* Self-test of the timeout path: launches one CTA that waits on an mbarrier
+ * nothing ever arrives at, with a spin limit of `spin_limit` polls; the
+ * kernel records the timeout, releases what it holds and exits.  Returns the
+ * status la_device_status() then reports (LA_ERR_DEVICE_TIMEOUT expected). */
+la_status la_selftest_wait_timeout(unsigned int spin_limit, void *cuda_stream);
+
+/* Message for the last non-zero status on this thread ("" if none). */
+const char *la_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_GB300_H */

@@ -1,0 +1,89 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching the GPU.  CPU only
+(the library must have been built; the build runs here without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from causal_linear_attention_chunkwise_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def declared_symbols():
+    names = set()
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(la_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_native.LIB_PATH):
+        build.build()
+    return _native.load()
+
+
+def test_header_declares_the_three_core_calls():
+    names = declared_symbols()
+    assert {"la_chunk_fwd", "la_decode_step", "la_set_feature_map"} <= names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in sorted(declared_symbols()) if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+    assert set(_native.SIGNATURES) == declared_symbols()
+
+
+def test_feature_map_roundtrip(lib):
+    assert lib.la_set_feature_map(7) == 1
+    assert b"unknown feature map" in lib.la_last_error()
+    assert lib.la_set_feature_map(1) == 0 and lib.la_get_feature_map() == 1
+    assert lib.la_set_feature_map(0) == 0 and lib.la_get_feature_map() == 0
+
+
+def test_validation_before_any_device_work(lib):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    # unknown dtype
+    assert lib.la_chunk_fwd(p, p, p, 9, 1, 1, 8, 16, 16, 64, 0, None, None, p, None, None, 0,
+                            None) == 1
+    # negative size
+    assert lib.la_chunk_fwd(p, p, p, 1, 1, 1, -1, 16, 16, 64, 0, None, None, p, None, None, 0,
+                            None) == 1
+    # unsupported head size and chunk
+    assert lib.la_chunk_fwd(p, p, p, 1, 1, 1, 8, 48, 48, 64, 0, None, None, p, None, None, 0,
+                            None) == 2
+    assert lib.la_chunk_fwd(p, p, p, 1, 1, 1, 8, 64, 64, 128, 0, None, None, p, None, None, 0,
+                            None) == 2
+    # null tensors, decay without values, misaligned pointer
+    assert lib.la_chunk_fwd(None, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, p, None, None, 0,
+                            None) == 1
+    assert lib.la_chunk_fwd(p, p, p, 1, 1, 1, 8, 16, 16, 64, 2, None, None, p, None, None, 0,
+                            None) == 1
+    assert b"decay pointer" in lib.la_last_error()
+    q = ctypes.c_void_p(0x1002)
+    assert lib.la_chunk_fwd(q, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, p, None, None, 0,
+                            None) == 1
+    assert b"16-byte" in lib.la_last_error()
+    # empty batch and empty sequence without a final state are no-ops
+    assert lib.la_chunk_fwd(p, p, p, 1, 0, 4, 8, 16, 16, 64, 0, None, None, p, None, None, 0,
+                            None) == 0
+    assert lib.la_chunk_fwd(None, None, None, 1, 2, 2, 0, 16, 16, 64, 0, None, None, None, None,
+                            None, 0, None) == 0
+    # decode: unsupported shapes and null state
+    assert lib.la_decode_step(p, p, p, 1, 1, 1, 128, 64, None, p, p, None) == 2
+    assert lib.la_decode_step(p, p, p, 1, 1, 1, 128, 128, None, None, p, None) == 1
+
+
+def test_workspace_query_is_host_only(lib):
+    for args in [(4, 16, 4096, 64, 64, 64, 1), (1, 16, 32768, 128, 128, 64, 1),
+                 (1, 1, 300, 16, 16, 64, 0), (0, 1, 10, 64, 64, 64, 1)]:
+        n = lib.la_chunk_fwd_workspace_bytes(*args)
+        assert n >= 0

@@ -1,0 +1,183 @@
+"""GPU parity of la_chunk_fwd against the fp64 oracle (element by element on
+the same seeded inputs), plus its edge cases.  Needs a GB300."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_linear_attention_chunkwise_gb300 import api
+from causal_linear_attention_chunkwise_gb300 import workloads as W
+from tests import parity
+from tests.gpu_helpers import gpu_prefill, oracle_prefill, select_pairs, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# Small cases: several chunks and a ragged tail, every phi / decay / dtype /
+# head size, chosen so the oracle finishes in well under a second each.
+SMALL = [
+    # (B, H, L, dk, dv, dtype, phi, decay, chunk, s0)
+    (1, 1, 300, 16, 16, "f32", "identity", "none", 64, None),
+    (2, 3, 200, 32, 32, "f32", "elu1", "head", 64, 0.1),
+    (1, 2, 130, 64, 64, "f32", "identity", "logit", 64, 0.1),
+    (1, 2, 77, 128, 128, "f32", "elu1", "token", 64, None),
+    (1, 1, 45, 16, 32, "f32", "identity", "none", 7, 0.5),
+    (2, 2, 257, 64, 64, "bf16", "elu1", "none", 64, None),
+    (1, 3, 321, 64, 64, "bf16", "identity", "head", 64, 0.1),
+    (1, 2, 200, 64, 64, "bf16", "identity", "logit", 64, 0.1),
+    (2, 2, 257, 128, 128, "bf16", "identity", "none", 64, None),
+    (1, 2, 321, 128, 128, "bf16", "elu1", "head", 64, None),
+    (1, 2, 190, 128, 128, "bf16", "identity", "logit", 64, 0.1),
+    (1, 2, 129, 128, 128, "bf16", "identity", "token", 64, 0.1),
+    (1, 1, 64, 128, 128, "bf16", "identity", "none", 64, None),
+    (1, 1, 1, 64, 64, "bf16", "elu1", "logit", 64, 0.1),
+    (1, 2, 63, 32, 16, "bf16", "identity", "head", 64, None),
+    (3, 1, 100, 16, 16, "bf16", "elu1", "none", 4, None),
+]
+
+
+def _make(B, H, L, dk, dv, dtype, phi, decay, chunk, s0, seed=0):
+    w = W.small_prefill(B, H, L, dk, dv, dtype, phi, "logit" if decay == "token" else decay,
+                        chunk, s0_std=s0)
+    inp = W.make_prefill_inputs(w, seed=seed)
+    if decay == "token":  # per-token log alpha given directly: log alpha = -softplus(g)
+        inp["decay_kind"] = "token"
+        inp["decay"] = -torch.nn.functional.softplus(inp["decay"].double()).float()
+    return w, inp
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"{c[0]}x{c[1]}x{c[2]}_d{c[3]}x{c[4]}_{c[5]}_{c[6]}_{c[7]}_C{c[8]}"
+                                             for c in SMALL])
+def test_small_cases_match_oracle(case):
+    w, inp = _make(*case)
+    O, S = gpu_prefill(inp, w.phi, case[8])
+    O_ref, S_ref = oracle_prefill(inp, w.phi)
+    parity.check(O, O_ref, w.dtype, "O")
+    parity.check(S, S_ref, w.dtype, "S_final")
+
+
+@pytest.mark.parametrize("chunk", [1, 4, 7, 33, 64])
+def test_chunk_size_invariance_fp32(chunk):
+    """The output does not depend on C (page 1 checks [a], [b]) -- here on the
+    GPU against the oracle at fp32 tolerance, L = 300, d = 16."""
+    w = W.PREFILL["L300_d16_f32"]
+    inp = W.make_prefill_inputs(w)
+    O, S = gpu_prefill(inp, w.phi, chunk)
+    O_ref, S_ref = oracle_prefill(inp, w.phi)
+    parity.check(O, O_ref, "f32", f"O C={chunk}")
+    parity.check(S, S_ref, "f32", f"S C={chunk}")
+
+
+def test_headline_fp32_workload():
+    """B=1, H=1, L=300, d=16, fp32, chunk 64 (ragged 44-token tail): the whole
+    output at relative Frobenius error <= 1e-5."""
+    w = W.PREFILL["L300_d16_f32"]
+    inp = W.make_prefill_inputs(w)
+    O, S = gpu_prefill(inp, w.phi, w.chunk)
+    O_ref, S_ref = oracle_prefill(inp, w.phi)
+    parity.check(O, O_ref, "f32", "O")
+    parity.check(S, S_ref, "f32", "S_final")
+
+
+FULL = {
+    "B4_H16_L4096_d64_elu1": [(0, 0), (1, 7), (2, 13), (3, 15)],
+    "B2_H32_L8192_d128_retnet": [(0, 0), (0, 31), (1, 16), (1, 5)],
+    "B1_H16_L32768_d128_gate": [(0, 0), (0, 9), (0, 15)],
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_workloads_on_sampled_sequences(name):
+    """The bf16 workloads at full size, launched as the benchmark launches
+    them; the oracle recomputes a sample of whole (b, h) sequences."""
+    w = W.PREFILL[name]
+    inp = W.make_prefill_inputs(w)
+    O, S = gpu_prefill(inp, w.phi, w.chunk)
+    assert torch.isfinite(O.float()).all() and torch.isfinite(S).all()
+    pairs = FULL[name]
+    O_ref, S_ref = oracle_prefill(inp, w.phi, pairs)
+    parity.check(select_pairs(O, pairs), O_ref, w.dtype, f"{name} O")
+    parity.check(select_pairs(S, pairs), S_ref, w.dtype, f"{name} S_final")
+
+
+def test_empty_sequence_returns_initial_state():
+    S0 = torch.randn(2, 3, 64, 64, device="cuda")
+    q = torch.empty(2, 3, 0, 64, dtype=torch.bfloat16, device="cuda")
+    O, S = api.la_chunk_fwd(q, q, q, 64, S0=S0)
+    api.la_device_status()
+    assert O.shape == (2, 3, 0, 64)
+    assert torch.equal(S, S0)
+    O, S = api.la_chunk_fwd(q, q, q, 64)
+    assert torch.count_nonzero(S) == 0
+
+
+def test_empty_batch_is_a_no_op():
+    q = torch.empty(0, 4, 16, 64, dtype=torch.bfloat16, device="cuda")
+    O, S = api.la_chunk_fwd(q, q, q, 64)
+    api.la_device_status()
+    assert O.numel() == 0 and S.numel() == 0
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 16), ("bf16", 64), ("bf16", 128)])
+def test_final_state_may_alias_initial_state(dtype, d):
+    w, inp = _make(1, 2, 150, d, d, dtype, "identity", "logit", 64, 0.1)
+    O_ref, S_ref = gpu_prefill(inp, "identity")
+    S = to_dev(inp["S0"])
+    api.la_set_feature_map("identity")
+    O, S_out = api.la_chunk_fwd(to_dev(inp["q"]), to_dev(inp["k"]), to_dev(inp["v"]), 64, "logit",
+                                to_dev(inp["decay"]), S, S_final=S)
+    api.la_device_status()
+    assert S_out.data_ptr() == S.data_ptr()
+    assert torch.equal(O.cpu(), O_ref) and torch.equal(S.cpu(), S_ref)
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 32), ("bf16", 128)])
+def test_resume_from_carried_state(dtype, d):
+    """Running [0, m) and then [m, L) from the returned state equals one run."""
+    w, inp = _make(1, 2, 300, d, d, dtype, "identity", "logit", 64, 0.1)
+    O_ref, S_ref = oracle_prefill(inp, "identity")
+    m = 131
+    first = {k_: (v_[:, :, :m].contiguous() if k_ in "qkv" else v_) for k_, v_ in inp.items()}
+    first["decay"] = inp["decay"][:, :, :m].contiguous()
+    O1, S1 = gpu_prefill(first, "identity")
+    second = {k_: (v_[:, :, m:].contiguous() if k_ in "qkv" else v_) for k_, v_ in inp.items()}
+    second["decay"] = inp["decay"][:, :, m:].contiguous()
+    second["S0"] = S1
+    O2, S2 = gpu_prefill(second, "identity")
+    parity.check(torch.cat([O1, O2], dim=2), O_ref, dtype, "resumed O")
+    parity.check(S2, S_ref, dtype, "resumed S")
+
+
+def test_unsupported_and_invalid_requests_raise():
+    q = torch.zeros(1, 1, 8, 48, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(api.LAError) as e:
+        api.la_chunk_fwd(q, q, q, 64)
+    assert e.value.status == api.LA_ERR_UNSUPPORTED
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(api.LAError) as e:
+        api.la_chunk_fwd(q, q, q, 64, "head", None)
+    assert e.value.status == api.LA_ERR_INVALID_ARG
+    buf = torch.zeros(1 * 1 * 8 * 64 + 1, dtype=torch.bfloat16, device="cuda")
+    mis = buf[1:].view(1, 1, 8, 64)  # 2-byte offset: not 16-byte aligned
+    with pytest.raises(api.LAError) as e:
+        api.la_chunk_fwd(mis, q, q, 64)
+    assert e.value.status == api.LA_ERR_INVALID_ARG
+
+
+def test_host_buffers_roundtrip():
+    """CPU tensors in, CPU tensors out: same kernels, copies around them."""
+    w, inp = _make(1, 2, 130, 64, 64, "bf16", "elu1", "none", 64, None)
+    O_dev, S_dev = gpu_prefill(inp, "elu1")
+    api.la_set_feature_map("elu1")
+    O_h, S_h = api.la_chunk_fwd(inp["q"].pin_memory(), inp["k"].pin_memory(),
+                                inp["v"].pin_memory(), 64)
+    assert not O_h.is_cuda
+    assert torch.equal(O_h, O_dev) and torch.equal(S_h, S_dev)
+
+
+def test_timeout_selftest_reports_and_context_survives():
+    assert api.la_selftest_wait_timeout(200) == api.LA_ERR_DEVICE_TIMEOUT
+    assert "timed out" in api.la_last_error()
+    w, inp = _make(1, 1, 70, 64, 64, "bf16", "identity", "none", 64, None)
+    O, S = gpu_prefill(inp, "identity")
+    O_ref, S_ref = oracle_prefill(inp, "identity")
+    parity.check(O, O_ref, "bf16", "O after self-test")
