@@ -1,18 +1,901 @@
-// la_prefill_tc.cu -- tensor-core (tcgen05) chunkwise prefill.  Not yet enabled:
-// every bf16 request currently runs the SIMT kernel.
+// la_prefill_tc.cu -- chunkwise causal linear attention prefill on the 5th-gen
+// tensor cores (tcgen05 MMAs into TMEM, TMA-staged tiles), bf16 inputs with
+// fp32 accumulation, chunk C = 64, d_k = d_v = D in {64, 128}.
+//
+// The chunkwise form ("Linear / Sparse Attention - minimal runnable
+// implementation", linear_attn_chunkwise; "Linear / sparse attention tutorial"
+// section 6.2) for chunk c with incoming state S_c, within-chunk inclusive
+// log-decay prefix Lam_i and chunk total A_c = Lam_{n-1}:
+//
+//   P     = phi(Q_c) phi(K_c)^T                                  (MMA1, 64x64)
+//   P_ij <- P_ij exp(Lam_i - Lam_j) if j <= i else 0             (registers)
+//   O_c   = P V_c                                                (MMA2)
+//         + Qt_c S_c,       Qt_i = exp(Lam_i) phi(q_i)           (MMA3)
+//   S_c+1 = exp(A_c) S_c + Kt_c^T V_c,  Kt_j = exp(A_c - Lam_j) phi(k_j)  (MMA4)
+//
+// Gate factors are the expansion of S_t = a_t S_{t-1} + phi(k_t) v_t^T over one
+// chunk ("CS336 lecture 4, code 1: linear attention",
+// gated_linear_attention_recurrent / _parallel); every exponent is a
+// difference with i >= j or a chunk-local sum <= 0, so nothing overflows.
+//
+// Parallelism over the sequence.  A sequence of NC chunks is cut into NS
+// segments of G chunks.  Three kernels, launched back to back on one stream:
+//   segment_state_kernel  per (b, h, segment s < NS-1): the segment's own
+//       state  dS_s = sum_t exp(Lam_end - Lam_t) phi(k_t) v_t^T  (one long
+//       K = tokens GEMM, weights relative to the segment end, so no rescaling
+//       between chunks) and its total log decay A_s;
+//   state_scan_kernel     per (b, h), elementwise over the state:
+//       S_in[0] = S0 (or 0),  S_in[s+1] = exp(A_s) S_in[s] + dS_s;
+//   chunk_output_kernel   per (b, h, segment): the chunk loop above from
+//       S_in[s]; the last segment also writes S_final.
+// With NS = 1 only the output kernel runs.  The associative combination of
+// (decay, state) pairs across segments is the same state passing the chunk
+// loop performs across chunks.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/la_gb300.h"
+#include "la_common.cuh"
 #include "la_internal.h"
+#include "la_ptx.cuh"
+#include "la_tma_host.h"
 
 namespace la {
+namespace {
 
-bool prefill_tc_supported(const PrefillArgs &) { return false; }
+constexpr int CH = 64;                  // tokens per chunk
+constexpr int BOX = 64;                 // TMA box: 64 rows x 64 bf16 (128 bytes)
+constexpr uint32_t BOX_BYTES = 8192;
+constexpr uint32_t kSpin = 1u << 22;    // polls before a wait gives up
+constexpr int kMaxSegChunks = 32;       // G <= 32 (2048 tokens per segment)
 
-size_t prefill_tc_workspace_bytes(int, int, int, int) { return 0; }
+// Warp roles (both tcgen05 kernels).
+constexpr int W_TMA = 0, W_MMA = 1, WG1 = 4, WG2 = 8;
+constexpr int kThreadsOut = 384;        // warps 0..11
+constexpr int kThreadsState = 256;      // warps 0..7 (WG1 = warps 4..7)
+constexpr uint32_t BAR_WG1 = 1, BAR_WG2 = 2;
 
-int prefill_tc_kernel_count(int, int, int, int) { return 0; }
+struct Ctl {
+  uint32_t abort;
+  uint32_t tmem_base;
+};
 
-cudaError_t launch_prefill_tc(const PrefillArgs &, const char **why) {
-  if (why) *why = "tcgen05 prefill not available";
-  return cudaErrorNotSupported;
+// ---------------------------------------------------------------- waits
+// Single-thread bounded wait; on timeout records the error and sets abort.
+__device__ __forceinline__ bool wait1(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                      unsigned int *err, uint32_t kid, uint32_t site) {
+  for (uint32_t i = 0; i < kSpin; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *(volatile uint32_t *)&ctl->abort) return false;
+  }
+  atomicExch(&ctl->abort, 1u);
+  record_device_error(err, kid, site);
+  return false;
+}
+
+// Warpgroup-wide bounded wait: every thread polls, then the group agrees on
+// the outcome through a reducing named barrier, so all leave together.
+__device__ __forceinline__ bool wait_wg(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                        unsigned int *err, uint32_t kid, uint32_t site,
+                                        uint32_t bar_id) {
+  bool ok = wait1(bar, parity, ctl, err, kid, site);
+  uint32_t any_fail;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(any_fail)
+      : "r"(ok ? 1u : 0u), "r"(bar_id)
+      : "memory");
+  return any_fail == 0;
+}
+
+// ---------------------------------------------------------------- math helpers
+__device__ __forceinline__ float token_lambda(int kind, const float *__restrict__ decay, int h,
+                                              size_t bhL, int tok, int L) {
+  if (tok >= L) return 0.f;  // padding beyond the sequence decays nothing
+  switch (kind) {
+    case LA_DECAY_HEAD: return decay[h];
+    case LA_DECAY_TOKEN: return decay[bhL + tok];
+    case LA_DECAY_GATE_LOGIT: return neg_softplus(decay[bhL + tok]);
+    default: return 0.f;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
+  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
+  return __bfloat1622float2(v);
+}
+
+// Rows of an M=64 accumulator: row 16*i + t lives in TMEM lane 32*i + t
+// (t < 16) of lane quarter i; lanes 16..31 of each quarter are unused.
+// M=128: row = lane.
+template <int M>
+__device__ __forceinline__ int acc_row(int quarter, int lane) {
+  if (M == 128) return quarter * 32 + lane;
+  return lane < 16 ? quarter * 16 + lane : -1;
+}
+
+// Transform a bf16 tile (64 rows, D columns, stored as D/64 swizzled boxes)
+// in place: x <- phi(x) * scale[row] (scale may be null).  Elementwise, so the
+// swizzle matters only for recovering each 16-byte chunk's row.
+template <int D>
+__device__ __forceinline__ void transform_tile(unsigned char *tile, int phi, const float *scale,
+                                               int t, int nthreads) {
+  constexpr int kChunks = 64 * D * 2 / 16;
+  for (int x = t; x < kChunks; x += nthreads) {
+    const int row = (x & 511) >> 3;  // 512 chunks per 8 KB box, 8 per 128-byte row
+    uint4 *p = reinterpret_cast<uint4 *>(tile + (size_t)x * 16);
+    uint4 u = *p;
+    const float s = scale ? scale[row] : 1.f;
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 f = unpack_bf16(w[j]);
+      f.x = feature_map(phi, f.x) * s;
+      f.y = feature_map(phi, f.y) * s;
+      w[j] = pack_bf16(f.x, f.y);
+    }
+    *p = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// ---------------------------------------------------------------- parameters
+struct TcParams {
+  int H, L;
+  int n_chunks;     // chunks per sequence (NC)
+  int seg_chunks;   // G
+  int n_seg;        // NS
+  int phi, decay_kind;
+  const float *decay;
+  const float *S0;  // read directly only when NS == 1
+  float *S_final;
+  float *ws_state;  // [BH][NS][D][D]: slot s = incoming state of segment s
+  float *ws_logdec; // [BH][NS]: total log decay of segment s (s < NS-1)
+  unsigned int *err;
+};
+
+// ================================================================ segment state
+// Shared memory: NST stages of {K tile, V tile}; the segment's suffix log
+// decays; barriers.
+template <int D>
+struct StateSmem {
+  static constexpr int NST = (D == 128) ? 3 : 4;
+  static constexpr uint32_t TILE = 64 * D * 2;
+  static constexpr uint32_t STAGE = 2 * TILE;
+  static constexpr uint32_t OFF_SUF = NST * STAGE;                       // floats [G*64]
+  static constexpr uint32_t OFF_BAR = OFF_SUF + kMaxSegChunks * CH * 4;   // barriers
+  static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
+  static constexpr uint32_t OFF_SCR = OFF_CTL + 64;                       // 8 floats
+  static constexpr uint32_t BYTES = OFF_SCR + 64;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsState, 1)
+segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, TcParams p) {
+  using SM = StateSmem<D>;
+  constexpr int NST = SM::NST;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *suf = reinterpret_cast<float *>(smem + SM::OFF_SUF);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
+  uint64_t *empty = full + NST;
+  uint64_t *ready = empty + NST;   // K tile transformed
+  uint64_t *done = ready + NST;    // all MMAs finished
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
+  float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
+  const int c0 = seg * p.seg_chunks;
+  const int nc = min(p.seg_chunks, p.n_chunks - c0);
+  const int tok0 = c0 * CH;
+  const size_t bhL = (size_t)bh * p.L;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&ready[s], 1);
+    }
+    mbar_init(done, 1);
+    ctl->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == W_MMA) {
+    tmem_alloc(&ctl->tmem_base, D);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == W_TMA) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (c >= NST &&
+            !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 1))
+          break;
+        unsigned char *st = smem + s * SM::STAGE;
+        mbar_arrive_expect_tx(&full[s], SM::STAGE);
+        for (int b = 0; b < D / BOX; ++b) {
+          tma_load_3d(st + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok0 + c * CH, bh);
+          tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok0 + c * CH, bh);
+        }
+      }
+    }
+  } else if (warp == W_MMA) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(D, D, true, true);
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (!wait1(&ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 2)) break;
+        tc_fence_after();
+        const uint32_t kt = smem_u32(smem + s * SM::STAGE);
+        const uint32_t vt = kt + SM::TILE;
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)
+          mma_bf16(tmem, smem_desc_sw128(kt + 2048 * kk, BOX_BYTES, 1024),
+                   smem_desc_sw128(vt + 2048 * kk, BOX_BYTES, 1024), idesc, (c | kk) != 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(done);
+    }
+  } else if (warp >= WG1) {
+    const int t = tid - WG1 * 32;  // 0..127
+    // Suffix sums of the segment's log decays: suf[i] = sum_{r > i} lambda_r,
+    // so token i's weight is exp(suf[i]); A_s = sum of all lambda.
+    const int ntok = nc * CH;
+    float carry = 0.f;  // sum of lambda over tokens after the current block
+    for (int blk = (ntok - 1) / 128; blk >= 0; --blk) {
+      const int i = blk * 128 + t;
+      float lam = (i < ntok) ? token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + i, p.L) : 0.f;
+      // inclusive suffix scan within the block (reverse order)
+      float x = lam;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        float y = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32) x += y;
+      }
+      if (lane == 0) scr[warp - WG1] = x;  // warp total
+      named_bar_sync(BAR_WG1, 128);
+      float later = carry;
+      for (int w2 = (warp - WG1) + 1; w2 < 4; ++w2) later += scr[w2];
+      if (i < ntok) suf[i] = x - lam + later;  // exclusive suffix
+      float block_total = scr[0] + scr[1] + scr[2] + scr[3];
+      named_bar_sync(BAR_WG1, 128);
+      carry += block_total;
+    }
+    const float seg_total = carry;
+    named_bar_sync(BAR_WG1, 128);
+    const bool scale = p.decay_kind != LA_DECAY_NONE;
+    const bool xform = scale || p.phi != LA_PHI_IDENTITY;
+    for (int c = 0; c < nc; ++c) {
+      const int s = c % NST;
+      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, BAR_WG1)) break;
+      if (xform) {
+        // weight exp(suf) per row of this chunk, staged through scr-free math
+        unsigned char *kt = smem + s * SM::STAGE;
+        constexpr int kChunks = 64 * D * 2 / 16;
+        for (int x = t; x < kChunks; x += 128) {
+          const int row = (x & 511) >> 3;
+          const float w = scale ? __expf(suf[c * CH + row]) : 1.f;
+          uint4 *q4 = reinterpret_cast<uint4 *>(kt + (size_t)x * 16);
+          uint4 u = *q4;
+          uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float2 f = unpack_bf16(wv[j]);
+            wv[j] = pack_bf16(feature_map(p.phi, f.x) * w, feature_map(p.phi, f.y) * w);
+          }
+          *q4 = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(BAR_WG1, 128);
+      if (t == 0) mbar_arrive(&ready[s]);
+    }
+    // Read the accumulated state out of TMEM and store it as segment slot s+1.
+    if (wait_wg(done, 0, ctl, p.err, KID_PREFILL_TC_STATE, 4, BAR_WG1)) {
+      tc_fence_after();
+      const int quarter = warp & 3;
+      const int row = acc_row<D>(quarter, lane);
+      float *dst = p.ws_state + (((size_t)bh * p.n_seg + seg + 1) * D) * D;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + col, r);
+        tmem_ld_wait();
+        if (row >= 0) {
+          float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * D + col);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (t == 0) p.ws_logdec[(size_t)bh * p.n_seg + seg] = seg_total;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_MMA) {
+    __syncwarp();
+    tmem_dealloc(tmem, D);
+  }
+}
+
+// ================================================================ state scan
+// slot 0 <- S0 (or 0); slot s+1 <- exp(A_s) slot s + slot s+1, for s < NS-1.
+__global__ void __launch_bounds__(256)
+state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_state,
+                  const float *__restrict__ ws_logdec) {
+  const int bh = blockIdx.y;
+  const size_t n4 = (size_t)D * D / 4;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  float4 *slots = reinterpret_cast<float4 *>(ws_state) + (size_t)bh * n_seg * n4;
+  float4 cur = S0 ? reinterpret_cast<const float4 *>(S0)[(size_t)bh * n4 + i]
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  slots[i] = cur;
+  float4 nxt = n_seg > 1 ? slots[n4 + i] : cur;
+  for (int s = 0; s + 1 < n_seg; ++s) {
+    const float a = __expf(ws_logdec[(size_t)bh * n_seg + s]);
+    const float4 d = nxt;
+    if (s + 2 < n_seg) nxt = slots[(size_t)(s + 2) * n4 + i];
+    cur.x = fmaf(a, cur.x, d.x);
+    cur.y = fmaf(a, cur.y, d.y);
+    cur.z = fmaf(a, cur.z, d.z);
+    cur.w = fmaf(a, cur.w, d.w);
+    slots[(size_t)(s + 1) * n4 + i] = cur;
+  }
+}
+
+// ================================================================ chunk output
+template <int D>
+struct OutSmem {
+  static constexpr int NST = (D == 128) ? 3 : 4;
+  static constexpr uint32_t TILE = 64 * D * 2;            // Q, K or V tile of one chunk
+  static constexpr uint32_t STAGE = 3 * TILE;
+  static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
+  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // [D][D] bf16, MN-major blocks
+  static constexpr uint32_t S_BLOCK = D * 128;             // one 64-column block
+  static constexpr uint32_t OFF_O = OFF_S + D * D * 2;     // [64][D] bf16 store staging
+  static constexpr uint32_t OFF_LAM = OFF_O + TILE;        // [NST][64] floats
+  static constexpr uint32_t OFF_A = OFF_LAM + NST * 64 * 4;
+  static constexpr uint32_t OFF_SCR = OFF_A + 16 * 4;      // warp carries
+  static constexpr uint32_t OFF_BAR = OFF_SCR + 16 * 4;
+  static constexpr int NBAR = 3 * NST + 2 * 5 + 1;
+  static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
+  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  // TMEM columns
+  static constexpr uint32_t T_P = 0;          // 2 x 64 columns
+  static constexpr uint32_t T_O = 128;        // 2 x D columns
+  static constexpr uint32_t T_S = 128 + 2 * D;
+  static constexpr uint32_t T_COLS = 512;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsOut, 1)
+chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
+                    const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV,
+                    const __grid_constant__ CUtensorMap tmO, TcParams p) {
+  using SM = OutSmem<D>;
+  constexpr int NST = SM::NST;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
+  float *Aend = reinterpret_cast<float *>(smem + SM::OFF_A);
+  float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
+  uint64_t *empty = full + NST;
+  uint64_t *xdone = empty + NST;       // stage transformed (phi), Lam ready
+  uint64_t *p_full = xdone + NST;      // [2] MMA1 done
+  uint64_t *p_ready = p_full + 2;      // [2] P in smem, Q/K rescaled
+  uint64_t *p_free = p_ready + 2;      // [2] MMA2 done reading P smem
+  uint64_t *c_done = p_free + 2;       // [2] MMA3 + MMA4 done
+  uint64_t *o_free = c_done + 2;       // [2] O TMEM buffer read
+  uint64_t *s_ready = o_free + 2;      // S smem (and TMEM S) ready
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
+  const int c0 = seg * p.seg_chunks;
+  const int nc = min(p.seg_chunks, p.n_chunks - c0);
+  const int tok0 = c0 * CH;
+  const size_t bhL = (size_t)bh * p.L;
+  const bool last_seg = seg == p.n_seg - 1;
+  const float *S_in = nullptr;
+  if (p.n_seg > 1) {
+    if (seg > 0 || p.S0) S_in = p.ws_state + ((size_t)bh * p.n_seg + seg) * D * D;
+  } else {
+    S_in = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
+  }
+  const bool has_init = S_in != nullptr;
+  const bool decay = p.decay_kind != LA_DECAY_NONE;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&xdone[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&p_ready[i], 1);
+      mbar_init(&p_free[i], 1);
+      mbar_init(&c_done[i], 1);
+      mbar_init(&o_free[i], 1);
+    }
+    mbar_init(s_ready, 1);
+    ctl->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == W_MMA) {
+    tmem_alloc(&ctl->tmem_base, SM::T_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == W_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (c >= NST &&
+            !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 1))
+          break;
+        unsigned char *st = smem + s * SM::STAGE;
+        mbar_arrive_expect_tx(&full[s], SM::STAGE);
+        const int tok = tok0 + c * CH;
+        for (int b = 0; b < D / BOX; ++b) {
+          tma_load_3d(st + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
+          tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
+          tma_load_3d(st + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
+        }
+      }
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nc > 0) {
+      constexpr uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_f32(64, D, false, true);
+      constexpr uint32_t id_qs = idesc_bf16_f32(64, D, false, true);
+      constexpr uint32_t id_kv = idesc_bf16_f32(D, D, true, true);
+      const uint32_t sbase = smem_u32(smem);
+      const uint32_t s_smem = sbase + SM::OFF_S;
+      auto q_of = [&](int s) { return sbase + s * SM::STAGE; };
+      auto issue_qk = [&](int c) {
+        const int s = c % NST;
+        const uint32_t qa = q_of(s), ka = qa + SM::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+          mma_bf16(tmem + SM::T_P + 64 * (c & 1), smem_desc_sw128(qa + off, 16, 1024),
+                   smem_desc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
+        }
+        mma_commit(&p_full[c & 1]);
+      };
+      bool ok = wait1(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 2);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
+      }
+      for (int c = 0; ok && c < nc; ++c) {
+        const int s = c % NST, b = c & 1;
+        const uint32_t qa = q_of(s), ka = qa + SM::TILE, va = qa + 2 * SM::TILE;
+        const uint32_t o_t = tmem + SM::T_O + D * b;
+        if (!(ok = wait1(&p_ready[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
+        if (c >= 2 &&
+            !(ok = wait1(&o_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
+          break;
+        tc_fence_after();
+        const uint32_t pa = sbase + SM::OFF_P + 8192 * b;
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)   // O = P V
+          mma_bf16(o_t, smem_desc_sw128(pa + 32 * kk, 16, 1024),
+                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_pv, kk > 0);
+        mma_commit(&p_free[b]);
+        if (c + 1 < nc) {
+          const int s1 = (c + 1) % NST;
+          if (!(ok = wait1(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
+            break;
+          tc_fence_after();
+          issue_qk(c + 1);
+        }
+        if (!(ok = wait1(s_ready, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
+        tc_fence_after();
+        if (has_init || c > 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {  // O += Qt S
+            const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+            mma_bf16(o_t, smem_desc_sw128(qa + off, 16, 1024),
+                     smem_desc_sw128(s_smem + 2048 * kk, SM::S_BLOCK, 1024), id_qs, 1);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)   // S = exp(A) S + Kt^T V
+          mma_bf16(tmem + SM::T_S, smem_desc_sw128(ka + 2048 * kk, BOX_BYTES, 1024),
+                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_kv,
+                   (has_init || c > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&c_done[b]);
+        mma_commit(&empty[s]);
+      }
+    }
+  } else if (warp >= WG1 && warp < WG2) {
+    // ------------------------------------------------------------ WG1: phi, Lam, P
+    const int t = tid - WG1 * 32;
+    const int quarter = warp & 3;
+    const int prow = acc_row<64>(quarter, lane);
+    for (int c = 0; c < nc; ++c) {
+      const int s = c % NST, b = c & 1;
+      unsigned char *qt = smem + s * SM::STAGE;
+      unsigned char *kt = qt + SM::TILE;
+      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 7, BAR_WG1)) break;
+      // inclusive prefix of the chunk's log decays over 64 tokens (warps 4, 5)
+      if (t < 64) {
+        const int tok = tok0 + c * CH + t;
+        float x = decay ? token_lambda(p.decay_kind, p.decay, h, bhL, tok, p.L) : 0.f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          float y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        if (t == 31) scr[0] = x;
+        lam[s * 64 + t] = x;
+      }
+      if (p.phi != LA_PHI_IDENTITY) {
+        transform_tile<D>(qt, p.phi, nullptr, t, 128);
+        transform_tile<D>(kt, p.phi, nullptr, t, 128);
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(BAR_WG1, 128);
+      if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
+      named_bar_sync(BAR_WG1, 128);
+      if (t == 63) Aend[s] = lam[s * 64 + 63];
+      named_bar_sync(BAR_WG1, 128);
+      if (t == 0) mbar_arrive(&xdone[s]);
+
+      // P epilogue: mask, decay, bf16, into P smem (K-major, 64 x 64)
+      if (!wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 8, BAR_WG1)) break;
+      if (c >= 2 &&
+          !wait_wg(&p_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG1))
+        break;
+      tc_fence_after();
+      const float *lm = lam + s * 64;
+      unsigned char *ps = smem + SM::OFF_P + 8192 * b;
+#pragma unroll 1
+      for (int col = 0; col < 64; col += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + SM::T_P + 64 * b + col, r);
+        tmem_ld_wait();
+        if (prow >= 0) {
+          const float li = lm[prow];
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            const int j0 = col + j, j1 = col + j + 1;
+            float v0 = j0 <= prow ? __uint_as_float(r[j]) : 0.f;
+            float v1 = j1 <= prow ? __uint_as_float(r[j + 1]) : 0.f;
+            if (decay) {
+              v0 *= j0 <= prow ? __expf(li - lm[j0]) : 0.f;
+              v1 *= j1 <= prow ? __expf(li - lm[j1]) : 0.f;
+            }
+            pk[j >> 1] = pack_bf16(v0, v1);
+          }
+          const int ch0 = col >> 3;
+          *reinterpret_cast<uint4 *>(ps + prow * 128 + (((ch0) ^ (prow & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4 *>(ps + prow * 128 + (((ch0 + 1) ^ (prow & 7)) << 4)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      if (decay) {  // Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j, in place
+        const float A = Aend[s];
+        constexpr int kChunks = 64 * D * 2 / 16;
+        for (int x = t; x < 2 * kChunks; x += 128) {
+          const bool isk = x >= kChunks;
+          const int xx = isk ? x - kChunks : x;
+          const int row = (xx & 511) >> 3;
+          const float w = isk ? __expf(A - lm[row]) : __expf(lm[row]);
+          uint4 *q4 = reinterpret_cast<uint4 *>((isk ? kt : qt) + (size_t)xx * 16);
+          uint4 u = *q4;
+          uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float2 f = unpack_bf16(wv[j]);
+            wv[j] = pack_bf16(f.x * w, f.y * w);
+          }
+          *q4 = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_WG1, 128);
+      if (t == 0) mbar_arrive(&p_ready[b]);
+    }
+  } else if (warp >= WG2) {
+    // ------------------------------------------------------------ WG2: state, O
+    const int t = tid - WG2 * 32;
+    const int quarter = warp & 3;
+    const int srow = acc_row<D>(quarter, lane);    // state row (d_k index)
+    const int orow = acc_row<64>(quarter, lane);   // output row within the chunk
+    unsigned char *s_sm = smem + SM::OFF_S;
+    unsigned char *o_sm = smem + SM::OFF_O;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // Write one 16-column piece of state row `srow`: bf16 copy into S smem
+    // (MN-major: row = d_k index, 64-column blocks), and optionally a scaled
+    // fp32 copy back into TMEM.
+    auto put_state = [&](int col, const float *v, float scale, bool to_tmem) {
+      if (srow >= 0) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) pk[j] = pack_bf16(v[2 * j], v[2 * j + 1]);
+        unsigned char *blk = s_sm + (col / 64) * SM::S_BLOCK + srow * 128;
+        const int ch0 = (col % 64) >> 3;
+        *reinterpret_cast<uint4 *>(blk + ((ch0 ^ (srow & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4 *>(blk + (((ch0 + 1) ^ (srow & 7)) << 4)) =
+            make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+      if (to_tmem) {
+        uint32_t r[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(v[j] * scale);
+        tmem_st16(tmem + lane_off + SM::T_S + col, r);
+      }
+    };
+    bool ok = true;
+    // initial state for chunk 0
+    if (nc > 0) {
+      ok = wait_wg(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 10, BAR_WG2);
+      if (ok && has_init) {
+        const float a0 = __expf(Aend[0]);
+#pragma unroll 1
+        for (int col = 0; col < D; col += 16) {
+          float v[16];
+          if (srow >= 0) {
+            const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              float4 f = src[j];
+              v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
+          }
+          put_state(col, v, a0, true);
+        }
+        tmem_st_wait();
+      }
+      if (ok) {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(BAR_WG2, 128);
+        if (t == 0) mbar_arrive(s_ready);
+      }
+    }
+    for (int c = 0; ok && c < nc; ++c) {
+      const int b = c & 1;
+      if (!(ok = wait_wg(&c_done[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11,
+                         BAR_WG2)))
+        break;
+      tc_fence_after();
+      // ---- state for the next chunk (critical path first)
+      if (c + 1 < nc) {
+        const int s1 = (c + 1) % NST;
+        if (!(ok = wait_wg(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 12,
+                           BAR_WG2)))
+          break;
+        const float a1 = __expf(Aend[s1]);
+#pragma unroll 1
+        for (int col = 0; col < D; col += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_off + SM::T_S + col, r);
+          tmem_ld_wait();
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+          put_state(col, v, a1, decay);
+        }
+        if (decay) tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(BAR_WG2, 128);
+        if (t == 0) mbar_arrive(s_ready);
+      } else if (last_seg && p.S_final) {
+#pragma unroll 1
+        for (int col = 0; col < D; col += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_off + SM::T_S + col, r);
+          tmem_ld_wait();
+          if (srow >= 0) {
+            float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+        }
+      }
+      // ---- output of chunk c: TMEM -> bf16 -> staging smem -> TMA store
+      if (t == 0) tma_store_wait_read_all();  // previous store done reading staging
+      named_bar_sync(BAR_WG2, 128);
+#pragma unroll 1
+      for (int col = 0; col < D; col += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_off + SM::T_O + D * b + col, r);
+        tmem_ld_wait();
+        if (orow >= 0) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          unsigned char *box = o_sm + (col / 64) * BOX_BYTES + orow * 128;
+          const int ch0 = (col % 64) >> 3;
+          *reinterpret_cast<uint4 *>(box + ((ch0 ^ (orow & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4 *>(box + (((ch0 + 1) ^ (orow & 7)) << 4)) =
+              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_WG2, 128);
+      if (t == 0) {
+        mbar_arrive(&o_free[b]);
+        for (int bb = 0; bb < D / BOX; ++bb)
+          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok0 + c * CH, bh);
+        tma_store_commit();
+      }
+    }
+    if (t == 0) tma_store_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_MMA) {
+    __syncwarp();
+    tmem_dealloc(tmem, SM::T_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- planning
+struct Plan {
+  int n_chunks, seg_chunks, n_seg;
+};
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
+}
+
+#ifndef LA_TC_TARGET_WAVES
+#define LA_TC_TARGET_WAVES 2
+#endif
+
+Plan make_plan(int B, int H, int L) {
+  Plan pl;
+  pl.n_chunks = (L + CH - 1) / CH;
+  const long bh = (long)B * H;
+  const long target = (long)LA_TC_TARGET_WAVES * sm_count();
+  long ns = (target + bh - 1) / bh;
+  ns = std::max(1L, std::min(ns, (long)pl.n_chunks));
+  int g = (int)((pl.n_chunks + ns - 1) / ns);
+  g = std::min(g, kMaxSegChunks);
+  g = std::max(g, 1);
+  pl.seg_chunks = g;
+  pl.n_seg = (pl.n_chunks + g - 1) / g;
+  return pl;
+}
+
+size_t ws_bytes_for(int B, int H, int L, int D) {
+  Plan pl = make_plan(B, H, L);
+  if (pl.n_seg <= 1) return 0;
+  const size_t bh = (size_t)B * H;
+  const size_t st = bh * pl.n_seg * (size_t)D * D * sizeof(float);
+  return st + ((bh * pl.n_seg * sizeof(float) + 255) & ~(size_t)255);
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillArgs &a, const char **why) {
+  const Plan pl = make_plan(a.B, a.H, a.L);
+  const int BH = a.B * a.H;
+  TcParams p{};
+  p.H = a.H;
+  p.L = a.L;
+  p.n_chunks = pl.n_chunks;
+  p.seg_chunks = pl.seg_chunks;
+  p.n_seg = pl.n_seg;
+  p.phi = a.phi;
+  p.decay_kind = a.decay_kind;
+  p.decay = a.decay;
+  p.S0 = a.S0;
+  p.S_final = a.S_final;
+  p.err = device_error_word();
+  if (pl.n_seg > 1) {
+    p.ws_state = static_cast<float *>(a.workspace);
+    p.ws_logdec = p.ws_state + (size_t)BH * pl.n_seg * D * D;
+  }
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tk, a.k, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX)) {
+    if (why) *why = "la_chunk_fwd: TMA tensor map creation failed";
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t e;
+  if (pl.n_seg > 1) {
+    using SS = StateSmem<D>;
+    auto ks = segment_state_kernel<D>;
+    e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS::BYTES);
+    if (e != cudaSuccess) return e;
+    ks<<<dim3(pl.n_seg - 1, BH), kThreadsState, SS::BYTES, a.stream>>>(tk, tv, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) {
+      if (why) *why = "la_chunk_fwd: segment-state kernel launch";
+      return e;
+    }
+    const int n4 = D * D / 4;
+    state_scan_kernel<<<dim3((n4 + 255) / 256, BH), 256, 0, a.stream>>>(
+        D, pl.n_seg, a.S0, p.ws_state, p.ws_logdec);
+    if ((e = cudaGetLastError()) != cudaSuccess) {
+      if (why) *why = "la_chunk_fwd: state-scan kernel launch";
+      return e;
+    }
+  }
+  using OS = OutSmem<D>;
+  auto ko = chunk_output_kernel<D>;
+  e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)OS::BYTES);
+  if (e != cudaSuccess) return e;
+  ko<<<dim3(pl.n_seg, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  if ((e = cudaGetLastError()) != cudaSuccess && why)
+    *why = "la_chunk_fwd: chunk-output kernel launch";
+  return e;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillArgs &a) {
+  return a.dtype == LA_BF16 && a.chunk == CH && a.dk == a.dv && (a.dk == 64 || a.dk == 128);
+}
+
+size_t prefill_tc_workspace_bytes(int B, int H, int L, int d) {
+  if (B <= 0 || H <= 0 || L <= 0) return 0;
+  return ws_bytes_for(B, H, L, d);
+}
+
+int prefill_tc_kernel_count(int B, int H, int L, int) {
+  return make_plan(B, H, L).n_seg > 1 ? 3 : 1;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why) {
+  if (a.dk == 128) return launch_d<128>(a, why);
+  return launch_d<64>(a, why);
 }
 
 }  // namespace la
