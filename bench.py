@@ -227,7 +227,7 @@ def _dev_inputs(inp, dev):
     return {k: (v.to(dev).contiguous() if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
-def bench_prefill(w, steps, warmup, dev, peaks, peak_kind):
+def bench_prefill(w, steps, warmup, dev, peaks, peak_kind, min_warmup_s=1.0):
     from causal_linear_attention_chunkwise_gb300 import api
     api.la_set_feature_map(w.phi)
     host = W.make_prefill_inputs(w, seed=0)
@@ -252,7 +252,7 @@ def bench_prefill(w, steps, warmup, dev, peaks, peak_kind):
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     t0 = time.time()
     i = 0
-    while i < warmup or time.time() - t0 < 1.0:
+    while i < warmup or time.time() - t0 < min_warmup_s:
         step(i)
         i += 1
         if i % 50 == 0:
@@ -457,6 +457,23 @@ def run_gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
+def run_profile(args):
+    """One leg only, W warm-up and K timed steps, no minimum warm-up time: the
+    command the committed ncu summaries are taken with."""
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks, peak_kind = load_peaks()
+    if args.profile == "prefill":
+        w = W.PREFILL[args.workload]
+        r = bench_prefill(w, args.steps, args.warmup, dev, peaks, peak_kind, min_warmup_s=0.0)
+        print(json.dumps({"profile": "prefill", "workload": w.name,
+                          "per_call_ms": round(r["per_call_ms"], 5), "roofline": r["roofline"]}))
+    else:
+        dw, _, per, rl = bench_decode(args.steps, args.warmup, dev, peaks, peak_kind)
+        print(json.dumps({"profile": "decode", "workload": dw.name, "per_step_ms": round(per, 5),
+                          "roofline": rl}))
+
+
 def _cpu_name():
     try:
         with open("/proc/cpuinfo") as f:
@@ -512,9 +529,13 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.PREFILL))
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile", choices=["prefill", "decode"], default=None,
+                   help="run one leg only (for ncu captures); prints no benchmark line")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile:
+        run_profile(args)
+    elif args.impl == "reference":
         run_reference_arm(args)
     else:
         run_gpu_arm(args)

@@ -49,3 +49,22 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 }  // namespace la
+
+// Opt-in event trace for kernel development.  Built with -DLA_TRACE, kernels
+// record clock64() stamps of pipeline events for one chosen CTA into
+// la::g_trace[event][chunk] (relative to the CTA's start), which the using
+// translation unit defines; otherwise every LA_TRACE_EVENT compiles to nothing.
+namespace la {
+constexpr int kTraceEvents = 16, kTraceChunks = 64;
+}  // namespace la
+#ifdef LA_TRACE
+#define LA_TRACE_EVENT(on, t0, ev, c)                                          \
+  do {                                                                         \
+    if ((on) && (c) < ::la::kTraceChunks)                                      \
+      ::la::g_trace[(ev)][(c)] = clock64() - (t0);                             \
+  } while (0)
+#else
+#define LA_TRACE_EVENT(on, t0, ev, c) \
+  do {                                \
+  } while (0)
+#endif

@@ -43,6 +43,15 @@
 #include "la_ptx.cuh"
 #include "la_tma_host.h"
 
+#ifdef LA_TRACE
+namespace la {
+__device__ long long g_trace[kTraceEvents][kTraceChunks];
+}
+extern "C" int la_trace_read(long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, la::g_trace, sizeof(la::g_trace));
+}
+#endif
+
 namespace la {
 namespace {
 
@@ -54,8 +63,6 @@ constexpr int kMaxSegChunks = 32;       // G <= 32 (2048 tokens per segment)
 
 // Warp roles (both tcgen05 kernels).
 constexpr int W_TMA = 0, W_MMA = 1, WG1 = 4, WG2 = 8;
-constexpr int kThreadsOut = 384;        // warps 0..11
-constexpr int kThreadsState = 256;      // warps 0..7 (WG1 = warps 4..7)
 constexpr uint32_t BAR_WG1 = 1, BAR_WG2 = 2;
 
 struct Ctl {
@@ -76,21 +83,45 @@ __device__ __forceinline__ bool wait1(uint64_t *bar, uint32_t parity, Ctl *ctl,
   return false;
 }
 
-// Warpgroup-wide bounded wait: every thread polls, then the group agrees on
-// the outcome through a reducing named barrier, so all leave together.
+// After an abort: wait (bounded, ignoring the abort flag) for a phase that
+// in-flight asynchronous work will still complete, so that no TMA write or
+// MMA outlives the CTA's shared memory and TMEM.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpin; ++i)
+    if (mbar_try_wait(bar, parity)) return;
+}
+
+// Warpgroup-wide bounded wait: the group's first thread polls while the
+// others sleep in a reducing named barrier that also hands them the outcome,
+// so all leave together.  The barrier orders the group's later accesses after
+// the leader's acquire of the mbarrier phase.
 __device__ __forceinline__ bool wait_wg(uint64_t *bar, uint32_t parity, Ctl *ctl,
                                         unsigned int *err, uint32_t kid, uint32_t site,
                                         uint32_t bar_id) {
-  bool ok = wait1(bar, parity, ctl, err, kid, site);
+  bool ok = true;
+  if ((threadIdx.x & 127) == 0) ok = wait1(bar, parity, ctl, err, kid, site);
+  __syncwarp();
   uint32_t any_fail;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "barrier.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(any_fail)
       : "r"(ok ? 1u : 0u), "r"(bar_id)
       : "memory");
-  return any_fail == 0;
+  if (any_fail) return false;
+  if ((threadIdx.x & 127) != 0) mbar_try_wait(bar, parity);  // completed: own acquire
+  __syncwarp();
+  return true;
 }
+
+// Debug builds (-DLA_CHECKED) bounds-check every runtime-computed TMA
+// coordinate and global index, record the first violation in the device
+// error word (wait site 200 + n) and skip the access.
+#ifdef LA_CHECKED
+#define LA_CHK(cond, kid, site) ((cond) ? true : (record_device_error(p.err, (kid), 200u + (site)), false))
+#else
+#define LA_CHK(cond, kid, site) true
+#endif
 
 // ---------------------------------------------------------------- math helpers
 __device__ __forceinline__ float token_lambda(int kind, const float *__restrict__ decay, int h,
@@ -122,33 +153,9 @@ __device__ __forceinline__ int acc_row(int quarter, int lane) {
   return lane < 16 ? quarter * 16 + lane : -1;
 }
 
-// Transform a bf16 tile (64 rows, D columns, stored as D/64 swizzled boxes)
-// in place: x <- phi(x) * scale[row] (scale may be null).  Elementwise, so the
-// swizzle matters only for recovering each 16-byte chunk's row.
-template <int D>
-__device__ __forceinline__ void transform_tile(unsigned char *tile, int phi, const float *scale,
-                                               int t, int nthreads) {
-  constexpr int kChunks = 64 * D * 2 / 16;
-  for (int x = t; x < kChunks; x += nthreads) {
-    const int row = (x & 511) >> 3;  // 512 chunks per 8 KB box, 8 per 128-byte row
-    uint4 *p = reinterpret_cast<uint4 *>(tile + (size_t)x * 16);
-    uint4 u = *p;
-    const float s = scale ? scale[row] : 1.f;
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float2 f = unpack_bf16(w[j]);
-      f.x = feature_map(phi, f.x) * s;
-      f.y = feature_map(phi, f.y) * s;
-      w[j] = pack_bf16(f.x, f.y);
-    }
-    *p = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 // ---------------------------------------------------------------- parameters
 struct TcParams {
-  int H, L;
+  int H, L, BH;
   int n_chunks;     // chunks per sequence (NC)
   int seg_chunks;   // G
   int n_seg;        // NS
@@ -161,20 +168,81 @@ struct TcParams {
   unsigned int *err;
 };
 
+// ================================================================ shared pieces
+// Elementwise pass over a bf16 tile of 64 rows x D columns (D/64 swizzled 8 KB
+// boxes, 8 sixteen-byte chunks per 128-byte row): x <- phi(x) * fac[row].
+// Each thread takes chunks t, t + n, ...; four loads are issued before any use.
+template <int D, bool PHI, bool SCALE>
+__device__ __forceinline__ void tile_pass(unsigned char *tile, const float *fac, int t, int n) {
+  constexpr int kChunks = 64 * D * 2 / 16;
+  for (int base = 0; base < kChunks; base += 4 * n) {
+    uint4 u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = base + j * n + t;
+      if (x < kChunks) u[j] = *reinterpret_cast<const uint4 *>(tile + (size_t)x * 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = base + j * n + t;
+      if (x >= kChunks) continue;
+      const float s = SCALE ? fac[(x & 511) >> 3] : 1.f;
+      uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = unpack_bf16(w[e]);
+        if (PHI) {
+          f.x = f.x > 0.f ? f.x + 1.f : __expf(f.x);
+          f.y = f.y > 0.f ? f.y + 1.f : __expf(f.y);
+        }
+        w[e] = pack_bf16(f.x * s, f.y * s);
+      }
+      u[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = base + j * n + t;
+      if (x < kChunks) *reinterpret_cast<uint4 *>(tile + (size_t)x * 16) = u[j];
+    }
+  }
+}
+
+// Store 16 consecutive bf16 values (8 packed words) of `row` at column `col`
+// (a multiple of 16) into a swizzled tile whose 64-column blocks are `blk`
+// bytes apart.
+__device__ __forceinline__ void st_row16(unsigned char *base, uint32_t blk, int row, int col,
+                                         const uint32_t *pk) {
+  unsigned char *p = base + (col / 64) * blk + row * 128;
+  const int ch0 = (col % 64) >> 3;
+  *reinterpret_cast<uint4 *>(p + ((ch0 ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  *reinterpret_cast<uint4 *>(p + (((ch0 + 1) ^ (row & 7)) << 4)) =
+      make_uint4(pk[4], pk[5], pk[6], pk[7]);
+}
+
 // ================================================================ segment state
 // Shared memory: NST stages of {K tile, V tile}; the segment's suffix log
-// decays; barriers.
+// decays; per-stage row weights; barriers.
 template <int D>
 struct StateSmem {
-  static constexpr int NST = (D == 128) ? 3 : 4;
+  // The two transform groups take alternate chunks, so the stage count must be
+  // even: stage s is then always used by group s % 2, and every phase of its
+  // barriers is waited on, in order, by that one group.  (With an odd count a
+  // group could wait on a stage whose previous phase belongs to the other
+  // group and has not completed yet; the parity test would then pass early.)
+  static constexpr int NST = 4;
+  static_assert(NST % 2 == 0, "stages must alternate between the two transform groups");
   static constexpr uint32_t TILE = 64 * D * 2;
   static constexpr uint32_t STAGE = 2 * TILE;
   static constexpr uint32_t OFF_SUF = NST * STAGE;                       // floats [G*64]
-  static constexpr uint32_t OFF_BAR = OFF_SUF + kMaxSegChunks * CH * 4;   // barriers
+  static constexpr uint32_t OFF_W = OFF_SUF + kMaxSegChunks * CH * 4;     // [NST][64] floats
+  static constexpr uint32_t OFF_BAR = OFF_W + NST * 64 * 4;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
   static constexpr uint32_t OFF_SCR = OFF_CTL + 64;                       // 8 floats
   static constexpr uint32_t BYTES = OFF_SCR + 64;
 };
+
+constexpr int kThreadsState = 384;  // warps 0..11: TMA, MMA, -, -, XG0 (4..7), XG1 (8..11)
+constexpr uint32_t BAR_XG0 = 1, BAR_XG1 = 2, BAR_XG = 3;
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsState, 1)
@@ -184,6 +252,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   constexpr int NST = SM::NST;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *suf = reinterpret_cast<float *>(smem + SM::OFF_SUF);
+  float *wrow = reinterpret_cast<float *>(smem + SM::OFF_W);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
   uint64_t *ready = empty + NST;   // K tile transformed
@@ -221,6 +290,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      int issued = 0;
       for (int c = 0; c < nc; ++c) {
         const int s = c % NST;
         if (c >= NST &&
@@ -229,10 +299,18 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         unsigned char *st = smem + s * SM::STAGE;
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
         for (int b = 0; b < D / BOX; ++b) {
+          if (!LA_CHK(b * BOX + BOX <= D && tok0 + c * CH < p.L && bh < p.BH,
+                      KID_PREFILL_TC_STATE, 1))
+            continue;
           tma_load_3d(st + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok0 + c * CH, bh);
           tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok0 + c * CH, bh);
         }
+        issued = c + 1;
       }
+      if (*(volatile uint32_t *)&ctl->abort)
+        for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+      // Producer tail: wait for the last stage releases (tcgen05.commit arrivals).
+      for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
     }
   } else if (warp == W_MMA) {
     if (lane == 0) {
@@ -250,76 +328,74 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         mma_commit(&empty[s]);
       }
       mma_commit(done);
+      drain_wait(done, 0);  // every issued MMA has finished before TMEM is released
     }
   } else if (warp >= WG1) {
-    const int t = tid - WG1 * 32;  // 0..127
-    // Suffix sums of the segment's log decays: suf[i] = sum_{r > i} lambda_r,
-    // so token i's weight is exp(suf[i]); A_s = sum of all lambda.
+    const int g = (warp - WG1) >> 2;           // transform group 0 or 1
+    const int t = tid - WG1 * 32 - 128 * g;    // 0..127 within the group
+    const uint32_t gbar = g ? BAR_XG1 : BAR_XG0;
+    // Suffix sums of the segment's log decays (group 0): suf[i] = sum_{r > i}
+    // lambda_r, so token i's weight is exp(suf[i]); A_s = sum of all lambda.
     const int ntok = nc * CH;
-    float carry = 0.f;  // sum of lambda over tokens after the current block
-    for (int blk = (ntok - 1) / 128; blk >= 0; --blk) {
-      const int i = blk * 128 + t;
-      float lam = (i < ntok) ? token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + i, p.L) : 0.f;
-      // inclusive suffix scan within the block (reverse order)
-      float x = lam;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        float y = __shfl_down_sync(0xffffffffu, x, off);
-        if (lane + off < 32) x += y;
-      }
-      if (lane == 0) scr[warp - WG1] = x;  // warp total
-      named_bar_sync(BAR_WG1, 128);
-      float later = carry;
-      for (int w2 = (warp - WG1) + 1; w2 < 4; ++w2) later += scr[w2];
-      if (i < ntok) suf[i] = x - lam + later;  // exclusive suffix
-      float block_total = scr[0] + scr[1] + scr[2] + scr[3];
-      named_bar_sync(BAR_WG1, 128);
-      carry += block_total;
-    }
-    const float seg_total = carry;
-    named_bar_sync(BAR_WG1, 128);
     const bool scale = p.decay_kind != LA_DECAY_NONE;
-    const bool xform = scale || p.phi != LA_PHI_IDENTITY;
-    for (int c = 0; c < nc; ++c) {
-      const int s = c % NST;
-      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, BAR_WG1)) break;
-      if (xform) {
-        // weight exp(suf) per row of this chunk, staged through scr-free math
-        unsigned char *kt = smem + s * SM::STAGE;
-        constexpr int kChunks = 64 * D * 2 / 16;
-        for (int x = t; x < kChunks; x += 128) {
-          const int row = (x & 511) >> 3;
-          const float w = scale ? __expf(suf[c * CH + row]) : 1.f;
-          uint4 *q4 = reinterpret_cast<uint4 *>(kt + (size_t)x * 16);
-          uint4 u = *q4;
-          uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    float seg_total = 0.f;
+    if (g == 0 && scale) {
+      float carry = 0.f;
+      for (int blk = (ntok - 1) / 128; blk >= 0; --blk) {
+        const int i = blk * 128 + t;
+        float lam = (i < ntok) ? token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + i, p.L) : 0.f;
+        float x = lam;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float2 f = unpack_bf16(wv[j]);
-            wv[j] = pack_bf16(feature_map(p.phi, f.x) * w, feature_map(p.phi, f.y) * w);
-          }
-          *q4 = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        for (int off = 1; off < 32; off <<= 1) {
+          float y = __shfl_down_sync(0xffffffffu, x, off);
+          if (lane + off < 32) x += y;
         }
-        fence_proxy_async_smem();
+        if (lane == 0) scr[warp - WG1] = x;
+        named_bar_sync(BAR_XG0, 128);
+        float later = carry;
+        for (int w2 = (warp - WG1) + 1; w2 < 4; ++w2) later += scr[w2];
+        if (i < ntok) suf[i] = x - lam + later;
+        const float block_total = scr[0] + scr[1] + scr[2] + scr[3];
+        named_bar_sync(BAR_XG0, 128);
+        carry += block_total;
       }
-      named_bar_sync(BAR_WG1, 128);
+      seg_total = carry;
+    }
+    named_bar_sync(BAR_XG, 256);  // suffix sums visible to both groups
+    const bool phi = p.phi != LA_PHI_IDENTITY;
+    for (int c = g; c < nc; c += 2) {
+      const int s = c % NST;
+      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, gbar)) break;
+      unsigned char *kt = smem + s * SM::STAGE;
+      if (scale) {
+        if (t < 64) wrow[s * 64 + t] = __expf(suf[c * CH + t]);
+        named_bar_sync(gbar, 128);
+      }
+      const float *w = wrow + s * 64;
+      if (phi && scale) tile_pass<D, true, true>(kt, w, t, 128);
+      else if (phi) tile_pass<D, true, false>(kt, w, t, 128);
+      else if (scale) tile_pass<D, false, true>(kt, w, t, 128);
+      fence_proxy_async_smem();
+      named_bar_sync(gbar, 128);
       if (t == 0) mbar_arrive(&ready[s]);
     }
-    // Read the accumulated state out of TMEM and store it as segment slot s+1.
-    if (wait_wg(done, 0, ctl, p.err, KID_PREFILL_TC_STATE, 4, BAR_WG1)) {
+    // Read the accumulated state out of TMEM (group 0) into segment slot s+1.
+    if (g == 0 && wait_wg(done, 0, ctl, p.err, KID_PREFILL_TC_STATE, 4, BAR_XG0)) {
       tc_fence_after();
       const int quarter = warp & 3;
       const int row = acc_row<D>(quarter, lane);
-      float *dst = p.ws_state + (((size_t)bh * p.n_seg + seg + 1) * D) * D;
+      if (!LA_CHK(seg + 1 < p.n_seg && bh < p.BH, KID_PREFILL_TC_STATE, 4)) seg_total = 0.f;
+      float *dst = p.ws_state + (((size_t)bh * p.n_seg + min(seg + 1, p.n_seg - 1)) * D) * D;
 #pragma unroll 1
-      for (int col = 0; col < D; col += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + col, r);
+      for (int col = 0; col < D; col += 32) {
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, r);
         tmem_ld_wait();
         if (row >= 0) {
           float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * D + col);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
+          for (int j = 0; j < 8; ++j)
             o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
         }
@@ -327,6 +403,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       if (t == 0) p.ws_logdec[(size_t)bh * p.n_seg + seg] = seg_total;
     }
   }
+  __syncwarp();  // lanes that skipped a lane-0 role loop wait for lane 0
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -371,12 +448,13 @@ struct OutSmem {
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
   static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // [D][D] bf16, MN-major blocks
   static constexpr uint32_t S_BLOCK = D * 128;             // one 64-column block
-  static constexpr uint32_t OFF_O = OFF_S + D * D * 2;     // [64][D] bf16 store staging
-  static constexpr uint32_t OFF_LAM = OFF_O + TILE;        // [NST][64] floats
-  static constexpr uint32_t OFF_A = OFF_LAM + NST * 64 * 4;
-  static constexpr uint32_t OFF_SCR = OFF_A + 16 * 4;      // warp carries
+  static constexpr uint32_t OFF_O = OFF_S + D * D * 2;     // 2 x [64][D] bf16 store staging
+  static constexpr uint32_t OFF_LAM = OFF_O + 2 * TILE;    // [NST][64] inclusive prefix
+  static constexpr uint32_t OFF_QF = OFF_LAM + NST * 64 * 4;  // [NST][64] exp(Lam_i)
+  static constexpr uint32_t OFF_KF = OFF_QF + NST * 64 * 4;   // [NST][64] exp(A - Lam_j)
+  static constexpr uint32_t OFF_SCR = OFF_KF + NST * 64 * 4;  // 16 floats
   static constexpr uint32_t OFF_BAR = OFF_SCR + 16 * 4;
-  static constexpr int NBAR = 3 * NST + 2 * 5 + 1;
+  static constexpr int NBAR = 4 * NST + 2 * 5 + 2;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = OFF_CTL + 64;
   // TMEM columns
@@ -385,6 +463,10 @@ struct OutSmem {
   static constexpr uint32_t T_S = 128 + 2 * D;
   static constexpr uint32_t T_COLS = 512;
 };
+
+constexpr int kThreadsOut = 512;  // warps: 0 TMA, 1 MMA, 2-3 spare, 4-7 WG1, 8-11 WG2, 12-15 WG3
+constexpr int WG3 = 12;
+constexpr uint32_t BAR_WG3 = 3;
 
 template <int D>
 __global__ void __launch_bounds__(kThreadsOut, 1)
@@ -396,17 +478,20 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   constexpr int NST = SM::NST;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
-  float *Aend = reinterpret_cast<float *>(smem + SM::OFF_A);
+  float *qfac = reinterpret_cast<float *>(smem + SM::OFF_QF);
+  float *kfac = reinterpret_cast<float *>(smem + SM::OFF_KF);
   float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
-  uint64_t *xdone = empty + NST;       // stage transformed (phi), Lam ready
-  uint64_t *p_full = xdone + NST;      // [2] MMA1 done
-  uint64_t *p_ready = p_full + 2;      // [2] P in smem, Q/K rescaled
+  uint64_t *xdone = empty + NST;       // [NST] phi applied, Lam ready
+  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K rows rescaled by the decay factors
+  uint64_t *p_full = qk_ready + NST;   // [2] MMA1 done
+  uint64_t *p_ready = p_full + 2;      // [2] P in smem
   uint64_t *p_free = p_ready + 2;      // [2] MMA2 done reading P smem
   uint64_t *c_done = p_free + 2;       // [2] MMA3 + MMA4 done
   uint64_t *o_free = c_done + 2;       // [2] O TMEM buffer read
   uint64_t *s_ready = o_free + 2;      // S smem (and TMEM S) ready
+  uint64_t *drain = s_ready + 1;       // abort path: all issued MMAs done
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -424,12 +509,17 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   }
   const bool has_init = S_in != nullptr;
   const bool decay = p.decay_kind != LA_DECAY_NONE;
+  if (tid == 0) {
+    LA_CHK(bh < p.BH && seg < p.n_seg && nc >= 1 && nc <= p.seg_chunks, KID_PREFILL_TC_OUT, 5);
+    LA_CHK(!p.S_final || bh < p.BH, KID_PREFILL_TC_OUT, 6);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       mbar_init(&xdone[s], 1);
+      mbar_init(&qk_ready[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
@@ -439,6 +529,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&o_free[i], 1);
     }
     mbar_init(s_ready, 1);
+    mbar_init(drain, 1);
     ctl->abort = 0;
     fence_mbarrier_init();
   }
@@ -450,6 +541,10 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  const bool trace_on = blockIdx.x == (gridDim.x > 1 ? 1 : 0) && blockIdx.y == 0;
+  const long long t0 = clock64();
+  (void)trace_on;
+  (void)t0;
 
   if (warp == W_TMA) {
     // ------------------------------------------------------------ producer
@@ -458,6 +553,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmO);
+      int issued = 0;
       for (int c = 0; c < nc; ++c) {
         const int s = c % NST;
         if (c >= NST &&
@@ -467,11 +563,21 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
         const int tok = tok0 + c * CH;
         for (int b = 0; b < D / BOX; ++b) {
+          if (!LA_CHK(b * BOX + BOX <= D && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 2))
+            continue;
           tma_load_3d(st + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
           tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
           tma_load_3d(st + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
         }
+        LA_TRACE_EVENT(trace_on, t0, 0, c);
+        issued = c + 1;
       }
+      if (*(volatile uint32_t *)&ctl->abort)  // loads still landing must land first
+        for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+      // Producer tail: the releases of the last stages come from tcgen05.commit
+      // and land asynchronously; wait for them so that no mbarrier arrival
+      // reaches this CTA's shared memory after it has exited.
+      for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
     }
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
@@ -483,8 +589,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       const uint32_t sbase = smem_u32(smem);
       const uint32_t s_smem = sbase + SM::OFF_S;
       auto q_of = [&](int s) { return sbase + s * SM::STAGE; };
-      auto issue_qk = [&](int c) {
+      // QK^T of chunk c into P buffer c & 1, once its tile is transformed.
+      auto issue_qk = [&](int c) -> bool {
         const int s = c % NST;
+        if (!wait1(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 2)) return false;
+        tc_fence_after();
         const uint32_t qa = q_of(s), ka = qa + SM::TILE;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -493,36 +602,32 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                    smem_desc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
         }
         mma_commit(&p_full[c & 1]);
+        return true;
       };
-      bool ok = wait1(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 2);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0);
-      }
+      bool ok = issue_qk(0) && (nc < 2 || issue_qk(1));
       for (int c = 0; ok && c < nc; ++c) {
         const int s = c % NST, b = c & 1;
         const uint32_t qa = q_of(s), ka = qa + SM::TILE, va = qa + 2 * SM::TILE;
         const uint32_t o_t = tmem + SM::T_O + D * b;
         if (!(ok = wait1(&p_ready[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
+        if (decay &&
+            !(ok = wait1(&qk_ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
+          break;
         if (c >= 2 &&
-            !(ok = wait1(&o_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
+            !(ok = wait1(&o_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
           break;
         tc_fence_after();
+        LA_TRACE_EVENT(trace_on, t0, 5, c);
         const uint32_t pa = sbase + SM::OFF_P + 8192 * b;
 #pragma unroll
         for (int kk = 0; kk < CH / 16; ++kk)   // O = P V
           mma_bf16(o_t, smem_desc_sw128(pa + 32 * kk, 16, 1024),
                    smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_pv, kk > 0);
         mma_commit(&p_free[b]);
-        if (c + 1 < nc) {
-          const int s1 = (c + 1) % NST;
-          if (!(ok = wait1(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
-            break;
-          tc_fence_after();
-          issue_qk(c + 1);
-        }
+        LA_TRACE_EVENT(trace_on, t0, 6, c);
         if (!(ok = wait1(s_ready, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
         tc_fence_after();
+        LA_TRACE_EVENT(trace_on, t0, 8, c);
         if (has_init || c > 0) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {  // O += Qt S
@@ -538,22 +643,32 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                    (has_init || c > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&c_done[b]);
         mma_commit(&empty[s]);
+        LA_TRACE_EVENT(trace_on, t0, 9, c);
+        if (c + 2 < nc) {
+          ok = issue_qk(c + 2);
+          LA_TRACE_EVENT(trace_on, t0, 7, c);
+        }
       }
+      if (!ok) {  // let every issued MMA finish before TMEM is released
+        mma_commit(drain);
+        drain_wait(drain, 0);
+      }
+      // The last P-buffer releases are committed but never waited on by the
+      // P epilogue: observe them before the CTA can exit.
+      for (int c = max(0, nc - 2); c < nc; ++c) drain_wait(&p_free[c & 1], (c >> 1) & 1);
     }
   } else if (warp >= WG1 && warp < WG2) {
-    // ------------------------------------------------------------ WG1: phi, Lam, P
+    // ------------------------------------------------------------ WG1: Lam, phi, rescale
     const int t = tid - WG1 * 32;
-    const int quarter = warp & 3;
-    const int prow = acc_row<64>(quarter, lane);
-    for (int c = 0; c < nc; ++c) {
-      const int s = c % NST, b = c & 1;
+    const bool phi = p.phi != LA_PHI_IDENTITY;
+    auto prep = [&](int c) -> bool {
+      const int s = c % NST;
+      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 7, BAR_WG1))
+        return false;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);
       unsigned char *qt = smem + s * SM::STAGE;
-      unsigned char *kt = qt + SM::TILE;
-      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 7, BAR_WG1)) break;
-      // inclusive prefix of the chunk's log decays over 64 tokens (warps 4, 5)
-      if (t < 64) {
-        const int tok = tok0 + c * CH + t;
-        float x = decay ? token_lambda(p.decay_kind, p.decay, h, bhL, tok, p.L) : 0.f;
+      if (decay && t < 64) {  // inclusive prefix of the chunk's log decays (warps 4, 5)
+        float x = token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + c * CH + t, p.L);
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
           float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -562,200 +677,129 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (t == 31) scr[0] = x;
         lam[s * 64 + t] = x;
       }
-      if (p.phi != LA_PHI_IDENTITY) {
-        transform_tile<D>(qt, p.phi, nullptr, t, 128);
-        transform_tile<D>(kt, p.phi, nullptr, t, 128);
+      if (phi) {
+        tile_pass<D, true, false>(qt, nullptr, t, 128);
+        tile_pass<D, true, false>(qt + SM::TILE, nullptr, t, 128);
         fence_proxy_async_smem();
       }
       named_bar_sync(BAR_WG1, 128);
-      if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
-      named_bar_sync(BAR_WG1, 128);
-      if (t == 63) Aend[s] = lam[s * 64 + 63];
+      if (decay) {
+        if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
+        named_bar_sync(BAR_WG1, 128);
+        if (t < 64) {
+          const float A = lam[s * 64 + 63];
+          const float li = lam[s * 64 + t];
+          qfac[s * 64 + t] = __expf(li);
+          kfac[s * 64 + t] = __expf(A - li);
+        }
+      } else if (t < 64) {
+        lam[s * 64 + t] = 0.f;
+      }
       named_bar_sync(BAR_WG1, 128);
       if (t == 0) mbar_arrive(&xdone[s]);
-
-      // P epilogue: mask, decay, bf16, into P smem (K-major, 64 x 64)
-      if (!wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 8, BAR_WG1)) break;
-      if (c >= 2 &&
-          !wait_wg(&p_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG1))
-        break;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
+      return true;
+    };
+    // Decay: once QK^T of chunk c has consumed the unscaled tiles, scale the
+    // rows in place: Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j.
+    auto rescale = [&](int c) -> bool {
+      const int s = c % NST, b = c & 1;
+      if (!wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 8, BAR_WG1))
+        return false;
+      unsigned char *qt = smem + s * SM::STAGE;
+      tile_pass<D, false, true>(qt, qfac + s * 64, t, 128);
+      tile_pass<D, false, true>(qt + SM::TILE, kfac + s * 64, t, 128);
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_WG1, 128);
+      if (t == 0) mbar_arrive(&qk_ready[s]);
+      return true;
+    };
+    bool ok = nc > 0 && prep(0);
+    for (int c = 0; ok && c < nc; ++c) {
+      if (c + 1 < nc && !(ok = prep(c + 1))) break;
+      if (decay && !(ok = rescale(c))) break;
+    }
+  } else if (warp >= WG2 && warp < WG3) {
+    // ------------------------------------------------------------ WG2: P and O epilogues
+    const int t = tid - WG2 * 32;
+    const int quarter = warp & 3;
+    const int row = acc_row<64>(quarter, lane);   // row within the chunk
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto p_epilogue = [&](int c) -> bool {
+      const int s = c % NST, b = c & 1;
+      if (!wait_wg(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 15, BAR_WG2) ||
+          !wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG2))
+        return false;
+      if (c >= 2 && !wait_wg(&p_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 10,
+                             BAR_WG2))
+        return false;
       tc_fence_after();
-      const float *lm = lam + s * 64;
-      unsigned char *ps = smem + SM::OFF_P + 8192 * b;
-#pragma unroll 1
-      for (int col = 0; col < 64; col += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + SM::T_P + 64 * b + col, r);
-        tmem_ld_wait();
-        if (prow >= 0) {
-          const float li = lm[prow];
-          uint32_t pk[8];
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 3, c);
+      __syncwarp();
+      uint32_t r[2][32];
+      tmem_ld32(tmem + lane_off + SM::T_P + 64 * b, r[0]);
+      tmem_ld32(tmem + lane_off + SM::T_P + 64 * b + 32, r[1]);
+      tmem_ld_wait();
+      if (row >= 0) {
+        const float *lm = lam + s * 64;
+        const float li = lm[row];
+        unsigned char *ps = smem + SM::OFF_P + 8192 * b;
 #pragma unroll
-          for (int j = 0; j < 16; j += 2) {
-            const int j0 = col + j, j1 = col + j + 1;
-            float v0 = j0 <= prow ? __uint_as_float(r[j]) : 0.f;
-            float v1 = j1 <= prow ? __uint_as_float(r[j + 1]) : 0.f;
-            if (decay) {
-              v0 *= j0 <= prow ? __expf(li - lm[j0]) : 0.f;
-              v1 *= j1 <= prow ? __expf(li - lm[j1]) : 0.f;
+        for (int hlf = 0; hlf < 2; ++hlf) {
+#pragma unroll
+          for (int q16 = 0; q16 < 2; ++q16) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+              const int j0 = hlf * 32 + q16 * 16 + j;
+              float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
+              float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
+              if (decay) {
+                v0 *= __expf(fminf(li - lm[j0], 0.f));
+                v1 *= __expf(fminf(li - lm[j0 + 1], 0.f));
+              }
+              pk[j >> 1] = pack_bf16(v0, v1);
             }
-            pk[j >> 1] = pack_bf16(v0, v1);
+            st_row16(ps, 8192, row, hlf * 32 + q16 * 16, pk);
           }
-          const int ch0 = col >> 3;
-          *reinterpret_cast<uint4 *>(ps + prow * 128 + (((ch0) ^ (prow & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4 *>(ps + prow * 128 + (((ch0 + 1) ^ (prow & 7)) << 4)) =
-              make_uint4(pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-      if (decay) {  // Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j, in place
-        const float A = Aend[s];
-        constexpr int kChunks = 64 * D * 2 / 16;
-        for (int x = t; x < 2 * kChunks; x += 128) {
-          const bool isk = x >= kChunks;
-          const int xx = isk ? x - kChunks : x;
-          const int row = (xx & 511) >> 3;
-          const float w = isk ? __expf(A - lm[row]) : __expf(lm[row]);
-          uint4 *q4 = reinterpret_cast<uint4 *>((isk ? kt : qt) + (size_t)xx * 16);
-          uint4 u = *q4;
-          uint32_t wv[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float2 f = unpack_bf16(wv[j]);
-            wv[j] = pack_bf16(f.x * w, f.y * w);
-          }
-          *q4 = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      named_bar_sync(BAR_WG1, 128);
-      if (t == 0) mbar_arrive(&p_ready[b]);
-    }
-  } else if (warp >= WG2) {
-    // ------------------------------------------------------------ WG2: state, O
-    const int t = tid - WG2 * 32;
-    const int quarter = warp & 3;
-    const int srow = acc_row<D>(quarter, lane);    // state row (d_k index)
-    const int orow = acc_row<64>(quarter, lane);   // output row within the chunk
-    unsigned char *s_sm = smem + SM::OFF_S;
-    unsigned char *o_sm = smem + SM::OFF_O;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // Write one 16-column piece of state row `srow`: bf16 copy into S smem
-    // (MN-major: row = d_k index, 64-column blocks), and optionally a scaled
-    // fp32 copy back into TMEM.
-    auto put_state = [&](int col, const float *v, float scale, bool to_tmem) {
-      if (srow >= 0) {
-        uint32_t pk[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) pk[j] = pack_bf16(v[2 * j], v[2 * j + 1]);
-        unsigned char *blk = s_sm + (col / 64) * SM::S_BLOCK + srow * 128;
-        const int ch0 = (col % 64) >> 3;
-        *reinterpret_cast<uint4 *>(blk + ((ch0 ^ (srow & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4 *>(blk + (((ch0 + 1) ^ (srow & 7)) << 4)) =
-            make_uint4(pk[4], pk[5], pk[6], pk[7]);
-      }
-      if (to_tmem) {
-        uint32_t r[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(v[j] * scale);
-        tmem_st16(tmem + lane_off + SM::T_S + col, r);
-      }
-    };
-    bool ok = true;
-    // initial state for chunk 0
-    if (nc > 0) {
-      ok = wait_wg(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 10, BAR_WG2);
-      if (ok && has_init) {
-        const float a0 = __expf(Aend[0]);
-#pragma unroll 1
-        for (int col = 0; col < D; col += 16) {
-          float v[16];
-          if (srow >= 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float4 f = src[j];
-              v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.f;
-          }
-          put_state(col, v, a0, true);
-        }
-        tmem_st_wait();
-      }
-      if (ok) {
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(BAR_WG2, 128);
-        if (t == 0) mbar_arrive(s_ready);
-      }
-    }
-    for (int c = 0; ok && c < nc; ++c) {
-      const int b = c & 1;
-      if (!(ok = wait_wg(&c_done[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11,
-                         BAR_WG2)))
-        break;
-      tc_fence_after();
-      // ---- state for the next chunk (critical path first)
-      if (c + 1 < nc) {
-        const int s1 = (c + 1) % NST;
-        if (!(ok = wait_wg(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 12,
-                           BAR_WG2)))
-          break;
-        const float a1 = __expf(Aend[s1]);
-#pragma unroll 1
-        for (int col = 0; col < D; col += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_off + SM::T_S + col, r);
-          tmem_ld_wait();
-          float v[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
-          put_state(col, v, a1, decay);
-        }
-        if (decay) tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(BAR_WG2, 128);
-        if (t == 0) mbar_arrive(s_ready);
-      } else if (last_seg && p.S_final) {
-#pragma unroll 1
-        for (int col = 0; col < D; col += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_off + SM::T_S + col, r);
-          tmem_ld_wait();
-          if (srow >= 0) {
-            float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-          }
-        }
-      }
-      // ---- output of chunk c: TMEM -> bf16 -> staging smem -> TMA store
-      if (t == 0) tma_store_wait_read_all();  // previous store done reading staging
       named_bar_sync(BAR_WG2, 128);
+      if (t == 0) mbar_arrive(&p_ready[b]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 4, c);
+      return true;
+    };
+    auto o_epilogue = [&](int c) -> bool {
+      const int b = c & 1;
+      if (!wait_wg(&c_done[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
+        return false;
+      tc_fence_after();
+      if (t == 0) tma_store_wait_read<1>();  // the store that used this buffer is done
+      __syncwarp();
+      named_bar_sync(BAR_WG2, 128);
+      unsigned char *o_sm = smem + SM::OFF_O + b * SM::TILE;
 #pragma unroll 1
-      for (int col = 0; col < D; col += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_off + SM::T_O + D * b + col, r);
+      for (int col = 0; col < D; col += 64) {
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row branch
+        uint32_t r[2][32];
+        tmem_ld32(tmem + lane_off + SM::T_O + D * b + col, r[0]);
+        tmem_ld32(tmem + lane_off + SM::T_O + D * b + col + 32, r[1]);
         tmem_ld_wait();
-        if (orow >= 0) {
-          uint32_t pk[8];
+        if (row >= 0) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            pk[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-          unsigned char *box = o_sm + (col / 64) * BOX_BYTES + orow * 128;
-          const int ch0 = (col % 64) >> 3;
-          *reinterpret_cast<uint4 *>(box + ((ch0 ^ (orow & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4 *>(box + (((ch0 + 1) ^ (orow & 7)) << 4)) =
-              make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          for (int hlf = 0; hlf < 2; ++hlf) {
+#pragma unroll
+            for (int q16 = 0; q16 < 2; ++q16) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                pk[j] = pack_bf16(__uint_as_float(r[hlf][q16 * 16 + 2 * j]),
+                                  __uint_as_float(r[hlf][q16 * 16 + 2 * j + 1]));
+              st_row16(o_sm, BOX_BYTES, row, col + hlf * 32 + q16 * 16, pk);
+            }
+          }
         }
       }
       fence_proxy_async_smem();
@@ -764,12 +808,130 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (t == 0) {
         mbar_arrive(&o_free[b]);
         for (int bb = 0; bb < D / BOX; ++bb)
-          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok0 + c * CH, bh);
+          if (LA_CHK(bb * BOX + BOX <= D && tok0 + c * CH < p.L && bh < p.BH,
+                     KID_PREFILL_TC_OUT, 3))
+            tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok0 + c * CH, bh);
         tma_store_commit();
+        LA_TRACE_EVENT(trace_on, t0, 12, c);
+      }
+      return true;
+    };
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      ok = p_epilogue(c);
+      if (ok && c >= 1) ok = o_epilogue(c - 1);
+    }
+    if (ok && nc > 0) o_epilogue(nc - 1);
+    if (t == 0) tma_store_wait_all();
+  } else if (warp >= WG3) {
+    // ------------------------------------------------------------ WG3: the state chain
+    const int t = tid - WG3 * 32;
+    const int quarter = warp & 3;
+    const int srow = acc_row<D>(quarter, lane);    // state row (d_k index)
+    unsigned char *s_sm = smem + SM::OFF_S;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    // 32 columns of state row srow: bf16 copy into S smem (MN-major blocks),
+    // and optionally the scaled fp32 values back into TMEM.
+    auto put32 = [&](int col, uint32_t (&r)[32], float scale, bool to_tmem) {
+      if (srow >= 0) {
+#pragma unroll
+        for (int q16 = 0; q16 < 2; ++q16) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            pk[j] = pack_bf16(__uint_as_float(r[q16 * 16 + 2 * j]),
+                              __uint_as_float(r[q16 * 16 + 2 * j + 1]));
+          st_row16(s_sm, SM::S_BLOCK, srow, col + q16 * 16, pk);
+        }
+      }
+      if (to_tmem) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * scale);
+        __syncwarp();
+        tmem_st32(tmem + lane_off + SM::T_S + col, r);
+      }
+    };
+    bool ok = true;
+    if (nc > 0) {
+      ok = wait_wg(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 12, BAR_WG3);
+      if (ok && has_init) {
+        const float a0 = __expf(lam[63]);
+#pragma unroll 1
+        for (int col = 0; col < D; col += 32) {
+          uint32_t r[32];
+          if (srow >= 0) {
+            const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4 f = src[j];
+              r[4 * j] = __float_as_uint(f.x);
+              r[4 * j + 1] = __float_as_uint(f.y);
+              r[4 * j + 2] = __float_as_uint(f.z);
+              r[4 * j + 3] = __float_as_uint(f.w);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          put32(col, r, a0, true);
+        }
+        tmem_st_wait();
+      }
+      if (ok) {
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(BAR_WG3, 128);
+        if (t == 0) mbar_arrive(s_ready);
       }
     }
-    if (t == 0) tma_store_wait_all();
+    for (int c = 0; ok && c < nc; ++c) {
+      const int b = c & 1;
+      if (!(ok = wait_wg(&c_done[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13,
+                         BAR_WG3)))
+        break;
+      tc_fence_after();
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 10, c);
+      if (c + 1 < nc) {
+        const int s1 = (c + 1) % NST;
+        if (!(ok = wait_wg(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
+                           BAR_WG3)))
+          break;
+        const float a1 = __expf(lam[s1 * 64 + 63]);
+#pragma unroll 1
+        for (int col = 0; col < D; col += 64) {
+          __syncwarp();
+          uint32_t r[2][32];
+          tmem_ld32(tmem + lane_off + SM::T_S + col, r[0]);
+          tmem_ld32(tmem + lane_off + SM::T_S + col + 32, r[1]);
+          tmem_ld_wait();
+          put32(col, r[0], a1, decay);
+          put32(col + 32, r[1], a1, decay);
+        }
+        if (decay) tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(BAR_WG3, 128);
+        if (t == 0) mbar_arrive(s_ready);
+        LA_TRACE_EVENT(trace_on && t == 0, t0, 11, c);
+      } else if (last_seg && p.S_final) {
+#pragma unroll 1
+        for (int col = 0; col < D; col += 32) {
+          __syncwarp();
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + SM::T_S + col, r);
+          tmem_ld_wait();
+          if (srow >= 0) {
+            float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D + col);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          }
+        }
+      }
+    }
   }
+  __syncwarp();  // lanes that skipped a lane-0 role loop wait for lane 0
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -821,6 +983,18 @@ size_t ws_bytes_for(int B, int H, int L, int D) {
   return st + ((bh * pl.n_seg * sizeof(float) + 255) & ~(size_t)255);
 }
 
+// Opt the kernels into their dynamic shared memory once per device.
+template <typename K>
+cudaError_t set_smem_once(K kern, size_t bytes, int *done_for_device) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && done_for_device[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev < 64) done_for_device[dev] = 1;
+  return e;
+}
+
 template <int D>
 cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   const Plan pl = make_plan(a.B, a.H, a.L);
@@ -828,6 +1002,7 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   TcParams p{};
   p.H = a.H;
   p.L = a.L;
+  p.BH = BH;
   p.n_chunks = pl.n_chunks;
   p.seg_chunks = pl.seg_chunks;
   p.n_seg = pl.n_seg;
@@ -853,13 +1028,20 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   if (pl.n_seg > 1) {
     using SS = StateSmem<D>;
     auto ks = segment_state_kernel<D>;
-    e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SS::BYTES);
+    static int smem_set_state[64];
+    e = set_smem_once(ks, SS::BYTES, smem_set_state);
     if (e != cudaSuccess) return e;
     ks<<<dim3(pl.n_seg - 1, BH), kThreadsState, SS::BYTES, a.stream>>>(tk, tv, p);
     if ((e = cudaGetLastError()) != cudaSuccess) {
       if (why) *why = "la_chunk_fwd: segment-state kernel launch";
       return e;
     }
+#ifdef LA_CHECKED
+    if ((e = cudaStreamSynchronize(a.stream)) != cudaSuccess) {
+      if (why) *why = "la_chunk_fwd [checked]: segment-state kernel failed";
+      return e;
+    }
+#endif
     const int n4 = D * D / 4;
     state_scan_kernel<<<dim3((n4 + 255) / 256, BH), 256, 0, a.stream>>>(
         D, pl.n_seg, a.S0, p.ws_state, p.ws_logdec);
@@ -867,14 +1049,25 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
       if (why) *why = "la_chunk_fwd: state-scan kernel launch";
       return e;
     }
+#ifdef LA_CHECKED
+    if ((e = cudaStreamSynchronize(a.stream)) != cudaSuccess) {
+      if (why) *why = "la_chunk_fwd [checked]: state-scan kernel failed";
+      return e;
+    }
+#endif
   }
   using OS = OutSmem<D>;
   auto ko = chunk_output_kernel<D>;
-  e = cudaFuncSetAttribute(ko, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)OS::BYTES);
+  static int smem_set_out[64];
+  e = set_smem_once(ko, OS::BYTES, smem_set_out);
   if (e != cudaSuccess) return e;
   ko<<<dim3(pl.n_seg, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
   if ((e = cudaGetLastError()) != cudaSuccess && why)
     *why = "la_chunk_fwd: chunk-output kernel launch";
+#ifdef LA_CHECKED
+  if (e == cudaSuccess && (e = cudaStreamSynchronize(a.stream)) != cudaSuccess && why)
+    *why = "la_chunk_fwd [checked]: chunk-output kernel failed";
+#endif
   return e;
 }
 

@@ -78,6 +78,34 @@ def test_headline_fp32_workload():
     parity.check(S, S_ref, "f32", "S_final")
 
 
+# Many (b, h) sequences of a few chunks each: the launcher then gives every
+# output CTA several chunks (G > 1) in one or more segments, which exercises
+# the stage ring, the lookahead and the state chain at small sizes.  B*H = 152
+# gives two segments of five chunks; B*H = 304 gives one segment of ten.
+MULTI = [
+    # (B, H, L, d, phi, decay, s0)
+    (2, 76, 640, 64, "identity", "none", None),
+    (2, 76, 640, 64, "elu1", "head", None),
+    (2, 76, 640, 64, "identity", "logit", 0.1),
+    (2, 76, 640, 128, "identity", "none", None),
+    (2, 76, 640, 128, "identity", "head", None),
+    (2, 76, 600, 128, "elu1", "logit", 0.1),
+    (4, 76, 640, 128, "identity", "head", 0.1),
+    (4, 76, 630, 64, "elu1", "token", None),
+]
+
+
+@pytest.mark.parametrize("case", MULTI, ids=[f"{c[0]}x{c[1]}x{c[2]}_d{c[3]}_{c[4]}_{c[5]}" for c in MULTI])
+def test_multi_chunk_segments_match_oracle(case):
+    B, H, L, d, phi, decay, s0 = case
+    w, inp = _make(B, H, L, d, d, "bf16", phi, decay, 64, s0)
+    O, S = gpu_prefill(inp, w.phi, 64)
+    pairs = [(0, 0), (B - 1, H - 1), (B // 2, H // 3), (1, 5)]
+    O_ref, S_ref = oracle_prefill(inp, w.phi, pairs)
+    parity.check(select_pairs(O, pairs), O_ref, "bf16", "O")
+    parity.check(select_pairs(S, pairs), S_ref, "bf16", "S_final")
+
+
 FULL = {
     "B4_H16_L4096_d64_elu1": [(0, 0), (1, 7), (2, 13), (3, 15)],
     "B2_H32_L8192_d128_retnet": [(0, 0), (0, 31), (1, 16), (1, 5)],
