@@ -113,6 +113,32 @@ def la_chunk_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, O=No
     return O, S_final
 
 
+def la_chunk_fwd_noalloc(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, O=None,
+                         S_final=None, want_final_state=True, stream=None):
+    """la_chunk_fwd without a caller workspace, for callers that cannot
+    allocate device memory at call time: the library's fixed static scratch
+    (la_chunk_fwd_noalloc_scratch_bytes() bytes per GPU) holds the segment
+    states.  Calls on one device share that scratch, so calls that may run
+    concurrently on the GPU must be ordered by the caller.  Output buffers
+    are allocated here only when not given; pass O and S_final to allocate
+    nothing at all."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if O is None:
+        O = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    if S_final is None and want_final_state:
+        S_final = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    _need_cuda(q, k, v, decay, S0, O, S_final)
+    _check(_native.load().la_chunk_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, chunk, DECAY[decay_kind],
+        _ptr(decay), _ptr(S0), _ptr(O), _ptr(S_final), _stream(stream)))
+    return O, S_final
+
+
+def la_chunk_fwd_noalloc_scratch_bytes() -> int:
+    return int(_native.load().la_chunk_fwd_noalloc_scratch_bytes())
+
+
 def _chunk_fwd_host(q, k, v, chunk, decay_kind, decay, S0, want_final_state):
     dev = torch.device("cuda", torch.cuda.current_device())
     to = lambda t: None if t is None else t.to(dev, non_blocking=True)  # noqa: E731

@@ -49,6 +49,8 @@ const char *kernel_name(unsigned int id) {
 }
 }  // namespace
 
+void set_last_error(const char *msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 unsigned int *device_error_word() {
   // The symbol's device address, looked up for the current device on each
   // call (cheap; avoids caching an address across devices).

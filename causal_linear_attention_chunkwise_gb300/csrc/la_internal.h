@@ -50,6 +50,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why);
 bool decode_supported(int dk, int dv);
 cudaError_t launch_decode(const DecodeArgs &a);
 
+// Set the message la_last_error() returns on the calling thread.
+void set_last_error(const char *msg);
+
 // Self-test of the bounded-wait timeout path.
 cudaError_t launch_wait_timeout_selftest(unsigned int spin_limit, cudaStream_t s);
 

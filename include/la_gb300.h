@@ -131,6 +131,41 @@ la_status la_decode_step(const void *q, const void *k, const void *v, int dtype,
                          int B, int H, int d_k, int d_v,
                          const float *log_alpha, float *S, void *o, void *cuda_stream);
 
+/*
+ * la_chunk_fwd for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is a deployment variant of la_chunk_fwd.)
+ *
+ * Some callers cannot call cudaMalloc where they run prefill -- code inside
+ * an allocator or memory-pool callback, processes whose device footprint is
+ * fixed after start-up, or code that runs while another component holds the
+ * allocator.  This entry point takes the same arguments as la_chunk_fwd
+ * without the workspace: the segment states live in one static device array
+ * of LA_NOALLOC_SCRATCH_BYTES that the library's CUDA module reserves on
+ * every GPU that loads it, held until the process exits.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   - Problems whose workspace (la_chunk_fwd_workspace_bytes) exceeds
+ *     LA_NOALLOC_SCRATCH_BYTES are rejected with LA_ERR_UNSUPPORTED before
+ *     any device work; la_last_error() names both sizes.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current) and caches it; make that first call before
+ *     any stream capture on the device.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind.  Nothing in it has to start at zero (each call writes every
+ *     part it reads before reading it), but calls whose kernels overlap on
+ *     the GPU (different streams, or different host threads without
+ *     ordering) race on it and give wrong results: order them.
+ * Errors: as la_chunk_fwd, plus LA_ERR_UNSUPPORTED for a too-large problem.
+ */
+#define LA_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+la_status la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, int dtype,
+                               int B, int H, int L, int d_k, int d_v, int chunk,
+                               int decay_kind, const float *decay,
+                               const float *S0, void *O, float *S_final, void *cuda_stream);
+
+/* Size in bytes of the static scratch la_chunk_fwd_noalloc uses. */
+size_t la_chunk_fwd_noalloc_scratch_bytes(void);
+
 /* Synchronise `cuda_stream`, then report and clear the device error word that
  * kernels set when a bounded wait runs out: LA_OK, LA_ERR_DEVICE_TIMEOUT (the
  * message names the kernel and the wait) or LA_ERR_CUDA. */
