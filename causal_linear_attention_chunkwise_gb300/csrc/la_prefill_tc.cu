@@ -58,7 +58,8 @@ namespace {
 constexpr int CH = 64;                  // tokens per chunk
 constexpr int BOX = 64;                 // TMA box: 64 rows x 64 bf16 (128 bytes)
 constexpr uint32_t BOX_BYTES = 8192;
-constexpr uint32_t kSpin = 1u << 22;    // polls before a wait gives up
+constexpr uint64_t kWaitNs = 2000000000ull;  // a wait gives up after 2 s
+constexpr uint32_t kSpinCap = 1u << 26;       // and after this many polls regardless
 constexpr int kMaxSegChunks = 32;       // G <= 32 (2048 tokens per segment)
 
 // Warp roles (both tcgen05 kernels).
@@ -72,23 +73,37 @@ struct Ctl {
 
 // ---------------------------------------------------------------- waits
 // Single-thread bounded wait; on timeout records the error and sets abort.
-__device__ __forceinline__ bool wait1(uint64_t *bar, uint32_t parity, Ctl *ctl,
-                                      unsigned int *err, uint32_t kid, uint32_t site) {
-  for (uint32_t i = 0; i < kSpin; ++i) {
+// The first test is inline; the polling loop is one shared out-of-line copy.
+__device__ __noinline__ bool wait1_slow(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                        unsigned int *err, uint32_t kid, uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1; i < kSpinCap; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *(volatile uint32_t *)&ctl->abort) return false;
+    if ((i & 63u) == 0) {
+      if (*(volatile uint32_t *)&ctl->abort) return false;
+      if (global_timer_ns() - t0 > kWaitNs) break;
+    }
   }
   atomicExch(&ctl->abort, 1u);
   record_device_error(err, kid, site);
   return false;
 }
 
+__device__ __forceinline__ bool wait1(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                      unsigned int *err, uint32_t kid, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait1_slow(bar, parity, ctl, err, kid, site);
+}
+
 // After an abort: wait (bounded, ignoring the abort flag) for a phase that
 // in-flight asynchronous work will still complete, so that no TMA write or
 // MMA outlives the CTA's shared memory and TMEM.
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpin; ++i)
+__device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0; i < kSpinCap; ++i) {
     if (mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) return;
+  }
 }
 
 // Warpgroup-wide bounded wait: the group's first thread polls while the
@@ -244,7 +259,7 @@ struct StateSmem {
 constexpr int kThreadsState = 384;  // warps 0..11: TMA, MMA, -, -, XG0 (4..7), XG1 (8..11)
 constexpr uint32_t BAR_XG0 = 1, BAR_XG1 = 2, BAR_XG = 3;
 
-template <int D>
+template <int D, bool PHI, bool DECAY>
 __global__ void __launch_bounds__(kThreadsState, 1)
 segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
@@ -337,7 +352,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     // Suffix sums of the segment's log decays (group 0): suf[i] = sum_{r > i}
     // lambda_r, so token i's weight is exp(suf[i]); A_s = sum of all lambda.
     const int ntok = nc * CH;
-    const bool scale = p.decay_kind != LA_DECAY_NONE;
+    constexpr bool scale = DECAY;
     float seg_total = 0.f;
     if (g == 0 && scale) {
       float carry = 0.f;
@@ -362,7 +377,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       seg_total = carry;
     }
     named_bar_sync(BAR_XG, 256);  // suffix sums visible to both groups
-    const bool phi = p.phi != LA_PHI_IDENTITY;
+    constexpr bool phi = PHI;
     for (int c = g; c < nc; c += 2) {
       const int s = c % NST;
       if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, gbar)) break;
@@ -372,9 +387,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         named_bar_sync(gbar, 128);
       }
       const float *w = wrow + s * 64;
-      if (phi && scale) tile_pass<D, true, true>(kt, w, t, 128);
-      else if (phi) tile_pass<D, true, false>(kt, w, t, 128);
-      else if (scale) tile_pass<D, false, true>(kt, w, t, 128);
+      if constexpr (phi || scale) tile_pass<D, phi, scale>(kt, w, t, 128);
       fence_proxy_async_smem();
       named_bar_sync(gbar, 128);
       if (t == 0) mbar_arrive(&ready[s]);
@@ -468,7 +481,7 @@ constexpr int kThreadsOut = 512;  // warps: 0 TMA, 1 MMA, 2-3 spare, 4-7 WG1, 8-
 constexpr int WG3 = 12;
 constexpr uint32_t BAR_WG3 = 3;
 
-template <int D>
+template <int D, bool PHI, bool DECAY>
 __global__ void __launch_bounds__(kThreadsOut, 1)
 chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
@@ -508,10 +521,10 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     S_in = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
   }
   const bool has_init = S_in != nullptr;
-  const bool decay = p.decay_kind != LA_DECAY_NONE;
+  constexpr bool decay = DECAY;
   if (tid == 0) {
-    LA_CHK(bh < p.BH && seg < p.n_seg && nc >= 1 && nc <= p.seg_chunks, KID_PREFILL_TC_OUT, 5);
-    LA_CHK(!p.S_final || bh < p.BH, KID_PREFILL_TC_OUT, 6);
+    (void)LA_CHK(bh < p.BH && seg < p.n_seg && nc >= 1 && nc <= p.seg_chunks, KID_PREFILL_TC_OUT, 5);
+    (void)LA_CHK(!p.S_final || bh < p.BH, KID_PREFILL_TC_OUT, 6);
   }
 
   if (tid == 0) {
@@ -660,7 +673,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   } else if (warp >= WG1 && warp < WG2) {
     // ------------------------------------------------------------ WG1: Lam, phi, rescale
     const int t = tid - WG1 * 32;
-    const bool phi = p.phi != LA_PHI_IDENTITY;
+    constexpr bool phi = PHI;
     auto prep = [&](int c) -> bool {
       const int s = c % NST;
       if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 7, BAR_WG1))
@@ -677,13 +690,13 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (t == 31) scr[0] = x;
         lam[s * 64 + t] = x;
       }
-      if (phi) {
+      if constexpr (phi) {
         tile_pass<D, true, false>(qt, nullptr, t, 128);
         tile_pass<D, true, false>(qt + SM::TILE, nullptr, t, 128);
         fence_proxy_async_smem();
       }
       named_bar_sync(BAR_WG1, 128);
-      if (decay) {
+      if constexpr (decay) {
         if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
         named_bar_sync(BAR_WG1, 128);
         if (t < 64) {
@@ -717,7 +730,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     bool ok = nc > 0 && prep(0);
     for (int c = 0; ok && c < nc; ++c) {
       if (c + 1 < nc && !(ok = prep(c + 1))) break;
-      if (decay && !(ok = rescale(c))) break;
+      if constexpr (decay) {
+        if (!(ok = rescale(c))) break;
+      }
     }
   } else if (warp >= WG2 && warp < WG3) {
     // ------------------------------------------------------------ WG2: P and O epilogues
@@ -754,7 +769,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
               const int j0 = hlf * 32 + q16 * 16 + j;
               float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
               float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
-              if (decay) {
+              if constexpr (decay) {
                 v0 *= __expf(fminf(li - lm[j0], 0.f));
                 v1 *= __expf(fminf(li - lm[j0 + 1], 0.f));
               }
@@ -995,7 +1010,7 @@ cudaError_t set_smem_once(K kern, size_t bytes, int *done_for_device) {
   return e;
 }
 
-template <int D>
+template <int D, bool PHI, bool DECAY>
 cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   const Plan pl = make_plan(a.B, a.H, a.L);
   const int BH = a.B * a.H;
@@ -1027,7 +1042,7 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   cudaError_t e;
   if (pl.n_seg > 1) {
     using SS = StateSmem<D>;
-    auto ks = segment_state_kernel<D>;
+    auto ks = segment_state_kernel<D, PHI, DECAY>;
     static int smem_set_state[64];
     e = set_smem_once(ks, SS::BYTES, smem_set_state);
     if (e != cudaSuccess) return e;
@@ -1057,7 +1072,7 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
 #endif
   }
   using OS = OutSmem<D>;
-  auto ko = chunk_output_kernel<D>;
+  auto ko = chunk_output_kernel<D, PHI, DECAY>;
   static int smem_set_out[64];
   e = set_smem_once(ko, OS::BYTES, smem_set_out);
   if (e != cudaSuccess) return e;
@@ -1086,9 +1101,18 @@ int prefill_tc_kernel_count(int B, int H, int L, int) {
   return make_plan(B, H, L).n_seg > 1 ? 3 : 1;
 }
 
+template <int D>
+cudaError_t launch_variant(const PrefillArgs &a, const char **why) {
+  const bool phi = a.phi != LA_PHI_IDENTITY, decay = a.decay_kind != LA_DECAY_NONE;
+  if (phi && decay) return launch_d<D, true, true>(a, why);
+  if (phi) return launch_d<D, true, false>(a, why);
+  if (decay) return launch_d<D, false, true>(a, why);
+  return launch_d<D, false, false>(a, why);
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why) {
-  if (a.dk == 128) return launch_d<128>(a, why);
-  return launch_d<64>(a, why);
+  if (a.dk == 128) return launch_variant<128>(a, why);
+  return launch_variant<64>(a, why);
 }
 
 }  // namespace la
