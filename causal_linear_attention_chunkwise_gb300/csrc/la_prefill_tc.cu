@@ -64,7 +64,7 @@ constexpr int kMaxSegChunks = 32;       // G <= 32 (2048 tokens per segment)
 
 // Warp roles (both tcgen05 kernels).
 constexpr int W_TMA = 0, W_MMA = 1, WG1 = 4, WG2 = 8;
-constexpr uint32_t BAR_WG1 = 1, BAR_WG2 = 2;
+constexpr uint32_t BAR_WG2 = 2;
 
 struct Ctl {
   uint32_t abort;
@@ -106,27 +106,36 @@ __device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
-// Warpgroup-wide bounded wait: the group's first thread polls while the
-// others sleep in a reducing named barrier that also hands them the outcome,
-// so all leave together.  The barrier orders the group's later accesses after
-// the leader's acquire of the mbarrier phase.
-__device__ __forceinline__ bool wait_wg(uint64_t *bar, uint32_t parity, Ctl *ctl,
-                                        unsigned int *err, uint32_t kid, uint32_t site,
-                                        uint32_t bar_id) {
+// Group-wide bounded wait for NT threads (t = index within the group): the
+// group's first thread polls while the others sleep in a reducing named
+// barrier that also hands them the outcome, so all leave together.  The
+// barrier orders the group's later accesses after the leader's acquire of the
+// mbarrier phase.
+template <int NT>
+__device__ __forceinline__ bool wait_grp(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                         unsigned int *err, uint32_t kid, uint32_t site,
+                                         uint32_t bar_id, int t) {
   bool ok = true;
-  if ((threadIdx.x & 127) == 0) ok = wait1(bar, parity, ctl, err, kid, site);
+  if (t == 0) ok = wait1(bar, parity, ctl, err, kid, site);
   __syncwarp();
   uint32_t any_fail;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
-      "barrier.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "barrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(any_fail)
-      : "r"(ok ? 1u : 0u), "r"(bar_id)
+      : "r"(ok ? 1u : 0u), "r"(bar_id), "n"(NT)
       : "memory");
   if (any_fail) return false;
-  if ((threadIdx.x & 127) != 0) mbar_try_wait(bar, parity);  // completed: own acquire
+  if (t != 0) mbar_try_wait(bar, parity);  // completed: own acquire
   __syncwarp();
   return true;
+}
+
+// The same for a warpgroup (four consecutive warps starting at a multiple of 4).
+__device__ __forceinline__ bool wait_wg(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                        unsigned int *err, uint32_t kid, uint32_t site,
+                                        uint32_t bar_id) {
+  return wait_grp<128>(bar, parity, ctl, err, kid, site, bar_id, threadIdx.x & 127);
 }
 
 // Debug builds (-DLA_CHECKED) bounds-check every runtime-computed TMA
@@ -154,10 +163,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&v);
 }
-__device__ __forceinline__ float2 unpack_bf16(uint32_t u) {
-  __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&u);
-  return __bfloat1622float2(v);
-}
 
 // Rows of an M=64 accumulator: row 16*i + t lives in TMEM lane 32*i + t
 // (t < 16) of lane quarter i; lanes 16..31 of each quarter are unused.
@@ -184,12 +189,25 @@ struct TcParams {
 };
 
 // ================================================================ shared pieces
-// Elementwise pass over a bf16 tile of 64 rows x D columns (D/64 swizzled 8 KB
-// boxes, 8 sixteen-byte chunks per 128-byte row): x <- phi(x) * fac[row].
-// Each thread takes chunks t, t + n, ...; four loads are issued before any use.
-template <int D, bool PHI, bool SCALE>
-__device__ __forceinline__ void tile_pass(unsigned char *tile, const float *fac, int t, int n) {
-  constexpr int kChunks = 64 * D * 2 / 16;
+// elu(x) + 1 without a branch: for x > 0 it is x + 1 > 1 = 2^0, and for x <= 0
+// exp(x) >= x + 1 (convexity), so max(x + 1, 2^(min(x, 0) log2 e)) takes the
+// right side in both cases.  The NaN-propagating max keeps a NaN input NaN.
+__device__ __forceinline__ float elu1_fast(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(x, 0.f) * 1.4426950408889634f));
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(x + 1.f), "f"(e));
+  return r;
+}
+
+// Elementwise pass over NT consecutive bf16 tiles of 64 rows x D columns (D/64
+// swizzled 8 KB boxes per tile, 8 sixteen-byte chunks per 128-byte row):
+// x <- phi(x) * fac(k, row) in tile k.  Threads t = 0..n-1 take chunks t,
+// t + n, ...; four loads are issued before any use.
+template <int D, int NT, bool PHI, bool SCALE, typename Fac>
+__device__ __forceinline__ void tile_pass(unsigned char *tile, Fac fac, int t, int n) {
+  constexpr int kTileChunks = 64 * D * 2 / 16;
+  constexpr int kChunks = NT * kTileChunks;
+#pragma unroll 1
   for (int base = 0; base < kChunks; base += 4 * n) {
     uint4 u[4];
 #pragma unroll
@@ -201,16 +219,17 @@ __device__ __forceinline__ void tile_pass(unsigned char *tile, const float *fac,
     for (int j = 0; j < 4; ++j) {
       const int x = base + j * n + t;
       if (x >= kChunks) continue;
-      const float s = SCALE ? fac[(x & 511) >> 3] : 1.f;
+      float sc = 1.f;
+      if (SCALE) sc = fac(NT == 1 || x < kTileChunks ? 0 : 1, (x & 511) >> 3);
       uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        float2 f = unpack_bf16(w[e]);
+        float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
         if (PHI) {
-          f.x = f.x > 0.f ? f.x + 1.f : __expf(f.x);
-          f.y = f.y > 0.f ? f.y + 1.f : __expf(f.y);
+          lo = elu1_fast(lo);
+          hi = elu1_fast(hi);
         }
-        w[e] = pack_bf16(f.x * s, f.y * s);
+        w[e] = pack_bf16(lo * sc, hi * sc);
       }
       u[j] = make_uint4(w[0], w[1], w[2], w[3]);
     }
@@ -387,7 +406,8 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         named_bar_sync(gbar, 128);
       }
       const float *w = wrow + s * 64;
-      if constexpr (phi || scale) tile_pass<D, phi, scale>(kt, w, t, 128);
+      if constexpr (phi || scale)
+        tile_pass<D, 1, phi, scale>(kt, [w](int, int r) { return w[r]; }, t, 128);
       fence_proxy_async_smem();
       named_bar_sync(gbar, 128);
       if (t == 0) mbar_arrive(&ready[s]);
@@ -456,20 +476,28 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
 template <int D>
 struct OutSmem {
   static constexpr int NST = (D == 128) ? 3 : 4;
+  // bf16 copies of the state: with two, the conversion of S_c+1 may overlap
+  // the MMA that still reads S_c (D = 64); D = 128 has room for one.
+  static constexpr int NSB = (D == 128) ? 1 : 2;
   static constexpr uint32_t TILE = 64 * D * 2;            // Q, K or V tile of one chunk
   static constexpr uint32_t STAGE = 3 * TILE;
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
-  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // [D][D] bf16, MN-major blocks
+  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // NSB x [D][D] bf16, MN-major blocks
   static constexpr uint32_t S_BLOCK = D * 128;             // one 64-column block
-  static constexpr uint32_t OFF_O = OFF_S + D * D * 2;     // 2 x [64][D] bf16 store staging
+  static constexpr uint32_t S_BYTES = D * D * 2;
+  static constexpr uint32_t OFF_O = OFF_S + NSB * S_BYTES; // 2 x [64][D] bf16 store staging
   static constexpr uint32_t OFF_LAM = OFF_O + 2 * TILE;    // [NST][64] inclusive prefix
-  static constexpr uint32_t OFF_QF = OFF_LAM + NST * 64 * 4;  // [NST][64] exp(Lam_i)
-  static constexpr uint32_t OFF_KF = OFF_QF + NST * 64 * 4;   // [NST][64] exp(A - Lam_j)
-  static constexpr uint32_t OFF_SCR = OFF_KF + NST * 64 * 4;  // 16 floats
+  static constexpr uint32_t OFF_RF = OFF_LAM + NST * 64 * 4;  // [NST][64] exp(Lam_i - A/2)
+  static constexpr uint32_t OFF_CF = OFF_RF + NST * 64 * 4;   // [NST][64] exp(A/2 - Lam_j)
+  static constexpr uint32_t OFF_SPLIT = OFF_CF + NST * 64 * 4; // [NST] factors usable
+  static constexpr uint32_t OFF_SCR = OFF_SPLIT + 16 * 4;      // 16 floats
   static constexpr uint32_t OFF_BAR = OFF_SCR + 16 * 4;
-  static constexpr int NBAR = 4 * NST + 2 * 5 + 2;
+  static constexpr int NBAR = 4 * NST + 2 * 5 + 3;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static_assert(OFF_P % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+  static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
   // TMEM columns
   static constexpr uint32_t T_P = 0;          // 2 x 64 columns
   static constexpr uint32_t T_O = 128;        // 2 x D columns
@@ -477,9 +505,18 @@ struct OutSmem {
   static constexpr uint32_t T_COLS = 512;
 };
 
-constexpr int kThreadsOut = 512;  // warps: 0 TMA, 1 MMA, 2-3 spare, 4-7 WG1, 8-11 WG2, 12-15 WG3
+// Warps: 0 TMA, 1 MMA, 2-7 PREP (192 threads), 8-11 WG2, 12-15 WG3.
+constexpr int kThreadsOut = 512;
+constexpr int W_PREP = 2, kPrepThreads = 192;
 constexpr int WG3 = 12;
-constexpr uint32_t BAR_WG3 = 3;
+constexpr uint32_t BAR_PREP = 1, BAR_WG3 = 3;
+
+// The intra-chunk decay exp(Lam_i - Lam_j) is applied to P in registers as
+// exp(Lam_i - A/2) * exp(A/2 - Lam_j): a row factor times a column factor.
+// For a chunk whose total log decay A is at least this bound both factors lie
+// in [e^-64, e^64], far inside fp32's range; below it each element takes its
+// own exponential.
+constexpr float kSplitMinLogDecay = -128.f;
 
 template <int D, bool PHI, bool DECAY>
 __global__ void __launch_bounds__(kThreadsOut, 1)
@@ -491,20 +528,22 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   constexpr int NST = SM::NST;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
-  float *qfac = reinterpret_cast<float *>(smem + SM::OFF_QF);
-  float *kfac = reinterpret_cast<float *>(smem + SM::OFF_KF);
+  float *rfac = reinterpret_cast<float *>(smem + SM::OFF_RF);
+  float *cfac = reinterpret_cast<float *>(smem + SM::OFF_CF);
+  uint32_t *split = reinterpret_cast<uint32_t *>(smem + SM::OFF_SPLIT);
   float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
-  uint64_t *xdone = empty + NST;       // [NST] phi applied, Lam ready
-  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K rows rescaled by the decay factors
+  uint64_t *xdone = empty + NST;       // [NST] phi applied, Lam and factors ready
+  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K rows rescaled by their decay factors
   uint64_t *p_full = qk_ready + NST;   // [2] MMA1 done
   uint64_t *p_ready = p_full + 2;      // [2] P in smem
   uint64_t *p_free = p_ready + 2;      // [2] MMA2 done reading P smem
-  uint64_t *c_done = p_free + 2;       // [2] MMA3 + MMA4 done
-  uint64_t *o_free = c_done + 2;       // [2] O TMEM buffer read
-  uint64_t *s_ready = o_free + 2;      // S smem (and TMEM S) ready
-  uint64_t *drain = s_ready + 1;       // abort path: all issued MMAs done
+  uint64_t *o_full = p_free + 2;       // [2] O of the chunk complete in TMEM
+  uint64_t *o_free = o_full + 2;       // [2] O TMEM buffer read
+  uint64_t *s_ready = o_free + 2;      // S_c in smem, scaled S_c in TMEM
+  uint64_t *s_done = s_ready + 1;      // MMA4 of the chunk done (and MMA3 with one S copy)
+  uint64_t *drain = s_done + 1;        // abort path: all issued MMAs done
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -521,7 +560,6 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     S_in = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
   }
   const bool has_init = S_in != nullptr;
-  constexpr bool decay = DECAY;
   if (tid == 0) {
     (void)LA_CHK(bh < p.BH && seg < p.n_seg && nc >= 1 && nc <= p.seg_chunks, KID_PREFILL_TC_OUT, 5);
     (void)LA_CHK(!p.S_final || bh < p.BH, KID_PREFILL_TC_OUT, 6);
@@ -538,10 +576,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       mbar_init(&p_full[i], 1);
       mbar_init(&p_ready[i], 1);
       mbar_init(&p_free[i], 1);
-      mbar_init(&c_done[i], 1);
+      mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], 1);
     }
     mbar_init(s_ready, 1);
+    mbar_init(s_done, 1);
     mbar_init(drain, 1);
     ctl->abort = 0;
     fence_mbarrier_init();
@@ -600,9 +639,8 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       constexpr uint32_t id_qs = idesc_bf16_f32(64, D, false, true);
       constexpr uint32_t id_kv = idesc_bf16_f32(D, D, true, true);
       const uint32_t sbase = smem_u32(smem);
-      const uint32_t s_smem = sbase + SM::OFF_S;
       auto q_of = [&](int s) { return sbase + s * SM::STAGE; };
-      // QK^T of chunk c into P buffer c & 1, once its tile is transformed.
+      // QK^T of chunk c into P buffer c & 1, once its tiles are transformed.
       auto issue_qk = [&](int c) -> bool {
         const int s = c % NST;
         if (!wait1(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 2)) return false;
@@ -622,41 +660,46 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int s = c % NST, b = c & 1;
         const uint32_t qa = q_of(s), ka = qa + SM::TILE, va = qa + 2 * SM::TILE;
         const uint32_t o_t = tmem + SM::T_O + D * b;
-        if (!(ok = wait1(&p_ready[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
-        if (decay &&
-            !(ok = wait1(&qk_ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
-          break;
+        const uint32_t s_sm = sbase + SM::OFF_S + (SM::NSB == 2 ? (uint32_t)b * SM::S_BYTES : 0u);
         if (c >= 2 &&
             !(ok = wait1(&o_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
           break;
+        if (!(ok = wait1(s_ready, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
+        if (DECAY &&
+            !(ok = wait1(&qk_ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
+          break;
+        tc_fence_after();
+        LA_TRACE_EVENT(trace_on, t0, 8, c);
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)   // S_c+1 = exp(A) S_c + Kt^T V (TMEM)
+          mma_bf16(tmem + SM::T_S, smem_desc_sw128(ka + 2048 * kk, BOX_BYTES, 1024),
+                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_kv,
+                   (has_init || c > 0 || kk > 0) ? 1u : 0u);
+        if (SM::NSB == 2) mma_commit(s_done);
+        const bool inter = has_init || c > 0;
+        if (inter) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {  // O = Qt S_c
+            const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+            mma_bf16(o_t, smem_desc_sw128(qa + off, 16, 1024),
+                     smem_desc_sw128(s_sm + 2048 * kk, SM::S_BLOCK, 1024), id_qs, kk > 0);
+          }
+        }
+        if (SM::NSB == 1) mma_commit(s_done);
+        LA_TRACE_EVENT(trace_on, t0, 9, c);
+        if (!(ok = wait1(&p_ready[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
         tc_fence_after();
         LA_TRACE_EVENT(trace_on, t0, 5, c);
         const uint32_t pa = sbase + SM::OFF_P + 8192 * b;
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)   // O = P V
+        for (int kk = 0; kk < CH / 16; ++kk)   // O += P V
           mma_bf16(o_t, smem_desc_sw128(pa + 32 * kk, 16, 1024),
-                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_pv, kk > 0);
+                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_pv,
+                   (inter || kk > 0) ? 1u : 0u);
         mma_commit(&p_free[b]);
-        LA_TRACE_EVENT(trace_on, t0, 6, c);
-        if (!(ok = wait1(s_ready, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
-        tc_fence_after();
-        LA_TRACE_EVENT(trace_on, t0, 8, c);
-        if (has_init || c > 0) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // O += Qt S
-            const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-            mma_bf16(o_t, smem_desc_sw128(qa + off, 16, 1024),
-                     smem_desc_sw128(s_smem + 2048 * kk, SM::S_BLOCK, 1024), id_qs, 1);
-          }
-        }
-#pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)   // S = exp(A) S + Kt^T V
-          mma_bf16(tmem + SM::T_S, smem_desc_sw128(ka + 2048 * kk, BOX_BYTES, 1024),
-                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_kv,
-                   (has_init || c > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&c_done[b]);
+        mma_commit(&o_full[b]);
         mma_commit(&empty[s]);
-        LA_TRACE_EVENT(trace_on, t0, 9, c);
+        LA_TRACE_EVENT(trace_on, t0, 6, c);
         if (c + 2 < nc) {
           ok = issue_qk(c + 2);
           LA_TRACE_EVENT(trace_on, t0, 7, c);
@@ -670,67 +713,69 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       // P epilogue: observe them before the CTA can exit.
       for (int c = max(0, nc - 2); c < nc; ++c) drain_wait(&p_free[c & 1], (c >> 1) & 1);
     }
-  } else if (warp >= WG1 && warp < WG2) {
-    // ------------------------------------------------------------ WG1: Lam, phi, rescale
-    const int t = tid - WG1 * 32;
-    constexpr bool phi = PHI;
+  } else if (warp >= W_PREP && warp < WG2) {
+    // ------------------------------------------------------------ PREP: Lam, phi, decay factors
+    const int t = tid - W_PREP * 32;  // 0..191
+    auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_PREFILL_TC_OUT, site, BAR_PREP, t);
+    };
     auto prep = [&](int c) -> bool {
       const int s = c % NST;
-      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 7, BAR_WG1))
-        return false;
+      if (!gwait(&full[s], (c / NST) & 1, 7)) return false;
       LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);
       unsigned char *qt = smem + s * SM::STAGE;
-      if (decay && t < 64) {  // inclusive prefix of the chunk's log decays (warps 4, 5)
-        float x = token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + c * CH + t, p.L);
+      if constexpr (DECAY) {
+        if (t < 64) {  // inclusive prefix of the chunk's log decays (warps 2, 3)
+          float x = token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + c * CH + t, p.L);
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          float y = __shfl_up_sync(0xffffffffu, x, off);
-          if (lane >= off) x += y;
+          for (int off = 1; off < 32; off <<= 1) {
+            float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+          }
+          if (t == 31) scr[0] = x;
+          lam[s * 64 + t] = x;
         }
-        if (t == 31) scr[0] = x;
-        lam[s * 64 + t] = x;
+        named_bar_sync(BAR_PREP, kPrepThreads);
+        if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
+        named_bar_sync(BAR_PREP, kPrepThreads);
+        if (t < 64) {
+          const float A = lam[s * 64 + 63], li = lam[s * 64 + t];
+          rfac[s * 64 + t] = __expf(li - 0.5f * A);
+          cfac[s * 64 + t] = __expf(0.5f * A - li);
+          if (t == 0) split[s] = A >= kSplitMinLogDecay ? 1u : 0u;
+        }
       }
-      if constexpr (phi) {
-        tile_pass<D, true, false>(qt, nullptr, t, 128);
-        tile_pass<D, true, false>(qt + SM::TILE, nullptr, t, 128);
+      if constexpr (PHI) {  // Q and K tiles are adjacent in the stage: one pass
+        tile_pass<D, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
         fence_proxy_async_smem();
       }
-      named_bar_sync(BAR_WG1, 128);
-      if constexpr (decay) {
-        if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
-        named_bar_sync(BAR_WG1, 128);
-        if (t < 64) {
-          const float A = lam[s * 64 + 63];
-          const float li = lam[s * 64 + t];
-          qfac[s * 64 + t] = __expf(li);
-          kfac[s * 64 + t] = __expf(A - li);
-        }
-      } else if (t < 64) {
-        lam[s * 64 + t] = 0.f;
-      }
-      named_bar_sync(BAR_WG1, 128);
+      named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&xdone[s]);
       LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
       return true;
     };
     // Decay: once QK^T of chunk c has consumed the unscaled tiles, scale the
-    // rows in place: Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j.
+    // rows in place: Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j (both
+    // factors <= 1).
     auto rescale = [&](int c) -> bool {
       const int s = c % NST, b = c & 1;
-      if (!wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 8, BAR_WG1))
-        return false;
-      unsigned char *qt = smem + s * SM::STAGE;
-      tile_pass<D, false, true>(qt, qfac + s * 64, t, 128);
-      tile_pass<D, false, true>(qt + SM::TILE, kfac + s * 64, t, 128);
+      if (!gwait(&p_full[b], (c >> 1) & 1, 8)) return false;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 13, c);
+      const float *lm = lam + s * 64;
+      const float A = lm[63];
+      tile_pass<D, 2, false, true>(
+          smem + s * SM::STAGE,
+          [lm, A](int k, int r) { return __expf(k == 0 ? lm[r] : A - lm[r]); }, t, kPrepThreads);
       fence_proxy_async_smem();
-      named_bar_sync(BAR_WG1, 128);
+      named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&qk_ready[s]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 14, c);
       return true;
     };
     bool ok = nc > 0 && prep(0);
     for (int c = 0; ok && c < nc; ++c) {
       if (c + 1 < nc && !(ok = prep(c + 1))) break;
-      if constexpr (decay) {
+      if constexpr (DECAY) {
         if (!(ok = rescale(c))) break;
       }
     }
@@ -742,8 +787,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     auto p_epilogue = [&](int c) -> bool {
       const int s = c % NST, b = c & 1;
-      if (!wait_wg(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 15, BAR_WG2) ||
-          !wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG2))
+      if (DECAY && !wait_wg(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 15, BAR_WG2))
+        return false;
+      if (!wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG2))
         return false;
       if (c >= 2 && !wait_wg(&p_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 10,
                              BAR_WG2))
@@ -756,9 +802,14 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       tmem_ld32(tmem + lane_off + SM::T_P + 64 * b + 32, r[1]);
       tmem_ld_wait();
       if (row >= 0) {
-        const float *lm = lam + s * 64;
-        const float li = lm[row];
         unsigned char *ps = smem + SM::OFF_P + 8192 * b;
+        const float *lm = lam + s * 64, *cf = cfac + s * 64;
+        // Causal mask, then the decay exp(Lam_i - Lam_j) between row token i
+        // and token j: a row factor times a column factor, or (chunks of very
+        // strong decay) one exponential per element.
+        const bool sp = DECAY && split[s];
+        const float li = DECAY ? lm[row] : 0.f;
+        const float rf = DECAY ? rfac[s * 64 + row] : 1.f;
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf) {
 #pragma unroll
@@ -769,9 +820,14 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
               const int j0 = hlf * 32 + q16 * 16 + j;
               float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
               float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
-              if constexpr (decay) {
-                v0 *= __expf(fminf(li - lm[j0], 0.f));
-                v1 *= __expf(fminf(li - lm[j0 + 1], 0.f));
+              if constexpr (DECAY) {
+                if (sp) {
+                  v0 = v0 * cf[j0] * rf;
+                  v1 = v1 * cf[j0 + 1] * rf;
+                } else {
+                  v0 *= __expf(fminf(li - lm[j0], 0.f));
+                  v1 *= __expf(fminf(li - lm[j0 + 1], 0.f));
+                }
               }
               pk[j >> 1] = pack_bf16(v0, v1);
             }
@@ -788,7 +844,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     };
     auto o_epilogue = [&](int c) -> bool {
       const int b = c & 1;
-      if (!wait_wg(&c_done[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
+      if (!wait_wg(&o_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
         return false;
       tc_fence_after();
       if (t == 0) tma_store_wait_read<1>();  // the store that used this buffer is done
@@ -843,11 +899,10 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int t = tid - WG3 * 32;
     const int quarter = warp & 3;
     const int srow = acc_row<D>(quarter, lane);    // state row (d_k index)
-    unsigned char *s_sm = smem + SM::OFF_S;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // 32 columns of state row srow: bf16 copy into S smem (MN-major blocks),
-    // and optionally the scaled fp32 values back into TMEM.
-    auto put32 = [&](int col, uint32_t (&r)[32], float scale, bool to_tmem) {
+    // 32 columns of state row srow: bf16 copy into an S buffer (MN-major
+    // blocks), and optionally the scaled fp32 values back into TMEM.
+    auto put32 = [&](unsigned char *s_sm, int col, uint32_t (&r)[32], float scale, bool to_tmem) {
       if (srow >= 0) {
 #pragma unroll
         for (int q16 = 0; q16 < 2; ++q16) {
@@ -866,31 +921,40 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         tmem_st32(tmem + lane_off + SM::T_S + col, r);
       }
     };
+    auto s_buf = [&](int c) {
+      return smem + SM::OFF_S + (SM::NSB == 2 ? (c & 1) * SM::S_BYTES : 0u);
+    };
     bool ok = true;
     if (nc > 0) {
-      ok = wait_wg(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 12, BAR_WG3);
-      if (ok && has_init) {
-        const float a0 = __expf(lam[63]);
-#pragma unroll 1
-        for (int col = 0; col < D; col += 32) {
-          uint32_t r[32];
-          if (srow >= 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float4 f = src[j];
-              r[4 * j] = __float_as_uint(f.x);
-              r[4 * j + 1] = __float_as_uint(f.y);
-              r[4 * j + 2] = __float_as_uint(f.z);
-              r[4 * j + 3] = __float_as_uint(f.w);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = 0u;
-          }
-          put32(col, r, a0, true);
+      if (has_init) {
+        // S smem <- S_in, TMEM S <- exp(A_0) S_in (the decay of chunk 0).
+        float a0 = 1.f;
+        if constexpr (DECAY) {
+          ok = wait_wg(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 12, BAR_WG3);
+          if (ok) a0 = __expf(lam[63]);
         }
-        tmem_st_wait();
+        if (ok) {
+#pragma unroll 1
+          for (int col = 0; col < D; col += 32) {
+            uint32_t r[32];
+            if (srow >= 0) {
+              const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float4 f = src[j];
+                r[4 * j] = __float_as_uint(f.x);
+                r[4 * j + 1] = __float_as_uint(f.y);
+                r[4 * j + 2] = __float_as_uint(f.z);
+                r[4 * j + 3] = __float_as_uint(f.w);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = 0u;
+            }
+            put32(s_buf(0), col, r, a0, true);
+          }
+          tmem_st_wait();
+        }
       }
       if (ok) {
         fence_proxy_async_smem();
@@ -900,18 +964,21 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
     }
     for (int c = 0; ok && c < nc; ++c) {
-      const int b = c & 1;
-      if (!(ok = wait_wg(&c_done[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13,
-                         BAR_WG3)))
-        break;
+      if (!(ok = wait_wg(s_done, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13, BAR_WG3))) break;
       tc_fence_after();
       LA_TRACE_EVENT(trace_on && t == 0, t0, 10, c);
       if (c + 1 < nc) {
+        // TMEM holds S_c+1.  Copy it to bf16 for chunk c+1's Qt S, and leave
+        // exp(A_c+1) S_c+1 in TMEM for its state update.
         const int s1 = (c + 1) % NST;
-        if (!(ok = wait_wg(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
-                           BAR_WG3)))
-          break;
-        const float a1 = __expf(lam[s1 * 64 + 63]);
+        float a1 = 1.f;
+        if constexpr (DECAY) {
+          if (!(ok = wait_wg(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
+                             BAR_WG3)))
+            break;
+          a1 = __expf(lam[s1 * 64 + 63]);
+        }
+        unsigned char *s_sm = s_buf(c + 1);
 #pragma unroll 1
         for (int col = 0; col < D; col += 64) {
           __syncwarp();
@@ -919,10 +986,10 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           tmem_ld32(tmem + lane_off + SM::T_S + col, r[0]);
           tmem_ld32(tmem + lane_off + SM::T_S + col + 32, r[1]);
           tmem_ld_wait();
-          put32(col, r[0], a1, decay);
-          put32(col + 32, r[1], a1, decay);
+          put32(s_sm, col, r[0], a1, DECAY);
+          put32(s_sm, col + 32, r[1], a1, DECAY);
         }
-        if (decay) tmem_st_wait();
+        if (DECAY) tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(BAR_WG3, 128);
