@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 
 #include "../../include/la_gb300.h"
@@ -473,36 +474,38 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
 }
 
 // ================================================================ chunk output
-template <int D>
+// One CTA runs two segments of one (b, h) sequence -- two independent state
+// chains, "streams" -- over one 64-wide slice of the value columns (the state
+// columns S[:, slice] and the output columns O[:, slice] depend on V[:, slice]
+// alone).  The chunks of the two streams are interleaved into one sequence of
+// virtual chunks k = 0, 1, ...: while both have chunks left they alternate, so
+// a stream's state hand-over (MMA, then the TMEM -> bf16 copy) overlaps the
+// other stream's chunk.
+template <int DK>
 struct OutSmem {
-  static constexpr int NST = (D == 128) ? 3 : 4;
-  // bf16 copies of the state: with two, the conversion of S_c+1 may overlap
-  // the MMA that still reads S_c (D = 64); D = 128 has room for one.
-  static constexpr int NSB = (D == 128) ? 1 : 2;
-  static constexpr uint32_t TILE = 64 * D * 2;            // Q, K or V tile of one chunk
-  static constexpr uint32_t STAGE = 3 * TILE;
+  static constexpr int NST = (DK == 128) ? 3 : 4;
+  static constexpr uint32_t QK_TILE = 64 * DK * 2;         // Q or K tile of one chunk
+  static constexpr uint32_t V_TILE = 64 * 64 * 2;          // the chunk's V slice
+  static constexpr uint32_t STAGE = 2 * QK_TILE + V_TILE;  // Q | K | V
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
-  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // NSB x [D][D] bf16, MN-major blocks
-  static constexpr uint32_t S_BLOCK = D * 128;             // one 64-column block
-  static constexpr uint32_t S_BYTES = D * D * 2;
-  static constexpr uint32_t OFF_O = OFF_S + NSB * S_BYTES; // 2 x [64][D] bf16 store staging
-  static constexpr uint32_t OFF_LAM = OFF_O + 2 * TILE;    // [NST][64] inclusive prefix
-  static constexpr uint32_t OFF_RF = OFF_LAM + NST * 64 * 4;  // [NST][64] exp(Lam_i - A/2)
-  static constexpr uint32_t OFF_CF = OFF_RF + NST * 64 * 4;   // [NST][64] exp(A/2 - Lam_j)
-  static constexpr uint32_t OFF_SPLIT = OFF_CF + NST * 64 * 4; // [NST] factors usable
+  static constexpr uint32_t S_BYTES = DK * 128;            // [DK][64] bf16, MN-major
+  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // one per stream
+  static constexpr uint32_t OFF_O = OFF_S + 2 * S_BYTES;   // 2 x [64][64] bf16 store staging
+  static constexpr uint32_t OFF_LAM = OFF_O + 2 * 8192;    // [NST][64] inclusive prefix
+  static constexpr uint32_t OFF_VF = OFF_LAM + NST * 64 * 4;   // [NST][64] exp(A/2 - Lam_j)
+  static constexpr uint32_t OFF_OF = OFF_VF + NST * 64 * 4;    // [NST][64] exp(Lam_i - A/2)
+  static constexpr uint32_t OFF_SPLIT = OFF_OF + NST * 64 * 4; // [NST] split decay used
   static constexpr uint32_t OFF_SCR = OFF_SPLIT + 16 * 4;      // 16 floats
   static constexpr uint32_t OFF_BAR = OFF_SCR + 16 * 4;
-  static constexpr int NBAR = 4 * NST + 2 * 5 + 3;
+  static constexpr int NBAR = 4 * NST + 4 * 2 + 2 * 2 + 1;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
   static constexpr uint32_t BYTES = OFF_CTL + 64;
-  static_assert(OFF_P % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
+  static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_S % 1024 == 0 &&
+                    OFF_O % 1024 == 0 && S_BYTES % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
-  // TMEM columns
-  static constexpr uint32_t T_P = 0;          // 2 x 64 columns
-  static constexpr uint32_t T_O = 128;        // 2 x D columns
-  static constexpr uint32_t T_S = 128 + 2 * D;
-  static constexpr uint32_t T_COLS = 512;
+  // TMEM columns: P and O by virtual chunk parity, S by stream.
+  static constexpr uint32_t T_P = 0, T_O = 128, T_S = 256, T_COLS = 512;
 };
 
 // Warps: 0 TMA, 1 MMA, 2-7 PREP (192 threads), 8-11 WG2, 12-15 WG3.
@@ -511,57 +514,93 @@ constexpr int W_PREP = 2, kPrepThreads = 192;
 constexpr int WG3 = 12;
 constexpr uint32_t BAR_PREP = 1, BAR_WG3 = 3;
 
-// The intra-chunk decay exp(Lam_i - Lam_j) is applied to P in registers as
-// exp(Lam_i - A/2) * exp(A/2 - Lam_j): a row factor times a column factor.
-// For a chunk whose total log decay A is at least this bound both factors lie
-// in [e^-64, e^64], far inside fp32's range; below it each element takes its
-// own exponential.
-constexpr float kSplitMinLogDecay = -128.f;
+// Decay of a chunk with total log decay A, reference r = A/2.  Split form:
+// the decay between tokens i >= j, exp(Lam_i - Lam_j) = exp(Lam_i - r) *
+// exp(r - Lam_j), has its token-j factor folded into the rows of V in shared
+// memory and its token-i factor applied to the output rows in registers:
+//   V'_j = exp(r - Lam_j) v_j,   O'_i = sum_{j<=i} (q_i . k_j) V'_j + q_i (e^r S_c),
+//   O_i  = exp(Lam_i - r) O'_i,  e^r S_c + K^T V' = exp(r - A) S_c+1 in TMEM.
+// P = QK^T stays the product of the unscaled operands (so the rounding to
+// bf16 comes after q . k cancels), and Q and K need no second pass.  With
+// A >= this bound every factor lies in [e^-40, e^40] and every product of two
+// in [e^-80, e^80], inside fp32's normal range.  Chunks of stronger decay
+// take the per-element form: P_ij exp(Lam_i - Lam_j) in registers, and Q, K
+// rescaled in place once QK^T has read them.
+constexpr float kSplitMinLogDecay = -80.f;
 
-template <int D, bool PHI, bool DECAY>
+// The virtual-chunk order of a CTA's two streams.
+struct Streams {
+  int nc[2];   // chunks per stream (stream 1 may have none)
+  int m;       // chunks both streams have: virtual 0 .. 2m-1 alternate
+  int longer;  // the stream whose chunks follow alone
+  __device__ void at(int k, int &sg, int &c) const {
+    if (k < 2 * m) {
+      sg = k & 1;
+      c = k >> 1;
+    } else {
+      sg = longer;
+      c = m + (k - 2 * m);
+    }
+  }
+  __device__ int index(int sg, int c) const { return c < m ? 2 * c + sg : 2 * m + (c - m); }
+};
+
+template <int DK, bool PHI, bool DECAY>
 __global__ void __launch_bounds__(kThreadsOut, 1)
 chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmO, TcParams p) {
-  using SM = OutSmem<D>;
+  using SM = OutSmem<DK>;
   constexpr int NST = SM::NST;
+  constexpr int D = DK;  // d_k = d_v: the state row length
   extern __shared__ __align__(1024) unsigned char smem[];
   float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
-  float *rfac = reinterpret_cast<float *>(smem + SM::OFF_RF);
-  float *cfac = reinterpret_cast<float *>(smem + SM::OFF_CF);
+  float *vfac = reinterpret_cast<float *>(smem + SM::OFF_VF);
+  float *ofac = reinterpret_cast<float *>(smem + SM::OFF_OF);
   uint32_t *split = reinterpret_cast<uint32_t *>(smem + SM::OFF_SPLIT);
   float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
-  uint64_t *xdone = empty + NST;       // [NST] phi applied, Lam and factors ready
-  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K rows rescaled by their decay factors
+  uint64_t *xdone = empty + NST;       // [NST] phi applied, Lam, V rows and factors ready
+  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K rows hold what MMA3 / MMA4 need
   uint64_t *p_full = qk_ready + NST;   // [2] MMA1 done
   uint64_t *p_ready = p_full + 2;      // [2] P in smem
-  uint64_t *p_free = p_ready + 2;      // [2] MMA2 done reading P smem
-  uint64_t *o_full = p_free + 2;       // [2] O of the chunk complete in TMEM
+  uint64_t *o_full = p_ready + 2;      // [2] MMA2 done: O complete in TMEM, P smem free
   uint64_t *o_free = o_full + 2;       // [2] O TMEM buffer read
-  uint64_t *s_ready = o_free + 2;      // S_c in smem, scaled S_c in TMEM
-  uint64_t *s_done = s_ready + 1;      // MMA4 of the chunk done (and MMA3 with one S copy)
-  uint64_t *drain = s_done + 1;        // abort path: all issued MMAs done
+  uint64_t *s_ready = o_free + 2;      // [stream] S_c in smem, scaled S_c in TMEM
+  uint64_t *s_done = s_ready + 2;      // [stream] MMA4 and MMA3 of the stream's chunk done
+  uint64_t *drain = s_done + 2;        // abort path: all issued MMAs done
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
-  const int c0 = seg * p.seg_chunks;
-  const int nc = min(p.seg_chunks, p.n_chunks - c0);
-  const int tok0 = c0 * CH;
+  const int pair = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
+  const int dv0 = blockIdx.z * 64;  // first value column of this CTA's slice
   const size_t bhL = (size_t)bh * p.L;
-  const bool last_seg = seg == p.n_seg - 1;
-  const float *S_in = nullptr;
-  if (p.n_seg > 1) {
-    if (seg > 0 || p.S0) S_in = p.ws_state + ((size_t)bh * p.n_seg + seg) * D * D;
-  } else {
-    S_in = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
+  Streams st;
+  int tok0[2], seg[2];
+  const float *S_in[2];
+  bool last_seg[2], has_init[2];
+  for (int sg = 0; sg < 2; ++sg) {
+    seg[sg] = 2 * pair + sg;
+    const int c0 = seg[sg] * p.seg_chunks;
+    st.nc[sg] = seg[sg] < p.n_seg ? min(p.seg_chunks, p.n_chunks - c0) : 0;
+    tok0[sg] = c0 * CH;
+    last_seg[sg] = seg[sg] == p.n_seg - 1;
+    S_in[sg] = nullptr;
+    if (p.n_seg > 1) {
+      if (seg[sg] > 0 || p.S0) S_in[sg] = p.ws_state + ((size_t)bh * p.n_seg + seg[sg]) * D * D;
+    } else {
+      S_in[sg] = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
+    }
+    has_init[sg] = S_in[sg] != nullptr;
   }
-  const bool has_init = S_in != nullptr;
+  st.m = min(st.nc[0], st.nc[1]);
+  st.longer = st.nc[0] >= st.nc[1] ? 0 : 1;
+  const int nk = st.nc[0] + st.nc[1];
   if (tid == 0) {
-    (void)LA_CHK(bh < p.BH && seg < p.n_seg && nc >= 1 && nc <= p.seg_chunks, KID_PREFILL_TC_OUT, 5);
+    (void)LA_CHK(bh < p.BH && seg[0] < p.n_seg && st.nc[0] >= 1 && dv0 + 64 <= D,
+                 KID_PREFILL_TC_OUT, 5);
     (void)LA_CHK(!p.S_final || bh < p.BH, KID_PREFILL_TC_OUT, 6);
   }
 
@@ -575,12 +614,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_ready[i], 1);
-      mbar_init(&p_free[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], 1);
+      mbar_init(&s_ready[i], 1);
+      mbar_init(&s_done[i], 1);
     }
-    mbar_init(s_ready, 1);
-    mbar_init(s_done, 1);
     mbar_init(drain, 1);
     ctl->abort = 0;
     fence_mbarrier_init();
@@ -593,7 +631,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const bool trace_on = blockIdx.x == (gridDim.x > 1 ? 1 : 0) && blockIdx.y == 0;
+  const bool trace_on = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
   const long long t0 = clock64();
   (void)trace_on;
   (void)t0;
@@ -606,112 +644,114 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmO);
       int issued = 0;
-      for (int c = 0; c < nc; ++c) {
-        const int s = c % NST;
-        if (c >= NST &&
-            !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 1))
+      for (int k = 0; k < nk; ++k) {
+        const int s = k % NST;
+        if (k >= NST &&
+            !wait1(&empty[s], ((k / NST) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 1))
           break;
-        unsigned char *st = smem + s * SM::STAGE;
+        int sg, c;
+        st.at(k, sg, c);
+        unsigned char *stg = smem + s * SM::STAGE;
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
-        const int tok = tok0 + c * CH;
-        for (int b = 0; b < D / BOX; ++b) {
-          if (!LA_CHK(b * BOX + BOX <= D && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 2))
+        const int tok = tok0[sg] + c * CH;
+        for (int b = 0; b < DK / BOX; ++b) {
+          if (!LA_CHK(b * BOX + BOX <= DK && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 2))
             continue;
-          tma_load_3d(st + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
-          tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
-          tma_load_3d(st + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
+          tma_load_3d(stg + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
+          tma_load_3d(stg + SM::QK_TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
         }
-        LA_TRACE_EVENT(trace_on, t0, 0, c);
-        issued = c + 1;
+        if (LA_CHK(dv0 + 64 <= D && tok < p.L, KID_PREFILL_TC_OUT, 4))
+          tma_load_3d(stg + 2 * SM::QK_TILE, &tmV, &full[s], dv0, tok, bh);
+        LA_TRACE_EVENT(trace_on, t0, 0, k);
+        issued = k + 1;
       }
       if (*(volatile uint32_t *)&ctl->abort)  // loads still landing must land first
-        for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+        for (int k = max(0, issued - NST); k < issued; ++k) drain_wait(&full[k % NST], (k / NST) & 1);
       // Producer tail: the releases of the last stages come from tcgen05.commit
       // and land asynchronously; wait for them so that no mbarrier arrival
       // reaches this CTA's shared memory after it has exited.
-      for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
+      for (int k = max(0, nk - NST); k < nk; ++k) drain_wait(&empty[k % NST], (k / NST) & 1);
     }
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nc > 0) {
+    if (lane == 0 && nk > 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(64, D, false, true);
-      constexpr uint32_t id_qs = idesc_bf16_f32(64, D, false, true);
-      constexpr uint32_t id_kv = idesc_bf16_f32(D, D, true, true);
+      constexpr uint32_t id_pv = idesc_bf16_f32(64, 64, false, true);
+      constexpr uint32_t id_qs = idesc_bf16_f32(64, 64, false, true);
+      constexpr uint32_t id_kv = idesc_bf16_f32(DK, 64, true, true);
+      // Operand descriptors: the base descriptor of each layout at the start
+      // of shared memory, plus (byte offset >> 4) in its 14-bit address field
+      // (shared memory ends below 256 KB, so the field never carries).
       const uint32_t sbase = smem_u32(smem);
-      auto q_of = [&](int s) { return sbase + s * SM::STAGE; };
-      // QK^T of chunk c into P buffer c & 1, once its tiles are transformed.
-      auto issue_qk = [&](int c) -> bool {
-        const int s = c % NST;
-        if (!wait1(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 2)) return false;
+      const uint64_t dKM = smem_desc_sw128(sbase, 16, 1024);          // K-major rows
+      const uint64_t dMN = smem_desc_sw128(sbase, BOX_BYTES, 1024);   // MN-major, 8 KB blocks
+      auto at = [](uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); };
+      // QK^T of virtual chunk k into P buffer k & 1, once its tiles are ready.
+      auto issue_qk = [&](int k) -> bool {
+        const int s = k % NST;
+        if (!wait1(&xdone[s], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 2)) return false;
         tc_fence_after();
-        const uint32_t qa = q_of(s), ka = qa + SM::TILE;
+        const uint32_t so = s * SM::STAGE;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-          mma_bf16(tmem + SM::T_P + 64 * (c & 1), smem_desc_sw128(qa + off, 16, 1024),
-                   smem_desc_sw128(ka + off, 16, 1024), id_qk, kk > 0);
+        for (int kk = 0; kk < DK / 16; ++kk) {
+          const uint32_t off = so + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+          mma_bf16(tmem + SM::T_P + 64 * (k & 1), at(dKM, off), at(dKM, off + SM::QK_TILE), id_qk,
+                   kk > 0);
         }
-        mma_commit(&p_full[c & 1]);
+        mma_commit(&p_full[k & 1]);
         return true;
       };
-      bool ok = issue_qk(0) && (nc < 2 || issue_qk(1));
-      for (int c = 0; ok && c < nc; ++c) {
-        const int s = c % NST, b = c & 1;
-        const uint32_t qa = q_of(s), ka = qa + SM::TILE, va = qa + 2 * SM::TILE;
-        const uint32_t o_t = tmem + SM::T_O + D * b;
-        const uint32_t s_sm = sbase + SM::OFF_S + (SM::NSB == 2 ? (uint32_t)b * SM::S_BYTES : 0u);
-        if (c >= 2 &&
-            !(ok = wait1(&o_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
+      bool ok = issue_qk(0) && (nk < 2 || issue_qk(1));
+      for (int k = 0; ok && k < nk; ++k) {
+        int sg, c;
+        st.at(k, sg, c);
+        const int s = k % NST, b = k & 1;
+        const uint32_t qo = s * SM::STAGE, ko = qo + SM::QK_TILE, vo = qo + 2 * SM::QK_TILE;
+        const uint32_t o_t = tmem + SM::T_O + 64 * b;
+        const uint32_t so = SM::OFF_S + sg * SM::S_BYTES;
+        if (k >= 2 &&
+            !(ok = wait1(&o_free[b], ((k >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
           break;
-        if (!(ok = wait1(s_ready, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
+        if (!(ok = wait1(&s_ready[sg], c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
         if (DECAY &&
-            !(ok = wait1(&qk_ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
+            !(ok = wait1(&qk_ready[s], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
           break;
         tc_fence_after();
-        LA_TRACE_EVENT(trace_on, t0, 8, c);
+        LA_TRACE_EVENT(trace_on, t0, 8, k);
+        const bool inter = has_init[sg] || c > 0;
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)   // S_c+1 = exp(A) S_c + Kt^T V (TMEM)
-          mma_bf16(tmem + SM::T_S, smem_desc_sw128(ka + 2048 * kk, BOX_BYTES, 1024),
-                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_kv,
-                   (has_init || c > 0 || kk > 0) ? 1u : 0u);
-        if (SM::NSB == 2) mma_commit(s_done);
-        const bool inter = has_init || c > 0;
+        for (int kk = 0; kk < CH / 16; ++kk)   // stream state: S (TMEM) += K^T V
+          mma_bf16(tmem + SM::T_S + 64 * sg, at(dMN, ko + 2048 * kk), at(dMN, vo + 2048 * kk),
+                   id_kv, (inter || kk > 0) ? 1u : 0u);
         if (inter) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {  // O = Qt S_c
-            const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-            mma_bf16(o_t, smem_desc_sw128(qa + off, 16, 1024),
-                     smem_desc_sw128(s_sm + 2048 * kk, SM::S_BLOCK, 1024), id_qs, kk > 0);
+          for (int kk = 0; kk < DK / 16; ++kk) {  // O = Q S_c
+            const uint32_t off = qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+            mma_bf16(o_t, at(dKM, off), at(dMN, so + 2048 * kk), id_qs, kk > 0);
           }
         }
-        if (SM::NSB == 1) mma_commit(s_done);
-        LA_TRACE_EVENT(trace_on, t0, 9, c);
-        if (!(ok = wait1(&p_ready[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
+        mma_commit(&s_done[sg]);
+        LA_TRACE_EVENT(trace_on, t0, 9, k);
+        if (!(ok = wait1(&p_ready[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
         tc_fence_after();
-        LA_TRACE_EVENT(trace_on, t0, 5, c);
-        const uint32_t pa = sbase + SM::OFF_P + 8192 * b;
+        LA_TRACE_EVENT(trace_on, t0, 5, k);
+        const uint32_t po = SM::OFF_P + 8192 * b;
 #pragma unroll
         for (int kk = 0; kk < CH / 16; ++kk)   // O += P V
-          mma_bf16(o_t, smem_desc_sw128(pa + 32 * kk, 16, 1024),
-                   smem_desc_sw128(va + 2048 * kk, BOX_BYTES, 1024), id_pv,
+          mma_bf16(o_t, at(dKM, po + 32 * kk), at(dMN, vo + 2048 * kk), id_pv,
                    (inter || kk > 0) ? 1u : 0u);
-        mma_commit(&p_free[b]);
         mma_commit(&o_full[b]);
         mma_commit(&empty[s]);
-        LA_TRACE_EVENT(trace_on, t0, 6, c);
-        if (c + 2 < nc) {
-          ok = issue_qk(c + 2);
-          LA_TRACE_EVENT(trace_on, t0, 7, c);
+        LA_TRACE_EVENT(trace_on, t0, 6, k);
+        if (k + 2 < nk) {
+          ok = issue_qk(k + 2);
+          LA_TRACE_EVENT(trace_on, t0, 7, k);
         }
       }
       if (!ok) {  // let every issued MMA finish before TMEM is released
         mma_commit(drain);
         drain_wait(drain, 0);
       }
-      // The last P-buffer releases are committed but never waited on by the
-      // P epilogue: observe them before the CTA can exit.
-      for (int c = max(0, nc - 2); c < nc; ++c) drain_wait(&p_free[c & 1], (c >> 1) & 1);
     }
   } else if (warp >= W_PREP && warp < WG2) {
     // ------------------------------------------------------------ PREP: Lam, phi, decay factors
@@ -719,14 +759,17 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_PREFILL_TC_OUT, site, BAR_PREP, t);
     };
-    auto prep = [&](int c) -> bool {
-      const int s = c % NST;
-      if (!gwait(&full[s], (c / NST) & 1, 7)) return false;
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);
+    auto prep = [&](int k) -> bool {
+      const int s = k % NST;
+      if (!gwait(&full[s], (k / NST) & 1, 7)) return false;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 1, k);
       unsigned char *qt = smem + s * SM::STAGE;
+      bool sp = false;  // uniform over the group
       if constexpr (DECAY) {
+        int sg, c;
+        st.at(k, sg, c);
         if (t < 64) {  // inclusive prefix of the chunk's log decays (warps 2, 3)
-          float x = token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + c * CH + t, p.L);
+          float x = token_lambda(p.decay_kind, p.decay, h, bhL, tok0[sg] + c * CH + t, p.L);
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
             float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -738,45 +781,55 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         named_bar_sync(BAR_PREP, kPrepThreads);
         if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
         named_bar_sync(BAR_PREP, kPrepThreads);
-        if (t < 64) {
-          const float A = lam[s * 64 + 63], li = lam[s * 64 + t];
-          rfac[s * 64 + t] = __expf(li - 0.5f * A);
-          cfac[s * 64 + t] = __expf(0.5f * A - li);
-          if (t == 0) split[s] = A >= kSplitMinLogDecay ? 1u : 0u;
+        const float A = lam[s * 64 + 63];
+        sp = A >= kSplitMinLogDecay;
+        if (t < 64 && sp) {
+          const float li = lam[s * 64 + t];
+          vfac[s * 64 + t] = __expf(0.5f * A - li);
+          ofac[s * 64 + t] = __expf(li - 0.5f * A);
         }
+        if (t == 0) split[s] = sp ? 1u : 0u;
+        if (sp) named_bar_sync(BAR_PREP, kPrepThreads);  // factors visible to the V pass
       }
-      if constexpr (PHI) {  // Q and K tiles are adjacent in the stage: one pass
-        tile_pass<D, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
-        fence_proxy_async_smem();
+      if constexpr (PHI)  // Q and K tiles are adjacent in the stage: one pass
+        tile_pass<DK, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
+      if (DECAY && sp) {
+        const float *vf = vfac + s * 64;
+        tile_pass<64, 1, false, true>(qt + 2 * SM::QK_TILE, [vf](int, int r) { return vf[r]; }, t,
+                                      kPrepThreads);
       }
+      if (PHI || sp) fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
-      if (t == 0) mbar_arrive(&xdone[s]);
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
+      if (t == 0) {
+        mbar_arrive(&xdone[s]);
+        if (sp) mbar_arrive(&qk_ready[s]);
+      }
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 2, k);
       return true;
     };
-    // Decay: once QK^T of chunk c has consumed the unscaled tiles, scale the
-    // rows in place: Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j (both
-    // factors <= 1).
-    auto rescale = [&](int c) -> bool {
-      const int s = c % NST, b = c & 1;
-      if (!gwait(&p_full[b], (c >> 1) & 1, 8)) return false;
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 13, c);
+    // Per-element decay form: once QK^T of the chunk has consumed the
+    // unscaled tiles, scale the rows in place: Qt_i = exp(Lam_i) q_i,
+    // Kt_j = exp(A - Lam_j) k_j (both factors <= 1).
+    auto rescale = [&](int k) -> bool {
+      const int s = k % NST, b = k & 1;
+      if (!gwait(&p_full[b], (k >> 1) & 1, 8)) return false;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 13, k);
       const float *lm = lam + s * 64;
       const float A = lm[63];
-      tile_pass<D, 2, false, true>(
+      tile_pass<DK, 2, false, true>(
           smem + s * SM::STAGE,
-          [lm, A](int k, int r) { return __expf(k == 0 ? lm[r] : A - lm[r]); }, t, kPrepThreads);
+          [lm, A](int kt, int r) { return __expf(kt == 0 ? lm[r] : A - lm[r]); }, t, kPrepThreads);
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&qk_ready[s]);
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 14, c);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 14, k);
       return true;
     };
-    bool ok = nc > 0 && prep(0);
-    for (int c = 0; ok && c < nc; ++c) {
-      if (c + 1 < nc && !(ok = prep(c + 1))) break;
+    bool ok = nk > 0 && prep(0);
+    for (int k = 0; ok && k < nk; ++k) {
+      if (k + 1 < nk && !(ok = prep(k + 1))) break;
       if constexpr (DECAY) {
-        if (!(ok = rescale(c))) break;
+        if (!split[k % NST] && !(ok = rescale(k))) break;
       }
     }
   } else if (warp >= WG2 && warp < WG3) {
@@ -785,17 +838,15 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int quarter = warp & 3;
     const int row = acc_row<64>(quarter, lane);   // row within the chunk
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    auto p_epilogue = [&](int c) -> bool {
-      const int s = c % NST, b = c & 1;
-      if (DECAY && !wait_wg(&xdone[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 15, BAR_WG2))
+    float of_cur = 1.f;  // output row factor of the chunk whose P was just formed
+    auto p_epilogue = [&](int k) -> bool {
+      const int s = k % NST, b = k & 1;
+      if (DECAY && !wait_wg(&xdone[s], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 15, BAR_WG2))
         return false;
-      if (!wait_wg(&p_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG2))
-        return false;
-      if (c >= 2 && !wait_wg(&p_free[b], ((c >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 10,
-                             BAR_WG2))
+      if (!wait_wg(&p_full[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 9, BAR_WG2))
         return false;
       tc_fence_after();
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 3, c);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 3, k);
       __syncwarp();
       uint32_t r[2][32];
       tmem_ld32(tmem + lane_off + SM::T_P + 64 * b, r[0]);
@@ -803,13 +854,12 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       tmem_ld_wait();
       if (row >= 0) {
         unsigned char *ps = smem + SM::OFF_P + 8192 * b;
-        const float *lm = lam + s * 64, *cf = cfac + s * 64;
-        // Causal mask, then the decay exp(Lam_i - Lam_j) between row token i
-        // and token j: a row factor times a column factor, or (chunks of very
-        // strong decay) one exponential per element.
+        const float *lm = lam + s * 64;
+        // Causal mask; per-element decay only for chunks outside the split
+        // form (whose row factor the O epilogue applies instead).
         const bool sp = DECAY && split[s];
         const float li = DECAY ? lm[row] : 0.f;
-        const float rf = DECAY ? rfac[s * 64 + row] : 1.f;
+        if (DECAY) of_cur = sp ? ofac[s * 64 + row] : 1.f;
 #pragma unroll
         for (int hlf = 0; hlf < 2; ++hlf) {
 #pragma unroll
@@ -821,10 +871,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
               float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
               float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
               if constexpr (DECAY) {
-                if (sp) {
-                  v0 = v0 * cf[j0] * rf;
-                  v1 = v1 * cf[j0 + 1] * rf;
-                } else {
+                if (!sp) {
                   v0 *= __expf(fminf(li - lm[j0], 0.f));
                   v1 *= __expf(fminf(li - lm[j0 + 1], 0.f));
                 }
@@ -839,37 +886,40 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       tc_fence_before();
       named_bar_sync(BAR_WG2, 128);
       if (t == 0) mbar_arrive(&p_ready[b]);
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 4, c);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 4, k);
       return true;
     };
-    auto o_epilogue = [&](int c) -> bool {
-      const int b = c & 1;
-      if (!wait_wg(&o_full[b], (c >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
+    auto o_epilogue = [&](int k, float f) -> bool {
+      const int b = k & 1;
+      if (!wait_wg(&o_full[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
         return false;
       tc_fence_after();
       if (t == 0) tma_store_wait_read<1>();  // the store that used this buffer is done
       __syncwarp();
       named_bar_sync(BAR_WG2, 128);
-      unsigned char *o_sm = smem + SM::OFF_O + b * SM::TILE;
-#pragma unroll 1
-      for (int col = 0; col < D; col += 64) {
-        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row branch
-        uint32_t r[2][32];
-        tmem_ld32(tmem + lane_off + SM::T_O + D * b + col, r[0]);
-        tmem_ld32(tmem + lane_off + SM::T_O + D * b + col + 32, r[1]);
-        tmem_ld_wait();
-        if (row >= 0) {
+      unsigned char *o_sm = smem + SM::OFF_O + b * 8192;
+      __syncwarp();  // tcgen05.ld is warp-collective: reconverge before it
+      uint32_t r[2][32];
+      tmem_ld32(tmem + lane_off + SM::T_O + 64 * b, r[0]);
+      tmem_ld32(tmem + lane_off + SM::T_O + 64 * b + 32, r[1]);
+      tmem_ld_wait();
+      if (row >= 0) {
 #pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
+        for (int hlf = 0; hlf < 2; ++hlf) {
 #pragma unroll
-            for (int q16 = 0; q16 < 2; ++q16) {
-              uint32_t pk[8];
+          for (int q16 = 0; q16 < 2; ++q16) {
+            uint32_t pk[8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                pk[j] = pack_bf16(__uint_as_float(r[hlf][q16 * 16 + 2 * j]),
-                                  __uint_as_float(r[hlf][q16 * 16 + 2 * j + 1]));
-              st_row16(o_sm, BOX_BYTES, row, col + hlf * 32 + q16 * 16, pk);
+            for (int j = 0; j < 8; ++j) {
+              float x0 = __uint_as_float(r[hlf][q16 * 16 + 2 * j]);
+              float x1 = __uint_as_float(r[hlf][q16 * 16 + 2 * j + 1]);
+              if (DECAY) {
+                x0 *= f;
+                x1 *= f;
+              }
+              pk[j] = pack_bf16(x0, x1);
             }
+            st_row16(o_sm, BOX_BYTES, row, hlf * 32 + q16 * 16, pk);
           }
         }
       }
@@ -878,136 +928,163 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       named_bar_sync(BAR_WG2, 128);
       if (t == 0) {
         mbar_arrive(&o_free[b]);
-        for (int bb = 0; bb < D / BOX; ++bb)
-          if (LA_CHK(bb * BOX + BOX <= D && tok0 + c * CH < p.L && bh < p.BH,
-                     KID_PREFILL_TC_OUT, 3))
-            tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok0 + c * CH, bh);
+        int sg, c;
+        st.at(k, sg, c);
+        const int tok = tok0[sg] + c * CH;
+        if (LA_CHK(dv0 + 64 <= D && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 3))
+          tma_store_3d(&tmO, o_sm, dv0, tok, bh);
         tma_store_commit();
-        LA_TRACE_EVENT(trace_on, t0, 12, c);
+        LA_TRACE_EVENT(trace_on, t0, 12, k);
       }
       return true;
     };
     bool ok = true;
-    for (int c = 0; ok && c < nc; ++c) {
-      ok = p_epilogue(c);
-      if (ok && c >= 1) ok = o_epilogue(c - 1);
+    float of_prev = 1.f;  // output row factor of the chunk whose O is next
+    for (int k = 0; ok && k < nk; ++k) {
+      ok = p_epilogue(k);
+      if (ok && k >= 1) ok = o_epilogue(k - 1, of_prev);
+      of_prev = of_cur;
     }
-    if (ok && nc > 0) o_epilogue(nc - 1);
+    if (ok && nk > 0) o_epilogue(nk - 1, of_prev);
     if (t == 0) tma_store_wait_all();
   } else if (warp >= WG3) {
-    // ------------------------------------------------------------ WG3: the state chain
+    // ------------------------------------------------------------ WG3: the state chains
     const int t = tid - WG3 * 32;
     const int quarter = warp & 3;
-    const int srow = acc_row<D>(quarter, lane);    // state row (d_k index)
+    const int srow = acc_row<DK>(quarter, lane);    // state row (d_k index)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // 32 columns of state row srow: bf16 copy into an S buffer (MN-major
-    // blocks), and optionally the scaled fp32 values back into TMEM.
-    auto put32 = [&](unsigned char *s_sm, int col, uint32_t (&r)[32], float scale, bool to_tmem) {
+    // 32 columns of state row srow: r * sm_scale as bf16 into a stream's S
+    // buffer, and optionally r * tm_scale back into the stream's TMEM state.
+    auto put32 = [&](int sg, int col, uint32_t (&r)[32], float sm_scale, float tm_scale,
+                     bool to_tmem) {
       if (srow >= 0) {
 #pragma unroll
         for (int q16 = 0; q16 < 2; ++q16) {
           uint32_t pk[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            pk[j] = pack_bf16(__uint_as_float(r[q16 * 16 + 2 * j]),
-                              __uint_as_float(r[q16 * 16 + 2 * j + 1]));
-          st_row16(s_sm, SM::S_BLOCK, srow, col + q16 * 16, pk);
+            pk[j] = pack_bf16(__uint_as_float(r[q16 * 16 + 2 * j]) * sm_scale,
+                              __uint_as_float(r[q16 * 16 + 2 * j + 1]) * sm_scale);
+          st_row16(smem + SM::OFF_S + sg * SM::S_BYTES, SM::S_BYTES, srow, col + q16 * 16, pk);
         }
       }
       if (to_tmem) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * scale);
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * tm_scale);
         __syncwarp();
-        tmem_st32(tmem + lane_off + SM::T_S + col, r);
+        tmem_st32(tmem + lane_off + SM::T_S + 64 * sg + col, r);
       }
     };
-    auto s_buf = [&](int c) {
-      return smem + SM::OFF_S + (SM::NSB == 2 ? (c & 1) * SM::S_BYTES : 0u);
+    // Scales of a stream's state at one of its chunks (decay kernels), as
+    // natural logarithms:
+    //   smem copy  S_c * e^{m}   (m = r = A/2 in the split form, else 0),
+    //   TMEM       S_c * e^{t}   (t = r in the split form, else A),
+    // and after the chunk's MMA4 the TMEM holds S_c+1 * e^{-g} (g = A - r =
+    // A/2 in the split form, else 0).  k is the chunk's virtual index.
+    auto log_scales = [&](int k, float &m, float &tt, float &g) {
+      const int s = k % NST;
+      const float A = lam[s * 64 + 63];
+      if (split[s]) {
+        m = tt = g = 0.5f * A;
+      } else {
+        m = g = 0.f;
+        tt = A;
+      }
     };
+    float g_prev[2] = {0.f, 0.f};  // g of each stream's chunk whose MMA4 is next awaited
     bool ok = true;
-    if (nc > 0) {
-      if (has_init) {
-        // S smem <- S_in, TMEM S <- exp(A_0) S_in (the decay of chunk 0).
-        float a0 = 1.f;
-        if constexpr (DECAY) {
-          ok = wait_wg(&xdone[0], 0, ctl, p.err, KID_PREFILL_TC_OUT, 12, BAR_WG3);
-          if (ok) a0 = __expf(lam[63]);
-        }
-        if (ok) {
+    // Initial states, in the order the streams' first chunks come (k = 0, 1).
+    for (int sg = 0; ok && sg < 2; ++sg) {
+      if (st.nc[sg] == 0) continue;
+      const int k = st.index(sg, 0);
+      float m0 = 0.f, t0s = 0.f;
+      if constexpr (DECAY) {
+        ok = wait_wg(&xdone[k % NST], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 12, BAR_WG3);
+        if (!ok) break;
+        float g0;
+        log_scales(k, m0, t0s, g0);
+        g_prev[sg] = g0;
+      }
+      if (has_init[sg]) {
+        const float sm0 = __expf(m0), tm0 = __expf(t0s);
 #pragma unroll 1
-          for (int col = 0; col < D; col += 32) {
-            uint32_t r[32];
-            if (srow >= 0) {
-              const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
+        for (int col = 0; col < 64; col += 32) {
+          uint32_t r[32];
+          if (srow >= 0) {
+            const float4 *src =
+                reinterpret_cast<const float4 *>(S_in[sg] + (size_t)srow * D + dv0 + col);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float4 f = src[j];
-                r[4 * j] = __float_as_uint(f.x);
-                r[4 * j + 1] = __float_as_uint(f.y);
-                r[4 * j + 2] = __float_as_uint(f.z);
-                r[4 * j + 3] = __float_as_uint(f.w);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) r[j] = 0u;
+            for (int j = 0; j < 8; ++j) {
+              float4 f = src[j];
+              r[4 * j] = __float_as_uint(f.x);
+              r[4 * j + 1] = __float_as_uint(f.y);
+              r[4 * j + 2] = __float_as_uint(f.z);
+              r[4 * j + 3] = __float_as_uint(f.w);
             }
-            put32(s_buf(0), col, r, a0, true);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
           }
-          tmem_st_wait();
+          put32(sg, col, r, sm0, tm0, true);
         }
+        tmem_st_wait();
       }
-      if (ok) {
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(BAR_WG3, 128);
-        if (t == 0) mbar_arrive(s_ready);
-      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_WG3, 128);
+      if (t == 0) mbar_arrive(&s_ready[sg]);
     }
-    for (int c = 0; ok && c < nc; ++c) {
-      if (!(ok = wait_wg(s_done, c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13, BAR_WG3))) break;
+    for (int k = 0; ok && k < nk; ++k) {
+      int sg, c;
+      st.at(k, sg, c);
+      if (!(ok = wait_wg(&s_done[sg], c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13, BAR_WG3))) break;
       tc_fence_after();
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 10, c);
-      if (c + 1 < nc) {
-        // TMEM holds S_c+1.  Copy it to bf16 for chunk c+1's Qt S, and leave
-        // exp(A_c+1) S_c+1 in TMEM for its state update.
-        const int s1 = (c + 1) % NST;
-        float a1 = 1.f;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 10, k);
+      if (c + 1 < st.nc[sg]) {
+        // TMEM holds S_c+1 * e^{-g_c}.  Copy S_c+1 * e^{m_c+1} to bf16 for
+        // the next chunk's Q S, and leave S_c+1 * e^{t_c+1} in TMEM for its
+        // state update.  Each scale is one exponential of a sum >= -80.
+        const int kn = st.index(sg, c + 1);
+        float sm = 1.f, tm = 1.f;
         if constexpr (DECAY) {
-          if (!(ok = wait_wg(&xdone[s1], ((c + 1) / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
+          if (!(ok = wait_wg(&xdone[kn % NST], (kn / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
                              BAR_WG3)))
             break;
-          a1 = __expf(lam[s1 * 64 + 63]);
+          float m1, t1, g1;
+          log_scales(kn, m1, t1, g1);
+          sm = __expf(g_prev[sg] + m1);
+          tm = __expf(g_prev[sg] + t1);
+          g_prev[sg] = g1;
         }
-        unsigned char *s_sm = s_buf(c + 1);
-#pragma unroll 1
-        for (int col = 0; col < D; col += 64) {
-          __syncwarp();
-          uint32_t r[2][32];
-          tmem_ld32(tmem + lane_off + SM::T_S + col, r[0]);
-          tmem_ld32(tmem + lane_off + SM::T_S + col + 32, r[1]);
-          tmem_ld_wait();
-          put32(s_sm, col, r[0], a1, DECAY);
-          put32(s_sm, col + 32, r[1], a1, DECAY);
-        }
+        __syncwarp();
+        uint32_t r[2][32];
+        tmem_ld32(tmem + lane_off + SM::T_S + 64 * sg, r[0]);
+        tmem_ld32(tmem + lane_off + SM::T_S + 64 * sg + 32, r[1]);
+        tmem_ld_wait();
+        put32(sg, 0, r[0], sm, tm, DECAY);
+        put32(sg, 32, r[1], sm, tm, DECAY);
         if (DECAY) tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(BAR_WG3, 128);
-        if (t == 0) mbar_arrive(s_ready);
-        LA_TRACE_EVENT(trace_on && t == 0, t0, 11, c);
-      } else if (last_seg && p.S_final) {
+        if (t == 0) mbar_arrive(&s_ready[sg]);
+        LA_TRACE_EVENT(trace_on && t == 0, t0, 11, k);
+      } else if (last_seg[sg] && p.S_final) {
+        const float fin = DECAY ? __expf(g_prev[sg]) : 1.f;
 #pragma unroll 1
-        for (int col = 0; col < D; col += 32) {
+        for (int col = 0; col < 64; col += 32) {
           __syncwarp();
           uint32_t r[32];
-          tmem_ld32(tmem + lane_off + SM::T_S + col, r);
+          tmem_ld32(tmem + lane_off + SM::T_S + 64 * sg + col, r);
           tmem_ld_wait();
           if (srow >= 0) {
-            float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D + col);
+            float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D +
+                                                     dv0 + col);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+              dst[j] = make_float4(__uint_as_float(r[4 * j]) * fin, __uint_as_float(r[4 * j + 1]) * fin,
+                                   __uint_as_float(r[4 * j + 2]) * fin,
+                                   __uint_as_float(r[4 * j + 3]) * fin);
           }
         }
       }
@@ -1038,27 +1115,46 @@ int sm_count() {
   return n;
 }
 
-#ifndef LA_TC_TARGET_WAVES
-#define LA_TC_TARGET_WAVES 2
-#endif
-
-Plan make_plan(int B, int H, int L) {
-  Plan pl;
-  pl.n_chunks = (L + CH - 1) / CH;
-  const long bh = (long)B * H;
-  const long target = (long)LA_TC_TARGET_WAVES * sm_count();
-  long ns = (target + bh - 1) / bh;
-  ns = std::max(1L, std::min(ns, (long)pl.n_chunks));
-  int g = (int)((pl.n_chunks + ns - 1) / ns);
-  g = std::min(g, kMaxSegChunks);
-  g = std::max(g, 1);
-  pl.seg_chunks = g;
-  pl.n_seg = (pl.n_chunks + g - 1) / g;
-  return pl;
+// Segment count.  The output kernel runs ceil(NS/2) x BH x (D/64) CTAs, each
+// over the chunks of two segments; the segment-state kernel (NS > 1) runs
+// (NS-1) x BH CTAs and reads K and V of all but the last segment once more;
+// the scan moves the segment states.  The estimate of each kernel is the
+// larger of its wave time -- waves x (fixed CTA cost + chunk steps x step
+// time) -- and its bytes over the HBM bandwidth; step times and fixed costs
+// are measured ones for these kernels on GB300 (microseconds).  G <= 32
+// bounds the segment-state kernel's suffix table.
+Plan make_plan(int B, int H, int L, int D) {
+  const int nc = (L + CH - 1) / CH;
+  const double bh = (double)B * H, sms = sm_count(), slices = D / 64;
+  const double t_out = D == 128 ? 0.8 : 0.7, t_state = D == 128 ? 0.7 : 0.4;
+  const double fill_out = 3.0, fill_state = 2.0, t_launch = 3.0, bw = 6.5e-3;  // bytes/us / 1e9
+  const double tile = 64.0 * D * 2, state = (double)D * D * 4;
+  Plan best{nc, nc, 1};
+  double best_t = 1e300;
+  for (int ns = 1; ns <= std::min(nc, 256); ++ns) {
+    const int g = (nc + ns - 1) / ns;
+    const int n_seg = (nc + g - 1) / g;
+    if (g > kMaxSegChunks || n_seg != ns) continue;
+    const double ctas = std::ceil(n_seg / 2.0) * bh * slices;
+    const double steps = n_seg > 1 ? 2.0 * g : (double)g;
+    const double out_bytes = bh * (nc * 4.0 * tile + (n_seg > 1 ? n_seg * state : 0.0));
+    double t = std::max(std::ceil(ctas / sms) * (fill_out + steps * t_out), out_bytes / bw * 1e-9);
+    if (n_seg > 1) {
+      const double sctas = (n_seg - 1) * bh;
+      const double st_bytes = bh * ((n_seg - 1) * (g * 2.0 * tile + state));
+      t += std::max(std::ceil(sctas / sms) * (fill_state + g * t_state), st_bytes / bw * 1e-9);
+      t += 2 * t_launch + bh * n_seg * 2.0 * state / bw * 1e-9;
+    }
+    if (t < best_t) {
+      best_t = t;
+      best = Plan{nc, g, n_seg};
+    }
+  }
+  return best;
 }
 
 size_t ws_bytes_for(int B, int H, int L, int D) {
-  Plan pl = make_plan(B, H, L);
+  Plan pl = make_plan(B, H, L, D);
   if (pl.n_seg <= 1) return 0;
   const size_t bh = (size_t)B * H;
   const size_t st = bh * pl.n_seg * (size_t)D * D * sizeof(float);
@@ -1079,7 +1175,7 @@ cudaError_t set_smem_once(K kern, size_t bytes, int *done_for_device) {
 
 template <int D, bool PHI, bool DECAY>
 cudaError_t launch_d(const PrefillArgs &a, const char **why) {
-  const Plan pl = make_plan(a.B, a.H, a.L);
+  const Plan pl = make_plan(a.B, a.H, a.L, D);
   const int BH = a.B * a.H;
   TcParams p{};
   p.H = a.H;
@@ -1143,7 +1239,7 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   static int smem_set_out[64];
   e = set_smem_once(ko, OS::BYTES, smem_set_out);
   if (e != cudaSuccess) return e;
-  ko<<<dim3(pl.n_seg, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  ko<<<dim3((pl.n_seg + 1) / 2, BH, D / 64), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
   if ((e = cudaGetLastError()) != cudaSuccess && why)
     *why = "la_chunk_fwd: chunk-output kernel launch";
 #ifdef LA_CHECKED
@@ -1164,8 +1260,8 @@ size_t prefill_tc_workspace_bytes(int B, int H, int L, int d) {
   return ws_bytes_for(B, H, L, d);
 }
 
-int prefill_tc_kernel_count(int B, int H, int L, int) {
-  return make_plan(B, H, L).n_seg > 1 ? 3 : 1;
+int prefill_tc_kernel_count(int B, int H, int L, int d) {
+  return make_plan(B, H, L, d).n_seg > 1 ? 3 : 1;
 }
 
 template <int D>

@@ -78,10 +78,9 @@ def test_headline_fp32_workload():
     parity.check(S, S_ref, "f32", "S_final")
 
 
-# Many (b, h) sequences of a few chunks each: the launcher then gives every
-# output CTA several chunks (G > 1) in one or more segments, which exercises
-# the stage ring, the lookahead and the state chain at small sizes.  B*H = 152
-# gives two segments of five chunks; B*H = 304 gives one segment of ten.
+# Many (b, h) sequences of ten chunks each: the launcher keeps each sequence
+# in one segment, so every output CTA runs one long state chain through the
+# stage ring and the lookahead (d = 128 over two value-column slices).
 MULTI = [
     # (B, H, L, d, phi, decay, s0)
     (2, 76, 640, 64, "identity", "none", None),
@@ -101,6 +100,68 @@ def test_multi_chunk_segments_match_oracle(case):
     w, inp = _make(B, H, L, d, d, "bf16", phi, decay, 64, s0)
     O, S = gpu_prefill(inp, w.phi, 64)
     pairs = [(0, 0), (B - 1, H - 1), (B // 2, H // 3), (1, 5)]
+    O_ref, S_ref = oracle_prefill(inp, w.phi, pairs)
+    parity.check(select_pairs(O, pairs), O_ref, "bf16", "O")
+    parity.check(select_pairs(S, pairs), S_ref, "bf16", "S_final")
+
+
+# Sequences the launcher cuts into segments: a segment-state pass and a scan
+# give each segment its incoming state, and each output CTA interleaves two
+# segments.  The shapes cover one-chunk segments, an odd segment count (the
+# last CTA has one segment), a short last segment, and both head sizes.
+SEGMENTED = [
+    # (B, H, L, d, phi, decay, s0, sampled pairs or None for all)
+    (1, 2, 1000, 64, "elu1", "none", None, None),
+    (1, 2, 2100, 128, "identity", "head", 0.1, None),
+    (2, 4, 3000, 64, "identity", "logit", 0.1, None),
+    (1, 2, 6000, 64, "elu1", "head", None, None),
+    (2, 4, 1500, 128, "elu1", "none", 0.1, None),
+    (2, 4, 6000, 128, "identity", "logit", 0.1, [(0, 0), (1, 3), (0, 2)]),
+]
+
+
+@pytest.mark.parametrize("case", SEGMENTED,
+                         ids=[f"{c[0]}x{c[1]}x{c[2]}_d{c[3]}_{c[4]}_{c[5]}" for c in SEGMENTED])
+def test_segmented_sequences_match_oracle(case):
+    B, H, L, d, phi, decay, s0, pairs = case
+    assert api.la_chunk_fwd_workspace_bytes(B, H, L, d, d, 64) > 0  # segments in use
+    w, inp = _make(B, H, L, d, d, "bf16", phi, decay, 64, s0)
+    O, S = gpu_prefill(inp, w.phi, 64)
+    if pairs is None:
+        O_ref, S_ref = oracle_prefill(inp, w.phi)
+        parity.check(O, O_ref, "bf16", "O")
+        parity.check(S, S_ref, "bf16", "S_final")
+    else:
+        O_ref, S_ref = oracle_prefill(inp, w.phi, pairs)
+        parity.check(select_pairs(O, pairs), O_ref, "bf16", "O")
+        parity.check(select_pairs(S, pairs), S_ref, "bf16", "S_final")
+
+
+# Per-token decays whose strength alternates by chunk: odd chunks decay hard
+# (log a ~ -2.4 per token, chunk total ~ -155), even chunks gently (~ -15).
+# The tensor-core kernel treats the two kinds of chunk differently (the decay
+# folded into V rows and output rows, or applied per element), so this checks
+# both and the hand-over of the state between them.
+MIXED = [
+    # (B, H, L, d, phi)
+    (1, 2, 300, 64, "identity"),
+    (1, 2, 300, 128, "elu1"),
+    (2, 76, 640, 128, "identity"),
+    (2, 76, 600, 64, "elu1"),
+    (2, 4, 3000, 128, "identity"),
+    (2, 4, 3000, 64, "elu1"),
+]
+
+
+@pytest.mark.parametrize("case", MIXED, ids=[f"{c[0]}x{c[1]}x{c[2]}_d{c[3]}_{c[4]}" for c in MIXED])
+def test_mixed_strong_and_weak_decay_chunks(case):
+    B, H, L, d, phi = case
+    w, inp = _make(B, H, L, d, d, "bf16", phi, "token", 64, 0.1)
+    g = torch.randn(B, H, L, generator=torch.Generator().manual_seed(7), dtype=torch.float64)
+    strength = torch.where((torch.arange(L) // 64) % 2 == 1, 3.0, 0.3).double()
+    inp["decay"] = (-strength * torch.nn.functional.softplus(g)).float()
+    O, S = gpu_prefill(inp, w.phi, 64)
+    pairs = [(0, 0), (B - 1, H - 1), (B // 2, H // 3)]
     O_ref, S_ref = oracle_prefill(inp, w.phi, pairs)
     parity.check(select_pairs(O, pairs), O_ref, "bf16", "O")
     parity.check(select_pairs(S, pairs), S_ref, "bf16", "S_final")

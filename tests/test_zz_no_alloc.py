@@ -26,8 +26,8 @@ def _inputs(B, H, L, d, phi, decay, s0, seed):
 @pytest.mark.parametrize("d", [64, 128])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(d):
     cases = [  # both split each sequence into segments, so the scratch is used
-        (2, 76, 640, d, "identity", "head", None, 0),
-        (2, 76, 600, d, "identity", "logit", 0.1, 1),
+        (2, 4, 3000, d, "identity", "head", None, 0),
+        (2, 4, 1500, d, "identity", "logit", 0.1, 1),
     ]
     api.la_set_feature_map("identity")
     runs = []
