@@ -160,6 +160,18 @@ __device__ __forceinline__ float token_lambda(int kind, const float *__restrict_
   }
 }
 
+// The same in two steps: the stored input of a token (a gate logit for
+// LA_DECAY_GATE_LOGIT; 0 beyond the sequence, where the log decay is 0
+// for every kind), then its log decay.
+__device__ __forceinline__ float token_decay_raw(int kind, const float *__restrict__ decay, int h,
+                                                 size_t bhL, int tok, int L) {
+  if (tok >= L) return kind == LA_DECAY_GATE_LOGIT ? -INFINITY : 0.f;
+  return kind == LA_DECAY_HEAD ? decay[h] : decay[bhL + tok];
+}
+__device__ __forceinline__ float token_log_decay(int kind, float raw) {
+  return kind == LA_DECAY_GATE_LOGIT ? neg_softplus(raw) : raw;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t *>(&v);
@@ -474,24 +486,33 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
 }
 
 // ================================================================ chunk output
-// One CTA runs two segments of one (b, h) sequence -- two independent state
-// chains, "streams" -- over one 64-wide slice of the value columns (the state
-// columns S[:, slice] and the output columns O[:, slice] depend on V[:, slice]
-// alone).  The chunks of the two streams are interleaved into one sequence of
-// virtual chunks k = 0, 1, ...: while both have chunks left they alternate, so
-// a stream's state hand-over (MMA, then the TMEM -> bf16 copy) overlaps the
-// other stream's chunk.
+// Each output CTA carries two independent state chains, each a [d_k x 64]
+// block of state with its own hand-over (MMA into TMEM, then the TMEM -> bf16
+// copy), so that one chain's hand-over overlaps the other chain's work:
+//   d = 64:  the two chains are two segments of one (b, h) sequence.  Their
+//            chunks are interleaved into one sequence of virtual chunks
+//            k = 0, 1, ...: while both have chunks left they alternate.
+//   d = 128: the two chains are the two 64-column halves of one segment's
+//            state (S[:, half] and O[:, half] depend on V[:, half] alone);
+//            virtual chunk k is chunk k of the segment, and both halves
+//            advance in it.
+#ifndef LA_D128_CHAINS
+#define LA_D128_CHAINS 1
+#endif
 template <int DK>
 struct OutSmem {
-  static constexpr int NST = (DK == 128) ? 3 : 4;
-  static constexpr uint32_t QK_TILE = 64 * DK * 2;         // Q or K tile of one chunk
-  static constexpr uint32_t V_TILE = 64 * 64 * 2;          // the chunk's V slice
-  static constexpr uint32_t STAGE = 2 * QK_TILE + V_TILE;  // Q | K | V
+  static constexpr bool PAIRS = DK == 64;                       // two segments per CTA
+  static constexpr int NCHAIN = PAIRS ? 2 : LA_D128_CHAINS;     // state chains
+  static constexpr int CW = PAIRS ? 64 : DK / NCHAIN;           // state columns per chain
+  static constexpr int NST = PAIRS ? 4 : 3;
+  static constexpr uint32_t TILE = 64 * DK * 2;            // Q, K, V or O tile of one chunk
+  static constexpr uint32_t STAGE = 3 * TILE;              // Q | K | V
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
-  static constexpr uint32_t S_BYTES = DK * 128;            // [DK][64] bf16, MN-major
-  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;      // one per stream
-  static constexpr uint32_t OFF_O = OFF_S + 2 * S_BYTES;   // 2 x [64][64] bf16 store staging
-  static constexpr uint32_t OFF_LAM = OFF_O + 2 * 8192;    // [NST][64] inclusive prefix
+  static constexpr uint32_t S_BLOCK = DK * 128;            // [DK][64] bf16, MN-major
+  static constexpr uint32_t S_BYTES = S_BLOCK * (CW / 64); // one chain's bf16 state
+  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;
+  static constexpr uint32_t OFF_O = OFF_S + NCHAIN * S_BYTES;  // 2 x O tile store staging
+  static constexpr uint32_t OFF_LAM = OFF_O + 2 * TILE;    // [NST][64] inclusive prefix
   static constexpr uint32_t OFF_VF = OFF_LAM + NST * 64 * 4;   // [NST][64] exp(A/2 - Lam_j)
   static constexpr uint32_t OFF_OF = OFF_VF + NST * 64 * 4;    // [NST][64] exp(Lam_i - A/2)
   static constexpr uint32_t OFF_SPLIT = OFF_OF + NST * 64 * 4; // [NST] split decay used
@@ -504,8 +525,9 @@ struct OutSmem {
                     OFF_O % 1024 == 0 && S_BYTES % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
-  // TMEM columns: P and O by virtual chunk parity, S by stream.
-  static constexpr uint32_t T_P = 0, T_O = 128, T_S = 256, T_COLS = 512;
+  // TMEM columns: P and O by virtual chunk parity, S by chain (CW columns each).
+  static constexpr uint32_t T_P = 0, T_O = 128, T_S = 128 + 2 * DK, T_COLS = 512;
+  static_assert(T_S + NCHAIN * CW <= T_COLS, "TMEM budget");
 };
 
 // Warps: 0 TMA, 1 MMA, 2-7 PREP (192 threads), 8-11 WG2, 12-15 WG3.
@@ -528,11 +550,50 @@ constexpr uint32_t BAR_PREP = 1, BAR_WG3 = 3;
 // rescaled in place once QK^T has read them.
 constexpr float kSplitMinLogDecay = -80.f;
 
-// The virtual-chunk order of a CTA's two streams.
+// P epilogue of a chunk outside the split decay form (total log decay below
+// the bound): mask and exp(Lam_i - Lam_j) per element, from TMEM to the
+// swizzled bf16 P tile.  Rare, so one compact out-of-line copy: 16 columns
+// per step.  Called by all 32 lanes of each warp of the epilogue warpgroup
+// (tcgen05.ld is warp-collective).
+__device__ __noinline__ void p_tile_strong_decay(uint32_t t_p, int row, const float *lm,
+                                                 unsigned char *ps) {
+  const float li = row >= 0 ? lm[row] : 0.f;
+#pragma unroll 1
+  for (int j16 = 0; j16 < 64; j16 += 16) {
+    uint32_t r[16];
+    __syncwarp();
+    tmem_ld16(t_p + j16, r);
+    tmem_ld_wait();
+    if (row >= 0) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int j = 0; j < 16; j += 2) {
+        const int j0 = j16 + j;
+        const float v0 = j0 <= row ? __uint_as_float(r[j]) * __expf(fminf(li - lm[j0], 0.f)) : 0.f;
+        const float v1 =
+            j0 + 1 <= row ? __uint_as_float(r[j + 1]) * __expf(fminf(li - lm[j0 + 1], 0.f)) : 0.f;
+        pk[j >> 1] = pack_bf16(v0, v1);
+      }
+      st_row16(ps, 8192, row, j16, pk);
+    }
+  }
+}
+
+// Rows of the chunk's Q and K tiles scaled in place for the per-element decay
+// form: Qt_i = exp(Lam_i) q_i, Kt_j = exp(A - Lam_j) k_j.  Rare; out of line.
+template <int DK>
+__device__ __noinline__ void rescale_qk_rows(unsigned char *stage, const float *lm, int t, int n) {
+  const float A = lm[63];
+  tile_pass<DK, 2, false, true>(
+      stage, [lm, A](int kt, int r) { return __expf(kt == 0 ? lm[r] : A - lm[r]); }, t, n);
+}
+
+// The virtual-chunk order of a CTA's two segments (d = 64), or of its one
+// segment (d = 128: nc[1] = 0).
 struct Streams {
-  int nc[2];   // chunks per stream (stream 1 may have none)
-  int m;       // chunks both streams have: virtual 0 .. 2m-1 alternate
-  int longer;  // the stream whose chunks follow alone
+  int nc[2];   // chunks per segment (the second may have none)
+  int m;       // chunks both have: virtual 0 .. 2m-1 alternate
+  int longer;  // the segment whose chunks follow alone
   __device__ void at(int k, int &sg, int &c) const {
     if (k < 2 * m) {
       sg = k & 1;
@@ -553,6 +614,8 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmO, TcParams p) {
   using SM = OutSmem<DK>;
   constexpr int NST = SM::NST;
+  constexpr bool PAIRS = SM::PAIRS;
+  constexpr int NCHAIN = SM::NCHAIN, CW = SM::CW;
   constexpr int D = DK;  // d_k = d_v: the state row length
   extern __shared__ __align__(1024) unsigned char smem[];
   float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
@@ -563,44 +626,49 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
   uint64_t *xdone = empty + NST;       // [NST] phi applied, Lam, V rows and factors ready
-  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K rows hold what MMA3 / MMA4 need
+  uint64_t *qk_ready = xdone + NST;    // [NST] Q, K, V rows hold what MMA2-4 need
   uint64_t *p_full = qk_ready + NST;   // [2] MMA1 done
   uint64_t *p_ready = p_full + 2;      // [2] P in smem
   uint64_t *o_full = p_ready + 2;      // [2] MMA2 done: O complete in TMEM, P smem free
   uint64_t *o_free = o_full + 2;       // [2] O TMEM buffer read
-  uint64_t *s_ready = o_free + 2;      // [stream] S_c in smem, scaled S_c in TMEM
-  uint64_t *s_done = s_ready + 2;      // [stream] MMA4 and MMA3 of the stream's chunk done
+  uint64_t *s_ready = o_free + 2;      // [chain] S_c in smem, scaled S_c in TMEM
+  uint64_t *s_done = s_ready + 2;      // [chain] the chain's MMA4 and MMA3 of a chunk done
   uint64_t *drain = s_done + 2;        // abort path: all issued MMAs done
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pair = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
-  const int dv0 = blockIdx.z * 64;  // first value column of this CTA's slice
+  const int bh = blockIdx.y, h = bh % p.H;
   const size_t bhL = (size_t)bh * p.L;
+  // Segments of this CTA (one for d = 128).
   Streams st;
   int tok0[2], seg[2];
-  const float *S_in[2];
-  bool last_seg[2], has_init[2];
+  const float *S_seg[2];
   for (int sg = 0; sg < 2; ++sg) {
-    seg[sg] = 2 * pair + sg;
+    seg[sg] = PAIRS ? 2 * (int)blockIdx.x + sg : (sg == 0 ? (int)blockIdx.x : p.n_seg);
     const int c0 = seg[sg] * p.seg_chunks;
     st.nc[sg] = seg[sg] < p.n_seg ? min(p.seg_chunks, p.n_chunks - c0) : 0;
     tok0[sg] = c0 * CH;
-    last_seg[sg] = seg[sg] == p.n_seg - 1;
-    S_in[sg] = nullptr;
+    S_seg[sg] = nullptr;
     if (p.n_seg > 1) {
-      if (seg[sg] > 0 || p.S0) S_in[sg] = p.ws_state + ((size_t)bh * p.n_seg + seg[sg]) * D * D;
+      if (seg[sg] > 0 || p.S0) S_seg[sg] = p.ws_state + ((size_t)bh * p.n_seg + seg[sg]) * D * D;
     } else {
-      S_in[sg] = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
+      S_seg[sg] = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
     }
-    has_init[sg] = S_in[sg] != nullptr;
   }
   st.m = min(st.nc[0], st.nc[1]);
   st.longer = st.nc[0] >= st.nc[1] ? 0 : 1;
   const int nk = st.nc[0] + st.nc[1];
+  // Chain ch: its segment, its first state column, and its chunk index in
+  // virtual chunk k.
+  auto ch_seg = [&](int ch) { return PAIRS ? ch : 0; };
+  auto ch_col = [](int ch) { return PAIRS ? 0 : CW * ch; };
+  auto ch_chunk = [&](int ch, int k) {
+    int sg, c;
+    st.at(k, sg, c);
+    return PAIRS ? c : k;
+  };
   if (tid == 0) {
-    (void)LA_CHK(bh < p.BH && seg[0] < p.n_seg && st.nc[0] >= 1 && dv0 + 64 <= D,
-                 KID_PREFILL_TC_OUT, 5);
+    (void)LA_CHK(bh < p.BH && seg[0] < p.n_seg && st.nc[0] >= 1, KID_PREFILL_TC_OUT, 5);
     (void)LA_CHK(!p.S_final || bh < p.BH, KID_PREFILL_TC_OUT, 6);
   }
 
@@ -631,7 +699,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const bool trace_on = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  const bool trace_on = blockIdx.x == 0 && blockIdx.y == 0;
   const long long t0 = clock64();
   (void)trace_on;
   (void)t0;
@@ -658,10 +726,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           if (!LA_CHK(b * BOX + BOX <= DK && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 2))
             continue;
           tma_load_3d(stg + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
-          tma_load_3d(stg + SM::QK_TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
+          tma_load_3d(stg + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
+          tma_load_3d(stg + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
         }
-        if (LA_CHK(dv0 + 64 <= D && tok < p.L, KID_PREFILL_TC_OUT, 4))
-          tma_load_3d(stg + 2 * SM::QK_TILE, &tmV, &full[s], dv0, tok, bh);
         LA_TRACE_EVENT(trace_on, t0, 0, k);
         issued = k + 1;
       }
@@ -676,77 +743,123 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nk > 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(64, 64, false, true);
-      constexpr uint32_t id_qs = idesc_bf16_f32(64, 64, false, true);
-      constexpr uint32_t id_kv = idesc_bf16_f32(DK, 64, true, true);
+      constexpr uint32_t id_pv = idesc_bf16_f32(64, DK, false, true);
+      constexpr uint32_t id_qs = idesc_bf16_f32(64, CW, false, true);
+      constexpr uint32_t id_kv = idesc_bf16_f32(DK, CW, true, true);
       // Operand descriptors: the base descriptor of each layout at the start
       // of shared memory, plus (byte offset >> 4) in its 14-bit address field
       // (shared memory ends below 256 KB, so the field never carries).
       const uint32_t sbase = smem_u32(smem);
       const uint64_t dKM = smem_desc_sw128(sbase, 16, 1024);          // K-major rows
       const uint64_t dMN = smem_desc_sw128(sbase, BOX_BYTES, 1024);   // MN-major, 8 KB blocks
+      const uint64_t dMS = smem_desc_sw128(sbase, SM::S_BLOCK, 1024); // MN-major state blocks
       auto at = [](uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); };
-      // QK^T of virtual chunk k into P buffer k & 1, once its tiles are ready.
-      auto issue_qk = [&](int k) -> bool {
-        const int s = k % NST;
-        if (!wait1(&xdone[s], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 2)) return false;
-        tc_fence_after();
-        const uint32_t so = s * SM::STAGE;
+      // Three streams of MMA work, issued as each becomes ready (non-blocking
+      // tests), so that a late input of one never holds up another:
+      //   chain step kc: per chain, S += K^T V and O = Q S_c (needs the
+      //     chain's state, Q/K/V rows in final form, O buffer kc & 1 free);
+      //   P V of chunk km (needs P in smem; after its chain step);
+      //   QK^T of chunk kq (needs its tiles; P buffer kq & 1 free once
+      //     P V of chunk kq - 2 is issued: kq <= km + 1).
+      // In each stream the chunks go in order, and every test is of a phase
+      // that cannot yet be overtaken by the next one on the same barrier.
+      int kq = 0, kc = 0, cc = 0, km = 0;  // cc: next chain within step kc
+      bool ok = true;
+      uint64_t idle_since = 0;
+      uint32_t idle_polls = 0;
+      while (ok && km < nk) {
+        bool did = false;
+        if (kc < nk) {  // ---- chain step
+          int sg, c;
+          st.at(kc, sg, c);
+          const int s = kc % NST, b = kc & 1;
+          const int ch = PAIRS ? sg : cc;
+          // Q, K, V of the chunk in their final form: phi applied (xdone) and,
+          // with decay, the rows scaled (qk_ready, which follows xdone).
+          const bool inputs =
+              (cc > 0) || ((kc < 2 || mbar_test(&o_free[b], ((kc >> 1) - 1) & 1)) &&
+                           mbar_test(DECAY ? &qk_ready[s] : &xdone[s], (kc / NST) & 1));
+          if (inputs && mbar_test(&s_ready[ch], ch_chunk(ch, kc) & 1)) {
+            tc_fence_after();
+            LA_TRACE_EVENT(trace_on && cc == 0, t0, 8, kc);
+            const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
+            const uint32_t o_t = tmem + SM::T_O + DK * b;
+            const bool inter = S_seg[sg] != nullptr || c > 0;
+            const uint32_t vb = vo + (PAIRS ? 0u : (uint32_t)(ch * (CW / 64)) * BOX_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < DK / 16; ++kk) {
-          const uint32_t off = so + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-          mma_bf16(tmem + SM::T_P + 64 * (k & 1), at(dKM, off), at(dKM, off + SM::QK_TILE), id_qk,
-                   kk > 0);
-        }
-        mma_commit(&p_full[k & 1]);
-        return true;
-      };
-      bool ok = issue_qk(0) && (nk < 2 || issue_qk(1));
-      for (int k = 0; ok && k < nk; ++k) {
-        int sg, c;
-        st.at(k, sg, c);
-        const int s = k % NST, b = k & 1;
-        const uint32_t qo = s * SM::STAGE, ko = qo + SM::QK_TILE, vo = qo + 2 * SM::QK_TILE;
-        const uint32_t o_t = tmem + SM::T_O + 64 * b;
-        const uint32_t so = SM::OFF_S + sg * SM::S_BYTES;
-        if (k >= 2 &&
-            !(ok = wait1(&o_free[b], ((k >> 1) - 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 5)))
-          break;
-        if (!(ok = wait1(&s_ready[sg], c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 6))) break;
-        if (DECAY &&
-            !(ok = wait1(&qk_ready[s], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 4)))
-          break;
-        tc_fence_after();
-        LA_TRACE_EVENT(trace_on, t0, 8, k);
-        const bool inter = has_init[sg] || c > 0;
+            for (int kk = 0; kk < CH / 16; ++kk)   // chain state: S (TMEM) += K^T V
+              mma_bf16(tmem + SM::T_S + CW * ch, at(dMN, ko + 2048 * kk), at(dMN, vb + 2048 * kk),
+                       id_kv, (inter || kk > 0) ? 1u : 0u);
+            if (inter) {
+              const uint32_t so = SM::OFF_S + ch * SM::S_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)   // stream state: S (TMEM) += K^T V
-          mma_bf16(tmem + SM::T_S + 64 * sg, at(dMN, ko + 2048 * kk), at(dMN, vo + 2048 * kk),
-                   id_kv, (inter || kk > 0) ? 1u : 0u);
-        if (inter) {
-#pragma unroll
-          for (int kk = 0; kk < DK / 16; ++kk) {  // O = Q S_c
-            const uint32_t off = qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-            mma_bf16(o_t, at(dKM, off), at(dMN, so + 2048 * kk), id_qs, kk > 0);
+              for (int kk = 0; kk < DK / 16; ++kk) {  // O[:, chain] = Q S_c[:, chain]
+                const uint32_t off = qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+                mma_bf16(o_t + ch_col(ch), at(dKM, off), at(dMS, so + 2048 * kk), id_qs, kk > 0);
+              }
+            }
+            mma_commit(&s_done[ch]);
+            if (PAIRS || ++cc == NCHAIN) {
+              cc = 0;
+              ++kc;
+              LA_TRACE_EVENT(trace_on, t0, 9, kc - 1);
+            }
+            did = true;
           }
         }
-        mma_commit(&s_done[sg]);
-        LA_TRACE_EVENT(trace_on, t0, 9, k);
-        if (!(ok = wait1(&p_ready[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 3))) break;
-        tc_fence_after();
-        LA_TRACE_EVENT(trace_on, t0, 5, k);
-        const uint32_t po = SM::OFF_P + 8192 * b;
+        if (km < kc) {  // ---- P V
+          int sg, c;
+          st.at(km, sg, c);
+          const int s = km % NST, b = km & 1;
+          if (mbar_test(&p_ready[b], (km >> 1) & 1)) {
+            tc_fence_after();
+            LA_TRACE_EVENT(trace_on, t0, 5, km);
+            const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * b;
+            const bool inter = S_seg[sg] != nullptr || c > 0;
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)   // O += P V
-          mma_bf16(o_t, at(dKM, po + 32 * kk), at(dMN, vo + 2048 * kk), id_pv,
-                   (inter || kk > 0) ? 1u : 0u);
-        mma_commit(&o_full[b]);
-        mma_commit(&empty[s]);
-        LA_TRACE_EVENT(trace_on, t0, 6, k);
-        if (k + 2 < nk) {
-          ok = issue_qk(k + 2);
-          LA_TRACE_EVENT(trace_on, t0, 7, k);
+            for (int kk = 0; kk < CH / 16; ++kk)   // O += P V
+              mma_bf16(tmem + SM::T_O + DK * b, at(dKM, po + 32 * kk), at(dMN, vo + 2048 * kk),
+                       id_pv, (inter || kk > 0) ? 1u : 0u);
+            mma_commit(&o_full[b]);
+            mma_commit(&empty[s]);
+            LA_TRACE_EVENT(trace_on, t0, 6, km);
+            ++km;
+            did = true;
+          }
         }
+        if (kq < nk && kq <= km + 1) {  // ---- QK^T
+          const int s = kq % NST;
+          if (mbar_test(&xdone[s], (kq / NST) & 1)) {
+            tc_fence_after();
+            const uint32_t so = s * SM::STAGE;
+#pragma unroll
+            for (int kk = 0; kk < DK / 16; ++kk) {
+              const uint32_t off = so + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+              mma_bf16(tmem + SM::T_P + 64 * (kq & 1), at(dKM, off), at(dKM, off + SM::TILE),
+                       id_qk, kk > 0);
+            }
+            mma_commit(&p_full[kq & 1]);
+            LA_TRACE_EVENT(trace_on, t0, 7, kq);
+            ++kq;
+            did = true;
+          }
+        }
+        if (did) {
+          idle_polls = 0;
+        } else if (__nanosleep(20), ++idle_polls == 64) {  // bounded: give up after the limit
+          const uint64_t now = global_timer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > kWaitNs || *(volatile uint32_t *)&ctl->abort) {
+            if (!*(volatile uint32_t *)&ctl->abort) {
+              atomicExch(&ctl->abort, 1u);
+              record_device_error(p.err, KID_PREFILL_TC_OUT, 20);
+            }
+            ok = false;
+          }
+          idle_polls = 0;
+        }
+        if (did) idle_since = 0;
       }
       if (!ok) {  // let every issued MMA finish before TMEM is released
         mma_commit(drain);
@@ -759,6 +872,15 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_PREFILL_TC_OUT, site, BAR_PREP, t);
     };
+    // Threads t < 64 load their token's decay input one chunk ahead, so the
+    // global load is in flight while the previous chunk is prepared.
+    auto decay_raw = [&](int k) -> float {
+      int sg, c;
+      st.at(k, sg, c);
+      return token_decay_raw(p.decay_kind, p.decay, h, bhL, tok0[sg] + c * CH + t, p.L);
+    };
+    float raw_next = 0.f;
+    if (DECAY && t < 64 && nk > 0) raw_next = decay_raw(0);
     auto prep = [&](int k) -> bool {
       const int s = k % NST;
       if (!gwait(&full[s], (k / NST) & 1, 7)) return false;
@@ -766,10 +888,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       unsigned char *qt = smem + s * SM::STAGE;
       bool sp = false;  // uniform over the group
       if constexpr (DECAY) {
-        int sg, c;
-        st.at(k, sg, c);
         if (t < 64) {  // inclusive prefix of the chunk's log decays (warps 2, 3)
-          float x = token_lambda(p.decay_kind, p.decay, h, bhL, tok0[sg] + c * CH + t, p.L);
+          float x = token_log_decay(p.decay_kind, raw_next);
+          if (k + 1 < nk) raw_next = decay_raw(k + 1);
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
             float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -791,20 +912,21 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (t == 0) split[s] = sp ? 1u : 0u;
         if (sp) named_bar_sync(BAR_PREP, kPrepThreads);  // factors visible to the V pass
       }
-      if constexpr (PHI)  // Q and K tiles are adjacent in the stage: one pass
+      if constexpr (PHI) {  // Q and K tiles are adjacent in the stage: one pass
         tile_pass<DK, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
-      if (DECAY && sp) {
-        const float *vf = vfac + s * 64;
-        tile_pass<64, 1, false, true>(qt + 2 * SM::QK_TILE, [vf](int, int r) { return vf[r]; }, t,
-                                      kPrepThreads);
+        fence_proxy_async_smem();
       }
-      if (PHI || sp) fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
-      if (t == 0) {
-        mbar_arrive(&xdone[s]);
-        if (sp) mbar_arrive(&qk_ready[s]);
-      }
+      if (t == 0) mbar_arrive(&xdone[s]);  // QK^T may start; V is scaled meanwhile
       LA_TRACE_EVENT(trace_on && t == 0, t0, 2, k);
+      if (DECAY && sp) {  // the MMAs that read V wait for qk_ready
+        const float *vf = vfac + s * 64;
+        tile_pass<DK, 1, false, true>(qt + 2 * SM::TILE, [vf](int, int r) { return vf[r]; }, t,
+                                      kPrepThreads);
+        fence_proxy_async_smem();
+        named_bar_sync(BAR_PREP, kPrepThreads);
+        if (t == 0) mbar_arrive(&qk_ready[s]);
+      }
       return true;
     };
     // Per-element decay form: once QK^T of the chunk has consumed the
@@ -814,11 +936,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       const int s = k % NST, b = k & 1;
       if (!gwait(&p_full[b], (k >> 1) & 1, 8)) return false;
       LA_TRACE_EVENT(trace_on && t == 0, t0, 13, k);
-      const float *lm = lam + s * 64;
-      const float A = lm[63];
-      tile_pass<DK, 2, false, true>(
-          smem + s * SM::STAGE,
-          [lm, A](int kt, int r) { return __expf(kt == 0 ? lm[r] : A - lm[r]); }, t, kPrepThreads);
+      rescale_qk_rows<DK>(smem + s * SM::STAGE, lam + s * 64, t, kPrepThreads);
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&qk_ready[s]);
@@ -847,38 +965,35 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         return false;
       tc_fence_after();
       LA_TRACE_EVENT(trace_on && t == 0, t0, 3, k);
-      __syncwarp();
-      uint32_t r[2][32];
-      tmem_ld32(tmem + lane_off + SM::T_P + 64 * b, r[0]);
-      tmem_ld32(tmem + lane_off + SM::T_P + 64 * b + 32, r[1]);
-      tmem_ld_wait();
-      if (row >= 0) {
-        unsigned char *ps = smem + SM::OFF_P + 8192 * b;
-        const float *lm = lam + s * 64;
-        // Causal mask; per-element decay only for chunks outside the split
-        // form (whose row factor the O epilogue applies instead).
-        const bool sp = DECAY && split[s];
-        const float li = DECAY ? lm[row] : 0.f;
-        if (DECAY) of_cur = sp ? ofac[s * 64 + row] : 1.f;
+      unsigned char *ps = smem + SM::OFF_P + 8192 * b;
+      // Causal mask.  Split-form chunks need nothing more here (their row
+      // factor is applied by the O epilogue); others take their decay per
+      // element, out of line.
+      const bool sp = !DECAY || split[s];
+      if (DECAY && row >= 0) of_cur = sp ? ofac[s * 64 + row] : 1.f;
+      if (!sp) {
+        p_tile_strong_decay(tmem + lane_off + SM::T_P + 64 * b, row, lam + s * 64, ps);
+      } else {
+        __syncwarp();
+        uint32_t r[2][32];
+        tmem_ld32(tmem + lane_off + SM::T_P + 64 * b, r[0]);
+        tmem_ld32(tmem + lane_off + SM::T_P + 64 * b + 32, r[1]);
+        tmem_ld_wait();
+        if (row >= 0) {
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
+          for (int hlf = 0; hlf < 2; ++hlf) {
 #pragma unroll
-          for (int q16 = 0; q16 < 2; ++q16) {
-            uint32_t pk[8];
+            for (int q16 = 0; q16 < 2; ++q16) {
+              uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              const int j0 = hlf * 32 + q16 * 16 + j;
-              float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
-              float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
-              if constexpr (DECAY) {
-                if (!sp) {
-                  v0 *= __expf(fminf(li - lm[j0], 0.f));
-                  v1 *= __expf(fminf(li - lm[j0 + 1], 0.f));
-                }
+              for (int j = 0; j < 16; j += 2) {
+                const int j0 = hlf * 32 + q16 * 16 + j;
+                const float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
+                const float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
+                pk[j >> 1] = pack_bf16(v0, v1);
               }
-              pk[j >> 1] = pack_bf16(v0, v1);
+              st_row16(ps, 8192, row, hlf * 32 + q16 * 16, pk);
             }
-            st_row16(ps, 8192, row, hlf * 32 + q16 * 16, pk);
           }
         }
       }
@@ -897,29 +1012,32 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (t == 0) tma_store_wait_read<1>();  // the store that used this buffer is done
       __syncwarp();
       named_bar_sync(BAR_WG2, 128);
-      unsigned char *o_sm = smem + SM::OFF_O + b * 8192;
-      __syncwarp();  // tcgen05.ld is warp-collective: reconverge before it
-      uint32_t r[2][32];
-      tmem_ld32(tmem + lane_off + SM::T_O + 64 * b, r[0]);
-      tmem_ld32(tmem + lane_off + SM::T_O + 64 * b + 32, r[1]);
-      tmem_ld_wait();
-      if (row >= 0) {
+      unsigned char *o_sm = smem + SM::OFF_O + b * SM::TILE;
+#pragma unroll 1
+      for (int col = 0; col < DK; col += 64) {
+        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row branch
+        uint32_t r[2][32];
+        tmem_ld32(tmem + lane_off + SM::T_O + DK * b + col, r[0]);
+        tmem_ld32(tmem + lane_off + SM::T_O + DK * b + col + 32, r[1]);
+        tmem_ld_wait();
+        if (row >= 0) {
 #pragma unroll
-        for (int hlf = 0; hlf < 2; ++hlf) {
+          for (int hlf = 0; hlf < 2; ++hlf) {
 #pragma unroll
-          for (int q16 = 0; q16 < 2; ++q16) {
-            uint32_t pk[8];
+            for (int q16 = 0; q16 < 2; ++q16) {
+              uint32_t pk[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float x0 = __uint_as_float(r[hlf][q16 * 16 + 2 * j]);
-              float x1 = __uint_as_float(r[hlf][q16 * 16 + 2 * j + 1]);
-              if (DECAY) {
-                x0 *= f;
-                x1 *= f;
+              for (int j = 0; j < 8; ++j) {
+                float x0 = __uint_as_float(r[hlf][q16 * 16 + 2 * j]);
+                float x1 = __uint_as_float(r[hlf][q16 * 16 + 2 * j + 1]);
+                if (DECAY) {
+                  x0 *= f;
+                  x1 *= f;
+                }
+                pk[j] = pack_bf16(x0, x1);
               }
-              pk[j] = pack_bf16(x0, x1);
+              st_row16(o_sm, BOX_BYTES, row, col + hlf * 32 + q16 * 16, pk);
             }
-            st_row16(o_sm, BOX_BYTES, row, hlf * 32 + q16 * 16, pk);
           }
         }
       }
@@ -931,8 +1049,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         int sg, c;
         st.at(k, sg, c);
         const int tok = tok0[sg] + c * CH;
-        if (LA_CHK(dv0 + 64 <= D && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 3))
-          tma_store_3d(&tmO, o_sm, dv0, tok, bh);
+        for (int bb = 0; bb < DK / BOX; ++bb)
+          if (LA_CHK(bb * BOX + BOX <= DK && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 3))
+            tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok, bh);
         tma_store_commit();
         LA_TRACE_EVENT(trace_on, t0, 12, k);
       }
@@ -953,9 +1072,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int quarter = warp & 3;
     const int srow = acc_row<DK>(quarter, lane);    // state row (d_k index)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // 32 columns of state row srow: r * sm_scale as bf16 into a stream's S
-    // buffer, and optionally r * tm_scale back into the stream's TMEM state.
-    auto put32 = [&](int sg, int col, uint32_t (&r)[32], float sm_scale, float tm_scale,
+    // 32 columns of state row srow: r * sm_scale as bf16 into a chain's S
+    // buffer, and optionally r * tm_scale back into the chain's TMEM state.
+    auto put32 = [&](int ch, int col, uint32_t (&r)[32], float sm_scale, float tm_scale,
                      bool to_tmem) {
       if (srow >= 0) {
 #pragma unroll
@@ -965,17 +1084,17 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           for (int j = 0; j < 8; ++j)
             pk[j] = pack_bf16(__uint_as_float(r[q16 * 16 + 2 * j]) * sm_scale,
                               __uint_as_float(r[q16 * 16 + 2 * j + 1]) * sm_scale);
-          st_row16(smem + SM::OFF_S + sg * SM::S_BYTES, SM::S_BYTES, srow, col + q16 * 16, pk);
+          st_row16(smem + SM::OFF_S + ch * SM::S_BYTES, SM::S_BLOCK, srow, col + q16 * 16, pk);
         }
       }
       if (to_tmem) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * tm_scale);
         __syncwarp();
-        tmem_st32(tmem + lane_off + SM::T_S + 64 * sg + col, r);
+        tmem_st32(tmem + lane_off + SM::T_S + CW * ch + col, r);
       }
     };
-    // Scales of a stream's state at one of its chunks (decay kernels), as
+    // Scales of a chain's state at one of its chunks (decay kernels), as
     // natural logarithms:
     //   smem copy  S_c * e^{m}   (m = r = A/2 in the split form, else 0),
     //   TMEM       S_c * e^{t}   (t = r in the split form, else A),
@@ -991,28 +1110,29 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         tt = A;
       }
     };
-    float g_prev[2] = {0.f, 0.f};  // g of each stream's chunk whose MMA4 is next awaited
+    float g_prev[2] = {0.f, 0.f};  // per chain: g of its chunk whose MMA4 is next awaited
     bool ok = true;
-    // Initial states, in the order the streams' first chunks come (k = 0, 1).
-    for (int sg = 0; ok && sg < 2; ++sg) {
+    // Initial states, chain by chain (a chain's first chunk is virtual 0 or 1).
+    for (int ch = 0; ok && ch < NCHAIN; ++ch) {
+      const int sg = ch_seg(ch);
       if (st.nc[sg] == 0) continue;
-      const int k = st.index(sg, 0);
+      const int k = PAIRS ? st.index(sg, 0) : 0;
       float m0 = 0.f, t0s = 0.f;
       if constexpr (DECAY) {
         ok = wait_wg(&xdone[k % NST], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 12, BAR_WG3);
         if (!ok) break;
         float g0;
         log_scales(k, m0, t0s, g0);
-        g_prev[sg] = g0;
+        g_prev[ch] = g0;
       }
-      if (has_init[sg]) {
+      if (S_seg[sg] != nullptr) {
         const float sm0 = __expf(m0), tm0 = __expf(t0s);
 #pragma unroll 1
-        for (int col = 0; col < 64; col += 32) {
+        for (int col = 0; col < CW; col += 32) {
           uint32_t r[32];
           if (srow >= 0) {
-            const float4 *src =
-                reinterpret_cast<const float4 *>(S_in[sg] + (size_t)srow * D + dv0 + col);
+            const float4 *src = reinterpret_cast<const float4 *>(S_seg[sg] + (size_t)srow * D +
+                                                                 ch_col(ch) + col);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               float4 f = src[j];
@@ -1025,66 +1145,76 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = 0u;
           }
-          put32(sg, col, r, sm0, tm0, true);
+          put32(ch, col, r, sm0, tm0, true);
         }
         tmem_st_wait();
       }
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(BAR_WG3, 128);
-      if (t == 0) mbar_arrive(&s_ready[sg]);
+      if (t == 0) mbar_arrive(&s_ready[ch]);
     }
     for (int k = 0; ok && k < nk; ++k) {
       int sg, c;
       st.at(k, sg, c);
-      if (!(ok = wait_wg(&s_done[sg], c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13, BAR_WG3))) break;
-      tc_fence_after();
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 10, k);
-      if (c + 1 < st.nc[sg]) {
-        // TMEM holds S_c+1 * e^{-g_c}.  Copy S_c+1 * e^{m_c+1} to bf16 for
-        // the next chunk's Q S, and leave S_c+1 * e^{t_c+1} in TMEM for its
-        // state update.  Each scale is one exponential of a sum >= -80.
-        const int kn = st.index(sg, c + 1);
-        float sm = 1.f, tm = 1.f;
-        if constexpr (DECAY) {
-          if (!(ok = wait_wg(&xdone[kn % NST], (kn / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
-                             BAR_WG3)))
-            break;
-          float m1, t1, g1;
-          log_scales(kn, m1, t1, g1);
-          sm = __expf(g_prev[sg] + m1);
-          tm = __expf(g_prev[sg] + t1);
-          g_prev[sg] = g1;
-        }
-        __syncwarp();
-        uint32_t r[2][32];
-        tmem_ld32(tmem + lane_off + SM::T_S + 64 * sg, r[0]);
-        tmem_ld32(tmem + lane_off + SM::T_S + 64 * sg + 32, r[1]);
-        tmem_ld_wait();
-        put32(sg, 0, r[0], sm, tm, DECAY);
-        put32(sg, 32, r[1], sm, tm, DECAY);
-        if (DECAY) tmem_st_wait();
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(BAR_WG3, 128);
-        if (t == 0) mbar_arrive(&s_ready[sg]);
-        LA_TRACE_EVENT(trace_on && t == 0, t0, 11, k);
-      } else if (last_seg[sg] && p.S_final) {
-        const float fin = DECAY ? __expf(g_prev[sg]) : 1.f;
+      const bool more = c + 1 < st.nc[sg];
+      const int kn = PAIRS ? (more ? st.index(sg, c + 1) : 0) : k + 1;
+      float lm1 = 0.f, lt1 = 0.f, lg1 = 0.f;  // log scales of the chain's next chunk
+      if (DECAY && more) {
+        if (!(ok = wait_wg(&xdone[kn % NST], (kn / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 14,
+                           BAR_WG3)))
+          break;
+        log_scales(kn, lm1, lt1, lg1);
+      }
+      for (int ch = PAIRS ? sg : 0; ok && ch <= (PAIRS ? sg : NCHAIN - 1); ++ch) {
+        if (!(ok = wait_wg(&s_done[ch], c & 1, ctl, p.err, KID_PREFILL_TC_OUT, 13, BAR_WG3)))
+          break;
+        tc_fence_after();
+        LA_TRACE_EVENT(trace_on && t == 0, t0, 10, k);
+        if (more) {
+          // TMEM holds S_c+1 * e^{-g_c}.  Copy S_c+1 * e^{m_c+1} to bf16 for
+          // the next chunk's Q S, and leave S_c+1 * e^{t_c+1} in TMEM for its
+          // state update.  Each scale is one exponential of a sum >= -80.
+          float sm = 1.f, tm = 1.f;
+          if constexpr (DECAY) {
+            sm = __expf(g_prev[ch] + lm1);
+            tm = __expf(g_prev[ch] + lt1);
+            g_prev[ch] = lg1;
+          }
 #pragma unroll 1
-        for (int col = 0; col < 64; col += 32) {
-          __syncwarp();
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + SM::T_S + 64 * sg + col, r);
-          tmem_ld_wait();
-          if (srow >= 0) {
-            float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D +
-                                                     dv0 + col);
+          for (int col = 0; col < CW; col += 64) {
+            __syncwarp();
+            uint32_t r[2][32];
+            tmem_ld32(tmem + lane_off + SM::T_S + CW * ch + col, r[0]);
+            tmem_ld32(tmem + lane_off + SM::T_S + CW * ch + col + 32, r[1]);
+            tmem_ld_wait();
+            put32(ch, col, r[0], sm, tm, DECAY);
+            put32(ch, col + 32, r[1], sm, tm, DECAY);
+          }
+          if (DECAY) tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          named_bar_sync(BAR_WG3, 128);
+          if (t == 0) mbar_arrive(&s_ready[ch]);
+          LA_TRACE_EVENT(trace_on && t == 0, t0, 11, k);
+        } else if (seg[sg] == p.n_seg - 1 && p.S_final) {
+          const float fin = DECAY ? __expf(g_prev[ch]) : 1.f;
+#pragma unroll 1
+          for (int col = 0; col < CW; col += 32) {
+            __syncwarp();
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + SM::T_S + CW * ch + col, r);
+            tmem_ld_wait();
+            if (srow >= 0) {
+              float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D +
+                                                       ch_col(ch) + col);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(__uint_as_float(r[4 * j]) * fin, __uint_as_float(r[4 * j + 1]) * fin,
-                                   __uint_as_float(r[4 * j + 2]) * fin,
-                                   __uint_as_float(r[4 * j + 3]) * fin);
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(r[4 * j]) * fin,
+                                     __uint_as_float(r[4 * j + 1]) * fin,
+                                     __uint_as_float(r[4 * j + 2]) * fin,
+                                     __uint_as_float(r[4 * j + 3]) * fin);
+            }
           }
         }
       }
@@ -1115,19 +1245,20 @@ int sm_count() {
   return n;
 }
 
-// Segment count.  The output kernel runs ceil(NS/2) x BH x (D/64) CTAs, each
-// over the chunks of two segments; the segment-state kernel (NS > 1) runs
-// (NS-1) x BH CTAs and reads K and V of all but the last segment once more;
-// the scan moves the segment states.  The estimate of each kernel is the
-// larger of its wave time -- waves x (fixed CTA cost + chunk steps x step
-// time) -- and its bytes over the HBM bandwidth; step times and fixed costs
-// are measured ones for these kernels on GB300 (microseconds).  G <= 32
-// bounds the segment-state kernel's suffix table.
+// Segment count.  The output kernel runs ceil(NS/2) x BH CTAs of two
+// segments each (d = 64) or NS x BH CTAs of one (d = 128); the segment-state
+// kernel (NS > 1) runs (NS-1) x BH CTAs and reads K and V of all but the last
+// segment once more; the scan moves the segment states.  The estimate of each
+// kernel is the larger of its wave time -- waves x (fixed CTA cost + chunk
+// steps x step time) -- and its bytes over the HBM bandwidth; step times and
+// fixed costs are measured ones for these kernels on GB300 (microseconds).
+// G <= 32 bounds the segment-state kernel's suffix table.
 Plan make_plan(int B, int H, int L, int D) {
   const int nc = (L + CH - 1) / CH;
-  const double bh = (double)B * H, sms = sm_count(), slices = D / 64;
-  const double t_out = D == 128 ? 0.8 : 0.7, t_state = D == 128 ? 0.7 : 0.4;
-  const double fill_out = 3.0, fill_state = 2.0, t_launch = 3.0, bw = 6.5e-3;  // bytes/us / 1e9
+  const bool halves = D == 128;  // one segment per output CTA
+  const double bh = (double)B * H, sms = sm_count();
+  const double t_out = halves ? 1.4 : 1.3, t_state = halves ? 0.7 : 0.4;
+  const double fill_out = 3.0, fill_state = 2.0, t_launch = 3.0, bw = 6.5e3;  // bytes per us / 1e3
   const double tile = 64.0 * D * 2, state = (double)D * D * 4;
   Plan best{nc, nc, 1};
   double best_t = 1e300;
@@ -1135,15 +1266,15 @@ Plan make_plan(int B, int H, int L, int D) {
     const int g = (nc + ns - 1) / ns;
     const int n_seg = (nc + g - 1) / g;
     if (g > kMaxSegChunks || n_seg != ns) continue;
-    const double ctas = std::ceil(n_seg / 2.0) * bh * slices;
-    const double steps = n_seg > 1 ? 2.0 * g : (double)g;
+    const double ctas = (halves ? (double)n_seg : std::ceil(n_seg / 2.0)) * bh;
+    const double steps = (halves || n_seg == 1) ? (double)g : 2.0 * g;
     const double out_bytes = bh * (nc * 4.0 * tile + (n_seg > 1 ? n_seg * state : 0.0));
-    double t = std::max(std::ceil(ctas / sms) * (fill_out + steps * t_out), out_bytes / bw * 1e-9);
+    double t = std::max(std::ceil(ctas / sms) * (fill_out + steps * t_out), out_bytes / bw * 1e-3);
     if (n_seg > 1) {
       const double sctas = (n_seg - 1) * bh;
       const double st_bytes = bh * ((n_seg - 1) * (g * 2.0 * tile + state));
-      t += std::max(std::ceil(sctas / sms) * (fill_state + g * t_state), st_bytes / bw * 1e-9);
-      t += 2 * t_launch + bh * n_seg * 2.0 * state / bw * 1e-9;
+      t += std::max(std::ceil(sctas / sms) * (fill_state + g * t_state), st_bytes / bw * 1e-3);
+      t += 2 * t_launch + bh * n_seg * 2.0 * state / bw * 1e-3;
     }
     if (t < best_t) {
       best_t = t;
@@ -1239,7 +1370,8 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   static int smem_set_out[64];
   e = set_smem_once(ko, OS::BYTES, smem_set_out);
   if (e != cudaSuccess) return e;
-  ko<<<dim3((pl.n_seg + 1) / 2, BH, D / 64), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  const int out_x = OS::PAIRS ? (pl.n_seg + 1) / 2 : pl.n_seg;
+  ko<<<dim3(out_x, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
   if ((e = cudaGetLastError()) != cudaSuccess && why)
     *why = "la_chunk_fwd: chunk-output kernel launch";
 #ifdef LA_CHECKED

@@ -107,14 +107,17 @@ def test_multi_chunk_segments_match_oracle(case):
 
 # Sequences the launcher cuts into segments: a segment-state pass and a scan
 # give each segment its incoming state, and each output CTA interleaves two
-# segments.  The shapes cover one-chunk segments, an odd segment count (the
-# last CTA has one segment), a short last segment, and both head sizes.
+# segments (d = 64).  The shapes cover one-chunk segments, odd segment counts
+# (the last d = 64 CTA has one segment), a short last segment, and both head
+# sizes.
 SEGMENTED = [
     # (B, H, L, d, phi, decay, s0, sampled pairs or None for all)
     (1, 2, 1000, 64, "elu1", "none", None, None),
     (1, 2, 2100, 128, "identity", "head", 0.1, None),
     (2, 4, 3000, 64, "identity", "logit", 0.1, None),
     (1, 2, 6000, 64, "elu1", "head", None, None),
+    (2, 4, 3100, 64, "elu1", "head", None, None),
+    (2, 4, 2800, 64, "identity", "logit", 0.1, None),
     (2, 4, 1500, 128, "elu1", "none", 0.1, None),
     (2, 4, 6000, 128, "identity", "logit", 0.1, [(0, 0), (1, 3), (0, 2)]),
 ]
