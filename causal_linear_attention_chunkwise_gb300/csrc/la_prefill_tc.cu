@@ -276,7 +276,8 @@ struct StateSmem {
   // barriers is waited on, in order, by that one group.  (With an odd count a
   // group could wait on a stage whose previous phase belongs to the other
   // group and has not completed yet; the parity test would then pass early.)
-  static constexpr int NST = 4;
+  // Two stages for D = 128 keep the block small enough for two per SM.
+  static constexpr int NST = D == 128 ? 2 : 4;
   static_assert(NST % 2 == 0, "stages must alternate between the two transform groups");
   static constexpr uint32_t TILE = 64 * D * 2;
   static constexpr uint32_t STAGE = 2 * TILE;
@@ -292,7 +293,7 @@ constexpr int kThreadsState = 384;  // warps 0..11: TMA, MMA, -, -, XG0 (4..7), 
 constexpr uint32_t BAR_XG0 = 1, BAR_XG1 = 2, BAR_XG = 3;
 
 template <int D, bool PHI, bool DECAY>
-__global__ void __launch_bounds__(kThreadsState, 1)
+__global__ void __launch_bounds__(kThreadsState, 2)  // two CTAs per SM
 segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
   using SM = StateSmem<D>;
@@ -1247,8 +1248,8 @@ int sm_count() {
 
 // Segment count.  The output kernel runs ceil(NS/2) x BH CTAs of two
 // segments each (d = 64) or NS x BH CTAs of one (d = 128); the segment-state
-// kernel (NS > 1) runs (NS-1) x BH CTAs and reads K and V of all but the last
-// segment once more; the scan moves the segment states.  The estimate of each
+// kernel (NS > 1) runs (NS-1) x BH CTAs, two per SM, and reads K and V of all
+// but the last segment once more; the scan moves the segment states.  The estimate of each
 // kernel is the larger of its wave time -- waves x (fixed CTA cost + chunk
 // steps x step time) -- and its bytes over the HBM bandwidth; step times and
 // fixed costs are measured ones for these kernels on GB300 (microseconds).
@@ -1257,7 +1258,7 @@ Plan make_plan(int B, int H, int L, int D) {
   const int nc = (L + CH - 1) / CH;
   const bool halves = D == 128;  // one segment per output CTA
   const double bh = (double)B * H, sms = sm_count();
-  const double t_out = halves ? 1.4 : 1.3, t_state = halves ? 0.7 : 0.4;
+  const double t_out = halves ? 3.5 : 1.5, t_state = halves ? 0.7 : 0.4;
   const double fill_out = 3.0, fill_state = 2.0, t_launch = 3.0, bw = 6.5e3;  // bytes per us / 1e3
   const double tile = 64.0 * D * 2, state = (double)D * D * 4;
   Plan best{nc, nc, 1};
@@ -1273,7 +1274,8 @@ Plan make_plan(int B, int H, int L, int D) {
     if (n_seg > 1) {
       const double sctas = (n_seg - 1) * bh;
       const double st_bytes = bh * ((n_seg - 1) * (g * 2.0 * tile + state));
-      t += std::max(std::ceil(sctas / sms) * (fill_state + g * t_state), st_bytes / bw * 1e-3);
+      // (a last partial wave at two CTAs per SM runs its CTAs faster: fractional)
+      t += std::max(sctas / (2 * sms) * (fill_state + g * t_state), st_bytes / bw * 1e-3);
       t += 2 * t_launch + bh * n_seg * 2.0 * state / bw * 1e-3;
     }
     if (t < best_t) {
