@@ -505,15 +505,19 @@ struct OutSmem {
   static constexpr bool PAIRS = DK == 64;                       // two segments per CTA
   static constexpr int NCHAIN = PAIRS ? 2 : LA_D128_CHAINS;     // state chains
   static constexpr int CW = PAIRS ? 64 : DK / NCHAIN;           // state columns per chain
+  // d = 128 keeps the output and the state transposed in TMEM (see the kernel):
+  // its bf16 state copy lives in TMEM, not in shared memory.
+  static constexpr bool TRANS = DK == 128 && NCHAIN == 1;
   static constexpr int NST = PAIRS ? 4 : 3;
   static constexpr uint32_t TILE = 64 * DK * 2;            // Q, K, V or O tile of one chunk
   static constexpr uint32_t STAGE = 3 * TILE;              // Q | K | V
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
   static constexpr uint32_t S_BLOCK = DK * 128;            // [DK][64] bf16, MN-major
-  static constexpr uint32_t S_BYTES = S_BLOCK * (CW / 64); // one chain's bf16 state
+  static constexpr uint32_t S_BYTES = TRANS ? 0 : S_BLOCK * (CW / 64);  // one chain's bf16 state
   static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;
   static constexpr uint32_t OFF_O = OFF_S + NCHAIN * S_BYTES;  // 2 x O tile store staging
-  static constexpr uint32_t OFF_LAM = OFF_O + 2 * TILE;    // [NST][64] inclusive prefix
+  static constexpr uint32_t OFF_OFR = OFF_O + 2 * TILE;    // [2][64] output token factors (TRANS)
+  static constexpr uint32_t OFF_LAM = OFF_OFR + 2 * 64 * 4;  // [NST][64] inclusive prefix
   static constexpr uint32_t OFF_VF = OFF_LAM + NST * 64 * 4;   // [NST][64] exp(A/2 - Lam_j)
   static constexpr uint32_t OFF_OF = OFF_VF + NST * 64 * 4;    // [NST][64] exp(Lam_i - A/2)
   static constexpr uint32_t OFF_SPLIT = OFF_OF + NST * 64 * 4; // [NST] split decay used
@@ -527,8 +531,11 @@ struct OutSmem {
                 "swizzled tiles need 1024-byte alignment");
   static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
   // TMEM columns: P and O by virtual chunk parity, S by chain (CW columns each).
-  static constexpr uint32_t T_P = 0, T_O = 128, T_S = 128 + 2 * DK, T_COLS = 512;
-  static_assert(T_S + NCHAIN * CW <= T_COLS, "TMEM budget");
+  // TRANS: O^T buffers of 64 columns (lanes = value columns), S^T fp32 (128
+  // columns), and two bf16 copies of S^T as MMA A operands (64 columns each).
+  static constexpr uint32_t T_P = 0, T_O = 128, T_OW = TRANS ? 64 : DK;
+  static constexpr uint32_t T_S = 128 + 2 * T_OW, T_SB = T_S + 128, T_COLS = 512;
+  static_assert(T_S + NCHAIN * CW <= T_COLS && (!TRANS || T_SB + 128 <= T_COLS), "TMEM budget");
 };
 
 // Warps: 0 TMA, 1 MMA, 2-7 PREP (192 threads), 8-11 WG2, 12-15 WG3.
@@ -747,6 +754,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       constexpr uint32_t id_pv = idesc_bf16_f32(64, DK, false, true);
       constexpr uint32_t id_qs = idesc_bf16_f32(64, CW, false, true);
       constexpr uint32_t id_kv = idesc_bf16_f32(DK, CW, true, true);
+      // Transposed forms (TRANS): S^T += V^T K, O^T = S^T Q^T (A in TMEM),
+      // O^T += V^T P^T.  M = 128 value columns in every one.
+      constexpr uint32_t id_kvT = idesc_bf16_f32(DK, DK, true, true);
+      constexpr uint32_t id_qsT = idesc_bf16_f32(DK, 64, false, false);
+      constexpr uint32_t id_pvT = idesc_bf16_f32(DK, 64, true, false);
       // Operand descriptors: the base descriptor of each layout at the start
       // of shared memory, plus (byte offset >> 4) in its 14-bit address field
       // (shared memory ends below 256 KB, so the field never carries).
@@ -784,8 +796,28 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             tc_fence_after();
             LA_TRACE_EVENT(trace_on && cc == 0, t0, 8, kc);
             const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
-            const uint32_t o_t = tmem + SM::T_O + DK * b;
+            const uint32_t o_t = tmem + SM::T_O + SM::T_OW * b;
             const bool inter = S_seg[sg] != nullptr || c > 0;
+            if constexpr (SM::TRANS) {
+              // The chain is S^T += V^T K alone; O^T = S^T Q^T follows it off the
+              // chain (its bf16 S^T copy is double-buffered in TMEM).
+#pragma unroll
+              for (int kk = 0; kk < CH / 16; ++kk)
+                mma_bf16(tmem + SM::T_S, at(dMN, vo + 2048 * kk), at(dMN, ko + 2048 * kk), id_kvT,
+                         (inter || kk > 0) ? 1u : 0u);
+              mma_commit(&s_done[0]);
+              if (inter) {
+                const uint32_t sb = tmem + SM::T_SB + 64 * (c & 1);
+#pragma unroll
+                for (int kk = 0; kk < DK / 16; ++kk) {
+                  const uint32_t off = qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+                  mma_bf16_ta(o_t, sb + 8 * kk, at(dKM, off), id_qsT, kk > 0);
+                }
+              }
+              ++kc;
+              LA_TRACE_EVENT(trace_on, t0, 9, kc - 1);
+              did = true;
+            } else {
             const uint32_t vb = vo + (PAIRS ? 0u : (uint32_t)(ch * (CW / 64)) * BOX_BYTES);
 #pragma unroll
             for (int kk = 0; kk < CH / 16; ++kk)   // chain state: S (TMEM) += K^T V
@@ -806,6 +838,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
               LA_TRACE_EVENT(trace_on, t0, 9, kc - 1);
             }
             did = true;
+            }
           }
         }
         if (km < kc) {  // ---- P V
@@ -818,9 +851,14 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * b;
             const bool inter = S_seg[sg] != nullptr || c > 0;
 #pragma unroll
-            for (int kk = 0; kk < CH / 16; ++kk)   // O += P V
-              mma_bf16(tmem + SM::T_O + DK * b, at(dKM, po + 32 * kk), at(dMN, vo + 2048 * kk),
-                       id_pv, (inter || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < CH / 16; ++kk) {  // O += P V   (TRANS: O^T += V^T P^T)
+              if constexpr (SM::TRANS)
+                mma_bf16(tmem + SM::T_O + SM::T_OW * b, at(dMN, vo + 2048 * kk), at(dKM, po + 32 * kk),
+                         id_pvT, (inter || kk > 0) ? 1u : 0u);
+              else
+                mma_bf16(tmem + SM::T_O + SM::T_OW * b, at(dKM, po + 32 * kk), at(dMN, vo + 2048 * kk),
+                         id_pv, (inter || kk > 0) ? 1u : 0u);
+            }
             mma_commit(&o_full[b]);
             mma_commit(&empty[s]);
             LA_TRACE_EVENT(trace_on, t0, 6, km);
@@ -956,6 +994,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int t = tid - WG2 * 32;
     const int quarter = warp & 3;
     const int row = acc_row<64>(quarter, lane);   // row within the chunk
+    float *ofr = reinterpret_cast<float *>(smem + SM::OFF_OFR);  // [2][64] (TRANS)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     float of_cur = 1.f;  // output row factor of the chunk whose P was just formed
     auto p_epilogue = [&](int k) -> bool {
@@ -971,6 +1010,8 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       // factor is applied by the O epilogue); others take their decay per
       // element, out of line.
       const bool sp = !DECAY || split[s];
+      if (SM::TRANS && DECAY && t < 64)  // the O epilogue needs every token's factor
+        ofr[b * 64 + t] = sp ? ofac[s * 64 + t] : 1.f;
       if (DECAY && row >= 0) of_cur = sp ? ofac[s * 64 + row] : 1.f;
       if (!sp) {
         p_tile_strong_decay(tmem + lane_off + SM::T_P + 64 * b, row, lam + s * 64, ps);
@@ -1014,6 +1055,46 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       __syncwarp();
       named_bar_sync(BAR_WG2, 128);
       unsigned char *o_sm = smem + SM::OFF_O + b * SM::TILE;
+      if constexpr (SM::TRANS) {
+        // O^T: TMEM lanes are value columns, columns the chunk's 64 tokens.
+        // Per 16 lanes (16x256b loads), each 8x8 block (8 value columns x 8
+        // tokens) is scaled by its tokens' factors, packed to bf16 and stored
+        // transposed (stmatrix .trans): one 16-byte chunk of a token's row of
+        // the swizzled staging tile per stored row.
+        const int tq = lane & 3;
+        float2 fq[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          fq[q] = DECAY ? *reinterpret_cast<const float2 *>(ofr + b * 64 + 8 * q + 2 * tq)
+                        : make_float2(1.f, 1.f);
+        const uint32_t o_base = smem_u32(o_sm);
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          __syncwarp();
+          uint32_t r[32];
+          tmem_ld_16x256b_x8(tmem + ((uint32_t)(quarter * 32 + 16 * g) << 16) + SM::T_O +
+                                 SM::T_OW * b,
+                             r);
+          tmem_ld_wait();
+          uint32_t pa[8], pb[8];  // value rows 0-7 and 8-15 of the 16, per token chunk
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            pa[q] = pack_bf16(__uint_as_float(r[4 * q]) * fq[q].x,
+                              __uint_as_float(r[4 * q + 1]) * fq[q].y);
+            pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]) * fq[q].x,
+                              __uint_as_float(r[4 * q + 3]) * fq[q].y);
+          }
+#pragma unroll
+          for (int qq = 0; qq < 8; qq += 2) {
+            // matrices (qq, rows 0-7), (qq, 8-15), (qq+1, 0-7), (qq+1, 8-15)
+            const int mi = lane >> 3, tok = 8 * (qq + (mi >> 1)) + (lane & 7);
+            const int dv0 = quarter * 32 + 16 * g + 8 * (mi & 1);
+            const uint32_t addr = o_base + (dv0 >> 6) * BOX_BYTES + tok * 128 +
+                                  ((((dv0 & 63) >> 3) ^ (tok & 7)) << 4);
+            stmatrix_x4_trans(addr, pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int col = 0; col < DK; col += 64) {
         __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row branch
@@ -1041,6 +1122,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             }
           }
         }
+      }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1095,6 +1177,24 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         tmem_st32(tmem + lane_off + SM::T_S + CW * ch + col, r);
       }
     };
+    // TRANS: this thread's TMEM lane is value column dv = t of S^T.  32 state
+    // rows (d_k = 32 cb ..) of that column: r * sm packed to bf16 pairs into
+    // A-operand copy `buf` (column = pair of d_k), and r * tm back into the
+    // fp32 S^T when to_fp32.
+    auto put_trans = [&](int cb, int buf, uint32_t (&r)[32], float sm, float tm, bool to_fp32) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        pk[j] = pack_bf16(__uint_as_float(r[2 * j]) * sm, __uint_as_float(r[2 * j + 1]) * sm);
+      __syncwarp();
+      tmem_st16(tmem + lane_off + SM::T_SB + 64 * buf + 16 * cb, pk);
+      if (to_fp32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * tm);
+        __syncwarp();
+        tmem_st32(tmem + lane_off + SM::T_S + 32 * cb, r);
+      }
+    };
     // Scales of a chain's state at one of its chunks (decay kernels), as
     // natural logarithms:
     //   smem copy  S_c * e^{m}   (m = r = A/2 in the split form, else 0),
@@ -1126,7 +1226,18 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         log_scales(k, m0, t0s, g0);
         g_prev[ch] = g0;
       }
-      if (S_seg[sg] != nullptr) {
+      if (SM::TRANS && S_seg[sg] != nullptr) {
+        const float sm0 = __expf(m0), tm0 = __expf(t0s);
+#pragma unroll 1
+        for (int cb = 0; cb < DK / 32; ++cb) {
+          uint32_t r[32];
+          const float *src = S_seg[sg] + (size_t)(32 * cb) * D + t;  // column t, rows 32 cb ..
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(src[(size_t)j * D]);
+          put_trans(cb, 0, r, sm0, tm0, true);
+        }
+        tmem_st_wait();
+      } else if (S_seg[sg] != nullptr) {
         const float sm0 = __expf(m0), tm0 = __expf(t0s);
 #pragma unroll 1
         for (int col = 0; col < CW; col += 32) {
@@ -1182,6 +1293,20 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             tm = __expf(g_prev[ch] + lt1);
             g_prev[ch] = lg1;
           }
+          if constexpr (SM::TRANS) {
+            // TMEM to TMEM: the copy for chunk c+1 goes to buffer (c+1) & 1;
+            // the Q S of chunk c-1 that read it finished before this chunk's
+            // state MMA (s_done tracks every earlier MMA).
+#pragma unroll 1
+            for (int cb = 0; cb < DK / 32; ++cb) {
+              __syncwarp();
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_off + SM::T_S + 32 * cb, r);
+              tmem_ld_wait();
+              put_trans(cb, (c + 1) & 1, r, sm, tm, DECAY);
+            }
+            tmem_st_wait();
+          } else {
 #pragma unroll 1
           for (int col = 0; col < CW; col += 64) {
             __syncwarp();
@@ -1193,11 +1318,24 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             put32(ch, col + 32, r[1], sm, tm, DECAY);
           }
           if (DECAY) tmem_st_wait();
+          }
           fence_proxy_async_smem();
           tc_fence_before();
           named_bar_sync(BAR_WG3, 128);
           if (t == 0) mbar_arrive(&s_ready[ch]);
           LA_TRACE_EVENT(trace_on && t == 0, t0, 11, k);
+        } else if (SM::TRANS && seg[sg] == p.n_seg - 1 && p.S_final) {
+          const float fin = DECAY ? __expf(g_prev[ch]) : 1.f;
+#pragma unroll 1
+          for (int cb = 0; cb < DK / 32; ++cb) {
+            __syncwarp();
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + SM::T_S + 32 * cb, r);
+            tmem_ld_wait();
+            float *dst = p.S_final + ((size_t)bh * D + 32 * cb) * D + t;  // column t
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[(size_t)j * D] = __uint_as_float(r[j]) * fin;
+          }
         } else if (seg[sg] == p.n_seg - 1 && p.S_final) {
           const float fin = DECAY ? __expf(g_prev[ch]) : 1.f;
 #pragma unroll 1
