@@ -749,11 +749,18 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nk > 0) {
+    // The whole warp runs the scheduler, with every readiness test made
+    // warp-uniform by a vote, and one elected lane issues each group of MMAs
+    // and its commits.  Operands go in as 32-bit descriptor low words (the
+    // high word is one constant): the per-MMA operand arithmetic then stays a
+    // 32-bit add, which roughly halves the issue cost of a small MMA against
+    // one thread adding 64-bit descriptors.
+    if (nk > 0) {
       // d = 128 issues its MMAs from rolled loops: the kernel's hot code then
       // stays within the instruction cache (ncu: hit rate 81% -> 92%).  d = 64
-      // is bound by MMA issue and keeps them unrolled.
+      // keeps them unrolled.
       constexpr int kMmaUnroll = DK == 128 ? 1 : 8;
+      constexpr uint32_t FULL = 0xffffffffu;
       constexpr uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(64, DK, false, true);
       constexpr uint32_t id_qs = idesc_bf16_f32(64, CW, false, true);
@@ -763,14 +770,16 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       constexpr uint32_t id_kvT = idesc_bf16_f32(DK, DK, true, true);
       constexpr uint32_t id_qsT = idesc_bf16_f32(DK, 64, false, false);
       constexpr uint32_t id_pvT = idesc_bf16_f32(DK, 64, true, false);
-      // Operand descriptors: the base descriptor of each layout at the start
-      // of shared memory, plus (byte offset >> 4) in its 14-bit address field
-      // (shared memory ends below 256 KB, so the field never carries).
+      // Descriptor low words of each layout at the start of shared memory;
+      // an operand at byte offset off adds off >> 4 (shared memory ends below
+      // 256 KB, so the 14-bit address field never carries).
+      constexpr uint32_t HI = smem_desc_sw128_hi(1024);
       const uint32_t sbase = smem_u32(smem);
-      const uint64_t dKM = smem_desc_sw128(sbase, 16, 1024);          // K-major rows
-      const uint64_t dMN = smem_desc_sw128(sbase, BOX_BYTES, 1024);   // MN-major, 8 KB blocks
-      const uint64_t dMS = smem_desc_sw128(sbase, SM::S_BLOCK, 1024); // MN-major state blocks
-      auto at = [](uint64_t d, uint32_t off) { return d + (uint64_t)(off >> 4); };
+      const uint32_t dKM = smem_desc_sw128_lo(sbase, 16);          // K-major rows
+      const uint32_t dMN = smem_desc_sw128_lo(sbase, BOX_BYTES);   // MN-major, 8 KB blocks
+      const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::S_BLOCK); // MN-major state blocks
+      auto at = [](uint32_t d, uint32_t off) { return d + (off >> 4); };
+      auto ready = [&](uint64_t *bar, uint32_t par) { return __all_sync(FULL, mbar_test(bar, par)); };
       // Three streams of MMA work, issued as each becomes ready (non-blocking
       // tests), so that a late input of one never holds up another:
       //   chain step kc: per chain, S += K^T V and O = Q S_c (needs the
@@ -794,119 +803,132 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           // Q, K, V of the chunk in their final form: phi applied (xdone) and,
           // with decay, the rows scaled (qk_ready, which follows xdone).
           const bool inputs =
-              (cc > 0) || ((kc < 2 || mbar_test(&o_free[b], ((kc >> 1) - 1) & 1)) &&
-                           mbar_test(DECAY ? &qk_ready[s] : &xdone[s], (kc / NST) & 1));
-          if (inputs && mbar_test(&s_ready[ch], ch_chunk(ch, kc) & 1)) {
+              (cc > 0) || ((kc < 2 || ready(&o_free[b], ((kc >> 1) - 1) & 1)) &&
+                           ready(DECAY ? &qk_ready[s] : &xdone[s], (kc / NST) & 1));
+          if (inputs && ready(&s_ready[ch], ch_chunk(ch, kc) & 1)) {
             tc_fence_after();
-            LA_TRACE_EVENT(trace_on && cc == 0, t0, 8, kc);
+            LA_TRACE_EVENT(trace_on && lane == 0 && cc == 0, t0, 8, kc);
             const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
             const uint32_t o_t = tmem + SM::T_O + SM::T_OW * b;
             const bool inter = S_seg[sg] != nullptr || c > 0;
             if constexpr (SM::TRANS) {
               // The chain is S^T += V^T K alone; O^T = S^T Q^T follows it off the
               // chain (its bf16 S^T copy is double-buffered in TMEM).
+              const uint32_t sb = tmem + SM::T_SB + 64 * (c & 1);
+              if (elect_one()) {
 #pragma unroll kMmaUnroll
-              for (int kk = 0; kk < CH / 16; ++kk)
-                mma_bf16(tmem + SM::T_S, at(dMN, vo + 2048 * kk), at(dMN, ko + 2048 * kk), id_kvT,
-                         (inter || kk > 0) ? 1u : 0u);
-              mma_commit(&s_done[0]);
-              if (inter) {
-                const uint32_t sb = tmem + SM::T_SB + 64 * (c & 1);
+                for (int kk = 0; kk < CH / 16; ++kk)
+                  mma_bf16_w(tmem + SM::T_S, at(dMN, vo + 2048 * kk), at(dMN, ko + 2048 * kk), HI,
+                             id_kvT, (inter || kk > 0) ? 1u : 0u);
+                mma_commit(&s_done[0]);
+                if (inter) {
 #pragma unroll kMmaUnroll
-                for (int kk = 0; kk < DK / 16; ++kk) {
-                  const uint32_t off = qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-                  mma_bf16_ta(o_t, sb + 8 * kk, at(dKM, off), id_qsT, kk > 0);
+                  for (int kk = 0; kk < DK / 16; ++kk)
+                    mma_bf16_ta_w(o_t, sb + 8 * kk,
+                                  at(dKM, qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)), HI, id_qsT,
+                                  kk > 0);
                 }
               }
+              __syncwarp();
               ++kc;
-              LA_TRACE_EVENT(trace_on, t0, 9, kc - 1);
-              did = true;
             } else {
-            const uint32_t vb = vo + (PAIRS ? 0u : (uint32_t)(ch * (CW / 64)) * BOX_BYTES);
-#pragma unroll
-            for (int kk = 0; kk < CH / 16; ++kk)   // chain state: S (TMEM) += K^T V
-              mma_bf16(tmem + SM::T_S + CW * ch, at(dMN, ko + 2048 * kk), at(dMN, vb + 2048 * kk),
-                       id_kv, (inter || kk > 0) ? 1u : 0u);
-            if (inter) {
+              const uint32_t vb = vo + (PAIRS ? 0u : (uint32_t)(ch * (CW / 64)) * BOX_BYTES);
               const uint32_t so = SM::OFF_S + ch * SM::S_BYTES;
+              if (elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < DK / 16; ++kk) {  // O[:, chain] = Q S_c[:, chain]
-                const uint32_t off = qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-                mma_bf16(o_t + ch_col(ch), at(dKM, off), at(dMS, so + 2048 * kk), id_qs, kk > 0);
+                for (int kk = 0; kk < CH / 16; ++kk)  // chain state: S (TMEM) += K^T V
+                  mma_bf16_w(tmem + SM::T_S + CW * ch, at(dMN, ko + 2048 * kk),
+                             at(dMN, vb + 2048 * kk), HI, id_kv, (inter || kk > 0) ? 1u : 0u);
+                if (inter) {
+#pragma unroll
+                  for (int kk = 0; kk < DK / 16; ++kk)  // O[:, chain] = Q S_c[:, chain]
+                    mma_bf16_w(o_t + ch_col(ch), at(dKM, qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)),
+                               at(dMS, so + 2048 * kk), HI, id_qs, kk > 0);
+                }
+                mma_commit(&s_done[ch]);
+              }
+              __syncwarp();
+              if (PAIRS || ++cc == NCHAIN) {
+                cc = 0;
+                ++kc;
               }
             }
-            mma_commit(&s_done[ch]);
-            if (PAIRS || ++cc == NCHAIN) {
-              cc = 0;
-              ++kc;
-              LA_TRACE_EVENT(trace_on, t0, 9, kc - 1);
-            }
+            if (cc == 0) LA_TRACE_EVENT(trace_on && lane == 0, t0, 9, kc - 1);
             did = true;
-            }
           }
         }
         if (km < kc) {  // ---- P V
           int sg, c;
           st.at(km, sg, c);
           const int s = km % NST, b = km & 1;
-          if (mbar_test(&p_ready[b], (km >> 1) & 1)) {
+          if (ready(&p_ready[b], (km >> 1) & 1)) {
             tc_fence_after();
-            LA_TRACE_EVENT(trace_on, t0, 5, km);
+            LA_TRACE_EVENT(trace_on && lane == 0, t0, 5, km);
             const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * b;
             const bool inter = S_seg[sg] != nullptr || c > 0;
+            if (elect_one()) {
 #pragma unroll kMmaUnroll
-            for (int kk = 0; kk < CH / 16; ++kk) {  // O += P V   (TRANS: O^T += V^T P^T)
-              if constexpr (SM::TRANS)
-                mma_bf16(tmem + SM::T_O + SM::T_OW * b, at(dMN, vo + 2048 * kk), at(dKM, po + 32 * kk),
-                         id_pvT, (inter || kk > 0) ? 1u : 0u);
-              else
-                mma_bf16(tmem + SM::T_O + SM::T_OW * b, at(dKM, po + 32 * kk), at(dMN, vo + 2048 * kk),
-                         id_pv, (inter || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < CH / 16; ++kk) {  // O += P V   (TRANS: O^T += V^T P^T)
+                if constexpr (SM::TRANS)
+                  mma_bf16_w(tmem + SM::T_O + SM::T_OW * b, at(dMN, vo + 2048 * kk),
+                             at(dKM, po + 32 * kk), HI, id_pvT, (inter || kk > 0) ? 1u : 0u);
+                else
+                  mma_bf16_w(tmem + SM::T_O + SM::T_OW * b, at(dKM, po + 32 * kk),
+                             at(dMN, vo + 2048 * kk), HI, id_pv, (inter || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&o_full[b]);
+              mma_commit(&empty[s]);
             }
-            mma_commit(&o_full[b]);
-            mma_commit(&empty[s]);
-            LA_TRACE_EVENT(trace_on, t0, 6, km);
+            __syncwarp();
+            LA_TRACE_EVENT(trace_on && lane == 0, t0, 6, km);
             ++km;
             did = true;
           }
         }
         if (kq < nk && kq <= km + 1) {  // ---- QK^T
           const int s = kq % NST;
-          if (mbar_test(&xdone[s], (kq / NST) & 1)) {
+          if (ready(&xdone[s], (kq / NST) & 1)) {
             tc_fence_after();
             const uint32_t so = s * SM::STAGE;
+            if (elect_one()) {
 #pragma unroll kMmaUnroll
-            for (int kk = 0; kk < DK / 16; ++kk) {
-              const uint32_t off = so + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
-              mma_bf16(tmem + SM::T_P + 64 * (kq & 1), at(dKM, off), at(dKM, off + SM::TILE),
-                       id_qk, kk > 0);
+              for (int kk = 0; kk < DK / 16; ++kk) {
+                const uint32_t off = so + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+                mma_bf16_w(tmem + SM::T_P + 64 * (kq & 1), at(dKM, off), at(dKM, off + SM::TILE), HI,
+                           id_qk, kk > 0);
+              }
+              mma_commit(&p_full[kq & 1]);
             }
-            mma_commit(&p_full[kq & 1]);
-            LA_TRACE_EVENT(trace_on, t0, 7, kq);
+            __syncwarp();
+            LA_TRACE_EVENT(trace_on && lane == 0, t0, 7, kq);
             ++kq;
             did = true;
           }
         }
         if (did) {
           idle_polls = 0;
+          idle_since = 0;
         } else if (__nanosleep(20), ++idle_polls == 64) {  // bounded: give up after the limit
-          const uint64_t now = global_timer_ns();
+          idle_polls = 0;
+          const uint64_t now = __shfl_sync(FULL, global_timer_ns(), 0);
           if (idle_since == 0) {
             idle_since = now;
-          } else if (now - idle_since > kWaitNs || *(volatile uint32_t *)&ctl->abort) {
-            if (!*(volatile uint32_t *)&ctl->abort) {
+          } else if (now - idle_since > kWaitNs ||
+                     __any_sync(FULL, *(volatile uint32_t *)&ctl->abort != 0)) {
+            if (lane == 0 && !*(volatile uint32_t *)&ctl->abort) {
               atomicExch(&ctl->abort, 1u);
               record_device_error(p.err, KID_PREFILL_TC_OUT, 20);
             }
             ok = false;
           }
-          idle_polls = 0;
         }
-        if (did) idle_since = 0;
       }
       if (!ok) {  // let every issued MMA finish before TMEM is released
-        mma_commit(drain);
-        drain_wait(drain, 0);
+        if (elect_one()) {  // the lane that issued them
+          mma_commit(drain);
+          drain_wait(drain, 0);
+        }
+        __syncwarp();
       }
     }
   } else if (warp >= W_PREP && warp < WG2) {
