@@ -756,10 +756,6 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     // 32-bit add, which roughly halves the issue cost of a small MMA against
     // one thread adding 64-bit descriptors.
     if (nk > 0) {
-      // d = 128 issues its MMAs from rolled loops: the kernel's hot code then
-      // stays within the instruction cache (ncu: hit rate 81% -> 92%).  d = 64
-      // keeps them unrolled.
-      constexpr int kMmaUnroll = DK == 128 ? 1 : 8;
       constexpr uint32_t FULL = 0xffffffffu;
       constexpr uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(64, DK, false, true);
@@ -816,13 +812,13 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
               // chain (its bf16 S^T copy is double-buffered in TMEM).
               const uint32_t sb = tmem + SM::T_SB + 64 * (c & 1);
               if (elect_one()) {
-#pragma unroll kMmaUnroll
+#pragma unroll
                 for (int kk = 0; kk < CH / 16; ++kk)
                   mma_bf16_w(tmem + SM::T_S, at(dMN, vo + 2048 * kk), at(dMN, ko + 2048 * kk), HI,
                              id_kvT, (inter || kk > 0) ? 1u : 0u);
                 mma_commit(&s_done[0]);
                 if (inter) {
-#pragma unroll kMmaUnroll
+#pragma unroll
                   for (int kk = 0; kk < DK / 16; ++kk)
                     mma_bf16_ta_w(o_t, sb + 8 * kk,
                                   at(dKM, qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)), HI, id_qsT,
@@ -867,7 +863,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * b;
             const bool inter = S_seg[sg] != nullptr || c > 0;
             if (elect_one()) {
-#pragma unroll kMmaUnroll
+#pragma unroll
               for (int kk = 0; kk < CH / 16; ++kk) {  // O += P V   (TRANS: O^T += V^T P^T)
                 if constexpr (SM::TRANS)
                   mma_bf16_w(tmem + SM::T_O + SM::T_OW * b, at(dMN, vo + 2048 * kk),
@@ -891,7 +887,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             tc_fence_after();
             const uint32_t so = s * SM::STAGE;
             if (elect_one()) {
-#pragma unroll kMmaUnroll
+#pragma unroll
               for (int kk = 0; kk < DK / 16; ++kk) {
                 const uint32_t off = so + (kk / 4) * BOX_BYTES + 32 * (kk % 4);
                 mma_bf16_w(tmem + SM::T_P + 64 * (kq & 1), at(dKM, off), at(dKM, off + SM::TILE), HI,
@@ -1022,7 +1018,6 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int row = acc_row<64>(quarter, lane);   // row within the chunk
     float *ofr = reinterpret_cast<float *>(smem + SM::OFF_OFR);  // [2][64] (TRANS)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    float of_cur = 1.f;  // output row factor of the chunk whose P was just formed
     auto p_epilogue = [&](int k) -> bool {
       const int s = k % NST, b = k & 1;
       if (DECAY && !wait_wg(&xdone[s], (k / NST) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 15, BAR_WG2))
@@ -1036,33 +1031,35 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       // factor is applied by the O epilogue); others take their decay per
       // element, out of line.
       const bool sp = !DECAY || split[s];
-      if (SM::TRANS && DECAY && t < 64)  // the O epilogue needs every token's factor
+      if (DECAY && t < 64)  // the chunk's output row factors, for its O epilogue
         ofr[b * 64 + t] = sp ? ofac[s * 64 + t] : 1.f;
-      if (DECAY && row >= 0) of_cur = sp ? ofac[s * 64 + row] : 1.f;
       if (!sp) {
         p_tile_strong_decay(tmem + lane_off + SM::T_P + 64 * b, row, lam + s * 64, ps);
       } else {
+        // P has M = 64: rows 16 quarter + 0..15 sit in the quarter's first 16
+        // lanes.  A 16x256b load spreads them over all 32 threads in the 8x8
+        // fragment layout (rows ra and ra + 8, columns 8 q + c2, +1), which
+        // stmatrix stores into the swizzled tile, 16 bytes per matrix row.
         __syncwarp();
-        uint32_t r[2][32];
-        tmem_ld32(tmem + lane_off + SM::T_P + 64 * b, r[0]);
-        tmem_ld32(tmem + lane_off + SM::T_P + 64 * b + 32, r[1]);
+        uint32_t r[32];
+        tmem_ld_16x256b_x8(tmem + lane_off + SM::T_P + 64 * b, r);
         tmem_ld_wait();
-        if (row >= 0) {
+        const int ra = 16 * quarter + (lane >> 2), c2 = 2 * (lane & 3);
+        uint32_t pa[8], pb[8];
 #pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
+        for (int q = 0; q < 8; ++q) {
+          const int j = 8 * q + c2;  // causal mask: keep key j <= query row
+          pa[q] = pack_bf16(j <= ra ? __uint_as_float(r[4 * q]) : 0.f,
+                            j + 1 <= ra ? __uint_as_float(r[4 * q + 1]) : 0.f);
+          pb[q] = pack_bf16(j <= ra + 8 ? __uint_as_float(r[4 * q + 2]) : 0.f,
+                            j + 1 <= ra + 8 ? __uint_as_float(r[4 * q + 3]) : 0.f);
+        }
+        const int mi = lane >> 3, srow = 16 * quarter + 8 * (mi & 1) + (lane & 7);
+        const uint32_t rbase = smem_u32(ps) + srow * 128;
 #pragma unroll
-            for (int q16 = 0; q16 < 2; ++q16) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int j = 0; j < 16; j += 2) {
-                const int j0 = hlf * 32 + q16 * 16 + j;
-                const float v0 = j0 <= row ? __uint_as_float(r[hlf][q16 * 16 + j]) : 0.f;
-                const float v1 = j0 + 1 <= row ? __uint_as_float(r[hlf][q16 * 16 + j + 1]) : 0.f;
-                pk[j >> 1] = pack_bf16(v0, v1);
-              }
-              st_row16(ps, 8192, row, hlf * 32 + q16 * 16, pk);
-            }
-          }
+        for (int qq = 0; qq < 8; qq += 2) {
+          const int q = qq + (mi >> 1);
+          stmatrix_x4(rbase + ((q ^ (srow & 7)) << 4), pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
         }
       }
       fence_proxy_async_smem();
@@ -1072,7 +1069,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       LA_TRACE_EVENT(trace_on && t == 0, t0, 4, k);
       return true;
     };
-    auto o_epilogue = [&](int k, float f) -> bool {
+    auto o_epilogue = [&](int k) -> bool {
       const int b = k & 1;
       if (!wait_wg(&o_full[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
         return false;
@@ -1121,34 +1118,29 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
         }
       } else {
+        // O has M = 64 as P: 16x256b loads, the rows' output factors, stmatrix.
+        const int ra = 16 * quarter + (lane >> 2);
+        const float fa = DECAY ? ofr[b * 64 + ra] : 1.f, fb = DECAY ? ofr[b * 64 + ra + 8] : 1.f;
+        const int mi = lane >> 3, srow = 16 * quarter + 8 * (mi & 1) + (lane & 7);
 #pragma unroll 1
-      for (int col = 0; col < DK; col += 64) {
-        __syncwarp();  // tcgen05.ld is warp-collective: reconverge after the row branch
-        uint32_t r[2][32];
-        tmem_ld32(tmem + lane_off + SM::T_O + DK * b + col, r[0]);
-        tmem_ld32(tmem + lane_off + SM::T_O + DK * b + col + 32, r[1]);
-        tmem_ld_wait();
-        if (row >= 0) {
+        for (int col = 0; col < DK; col += 64) {
+          __syncwarp();
+          uint32_t r[32];
+          tmem_ld_16x256b_x8(tmem + lane_off + SM::T_O + DK * b + col, r);
+          tmem_ld_wait();
+          uint32_t pa[8], pb[8];
 #pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
+          for (int q = 0; q < 8; ++q) {
+            pa[q] = pack_bf16(__uint_as_float(r[4 * q]) * fa, __uint_as_float(r[4 * q + 1]) * fa);
+            pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]) * fb, __uint_as_float(r[4 * q + 3]) * fb);
+          }
+          const uint32_t rbase = smem_u32(o_sm) + (col / 64) * BOX_BYTES + srow * 128;
 #pragma unroll
-            for (int q16 = 0; q16 < 2; ++q16) {
-              uint32_t pk[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float x0 = __uint_as_float(r[hlf][q16 * 16 + 2 * j]);
-                float x1 = __uint_as_float(r[hlf][q16 * 16 + 2 * j + 1]);
-                if (DECAY) {
-                  x0 *= f;
-                  x1 *= f;
-                }
-                pk[j] = pack_bf16(x0, x1);
-              }
-              st_row16(o_sm, BOX_BYTES, row, col + hlf * 32 + q16 * 16, pk);
-            }
+          for (int qq = 0; qq < 8; qq += 2) {
+            const int q = qq + (mi >> 1);
+            stmatrix_x4(rbase + ((q ^ (srow & 7)) << 4), pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
           }
         }
-      }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -1167,13 +1159,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       return true;
     };
     bool ok = true;
-    float of_prev = 1.f;  // output row factor of the chunk whose O is next
     for (int k = 0; ok && k < nk; ++k) {
       ok = p_epilogue(k);
-      if (ok && k >= 1) ok = o_epilogue(k - 1, of_prev);
-      of_prev = of_cur;
+      if (ok && k >= 1) ok = o_epilogue(k - 1);
     }
-    if (ok && nk > 0) o_epilogue(nk - 1, of_prev);
+    if (ok && nk > 0) o_epilogue(nk - 1);
     if (t == 0) tma_store_wait_all();
   } else if (warp >= WG3) {
     // ------------------------------------------------------------ WG3: the state chains

@@ -250,6 +250,16 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// Four 8x8 bf16 matrices in the mma fragment layout (thread t holds row t / 4,
+// columns 2 (t % 4), +1 of each), stored untransposed: thread 8 i + j gives
+// the address of row j of matrix i, 16 bytes.
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                            uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // Four 8x8 b16 matrices from fragments (register i: matrix i, thread t holding
 // row t / 4, columns 2 (t % 4), +1), stored transposed: thread 8 i + j gives the
 // address of stored row j (= fragment column j) of matrix i, 16 bytes.
