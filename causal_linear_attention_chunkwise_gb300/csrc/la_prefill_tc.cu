@@ -212,6 +212,23 @@ __device__ __forceinline__ float elu1_fast(float x) {
   return r;
 }
 
+// The same on a pair of bf16 values, in packed bf16 arithmetic.  For x > 0,
+// x + 1 is computed exactly and rounded once, as from fp32.  For x <= 0 the
+// argument t = x log2 e takes log2 e as the bf16 pair hi + lo
+// (hi = 0x3FB9 = 1.4453125, lo = 0xBB2C ~ -2.6245e-3; hi + lo matches log2 e
+// to 5e-6 relative), so that t carries one bf16 rounding and no bias; 2^t
+// then adds the rounding of its bf16 result.
+__device__ __forceinline__ uint32_t elu1_bf16x2(uint32_t x) {
+  uint32_t m, tl, tt, e, p1, r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(0u));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(tl) : "r"(m), "r"(0xBB2CBB2Cu));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(tt) : "r"(m), "r"(0x3FB93FB9u), "r"(tl));
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(tt));
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(p1) : "r"(x), "r"(0x3F803F80u));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(p1), "r"(e));
+  return r;
+}
+
 // Elementwise pass over NT consecutive bf16 tiles of 64 rows x D columns (D/64
 // swizzled 8 KB boxes per tile, 8 sixteen-byte chunks per 128-byte row):
 // x <- phi(x) * fac(k, row) in tile k.  Threads t = 0..n-1 take chunks t,
@@ -237,6 +254,10 @@ __device__ __forceinline__ void tile_pass(unsigned char *tile, Fac fac, int t, i
       uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
+        if constexpr (PHI && !SCALE) {  // phi alone: packed bf16 arithmetic
+          w[e] = elu1_bf16x2(w[e]);
+          continue;
+        }
         float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
         if (PHI) {
           lo = elu1_fast(lo);
@@ -508,7 +529,7 @@ struct OutSmem {
   // d = 128 keeps the output and the state transposed in TMEM (see the kernel):
   // its bf16 state copy lives in TMEM, not in shared memory.
   static constexpr bool TRANS = DK == 128 && NCHAIN == 1;
-  static constexpr int NST = PAIRS ? 4 : 3;
+  static constexpr int NST = PAIRS ? 5 : 3;
   static constexpr uint32_t TILE = 64 * DK * 2;            // Q, K, V or O tile of one chunk
   static constexpr uint32_t STAGE = 3 * TILE;              // Q | K | V
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
@@ -987,6 +1008,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         fence_proxy_async_smem();
         named_bar_sync(BAR_PREP, kPrepThreads);
         if (t == 0) mbar_arrive(&qk_ready[s]);
+        LA_TRACE_EVENT(trace_on && t == 0, t0, 15, k);
       }
       return true;
     };
