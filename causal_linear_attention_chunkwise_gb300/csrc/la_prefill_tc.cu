@@ -328,6 +328,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   uint64_t *done = ready + NST;    // all MMAs finished
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
   float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
+  pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
@@ -486,6 +487,10 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
 __global__ void __launch_bounds__(256)
 state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_state,
                   const float *__restrict__ ws_logdec) {
+  // Launched as a programmatic dependent of the segment-state kernel: let the
+  // output kernel's CTAs start, then wait until the segment states are written.
+  pdl_launch_dependents();
+  pdl_wait_previous();
   const int bh = blockIdx.y;
   const size_t n4 = (size_t)D * D / 4;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1251,6 +1256,10 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     };
     float g_prev[2] = {0.f, 0.f};  // per chain: g of its chunk whose MMA4 is next awaited
     bool ok = true;
+    // The incoming segment states come from the scan, which this kernel may
+    // have been launched alongside (programmatic dependent launch): only this
+    // warpgroup reads them, so only it waits for the scan grid to finish.
+    if (p.n_seg > 1) pdl_wait_previous();
     // Initial states, chain by chain (a chain's first chunk is virtual 0 or 1).
     for (int ch = 0; ok && ch < NCHAIN; ++ch) {
       const int sg = ch_seg(ch);
@@ -1482,6 +1491,25 @@ cudaError_t set_smem_once(K kern, size_t bytes, int *done_for_device) {
   return e;
 }
 
+// Launch `kern` as a programmatic dependent of the previous kernel on the
+// stream: it may start before that kernel finishes, and waits for it
+// (griddepcontrol.wait) before it reads what that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, int threads, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D, bool PHI, bool DECAY>
 cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   const Plan pl = make_plan(a.B, a.H, a.L, D);
@@ -1530,9 +1558,9 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
     }
 #endif
     const int n4 = D * D / 4;
-    state_scan_kernel<<<dim3((n4 + 255) / 256, BH), 256, 0, a.stream>>>(
-        D, pl.n_seg, a.S0, p.ws_state, p.ws_logdec);
-    if ((e = cudaGetLastError()) != cudaSuccess) {
+    e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, pl.n_seg,
+                   a.S0, p.ws_state, (const float *)p.ws_logdec);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
       if (why) *why = "la_chunk_fwd: state-scan kernel launch";
       return e;
     }
@@ -1549,8 +1577,14 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   e = set_smem_once(ko, OS::BYTES, smem_set_out);
   if (e != cudaSuccess) return e;
   const int out_x = OS::PAIRS ? (pl.n_seg + 1) / 2 : pl.n_seg;
-  ko<<<dim3(out_x, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
-  if ((e = cudaGetLastError()) != cudaSuccess && why)
+  // With segments, the output kernel is a programmatic dependent of the scan
+  // (its inputs were complete before the segment-state kernel started).  A
+  // single segment has no predecessor of its own: ordinary stream order.
+  if (pl.n_seg > 1)
+    e = launch_pdl(ko, dim3(out_x, BH), kThreadsOut, OS::BYTES, a.stream, tq, tk, tv, to, p);
+  else
+    ko<<<dim3(out_x, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  if ((e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) && why)
     *why = "la_chunk_fwd: chunk-output kernel launch";
 #ifdef LA_CHECKED
   if (e == cudaSuccess && (e = cudaStreamSynchronize(a.stream)) != cudaSuccess && why)
