@@ -297,8 +297,9 @@ struct StateSmem {
   // barriers is waited on, in order, by that one group.  (With an odd count a
   // group could wait on a stage whose previous phase belongs to the other
   // group and has not completed yet; the parity test would then pass early.)
-  // Two stages for D = 128 keep the block small enough for two per SM.
-  static constexpr int NST = D == 128 ? 2 : 4;
+  // Two stages for D = 128 and six for D = 64 keep the block small enough
+  // for two per SM.
+  static constexpr int NST = D == 128 ? 2 : 6;
   static_assert(NST % 2 == 0, "stages must alternate between the two transform groups");
   static constexpr uint32_t TILE = 64 * D * 2;
   static constexpr uint32_t STAGE = 2 * TILE;
@@ -496,33 +497,49 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n4) return;
   float4 *slots = reinterpret_cast<float4 *>(ws_state) + (size_t)bh * n_seg * n4;
+  const float *logdec = ws_logdec + (size_t)bh * n_seg;
   float4 cur = S0 ? reinterpret_cast<const float4 *>(S0)[(size_t)bh * n4 + i]
                   : make_float4(0.f, 0.f, 0.f, 0.f);
   slots[i] = cur;
-  float4 nxt = n_seg > 1 ? slots[n4 + i] : cur;
-  for (int s = 0; s + 1 < n_seg; ++s) {
-    const float a = __expf(ws_logdec[(size_t)bh * n_seg + s]);
-    const float4 d = nxt;
-    if (s + 2 < n_seg) nxt = slots[(size_t)(s + 2) * n4 + i];
-    cur.x = fmaf(a, cur.x, d.x);
-    cur.y = fmaf(a, cur.y, d.y);
-    cur.z = fmaf(a, cur.z, d.z);
-    cur.w = fmaf(a, cur.w, d.w);
-    slots[(size_t)(s + 1) * n4 + i] = cur;
+  // Segments in batches of eight: every load of a batch is issued before the
+  // first use, so a batch costs one memory round trip.
+  constexpr int kB = 8;
+  for (int s0 = 0; s0 + 1 < n_seg; s0 += kB) {
+    float4 d[kB];
+    float a[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      if (s0 + j + 1 < n_seg) {
+        d[j] = slots[(size_t)(s0 + j + 1) * n4 + i];
+        a[j] = logdec[s0 + j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      if (s0 + j + 1 < n_seg) {
+        const float e = __expf(a[j]);
+        cur.x = fmaf(e, cur.x, d[j].x);
+        cur.y = fmaf(e, cur.y, d[j].y);
+        cur.z = fmaf(e, cur.z, d[j].z);
+        cur.w = fmaf(e, cur.w, d[j].w);
+        slots[(size_t)(s0 + j + 1) * n4 + i] = cur;
+      }
+    }
   }
 }
 
 // ================================================================ chunk output
-// Each output CTA carries two independent state chains, each a [d_k x 64]
-// block of state with its own hand-over (MMA into TMEM, then the TMEM -> bf16
-// copy), so that one chain's hand-over overlaps the other chain's work:
-//   d = 64:  the two chains are two segments of one (b, h) sequence.  Their
-//            chunks are interleaved into one sequence of virtual chunks
-//            k = 0, 1, ...: while both have chunks left they alternate.
-//   d = 128: the two chains are the two 64-column halves of one segment's
-//            state (S[:, half] and O[:, half] depend on V[:, half] alone);
-//            virtual chunk k is chunk k of the segment, and both halves
-//            advance in it.
+// d = 64: each output CTA carries two independent state chains, the states of
+//   two segments of one (b, h) sequence, each with its own hand-over (MMA into
+//   TMEM, then the TMEM -> bf16 copy), so that one chain's hand-over overlaps
+//   the other chain's work.  Their chunks are interleaved into one sequence
+//   of virtual chunks k = 0, 1, ...: while both have chunks left they
+//   alternate.
+// d = 128: one segment per CTA and one 128-column chain, computed transposed
+//   so that every product has M = 128: S^T += V^T K, O^T = S^T Q^T (A, the
+//   bf16 copy of S^T, read from TMEM) and O^T += V^T P^T.  The state hand-over
+//   then stays in TMEM.  (Building with LA_D128_CHAINS=2 restores the older
+//   untransposed form with two 64-column half-chains.)
 #ifndef LA_D128_CHAINS
 #define LA_D128_CHAINS 1
 #endif
