@@ -140,6 +140,35 @@ def test_segmented_sequences_match_oracle(case):
         parity.check(select_pairs(S, pairs), S_ref, "bf16", "S_final")
 
 
+# elu + 1 over a wide input range: q and k scaled by a power of two (exact in
+# bf16) to a standard deviation of about 4, so that many entries lie deep in
+# the exponential branch, where the packed-bf16 form
+# of phi rounds the exponent argument.  Covers the output kernel (phi alone on
+# Q and K), the segment-state kernel without decay (phi alone on K) and with
+# decay (phi and K's weight in one fp32 pass).
+WIDE = [
+    # (B, H, L, d, decay)
+    (2, 4, 1000, 64, "none"),
+    (1, 2, 2100, 128, "none"),
+    (1, 3, 1500, 64, "head"),
+    (1, 2, 1300, 128, "logit"),
+]
+
+
+@pytest.mark.parametrize("case", WIDE, ids=[f"{c[0]}x{c[1]}x{c[2]}_d{c[3]}_{c[4]}" for c in WIDE])
+def test_elu1_on_wide_range_inputs(case):
+    B, H, L, d, decay = case
+    w, inp = _make(B, H, L, d, d, "bf16", "elu1", decay, 64, None)
+    scale = 32 if d == 64 else 64  # inputs are N(0, 1/d)
+    inp["q"] = inp["q"] * scale
+    inp["k"] = inp["k"] * scale
+    assert float((inp["k"].float() < -4).float().mean()) > 0.1  # deep in exp(x)
+    O, S = gpu_prefill(inp, w.phi, 64)
+    O_ref, S_ref = oracle_prefill(inp, w.phi)
+    parity.check(O, O_ref, "bf16", "O")
+    parity.check(S, S_ref, "bf16", "S_final")
+
+
 # Per-token decays whose strength alternates by chunk: odd chunks decay hard
 # (log a ~ -2.4 per token, chunk total ~ -155), even chunks gently (~ -15).
 # The tensor-core kernel treats the two kinds of chunk differently (the decay
