@@ -79,8 +79,9 @@ def _bind(lib):
     sig = [i, i, i, i, i, dp, dp, dp, i, i, dp, dp, dp, dp]
     lib.oracle_recurrent.argtypes = sig
     lib.oracle_parallel.argtypes = sig
+    lib.oracle_noncausal.argtypes = sig
     lib.oracle_chunkwise.argtypes = [i, i, i, i, i, i, dp, dp, dp, i, i, dp, dp, dp, dp]
-    for f in (lib.oracle_recurrent, lib.oracle_parallel, lib.oracle_chunkwise):
+    for f in (lib.oracle_recurrent, lib.oracle_parallel, lib.oracle_chunkwise, lib.oracle_noncausal):
         f.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
@@ -175,6 +176,12 @@ def parallel(q, k, v, phi="identity", decay_kind="none", decay=None, S0=None, li
 def chunkwise(q, k, v, chunk, phi="identity", decay_kind="none", decay=None, S0=None, lib=None):
     """Chunkwise form with chunk size ``chunk``; returns (O, S_final)."""
     return _run("oracle_chunkwise", q, k, v, phi, decay_kind, decay, S0, chunk=chunk, lib=lib)
+
+
+def noncausal(q, k, v, phi="identity", lib=None):
+    """Non-causal matrix form O = phi(Q) (phi(K)^T V); returns (O, S) with S
+    = phi(K)^T V, the state every token reads."""
+    return _run("oracle_noncausal", q, k, v, phi, "none", None, None, lib=lib)
 
 
 def decode(q, k, v, S0, log_alpha=None, phi="elu1", lib=None):

@@ -41,6 +41,12 @@
  *           state exp(Lam_end) and exp(Lam_end - Lam_j)) are the plain
  *           expansion of the gated recurrence over one chunk.
  *
+ *   oracle_noncausal  the non-causal matrix form (no mask, no decay, no S0)
+ *       "adv13 - Linear Attention / SSM" section 4.3, linear_attention_matrix:
+ *           S = phi(K)^T V over the whole sequence, then O = phi(Q) S;
+ *       "CS336 lecture 4, code 1", demo_associativity: (Q K^T) V = Q (K^T V).
+ *       Every token reads the same S, the state after the last token.
+ *
  * Decay is given per token in log space, lambda_t = log(decay factor):
  *   kind 0  none                  lambda_t = 0
  *   kind 1  per head  [H]         lambda_t = log_gamma[h]          (RetNet)
@@ -274,6 +280,45 @@ int oracle_chunkwise(int B, int H, int L, int dk, int dv, int C,
 
 /* Number of threads an OpenMP parallel region in this library would use (1
  * when built without OpenMP); reported beside the CPU timings. */
+/* The non-causal form: S = sum_t phi(k_t) v_t^T over all L tokens of (b,h),
+ * then o_t = phi(q_t)^T S for every t.  kind must be 0 and S0 NULL (the form
+ * has neither); S_final receives S. */
+int oracle_noncausal(int B, int H, int L, int dk, int dv,
+                     const double *q, const double *k, const double *v,
+                     int phi, int kind, const double *decay,
+                     const double *S0, double *O, double *S_final)
+{
+    if (check_args(B, H, L, dk, dv, phi, kind, decay) || kind != 0 || S0 != NULL) return -1;
+    int err = 0;
+    long nseq = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (long bh = 0; bh < nseq; ++bh) {
+        double *S = calloc((size_t)dk * dv, sizeof(double));
+        double *f = malloc(sizeof(double) * (size_t)dk);
+        if (!S || !f) { free(S); free(f); err |= 1; continue; }
+        for (int t = 0; t < L; ++t) {  /* S = phi(K)^T V */
+            const double *kt = k + ((size_t)bh * L + t) * dk;
+            const double *vt = v + ((size_t)bh * L + t) * dv;
+            for (int i = 0; i < dk; ++i) f[i] = feature(phi, kt[i]);
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += f[i] * vt[j];
+        }
+        for (int t = 0; t < L; ++t) {  /* O = phi(Q) S */
+            const double *qt = q + ((size_t)bh * L + t) * dk;
+            double *ot = O + ((size_t)bh * L + t) * dv;
+            for (int i = 0; i < dk; ++i) f[i] = feature(phi, qt[i]);
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += f[i] * S[(size_t)i * dv + j];
+                ot[j] = acc;
+            }
+        }
+        if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+        free(S); free(f);
+    }
+    return err ? -2 : 0;
+}
+
 #ifdef _OPENMP
 #include <omp.h>
 int oracle_num_threads(void) { return omp_get_max_threads(); }

@@ -15,7 +15,9 @@ planted mistake) and raises AssertionError when the oracle disagrees with:
   at n = 200, d = 16, gamma = sigmoid(k.w + 3) ("CS336 lecture 4, code 1:
   linear attention", demo_two_forms and demo_gating);
 * the resume invariant: running [0, m) then [m, L) from the carried state
-  equals one run over [0, L).
+  equals one run over [0, L);
+* for the non-causal form: the causal final state and last row, the n x n
+  association order, one-hot values and L = 0 (``pin_noncausal``).
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in a copy of the
 oracle's C source and checks that at least one pin fails for each.
@@ -269,6 +271,39 @@ def pin_state_shape(lib):
         assert S.shape == (6, 4), S.shape
 
 
+def pin_noncausal(lib):
+    """The non-causal form ("adv13 - Linear Attention / SSM" section 4.3):
+    - its state is the causal recurrence's final state with no decay and S0 = 0;
+    - its last output row is the recurrence's last row (both read that state);
+    - (phi(Q) phi(K)^T) V, the n x n order of "CS336 lecture 4, code 1"
+      demo_associativity, computed by numpy with torch's ELU for phi, equals it;
+    - one-hot queries and keys: o_t = sum_s [q_t = k_s] v_s by hand;
+    - L = 0 gives an empty output and a zero state."""
+    r = _rng(12)
+    B, H, L, dk, dv = 2, 2, 23, 5, 4
+    q, k, v = r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dv))
+    for phi in ("identity", "elu1"):
+        O, S = oracle.noncausal(q, k, v, phi=phi, lib=lib)
+        Oc, Sc = oracle.recurrent(q, k, v, phi=phi, lib=lib)
+        _close(S, Sc, 1e-12, f"noncausal state = causal final state/{phi}")
+        _close(O[:, :, -1], Oc[:, :, -1], 1e-12, f"noncausal last row = causal last row/{phi}")
+        fq, fk = (q, k) if phi == "identity" else (_elu1(q), _elu1(k))
+        scores = np.matmul(fq, np.swapaxes(fk, -1, -2))  # [B,H,L,L], no mask
+        _close(O, np.matmul(scores, v), 1e-12, f"(QK^T)V = Q(K^TV)/{phi}")
+    # one-hot: token t has q_t = e_{t mod dk}, k_s = e_{s mod dk}
+    Lh, d = 7, 3
+    eye = np.eye(d)
+    qh = np.stack([eye[t % d] for t in range(Lh)])
+    kh = np.stack([eye[(2 * s) % d] for s in range(Lh)])
+    vh = np.arange(Lh * 2, dtype=np.float64).reshape(Lh, 2)
+    O, S = oracle.noncausal(qh, kh, vh, lib=lib)
+    want = np.stack([sum(vh[s] for s in range(Lh) if (2 * s) % d == t % d) for t in range(Lh)])
+    _close(O, want, 0.0, "noncausal one-hot")
+    O, S = oracle.noncausal(q[:, :, :0], k[:, :, :0], v[:, :, :0], lib=lib)
+    assert O.shape == (B, H, 0, dv)
+    _close(S, np.zeros((B, H, dk, dv)), 0.0, "noncausal L=0 state")
+
+
 PINS = [pin_golden, pin_closed_form_additive, pin_closed_form_constant_decay, pin_single_token,
         pin_one_hot, pin_orthonormal_keys, pin_chunk_invariance, pin_parallel_equals_recurrent,
-        pin_split_invariance, pin_library_pieces, pin_state_shape]
+        pin_split_invariance, pin_library_pieces, pin_state_shape, pin_noncausal]

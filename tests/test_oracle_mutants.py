@@ -79,6 +79,12 @@ MUTANTS = [
     ("chunk_intra_excludes_diagonal",
      "for (int jj = 0; jj <= i; ++jj) {",
      "for (int jj = 0; jj < i; ++jj) {"),
+    ("noncausal_state_transposed",
+     "for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += f[i] * vt[j];",
+     "for (int j = 0; j < dv; ++j) S[(size_t)j * dk + i] += f[i] * vt[j];"),
+    ("noncausal_phi_not_on_q",
+     "for (int i = 0; i < dk; ++i) f[i] = feature(phi, qt[i]);",
+     "for (int i = 0; i < dk; ++i) f[i] = qt[i];"),
 ]
 
 
