@@ -23,6 +23,8 @@ SIGNATURES = {
     "la_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                   _vp, _vp]),
     "la_chunk_fwd_noalloc_scratch_bytes": (_sz, []),
+    "la_noncausal_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
+    "la_noncausal_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "la_device_status": (_i, [_vp]),
     "la_selftest_wait_timeout": (_i, [_u, _vp]),
     "la_last_error": (ctypes.c_char_p, []),

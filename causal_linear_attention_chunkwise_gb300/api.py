@@ -113,6 +113,33 @@ def la_chunk_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, O=No
     return O, S_final
 
 
+def la_noncausal_fwd_workspace_bytes(B, H, L, d_k, d_v) -> int:
+    return int(_native.load().la_noncausal_fwd_workspace_bytes(B, H, L, d_k, d_v))
+
+
+def la_noncausal_fwd(q, k, v, O=None, S=None, want_state=True, workspace=None, stream=None):
+    """Non-causal linear attention O = phi(Q) (phi(K)^T V) over [B,H,L,d] bf16
+    sequences on the GPU.  Returns ``(O, S)`` with S = phi(K)^T V, fp32
+    [B,H,d,d] (None when ``want_state`` is false and no buffer is given)."""
+    B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or v.dtype != q.dtype or k.dtype != q.dtype:
+        raise ValueError("q, k, v must agree in [B,H,L] and dtype")
+    if O is None:
+        O = torch.empty(B, H, L, dv, dtype=q.dtype, device=q.device)
+    if S is None and want_state:
+        S = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    _need_cuda(q, k, v, O, S)
+    lib = _native.load()
+    if workspace is None:
+        workspace = _workspace(la_noncausal_fwd_workspace_bytes(B, H, L, dk, dv), q.device)
+    _check(lib.la_noncausal_fwd(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, _ptr(O), _ptr(S),
+        _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return O, S
+
+
 def la_chunk_fwd_noalloc(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, O=None,
                          S_final=None, want_final_state=True, stream=None):
     """la_chunk_fwd without a caller workspace, for callers that cannot

@@ -44,6 +44,7 @@ const char *kernel_name(unsigned int id) {
     case KID_PREFILL_TC_STATE: return "prefill segment-state kernel";
     case KID_PREFILL_TC_OUT: return "prefill chunk-output kernel";
     case KID_SELFTEST: return "wait-timeout self-test kernel";
+    case KID_NONCAUSAL: return "non-causal output kernel";
     default: return "unknown kernel";
   }
 }
@@ -154,6 +155,51 @@ la_status la_chunk_fwd(const void *q, const void *k, const void *v, int dtype, i
   }
   cudaError_t e = launch_prefill_simt(a);
   if (e != cudaSuccess) return cuda_fail(e, "la_chunk_fwd (SIMT path)");
+  return ok();
+}
+
+size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v) {
+  if (d_k != d_v || (d_k != 64 && d_k != 128)) return 0;
+  return noncausal_workspace_bytes(B, H, L, d_k);
+}
+
+la_status la_noncausal_fwd(const void *q, const void *k, const void *v, int dtype, int B, int H,
+                           int L, int d_k, int d_v, void *O, float *S, void *workspace,
+                           size_t ws_bytes, void *cuda_stream) {
+  if (dtype != LA_F32 && dtype != LA_BF16)
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: unknown dtype %d", dtype);
+  if (B < 0 || H < 0 || L < 0 || d_k <= 0 || d_v <= 0)
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: bad sizes B=%d H=%d L=%d d_k=%d d_v=%d",
+                B, H, L, d_k, d_v);
+  if (dtype != LA_BF16 || d_k != d_v || (d_k != 64 && d_k != 128))
+    return fail(LA_ERR_UNSUPPORTED,
+                "la_noncausal_fwd: needs bf16 with d_k = d_v in {64, 128} (dtype %d, %d x %d)",
+                dtype, d_k, d_v);
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if ((size_t)B * H == 0) return ok();
+  if (S && !aligned16(S))
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: S must start on a 16-byte boundary");
+  if (L == 0) {  // no tokens: the state is zero and there is no output
+    if (S) {
+      cudaError_t e = cudaMemsetAsync(S, 0, (size_t)B * H * d_k * d_v * sizeof(float), st);
+      if (e != cudaSuccess) return cuda_fail(e, "la_noncausal_fwd (L=0)");
+    }
+    return ok();
+  }
+  if (!q || !k || !v || !O)
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: q, k, v and O must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(O))
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: tensors must start on a 16-byte boundary");
+  const size_t need = noncausal_workspace_bytes(B, H, L, d_k);
+  if (!workspace || ws_bytes < need)
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: workspace of %zu bytes needed, %zu given",
+                need, workspace ? ws_bytes : (size_t)0);
+  if (!aligned16(workspace))
+    return fail(LA_ERR_INVALID_ARG, "la_noncausal_fwd: workspace must be 16-byte aligned");
+  NoncausalArgs a{q, k, v, B, H, L, d_k, g_phi.load(), O, S, workspace, ws_bytes, st};
+  const char *why = nullptr;
+  cudaError_t e = launch_noncausal(a, &why);
+  if (e != cudaSuccess) return cuda_fail(e, why ? why : "la_noncausal_fwd");
   return ok();
 }
 

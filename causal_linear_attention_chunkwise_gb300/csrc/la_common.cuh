@@ -12,6 +12,7 @@ enum : unsigned int {
   KID_PREFILL_TC_STATE = 1,
   KID_PREFILL_TC_OUT = 2,
   KID_SELFTEST = 3,
+  KID_NONCAUSAL = 4,
 };
 
 __device__ __forceinline__ void record_device_error(unsigned int *word, unsigned int kernel,

@@ -46,6 +46,20 @@ size_t prefill_tc_workspace_bytes(int B, int H, int L, int d);
 int prefill_tc_kernel_count(int B, int H, int L, int d);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why);
 
+// Non-causal form O = phi(Q) (phi(K)^T V): bf16, d_k == d_v in {64, 128}.
+struct NoncausalArgs {
+  const void *q, *k, *v;
+  int B, H, L, d;
+  int phi;
+  void *O;
+  float *S;  // [B,H,d,d] fp32 or null
+  void *workspace;
+  size_t ws_bytes;
+  cudaStream_t stream;
+};
+size_t noncausal_workspace_bytes(int B, int H, int L, int d);
+cudaError_t launch_noncausal(const NoncausalArgs &a, const char **why);
+
 // Decode step.
 bool decode_supported(int dk, int dv);
 cudaError_t launch_decode(const DecodeArgs &a);

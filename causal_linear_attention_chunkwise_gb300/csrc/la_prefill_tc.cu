@@ -1610,6 +1610,271 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   return e;
 }
 
+
+// ================================================================ non-causal form
+// O = phi(Q) S for every token of a (b,h) sequence, with S = phi(K)^T V over
+// the whole sequence ("adv13 - Linear Attention / SSM" section 4.3,
+// linear_attention_matrix; "CS336 lecture 4, code 1", demo_associativity).
+// S comes from the segment-state kernel run over every chunk and summed by
+// the scan into the sequence's last workspace slot.  This kernel reads S once
+// per CTA as the bf16 B operand of O_c = phi(Q_c) S and streams the CTA's
+// chunks of Q to O.  One warpgroup: thread 0 issues the TMA loads, the MMAs
+// and the stores; all 128 threads apply phi and run the epilogue.
+template <int D>
+struct NcSmem {
+  static constexpr int NQ = 3;                    // Q stages
+  static constexpr uint32_t TILE = 64 * D * 2;    // [64][D] bf16 in D/64 boxes
+  static constexpr uint32_t S_BLOCK = D * 128;    // [D][64] bf16 block of S, MN-major
+  static constexpr uint32_t OFF_S = NQ * TILE;
+  static constexpr uint32_t OFF_O = OFF_S + (D / 64) * S_BLOCK;  // 2 x O staging
+  static constexpr uint32_t OFF_BAR = OFF_O + 2 * TILE;          // full[NQ], mma_done
+  static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (NQ + 1);
+  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static_assert(TILE % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+};
+constexpr int kNcThreads = 128;
+constexpr uint32_t BAR_NC = 1;
+
+template <int D, bool PHI>
+__global__ void __launch_bounds__(kNcThreads)
+noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmO, TcParams p,
+                        int chunks_per_cta) {
+  using SM = NcSmem<D>;
+  constexpr int NQ = SM::NQ;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
+  uint64_t *mma_done = full + NQ;
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.y;
+  const int c0 = blockIdx.x * chunks_per_cta;
+  const int n = max(0, min(chunks_per_cta, p.n_chunks - c0));
+  if (tid == 0) {
+    for (int s = 0; s < NQ; ++s) mbar_init(&full[s], 1);
+    mbar_init(mma_done, 1);
+    ctl->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem_base, D);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  int issued = 0;  // thread 0: Q tiles requested
+  auto load_q = [&](int i) {
+    const int s = i % NQ;
+    mbar_arrive_expect_tx(&full[s], SM::TILE);
+    for (int b = 0; b < D / BOX; ++b)
+      if (LA_CHK((c0 + i) * CH < p.L && bh < p.BH, KID_NONCAUSAL, 3))
+        tma_load_3d(smem + s * SM::TILE + b * BOX_BYTES, &tmQ, &full[s], b * BOX, (c0 + i) * CH, bh);
+    issued = i + 1;
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmO);
+    for (int i = 0; i < min(n, NQ); ++i) load_q(i);  // Q does not depend on S
+  }
+  // S, the scan's last slot of this sequence, is written by the kernel before
+  // this one (a programmatic dependent launch): wait for it, then convert it
+  // to the bf16 B operand, MN-major with the 128-byte swizzle.
+  pdl_wait_previous();
+  {
+    const float *S = p.ws_state + ((size_t)bh * p.n_seg + (p.n_seg - 1)) * D * D;
+    unsigned char *sb = smem + SM::OFF_S;
+    for (int idx = tid; idx < D * D / 8; idx += kNcThreads) {
+      const int i = idx / (D / 8), j0 = (idx % (D / 8)) * 8;
+      const float4 x = *reinterpret_cast<const float4 *>(S + (size_t)i * D + j0);
+      const float4 y = *reinterpret_cast<const float4 *>(S + (size_t)i * D + j0 + 4);
+      *reinterpret_cast<uint4 *>(sb + (j0 / 64) * SM::S_BLOCK + i * 128 +
+                                 ((((j0 % 64) >> 3) ^ (i & 7)) << 4)) =
+          make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y),
+                     pack_bf16(y.z, y.w));
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  constexpr uint32_t HI = smem_desc_sw128_hi(1024);
+  constexpr uint32_t idesc = idesc_bf16_f32(64, D, false, true);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t dKM = smem_desc_sw128_lo(sbase, 16);          // Q: K-major rows
+  const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::S_BLOCK); // S: MN-major blocks
+  // The accumulator has M = 64: rows 16 w + 0..15 in the first 16 lanes of
+  // warp w's quarter.  A 16x256b load gives each thread rows ra and ra + 8 in
+  // the 8x8 fragment layout, which stmatrix writes to the swizzled tile.
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  const int mi = lane >> 3, srow = 16 * warp + 8 * (mi & 1) + (lane & 7);
+  bool ok = true;
+  int consumed = 0, mma_pending = -1;
+  for (int i = 0; ok && i < n; ++i) {
+    const int s = i % NQ, b = i & 1;
+    if (!wait_grp<kNcThreads>(&full[s], (i / NQ) & 1, ctl, p.err, KID_NONCAUSAL, 1, BAR_NC, tid)) {
+      ok = false;
+      break;
+    }
+    consumed = i + 1;
+    if constexpr (PHI) {
+      tile_pass<D, 1, true, false>(smem + s * SM::TILE, [](int, int) { return 1.f; }, tid,
+                                   kNcThreads);
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_NC, kNcThreads);
+    }
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t qo = s * SM::TILE;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_w(tmem, dKM + ((qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)) >> 4),
+                   dMS + ((SM::OFF_S + 2048 * kk) >> 4), HI, idesc, kk > 0 ? 1u : 0u);
+      mma_commit(mma_done);
+    }
+    mma_pending = i;
+    if (!wait_grp<kNcThreads>(mma_done, i & 1, ctl, p.err, KID_NONCAUSAL, 2, BAR_NC, tid)) {
+      ok = false;
+      break;
+    }
+    mma_pending = -1;
+    tc_fence_after();
+    if (tid == 0) {
+      if (i + NQ < n) load_q(i + NQ);  // the MMA has read this stage
+      tma_store_wait_read<1>();        // the store that used staging tile b has read it
+    }
+    __syncwarp();
+    named_bar_sync(BAR_NC, kNcThreads);
+    unsigned char *o_sm = smem + SM::OFF_O + b * SM::TILE;
+#pragma unroll 1
+    for (int col = 0; col < D; col += 64) {
+      __syncwarp();
+      uint32_t r[32];
+      tmem_ld_16x256b_x8(tmem + lane_off + col, r);
+      tmem_ld_wait();
+      uint32_t pa[8], pb[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        pa[q] = pack_bf16(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]));
+        pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+      }
+      const uint32_t rbase = smem_u32(o_sm) + (col / 64) * BOX_BYTES + srow * 128;
+#pragma unroll
+      for (int qq = 0; qq < 8; qq += 2) {
+        const int q = qq + (mi >> 1);
+        stmatrix_x4(rbase + ((q ^ (srow & 7)) << 4), pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(BAR_NC, kNcThreads);
+    if (tid == 0) {
+      const int tok = (c0 + i) * CH;
+      for (int bb = 0; bb < D / BOX; ++bb)
+        if (LA_CHK(tok < p.L && bh < p.BH, KID_NONCAUSAL, 4))
+          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok, bh);
+      tma_store_commit();
+    }
+  }
+  if (tid == 0) {
+    tma_store_wait_all();
+    if (!ok) {  // asynchronous work still in flight lands before the CTA exits
+      for (int c = consumed; c < issued; ++c) drain_wait(&full[c % NQ], (c / NQ) & 1);
+      if (mma_pending >= 0) drain_wait(mma_done, mma_pending & 1);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    __syncwarp();
+    tmem_dealloc(tmem, D);
+  }
+}
+
+// Segments of the non-causal state pass: G <= 32 chunks, and about two
+// segment-state blocks per SM.  The scan adds one slot, the sum of all.
+Plan make_noncausal_plan(int B, int H, int L) {
+  const int nc = (L + CH - 1) / CH;
+  const int bh = std::max(1, B * H);
+  int ns = std::max((nc + kMaxSegChunks - 1) / kMaxSegChunks,
+                    std::min(nc, (2 * sm_count() + bh - 1) / bh));
+  const int g = (nc + ns - 1) / ns;
+  ns = (nc + g - 1) / g;
+  return Plan{nc, g, ns};
+}
+
+size_t noncausal_ws_bytes_for(int B, int H, int L, int D) {
+  const Plan pl = make_noncausal_plan(B, H, L);
+  const size_t bh = (size_t)B * H, slots = (size_t)pl.n_seg + 1;
+  return bh * slots * D * D * sizeof(float) + ((bh * slots * sizeof(float) + 255) & ~(size_t)255);
+}
+
+template <int D, bool PHI>
+cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
+  const Plan pl = make_noncausal_plan(a.B, a.H, a.L);
+  const int BH = a.B * a.H, slots = pl.n_seg + 1;
+  TcParams p{};
+  p.H = a.H;
+  p.L = a.L;
+  p.BH = BH;
+  p.n_chunks = pl.n_chunks;
+  p.seg_chunks = pl.seg_chunks;
+  p.n_seg = slots;  // segments 0..NS-1 cover every chunk; slot NS receives the sum
+  p.phi = a.phi;
+  p.decay_kind = LA_DECAY_NONE;
+  p.err = device_error_word();
+  p.ws_state = static_cast<float *>(a.workspace);
+  p.ws_logdec = p.ws_state + (size_t)BH * slots * D * D;
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tk, a.k, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX)) {
+    if (why) *why = "la_noncausal_fwd: TMA tensor map creation failed";
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t e;
+  using SS = StateSmem<D>;
+  auto ks = segment_state_kernel<D, PHI, false>;
+  static int smem_set_state[64];
+  if ((e = set_smem_once(ks, SS::BYTES, smem_set_state)) != cudaSuccess) return e;
+  ks<<<dim3(pl.n_seg, BH), kThreadsState, SS::BYTES, a.stream>>>(tk, tv, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) {
+    if (why) *why = "la_noncausal_fwd: segment-state kernel launch";
+    return e;
+  }
+  const int n4 = D * D / 4;
+  e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, slots,
+                 (const float *)nullptr, p.ws_state, (const float *)p.ws_logdec);
+  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
+    if (why) *why = "la_noncausal_fwd: state-scan kernel launch";
+    return e;
+  }
+  using NS_ = NcSmem<D>;
+  auto kn = noncausal_output_kernel<D, PHI>;
+  static int smem_set_nc[64];
+  if ((e = set_smem_once(kn, NS_::BYTES, smem_set_nc)) != cudaSuccess) return e;
+  const int per_sm = D == 64 ? 4 : 2;  // blocks per SM that fit in shared memory
+  const long total = (long)pl.n_chunks * BH;
+  const int cpc = (int)std::max(1L, (total + (long)per_sm * sm_count() - 1) / ((long)per_sm * sm_count()));
+  const int nx = (pl.n_chunks + cpc - 1) / cpc;
+  e = launch_pdl(kn, dim3(nx, BH), kNcThreads, NS_::BYTES, a.stream, tq, to, p, cpc);
+  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
+    if (why) *why = "la_noncausal_fwd: output kernel launch";
+    return e;
+  }
+  if (a.S) {  // the sum slot of every sequence
+    e = cudaMemcpy2DAsync(a.S, (size_t)D * D * sizeof(float),
+                          p.ws_state + (size_t)pl.n_seg * D * D,
+                          (size_t)slots * D * D * sizeof(float), (size_t)D * D * sizeof(float),
+                          BH, cudaMemcpyDeviceToDevice, a.stream);
+    if (e != cudaSuccess && why) *why = "la_noncausal_fwd: state copy";
+  }
+  return e;
+}
+
 }  // namespace
 
 bool prefill_tc_supported(const PrefillArgs &a) {
@@ -1637,6 +1902,17 @@ cudaError_t launch_variant(const PrefillArgs &a, const char **why) {
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why) {
   if (a.dk == 128) return launch_variant<128>(a, why);
   return launch_variant<64>(a, why);
+}
+
+size_t noncausal_workspace_bytes(int B, int H, int L, int d) {
+  if (B <= 0 || H <= 0 || L <= 0) return 0;
+  return noncausal_ws_bytes_for(B, H, L, d);
+}
+
+cudaError_t launch_noncausal(const NoncausalArgs &a, const char **why) {
+  const bool phi = a.phi != LA_PHI_IDENTITY;
+  if (a.d == 128) return phi ? launch_noncausal_d<128, true>(a, why) : launch_noncausal_d<128, false>(a, why);
+  return phi ? launch_noncausal_d<64, true>(a, why) : launch_noncausal_d<64, false>(a, why);
 }
 
 }  // namespace la

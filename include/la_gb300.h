@@ -132,6 +132,35 @@ la_status la_decode_step(const void *q, const void *k, const void *v, int dtype,
                          const float *log_alpha, float *S, void *o, void *cuda_stream);
 
 /*
+ * The non-causal matrix form, for B*H independent sequences of L tokens:
+ *
+ *     S = phi(K)^T V  (summed over all L tokens) ;   O = phi(Q) S
+ *
+ * (page "adv13 - Linear Attention / SSM", section 4.3, linear_attention_matrix;
+ * page "CS336 lecture 4, code 1: linear attention", demo_associativity: the
+ * order (Q K^T) V = Q (K^T V)).  Every token reads the same state: there is no
+ * causal mask, no decay and no initial state.  The feature map is the one set
+ * by la_set_feature_map.
+ *
+ *   q, k       [B,H,L,d] bf16                          (read)
+ *   v          [B,H,L,d] bf16                          (read)
+ *   O          [B,H,L,d] bf16                          (write)
+ *   S          [B,H,d,d] fp32, the state phi(K)^T V, or NULL (write)
+ *   workspace  device scratch of la_noncausal_fwd_workspace_bytes(...) bytes
+ *
+ * All pointers are device pointers owned by the caller, row-major and
+ * 16-byte aligned; the call is asynchronous on `cuda_stream`.
+ * Supported: bf16 with d_k = d_v = d in {64, 128}.  L = 0 writes S = 0.
+ * Errors: LA_ERR_INVALID_ARG (null or misaligned pointer, negative size,
+ * workspace too small), LA_ERR_UNSUPPORTED (another dtype or d), LA_ERR_CUDA.
+ */
+la_status la_noncausal_fwd(const void *q, const void *k, const void *v, int dtype,
+                           int B, int H, int L, int d_k, int d_v,
+                           void *O, float *S, void *workspace, size_t ws_bytes,
+                           void *cuda_stream);
+size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v);
+
+/*
  * la_chunk_fwd for callers that cannot allocate device memory.  (The pages
  * have no counterpart: this is a deployment variant of la_chunk_fwd.)
  *
