@@ -281,6 +281,56 @@ def bench_prefill(w, steps, warmup, dev, peaks, peak_kind, min_warmup_s=1.0):
             "set_bytes": set_bytes}
 
 
+def noncausal_bytes(w) -> int:
+    """Bytes the non-causal form must move: q, k, v read and O written once,
+    and the state phi(K)^T V written."""
+    e = ELT[w.dtype]
+    n = w.B * w.H * w.L
+    return n * (2 * w.dk + 2 * w.dv) * e + w.B * w.H * w.dk * w.dv * 4
+
+
+def bench_noncausal(w, steps, warmup, dev, peaks, peak_kind):
+    """la_noncausal_fwd on the shape (and phi) of prefill workload ``w``, its
+    decay and initial state dropped: the form has neither."""
+    from causal_linear_attention_chunkwise_gb300 import api
+    api.la_set_feature_map(w.phi)
+    set_bytes = noncausal_bytes(w)
+    n_sets = min(16, max(2, math.ceil(3 * L2_BYTES / set_bytes)))
+    sets = []
+    for i in range(n_sets):
+        d = _dev_inputs(W.make_prefill_inputs(w, seed=i), dev)
+        d["O"] = torch.empty(w.B, w.H, w.L, w.dv, dtype=d["q"].dtype, device=dev)
+        d["S"] = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+        sets.append(d)
+    ws = torch.empty(max(api.la_noncausal_fwd_workspace_bytes(w.B, w.H, w.L, w.dk, w.dv), 16),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        s = sets[i % n_sets]
+        api.la_noncausal_fwd(s["q"], s["k"], s["v"], O=s["O"], S=s["S"], workspace=ws,
+                             stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    api.la_device_status()
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for j in range(steps):
+        starts[j].record(stream)
+        step(warmup + j)
+        ends[j].record(stream)
+    torch.cuda.synchronize(dev)
+    api.la_device_status()
+    per_call_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    flops = 4 * w.B * w.H * w.L * w.dk * w.dv  # phi(K)^T V and phi(Q) S
+    rl = roofline(set_bytes, flops, per_call_ms / 1e3, peaks, peak_kind, False)
+    rl["kernel"] = "la_noncausal_fwd call (all its kernels)"
+    rl["traffic"] = traffic_from_profiles(f"noncausal:{w.name}")
+    return per_call_ms, rl
+
+
 def bench_prefill_e2e(w, steps, dev):
     """Same metric with host buffers: pinned Q/K/V (+gate, S0) copied in and
     O and S_final copied out inside the timed region, every step."""
@@ -468,6 +518,11 @@ def run_profile(args):
         r = bench_prefill(w, args.steps, args.warmup, dev, peaks, peak_kind, min_warmup_s=0.0)
         print(json.dumps({"profile": "prefill", "workload": w.name,
                           "per_call_ms": round(r["per_call_ms"], 5), "roofline": r["roofline"]}))
+    elif args.profile == "noncausal":
+        w = W.PREFILL[args.workload]
+        per, rl = bench_noncausal(w, args.steps, args.warmup, dev, peaks, peak_kind)
+        print(json.dumps({"profile": "noncausal", "workload": w.name, "per_call_ms": round(per, 5),
+                          "roofline": rl}))
     else:
         dw, _, per, rl = bench_decode(args.steps, args.warmup, dev, peaks, peak_kind)
         print(json.dumps({"profile": "decode", "workload": dw.name, "per_step_ms": round(per, 5),
@@ -529,7 +584,7 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.PREFILL))
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--profile", choices=["prefill", "decode"], default=None,
+    p.add_argument("--profile", choices=["prefill", "decode", "noncausal"], default=None,
                    help="run one leg only (for ncu captures); prints no benchmark line")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps

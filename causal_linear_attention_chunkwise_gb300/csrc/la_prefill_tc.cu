@@ -1617,9 +1617,12 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
 // linear_attention_matrix; "CS336 lecture 4, code 1", demo_associativity).
 // S comes from the segment-state kernel run over every chunk and summed by
 // the scan into the sequence's last workspace slot.  This kernel reads S once
-// per CTA as the bf16 B operand of O_c = phi(Q_c) S and streams the CTA's
-// chunks of Q to O.  One warpgroup: thread 0 issues the TMA loads, the MMAs
-// and the stores; all 128 threads apply phi and run the epilogue.
+// per sequence as the bf16 B operand of O_c = phi(Q_c) S and streams Q to O.
+// The grid is a fixed number of blocks per SM; block j takes the j-th equal
+// run of the (b,h)-major list of all chunks, so every SM gets the same share
+// (a run may cross into the next sequence, which reloads S).  One warpgroup:
+// thread 0 issues the TMA loads, the MMAs and the stores; all 128 threads
+// apply phi and run the epilogue.
 template <int D>
 struct NcSmem {
   static constexpr int NQ = 3;                    // Q stages
@@ -1648,9 +1651,11 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   uint64_t *mma_done = full + NQ;
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y;
-  const int c0 = blockIdx.x * chunks_per_cta;
-  const int n = max(0, min(chunks_per_cta, p.n_chunks - c0));
+  const long total = (long)p.BH * p.n_chunks;
+  const long g0 = (long)blockIdx.x * chunks_per_cta;
+  const int n = (int)max(0L, min((long)chunks_per_cta, total - g0));
+  auto item_bh = [&](int i) { return (int)((g0 + i) / p.n_chunks); };
+  auto item_c = [&](int i) { return (int)((g0 + i) % p.n_chunks); };
   if (tid == 0) {
     for (int s = 0; s < NQ; ++s) mbar_init(&full[s], 1);
     mbar_init(mma_done, 1);
@@ -1667,11 +1672,11 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   const uint32_t tmem = ctl->tmem_base;
   int issued = 0;  // thread 0: Q tiles requested
   auto load_q = [&](int i) {
-    const int s = i % NQ;
+    const int s = i % NQ, bh = item_bh(i), tok = item_c(i) * CH;
     mbar_arrive_expect_tx(&full[s], SM::TILE);
     for (int b = 0; b < D / BOX; ++b)
-      if (LA_CHK((c0 + i) * CH < p.L && bh < p.BH, KID_NONCAUSAL, 3))
-        tma_load_3d(smem + s * SM::TILE + b * BOX_BYTES, &tmQ, &full[s], b * BOX, (c0 + i) * CH, bh);
+      if (LA_CHK(tok < p.L && bh < p.BH, KID_NONCAUSAL, 3))
+        tma_load_3d(smem + s * SM::TILE + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
     issued = i + 1;
   };
   if (tid == 0) {
@@ -1679,11 +1684,13 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     tma_prefetch_desc(&tmO);
     for (int i = 0; i < min(n, NQ); ++i) load_q(i);  // Q does not depend on S
   }
-  // S, the scan's last slot of this sequence, is written by the kernel before
-  // this one (a programmatic dependent launch): wait for it, then convert it
-  // to the bf16 B operand, MN-major with the 128-byte swizzle.
+  // S, the scan's last slot of a sequence, is written by the kernel before
+  // this one (a programmatic dependent launch): wait for it once.  load_s
+  // converts sequence bh's S to the bf16 B operand, MN-major with the
+  // 128-byte swizzle; every thread calls it, after every MMA that read the
+  // previous S has completed.
   pdl_wait_previous();
-  {
+  auto load_s = [&](int bh) {
     const float *S = p.ws_state + ((size_t)bh * p.n_seg + (p.n_seg - 1)) * D * D;
     unsigned char *sb = smem + SM::OFF_S;
     for (int idx = tid; idx < D * D / 8; idx += kNcThreads) {
@@ -1696,8 +1703,9 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                      pack_bf16(y.z, y.w));
     }
     fence_proxy_async_smem();
-  }
-  __syncthreads();
+    __syncthreads();
+  };
+  int s_bh = -1;  // the sequence whose S is in shared memory
   constexpr uint32_t HI = smem_desc_sw128_hi(1024);
   constexpr uint32_t idesc = idesc_bf16_f32(64, D, false, true);
   const uint32_t sbase = smem_u32(smem);
@@ -1717,6 +1725,10 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       break;
     }
     consumed = i + 1;
+    if (item_bh(i) != s_bh) {
+      s_bh = item_bh(i);
+      load_s(s_bh);
+    }
     if constexpr (PHI) {
       tile_pass<D, 1, true, false>(smem + s * SM::TILE, [](int, int) { return 1.f; }, tid,
                                    kNcThreads);
@@ -1769,7 +1781,7 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     tc_fence_before();
     named_bar_sync(BAR_NC, kNcThreads);
     if (tid == 0) {
-      const int tok = (c0 + i) * CH;
+      const int tok = item_c(i) * CH, bh = item_bh(i);
       for (int bb = 0; bb < D / BOX; ++bb)
         if (LA_CHK(tok < p.L && bh < p.BH, KID_NONCAUSAL, 4))
           tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok, bh);
@@ -1799,7 +1811,7 @@ Plan make_noncausal_plan(int B, int H, int L) {
   const int nc = (L + CH - 1) / CH;
   const int bh = std::max(1, B * H);
   int ns = std::max((nc + kMaxSegChunks - 1) / kMaxSegChunks,
-                    std::min(nc, (2 * sm_count() + bh - 1) / bh));
+                    std::min(nc, std::max(1, 2 * sm_count() / bh)));  // one wave at 2 per SM
   const int g = (nc + ns - 1) / ns;
   ns = (nc + g - 1) / g;
   return Plan{nc, g, ns};
@@ -1857,10 +1869,10 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
   static int smem_set_nc[64];
   if ((e = set_smem_once(kn, NS_::BYTES, smem_set_nc)) != cudaSuccess) return e;
   const int per_sm = D == 64 ? 4 : 2;  // blocks per SM that fit in shared memory
-  const long total = (long)pl.n_chunks * BH;
-  const int cpc = (int)std::max(1L, (total + (long)per_sm * sm_count() - 1) / ((long)per_sm * sm_count()));
-  const int nx = (pl.n_chunks + cpc - 1) / cpc;
-  e = launch_pdl(kn, dim3(nx, BH), kNcThreads, NS_::BYTES, a.stream, tq, to, p, cpc);
+  const long total = (long)pl.n_chunks * BH, slots_all = (long)per_sm * sm_count();
+  const int cpc = (int)std::max(1L, (total + slots_all - 1) / slots_all);
+  const int nx = (int)((total + cpc - 1) / cpc);
+  e = launch_pdl(kn, dim3(nx), kNcThreads, NS_::BYTES, a.stream, tq, to, p, cpc);
   if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
     if (why) *why = "la_noncausal_fwd: output kernel launch";
     return e;
