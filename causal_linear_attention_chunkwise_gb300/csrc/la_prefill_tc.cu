@@ -30,7 +30,14 @@
 //       S_in[s]; the last segment also writes S_final.
 // With NS = 1 only the output kernel runs.  The associative combination of
 // (decay, state) pairs across segments is the same state passing the chunk
-// loop performs across chunks.
+// loop performs across chunks.  The scan and the output kernel are
+// programmatic dependent launches: each may start while the kernel before it
+// runs, and waits for it (griddepcontrol.wait) before reading what it wrote.
+//
+// The non-causal form O = phi(Q) (phi(K)^T V) ("adv13 - Linear Attention /
+// SSM" section 4.3) reuses the segment-state kernel over every chunk and the
+// scan, which sums the segments into one extra slot, then runs
+// noncausal_output_kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
