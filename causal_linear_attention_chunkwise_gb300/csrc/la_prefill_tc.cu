@@ -695,14 +695,16 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y, h = bh % p.H;
+  // Grid (B*H, segment pairs or segments): blocks launch segment by segment,
+  // so the shorter last segments of every sequence come last.
+  const int bh = blockIdx.x, h = bh % p.H;
   const size_t bhL = (size_t)bh * p.L;
   // Segments of this CTA (one for d = 128).
   Streams st;
   int tok0[2], seg[2];
   const float *S_seg[2];
   for (int sg = 0; sg < 2; ++sg) {
-    seg[sg] = PAIRS ? 2 * (int)blockIdx.x + sg : (sg == 0 ? (int)blockIdx.x : p.n_seg);
+    seg[sg] = PAIRS ? 2 * (int)blockIdx.y + sg : (sg == 0 ? (int)blockIdx.y : p.n_seg);
     const int c0 = seg[sg] * p.seg_chunks;
     st.nc[sg] = seg[sg] < p.n_seg ? min(p.seg_chunks, p.n_chunks - c0) : 0;
     tok0[sg] = c0 * CH;
@@ -1605,9 +1607,9 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   // (its inputs were complete before the segment-state kernel started).  A
   // single segment has no predecessor of its own: ordinary stream order.
   if (pl.n_seg > 1)
-    e = launch_pdl(ko, dim3(out_x, BH), kThreadsOut, OS::BYTES, a.stream, tq, tk, tv, to, p);
+    e = launch_pdl(ko, dim3(BH, out_x), kThreadsOut, OS::BYTES, a.stream, tq, tk, tv, to, p);
   else
-    ko<<<dim3(out_x, BH), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
+    ko<<<dim3(BH, out_x), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
   if ((e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) && why)
     *why = "la_chunk_fwd: chunk-output kernel launch";
 #ifdef LA_CHECKED
