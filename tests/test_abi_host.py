@@ -87,3 +87,37 @@ def test_workspace_query_is_host_only(lib):
                  (1, 1, 300, 16, 16, 64, 0), (0, 1, 10, 64, 64, 64, 1)]:
         n = lib.la_chunk_fwd_workspace_bytes(*args)
         assert n >= 0
+
+
+def test_noncausal_validation_and_workspace(lib):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    # fp32, mismatched or unsupported head sizes: unsupported
+    assert lib.la_noncausal_fwd(p, p, p, 0, 1, 1, 64, 64, 64, p, None, p, 1 << 20, None) == 2
+    assert lib.la_noncausal_fwd(p, p, p, 1, 1, 1, 64, 64, 128, p, None, p, 1 << 20, None) == 2
+    assert lib.la_noncausal_fwd(p, p, p, 1, 1, 1, 64, 32, 32, p, None, p, 1 << 20, None) == 2
+    assert b"bf16" in lib.la_last_error()
+    # unknown dtype, negative size, null tensors, misaligned pointer
+    assert lib.la_noncausal_fwd(p, p, p, 5, 1, 1, 64, 64, 64, p, None, p, 1 << 20, None) == 1
+    assert lib.la_noncausal_fwd(p, p, p, 1, 1, 1, -3, 64, 64, p, None, p, 1 << 20, None) == 1
+    assert lib.la_noncausal_fwd(None, p, p, 1, 1, 1, 64, 64, 64, p, None, p, 1 << 20, None) == 1
+    assert lib.la_noncausal_fwd(ctypes.c_void_p(0x1004), p, p, 1, 1, 1, 64, 64, 64, p, None, p,
+                                1 << 20, None) == 1
+    # workspace too small or missing
+    need = lib.la_noncausal_fwd_workspace_bytes(2, 3, 1000, 64, 64)
+    assert need > 0
+    assert lib.la_noncausal_fwd(p, p, p, 1, 2, 3, 1000, 64, 64, p, None, p, need - 1, None) == 1
+    assert b"workspace" in lib.la_last_error()
+    assert lib.la_noncausal_fwd(p, p, p, 1, 2, 3, 1000, 64, 64, p, None, None, 0, None) == 1
+    # the workspace holds one fp32 d x d state per segment and sequence plus the
+    # sum slot, then one log decay per slot (256-byte aligned); segments are at
+    # most 32 chunks
+    for B, H, L, d in [(1, 1, 1, 64), (4, 16, 4096, 64), (2, 32, 8192, 128), (1, 16, 32768, 128)]:
+        ws = lib.la_noncausal_fwd_workspace_bytes(B, H, L, d, d)
+        bh, nc = B * H, (L + 63) // 64
+        slots = [n for n in range(2, nc + 2)
+                 if bh * n * d * d * 4 + (bh * n * 4 + 255) // 256 * 256 == ws]
+        assert len(slots) == 1, (B, H, L, d, ws)
+        assert -(-nc // (slots[0] - 1)) <= 32
+    assert lib.la_noncausal_fwd_workspace_bytes(1, 1, 64, 64, 128) == 0
+    # empty batch is a no-op
+    assert lib.la_noncausal_fwd(p, p, p, 1, 0, 4, 64, 64, 64, p, None, None, 0, None) == 0
