@@ -333,38 +333,58 @@ def bench_noncausal(w, steps, warmup, dev, peaks, peak_kind):
 
 def bench_prefill_e2e(w, steps, dev):
     """Same metric with host buffers: pinned Q/K/V (+gate, S0) copied in and
-    O and S_final copied out inside the timed region, every step."""
+    O and S_final copied out inside the timed region, every step.  The
+    copies are pipelined the way a streaming caller would run them: two sets
+    of device buffers, inputs copied in on one stream while the previous
+    step computes, results copied out on a third while the next step's
+    inputs copy in.  The timed region runs from the first copy in to the
+    last copy out."""
     from causal_linear_attention_chunkwise_gb300 import api
     api.la_set_feature_map(w.phi)
     host = W.make_prefill_inputs(w, seed=0)
     h_in = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in host.items()}
-    d_in = _dev_inputs(host, dev)
-    O_d = torch.empty(w.B, w.H, w.L, w.dv, dtype=d_in["q"].dtype, device=dev)
-    S_d = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
-    O_h = torch.empty(O_d.shape, dtype=O_d.dtype, pin_memory=True)
-    S_h = torch.empty(S_d.shape, dtype=S_d.dtype, pin_memory=True)
-    stream = torch.cuda.current_stream(dev)
     names = [k for k in ("q", "k", "v", "decay", "S0") if torch.is_tensor(h_in.get(k))]
+    comp = torch.cuda.current_stream(dev)
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    sets = []
+    for _ in range(2):
+        d = _dev_inputs(host, dev)
+        d["O"] = torch.empty(w.B, w.H, w.L, w.dv, dtype=d["q"].dtype, device=dev)
+        d["S"] = torch.empty(w.B, w.H, w.dk, w.dv, dtype=torch.float32, device=dev)
+        d["in_done"], d["comp_done"], d["out_done"] = (torch.cuda.Event() for _ in range(3))
+        sets.append(d)
+    O_h = torch.empty(sets[0]["O"].shape, dtype=sets[0]["O"].dtype, pin_memory=True)
+    S_h = torch.empty(sets[0]["S"].shape, dtype=torch.float32, pin_memory=True)
     h2d = sum(h_in[k].numel() * h_in[k].element_size() for k in names)
     d2h = O_h.numel() * O_h.element_size() + S_h.numel() * S_h.element_size()
 
-    def step():
-        for k in names:
-            d_in[k].copy_(h_in[k], non_blocking=True)
-        api.la_chunk_fwd(d_in["q"], d_in["k"], d_in["v"], w.chunk, d_in["decay_kind"],
-                         d_in["decay"], d_in["S0"], O=O_d, S_final=S_d, stream=stream)
-        O_h.copy_(O_d, non_blocking=True)
-        S_h.copy_(S_d, non_blocking=True)
+    def step(i):
+        d = sets[i % 2]
+        cin.wait_event(d["comp_done"])  # step i - 2 has read this set's inputs
+        with torch.cuda.stream(cin):
+            for k in names:
+                d[k].copy_(h_in[k], non_blocking=True)
+        d["in_done"].record(cin)
+        comp.wait_event(d["in_done"])
+        comp.wait_event(d["out_done"])  # step i - 2's results have been copied out
+        api.la_chunk_fwd(d["q"], d["k"], d["v"], w.chunk, d["decay_kind"], d["decay"], d["S0"],
+                         O=d["O"], S_final=d["S"], stream=comp)
+        d["comp_done"].record(comp)
+        cout.wait_event(d["comp_done"])
+        with torch.cuda.stream(cout):
+            O_h.copy_(d["O"], non_blocking=True)
+            S_h.copy_(d["S"], non_blocking=True)
+        d["out_done"].record(cout)
 
-    for _ in range(3):
-        step()
+    for i in range(3):
+        step(i)
     torch.cuda.synchronize(dev)
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(cin)
+    for i in range(steps):
+        step(3 + i)
+    b.record(cout)
     torch.cuda.synchronize(dev)
     barrier()
     api.la_device_status()
