@@ -121,3 +121,26 @@ def test_noncausal_validation_and_workspace(lib):
     assert lib.la_noncausal_fwd_workspace_bytes(1, 1, 64, 64, 128) == 0
     # empty batch is a no-op
     assert lib.la_noncausal_fwd(p, p, p, 1, 0, 4, 64, 64, 64, p, None, None, 0, None) == 0
+
+
+def test_prefill_plan_invariants(lib):
+    """The tensor-core launcher's segment plan, seen through the workspace query: segments of at
+    most 32 chunks, at most one per chunk, and three kernels exactly when a workspace is used."""
+    for B, H, L in [(1, 1, 64), (1, 1, 100), (4, 16, 4096), (2, 32, 8192), (1, 16, 32768),
+                    (8, 32, 32768), (1, 2, 6000), (2, 4, 3000), (64, 64, 512), (1, 1, 1 << 17)]:
+        for d in (64, 128):
+            ws = lib.la_chunk_fwd_workspace_bytes(B, H, L, d, d, 64, 1)
+            kernels = lib.la_chunk_fwd_kernel_count(B, H, L, d, d, 64, 1)
+            bh, nc = B * H, (L + 63) // 64
+            if ws == 0:
+                assert kernels == 1 and nc <= 32, (B, H, L, d)
+                continue
+            assert kernels == 3
+            ns = [n for n in range(2, nc + 1)
+                  if bh * n * d * d * 4 + (bh * n * 4 + 255) // 256 * 256 == ws]
+            assert len(ns) == 1, (B, H, L, d, ws)
+            g = -(-nc // ns[0])
+            assert g <= 32 and -(-nc // g) == ns[0], (B, H, L, d, ns[0])
+    # fp32 and other shapes take the SIMT path: no workspace
+    assert lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 0) == 0
+    assert lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 32, 32, 64, 1) == 0
