@@ -545,15 +545,11 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
 // d = 128: one segment per CTA and one 128-column chain, computed transposed
 //   so that every product has M = 128: S^T += V^T K, O^T = S^T Q^T (A, the
 //   bf16 copy of S^T, read from TMEM) and O^T += V^T P^T.  The state hand-over
-//   then stays in TMEM.  (Building with LA_D128_CHAINS=2 restores the older
-//   untransposed form with two 64-column half-chains.)
-#ifndef LA_D128_CHAINS
-#define LA_D128_CHAINS 1
-#endif
+//   then stays in TMEM.
 template <int DK>
 struct OutSmem {
   static constexpr bool PAIRS = DK == 64;                       // two segments per CTA
-  static constexpr int NCHAIN = PAIRS ? 2 : LA_D128_CHAINS;     // state chains
+  static constexpr int NCHAIN = PAIRS ? 2 : 1;                  // state chains
   static constexpr int CW = PAIRS ? 64 : DK / NCHAIN;           // state columns per chain
   // d = 128 keeps the output and the state transposed in TMEM (see the kernel):
   // its bf16 state copy lives in TMEM, not in shared memory.
