@@ -80,8 +80,11 @@ def _bind(lib):
     lib.oracle_recurrent.argtypes = sig
     lib.oracle_parallel.argtypes = sig
     lib.oracle_noncausal.argtypes = sig
+    lib.oracle_normalised.argtypes = [i, i, i, i, i, dp, dp, dp, i, i, dp, dp, dp, dp, dp, dp]
+    lib.oracle_channel_gate.argtypes = [i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp]
     lib.oracle_chunkwise.argtypes = [i, i, i, i, i, i, dp, dp, dp, i, i, dp, dp, dp, dp]
-    for f in (lib.oracle_recurrent, lib.oracle_parallel, lib.oracle_chunkwise, lib.oracle_noncausal):
+    for f in (lib.oracle_recurrent, lib.oracle_parallel, lib.oracle_chunkwise, lib.oracle_noncausal,
+              lib.oracle_normalised, lib.oracle_channel_gate):
         f.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
@@ -182,6 +185,37 @@ def noncausal(q, k, v, phi="identity", lib=None):
     """Non-causal matrix form O = phi(Q) (phi(K)^T V); returns (O, S) with S
     = phi(K)^T V, the state every token reads."""
     return _run("oracle_noncausal", q, k, v, phi, "none", None, None, lib=lib)
+
+
+def normalised(q, k, v, phi="elu1", decay_kind="none", decay=None, S0=None, z0=None, lib=None):
+    """Normalised form o_t = phi(q_t)^T S_t / phi(q_t)^T z_t, with z the state of
+    a value column of ones; returns (O, S_final, z_final)."""
+    q, k, v, p, dkind, decay, S0, (B, H, L, dk, dv) = _prepare(q, k, v, phi, decay_kind, decay, S0)
+    z0 = _f64(z0)
+    if z0 is not None and z0.shape != (B, H, dk):
+        raise ValueError("z0 must be [B,H,dk]")
+    O, Sf, zf = np.zeros((B, H, L, dv)), np.zeros((B, H, dk, dv)), np.zeros((B, H, dk))
+    rc = (lib or load_library()).oracle_normalised(
+        B, H, L, dk, dv, _ptr(q), _ptr(k), _ptr(v), p, dkind, _ptr(decay), _ptr(S0), _ptr(z0),
+        _ptr(O), _ptr(Sf), _ptr(zf))
+    if rc != 0:
+        raise RuntimeError(f"oracle_normalised failed with code {rc}")
+    return O, Sf, zf
+
+
+def channel_gate(q, k, v, log_alpha, phi="identity", S0=None, lib=None):
+    """Per-channel gate S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T, with
+    log_alpha [B,H,L,dk]; returns (O, S_final)."""
+    q, k, v, p, _, _, S0, (B, H, L, dk, dv) = _prepare(q, k, v, phi, "none", None, S0)
+    la = _f64(log_alpha)
+    if la.shape != (B, H, L, dk):
+        raise ValueError("log_alpha must be [B,H,L,dk]")
+    O, Sf = np.zeros((B, H, L, dv)), np.zeros((B, H, dk, dv))
+    rc = (lib or load_library()).oracle_channel_gate(
+        B, H, L, dk, dv, _ptr(q), _ptr(k), _ptr(v), p, _ptr(la), _ptr(S0), _ptr(O), _ptr(Sf))
+    if rc != 0:
+        raise RuntimeError(f"oracle_channel_gate failed with code {rc}")
+    return O, Sf
 
 
 def decode(q, k, v, S0, log_alpha=None, phi="elu1", lib=None):

@@ -47,6 +47,16 @@
  *       "CS336 lecture 4, code 1", demo_associativity: (Q K^T) V = Q (K^T V).
  *       Every token reads the same S, the state after the last token.
  *
+ *   oracle_normalised  the normalised form, a "next" row
+ *       "Linear / sparse attention tutorial" Q11: o_t = phi(q_t)^T S_t /
+ *           (phi(q_t)^T z_t), z_t the running sum of phi(k_j); section 2.2:
+ *           z_t is the state of one extra value column of ones, so it decays
+ *           with S: z_t = a_t z_{t-1} + phi(k_t).
+ *
+ *   oracle_channel_gate  the per-channel (diagonal) gate, a "next" row
+ *       "Linear / sparse attention tutorial" Q21 (GLA):
+ *           S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T, alpha_t in (0,1]^dk.
+ *
  * Decay is given per token in log space, lambda_t = log(decay factor):
  *   kind 0  none                  lambda_t = 0
  *   kind 1  per head  [H]         lambda_t = log_gamma[h]          (RetNet)
@@ -315,6 +325,104 @@ int oracle_noncausal(int B, int H, int L, int dk, int dv,
         }
         if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
         free(S); free(f);
+    }
+    return err ? -2 : 0;
+}
+
+/* The normalised form, token by token:
+ *     S <- a_t S + phi(k_t) v_t^T ;  z <- a_t z + phi(k_t)
+ *     o_t = phi(q_t)^T S / (phi(q_t)^T z)
+ * z0 [B,H,dk] may be NULL (zero); z_final [B,H,dk] may be NULL.  A zero
+ * denominator gives inf or NaN, as the formula does. */
+int oracle_normalised(int B, int H, int L, int dk, int dv,
+                      const double *q, const double *k, const double *v,
+                      int phi, int kind, const double *decay,
+                      const double *S0, const double *z0,
+                      double *O, double *S_final, double *z_final)
+{
+    if (check_args(B, H, L, dk, dv, phi, kind, decay)) return -1;
+    int err = 0;
+    long nseq = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (long bh = 0; bh < nseq; ++bh) {
+        int b = (int)(bh / H), h = (int)(bh % H);
+        double *S = malloc(sizeof(double) * (size_t)dk * dv);
+        double *z = malloc(sizeof(double) * (size_t)dk);
+        double *kf = malloc(sizeof(double) * (size_t)dk);
+        double *qf = malloc(sizeof(double) * (size_t)dk);
+        if (!S || !z || !kf || !qf) { free(S); free(z); free(kf); free(qf); err |= 1; continue; }
+        if (S0) memcpy(S, S0 + (size_t)bh * dk * dv, sizeof(double) * (size_t)dk * dv);
+        else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+        if (z0) memcpy(z, z0 + (size_t)bh * dk, sizeof(double) * (size_t)dk);
+        else memset(z, 0, sizeof(double) * (size_t)dk);
+        for (int t = 0; t < L; ++t) {
+            const double *qt = q + ((size_t)bh * L + t) * dk;
+            const double *kt = k + ((size_t)bh * L + t) * dk;
+            const double *vt = v + ((size_t)bh * L + t) * dv;
+            double a = exp(log_decay(kind, decay, H, L, b, h, t));
+            for (int i = 0; i < dk; ++i) kf[i] = feature(phi, kt[i]);
+            for (int i = 0; i < dk; ++i) {
+                for (int j = 0; j < dv; ++j)
+                    S[(size_t)i * dv + j] = a * S[(size_t)i * dv + j] + kf[i] * vt[j];
+                z[i] = a * z[i] + kf[i];
+            }
+            for (int i = 0; i < dk; ++i) qf[i] = feature(phi, qt[i]);
+            double den = 0.0;
+            for (int i = 0; i < dk; ++i) den += qf[i] * z[i];
+            double *ot = O + ((size_t)bh * L + t) * dv;
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += qf[i] * S[(size_t)i * dv + j];
+                ot[j] = acc / den;
+            }
+        }
+        if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+        if (z_final) memcpy(z_final + (size_t)bh * dk, z, sizeof(double) * (size_t)dk);
+        free(S); free(z); free(kf); free(qf);
+    }
+    return err ? -2 : 0;
+}
+
+/* The per-channel gate, token by token:
+ *     S[i,:] <- alpha_t[i] S[i,:] + phi(k_t)[i] v_t^T ;   o_t = phi(q_t)^T S
+ * log_alpha [B,H,L,dk] holds log alpha_t[i] (<= 0). */
+int oracle_channel_gate(int B, int H, int L, int dk, int dv,
+                        const double *q, const double *k, const double *v,
+                        int phi, const double *log_alpha,
+                        const double *S0, double *O, double *S_final)
+{
+    if (check_args(B, H, L, dk, dv, phi, 0, NULL) || !log_alpha) return -1;
+    int err = 0;
+    long nseq = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (long bh = 0; bh < nseq; ++bh) {
+        double *S = malloc(sizeof(double) * (size_t)dk * dv);
+        double *kf = malloc(sizeof(double) * (size_t)dk);
+        double *qf = malloc(sizeof(double) * (size_t)dk);
+        if (!S || !kf || !qf) { free(S); free(kf); free(qf); err |= 1; continue; }
+        if (S0) memcpy(S, S0 + (size_t)bh * dk * dv, sizeof(double) * (size_t)dk * dv);
+        else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+        for (int t = 0; t < L; ++t) {
+            const double *qt = q + ((size_t)bh * L + t) * dk;
+            const double *kt = k + ((size_t)bh * L + t) * dk;
+            const double *vt = v + ((size_t)bh * L + t) * dv;
+            const double *la = log_alpha + ((size_t)bh * L + t) * dk;
+            for (int i = 0; i < dk; ++i) kf[i] = feature(phi, kt[i]);
+            for (int i = 0; i < dk; ++i) {
+                const double a = exp(la[i]);
+                for (int j = 0; j < dv; ++j)
+                    S[(size_t)i * dv + j] = a * S[(size_t)i * dv + j] + kf[i] * vt[j];
+            }
+            for (int i = 0; i < dk; ++i) qf[i] = feature(phi, qt[i]);
+            double *ot = O + ((size_t)bh * L + t) * dv;
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += qf[i] * S[(size_t)i * dv + j];
+                ot[j] = acc;
+            }
+        }
+        if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+        free(S); free(kf); free(qf);
     }
     return err ? -2 : 0;
 }

@@ -17,7 +17,11 @@ planted mistake) and raises AssertionError when the oracle disagrees with:
 * the resume invariant: running [0, m) then [m, L) from the carried state
   equals one run over [0, L);
 * for the non-causal form: the causal final state and last row, the n x n
-  association order, one-hot values and L = 0 (``pin_noncausal``).
+  association order, one-hot values and L = 0 (``pin_noncausal``);
+* for the normalised form and the per-channel gate (rows the library does not
+  build yet): the ratio of two plain recurrences, constant values, one token;
+  equal-channel and zero gates, and an O(L^2) form written with numpy
+  (``pin_normalised``, ``pin_channel_gate``).
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in a copy of the
 oracle's C source and checks that at least one pin fails for each.
@@ -304,6 +308,74 @@ def pin_noncausal(lib):
     _close(S, np.zeros((B, H, dk, dv)), 0.0, "noncausal L=0 state")
 
 
+def pin_normalised(lib):
+    """The normalised form ("Linear / sparse attention tutorial" Q11, section 2.2):
+    - it is the ratio of two runs of the plain recurrence, one with v and one with a
+      value column of ones (z0 as that column's initial state), decay and S0 included;
+    - with phi = elu + 1 and the same value vector c at every token (S0 = z0 c^T), every
+      output is c: a convex combination of equal vectors;
+    - one token from zero state gives o = v;
+    - z_final is the ones column's final state."""
+    r = _rng(13)
+    B, H, L, dk, dv = 2, 2, 29, 5, 3
+    q, k, v = r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dv))
+    g = r.normal(size=(B, H, L))
+    z0 = r.uniform(0.1, 1.0, size=(B, H, dk))
+    S0 = r.normal(size=(B, H, dk, dv)) * 0.1
+    for phi in ("identity", "elu1"):
+        O, S, z = oracle.normalised(q, k, v, phi=phi, decay_kind="logit", decay=g, S0=S0, z0=z0,
+                                    lib=lib)
+        num, Sn = oracle.recurrent(q, k, v, phi=phi, decay_kind="logit", decay=g, S0=S0, lib=lib)
+        den, Sd = oracle.recurrent(q, k, np.ones((B, H, L, 1)), phi=phi, decay_kind="logit",
+                                   decay=g, S0=z0[..., None], lib=lib)
+        _close(O, num / den, 1e-9, f"normalised = num / den/{phi}")
+        _close(S, Sn, 1e-12, f"normalised S/{phi}")
+        _close(z, Sd[..., 0], 1e-12, f"normalised z/{phi}")
+    c = r.normal(size=dv)
+    vc = np.broadcast_to(c, (B, H, L, dv)).copy()
+    O, _, _ = oracle.normalised(q, k, vc, phi="elu1", decay_kind="logit", decay=g,
+                                S0=z0[..., None] * c, z0=z0, lib=lib)
+    _close(O, vc, 1e-12, "normalised constant v")
+    O, _, _ = oracle.normalised(q[:, :, :1], k[:, :, :1], v[:, :, :1], phi="elu1", lib=lib)
+    _close(O, v[:, :, :1], 1e-12, "normalised one token")
+
+
+def pin_channel_gate(lib):
+    """The per-channel gate ("Linear / sparse attention tutorial" Q21, GLA):
+    - equal gates on every channel give the scalar per-token gate of the recurrence;
+    - gates of zero log give the plain additive recurrence;
+    - it equals the O(L^2) form written with numpy: o_t = sum_{s<=t} sum_i phi(q)_ti
+      phi(k)_si exp(cum_ti - cum_si) v_s + sum_i phi(q)_ti exp(cum_ti) S0[i,:], and
+      S_L[i,:] = exp(cum_Li) S0[i,:] + sum_s exp(cum_Li - cum_si) phi(k)_si v_s."""
+    r = _rng(14)
+    B, H, L, dk, dv = 2, 2, 23, 5, 4
+    q, k, v = r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dk)), r.normal(size=(B, H, L, dv))
+    S0 = r.normal(size=(B, H, dk, dv))
+    lam = -np.logaddexp(0.0, r.normal(size=(B, H, L)))
+    O, S = oracle.channel_gate(q, k, v, np.repeat(lam[..., None], dk, axis=-1), S0=S0, lib=lib)
+    Oc, Sc = oracle.recurrent(q, k, v, decay_kind="token", decay=lam, S0=S0, lib=lib)
+    _close(O, Oc, 1e-12, "channel gate, equal channels")
+    _close(S, Sc, 1e-12, "channel gate S, equal channels")
+    O, S = oracle.channel_gate(q, k, v, np.zeros((B, H, L, dk)), S0=S0, lib=lib)
+    Oc, Sc = oracle.recurrent(q, k, v, S0=S0, lib=lib)
+    _close(O, Oc, 1e-12, "channel gate, no decay")
+    la = -np.logaddexp(0.0, r.normal(size=(B, H, L, dk)) * 2)
+    for phi in ("identity", "elu1"):
+        O, S = oracle.channel_gate(q, k, v, la, phi=phi, S0=S0, lib=lib)
+        fq, fk = (q, k) if phi == "identity" else (_elu1(q), _elu1(k))
+        cum = np.cumsum(la, axis=2)                                         # [B,H,L,dk]
+        w = np.exp(cum[:, :, :, None, :] - cum[:, :, None, :, :])          # [B,H,t,s,dk]
+        mask = np.tril(np.ones((L, L)))[None, None, :, :, None]
+        scores = np.einsum("bhti,bhtsi,bhsi->bhts", fq, w * mask, fk)
+        ref = np.einsum("bhts,bhse->bhte", scores, v)
+        ref += np.einsum("bhti,bhie->bhte", fq * np.exp(cum), S0)
+        _close(O, ref, 1e-10, f"channel gate O(L^2) form/{phi}")
+        SL = np.exp(cum[:, :, -1, :])[..., None] * S0 + np.einsum(
+            "bhsi,bhse->bhie", fk * np.exp(cum[:, :, -1:, :] - cum), v)
+        _close(S, SL, 1e-10, f"channel gate final state/{phi}")
+
+
 PINS = [pin_golden, pin_closed_form_additive, pin_closed_form_constant_decay, pin_single_token,
         pin_one_hot, pin_orthonormal_keys, pin_chunk_invariance, pin_parallel_equals_recurrent,
-        pin_split_invariance, pin_library_pieces, pin_state_shape, pin_noncausal]
+        pin_split_invariance, pin_library_pieces, pin_state_shape, pin_noncausal, pin_normalised,
+        pin_channel_gate]

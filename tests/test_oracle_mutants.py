@@ -85,6 +85,15 @@ MUTANTS = [
     ("noncausal_phi_not_on_q",
      "for (int i = 0; i < dk; ++i) f[i] = feature(phi, qt[i]);",
      "for (int i = 0; i < dk; ++i) f[i] = qt[i];"),
+    ("normaliser_not_decayed",
+     "z[i] = a * z[i] + kf[i];",
+     "z[i] = z[i] + kf[i];"),
+    ("normaliser_uses_key",
+     "for (int i = 0; i < dk; ++i) den += qf[i] * z[i];",
+     "for (int i = 0; i < dk; ++i) den += kf[i] * z[i];"),
+    ("channel_gate_one_channel",
+     "const double a = exp(la[i]);",
+     "const double a = exp(la[0]);"),
 ]
 
 
