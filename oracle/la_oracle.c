@@ -57,6 +57,17 @@
  *       "Linear / sparse attention tutorial" Q21 (GLA):
  *           S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T, alpha_t in (0,1]^dk.
  *
+ *   oracle_delta  the (gated) delta rule, a "next" row
+ *       "Linear / Sparse Attention - minimal runnable implementation",
+ *           delta_rule_recurrent: S_t = S_{t-1}(I - beta_t k_t k_t^T) +
+ *           beta_t v_t k_t^T (S as [d_v, d_k]: erase along k, then write);
+ *       "Linear / sparse attention tutorial" Q21: the gated version also
+ *           multiplies the old state by alpha_t.  Here the state is kept as
+ *           its transpose, [d_k, d_v] like the others:
+ *           S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+ *           o_t = phi(q_t)^T S_t, with k_t = phi(k_t) as given (the page
+ *           assumes unit-norm keys; the caller normalises).
+ *
  * Decay is given per token in log space, lambda_t = log(decay factor):
  *   kind 0  none                  lambda_t = 0
  *   kind 1  per head  [H]         lambda_t = log_gamma[h]          (RetNet)
@@ -423,6 +434,57 @@ int oracle_channel_gate(int B, int H, int L, int dk, int dv,
         }
         if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
         free(S); free(kf); free(qf);
+    }
+    return err ? -2 : 0;
+}
+
+/* The gated delta rule, token by token, with the state as [d_k, d_v]:
+ *     S <- alpha_t (S - beta_t k (k^T S)) + beta_t k v_t^T ;  o_t = q^T S
+ * with k = phi(k_t), q = phi(q_t).  beta [B,H,L]; log_alpha [B,H,L] or NULL
+ * (alpha = 1). */
+int oracle_delta(int B, int H, int L, int dk, int dv,
+                 const double *q, const double *k, const double *v,
+                 int phi, const double *beta, const double *log_alpha,
+                 const double *S0, double *O, double *S_final)
+{
+    if (check_args(B, H, L, dk, dv, phi, 0, NULL) || !beta) return -1;
+    int err = 0;
+    long nseq = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (long bh = 0; bh < nseq; ++bh) {
+        double *S = malloc(sizeof(double) * (size_t)dk * dv);
+        double *kf = malloc(sizeof(double) * (size_t)dk);
+        double *qf = malloc(sizeof(double) * (size_t)dk);
+        double *ks = malloc(sizeof(double) * (size_t)dv);
+        if (!S || !kf || !qf || !ks) { free(S); free(kf); free(qf); free(ks); err |= 1; continue; }
+        if (S0) memcpy(S, S0 + (size_t)bh * dk * dv, sizeof(double) * (size_t)dk * dv);
+        else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+        for (int t = 0; t < L; ++t) {
+            const double *qt = q + ((size_t)bh * L + t) * dk;
+            const double *kt = k + ((size_t)bh * L + t) * dk;
+            const double *vt = v + ((size_t)bh * L + t) * dv;
+            const double bt = beta[(size_t)bh * L + t];
+            const double a = log_alpha ? exp(log_alpha[(size_t)bh * L + t]) : 1.0;
+            for (int i = 0; i < dk; ++i) kf[i] = feature(phi, kt[i]);
+            for (int j = 0; j < dv; ++j) {  /* k^T S, a row of d_v values */
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += kf[i] * S[(size_t)i * dv + j];
+                ks[j] = acc;
+            }
+            for (int i = 0; i < dk; ++i)
+                for (int j = 0; j < dv; ++j)
+                    S[(size_t)i * dv + j] = a * (S[(size_t)i * dv + j] - bt * kf[i] * ks[j]) +
+                                            bt * kf[i] * vt[j];
+            for (int i = 0; i < dk; ++i) qf[i] = feature(phi, qt[i]);
+            double *ot = O + ((size_t)bh * L + t) * dv;
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < dk; ++i) acc += qf[i] * S[(size_t)i * dv + j];
+                ot[j] = acc;
+            }
+        }
+        if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+        free(S); free(kf); free(qf); free(ks);
     }
     return err ? -2 : 0;
 }

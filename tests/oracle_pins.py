@@ -21,7 +21,10 @@ planted mistake) and raises AssertionError when the oracle disagrees with:
 * for the normalised form and the per-channel gate (rows the library does not
   build yet): the ratio of two plain recurrences, constant values, one token;
   equal-channel and zero gates, and an O(L^2) form written with numpy
-  (``pin_normalised``, ``pin_channel_gate``).
+  (``pin_normalised``, ``pin_channel_gate``);
+* for the delta rule: the page's checks [d]/[e] (orthonormal keys give the
+  additive rule, random keys do not), exact retrieval of the value just
+  written, beta = 0, one token (``pin_delta``).
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in a copy of the
 oracle's C source and checks that at least one pin fails for each.
@@ -375,7 +378,49 @@ def pin_channel_gate(lib):
         _close(S, SL, 1e-10, f"channel gate final state/{phi}")
 
 
+def pin_delta(lib):
+    """The (gated) delta rule ("Linear / Sparse Attention - minimal runnable
+    implementation", delta_rule_recurrent and its checks [d], [e]):
+    - orthonormal keys with beta = 1 give the additive recurrence (check [e]), and
+      random unit keys do not;
+    - reading with the key just written (unit norm, beta = 1) returns exactly its
+      value whatever the history and alpha: k^T S_t = v_t^T (the erase-then-write);
+    - beta = 0 only decays the initial state: o_t = exp(cum_t) q_t^T S0;
+    - one token from zero state: o = beta (q . k) v."""
+    r = _rng(15)
+    B, H, d, dv = 2, 2, 6, 4
+    Q, _ = np.linalg.qr(r.normal(size=(B, H, d, d)))        # columns orthonormal
+    Ko = np.swapaxes(Q, -1, -2)                               # rows orthonormal: L = d keys
+    v = r.normal(size=(B, H, d, dv))
+    q = r.normal(size=(B, H, d, d))
+    ones = np.ones((B, H, d))
+    O, S = oracle.delta(q, Ko, v, ones, lib=lib)
+    Oa, Sa = oracle.recurrent(q, Ko, v, lib=lib)
+    _close(O, Oa, 1e-12, "delta = additive for orthonormal keys")
+    _close(S, Sa, 1e-12, "delta state = additive for orthonormal keys")
+    L = 17
+    kr = r.normal(size=(B, H, L, d))
+    kr /= np.linalg.norm(kr, axis=-1, keepdims=True)
+    vr = r.normal(size=(B, H, L, dv))
+    S0 = r.normal(size=(B, H, d, dv))
+    la = -np.logaddexp(0.0, r.normal(size=(B, H, L)))
+    _, Sd = oracle.delta(kr, kr, vr, np.ones((B, H, L)), lib=lib)
+    _, Sadd = oracle.recurrent(kr, kr, vr, lib=lib)
+    assert np.linalg.norm(Sd - Sadd) > 1e-3, "delta must differ from additive for random keys"
+    O, _ = oracle.delta(kr, kr, vr, np.ones((B, H, L)), log_alpha=la, S0=S0, lib=lib)
+    _close(O, vr, 1e-12, "delta: reading the key just written returns its value")
+    qz = r.normal(size=(B, H, L, d))
+    O, S = oracle.delta(qz, kr, vr, np.zeros((B, H, L)), log_alpha=la, S0=S0, lib=lib)
+    cum = np.cumsum(la, axis=2)
+    _close(O, np.exp(cum)[..., None] * np.einsum("bhti,bhie->bhte", qz, S0), 1e-12,
+           "delta with beta = 0")
+    be = r.uniform(0.1, 1.0, size=(B, H, 1))
+    O, _ = oracle.delta(qz[:, :, :1], kr[:, :, :1], vr[:, :, :1], be, lib=lib)
+    want = be[..., None] * np.einsum("bhti,bhti->bht", qz[:, :, :1], kr[:, :, :1])[..., None] * vr[:, :, :1]
+    _close(O, want, 1e-12, "delta one token")
+
+
 PINS = [pin_golden, pin_closed_form_additive, pin_closed_form_constant_decay, pin_single_token,
         pin_one_hot, pin_orthonormal_keys, pin_chunk_invariance, pin_parallel_equals_recurrent,
         pin_split_invariance, pin_library_pieces, pin_state_shape, pin_noncausal, pin_normalised,
-        pin_channel_gate]
+        pin_channel_gate, pin_delta]

@@ -94,6 +94,17 @@ MUTANTS = [
     ("channel_gate_one_channel",
      "const double a = exp(la[i]);",
      "const double a = exp(la[0]);"),
+    ("delta_gate_on_write",
+     "S[(size_t)i * dv + j] = a * (S[(size_t)i * dv + j] - bt * kf[i] * ks[j]) +\n"
+     "                                            bt * kf[i] * vt[j];",
+     "S[(size_t)i * dv + j] = a * (S[(size_t)i * dv + j] - bt * kf[i] * ks[j] +\n"
+     "                                            bt * kf[i] * vt[j]);"),
+    ("delta_no_erase",
+     "a * (S[(size_t)i * dv + j] - bt * kf[i] * ks[j])",
+     "a * (S[(size_t)i * dv + j])"),
+    ("delta_write_without_beta",
+     "                                            bt * kf[i] * vt[j];",
+     "                                            kf[i] * vt[j];"),
 ]
 
 
