@@ -331,6 +331,60 @@ def bench_noncausal(w, steps, warmup, dev, peaks, peak_kind):
     return per_call_ms, rl
 
 
+def variant_bytes(form, w) -> int:
+    """Bytes a further form must move at least: q, k, v read and O written once,
+    its per-token gate inputs read, and the final state written."""
+    e = ELT["bf16"]
+    n = w.B * w.H * w.L
+    per_token = {"normalised": 4, "channel_gate": 4 * w.dk, "delta": 8}[form]
+    state = w.B * w.H * (w.dk * w.dv + (w.dk if form == "normalised" else 0)) * 4
+    return n * ((2 * w.dk + 2 * w.dv) * e + per_token) + state
+
+
+def bench_variants(w, steps, warmup, dev, peaks, peak_kind):
+    """The normalised form, the per-channel gate and the delta rule, each on
+    the shape of prefill workload ``w`` in bf16 (elu + 1 for the first two;
+    identity with unit-norm keys for the delta rule).  One input set per form:
+    these CUDA-core kernels are bound by arithmetic, not by HBM."""
+    from causal_linear_attention_chunkwise_gb300 import api
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for form in ("normalised", "channel_gate", "delta"):
+        inp = W.make_variant_inputs(form, w.B, w.H, w.L, w.dk, w.dv, "bf16", seed=0,
+                                    with_state=True)
+        d = {k: (v.to(dev) if hasattr(v, "to") else v) for k, v in inp.items()}
+        if form == "normalised":
+            api.la_set_feature_map("elu1")
+            call = lambda: api.la_normalised_fwd(  # noqa: E731
+                d["q"], d["k"], d["v"], 64, d["decay_kind"], d["decay"], d["S0"], d["z0"],
+                stream=stream)
+        elif form == "channel_gate":
+            api.la_set_feature_map("elu1")
+            call = lambda: api.la_channel_gate_fwd(  # noqa: E731
+                d["q"], d["k"], d["v"], d["log_alpha"], 64, d["S0"], stream=stream)
+        else:
+            api.la_set_feature_map("identity")
+            call = lambda: api.la_delta_fwd(  # noqa: E731
+                d["q"], d["k"], d["v"], d["beta"], d["log_alpha"], d["S0"], stream=stream)
+        for _ in range(warmup):
+            call()
+        api.la_device_status()
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for j in range(steps):
+            starts[j].record(stream)
+            call()
+            ends[j].record(stream)
+        torch.cuda.synchronize(dev)
+        api.la_device_status()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
+        rl = roofline(variant_bytes(form, w), 0, ms / 1e3, peaks, peak_kind, False)
+        out[form] = {"per_call_ms": round(ms, 4),
+                     "tokens_per_s": w.B * w.H * w.L / (ms / 1e3), "roofline": rl}
+    return out
+
+
 def bench_prefill_e2e(w, steps, dev):
     """Same metric with host buffers: pinned Q/K/V (+gate, S0) copied in and
     O and S_final copied out inside the timed region, every step.  The
@@ -543,6 +597,10 @@ def run_profile(args):
         per, rl = bench_noncausal(w, args.steps, args.warmup, dev, peaks, peak_kind)
         print(json.dumps({"profile": "noncausal", "workload": w.name, "per_call_ms": round(per, 5),
                           "roofline": rl}))
+    elif args.profile == "variants":
+        w = W.PREFILL[args.workload]
+        r = bench_variants(w, args.steps, args.warmup, dev, peaks, peak_kind)
+        print(json.dumps({"profile": "variants", "workload": w.name, "dtype": "bf16", **r}))
     else:
         dw, _, per, rl = bench_decode(args.steps, args.warmup, dev, peaks, peak_kind)
         print(json.dumps({"profile": "decode", "workload": dw.name, "per_step_ms": round(per, 5),
@@ -604,7 +662,7 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.PREFILL))
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--profile", choices=["prefill", "decode", "noncausal"], default=None,
+    p.add_argument("--profile", choices=["prefill", "decode", "noncausal", "variants"], default=None,
                    help="run one leg only (for ncu captures); prints no benchmark line")
     args = p.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps

@@ -25,6 +25,11 @@ SIGNATURES = {
     "la_chunk_fwd_noalloc_scratch_bytes": (_sz, []),
     "la_noncausal_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "la_noncausal_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "la_normalised_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _vp]),
+    "la_channel_gate_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
+                                 _vp]),
+    "la_delta_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "la_device_status": (_i, [_vp]),
     "la_selftest_wait_timeout": (_i, [_u, _vp]),
     "la_last_error": (ctypes.c_char_p, []),

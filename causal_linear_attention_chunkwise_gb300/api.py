@@ -197,6 +197,76 @@ def la_decode_step(q, k, v, S, log_alpha=None, o=None, stream=None):
     return o
 
 
+def _state_bufs(q, v, want, S_final, extra=False, z_final=None):
+    B, H, _, dk = q.shape
+    dv = v.shape[-1]
+    if S_final is None and want:
+        S_final = torch.empty(B, H, dk, dv, dtype=torch.float32, device=q.device)
+    if extra and z_final is None and want:
+        z_final = torch.empty(B, H, dk, dtype=torch.float32, device=q.device)
+    return S_final, z_final
+
+
+def _qkv(q, k, v, O):
+    if k.shape != q.shape or v.shape[:3] != q.shape[:3] or v.dtype != q.dtype or k.dtype != q.dtype:
+        raise ValueError("q, k, v must agree in [B,H,L] and dtype")
+    B, H, L, _ = q.shape
+    if O is None:
+        O = torch.empty(B, H, L, v.shape[-1], dtype=q.dtype, device=q.device)
+    return O
+
+
+def la_normalised_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, z0=None,
+                      O=None, S_final=None, z_final=None, want_final_state=True, stream=None):
+    """Normalised form o_t = phi(q_t)^T S_t / phi(q_t)^T z_t over [B,H,L,d]
+    sequences, z the decayed key sum.  Returns ``(O, S_final, z_final)``.
+    ``S0`` fp32 [B,H,d_k,d_v], ``z0`` fp32 [B,H,d_k]; the outputs may be the
+    same tensors as the inputs (with L = 1 that is one decode step)."""
+    O = _qkv(q, k, v, O)
+    S_final, z_final = _state_bufs(q, v, want_final_state, S_final, True, z_final)
+    _need_cuda(q, k, v, decay, S0, z0, O, S_final, z_final)
+    B, H, L, dk = q.shape
+    _check(_native.load().la_normalised_fwd(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, v.shape[-1], chunk,
+        DECAY[decay_kind], _ptr(decay), _ptr(S0), _ptr(z0), _ptr(O), _ptr(S_final),
+        _ptr(z_final), _stream(stream)))
+    return O, S_final, z_final
+
+
+def la_channel_gate_fwd(q, k, v, log_alpha, chunk=64, S0=None, O=None, S_final=None,
+                        want_final_state=True, stream=None):
+    """Per-channel gate S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T with
+    ``log_alpha`` fp32 [B,H,L,d_k].  Returns ``(O, S_final)``."""
+    O = _qkv(q, k, v, O)
+    S_final, _ = _state_bufs(q, v, want_final_state, S_final)
+    _need_cuda(q, k, v, log_alpha, S0, O, S_final)
+    B, H, L, dk = q.shape
+    if log_alpha.shape != (B, H, L, dk) or log_alpha.dtype != torch.float32:
+        raise ValueError("log_alpha must be fp32 [B,H,L,d_k]")
+    _check(_native.load().la_channel_gate_fwd(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, v.shape[-1], chunk,
+        _ptr(log_alpha), _ptr(S0), _ptr(O), _ptr(S_final), _stream(stream)))
+    return O, S_final
+
+
+def la_delta_fwd(q, k, v, beta, log_alpha=None, S0=None, O=None, S_final=None,
+                 want_final_state=True, stream=None):
+    """(Gated) delta rule S <- alpha (S - beta k (k^T S)) + beta k v^T,
+    o = phi(q)^T S, token by token; ``beta`` and ``log_alpha`` fp32 [B,H,L]
+    (``log_alpha`` None: alpha = 1).  Returns ``(O, S_final)``."""
+    O = _qkv(q, k, v, O)
+    S_final, _ = _state_bufs(q, v, want_final_state, S_final)
+    _need_cuda(q, k, v, beta, log_alpha, S0, O, S_final)
+    B, H, L, dk = q.shape
+    for t in (beta, log_alpha):
+        if t is not None and (t.shape != (B, H, L) or t.dtype != torch.float32):
+            raise ValueError("beta and log_alpha must be fp32 [B,H,L]")
+    _check(_native.load().la_delta_fwd(
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, v.shape[-1], _ptr(beta),
+        _ptr(log_alpha), _ptr(S0), _ptr(O), _ptr(S_final), _stream(stream)))
+    return O, S_final
+
+
 def la_device_status(stream=None) -> None:
     """Synchronise and raise LAError if a kernel's bounded wait timed out."""
     _check(_native.load().la_device_status(_stream(stream)))

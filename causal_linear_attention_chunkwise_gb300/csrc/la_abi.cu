@@ -39,6 +39,58 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
+// Copy `src` to `dst` (or zero `dst` when src is null): the state after no tokens.
+cudaError_t pass_through_state(float *dst, const float *src, size_t bytes, cudaStream_t st) {
+  if (!dst) return cudaSuccess;
+  if (!src) return cudaMemsetAsync(dst, 0, bytes, st);
+  if (src == dst) return cudaSuccess;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+}
+
+// Checks shared by la_normalised_fwd, la_channel_gate_fwd and la_delta_fwd.
+// Returns LA_OK with *done = false when the kernel is to run; otherwise the
+// call ends with the returned status (LA_OK with *done = true: an empty batch,
+// or L = 0 with the states passed through).
+la_status check_variant(const char *fn, const void *q, const void *k, const void *v, int dtype,
+                        int B, int H, int L, int d_k, int d_v, int chunk, bool uses_chunk,
+                        const float *S0, const float *z0, void *O, float *S_final,
+                        float *z_final, cudaStream_t st, bool *done) {
+  *done = true;
+  if (dtype != LA_F32 && dtype != LA_BF16)
+    return fail(LA_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, dtype);
+  if (B < 0 || H < 0 || L < 0 || d_k <= 0 || d_v <= 0 || (uses_chunk && chunk <= 0))
+    return fail(LA_ERR_INVALID_ARG, "%s: bad sizes B=%d H=%d L=%d d_k=%d d_v=%d chunk=%d", fn,
+                B, H, L, d_k, d_v, chunk);
+  if (!supported_d(d_k) || !supported_d(d_v))
+    return fail(LA_ERR_UNSUPPORTED, "%s: d_k=%d d_v=%d not in {16,32,64,128}", fn, d_k, d_v);
+  if (uses_chunk && chunk > 64)
+    return fail(LA_ERR_UNSUPPORTED, "%s: chunk %d > 64 is not supported", fn, chunk);
+  if ((size_t)B * H == 0) return ok();
+  if ((S0 && !aligned16(S0)) || (S_final && !aligned16(S_final)) || (z0 && !aligned16(z0)) ||
+      (z_final && !aligned16(z_final)))
+    return fail(LA_ERR_INVALID_ARG, "%s: state pointers must be 16-byte aligned", fn);
+  if (L == 0) {
+    const size_t sb = (size_t)B * H * d_k * d_v * sizeof(float);
+    const size_t zb = (size_t)B * H * d_k * sizeof(float);
+    cudaError_t e = pass_through_state(S_final, S0, sb, st);
+    if (e == cudaSuccess) e = pass_through_state(z_final, z0, zb, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+    return ok();
+  }
+  if (!q || !k || !v || !O)
+    return fail(LA_ERR_INVALID_ARG, "%s: q, k, v and O must be non-null", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(O))
+    return fail(LA_ERR_INVALID_ARG, "%s: tensors must start on a 16-byte boundary", fn);
+  *done = false;
+  return ok();
+}
+
+la_status run_variant(const char *fn, const VariantArgs &a) {
+  cudaError_t e = launch_variant(a);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
+}
+
 const char *kernel_name(unsigned int id) {
   switch (id) {
     case KID_PREFILL_TC_STATE: return "prefill segment-state kernel";
@@ -225,6 +277,56 @@ la_status la_decode_step(const void *q, const void *k, const void *v, int dtype,
   cudaError_t e = launch_decode(a);
   if (e != cudaSuccess) return cuda_fail(e, "la_decode_step");
   return ok();
+}
+
+la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dtype, int B,
+                            int H, int L, int d_k, int d_v, int chunk, int decay_kind,
+                            const float *decay, const float *S0, const float *z0, void *O,
+                            float *S_final, float *z_final, void *cuda_stream) {
+  const char *fn = "la_normalised_fwd";
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (decay_kind < LA_DECAY_NONE || decay_kind > LA_DECAY_GATE_LOGIT)
+    return fail(LA_ERR_INVALID_ARG, "%s: unknown decay kind %d", fn, decay_kind);
+  if (decay_kind != LA_DECAY_NONE && !decay)
+    return fail(LA_ERR_INVALID_ARG, "%s: decay kind %d needs a decay pointer", fn, decay_kind);
+  bool done = false;
+  la_status s = check_variant(fn, q, k, v, dtype, B, H, L, d_k, d_v, chunk, true, S0, z0, O,
+                              S_final, z_final, st, &done);
+  if (s != LA_OK || done) return s;
+  VariantArgs a{VARIANT_NORMALISED, q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(),
+                decay_kind, decay_kind == LA_DECAY_NONE ? nullptr : decay, nullptr, S0, z0, O,
+                S_final, z_final, st};
+  return run_variant(fn, a);
+}
+
+la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int dtype, int B,
+                              int H, int L, int d_k, int d_v, int chunk, const float *log_alpha,
+                              const float *S0, void *O, float *S_final, void *cuda_stream) {
+  const char *fn = "la_channel_gate_fwd";
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  bool done = false;
+  la_status s = check_variant(fn, q, k, v, dtype, B, H, L, d_k, d_v, chunk, true, S0, nullptr,
+                              O, S_final, nullptr, st, &done);
+  if (s != LA_OK || done) return s;
+  if (!log_alpha) return fail(LA_ERR_INVALID_ARG, "%s: log_alpha must be non-null", fn);
+  VariantArgs a{VARIANT_CHANNEL_GATE, q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(),
+                LA_DECAY_NONE, log_alpha, nullptr, S0, nullptr, O, S_final, nullptr, st};
+  return run_variant(fn, a);
+}
+
+la_status la_delta_fwd(const void *q, const void *k, const void *v, int dtype, int B, int H,
+                       int L, int d_k, int d_v, const float *beta, const float *log_alpha,
+                       const float *S0, void *O, float *S_final, void *cuda_stream) {
+  const char *fn = "la_delta_fwd";
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  bool done = false;
+  la_status s = check_variant(fn, q, k, v, dtype, B, H, L, d_k, d_v, 0, false, S0, nullptr, O,
+                              S_final, nullptr, st, &done);
+  if (s != LA_OK || done) return s;
+  if (!beta) return fail(LA_ERR_INVALID_ARG, "%s: beta must be non-null", fn);
+  VariantArgs a{VARIANT_DELTA, q, k, v, dtype, B, H, L, d_k, d_v, 0, g_phi.load(),
+                LA_DECAY_NONE, log_alpha, beta, S0, nullptr, O, S_final, nullptr, st};
+  return run_variant(fn, a);
 }
 
 la_status la_device_status(void *cuda_stream) {

@@ -147,3 +147,49 @@ def small_prefill(B=1, H=2, L=200, dk=32, dv=32, dtype="bf16", phi="identity", d
     if scale is None:
         scale = 1.0 if dtype == "f32" else 1.0 / math.sqrt(dk)
     return PrefillWorkload(name, B, H, L, dk, dv, dtype, phi, decay, chunk, scale, s0_std)
+
+
+def make_variant_inputs(form: str, B: int, H: int, L: int, dk: int, dv: int, dtype: str = "bf16",
+                        seed: int = 0, with_state: bool = False, gated: bool = True,
+                        beta_max: float = 1.0) -> dict:
+    """Inputs of the three further forms (``form`` "normalised" |
+    "channel_gate" | "delta"), drawn in this order from one generator:
+
+    * q, k, v: ``randn`` (fp32) scaled by 1/sqrt(dk) for q and k, 1 for v, cast
+      to the dtype; for "delta" each key row is rescaled to unit L2 norm
+      before the cast (the rule assumes unit-norm keys);
+    * "channel_gate": log_alpha fp32 [B,H,L,dk] = -U(0.005, 0.7), i.e. alpha
+      per channel in (0.50, 0.995);
+    * "delta": beta fp32 [B,H,L] ~ U(0, beta_max), then (``gated``)
+      log_alpha fp32 [B,H,L] = -U(0.005, 0.3);
+    * "normalised": gate logits g ~ N(0, 1) fp32 [B,H,L] when ``gated``;
+    * with ``with_state``: S0 ~ 0.5 randn fp32 [B,H,dk,dv] and, for
+      "normalised", z0 ~ U(0.5, 2.5) fp32 [B,H,dk] (a positive key sum).
+    """
+    gen = torch.Generator().manual_seed(seed)
+    dt = DTYPES[dtype]
+    s = 1.0 / math.sqrt(dk)
+    q = torch.randn(B, H, L, dk, generator=gen) * s
+    k = torch.randn(B, H, L, dk, generator=gen) * s
+    v = torch.randn(B, H, L, dv, generator=gen)
+    if form == "delta":
+        k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    out = {"q": q.to(dt), "k": k.to(dt), "v": v.to(dt), "log_alpha": None, "beta": None,
+           "decay_kind": "none", "decay": None, "S0": None, "z0": None}
+    if form == "channel_gate":
+        out["log_alpha"] = -(torch.rand(B, H, L, dk, generator=gen) * 0.695 + 0.005)
+    elif form == "delta":
+        out["beta"] = torch.rand(B, H, L, generator=gen) * beta_max
+        if gated:
+            out["log_alpha"] = -(torch.rand(B, H, L, generator=gen) * 0.295 + 0.005)
+    elif form == "normalised":
+        if gated:
+            out["decay_kind"] = "logit"
+            out["decay"] = torch.randn(B, H, L, generator=gen)
+    else:
+        raise ValueError(f"unknown form {form!r}")
+    if with_state:
+        out["S0"] = torch.randn(B, H, dk, dv, generator=gen) * 0.5
+        if form == "normalised":
+            out["z0"] = torch.rand(B, H, dk, generator=gen) * 2.0 + 0.5
+    return out

@@ -161,6 +161,79 @@ la_status la_noncausal_fwd(const void *q, const void *k, const void *v, int dtyp
 size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v);
 
 /*
+ * Three further forms of the recurrence, on the CUDA cores (fp32 arithmetic;
+ * q, k, v and O in dtype = LA_F32 or LA_BF16; states fp32).  Each runs over
+ * whole sequences like la_chunk_fwd, and each is also its own decode step:
+ * with L = 1 and the output state aliasing the input state, one call advances
+ * every sequence by one token.  phi is the one set by la_set_feature_map.
+ * Supported: d_k, d_v in {16, 32, 64, 128}; chunk 1..64 where one is taken
+ * (the result does not depend on it up to rounding).  L = 0 passes the
+ * initial states through (or zeroes the outputs when none is given).  Errors:
+ * LA_ERR_INVALID_ARG (null or misaligned pointer, negative size, unknown
+ * enum), LA_ERR_UNSUPPORTED (a d or chunk outside the list), LA_ERR_CUDA.
+ * Pointers are device pointers owned by the caller, row-major, 16-byte
+ * aligned; the calls are asynchronous on `cuda_stream` and allocate nothing.
+ */
+
+/*
+ * Normalised linear attention ("Linear / sparse attention tutorial" Q11 and
+ * section 2.2): the state carries a key sum z next to S, which decays with S,
+ *
+ *     S_t = a_t S_{t-1} + phi(k_t) v_t^T,   z_t = a_t z_{t-1} + phi(k_t),
+ *     o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t).
+ *
+ * There is no epsilon in the denominator: choose a positive feature map
+ * (LA_PHI_ELU1), as the tutorial does, or the quotient may be undefined.
+ *
+ *   q, k   [B,H,L,d_k] dtype;  v, O [B,H,L,d_v] dtype
+ *   decay_kind / decay   as for la_chunk_fwd
+ *   S0     [B,H,d_k,d_v] fp32 or NULL (zero);  z0 [B,H,d_k] fp32 or NULL (zero)
+ *   S_final, z_final   the states after the last token, or NULL; each may be
+ *          the same buffer as S0 / z0.
+ */
+la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dtype,
+                            int B, int H, int L, int d_k, int d_v, int chunk,
+                            int decay_kind, const float *decay,
+                            const float *S0, const float *z0, void *O,
+                            float *S_final, float *z_final, void *cuda_stream);
+
+/*
+ * Per-channel (diagonal) gate, as in GLA ("Linear / sparse attention
+ * tutorial" Q21):
+ *
+ *     S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T,   o_t = phi(q_t)^T S_t,
+ *
+ * one decay per key channel and token.
+ *
+ *   log_alpha  [B,H,L,d_k] fp32, log alpha_t[i] (expected <= 0)   (read)
+ *   S0         [B,H,d_k,d_v] fp32 or NULL;  S_final may alias S0.
+ */
+la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int dtype,
+                              int B, int H, int L, int d_k, int d_v, int chunk,
+                              const float *log_alpha, const float *S0, void *O,
+                              float *S_final, void *cuda_stream);
+
+/*
+ * The (gated) delta rule ("Linear / Sparse Attention - minimal runnable
+ * implementation", delta_rule_recurrent; "Linear / sparse attention tutorial"
+ * Q21 for the gate), with the state as [d_k, d_v] like the others:
+ *
+ *     S_t = alpha_t (S_{t-1} - beta_t k (k^T S_{t-1})) + beta_t k v_t^T,
+ *     o_t = phi(q_t)^T S_t,      k = phi(k_t).
+ *
+ * Keys are used as given (after phi): the rule assumes unit-norm keys, and
+ * normalising them is the caller's step.  Runs token by token.
+ *
+ *   beta       [B,H,L] fp32 write strengths                        (read)
+ *   log_alpha  [B,H,L] fp32 log of the gate, or NULL for alpha = 1  (read)
+ *   S0         [B,H,d_k,d_v] fp32 or NULL;  S_final may alias S0.
+ */
+la_status la_delta_fwd(const void *q, const void *k, const void *v, int dtype,
+                       int B, int H, int L, int d_k, int d_v,
+                       const float *beta, const float *log_alpha,
+                       const float *S0, void *O, float *S_final, void *cuda_stream);
+
+/*
  * la_chunk_fwd for callers that cannot allocate device memory.  (The pages
  * have no counterpart: this is a deployment variant of la_chunk_fwd.)
  *

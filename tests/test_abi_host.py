@@ -144,3 +144,37 @@ def test_prefill_plan_invariants(lib):
     # fp32 and other shapes take the SIMT path: no workspace
     assert lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 0) == 0
     assert lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 32, 32, 64, 1) == 0
+
+
+def test_variant_validation_before_any_device_work(lib):
+    """la_normalised_fwd, la_channel_gate_fwd and la_delta_fwd reject bad
+    arguments before any device work."""
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x1008)
+    nf = lambda *a: lib.la_normalised_fwd(*a)  # noqa: E731
+    # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, decay_kind, decay, S0, z0, O, S_final, z_final, stream)
+    assert nf(p, p, p, 7, 1, 1, 8, 16, 16, 64, 0, None, None, None, p, None, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 48, 16, 64, 0, None, None, None, p, None, None, None) == 2
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 65, 0, None, None, None, p, None, None, None) == 2
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 0, 0, None, None, None, p, None, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 5, None, None, None, p, None, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 3, None, None, None, p, None, None, None) == 1
+    assert b"decay pointer" in lib.la_last_error()
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, None, None, None, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, odd, p, None, None, None) == 1
+    assert b"16-byte" in lib.la_last_error()
+    assert nf(p, p, p, 1, 0, 3, 8, 16, 16, 64, 0, None, None, None, p, None, None, None) == 0
+    cg = lambda *a: lib.la_channel_gate_fwd(*a)  # noqa: E731
+    # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, log_alpha, S0, O, S_final, stream)
+    assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, None, None, p, None, None) == 1
+    assert b"log_alpha" in lib.la_last_error()
+    assert cg(p, p, p, 1, 1, 1, 8, 16, 256, 64, p, None, p, None, None) == 2
+    assert cg(p, p, p, 1, 1, -1, 8, 16, 16, 64, p, None, p, None, None) == 1
+    assert cg(p, odd, p, 1, 1, 1, 8, 16, 16, 64, p, None, p, None, None) == 1
+    dl = lambda *a: lib.la_delta_fwd(*a)  # noqa: E731
+    # (q, k, v, dtype, B, H, L, d_k, d_v, beta, log_alpha, S0, O, S_final, stream)
+    assert dl(p, p, p, 1, 1, 1, 8, 16, 16, None, None, None, p, None, None) == 1
+    assert b"beta" in lib.la_last_error()
+    assert dl(p, p, p, 0, 1, 1, 8, 16, 24, p, None, None, p, None, None) == 2
+    assert dl(p, p, p, 1, 1, 1, 8, 16, 16, p, None, None, p, odd, None) == 1
+    assert dl(p, p, p, 2, 1, 1, 8, 16, 16, p, None, None, p, None, None) == 1

@@ -1,0 +1,244 @@
+"""GPU parity of the three further forms of the recurrence against the fp64
+oracle on the same seeded inputs: the normalised form (la_normalised_fwd,
+"Linear / sparse attention tutorial" Q11 and section 2.2), the per-channel
+gate (la_channel_gate_fwd, the tutorial's Q21, GLA) and the (gated) delta rule
+(la_delta_fwd, "Linear / Sparse Attention - minimal runnable implementation",
+delta_rule_recurrent).  Needs a GB300."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_linear_attention_chunkwise_gb300 import api
+from causal_linear_attention_chunkwise_gb300 import workloads as W
+from tests import parity
+from tests.gpu_helpers import to_dev
+
+pytestmark = pytest.mark.gpu
+
+# (B, H, L, dk, dv, dtype, chunk, phi, gated, with_state): one token, one chunk,
+# several chunks with a ragged tail, d_k != d_v, an odd chunk size.
+CASES = [
+    (1, 1, 1, 16, 16, "f32", 64, "elu1", False, False),
+    (2, 2, 200, 32, 32, "f32", 64, "elu1", True, True),
+    (1, 2, 130, 64, 64, "bf16", 64, "elu1", True, False),
+    (2, 2, 300, 128, 128, "bf16", 64, "elu1", True, True),
+    (1, 2, 150, 64, 128, "f32", 7, "identity", True, True),
+    (1, 1, 100, 128, 16, "bf16", 33, "identity", False, False),
+]
+IDS = [f"{c[0]}x{c[1]}x{c[2]}_dk{c[3]}_dv{c[4]}_{c[5]}_C{c[6]}_{c[7]}_{'g' if c[8] else 'ng'}"
+       f"{'_S0' if c[9] else ''}" for c in CASES]
+
+
+def _d(x):
+    return to_dev(x)
+
+
+# The quotient needs a positive feature map: the normalised form runs under elu + 1 only.
+NORM_CASES = [c[:7] + ("elu1",) + c[8:] for c in CASES]
+NORM_IDS = [i.replace("identity", "elu1") for i in IDS]
+
+
+@pytest.mark.parametrize("case", NORM_CASES, ids=NORM_IDS)
+def test_normalised_matches_oracle(case):
+    B, H, L, dk, dv, dtype, chunk, phi, gated, with_state = case
+    inp = W.make_variant_inputs("normalised", B, H, L, dk, dv, dtype, seed=1,
+                                with_state=with_state, gated=gated)
+    api.la_set_feature_map(phi)
+    O, S, z = api.la_normalised_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), chunk,
+                                    inp["decay_kind"], _d(inp["decay"]), _d(inp["S0"]),
+                                    _d(inp["z0"]))
+    api.la_device_status()
+    O_ref, S_ref, z_ref = oracle.normalised(inp["q"], inp["k"], inp["v"], phi=phi,
+                                            decay_kind=inp["decay_kind"], decay=inp["decay"],
+                                            S0=inp["S0"], z0=inp["z0"])
+    parity.check(O.cpu(), O_ref, dtype, "O")
+    parity.check(S.cpu(), S_ref, dtype, "S")
+    parity.check(z.cpu()[..., None], z_ref[..., None], dtype, "z")
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_channel_gate_matches_oracle(case):
+    B, H, L, dk, dv, dtype, chunk, phi, _, with_state = case
+    inp = W.make_variant_inputs("channel_gate", B, H, L, dk, dv, dtype, seed=2,
+                                with_state=with_state)
+    api.la_set_feature_map(phi)
+    O, S = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]),
+                                   _d(inp["log_alpha"]), chunk, _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], inp["log_alpha"], phi=phi,
+                                       S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, dtype, "O")
+    parity.check(S.cpu(), S_ref, dtype, "S")
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_delta_matches_oracle(case):
+    B, H, L, dk, dv, dtype, _, phi, gated, with_state = case
+    # unit-norm keys; under elu + 1 the keys grow to norm ~ sqrt(dk), so the
+    # write strength shrinks to keep I - beta k k^T a contraction
+    beta_max = 1.0 if phi == "identity" else 1.0 / dk
+    inp = W.make_variant_inputs("delta", B, H, L, dk, dv, dtype, seed=3, with_state=with_state,
+                                gated=gated, beta_max=beta_max)
+    api.la_set_feature_map(phi)
+    O, S = api.la_delta_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["beta"]),
+                            _d(inp["log_alpha"]), _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.delta(inp["q"], inp["k"], inp["v"], inp["beta"], inp["log_alpha"],
+                                phi=phi, S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, dtype, "O")
+    parity.check(S.cpu(), S_ref, dtype, "S")
+
+
+def test_delta_recalls_the_key_just_written():
+    """beta = 1 with unit keys and no gate: reading with the key just written
+    returns its value exactly (the write replaces the old association)."""
+    B, H, L, d = 2, 3, 64, 64
+    inp = W.make_variant_inputs("delta", B, H, L, d, d, "f32", seed=4, with_state=True,
+                                gated=False)
+    beta = torch.ones(B, H, L)
+    api.la_set_feature_map("identity")
+    O, _ = api.la_delta_fwd(_d(inp["k"]), _d(inp["k"]), _d(inp["v"]), _d(beta), None,
+                            _d(inp["S0"]))
+    api.la_device_status()
+    parity.check(O.cpu(), inp["v"], "f32", "recall")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_steps_equal_one_call(dtype):
+    """L calls with one token each, every call writing its states over its input
+    states (the decode step of each form), give the oracle's outputs over the L
+    tokens."""
+    B, H, L, d = 3, 2, 6, 64
+    api.la_set_feature_map("elu1")
+    # normalised
+    inp = W.make_variant_inputs("normalised", B, H, L, d, d, dtype, seed=5, with_state=True)
+    q, k, v, g = _d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["decay"])
+    S, z = _d(inp["S0"]).clone(), _d(inp["z0"]).clone()
+    outs = []
+    for t in range(L):
+        sl = lambda x: x[:, :, t:t + 1].contiguous()  # noqa: E731
+        o, _, _ = api.la_normalised_fwd(sl(q), sl(k), sl(v), 64, "logit", sl(g), S, z,
+                                        S_final=S, z_final=z)
+        outs.append(o)
+    O_ref, S_ref, z_ref = oracle.normalised(inp["q"], inp["k"], inp["v"], phi="elu1",
+                                            decay_kind="logit", decay=inp["decay"],
+                                            S0=inp["S0"], z0=inp["z0"])
+    api.la_device_status()
+    parity.check(torch.cat(outs, 2).cpu(), O_ref, dtype, "normalised steps")
+    parity.check(S.cpu(), S_ref, dtype, "normalised S")
+    parity.check(z.cpu()[..., None], z_ref[..., None], dtype, "normalised z")
+    # channel gate
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, dtype, seed=6, with_state=True)
+    q, k, v, la = _d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["log_alpha"])
+    S = _d(inp["S0"]).clone()
+    outs = []
+    for t in range(L):
+        sl = lambda x: x[:, :, t:t + 1].contiguous()  # noqa: E731
+        o, _ = api.la_channel_gate_fwd(sl(q), sl(k), sl(v), sl(la), 64, S, S_final=S)
+        outs.append(o)
+    O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], inp["log_alpha"],
+                                       phi="elu1", S0=inp["S0"])
+    api.la_device_status()
+    parity.check(torch.cat(outs, 2).cpu(), O_ref, dtype, "channel gate steps")
+    parity.check(S.cpu(), S_ref, dtype, "channel gate S")
+    # delta rule
+    inp = W.make_variant_inputs("delta", B, H, L, d, d, dtype, seed=7, with_state=True,
+                                beta_max=1.0 / d)
+    q, k, v = _d(inp["q"]), _d(inp["k"]), _d(inp["v"])
+    be, la = _d(inp["beta"]), _d(inp["log_alpha"])
+    S = _d(inp["S0"]).clone()
+    outs = []
+    for t in range(L):
+        sl = lambda x: x[:, :, t:t + 1].contiguous()  # noqa: E731
+        o, _ = api.la_delta_fwd(sl(q), sl(k), sl(v), sl(be), sl(la), S, S_final=S)
+        outs.append(o)
+    O_ref, S_ref = oracle.delta(inp["q"], inp["k"], inp["v"], inp["beta"], inp["log_alpha"],
+                                phi="elu1", S0=inp["S0"])
+    api.la_device_status()
+    parity.check(torch.cat(outs, 2).cpu(), O_ref, dtype, "delta steps")
+    parity.check(S.cpu(), S_ref, dtype, "delta S")
+
+
+def test_channel_gate_with_equal_channels_is_the_token_gate():
+    """Equal per-channel decays reduce the channel gate to la_chunk_fwd with
+    a per-token decay: two different kernels, one answer."""
+    B, H, L, d = 2, 2, 333, 64
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "f32", seed=8, with_state=True)
+    la_tok = inp["log_alpha"][..., 0].contiguous()
+    la_ch = la_tok[..., None].expand(B, H, L, d).contiguous()
+    api.la_set_feature_map("elu1")
+    O1, S1 = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(la_ch), 64,
+                                     _d(inp["S0"]))
+    O2, S2 = api.la_chunk_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), 64, "token",
+                              _d(la_tok), _d(inp["S0"]))
+    api.la_device_status()
+    parity.check(O1.cpu(), O2.cpu(), "f32", "O")
+    parity.check(S1.cpu(), S2.cpu(), "f32", "S")
+
+
+def test_empty_sequences_pass_the_state_through_and_bad_shapes_are_refused():
+    B, H, d = 2, 2, 32
+    x = torch.zeros(B, H, 0, d, device="cuda")
+    S0 = torch.randn(B, H, d, d, device="cuda")
+    z0 = torch.rand(B, H, d, device="cuda")
+    _, S, z = api.la_normalised_fwd(x, x, x, 64, "none", None, S0, z0)
+    _, S2 = api.la_channel_gate_fwd(x, x, x, torch.zeros(B, H, 0, d, device="cuda"), 64, None)
+    _, S3 = api.la_delta_fwd(x, x, x, torch.zeros(B, H, 0, device="cuda"), None, S0)
+    api.la_device_status()
+    assert torch.equal(S, S0) and torch.equal(z, z0) and torch.equal(S3, S0)
+    assert torch.count_nonzero(S2) == 0
+    y = torch.zeros(1, 1, 8, 48, device="cuda")
+    for call in (lambda: api.la_normalised_fwd(y, y, y),
+                 lambda: api.la_channel_gate_fwd(y, y, y, torch.zeros(1, 1, 8, 48, device="cuda")),
+                 lambda: api.la_delta_fwd(y, y, y, torch.zeros(1, 1, 8, device="cuda"))):
+        with pytest.raises(api.LAError) as e:
+            call()
+        assert e.value.status == api.LA_ERR_UNSUPPORTED
+
+
+def test_larger_shapes_on_sampled_sequences():
+    """A longer run of each form at d = 128 (B2 H4 L2048, bf16), checked on
+    two sequences the oracle recomputes alone."""
+    B, H, L, d = 2, 4, 2048, 128
+    api.la_set_feature_map("elu1")
+    pairs = [(0, 0), (1, 3)]
+
+    def sl(x, b, h):
+        return None if x is None else x[b:b + 1, h:h + 1]
+
+    inp = W.make_variant_inputs("normalised", B, H, L, d, d, "bf16", seed=9, with_state=True)
+    O, S, z = api.la_normalised_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), 64, "logit",
+                                    _d(inp["decay"]), _d(inp["S0"]), _d(inp["z0"]))
+    api.la_device_status()
+    for b, h in pairs:
+        O_ref, S_ref, _ = oracle.normalised(sl(inp["q"], b, h), sl(inp["k"], b, h),
+                                            sl(inp["v"], b, h), phi="elu1", decay_kind="logit",
+                                            decay=sl(inp["decay"], b, h), S0=sl(inp["S0"], b, h),
+                                            z0=sl(inp["z0"], b, h))
+        parity.check(sl(O, b, h).cpu(), O_ref, "bf16", f"normalised O[{b},{h}]")
+        parity.check(sl(S, b, h).cpu(), S_ref, "bf16", f"normalised S[{b},{h}]")
+
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=10, with_state=True)
+    O, S = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]),
+                                   _d(inp["log_alpha"]), 64, _d(inp["S0"]))
+    api.la_device_status()
+    for b, h in pairs:
+        O_ref, S_ref = oracle.channel_gate(sl(inp["q"], b, h), sl(inp["k"], b, h),
+                                           sl(inp["v"], b, h), sl(inp["log_alpha"], b, h),
+                                           phi="elu1", S0=sl(inp["S0"], b, h))
+        parity.check(sl(O, b, h).cpu(), O_ref, "bf16", f"channel gate O[{b},{h}]")
+        parity.check(sl(S, b, h).cpu(), S_ref, "bf16", f"channel gate S[{b},{h}]")
+
+    inp = W.make_variant_inputs("delta", B, H, L, d, d, "bf16", seed=11, with_state=True,
+                                beta_max=1.0 / d)
+    O, S = api.la_delta_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["beta"]),
+                            _d(inp["log_alpha"]), _d(inp["S0"]))
+    api.la_device_status()
+    for b, h in pairs:
+        O_ref, S_ref = oracle.delta(sl(inp["q"], b, h), sl(inp["k"], b, h), sl(inp["v"], b, h),
+                                    sl(inp["beta"], b, h), sl(inp["log_alpha"], b, h),
+                                    phi="elu1", S0=sl(inp["S0"], b, h))
+        parity.check(sl(O, b, h).cpu(), O_ref, "bf16", f"delta O[{b},{h}]")
+        parity.check(sl(S, b, h).cpu(), S_ref, "bf16", f"delta S[{b},{h}]")
+    assert np.isfinite(S.cpu().numpy()).all()
