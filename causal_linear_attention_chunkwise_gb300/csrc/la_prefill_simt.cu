@@ -43,12 +43,18 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
                     const float *__restrict__ decay, const float *S0, T *__restrict__ O,
                     float *S_final) {
   extern __shared__ float smem[];
-  float *qs = smem;                   // [C][dk]   phi(q) of the chunk
-  float *ks = qs + C * dk;            // [C][dk]   phi(k)
-  float *vs = ks + C * dk;            // [C][dvt]  value slice
+  // q and k rows are padded to dk + 1 floats: the score loop reads one k row
+  // per lane, and an unpadded stride of dk (a multiple of 16) would put all
+  // of a warp's reads in one or two shared-memory banks.
+  const int dkp = dk + 1;
+  float *qs = smem;                   // [C][dkp]  phi(q) of the chunk
+  float *ks = qs + C * dkp;           // [C][dkp]  phi(k)
+  float *vs = ks + C * dkp;           // [C][dvt]  value slice
   float *P = vs + C * dvt;            // [C][C]    masked, decayed scores
   float *S = P + C * C;               // [dk][dvt] state slice
   float *lam = S + dk * dvt;          // [C]       inclusive log-decay prefix
+  float *eq = lam + C;                // [C]       e^{Lam_i}, weight of row i's inter read
+  float *ek = eq + C;                 // [C]       e^{Lam_end - Lam_j}, weight of key j
 
   const int tid = threadIdx.x;
   const int bh = blockIdx.x;
@@ -66,8 +72,9 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     const int n = min(C, L - s0);
     __syncthreads();  // previous chunk's readers of qs/ks/vs/S are done
     for (int x = tid; x < n * dk; x += kThreads) {
-      qs[x] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
-      ks[x] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
+      const int t = x / dk, r = x % dk;
+      qs[t * dkp + r] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
+      ks[t * dkp + r] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
     }
     for (int x = tid; x < n * nv; x += kThreads) {
       int t = x / nv, c = x % nv;
@@ -93,28 +100,30 @@ prefill_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
       float p = 0.f;
       if (j <= i) {
         float dot = 0.f;
-        for (int c = 0; c < dk; ++c) dot = fmaf(qs[i * dk + c], ks[j * dk + c], dot);
+        for (int c = 0; c < dk; ++c) dot = fmaf(qs[i * dkp + c], ks[j * dkp + c], dot);
         p = dot * expf(lam[i] - lam[j]);
       }
       P[i * C + j] = p;
+    }
+    for (int i = tid; i < n; i += kThreads) {
+      eq[i] = expf(lam[i]);
+      ek[i] = expf(lam[n - 1] - lam[i]);
     }
     __syncthreads();
     for (int x = tid; x < n * nv; x += kThreads) {
       int i = x / nv, c = x % nv;
       float inter = 0.f;
-      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dk + r], S[r * dvt + c], inter);
+      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dkp + r], S[r * dvt + c], inter);
       float intra = 0.f;
       for (int j = 0; j <= i; ++j) intra = fmaf(P[i * C + j], vs[j * dvt + c], intra);
-      O[(bhL + s0 + i) * dv + j0 + c] = from_f32<T>(fmaf(expf(lam[i]), inter, intra));
+      O[(bhL + s0 + i) * dv + j0 + c] = from_f32<T>(fmaf(eq[i], inter, intra));
     }
     __syncthreads();  // all reads of S for this chunk's output are done
-    const float lend = lam[n - 1];
-    const float eend = expf(lend);
+    const float eend = eq[n - 1];
     for (int x = tid; x < dk * nv; x += kThreads) {
       int r = x / nv, c = x % nv;
       float acc = 0.f;
-      for (int j = 0; j < n; ++j)
-        acc = fmaf(expf(lend - lam[j]) * ks[j * dk + r], vs[j * dvt + c], acc);
+      for (int j = 0; j < n; ++j) acc = fmaf(ek[j] * ks[j * dkp + r], vs[j * dvt + c], acc);
       S[r * dvt + c] = fmaf(eend, S[r * dvt + c], acc);
     }
   }
@@ -134,8 +143,8 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a) {
   if (C < 1 || C > kMaxChunk || a.dk > 128 || a.dv > 128) return cudaErrorInvalidValue;
   const int dvt = a.dv < 32 ? a.dv : 32;
   const size_t smem =
-      sizeof(float) * ((size_t)2 * C * a.dk + (size_t)C * dvt + (size_t)C * C +
-                       (size_t)a.dk * dvt + C);
+      sizeof(float) * ((size_t)2 * C * (a.dk + 1) + (size_t)C * dvt + (size_t)C * C +
+                       (size_t)a.dk * dvt + 3 * C);
   dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dv + dvt - 1) / dvt));
   if (a.dtype == LA_F32) {
     auto kern = prefill_simt_kernel<float>;

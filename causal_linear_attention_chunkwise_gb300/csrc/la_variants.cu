@@ -71,42 +71,58 @@ __device__ __forceinline__ void chunk_log_prefix(float *lam, int n, int kind,
 }
 
 // ---------------------------------------------------------------------------
-// Normalised form.  One CTA per (b, h) holds the whole state S (d_k x d_v) and
-// z (d_k) in shared memory, so S0/S_final and z0/z_final may alias.
+// Normalised form.  One CTA per (b, h) and slice of dvt value columns, with
+// its slice of S (d_k x dvt) and the whole of z (d_k) in shared memory.  Every
+// slice advances its own copy of z (d_k values per chunk, the same in all
+// slices) for its denominators; slice 0 writes z_final.  When z_final aliases
+// z0 the launcher uses a single slice, so that no CTA reads z0 after another
+// has written it.  q and k rows are padded to dk + 1 floats: the score loop
+// reads one k row per lane, and a stride of dk (a multiple of 16) would put a
+// warp's reads in one or two shared-memory banks.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 normalised_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                  int H, int L, int dk, int dv, int C, int phi, int decay_kind,
+                  int H, int L, int dk, int dv, int C, int dvt, int phi, int decay_kind,
                   const float *__restrict__ decay, const float *S0, const float *z0,
                   T *__restrict__ O, float *S_final, float *z_final) {
   extern __shared__ float smem[];
-  float *qs = smem;         // [C][dk]  phi(q)
-  float *ks = qs + C * dk;  // [C][dk]  phi(k)
-  float *vs = ks + C * dk;  // [C][dv]
-  float *P = vs + C * dv;   // [C][C]   masked, decayed scores
-  float *S = P + C * C;     // [dk][dv]
-  float *z = S + dk * dv;   // [dk]
-  float *lam = z + dk;      // [C]      inclusive log-decay prefix
-  float *den = lam + C;     // [C]      denominators
-  float *eq = den + C;      // [C]      e^{Lam_i}: weight of the inter-chunk read of row i
-  float *ek = eq + C;       // [C]      e^{Lam_end - Lam_j}: weight of key j in the update
+  const int dkp = dk + 1;
+  float *qs = smem;          // [C][dkp]  phi(q)
+  float *ks = qs + C * dkp;  // [C][dkp]  phi(k)
+  float *vs = ks + C * dkp;  // [C][dvt]  value slice
+  float *P = vs + C * dvt;   // [C][C]    masked, decayed scores
+  float *S = P + C * C;      // [dk][dvt] state slice
+  float *z = S + dk * dvt;   // [dk]
+  float *lam = z + dk;       // [C]       inclusive log-decay prefix
+  float *den = lam + C;      // [C]       denominators
+  float *eq = den + C;       // [C]       e^{Lam_i}: weight of the inter-chunk read of row i
+  float *ek = eq + C;        // [C]       e^{Lam_end - Lam_j}: weight of key j in the update
 
   const int tid = threadIdx.x;
   const int bh = blockIdx.x;
   const int h = bh % H;
+  const int j0 = blockIdx.y * dvt;
+  const int nv = min(dvt, dv - j0);
   const size_t bhL = (size_t)bh * L;
 
-  for (int x = tid; x < dk * dv; x += kThreads) S[x] = S0 ? S0[(size_t)bh * dk * dv + x] : 0.f;
+  for (int x = tid; x < dk * nv; x += kThreads) {
+    const int r = x / nv, c = x % nv;
+    S[r * dvt + c] = S0 ? S0[((size_t)bh * dk + r) * dv + j0 + c] : 0.f;
+  }
   for (int r = tid; r < dk; r += kThreads) z[r] = z0 ? z0[(size_t)bh * dk + r] : 0.f;
 
   for (int s0 = 0; s0 < L; s0 += C) {
     const int n = min(C, L - s0);
     __syncthreads();  // the previous chunk's readers are done
     for (int x = tid; x < n * dk; x += kThreads) {
-      qs[x] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
-      ks[x] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
+      const int t = x / dk, r = x % dk;
+      qs[t * dkp + r] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
+      ks[t * dkp + r] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
     }
-    for (int x = tid; x < n * dv; x += kThreads) vs[x] = to_f32(v[(bhL + s0) * dv + x]);
+    for (int x = tid; x < n * nv; x += kThreads) {
+      const int t = x / nv, c = x % nv;
+      vs[t * dvt + c] = to_f32(v[(bhL + s0 + t) * dv + j0 + c]);
+    }
     if (tid < 32) chunk_log_prefix(lam, n, decay_kind, decay, h, bhL, s0, tid);
     __syncthreads();
     for (int x = tid; x < n * n; x += kThreads) {
@@ -114,7 +130,7 @@ normalised_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
       float p = 0.f;
       if (j <= i) {
         float dot = 0.f;
-        for (int c = 0; c < dk; ++c) dot = fmaf(qs[i * dk + c], ks[j * dk + c], dot);
+        for (int c = 0; c < dk; ++c) dot = fmaf(qs[i * dkp + c], ks[j * dkp + c], dot);
         p = dot * expf(lam[i] - lam[j]);
       }
       P[i * C + j] = p;
@@ -122,7 +138,7 @@ normalised_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
     __syncthreads();
     for (int i = tid; i < n; i += kThreads) {  // phi(q_i)^T z_i, in its two parts
       float inter = 0.f;
-      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dk + r], z[r], inter);
+      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dkp + r], z[r], inter);
       float intra = 0.f;
       for (int j = 0; j <= i; ++j) intra += P[i * C + j];
       eq[i] = expf(lam[i]);
@@ -130,38 +146,44 @@ normalised_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__r
       den[i] = fmaf(eq[i], inter, intra);
     }
     __syncthreads();
-    for (int x = tid; x < n * dv; x += kThreads) {
-      const int i = x / dv, c = x % dv;
+    for (int x = tid; x < n * nv; x += kThreads) {
+      const int i = x / nv, c = x % nv;
       float inter = 0.f;
-      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dk + r], S[r * dv + c], inter);
+      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dkp + r], S[r * dvt + c], inter);
       float intra = 0.f;
-      for (int j = 0; j <= i; ++j) intra = fmaf(P[i * C + j], vs[j * dv + c], intra);
-      O[(bhL + s0 + i) * dv + c] = from_f32<T>(fmaf(eq[i], inter, intra) / den[i]);
+      for (int j = 0; j <= i; ++j) intra = fmaf(P[i * C + j], vs[j * dvt + c], intra);
+      O[(bhL + s0 + i) * dv + j0 + c] = from_f32<T>(fmaf(eq[i], inter, intra) / den[i]);
     }
     __syncthreads();  // every read of S and z for this chunk's output is done
     const float eend = eq[n - 1];
-    for (int x = tid; x < dk * dv; x += kThreads) {
-      const int r = x / dv, c = x % dv;
+    for (int x = tid; x < dk * nv; x += kThreads) {
+      const int r = x / nv, c = x % nv;
       float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = fmaf(ek[j] * ks[j * dk + r], vs[j * dv + c], acc);
-      S[x] = fmaf(eend, S[x], acc);
+      for (int j = 0; j < n; ++j) acc = fmaf(ek[j] * ks[j * dkp + r], vs[j * dvt + c], acc);
+      S[r * dvt + c] = fmaf(eend, S[r * dvt + c], acc);
     }
     for (int r = tid; r < dk; r += kThreads) {
       float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = fmaf(ek[j], ks[j * dk + r], acc);
+      for (int j = 0; j < n; ++j) acc = fmaf(ek[j], ks[j * dkp + r], acc);
       z[r] = fmaf(eend, z[r], acc);
     }
   }
   __syncthreads();
-  if (S_final)
-    for (int x = tid; x < dk * dv; x += kThreads) S_final[(size_t)bh * dk * dv + x] = S[x];
-  if (z_final)
+  if (S_final) {
+    for (int x = tid; x < dk * nv; x += kThreads) {
+      const int r = x / nv, c = x % nv;
+      S_final[((size_t)bh * dk + r) * dv + j0 + c] = S[r * dvt + c];
+    }
+  }
+  if (z_final && blockIdx.y == 0)
     for (int r = tid; r < dk; r += kThreads) z_final[(size_t)bh * dk + r] = z[r];
 }
 
 // ---------------------------------------------------------------------------
 // Per-channel gate.  One CTA per (b, h) and slice of dvt value columns, with
 // its slice of S (d_k x dvt) in shared memory; log_alpha is [B,H,L,d_k].
+// Rows of q, k and the log-decay prefix are padded to dk + 1 floats, as in the
+// normalised kernel.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
@@ -169,10 +191,11 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
                     const float *__restrict__ log_alpha, const float *S0, T *__restrict__ O,
                     float *S_final) {
   extern __shared__ float smem[];
-  float *qs = smem;          // [C][dk]  phi(q), then e^{Lam_i} phi(q_i)
-  float *ks = qs + C * dk;   // [C][dk]  phi(k), then e^{Lam_end - Lam_j} phi(k_j)
-  float *lam = ks + C * dk;  // [C][dk]  per-channel inclusive log-decay prefix
-  float *vs = lam + C * dk;  // [C][dvt]
+  const int dkp = dk + 1;
+  float *qs = smem;           // [C][dkp]  phi(q), then e^{Lam_i} phi(q_i)
+  float *ks = qs + C * dkp;   // [C][dkp]  phi(k), then e^{Lam_end - Lam_j} phi(k_j)
+  float *lam = ks + C * dkp;  // [C][dkp]  per-channel inclusive log-decay prefix
+  float *vs = lam + C * dkp;  // [C][dvt]
   float *P = vs + C * dvt;   // [C][C]
   float *S = P + C * C;      // [dk][dvt]
 
@@ -191,8 +214,9 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     const int n = min(C, L - s0);
     __syncthreads();
     for (int x = tid; x < n * dk; x += kThreads) {
-      qs[x] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
-      ks[x] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
+      const int t = x / dk, r = x % dk;
+      qs[t * dkp + r] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
+      ks[t * dkp + r] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
     }
     for (int x = tid; x < n * nv; x += kThreads) {
       const int t = x / nv, c = x % nv;
@@ -202,7 +226,7 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
       float acc = 0.f;
       for (int t = 0; t < n; ++t) {
         acc += log_alpha[(bhL + s0 + t) * dk + r];
-        lam[t * dk + r] = acc;
+        lam[t * dkp + r] = acc;
       }
     }
     __syncthreads();
@@ -211,20 +235,21 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
       float p = 0.f;
       if (j <= i)
         for (int c = 0; c < dk; ++c)
-          p = fmaf(qs[i * dk + c] * ks[j * dk + c], expf(lam[i * dk + c] - lam[j * dk + c]), p);
+          p = fmaf(qs[i * dkp + c] * ks[j * dkp + c], expf(lam[i * dkp + c] - lam[j * dkp + c]),
+                   p);
       P[i * C + j] = p;
     }
     __syncthreads();
     for (int x = tid; x < n * dk; x += kThreads) {  // fold the decays into q and k
-      const int r = x % dk;
-      qs[x] *= expf(lam[x]);
-      ks[x] *= expf(lam[(n - 1) * dk + r] - lam[x]);
+      const int y = (x / dk) * dkp + x % dk;
+      qs[y] *= expf(lam[y]);
+      ks[y] *= expf(lam[(n - 1) * dkp + x % dk] - lam[y]);
     }
     __syncthreads();
     for (int x = tid; x < n * nv; x += kThreads) {
       const int i = x / nv, c = x % nv;
       float acc = 0.f;
-      for (int r = 0; r < dk; ++r) acc = fmaf(qs[i * dk + r], S[r * dvt + c], acc);
+      for (int r = 0; r < dk; ++r) acc = fmaf(qs[i * dkp + r], S[r * dvt + c], acc);
       for (int j = 0; j <= i; ++j) acc = fmaf(P[i * C + j], vs[j * dvt + c], acc);
       O[(bhL + s0 + i) * dv + j0 + c] = from_f32<T>(acc);
     }
@@ -232,8 +257,8 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     for (int x = tid; x < dk * nv; x += kThreads) {
       const int r = x / nv, c = x % nv;
       float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = fmaf(ks[j * dk + r], vs[j * dvt + c], acc);
-      S[r * dvt + c] = fmaf(expf(lam[(n - 1) * dk + r]), S[r * dvt + c], acc);
+      for (int j = 0; j < n; ++j) acc = fmaf(ks[j * dkp + r], vs[j * dvt + c], acc);
+      S[r * dvt + c] = fmaf(expf(lam[(n - 1) * dkp + r]), S[r * dvt + c], acc);
     }
   }
   __syncthreads();
@@ -247,15 +272,38 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
 
 // ---------------------------------------------------------------------------
 // Delta rule, token by token.  CTA (b, h, slice of 32 value columns); warp w
-// owns slice columns 4w .. 4w+3; lane l owns rows l + 32 m.  Tokens are staged
-// through shared memory kTok at a time.
+// owns slice columns 4w .. 4w+3.  Lane 8 cl + g holds column 4w + cl, rows
+// VW g + 8 VW i + e (i < RPL / VW, e < VW) of it in registers: RPL = d_k / 8
+// rows, read from shared memory as VW-wide vectors (a warp's read of one
+// vector index covers 8 VW consecutive floats, once per column: no bank
+// conflicts).  The two dot products of a step are reductions over the 8 lanes
+// of a column (xor 1, 2, 4).  Tokens are staged through shared memory kTok at
+// a time, and each step's k and q are loaded while the previous step runs.
 constexpr int kTok = 32;
 constexpr int kDeltaCols = 32;
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+__device__ __forceinline__ float group8_sum(float x) {
+  x += __shfl_xor_sync(kFull, x, 1);
+  x += __shfl_xor_sync(kFull, x, 2);
+  x += __shfl_xor_sync(kFull, x, 4);
   return x;
+}
+
+template <int VW>
+__device__ __forceinline__ void load_rows(float *dst, const float *row, int g, int ni) {
+  // dst[VW i + e] = row[VW g + 8 VW i + e]
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i >= ni) break;
+    const float *p = row + VW * g + 8 * VW * i;
+    if constexpr (VW == 4) {
+      const float4 x = *reinterpret_cast<const float4 *>(p);
+      dst[4 * i] = x.x; dst[4 * i + 1] = x.y; dst[4 * i + 2] = x.z; dst[4 * i + 3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2 *>(p);
+      dst[2 * i] = x.x; dst[2 * i + 1] = x.y;
+    }
+  }
 }
 
 template <typename T, int DK>
@@ -263,26 +311,29 @@ __global__ void __launch_bounds__(kThreads)
 delta_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v, int L,
              int dv, int phi, const float *__restrict__ beta, const float *__restrict__ log_alpha,
              const float *S0, T *__restrict__ O, float *S_final) {
-  constexpr int MR = (DK + 31) / 32;  // rows per lane
-  __shared__ float qf[kTok][DK], kf[kTok][DK], vv[kTok][kDeltaCols], bt[kTok], at[kTok];
+  static_assert(DK % 16 == 0 && DK <= 128, "d_k");
+  constexpr int RPL = DK / 8;                // rows per lane
+  constexpr int VW = RPL < 4 ? RPL : 4;      // vector width of a row read
+  constexpr int NI = RPL / VW;               // vectors per lane
+  __shared__ __align__(16) float qf[kTok][DK];
+  __shared__ __align__(16) float kf[kTok][DK];
+  __shared__ float vv[kTok][kDeltaCols], bt[kTok], at[kTok];
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
+  const int g = lane & 7, cl = lane >> 3;
   const int bh = blockIdx.x;
   const int j0 = blockIdx.y * kDeltaCols;
   const int nv = min(kDeltaCols, dv - j0);
-  const int cb = warp * 4;  // first slice column of this warp
+  const int c = warp * 4 + cl;  // this lane's slice column
+  const bool live = c < nv;
   const size_t bhL = (size_t)bh * L;
+  auto row_of = [&](int m) { return VW * g + 8 * VW * (m / VW) + m % VW; };
 
-  float s[MR][4];
+  float s[RPL];
 #pragma unroll
-  for (int m = 0; m < MR; ++m)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int r = lane + 32 * m;
-      s[m][c] = (S0 && r < DK && cb + c < nv) ? S0[((size_t)bh * DK + r) * dv + j0 + cb + c]
-                                              : 0.f;
-    }
+  for (int m = 0; m < RPL; ++m)
+    s[m] = (S0 && live) ? S0[((size_t)bh * DK + row_of(m)) * dv + j0 + c] : 0.f;
 
   for (int t0 = 0; t0 < L; t0 += kTok) {
     const int nt = min(kTok, L - t0);
@@ -292,53 +343,51 @@ delta_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restri
       kf[x / DK][x % DK] = feature_map_precise(phi, to_f32(k[(bhL + t0) * DK + x]));
     }
     for (int x = tid; x < nt * kDeltaCols; x += kThreads) {
-      const int t = x / kDeltaCols, c = x % kDeltaCols;
-      vv[t][c] = c < nv ? to_f32(v[(bhL + t0 + t) * dv + j0 + c]) : 0.f;
+      const int t = x / kDeltaCols, cc = x % kDeltaCols;
+      vv[t][cc] = cc < nv ? to_f32(v[(bhL + t0 + t) * dv + j0 + cc]) : 0.f;
     }
     for (int t = tid; t < nt; t += kThreads) {
       bt[t] = beta[bhL + t0 + t];
       at[t] = log_alpha ? expf(log_alpha[bhL + t0 + t]) : 1.f;
     }
     __syncthreads();
+    float kr[RPL], qr[RPL];
+    load_rows<VW>(kr, kf[0], g, NI);
+    load_rows<VW>(qr, qf[0], g, NI);
     for (int t = 0; t < nt; ++t) {
-      float kr[MR], qr[MR];
-#pragma unroll
-      for (int m = 0; m < MR; ++m) {
-        const int r = lane + 32 * m;
-        kr[m] = r < DK ? kf[t][r] : 0.f;
-        qr[m] = r < DK ? qf[t][r] : 0.f;
-      }
+      float kn[RPL], qn[RPL];  // the next step's rows, loaded ahead
+      const int tn = t + 1 < nt ? t + 1 : t;
+      load_rows<VW>(kn, kf[tn], g, NI);
+      load_rows<VW>(qn, qf[tn], g, NI);
       const float a = at[t], b = bt[t];
-      float o[4];
+      float u0 = 0.f, u1 = 0.f;  // (k^T S)_c, two partial sums
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float u = 0.f;  // (k^T S)_c
-#pragma unroll
-        for (int m = 0; m < MR; ++m) u = fmaf(kr[m], s[m][c], u);
-        u = warp_sum(u);
-        const float w = b * (vv[t][cb + c] - a * u);  // what is written along k
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < MR; ++m) {
-          s[m][c] = fmaf(kr[m], w, a * s[m][c]);
-          acc = fmaf(qr[m], s[m][c], acc);
-        }
-        o[c] = warp_sum(acc);
+      for (int m = 0; m < RPL; m += 2) {
+        u0 = fmaf(kr[m], s[m], u0);
+        u1 = fmaf(kr[m + 1], s[m + 1], u1);
       }
-      if (lane < 4 && cb + lane < nv) {
-        const float mine = lane == 0 ? o[0] : lane == 1 ? o[1] : lane == 2 ? o[2] : o[3];
-        O[(bhL + t0 + t) * dv + j0 + cb + lane] = from_f32<T>(mine);
+      const float u = group8_sum(u0 + u1);
+      const float w = b * (vv[t][c] - a * u);  // what is written along k
+      float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+      for (int m = 0; m < RPL; m += 2) {
+        s[m] = fmaf(kr[m], w, a * s[m]);
+        s[m + 1] = fmaf(kr[m + 1], w, a * s[m + 1]);
+        o0 = fmaf(qr[m], s[m], o0);
+        o1 = fmaf(qr[m + 1], s[m + 1], o1);
+      }
+      const float o = group8_sum(o0 + o1);
+      if (g == 0 && live) O[(bhL + t0 + t) * dv + j0 + c] = from_f32<T>(o);
+#pragma unroll
+      for (int m = 0; m < RPL; ++m) {
+        kr[m] = kn[m];
+        qr[m] = qn[m];
       }
     }
   }
-  if (S_final) {
+  if (S_final && live) {
 #pragma unroll
-    for (int m = 0; m < MR; ++m)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int r = lane + 32 * m;
-        if (r < DK && cb + c < nv) S_final[((size_t)bh * DK + r) * dv + j0 + cb + c] = s[m][c];
-      }
+    for (int m = 0; m < RPL; ++m) S_final[((size_t)bh * DK + row_of(m)) * dv + j0 + c] = s[m];
   }
 }
 
@@ -350,15 +399,19 @@ cudaError_t allow_smem(Kern kern, size_t smem) {
 template <typename T>
 cudaError_t launch_normalised_t(const VariantArgs &a) {
   const int C = a.chunk;
-  const size_t smem = sizeof(float) * ((size_t)2 * C * a.dk + (size_t)C * a.dv + (size_t)C * C +
-                                       (size_t)a.dk * a.dv + a.dk + 4 * C);
+  // one slice when z_final overwrites z0 (see the kernel), else 32 columns per CTA
+  const bool z_alias = a.z0 && a.z0 == a.z_final;
+  const int dvt = (z_alias || a.dv < 32) ? a.dv : 32;
+  const size_t smem = sizeof(float) * ((size_t)2 * C * (a.dk + 1) + (size_t)C * dvt +
+                                       (size_t)C * C + (size_t)a.dk * dvt + a.dk + 4 * C);
   auto kern = normalised_kernel<T>;
   cudaError_t e = allow_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<(unsigned)(a.B * a.H), kThreads, smem, a.stream>>>(
+  dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dv + dvt - 1) / dvt));
+  kern<<<grid, kThreads, smem, a.stream>>>(
       static_cast<const T *>(a.q), static_cast<const T *>(a.k), static_cast<const T *>(a.v),
-      a.H, a.L, a.dk, a.dv, C, a.phi, a.decay_kind, a.decay, a.S0, a.z0, static_cast<T *>(a.O),
-      a.S_final, a.z_final);
+      a.H, a.L, a.dk, a.dv, C, dvt, a.phi, a.decay_kind, a.decay, a.S0, a.z0,
+      static_cast<T *>(a.O), a.S_final, a.z_final);
   return cudaGetLastError();
 }
 
@@ -366,8 +419,8 @@ template <typename T>
 cudaError_t launch_channel_gate_t(const VariantArgs &a) {
   const int C = a.chunk;
   const int dvt = a.dv < 32 ? a.dv : 32;
-  const size_t smem = sizeof(float) * ((size_t)3 * C * a.dk + (size_t)C * dvt + (size_t)C * C +
-                                       (size_t)a.dk * dvt);
+  const size_t smem = sizeof(float) * ((size_t)3 * C * (a.dk + 1) + (size_t)C * dvt +
+                                       (size_t)C * C + (size_t)a.dk * dvt);
   auto kern = channel_gate_kernel<T>;
   cudaError_t e = allow_smem(kern, smem);
   if (e != cudaSuccess) return e;
