@@ -381,7 +381,7 @@ def bench_variants(w, steps, warmup, dev, peaks, peak_kind):
         ms = statistics.mean(a.elapsed_time(b) for a, b in zip(starts, ends))
         rl = roofline(variant_bytes(form, w), 0, ms / 1e3, peaks, peak_kind, False)
         out[form] = {"per_call_ms": round(ms, 4),
-                     "tokens_per_s": w.B * w.H * w.L / (ms / 1e3), "roofline": rl}
+                     "tokens_per_s": w.B * w.L / (ms / 1e3), "roofline": rl}
     return out
 
 
