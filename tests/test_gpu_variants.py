@@ -90,6 +90,23 @@ def test_delta_matches_oracle(case):
     parity.check(S.cpu(), S_ref, dtype, "S")
 
 
+@pytest.mark.parametrize("L,d,dtype", [(2, 16, "f32"), (31, 128, "bf16"), (32, 64, "f32"),
+                                       (33, 32, "f32"), (64, 128, "f32"), (65, 64, "bf16")])
+def test_delta_short_sequences(L, d, dtype):
+    """Short sequences with gate and initial state around the kernel's staging
+    of 32 tokens at a time: inside one pass, exactly one, one and a token, two,
+    two and a token."""
+    inp = W.make_variant_inputs("delta", 2, 3, L, d, d, dtype, seed=12, with_state=True)
+    api.la_set_feature_map("identity")
+    O, S = api.la_delta_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["beta"]),
+                            _d(inp["log_alpha"]), _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.delta(inp["q"], inp["k"], inp["v"], inp["beta"], inp["log_alpha"],
+                                phi="identity", S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, dtype, "O")
+    parity.check(S.cpu(), S_ref, dtype, "S")
+
+
 def test_delta_recalls_the_key_just_written():
     """beta = 1 with unit keys and no gate: reading with the key just written
     returns its value exactly (the write replaces the old association)."""
