@@ -26,7 +26,8 @@ SIGNATURES = {
     "la_noncausal_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "la_noncausal_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "la_normalised_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
-                               _vp, _vp, _vp, _vp]),
+                               _vp, _vp, _vp, _vp, _sz, _vp]),
+    "la_normalised_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "la_channel_gate_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
                                  _vp]),
     "la_delta_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),

@@ -216,8 +216,14 @@ def _qkv(q, k, v, O):
     return O
 
 
+def la_normalised_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk=64, dtype=torch.bfloat16) -> int:
+    return int(_native.load().la_normalised_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk,
+                                                                DTYPE[dtype]))
+
+
 def la_normalised_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, z0=None,
-                      O=None, S_final=None, z_final=None, want_final_state=True, stream=None):
+                      O=None, S_final=None, z_final=None, want_final_state=True,
+                      workspace=None, stream=None):
     """Normalised form o_t = phi(q_t)^T S_t / phi(q_t)^T z_t over [B,H,L,d]
     sequences, z the decayed key sum.  Returns ``(O, S_final, z_final)``.
     ``S0`` fp32 [B,H,d_k,d_v], ``z0`` fp32 [B,H,d_k]; the outputs may be the
@@ -226,10 +232,16 @@ def la_normalised_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None,
     S_final, z_final = _state_bufs(q, v, want_final_state, S_final, True, z_final)
     _need_cuda(q, k, v, decay, S0, z0, O, S_final, z_final)
     B, H, L, dk = q.shape
+    dv = v.shape[-1]
+    if workspace is None:
+        workspace = _workspace(la_normalised_fwd_workspace_bytes(B, H, L, dk, dv, chunk, q.dtype),
+                               q.device)
     _check(_native.load().la_normalised_fwd(
-        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, v.shape[-1], chunk,
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, chunk,
         DECAY[decay_kind], _ptr(decay), _ptr(S0), _ptr(z0), _ptr(O), _ptr(S_final),
-        _ptr(z_final), _stream(stream)))
+        _ptr(z_final), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return O, S_final, z_final
 
 

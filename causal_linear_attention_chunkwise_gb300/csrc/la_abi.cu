@@ -37,6 +37,8 @@ la_status cuda_fail(cudaError_t e, const char *where) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
 bool supported_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
 
 // Copy `src` to `dst` (or zero `dst` when src is null): the state after no tokens.
@@ -279,10 +281,18 @@ la_status la_decode_step(const void *q, const void *k, const void *v, int dtype,
   return ok();
 }
 
+size_t la_normalised_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk,
+                                         int dtype) {
+  if (B <= 0 || H <= 0 || L <= 0 || !supported_d(d_k) || !supported_d(d_v)) return 0;
+  return align256(la_chunk_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk, dtype)) +
+         normaliser_workspace_bytes(B, H, L, d_k);
+}
+
 la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dtype, int B,
                             int H, int L, int d_k, int d_v, int chunk, int decay_kind,
                             const float *decay, const float *S0, const float *z0, void *O,
-                            float *S_final, float *z_final, void *cuda_stream) {
+                            float *S_final, float *z_final, void *workspace, size_t ws_bytes,
+                            void *cuda_stream) {
   const char *fn = "la_normalised_fwd";
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   if (decay_kind < LA_DECAY_NONE || decay_kind > LA_DECAY_GATE_LOGIT)
@@ -293,10 +303,32 @@ la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dty
   la_status s = check_variant(fn, q, k, v, dtype, B, H, L, d_k, d_v, chunk, true, S0, z0, O,
                               S_final, z_final, st, &done);
   if (s != LA_OK || done) return s;
-  VariantArgs a{VARIANT_NORMALISED, q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(),
-                decay_kind, decay_kind == LA_DECAY_NONE ? nullptr : decay, nullptr, S0, z0, O,
-                S_final, z_final, st};
-  return run_variant(fn, a);
+  const size_t num_ws = la_chunk_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk, dtype);
+  const size_t need = align256(num_ws) + normaliser_workspace_bytes(B, H, L, d_k);
+  if (!workspace || ws_bytes < need)
+    return fail(LA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace ? ws_bytes : (size_t)0);
+  if (!aligned16(workspace))
+    return fail(LA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
+  const int phi = g_phi.load();
+  const float *dec = decay_kind == LA_DECAY_NONE ? nullptr : decay;
+  // The numerator phi(q_t)^T S_t goes to O (and S_final) through the prefill
+  // kernels; the normaliser then forms z and divides O in place.
+  PrefillArgs a{q, k, v, dtype, B, H, L, d_k, d_v, chunk, phi, decay_kind, dec, S0, O,
+                S_final, num_ws ? workspace : nullptr, num_ws, st};
+  cudaError_t e;
+  const char *why = nullptr;
+  if (prefill_tc_supported(a)) {
+    e = launch_prefill_tc(a, &why);
+  } else {
+    e = launch_prefill_simt(a);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, why ? why : fn);
+  NormaliserArgs n{q, k, dtype, B, H, L, d_k, d_v, phi, decay_kind, dec, z0, O, z_final,
+                   static_cast<char *>(workspace) + align256(num_ws), st};
+  e = launch_normaliser(n);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return ok();
 }
 
 la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int dtype, int B,
@@ -310,7 +342,7 @@ la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int d
   if (s != LA_OK || done) return s;
   if (!log_alpha) return fail(LA_ERR_INVALID_ARG, "%s: log_alpha must be non-null", fn);
   VariantArgs a{VARIANT_CHANNEL_GATE, q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(),
-                LA_DECAY_NONE, log_alpha, nullptr, S0, nullptr, O, S_final, nullptr, st};
+                log_alpha, nullptr, S0, O, S_final, st};
   return run_variant(fn, a);
 }
 
@@ -324,8 +356,8 @@ la_status la_delta_fwd(const void *q, const void *k, const void *v, int dtype, i
                               S_final, nullptr, st, &done);
   if (s != LA_OK || done) return s;
   if (!beta) return fail(LA_ERR_INVALID_ARG, "%s: beta must be non-null", fn);
-  VariantArgs a{VARIANT_DELTA, q, k, v, dtype, B, H, L, d_k, d_v, 0, g_phi.load(),
-                LA_DECAY_NONE, log_alpha, beta, S0, nullptr, O, S_final, nullptr, st};
+  VariantArgs a{VARIANT_DELTA, q, k, v, dtype, B, H, L, d_k, d_v, 0, g_phi.load(), log_alpha,
+                beta, S0, O, S_final, st};
   return run_variant(fn, a);
 }
 

@@ -60,25 +60,41 @@ struct NoncausalArgs {
 size_t noncausal_workspace_bytes(int B, int H, int L, int d);
 cudaError_t launch_noncausal(const NoncausalArgs &a, const char **why);
 
-// Normalised form, per-channel gate and delta rule (CUDA cores, fp32 or bf16
-// inputs, d_k, d_v <= 128).
-enum VariantForm { VARIANT_NORMALISED = 0, VARIANT_CHANNEL_GATE = 1, VARIANT_DELTA = 2 };
+// Per-channel gate and delta rule (CUDA cores, fp32 or bf16 inputs,
+// d_k, d_v <= 128).
+enum VariantForm { VARIANT_CHANNEL_GATE = 1, VARIANT_DELTA = 2 };
 struct VariantArgs {
   int form;  // VariantForm
   const void *q, *k, *v;
   int dtype;
   int B, H, L, dk, dv, chunk;  // chunk: 1..64 (unused by the delta rule)
   int phi;
-  int decay_kind;      // normalised form: LA_DECAY_*
-  const float *decay;  // normalised: as la_chunk_fwd; channel gate: log alpha [B,H,L,dk];
-                       // delta rule: log alpha [B,H,L] or null
+  const float *decay;  // channel gate: log alpha [B,H,L,dk]; delta rule: log alpha [B,H,L] or null
   const float *beta;   // delta rule: [B,H,L]
-  const float *S0, *z0;
+  const float *S0;
   void *O;
-  float *S_final, *z_final;
+  float *S_final;
   cudaStream_t stream;
 };
 cudaError_t launch_variant(const VariantArgs &a);
+
+// Denominator of the normalised form and the division of O by it, after the
+// numerator has been written to O (d_k <= 128).
+struct NormaliserArgs {
+  const void *q, *k;
+  int dtype;
+  int B, H, L, dk, dv;
+  int phi;
+  int decay_kind;
+  const float *decay;
+  const float *z0;
+  void *O;
+  float *z_final;
+  void *workspace;  // normaliser_workspace_bytes(...) bytes, float-aligned
+  cudaStream_t stream;
+};
+size_t normaliser_workspace_bytes(int B, int H, int L, int dk);
+cudaError_t launch_normaliser(const NormaliserArgs &a);
 
 // Decode step.
 bool decode_supported(int dk, int dv);

@@ -1,9 +1,6 @@
-// la_variants.cu -- CUDA-core kernels for three forms of the state recurrence
-// beyond the plain one (fp32 arithmetic, fp32 or bf16 inputs):
+// la_variants.cu -- CUDA-core kernels for two further forms of the state
+// recurrence (fp32 arithmetic, fp32 or bf16 inputs):
 //
-//   normalised    o_t = phi(q_t)^T S_t / phi(q_t)^T z_t,  z_t = a_t z_{t-1} + phi(k_t)
-//                 ("Linear / sparse attention tutorial" Q11 and section 2.2: z is
-//                 the state of one extra value column of ones, so it decays with S)
 //   channel gate  S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T, alpha_t in (0,1]^{d_k}
 //                 ("Linear / sparse attention tutorial" Q21, GLA)
 //   delta rule    S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
@@ -11,24 +8,20 @@
 //                 delta_rule_recurrent, with the state transposed to [d_k, d_v];
 //                 "Linear / sparse attention tutorial" Q21 for the gate alpha_t)
 //
-// with o_t = phi(q_t)^T S_t (update before read) in all three.
+// with o_t = phi(q_t)^T S_t (update before read) in both.
 //
-// The first two are chunkwise, like the SIMT prefill kernel: per chunk of
+// The channel gate is chunkwise, like the SIMT prefill kernel: per chunk of
 // n <= C tokens the intra-chunk scores are formed exactly with their decay
 // (every exponent is a difference Lam_i - Lam_j with i >= j, so it is <= 0 for
 // log decays <= 0), the inter-chunk read uses the state of the previous chunk
-// and the state is then advanced by the whole chunk.  The normalised form adds
-// the denominator as the same two parts with v = 1: the decayed row sums of
-// the scores plus e^{Lam_i} phi(q_i).z.  The channel gate has one cumulative
-// log decay per key channel, so its score for (i, j) is
-// sum_c q_ic k_jc e^{Lam_ic - Lam_jc}; once the scores are formed the decays
-// are folded into q (e^{Lam_ic}) and k (e^{Lam_end,c - Lam_jc}) in place.
+// and the state is then advanced by the whole chunk.  With one cumulative log
+// decay per key channel, the score for (i, j) is sum_c q_ic k_jc
+// e^{Lam_ic - Lam_jc}; once the scores are formed the decays are folded into q
+// (e^{Lam_ic}) and k (e^{Lam_end,c - Lam_jc}) in place.
 //
 // The delta rule runs token by token: each step erases along k before it
 // writes, and every column of S is independent of the others
-// (S[:, c] <- a S[:, c] + k (beta (v_c - a k^T S[:, c]))), so a CTA owns 32
-// value columns, a warp 4 of them, and a lane rows lane + 32 m of those
-// columns in registers.  The two dot products of a step are warp reductions.
+// (S[:, c] <- a S[:, c] + k (beta (v_c - a k^T S[:, c]))).
 #include <cuda_bf16.h>
 
 #include "../../include/la_gb300.h"
@@ -42,148 +35,12 @@ constexpr int kThreads = 256;
 constexpr int kMaxChunk = 64;
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ float log_decay_at(int kind, const float *__restrict__ decay, int h,
-                                              size_t bhL, int t) {
-  switch (kind) {
-    case LA_DECAY_HEAD: return decay[h];
-    case LA_DECAY_TOKEN: return decay[bhL + t];
-    case LA_DECAY_GATE_LOGIT: return neg_softplus(decay[bhL + t]);
-    default: return 0.f;
-  }
-}
-
-// lam[i] = sum of the log decays of tokens s0 .. s0 + i (one warp, lanes 0..31).
-__device__ __forceinline__ void chunk_log_prefix(float *lam, int n, int kind,
-                                                 const float *__restrict__ decay, int h,
-                                                 size_t bhL, int s0, int lane) {
-  float carry = 0.f;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    float x = i < n ? log_decay_at(kind, decay, h, bhL, s0 + i) : 0.f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_up_sync(kFull, x, off);
-      if (lane >= off) x += y;
-    }
-    if (i < n) lam[i] = carry + x;
-    carry += __shfl_sync(kFull, x, 31);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Normalised form.  One CTA per (b, h) and slice of dvt value columns, with
-// its slice of S (d_k x dvt) and the whole of z (d_k) in shared memory.  Every
-// slice advances its own copy of z (d_k values per chunk, the same in all
-// slices) for its denominators; slice 0 writes z_final.  When z_final aliases
-// z0 the launcher uses a single slice, so that no CTA reads z0 after another
-// has written it.  q and k rows are padded to dk + 1 floats: the score loop
-// reads one k row per lane, and a stride of dk (a multiple of 16) would put a
-// warp's reads in one or two shared-memory banks.
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-normalised_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
-                  int H, int L, int dk, int dv, int C, int dvt, int phi, int decay_kind,
-                  const float *__restrict__ decay, const float *S0, const float *z0,
-                  T *__restrict__ O, float *S_final, float *z_final) {
-  extern __shared__ float smem[];
-  const int dkp = dk + 1;
-  float *qs = smem;          // [C][dkp]  phi(q)
-  float *ks = qs + C * dkp;  // [C][dkp]  phi(k)
-  float *vs = ks + C * dkp;  // [C][dvt]  value slice
-  float *P = vs + C * dvt;   // [C][C]    masked, decayed scores
-  float *S = P + C * C;      // [dk][dvt] state slice
-  float *z = S + dk * dvt;   // [dk]
-  float *lam = z + dk;       // [C]       inclusive log-decay prefix
-  float *den = lam + C;      // [C]       denominators
-  float *eq = den + C;       // [C]       e^{Lam_i}: weight of the inter-chunk read of row i
-  float *ek = eq + C;        // [C]       e^{Lam_end - Lam_j}: weight of key j in the update
-
-  const int tid = threadIdx.x;
-  const int bh = blockIdx.x;
-  const int h = bh % H;
-  const int j0 = blockIdx.y * dvt;
-  const int nv = min(dvt, dv - j0);
-  const size_t bhL = (size_t)bh * L;
-
-  for (int x = tid; x < dk * nv; x += kThreads) {
-    const int r = x / nv, c = x % nv;
-    S[r * dvt + c] = S0 ? S0[((size_t)bh * dk + r) * dv + j0 + c] : 0.f;
-  }
-  for (int r = tid; r < dk; r += kThreads) z[r] = z0 ? z0[(size_t)bh * dk + r] : 0.f;
-
-  for (int s0 = 0; s0 < L; s0 += C) {
-    const int n = min(C, L - s0);
-    __syncthreads();  // the previous chunk's readers are done
-    for (int x = tid; x < n * dk; x += kThreads) {
-      const int t = x / dk, r = x % dk;
-      qs[t * dkp + r] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
-      ks[t * dkp + r] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
-    }
-    for (int x = tid; x < n * nv; x += kThreads) {
-      const int t = x / nv, c = x % nv;
-      vs[t * dvt + c] = to_f32(v[(bhL + s0 + t) * dv + j0 + c]);
-    }
-    if (tid < 32) chunk_log_prefix(lam, n, decay_kind, decay, h, bhL, s0, tid);
-    __syncthreads();
-    for (int x = tid; x < n * n; x += kThreads) {
-      const int i = x / n, j = x % n;
-      float p = 0.f;
-      if (j <= i) {
-        float dot = 0.f;
-        for (int c = 0; c < dk; ++c) dot = fmaf(qs[i * dkp + c], ks[j * dkp + c], dot);
-        p = dot * expf(lam[i] - lam[j]);
-      }
-      P[i * C + j] = p;
-    }
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {  // phi(q_i)^T z_i, in its two parts
-      float inter = 0.f;
-      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dkp + r], z[r], inter);
-      float intra = 0.f;
-      for (int j = 0; j <= i; ++j) intra += P[i * C + j];
-      eq[i] = expf(lam[i]);
-      ek[i] = expf(lam[n - 1] - lam[i]);
-      den[i] = fmaf(eq[i], inter, intra);
-    }
-    __syncthreads();
-    for (int x = tid; x < n * nv; x += kThreads) {
-      const int i = x / nv, c = x % nv;
-      float inter = 0.f;
-      for (int r = 0; r < dk; ++r) inter = fmaf(qs[i * dkp + r], S[r * dvt + c], inter);
-      float intra = 0.f;
-      for (int j = 0; j <= i; ++j) intra = fmaf(P[i * C + j], vs[j * dvt + c], intra);
-      O[(bhL + s0 + i) * dv + j0 + c] = from_f32<T>(fmaf(eq[i], inter, intra) / den[i]);
-    }
-    __syncthreads();  // every read of S and z for this chunk's output is done
-    const float eend = eq[n - 1];
-    for (int x = tid; x < dk * nv; x += kThreads) {
-      const int r = x / nv, c = x % nv;
-      float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = fmaf(ek[j] * ks[j * dkp + r], vs[j * dvt + c], acc);
-      S[r * dvt + c] = fmaf(eend, S[r * dvt + c], acc);
-    }
-    for (int r = tid; r < dk; r += kThreads) {
-      float acc = 0.f;
-      for (int j = 0; j < n; ++j) acc = fmaf(ek[j], ks[j * dkp + r], acc);
-      z[r] = fmaf(eend, z[r], acc);
-    }
-  }
-  __syncthreads();
-  if (S_final) {
-    for (int x = tid; x < dk * nv; x += kThreads) {
-      const int r = x / nv, c = x % nv;
-      S_final[((size_t)bh * dk + r) * dv + j0 + c] = S[r * dvt + c];
-    }
-  }
-  if (z_final && blockIdx.y == 0)
-    for (int r = tid; r < dk; r += kThreads) z_final[(size_t)bh * dk + r] = z[r];
-}
-
 // ---------------------------------------------------------------------------
 // Per-channel gate.  One CTA per (b, h) and slice of dvt value columns, with
 // its slice of S (d_k x dvt) in shared memory; log_alpha is [B,H,L,d_k].
-// Rows of q, k and the log-decay prefix are padded to dk + 1 floats, as in the
-// normalised kernel.
+// Rows of q, k and the log-decay prefix are padded to dk + 1 floats: the score
+// loop reads one k row per lane, and a stride of dk (a multiple of 16) would put
+// a warp's reads in one or two shared-memory banks.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
@@ -397,25 +254,6 @@ cudaError_t allow_smem(Kern kern, size_t smem) {
 }
 
 template <typename T>
-cudaError_t launch_normalised_t(const VariantArgs &a) {
-  const int C = a.chunk;
-  // one slice when z_final overwrites z0 (see the kernel), else 32 columns per CTA
-  const bool z_alias = a.z0 && a.z0 == a.z_final;
-  const int dvt = (z_alias || a.dv < 32) ? a.dv : 32;
-  const size_t smem = sizeof(float) * ((size_t)2 * C * (a.dk + 1) + (size_t)C * dvt +
-                                       (size_t)C * C + (size_t)a.dk * dvt + a.dk + 4 * C);
-  auto kern = normalised_kernel<T>;
-  cudaError_t e = allow_smem(kern, smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(a.B * a.H), (unsigned)((a.dv + dvt - 1) / dvt));
-  kern<<<grid, kThreads, smem, a.stream>>>(
-      static_cast<const T *>(a.q), static_cast<const T *>(a.k), static_cast<const T *>(a.v),
-      a.H, a.L, a.dk, a.dv, C, dvt, a.phi, a.decay_kind, a.decay, a.S0, a.z0,
-      static_cast<T *>(a.O), a.S_final, a.z_final);
-  return cudaGetLastError();
-}
-
-template <typename T>
 cudaError_t launch_channel_gate_t(const VariantArgs &a) {
   const int C = a.chunk;
   const int dvt = a.dv < 32 ? a.dv : 32;
@@ -459,8 +297,6 @@ cudaError_t launch_variant(const VariantArgs &a) {
     return cudaErrorInvalidValue;
   const bool f32 = a.dtype == LA_F32;
   switch (a.form) {
-    case VARIANT_NORMALISED:
-      return f32 ? launch_normalised_t<float>(a) : launch_normalised_t<__nv_bfloat16>(a);
     case VARIANT_CHANNEL_GATE:
       return f32 ? launch_channel_gate_t<float>(a) : launch_channel_gate_t<__nv_bfloat16>(a);
     case VARIANT_DELTA:

@@ -161,9 +161,9 @@ la_status la_noncausal_fwd(const void *q, const void *k, const void *v, int dtyp
 size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v);
 
 /*
- * Three further forms of the recurrence, on the CUDA cores (fp32 arithmetic;
- * q, k, v and O in dtype = LA_F32 or LA_BF16; states fp32).  Each runs over
- * whole sequences like la_chunk_fwd, and each is also its own decode step:
+ * Three further forms of the recurrence (q, k, v and O in dtype = LA_F32 or
+ * LA_BF16; states fp32).  Each runs over whole sequences like la_chunk_fwd,
+ * and each is also its own decode step:
  * with L = 1 and the output state aliasing the input state, one call advances
  * every sequence by one token.  phi is the one set by la_set_feature_map.
  * Supported: d_k, d_v in {16, 32, 64, 128}; chunk 1..64 where one is taken
@@ -173,6 +173,7 @@ size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v);
  * enum), LA_ERR_UNSUPPORTED (a d or chunk outside the list), LA_ERR_CUDA.
  * Pointers are device pointers owned by the caller, row-major, 16-byte
  * aligned; the calls are asynchronous on `cuda_stream` and allocate nothing.
+ * The per-channel gate and the delta rule run on the CUDA cores in fp32.
  */
 
 /*
@@ -182,20 +183,28 @@ size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v);
  *     S_t = a_t S_{t-1} + phi(k_t) v_t^T,   z_t = a_t z_{t-1} + phi(k_t),
  *     o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t).
  *
- * There is no epsilon in the denominator: choose a positive feature map
- * (LA_PHI_ELU1), as the tutorial does, or the quotient may be undefined.
+ * The numerator runs on the same kernels as la_chunk_fwd (the tensor-core
+ * kernels for bf16 with d_k = d_v in {64, 128} and chunk 64), then a scan of z
+ * forms the denominators and divides O in place.  There is no epsilon in the
+ * denominator: choose a positive feature map (LA_PHI_ELU1), as the tutorial
+ * does, or the quotient may be undefined.
  *
  *   q, k   [B,H,L,d_k] dtype;  v, O [B,H,L,d_v] dtype
  *   decay_kind / decay   as for la_chunk_fwd
  *   S0     [B,H,d_k,d_v] fp32 or NULL (zero);  z0 [B,H,d_k] fp32 or NULL (zero)
  *   S_final, z_final   the states after the last token, or NULL; each may be
  *          the same buffer as S0 / z0.
+ *   workspace  device scratch of la_normalised_fwd_workspace_bytes(...) bytes
+ *          (never 0 for a non-empty problem); ws_bytes = its size.
  */
 la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dtype,
                             int B, int H, int L, int d_k, int d_v, int chunk,
                             int decay_kind, const float *decay,
                             const float *S0, const float *z0, void *O,
-                            float *S_final, float *z_final, void *cuda_stream);
+                            float *S_final, float *z_final,
+                            void *workspace, size_t ws_bytes, void *cuda_stream);
+size_t la_normalised_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk,
+                                         int dtype);
 
 /*
  * Per-channel (diagonal) gate, as in GLA ("Linear / sparse attention

@@ -151,19 +151,31 @@ def test_variant_validation_before_any_device_work(lib):
     arguments before any device work."""
     p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
     odd = ctypes.c_void_p(0x1008)
-    nf = lambda *a: lib.la_normalised_fwd(*a)  # noqa: E731
-    # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, decay_kind, decay, S0, z0, O, S_final, z_final, stream)
-    assert nf(p, p, p, 7, 1, 1, 8, 16, 16, 64, 0, None, None, None, p, None, None, None) == 1
-    assert nf(p, p, p, 1, 1, 1, 8, 48, 16, 64, 0, None, None, None, p, None, None, None) == 2
-    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 65, 0, None, None, None, p, None, None, None) == 2
-    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 0, 0, None, None, None, p, None, None, None) == 1
-    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 5, None, None, None, p, None, None, None) == 1
-    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 3, None, None, None, p, None, None, None) == 1
+    W = 1 << 20
+    nf = lambda *a: lib.la_normalised_fwd(*a, p, W, None)  # noqa: E731
+    # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, decay_kind, decay, S0, z0, O, S_final, z_final)
+    # + (workspace, ws_bytes, stream)
+    assert nf(p, p, p, 7, 1, 1, 8, 16, 16, 64, 0, None, None, None, p, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 48, 16, 64, 0, None, None, None, p, None, None) == 2
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 65, 0, None, None, None, p, None, None) == 2
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 0, 0, None, None, None, p, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 5, None, None, None, p, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 3, None, None, None, p, None, None) == 1
     assert b"decay pointer" in lib.la_last_error()
-    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, None, None, None, None, None) == 1
-    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, odd, p, None, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, None, None, None, None) == 1
+    assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, odd, p, None, None) == 1
     assert b"16-byte" in lib.la_last_error()
-    assert nf(p, p, p, 1, 0, 3, 8, 16, 16, 64, 0, None, None, None, p, None, None, None) == 0
+    assert nf(p, p, p, 1, 0, 3, 8, 16, 16, 64, 0, None, None, None, p, None, None) == 0
+    # the workspace: never empty for a non-empty problem, checked before any launch
+    need = lib.la_normalised_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 1)
+    assert need > lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 1) > 0
+    assert lib.la_normalised_fwd_workspace_bytes(1, 1, 300, 16, 16, 64, 0) > 0
+    assert lib.la_normalised_fwd_workspace_bytes(1, 1, 0, 16, 16, 64, 0) == 0
+    assert lib.la_normalised_fwd(p, p, p, 1, 4, 16, 4096, 64, 64, 64, 0, None, None, None, p,
+                                 None, None, p, need - 1, None) == 1
+    assert b"workspace" in lib.la_last_error()
+    assert lib.la_normalised_fwd(p, p, p, 1, 4, 16, 4096, 64, 64, 64, 0, None, None, None, p,
+                                 None, None, None, 0, None) == 1
     cg = lambda *a: lib.la_channel_gate_fwd(*a)  # noqa: E731
     # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, log_alpha, S0, O, S_final, stream)
     assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, None, None, p, None, None) == 1
