@@ -16,8 +16,12 @@
 // log decays <= 0), the inter-chunk read uses the state of the previous chunk
 // and the state is then advanced by the whole chunk.  With one cumulative log
 // decay per key channel, the score for (i, j) is sum_c q_ic k_jc
-// e^{Lam_ic - Lam_jc}; once the scores are formed the decays are folded into q
-// (e^{Lam_ic}) and k (e^{Lam_end,c - Lam_jc}) in place.
+// e^{Lam_ic - Lam_jc}.  When every cumulative log decay of the chunk lies in
+// [-80, 80] the factors split: q~_i = e^{Lam_i} q_i, k~_j = e^{-Lam_j} k_j and
+// the score is the plain dot product q~_i . k~_j (the state then advances as
+// S <- e^{Lam_end} (S + k~^T V)).  Otherwise each score term takes its own
+// factor, and the decays are folded into q (e^{Lam_ic}) and k
+// (e^{Lam_end,c - Lam_jc}) once the scores are formed.
 //
 // The delta rule runs token by token: each step erases along k before it
 // writes, and every column of S is independent of the others
@@ -33,6 +37,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxChunk = 64;
+constexpr float kSplitMax = 80.f;  // e^{80} * e^{80} stays inside the fp32 range
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---------------------------------------------------------------------------
@@ -79,14 +84,50 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
       const int t = x / nv, c = x % nv;
       vs[t * dvt + c] = to_f32(v[(bhL + s0 + t) * dv + j0 + c]);
     }
+    int wide = 0;  // a cumulative log decay of this chunk outside [-kSplitMax, kSplitMax]
     for (int r = tid; r < dk; r += kThreads) {  // one channel per thread, in token order
       float acc = 0.f;
       for (int t = 0; t < n; ++t) {
         acc += log_alpha[(bhL + s0 + t) * dk + r];
         lam[t * dkp + r] = acc;
+        wide |= !(fabsf(acc) <= kSplitMax);
       }
     }
-    __syncthreads();
+    if (!__syncthreads_or(wide)) {
+      // Split form: q~_i = e^{Lam_i} q_i and k~_j = e^{-Lam_j} k_j, every factor in
+      // [e^{-kSplitMax}, e^{kSplitMax}], so P_ij = q~_i . k~_j needs no exponential.
+      for (int x = tid; x < n * dk; x += kThreads) {
+        const int y = (x / dk) * dkp + x % dk;
+        const float l = lam[y];
+        qs[y] *= expf(l);
+        ks[y] *= expf(-l);
+      }
+      __syncthreads();
+      for (int x = tid; x < n * n; x += kThreads) {
+        const int i = x / n, j = x % n;
+        float p = 0.f;
+        if (j <= i)
+          for (int c = 0; c < dk; ++c) p = fmaf(qs[i * dkp + c], ks[j * dkp + c], p);
+        P[i * C + j] = p;
+      }
+      __syncthreads();
+      for (int x = tid; x < n * nv; x += kThreads) {
+        const int i = x / nv, c = x % nv;
+        float acc = 0.f;
+        for (int r = 0; r < dk; ++r) acc = fmaf(qs[i * dkp + r], S[r * dvt + c], acc);
+        for (int j = 0; j <= i; ++j) acc = fmaf(P[i * C + j], vs[j * dvt + c], acc);
+        O[(bhL + s0 + i) * dv + j0 + c] = from_f32<T>(acc);
+      }
+      __syncthreads();
+      for (int x = tid; x < dk * nv; x += kThreads) {  // S <- e^{Lam_end} (S + k~^T V)
+        const int r = x / nv, c = x % nv;
+        float acc = 0.f;
+        for (int j = 0; j < n; ++j) acc = fmaf(ks[j * dkp + r], vs[j * dvt + c], acc);
+        S[r * dvt + c] = expf(lam[(n - 1) * dkp + r]) * (S[r * dvt + c] + acc);
+      }
+      continue;
+    }
+    // Exact form for chunks with strong decay: every score term takes its own factor.
     for (int x = tid; x < n * n; x += kThreads) {
       const int i = x / n, j = x % n;
       float p = 0.f;

@@ -194,6 +194,27 @@ def test_channel_gate_with_equal_channels_is_the_token_gate():
     parity.check(S1.cpu(), S2.cpu(), "f32", "S")
 
 
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f32", 16)])
+def test_channel_gate_strong_decay_chunks(dtype, d):
+    """Chunks whose cumulative log decay leaves [-80, 80] take the exact
+    per-element form, the others the split form: the second and fourth chunks
+    here decay ten times harder (down to e^-448 over a chunk), so the two forms
+    alternate and hand the state to each other."""
+    B, H, L = 2, 2, 300
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, dtype, seed=13, with_state=True)
+    la = inp["log_alpha"].clone()
+    la[:, :, 64:128] *= 10.0
+    la[:, :, 192:256] *= 10.0
+    api.la_set_feature_map("elu1")
+    O, S = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(la), 64,
+                                   _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], la, phi="elu1",
+                                       S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, dtype, "O")
+    parity.check(S.cpu(), S_ref, dtype, "S")
+
+
 def test_empty_sequences_pass_the_state_through_and_bad_shapes_are_refused():
     B, H, d = 2, 2, 32
     x = torch.zeros(B, H, 0, d, device="cuda")
