@@ -74,7 +74,8 @@ template <> struct Vec16<__nv_bfloat16> {
 };
 
 // Stage rows [row0, row0 + nt) of a [*, dk] tensor into dst[t * dkp + c] as
-// phi(x) in fp32, with every 16-byte load of the pass issued before any use.
+// phi(x) in fp32, with every 16-byte load of the pass issued before any use
+// and 16-byte shared stores (dst and dkp are multiples of 4 floats).
 // phi uses the fast exponential: its relative error (a few 1e-7) stays far
 // below the fp32 tolerance of 1e-5, and the precise one made staging the
 // larger part of the kernels' instructions.
@@ -100,11 +101,13 @@ __device__ __forceinline__ void stage_rows(const T *__restrict__ src, size_t row
     if (vi < nvec) {
       float f[V::N];
       V::unpack(buf[i], f);
+      const int e = vi * V::N;  // a vector never spans two rows
+      float *d = dst + (e >> sh) * dkp + (e & (dk - 1));
 #pragma unroll
-      for (int u = 0; u < V::N; ++u) {
-        const int e = vi * V::N + u;
-        dst[(e >> sh) * dkp + (e & (dk - 1))] = feature_map(phi, f[u]);
-      }
+      for (int u = 0; u < V::N; u += 4)
+        *reinterpret_cast<float4 *>(d + u) =
+            make_float4(feature_map(phi, f[u]), feature_map(phi, f[u + 1]),
+                        feature_map(phi, f[u + 2]), feature_map(phi, f[u + 3]));
     }
   }
 }
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreadsN, 4)
 norm_block_totals_kernel(const T *__restrict__ k, int H, int L, int dk, int nblk, int phi,
                          int decay_kind, const float *__restrict__ decay,
                          const float *__restrict__ z0, void *ws) {
-  __shared__ float kf[kTok][kMaxDk + 1];  // phi(k) of the staged tokens
+  __shared__ __align__(16) float kf[kTok][kMaxDk + 4];  // phi(k) of the staged tokens
   __shared__ float el[kTok];              // e^{lambda_t}
   __shared__ float ll[kTok];              // lambda_t
   const int tid = threadIdx.x;
@@ -155,7 +158,7 @@ norm_block_totals_kernel(const T *__restrict__ k, int H, int L, int dk, int nblk
     const int nt = min(kTok, nb - t0);
     const size_t row0 = bhL + tb + t0;
     __syncthreads();  // the previous pass is done with the staging buffers
-    stage_rows(k, row0, nt, dk, kMaxDk + 1, phi, &kf[0][0], tid);
+    stage_rows(k, row0, nt, dk, kMaxDk + 4, phi, &kf[0][0], tid);
     for (int t = tid; t < nt; t += kThreadsN) {
       ll[t] = log_decay_of(decay_kind, decay, h, bhL, tb + t0 + t);
       el[t] = expf(ll[t]);
@@ -179,7 +182,9 @@ norm_apply_kernel(const T *__restrict__ q, const T *__restrict__ k, int H, int L
                   int dv, int nblk, int phi, int decay_kind, const float *__restrict__ decay,
                   const void *ws, T *O, float *z_final) {
   extern __shared__ float sm[];
-  const int dkp = dk + 1;
+  // Rows padded to dk + 4 floats: 16-byte stores when staging, and the four
+  // threads of a token in the den sum (rows t, t + 1, ...) land in distinct banks.
+  const int dkp = dk + 4;
   float *qf = sm;                // [kTok][dkp]  phi(q)
   float *kf = qf + kTok * dkp;   // [kTok][dkp]  phi(k)
   float *pr = kf + kTok * dkp;   // [kTok][dkp]  phi(q) .* z
@@ -263,7 +268,7 @@ cudaError_t launch_normaliser(const NormaliserArgs &a) {
   const int nblk = (a.L + kBlock - 1) / kBlock;
   const unsigned bh = (unsigned)((size_t)a.B * a.H);
   dim3 grid(bh, (unsigned)nblk);
-  const size_t smem = sizeof(float) * ((size_t)3 * kTok * (a.dk + 1) + 2 * kTok + kThreadsN);
+  const size_t smem = sizeof(float) * ((size_t)3 * kTok * (a.dk + 4) + 2 * kTok + kThreadsN);
   cudaError_t e = cudaFuncSetAttribute(norm_apply_kernel<float>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)

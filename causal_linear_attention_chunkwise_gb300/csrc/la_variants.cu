@@ -252,12 +252,13 @@ delta_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restri
     float kr[RPL], qr[RPL];
     load_rows<VW>(kr, kf[0], g, NI);
     load_rows<VW>(qr, qf[0], g, NI);
+    float a = at[0], b = bt[0], vc = vv[0][c];
     for (int t = 0; t < nt; ++t) {
-      float kn[RPL], qn[RPL];  // the next step's rows, loaded ahead
+      float kn[RPL], qn[RPL];  // the next step's rows and scalars, loaded ahead
       const int tn = t + 1 < nt ? t + 1 : t;
       load_rows<VW>(kn, kf[tn], g, NI);
       load_rows<VW>(qn, qf[tn], g, NI);
-      const float a = at[t], b = bt[t];
+      const float an = at[tn], bn = bt[tn], vn = vv[tn][c];
       float u0 = 0.f, u1 = 0.f;  // (k^T S)_c, two partial sums
 #pragma unroll
       for (int m = 0; m < RPL; m += 2) {
@@ -265,7 +266,7 @@ delta_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restri
         u1 = fmaf(kr[m + 1], s[m + 1], u1);
       }
       const float u = group8_sum(u0 + u1);
-      const float w = b * (vv[t][c] - a * u);  // what is written along k
+      const float w = b * (vc - a * u);  // what is written along k
       float o0 = 0.f, o1 = 0.f;
 #pragma unroll
       for (int m = 0; m < RPL; m += 2) {
@@ -281,6 +282,9 @@ delta_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restri
         kr[m] = kn[m];
         qr[m] = qn[m];
       }
+      a = an;
+      b = bn;
+      vc = vn;
     }
   }
   if (S_final && live) {
