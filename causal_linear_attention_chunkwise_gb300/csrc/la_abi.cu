@@ -341,6 +341,8 @@ la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int d
                               O, S_final, nullptr, st, &done);
   if (s != LA_OK || done) return s;
   if (!log_alpha) return fail(LA_ERR_INVALID_ARG, "%s: log_alpha must be non-null", fn);
+  if (!aligned16(log_alpha))
+    return fail(LA_ERR_INVALID_ARG, "%s: log_alpha must start on a 16-byte boundary", fn);
   VariantArgs a{VARIANT_CHANNEL_GATE, q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(),
                 log_alpha, nullptr, S0, O, S_final, st};
   return run_variant(fn, a);

@@ -49,6 +49,65 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
   return __float2bfloat16_rn(x);
 }
 
+// 16 bytes of T, unpacked to fp32.
+template <typename T> struct Pack16;
+template <> struct Pack16<float> {
+  static constexpr int N = 4;
+  __device__ static void unpack(const uint4 &u, float *f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+};
+template <> struct Pack16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void unpack(const uint4 &u, float *f) {
+    const __nv_bfloat162 *b = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(b[i]);
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+  }
+};
+
+// Copy nrows rows of `width` elements (row r at src + r * src_stride) to
+// dst[r * dst_stride + c] as op(x) in fp32, in 16-byte vectors.  Every load a
+// thread makes is issued before its first store, so the rows arrive in one
+// memory round trip rather than one per loop iteration.  Needs: src 16-byte
+// aligned; width a power of two, and width and src_stride multiples of
+// 16 bytes / sizeof(T); nrows * width / Pack16<T>::N <= MAXV * nthreads.
+template <typename T, int MAXV, typename Op>
+__device__ __forceinline__ void stage_slab(const T *__restrict__ src, size_t src_stride,
+                                           int nrows, int width, float *dst, int dst_stride,
+                                           Op op, int tid, int nthreads) {
+  using P = Pack16<T>;
+  const int vpr = width / P::N;  // vectors per row, a power of two
+  const int shv = __ffs(vpr) - 1;
+  const int nvec = nrows * vpr;
+  uint4 buf[MAXV];
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int vi = tid + i * nthreads;
+    if (vi < nvec)
+      buf[i] = *reinterpret_cast<const uint4 *>(src + (size_t)(vi >> shv) * src_stride +
+                                                (vi & (vpr - 1)) * P::N);
+  }
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int vi = tid + i * nthreads;
+    if (vi < nvec) {
+      float f[P::N];
+      P::unpack(buf[i], f);
+      float *d = dst + (vi >> shv) * dst_stride + (vi & (vpr - 1)) * P::N;
+#pragma unroll
+      for (int u = 0; u < P::N; ++u) d[u] = op(f[u]);
+    }
+  }
+}
+
 }  // namespace la
 
 // Opt-in event trace for kernel development.  Built with -DLA_TRACE, kernels

@@ -75,20 +75,18 @@ channel_gate_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
   for (int s0 = 0; s0 < L; s0 += C) {
     const int n = min(C, L - s0);
     __syncthreads();
-    for (int x = tid; x < n * dk; x += kThreads) {
-      const int t = x / dk, r = x % dk;
-      qs[t * dkp + r] = feature_map_precise(phi, to_f32(q[(bhL + s0) * dk + x]));
-      ks[t * dkp + r] = feature_map_precise(phi, to_f32(k[(bhL + s0) * dk + x]));
-    }
-    for (int x = tid; x < n * nv; x += kThreads) {
-      const int t = x / nv, c = x % nv;
-      vs[t * dvt + c] = to_f32(v[(bhL + s0 + t) * dv + j0 + c]);
-    }
+    const auto phi_of = [phi](float x) { return feature_map_precise(phi, x); };
+    const auto same = [](float x) { return x; };
+    stage_slab<T, 8>(q + (bhL + s0) * dk, dk, n, dk, qs, dkp, phi_of, tid, kThreads);
+    stage_slab<T, 8>(k + (bhL + s0) * dk, dk, n, dk, ks, dkp, phi_of, tid, kThreads);
+    stage_slab<T, 2>(v + (bhL + s0) * dv + j0, dv, n, nv, vs, dvt, same, tid, kThreads);
+    stage_slab<float, 8>(log_alpha + (bhL + s0) * dk, dk, n, dk, lam, dkp, same, tid, kThreads);
+    __syncthreads();
     int wide = 0;  // a cumulative log decay of this chunk outside [-kSplitMax, kSplitMax]
     for (int r = tid; r < dk; r += kThreads) {  // one channel per thread, in token order
       float acc = 0.f;
       for (int t = 0; t < n; ++t) {
-        acc += log_alpha[(bhL + s0 + t) * dk + r];
+        acc += lam[t * dkp + r];
         lam[t * dkp + r] = acc;
         wide |= !(fabsf(acc) <= kSplitMax);
       }
@@ -236,14 +234,14 @@ delta_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restri
   for (int t0 = 0; t0 < L; t0 += kTok) {
     const int nt = min(kTok, L - t0);
     __syncthreads();  // every warp is done with the previous tokens
-    for (int x = tid; x < nt * DK; x += kThreads) {
-      qf[x / DK][x % DK] = feature_map_precise(phi, to_f32(q[(bhL + t0) * DK + x]));
-      kf[x / DK][x % DK] = feature_map_precise(phi, to_f32(k[(bhL + t0) * DK + x]));
-    }
-    for (int x = tid; x < nt * kDeltaCols; x += kThreads) {
-      const int t = x / kDeltaCols, cc = x % kDeltaCols;
-      vv[t][cc] = cc < nv ? to_f32(v[(bhL + t0 + t) * dv + j0 + cc]) : 0.f;
-    }
+    const auto phi_of = [phi](float x) { return feature_map_precise(phi, x); };
+    const auto same = [](float x) { return x; };
+    stage_slab<T, 4>(q + (bhL + t0) * DK, DK, nt, DK, &qf[0][0], DK, phi_of, tid, kThreads);
+    stage_slab<T, 4>(k + (bhL + t0) * DK, DK, nt, DK, &kf[0][0], DK, phi_of, tid, kThreads);
+    stage_slab<T, 1>(v + (bhL + t0) * dv + j0, dv, nt, nv, &vv[0][0], kDeltaCols, same, tid,
+                     kThreads);
+    for (int x = tid; x < nt * kDeltaCols; x += kThreads)  // columns past d_v read as 0
+      if (x % kDeltaCols >= nv) vv[x / kDeltaCols][x % kDeltaCols] = 0.f;
     for (int t = tid; t < nt; t += kThreads) {
       bt[t] = beta[bhL + t0 + t];
       at[t] = log_alpha ? expf(log_alpha[bhL + t0 + t]) : 1.f;

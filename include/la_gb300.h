@@ -214,7 +214,8 @@ size_t la_normalised_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, 
  *
  * one decay per key channel and token.
  *
- *   log_alpha  [B,H,L,d_k] fp32, log alpha_t[i] (expected <= 0)   (read)
+ *   log_alpha  [B,H,L,d_k] fp32, log alpha_t[i] (expected <= 0), 16-byte
+ *              aligned like the other tensors                      (read)
  *   S0         [B,H,d_k,d_v] fp32 or NULL;  S_final may alias S0.
  */
 la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int dtype,

@@ -180,6 +180,8 @@ def test_variant_validation_before_any_device_work(lib):
     # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, log_alpha, S0, O, S_final, stream)
     assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, None, None, p, None, None) == 1
     assert b"log_alpha" in lib.la_last_error()
+    assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, odd, None, p, None, None) == 1
+    assert b"log_alpha" in lib.la_last_error()
     assert cg(p, p, p, 1, 1, 1, 8, 16, 256, 64, p, None, p, None, None) == 2
     assert cg(p, p, p, 1, 1, -1, 8, 16, 16, 64, p, None, p, None, None) == 1
     assert cg(p, odd, p, 1, 1, 1, 8, 16, 16, 64, p, None, p, None, None) == 1
