@@ -1,4 +1,4 @@
-// la_tma_host.h -- host-side creation of TMA tensor maps.  The driver's
+// la_tma_host.h -- host-side creation of TMA tensor maps.  The CUDA driver API's
 // cuTensorMapEncodeTiled is reached through the runtime's entry-point query,
 // so the library needs no link-time dependency on libcuda.
 #pragma once

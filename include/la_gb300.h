@@ -48,7 +48,7 @@ typedef int la_status;
 
 #define LA_OK                 0  /* success */
 #define LA_ERR_INVALID_ARG    1  /* bad pointer, size, alignment or enum value */
-#define LA_ERR_UNSUPPORTED    2  /* valid request this build has no kernel for */
+#define LA_ERR_UNSUPPORTED    2  /* valid request the library has no kernel for */
 #define LA_ERR_CUDA           3  /* a CUDA runtime call or launch failed */
 #define LA_ERR_DEVICE_TIMEOUT 4  /* a kernel's bounded wait ran out (la_device_status) */
 
