@@ -70,13 +70,18 @@ def la_chunk_fwd_kernel_count(B, H, L, d_k, d_v, chunk=64, dtype=torch.bfloat16)
 _ws_cache: dict = {}
 
 
-def _workspace(nbytes, device):
+def _workspace(nbytes, device, stream=None):
+    """A cached scratch buffer per (device, stream): calls ordered on one
+    stream may share it, calls on different streams never do."""
     if nbytes == 0:
         return None
-    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    key = (device.index, s.cuda_stream)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        if stream is not None:
+            buf.record_stream(s)  # the allocator must not hand it out while s may use it
         _ws_cache[key] = buf
     return buf
 
@@ -104,7 +109,7 @@ def la_chunk_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None, O=No
     lib = _native.load()
     ws_need = la_chunk_fwd_workspace_bytes(B, H, L, dk, dv, chunk, q.dtype)
     if workspace is None:
-        workspace = _workspace(ws_need, q.device)
+        workspace = _workspace(ws_need, q.device, stream)
     _check(lib.la_chunk_fwd(
         _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, chunk,
         DECAY[decay_kind], _ptr(decay), _ptr(S0), _ptr(O), _ptr(S_final),
@@ -132,7 +137,8 @@ def la_noncausal_fwd(q, k, v, O=None, S=None, want_state=True, workspace=None, s
     _need_cuda(q, k, v, O, S)
     lib = _native.load()
     if workspace is None:
-        workspace = _workspace(la_noncausal_fwd_workspace_bytes(B, H, L, dk, dv), q.device)
+        workspace = _workspace(la_noncausal_fwd_workspace_bytes(B, H, L, dk, dv), q.device,
+                               stream)
     _check(lib.la_noncausal_fwd(
         _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, _ptr(O), _ptr(S),
         _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
@@ -235,7 +241,7 @@ def la_normalised_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None,
     dv = v.shape[-1]
     if workspace is None:
         workspace = _workspace(la_normalised_fwd_workspace_bytes(B, H, L, dk, dv, chunk, q.dtype),
-                               q.device)
+                               q.device, stream)
     _check(_native.load().la_normalised_fwd(
         _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, chunk,
         DECAY[decay_kind], _ptr(decay), _ptr(S0), _ptr(z0), _ptr(O), _ptr(S_final),
