@@ -84,8 +84,10 @@ def _bind(lib):
     lib.oracle_channel_gate.argtypes = [i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp]
     lib.oracle_delta.argtypes = [i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp, dp]
     lib.oracle_chunkwise.argtypes = [i, i, i, i, i, i, dp, dp, dp, i, i, dp, dp, dp, dp]
+    lib.oracle_delta_chunkwise.argtypes = [i, i, i, i, i, i, dp, dp, dp, i, dp, dp, dp, dp, dp]
     for f in (lib.oracle_recurrent, lib.oracle_parallel, lib.oracle_chunkwise, lib.oracle_noncausal,
-              lib.oracle_normalised, lib.oracle_channel_gate, lib.oracle_delta):
+              lib.oracle_normalised, lib.oracle_channel_gate, lib.oracle_delta,
+              lib.oracle_delta_chunkwise):
         f.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
@@ -234,6 +236,24 @@ def delta(q, k, v, beta, log_alpha=None, phi="identity", S0=None, lib=None):
         _ptr(Sf))
     if rc != 0:
         raise RuntimeError(f"oracle_delta failed with code {rc}")
+    return O, Sf
+
+
+def delta_chunkwise(q, k, v, beta, chunk, log_alpha=None, phi="identity", S0=None, lib=None):
+    """The delta rule of ``delta`` evaluated a chunk of ``chunk`` tokens at a
+    time (the WY form: per chunk, a unit lower-triangular solve for the
+    written values u_t, then dense products).  Returns (O, S_final)."""
+    q, k, v, p, _, _, S0, (B, H, L, dk, dv) = _prepare(q, k, v, phi, "none", None, S0)
+    be = _f64(beta)
+    la = _f64(log_alpha)
+    if be.shape != (B, H, L) or (la is not None and la.shape != (B, H, L)):
+        raise ValueError("beta and log_alpha must be [B,H,L]")
+    O, Sf = np.zeros((B, H, L, dv)), np.zeros((B, H, dk, dv))
+    rc = (lib or load_library()).oracle_delta_chunkwise(
+        B, H, L, dk, dv, int(chunk), _ptr(q), _ptr(k), _ptr(v), p, _ptr(be), _ptr(la), _ptr(S0),
+        _ptr(O), _ptr(Sf))
+    if rc != 0:
+        raise RuntimeError(f"oracle_delta_chunkwise failed with code {rc}")
     return O, Sf
 
 

@@ -68,6 +68,17 @@
  *           o_t = phi(q_t)^T S_t, with k_t = phi(k_t) as given (the page
  *           assumes unit-norm keys; the caller normalises).
  *
+ *   oracle_delta_chunkwise  the same rule, a chunk at a time (WY form)
+ *       The pages give the delta rule only token by token.  Unrolling it over
+ *       a chunk of n tokens with state S before the chunk and Lam_t the
+ *       inclusive prefix of log alpha gives
+ *           u_t = beta_t (v_t - e^{Lam_t} S^T k_t
+ *                         - sum_{j<t} e^{Lam_t - Lam_j} (k_t.k_j) u_j),
+ *           S_t = e^{Lam_t} S + sum_{j<=t} e^{Lam_t - Lam_j} k_j u_j^T,
+ *       so each u_t is one row of a unit lower-triangular solve, o_t = q_t^T S_t
+ *       and the chunk ends at S_{n-1}.  C = 1 is the recurrence itself; the
+ *       pins check every C against oracle_delta.
+ *
  * Decay is given per token in log space, lambda_t = log(decay factor):
  *   kind 0  none                  lambda_t = 0
  *   kind 1  per head  [H]         lambda_t = log_gamma[h]          (RetNet)
@@ -485,6 +496,87 @@ int oracle_delta(int B, int H, int L, int dk, int dv,
         }
         if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
         free(S); free(kf); free(qf); free(ks);
+    }
+    return err ? -2 : 0;
+}
+
+/* The delta rule chunk by chunk (see the header): per chunk, the u_t by
+ * forward substitution, then every output and the state at the chunk end. */
+int oracle_delta_chunkwise(int B, int H, int L, int dk, int dv, int C,
+                           const double *q, const double *k, const double *v,
+                           int phi, const double *beta, const double *log_alpha,
+                           const double *S0, double *O, double *S_final)
+{
+    if (check_args(B, H, L, dk, dv, phi, 0, NULL) || !beta || C < 1) return -1;
+    int err = 0;
+    long nseq = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (long bh = 0; bh < nseq; ++bh) {
+        double *S = malloc(sizeof(double) * (size_t)dk * dv);
+        double *lam = malloc(sizeof(double) * (size_t)C);
+        double *qf = malloc(sizeof(double) * (size_t)C * dk);
+        double *kf = malloc(sizeof(double) * (size_t)C * dk);
+        double *U = malloc(sizeof(double) * (size_t)C * dv);
+        if (!S || !lam || !qf || !kf || !U) {
+            free(S); free(lam); free(qf); free(kf); free(U); err |= 1; continue;
+        }
+        if (S0) memcpy(S, S0 + (size_t)bh * dk * dv, sizeof(double) * (size_t)dk * dv);
+        else memset(S, 0, sizeof(double) * (size_t)dk * dv);
+        for (int s0 = 0; s0 < L; s0 += C) {
+            int n = L - s0 < C ? L - s0 : C;
+            double run = 0.0;
+            for (int t = 0; t < n; ++t) {
+                size_t row = (size_t)bh * L + s0 + t;
+                run += log_alpha ? log_alpha[row] : 0.0;
+                lam[t] = run;
+                for (int c = 0; c < dk; ++c) {
+                    qf[(size_t)t * dk + c] = feature(phi, q[row * dk + c]);
+                    kf[(size_t)t * dk + c] = feature(phi, k[row * dk + c]);
+                }
+            }
+            for (int t = 0; t < n; ++t) {  /* forward substitution, row by row */
+                size_t row = (size_t)bh * L + s0 + t;
+                double bt = beta[row], et = exp(lam[t]);
+                for (int j = 0; j < dv; ++j) {
+                    double kS = 0.0;
+                    for (int c = 0; c < dk; ++c) kS += kf[(size_t)t * dk + c] * S[(size_t)c * dv + j];
+                    double acc = v[row * dv + j] - et * kS;
+                    for (int i = 0; i < t; ++i) {
+                        double kk = 0.0;
+                        for (int c = 0; c < dk; ++c)
+                            kk += kf[(size_t)t * dk + c] * kf[(size_t)i * dk + c];
+                        acc -= exp(lam[t] - lam[i]) * kk * U[(size_t)i * dv + j];
+                    }
+                    U[(size_t)t * dv + j] = bt * acc;
+                }
+            }
+            for (int t = 0; t < n; ++t) {  /* o_t = q_t^T S_t */
+                double *ot = O + ((size_t)bh * L + s0 + t) * dv;
+                double et = exp(lam[t]);
+                for (int j = 0; j < dv; ++j) {
+                    double acc = 0.0;
+                    for (int c = 0; c < dk; ++c) acc += qf[(size_t)t * dk + c] * S[(size_t)c * dv + j];
+                    acc *= et;
+                    for (int i = 0; i <= t; ++i) {
+                        double qk = 0.0;
+                        for (int c = 0; c < dk; ++c)
+                            qk += qf[(size_t)t * dk + c] * kf[(size_t)i * dk + c];
+                        acc += exp(lam[t] - lam[i]) * qk * U[(size_t)i * dv + j];
+                    }
+                    ot[j] = acc;
+                }
+            }
+            double eEnd = exp(lam[n - 1]);  /* S <- S_{n-1} */
+            for (size_t x = 0; x < (size_t)dk * dv; ++x) S[x] *= eEnd;
+            for (int i = 0; i < n; ++i) {
+                double w = exp(lam[n - 1] - lam[i]);
+                for (int c = 0; c < dk; ++c)
+                    for (int j = 0; j < dv; ++j)
+                        S[(size_t)c * dv + j] += w * kf[(size_t)i * dk + c] * U[(size_t)i * dv + j];
+            }
+        }
+        if (S_final) memcpy(S_final + (size_t)bh * dk * dv, S, sizeof(double) * (size_t)dk * dv);
+        free(S); free(lam); free(qf); free(kf); free(U);
     }
     return err ? -2 : 0;
 }

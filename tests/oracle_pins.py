@@ -24,7 +24,9 @@ planted mistake) and raises AssertionError when the oracle disagrees with:
   (``pin_normalised``, ``pin_channel_gate``);
 * for the delta rule: the page's checks [d]/[e] (orthonormal keys give the
   additive rule, random keys do not), exact retrieval of the value just
-  written, beta = 0, one token (``pin_delta``).
+  written, beta = 0, one token (``pin_delta``);
+* for the delta rule's chunkwise (WY) form: equality with the token-by-token
+  rule for chunk sizes 1, 4, 7 and L (``pin_delta_chunkwise``).
 
 ``tests/test_oracle_mutants.py`` plants plausible mistakes in a copy of the
 oracle's C source and checks that at least one pin fails for each.
@@ -420,7 +422,33 @@ def pin_delta(lib):
     _close(O, want, 1e-12, "delta one token")
 
 
+def pin_delta_chunkwise(lib):
+    """The chunkwise (WY) form of the delta rule equals the token-by-token rule
+    for every chunk size: C = 1 is the recurrence itself, C = L one chunk, and
+    C in {4, 7} ragged chunks (the check [a]/[b] of "Linear / Sparse Attention -
+    minimal runnable implementation", chunkwise == recurrent, carried over to
+    the delta rule), with and without the gate, from S0, for both phi."""
+    r = _rng(16)
+    B, H, L, d, dv = 2, 2, 23, 5, 3
+    k = r.normal(size=(B, H, L, d))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = r.normal(size=(B, H, L, dv))
+    q = r.normal(size=(B, H, L, d))
+    S0 = r.normal(size=(B, H, d, dv))
+    la = -np.logaddexp(0.0, r.normal(size=(B, H, L)))
+    for phi, bmax in (("identity", 1.0), ("elu1", 1.0 / d)):
+        be = r.uniform(0.0, bmax, size=(B, H, L))
+        for gate in (None, la):
+            Or, Sr = oracle.delta(q, k, v, be, log_alpha=gate, phi=phi, S0=S0, lib=lib)
+            for C in (1, 4, 7, L):
+                O, S = oracle.delta_chunkwise(q, k, v, be, C, log_alpha=gate, phi=phi, S0=S0,
+                                              lib=lib)
+                what = f"delta chunkwise C={C}/{phi}/{'gated' if gate is not None else 'plain'}"
+                _close(O, Or, 1e-11, what)
+                _close(S, Sr, 1e-11, what + " state")
+
+
 PINS = [pin_golden, pin_closed_form_additive, pin_closed_form_constant_decay, pin_single_token,
         pin_one_hot, pin_orthonormal_keys, pin_chunk_invariance, pin_parallel_equals_recurrent,
         pin_split_invariance, pin_library_pieces, pin_state_shape, pin_noncausal, pin_normalised,
-        pin_channel_gate, pin_delta]
+        pin_channel_gate, pin_delta, pin_delta_chunkwise]

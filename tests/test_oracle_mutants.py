@@ -105,6 +105,19 @@ MUTANTS = [
     ("delta_write_without_beta",
      "                                            bt * kf[i] * vt[j];",
      "                                            kf[i] * vt[j];"),
+    ("delta_chunk_solve_includes_diagonal",
+     "                    for (int i = 0; i < t; ++i) {\n"
+     "                        double kk = 0.0;",
+     "                    for (int i = 0; i <= t; ++i) {\n"
+     "                        double kk = 0.0;"),
+    ("delta_chunk_rhs_state_not_decayed",
+     "double acc = v[row * dv + j] - et * kS;",
+     "double acc = v[row * dv + j] - kS;"),
+    ("delta_chunk_output_excludes_own_write",
+     "                    for (int i = 0; i <= t; ++i) {\n"
+     "                        double qk = 0.0;",
+     "                    for (int i = 0; i < t; ++i) {\n"
+     "                        double qk = 0.0;"),
 ]
 
 
