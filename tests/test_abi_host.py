@@ -192,3 +192,18 @@ def test_variant_validation_before_any_device_work(lib):
     assert dl(p, p, p, 0, 1, 1, 8, 16, 24, p, None, None, p, None, None) == 2
     assert dl(p, p, p, 1, 1, 1, 8, 16, 16, p, None, None, p, odd, None) == 1
     assert dl(p, p, p, 2, 1, 1, 8, 16, 16, p, None, None, p, None, None) == 1
+
+
+def test_normalised_workspace_layout(lib):
+    """la_normalised_fwd's workspace is the prefill's (rounded up to 256 bytes)
+    followed by the z scan's: per sequence and 256-token block a d_k total and a
+    log decay, and one incoming z0 per sequence, all fp32."""
+    for B, H, L, dk, dv, chunk, dtype in [(4, 16, 4096, 64, 64, 64, 1), (1, 16, 32768, 128, 128, 64, 1),
+                                          (2, 3, 300, 32, 16, 7, 0), (1, 1, 1, 16, 16, 64, 0),
+                                          (2, 32, 8192, 128, 128, 64, 1)]:
+        num = lib.la_chunk_fwd_workspace_bytes(B, H, L, dk, dv, chunk, dtype)
+        bh, nblk = B * H, -(-L // 256)
+        scan = 4 * (bh * nblk * dk + bh * nblk + bh * dk)
+        want = (num + 255) // 256 * 256 + scan
+        assert lib.la_normalised_fwd_workspace_bytes(B, H, L, dk, dv, chunk, dtype) == want
+    assert lib.la_normalised_fwd_workspace_bytes(1, 1, 64, 48, 48, 64, 1) == 0  # unsupported d
