@@ -3,22 +3,25 @@
 on one GB300 per process.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl reference] [--no-cpu-baseline]
+                    [--impl reference] [--no-cpu-baseline] [--legs main|all]
 
 One "step" is one la_chunk_fwd call over the whole workload batch (every
 prefill row of the path: feature map, gate prep, intra/inter products, state
-update, output and final-state stores).  The default workload is B=4, H=16,
-L=4096, d=64, bf16, phi = elu + 1, chunk 64.  ``value`` is prefill tokens/s
-(B*L tokens per step, all heads of a token counted once) with inputs resident
-in HBM; the line also carries the decode step (B=512, H=32, d=128, fp32 state
-in place) as ``decode``.
+update, output and final-state stores).  The headline workload is the largest
+single-GPU prefill problem: B=1, H=16, L=32768, d=128, bf16, per-token gate
+logits, a non-zero fp32 initial state, chunk 64.  ``value`` is prefill
+tokens/s (B*L tokens per step, all heads of a token counted once) with inputs
+resident in HBM.  The same line carries, each with its own time and roofline:
+the other prefill workloads (``legs``), the decode step (B=512, H=32, d=128,
+fp32 state in place) as ``decode``, the non-causal form (``noncausal``) and
+the normalised, per-channel-gate and delta-rule forms (``variants``).
 
-Timing: W untimed warm-up steps (at least ~1 s of them, so the clock sampler
-sees the GPU under load), then a barrier and a synchronize, K steps bracketed
-by CUDA events on the launching stream, a synchronize and a barrier; the max
-over ranks.  Inputs rotate over enough copies that each step's working set is
-out of L2 (129 MB).  Under torchrun (N > 1) every rank runs its own replica of
-the workload (no data-path collective; weak scaling).
+Timing: W untimed warm-up steps (at least ~1 s of them for the headline, so
+the clock sampler sees the GPU under load), then a barrier and a synchronize,
+K steps bracketed by CUDA events on the launching stream, a synchronize and a
+barrier; the max over ranks.  Inputs rotate over enough copies that each
+step's working set is out of L2 (129 MB).  Under torchrun (N > 1) every rank
+runs its own replica of the workload (no data-path collective; weak scaling).
 
 ``--impl reference`` times the fp64 CPU oracle on the same workload (bounded
 samples per step) on the host cores; only rank 0 works under torchrun.
@@ -42,7 +45,12 @@ sys.path.insert(0, ROOT)
 from causal_linear_attention_chunkwise_gb300 import workloads as W  # noqa: E402
 
 METRIC = "tokens/s per GB300 (chunkwise prefill, decode step); % of roofline"
-DEFAULT_WORKLOAD = "B4_H16_L4096_d64_elu1"
+DEFAULT_WORKLOAD = "B1_H16_L32768_d128_gate"
+# Further prefill workloads timed beside the headline (the fp32 L = 300 one is a
+# correctness / latency case: it fits in L2 and is launch-bound).
+SUB_LEGS = ("B2_H32_L8192_d128_retnet", "B4_H16_L4096_d64_elu1", "L300_d16_f32")
+NONCAUSAL_LEGS = ("B4_H16_L4096_d64_elu1", "B2_H32_L8192_d128_retnet")
+VARIANT_SHAPE = "B4_H16_L4096_d64_elu1"
 DECODE_WORKLOAD = "B512_H32_d128_decode"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -227,13 +235,30 @@ def _dev_inputs(inp, dev):
     return {k: (v.to(dev).contiguous() if torch.is_tensor(v) else v) for k, v in inp.items()}
 
 
+def rotation(w):
+    """(input sets, bytes per set) of the L2 rotation of prefill workload w."""
+    set_bytes = prefill_bytes(w)
+    return min(16, max(2, math.ceil(3 * L2_BYTES / set_bytes))), set_bytes
+
+
+def workload_config(w, n_ranks):
+    """The ``config`` object of a line on prefill workload w (the same for
+    both arms)."""
+    n_sets, set_bytes = rotation(w)
+    l2 = (f"inputs rotate over {n_sets} sets of {set_bytes / 2**20:.0f} MiB (> L2)"
+          if n_sets * set_bytes > L2_BYTES else
+          f"inputs rotate over {n_sets} sets of {set_bytes / 2**10:.0f} KiB (fit in L2)")
+    return {"workload": w.name, "global_batch": w.B * n_ranks, "seq_len": w.L, "heads": w.H,
+            "d_k": w.dk, "d_v": w.dv, "chunk": w.chunk, "phi": w.phi, "decay": w.decay,
+            "initial_state": w.s0_std is not None,
+            "parallelism": f"replicas{n_ranks}" if n_ranks > 1 else "single", "l2": l2}
+
+
 def bench_prefill(w, steps, warmup, dev, peaks, peak_kind, min_warmup_s=1.0):
     from causal_linear_attention_chunkwise_gb300 import api
     api.la_set_feature_map(w.phi)
     host = W.make_prefill_inputs(w, seed=0)
-    set_bytes = prefill_bytes(w)
-    n_sets = max(2, math.ceil(3 * L2_BYTES / set_bytes))
-    n_sets = min(n_sets, 16)
+    n_sets, set_bytes = rotation(w)
     sets = []
     for i in range(n_sets):
         d = _dev_inputs(host if i == 0 else W.make_prefill_inputs(w, seed=i), dev)
@@ -531,6 +556,18 @@ def cpu_oracle_decode_sample(w, budget_s=6.0):
 
 
 # ---------------------------------------------------------------- arms
+def prefill_leg(w, steps, warmup, dev, peaks, peak_kind, n_ranks, min_warmup_s):
+    """One prefill workload's sub-object: time, throughput, roofline, clocks."""
+    r = bench_prefill(w, steps, warmup, dev, peaks, peak_kind, min_warmup_s=min_warmup_s)
+    el_max = max_over_ranks(r["elapsed_ms"], dev)
+    return r, {"workload": w.name, "dtype": w.dtype,
+               "value": round(aggregate(w.tokens, steps, el_max, n_ranks), 1),
+               "unit": "tokens/s", "ms_per_step": round(el_max / steps, 5),
+               "per_call_ms": round(r["per_call_ms"], 5), "roofline": r["roofline"],
+               "gpu_launches": r["gpu_launches"], "clocks": r["clocks"],
+               "config": workload_config(w, n_ranks)}
+
+
 def run_gpu_arm(args):
     rank, ws = init_dist()
     _, _, local = world()
@@ -539,33 +576,49 @@ def run_gpu_arm(args):
     from causal_linear_attention_chunkwise_gb300 import api  # noqa: F401  (loads the library)
     peaks, peak_kind = load_peaks()
     w = W.PREFILL[args.workload]
-    res = bench_prefill(w, args.steps, args.warmup, dev, peaks, peak_kind)
+    res, head = prefill_leg(w, args.steps, args.warmup, dev, peaks, peak_kind, ws, 1.0)
     el_max = max_over_ranks(res["elapsed_ms"], dev)
     value = aggregate(w.tokens, args.steps, el_max, ws)
     e2e_ms, h2d, d2h = bench_prefill_e2e(w, args.steps, dev)
     e2e_max = max_over_ranks(e2e_ms, dev)
-    dw, d_el, d_per, d_rl = bench_decode(args.decode_steps, args.warmup, dev, peaks, peak_kind)
-    d_max = max_over_ranks(d_el, dev)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el_max / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "global_batch": w.B * ws, "seq_len": w.L, "heads": w.H,
-                   "d_k": w.dk, "d_v": w.dv, "chunk": w.chunk, "phi": w.phi, "decay": w.decay,
-                   "parallelism": f"replicas{ws}" if ws > 1 else "single",
-                   "l2": f"inputs rotate over {res['n_sets']} sets of "
-                         f"{res['set_bytes'] / 2**20:.0f} MiB (> L2)"},
+        "config": workload_config(w, ws),
         "clocks": res["clocks"],
         "e2e": {"value": round(aggregate(w.tokens, args.steps, e2e_max, ws), 1),
                 "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": res["gpu_launches"],
         "roofline": res["roofline"],
-        "decode": {"workload": dw.name, "value": round(aggregate(dw.B, args.decode_steps, d_max, ws), 1),
-                   "unit": "tokens/s", "steps": args.decode_steps,
-                   "ms_per_step": round(d_max / args.decode_steps, 5), "roofline": d_rl,
-                   "gpu_launches": args.decode_steps},
     }
+    if args.legs == "all":
+        legs = {}
+        for name in SUB_LEGS:
+            if name == w.name:
+                continue
+            _, legs[name] = prefill_leg(W.PREFILL[name], args.steps, args.warmup, dev, peaks,
+                                        peak_kind, ws, 0.3)
+        line["legs"] = legs
+    dw, d_el, d_per, d_rl = bench_decode(args.decode_steps, args.warmup, dev, peaks, peak_kind)
+    d_max = max_over_ranks(d_el, dev)
+    line["decode"] = {"workload": dw.name,
+                      "value": round(aggregate(dw.B, args.decode_steps, d_max, ws), 1),
+                      "unit": "tokens/s", "steps": args.decode_steps,
+                      "ms_per_step": round(d_max / args.decode_steps, 5), "roofline": d_rl,
+                      "gpu_launches": args.decode_steps}
+    if args.legs == "all":
+        nc = {}
+        for name in NONCAUSAL_LEGS:
+            nw = W.PREFILL[name]
+            per, rl = bench_noncausal(nw, args.steps, args.warmup, dev, peaks, peak_kind)
+            nc[name] = {"per_call_ms": round(per, 5), "unit": "tokens/s",
+                        "value": round(nw.tokens / (per / 1e3), 1), "roofline": rl}
+        line["noncausal"] = nc
+        vw = W.PREFILL[VARIANT_SHAPE]
+        line["variants"] = {"shape": vw.name, "dtype": "bf16",
+                            **bench_variants(vw, args.steps, args.warmup, dev, peaks, peak_kind)}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         inp = W.make_prefill_inputs(w, seed=0)
         tps, desc, cores, _ = cpu_oracle_prefill_sample(w, inp)
@@ -642,9 +695,7 @@ def run_reference_arm(args):
         "ms_per_step": round(1e3 * statistics.mean(secs), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.L, "heads": w.H,
-                   "d_k": w.dk, "d_v": w.dv, "chunk": w.chunk, "phi": w.phi, "decay": w.decay,
-                   "parallelism": "single"},
+        "config": workload_config(w, ws),
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores,
                          "kind": "oracle", "sample": "each step: " + desc, "cpu": _cpu_name()},
         "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -662,6 +713,9 @@ def main(argv=None):
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.PREFILL))
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--legs", choices=["main", "all"], default="all",
+                   help="main: the headline workload and decode only; all: also the other "
+                        "prefill workloads, the non-causal form and the further forms")
     p.add_argument("--profile", choices=["prefill", "decode", "noncausal", "variants"], default=None,
                    help="run one leg only (for ncu captures); prints no benchmark line")
     args = p.parse_args(argv)

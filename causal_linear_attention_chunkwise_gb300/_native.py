@@ -22,6 +22,7 @@ SIGNATURES = {
     "la_decode_step": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "la_chunk_fwd_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp,
                                   _vp, _vp]),
+    "la_chunk_fwd_noalloc_prepare": (_i, []),
     "la_chunk_fwd_noalloc_scratch_bytes": (_sz, []),
     "la_noncausal_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp]),
     "la_noncausal_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),

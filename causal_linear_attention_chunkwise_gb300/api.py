@@ -168,6 +168,13 @@ def la_chunk_fwd_noalloc(q, k, v, chunk=64, decay_kind="none", decay=None, S0=No
     return O, S_final
 
 
+def la_chunk_fwd_noalloc_prepare():
+    """Look up the static scratch on the current device (which is where lazy
+    module loading reserves it).  Call once per device at start-up, before
+    the point where the caller may no longer allocate."""
+    _check(_native.load().la_chunk_fwd_noalloc_prepare())
+
+
 def la_chunk_fwd_noalloc_scratch_bytes() -> int:
     return int(_native.load().la_chunk_fwd_noalloc_scratch_bytes())
 

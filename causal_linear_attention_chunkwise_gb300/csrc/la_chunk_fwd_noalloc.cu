@@ -6,8 +6,15 @@
 // allocation after start-up (fixed-footprint serving processes), or code
 // running while another component holds the allocator lock.  For them the
 // segment-state workspace that la_chunk_fwd takes from the caller lives here
-// instead, in one fixed-size array in device memory that the CUDA module
-// reserves when the library is loaded.
+// instead, in one fixed-size array in device memory.
+//
+// When the bytes are reserved.  The CUDA runtime loads a module lazily by
+// default (CUDA_MODULE_LOADING=LAZY): the array is placed in device memory
+// when this file's module is first used on a device, which is the
+// cudaGetSymbolAddress below.  la_chunk_fwd_noalloc_prepare() does that
+// lookup for the current device, so a caller that cannot allocate later calls
+// it once per device at start-up; la_chunk_fwd_noalloc does it itself on its
+// first call on a device that was not prepared.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -18,10 +25,11 @@
 
 namespace {
 
-// The scratch: enough for the segment states of about 300 sequences of 128x128
-// state at 2 segments each (every workload this library is tuned for needs at
-// most 21 MB).  Every GPU that loads the library holds these bytes until the
-// process exits.
+// The scratch.  The workspace of la_chunk_fwd is B*H*NS*d_k*d_v*4 bytes of
+// segment states plus B*H*NS log decays (NS = segments per sequence, chosen
+// by the launcher), so 32 MiB holds, for instance, about 250 sequences of
+// 128 x 128 state at 2 segments each.  Every GPU on which the module is loaded
+// holds these bytes until the process exits.
 constexpr size_t kScratchBytes = LA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -29,16 +37,17 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices];  // device address of g_scratch, per device
 
-// The array's device address for the current device, looked up once per device
-// with that device current.  (In host code `g_scratch` names a host-side
-// stand-in, not device memory, so it must never be passed to a kernel.)
-cudaError_t scratch_for_current_device(void **out) {
+// Look up (again, when `refresh`) the array's device address for the current
+// device, with that device current, and cache it.  In host code `g_scratch`
+// names a host-side stand-in, not device memory, so it is never passed to a
+// kernel: only the address returned here is.
+cudaError_t scratch_for_current_device(void **out, bool refresh) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (refresh || !g_scratch_ptr[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess) return e;
@@ -48,11 +57,25 @@ cudaError_t scratch_for_current_device(void **out) {
   return cudaSuccess;
 }
 
+la_status lookup_failed(cudaError_t e) {
+  char msg[256];
+  snprintf(msg, sizeof msg, "la_chunk_fwd_noalloc: scratch address lookup: %s",
+           cudaGetErrorString(e));
+  la::set_last_error(msg);
+  return LA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
 size_t la_chunk_fwd_noalloc_scratch_bytes(void) { return kScratchBytes; }
+
+la_status la_chunk_fwd_noalloc_prepare(void) {
+  void *p = nullptr;
+  const cudaError_t e = scratch_for_current_device(&p, true);
+  return e == cudaSuccess ? LA_OK : lookup_failed(e);
+}
 
 la_status la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, int dtype, int B,
                                int H, int L, int d_k, int d_v, int chunk, int decay_kind,
@@ -70,14 +93,8 @@ la_status la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, int 
   }
   void *scratch = nullptr;
   if (need > 0) {
-    cudaError_t e = scratch_for_current_device(&scratch);
-    if (e != cudaSuccess) {
-      char msg[256];
-      snprintf(msg, sizeof msg, "la_chunk_fwd_noalloc: scratch address lookup: %s",
-               cudaGetErrorString(e));
-      la::set_last_error(msg);
-      return LA_ERR_CUDA;
-    }
+    const cudaError_t e = scratch_for_current_device(&scratch, false);
+    if (e != cudaSuccess) return lookup_failed(e);
   }
   return la_chunk_fwd(q, k, v, dtype, B, H, L, d_k, d_v, chunk, decay_kind, decay, S0, O,
                       S_final, scratch, need > 0 ? kScratchBytes : 0, cuda_stream);

@@ -252,16 +252,21 @@ la_status la_delta_fwd(const void *q, const void *k, const void *v, int dtype,
  * fixed after start-up, or code that runs while another component holds the
  * allocator.  This entry point takes the same arguments as la_chunk_fwd
  * without the workspace: the segment states live in one static device array
- * of LA_NOALLOC_SCRATCH_BYTES that the library's CUDA module reserves on
- * every GPU that loads it, held until the process exits.  It calls no
- * cudaMalloc, cudaFree or other allocating routine.
+ * of LA_NOALLOC_SCRATCH_BYTES, held on each GPU until the process exits.  It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
  *
+ *   - When the bytes are reserved: the CUDA runtime loads modules lazily by
+ *     default, so the array is placed on a device when it is first looked
+ *     up there.  Call la_chunk_fwd_noalloc_prepare() once per device, with
+ *     that device current, at start-up (before any stream capture and before
+ *     the point where allocation is forbidden).  A device not prepared is
+ *     prepared by its first la_chunk_fwd_noalloc call, which may then
+ *     reserve the bytes itself.
+ *   - The looked-up address is cached per device.  It does not survive
+ *     cudaDeviceReset: call la_chunk_fwd_noalloc_prepare() again after one.
  *   - Problems whose workspace (la_chunk_fwd_workspace_bytes) exceeds
  *     LA_NOALLOC_SCRATCH_BYTES are rejected with LA_ERR_UNSUPPORTED before
  *     any device work; la_last_error() names both sizes.
- *   - The first call on each device looks up the array's device address
- *     (with that device current) and caches it; make that first call before
- *     any stream capture on the device.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind.  Nothing in it has to start at zero (each call writes every
  *     part it reads before reading it), but calls whose kernels overlap on
@@ -269,11 +274,16 @@ la_status la_delta_fwd(const void *q, const void *k, const void *v, int dtype,
  *     ordering) race on it and give wrong results: order them.
  * Errors: as la_chunk_fwd, plus LA_ERR_UNSUPPORTED for a too-large problem.
  */
-#define LA_NOALLOC_SCRATCH_BYTES ((size_t)24 << 20)
+#define LA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 la_status la_chunk_fwd_noalloc(const void *q, const void *k, const void *v, int dtype,
                                int B, int H, int L, int d_k, int d_v, int chunk,
                                int decay_kind, const float *decay,
                                const float *S0, void *O, float *S_final, void *cuda_stream);
+
+/* Look up (again) the static scratch on the current device and cache its
+ * address; under lazy module loading this is where the scratch is reserved.
+ * LA_OK, or LA_ERR_CUDA with the runtime's message. */
+la_status la_chunk_fwd_noalloc_prepare(void);
 
 /* Size in bytes of the static scratch la_chunk_fwd_noalloc uses. */
 size_t la_chunk_fwd_noalloc_scratch_bytes(void);

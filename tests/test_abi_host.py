@@ -89,6 +89,17 @@ def test_workspace_query_is_host_only(lib):
         assert n >= 0
 
 
+def test_noalloc_scratch_holds_every_prefill_workload(lib):
+    """The static scratch of la_chunk_fwd_noalloc is sized so that every prefill workload's
+    segment states fit (on the 152-SM plan the query assumes without a GPU)."""
+    from causal_linear_attention_chunkwise_gb300 import workloads as W
+    cap = lib.la_chunk_fwd_noalloc_scratch_bytes()
+    for w in W.PREFILL.values():
+        need = lib.la_chunk_fwd_workspace_bytes(w.B, w.H, w.L, w.dk, w.dv, w.chunk,
+                                                1 if w.dtype == "bf16" else 0)
+        assert need <= cap, (w.name, need, cap)
+
+
 def test_noncausal_validation_and_workspace(lib):
     p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
     # fp32, mismatched or unsupported head sizes: unsupported
