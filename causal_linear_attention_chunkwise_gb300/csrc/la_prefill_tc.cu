@@ -412,32 +412,47 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     const int g = (warp - WG1) >> 2;           // transform group 0 or 1
     const int t = tid - WG1 * 32 - 128 * g;    // 0..127 within the group
     const uint32_t gbar = g ? BAR_XG1 : BAR_XG0;
-    // Suffix sums of the segment's log decays (group 0): suf[i] = sum_{r > i}
-    // lambda_r, so token i's weight is exp(suf[i]); A_s = sum of all lambda.
+    // Suffix sums of the segment's log decays: suf[i] = sum_{r > i} lambda_r,
+    // so token i's weight is exp(suf[i]); A_s = sum of all lambda.  Both
+    // groups (256 threads) take PER consecutive tokens each: all of a
+    // thread's decay inputs are loaded before any is used, so the prologue
+    // costs one memory round trip, then a suffix scan over threads.
     const int ntok = nc * CH;
     constexpr bool scale = DECAY;
     float seg_total = 0.f;
-    if (g == 0 && scale) {
-      float carry = 0.f;
-      for (int blk = (ntok - 1) / 128; blk >= 0; --blk) {
-        const int i = blk * 128 + t;
-        float lam = (i < ntok) ? token_lambda(p.decay_kind, p.decay, h, bhL, tok0 + i, p.L) : 0.f;
-        float x = lam;
+    if (scale) {
+      constexpr int PER = kMaxSegChunks * CH / 256;
+      const int t2 = tid - WG1 * 32, wid = t2 >> 5;  // 0..255, warp 0..7
+      float raw[PER], sfx[PER];
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          float y = __shfl_down_sync(0xffffffffu, x, off);
-          if (lane + off < 32) x += y;
-        }
-        if (lane == 0) scr[warp - WG1] = x;
-        named_bar_sync(BAR_XG0, 128);
-        float later = carry;
-        for (int w2 = (warp - WG1) + 1; w2 < 4; ++w2) later += scr[w2];
-        if (i < ntok) suf[i] = x - lam + later;
-        const float block_total = scr[0] + scr[1] + scr[2] + scr[3];
-        named_bar_sync(BAR_XG0, 128);
-        carry += block_total;
+      for (int j = 0; j < PER; ++j) {
+        const int i = t2 * PER + j;
+        raw[j] = i < ntok ? token_decay_raw(p.decay_kind, p.decay, h, bhL, tok0 + i, p.L) : 0.f;
       }
-      seg_total = carry;
+      float run = 0.f;  // this thread's tokens after token j
+#pragma unroll
+      for (int j = PER - 1; j >= 0; --j) {
+        sfx[j] = run;
+        if (t2 * PER + j < ntok) run += token_log_decay(p.decay_kind, raw[j]);
+      }
+      float x = run;  // sum over this lane and the later lanes of the warp
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, off);
+        if (lane + off < 32) x += y;
+      }
+      if (lane == 0) scr[wid] = x;
+      named_bar_sync(BAR_XG, 256);
+      float later = x - run, total = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < 8; ++w2) {
+        total += scr[w2];
+        if (w2 > wid) later += scr[w2];
+      }
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if (t2 * PER + j < ntok) suf[t2 * PER + j] = sfx[j] + later;
+      seg_total = total;
     }
     named_bar_sync(BAR_XG, 256);  // suffix sums visible to both groups
     constexpr bool phi = PHI;
