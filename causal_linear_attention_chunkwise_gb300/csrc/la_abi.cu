@@ -99,6 +99,7 @@ const char *kernel_name(unsigned int id) {
     case KID_PREFILL_TC_OUT: return "prefill chunk-output kernel";
     case KID_SELFTEST: return "wait-timeout self-test kernel";
     case KID_NONCAUSAL: return "non-causal output kernel";
+    case KID_CHANNEL_GATE_TC: return "per-channel gate tensor-core kernel";
     default: return "unknown kernel";
   }
 }

@@ -1,0 +1,637 @@
+// la_channel_gate_tc.cu -- the per-channel (GLA) gate on the 5th-gen tensor
+// cores: bf16 q, k, v with fp32 accumulation, chunk C = 64, d_k = d_v = D in
+// {64, 128}.
+//
+// The recurrence ("Linear / sparse attention tutorial" section 2.4 and Q21):
+//   S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T,   o_t = phi(q_t)^T S_t,
+// with one gate per key channel c (a row of S), given as log alpha_{t,c} <= 0.
+// Over a chunk, Lam_{i,c} = sum_{r <= i} log alpha_{r,c} (inclusive prefix
+// from the chunk start) expands it to
+//   o_i   = sum_c q_ic e^{Lam_ic} S_c[c,:] + sum_{j <= i} P_ij v_j,
+//   P_ij  = sum_c q_ic k_jc e^{Lam_ic - Lam_jc},
+//   S_c+1 = diag(e^{Lam_end}) S_c + sum_j (k_j * e^{Lam_end - Lam_j}) v_j^T.
+// The decay sits inside P's channel sum, so it cannot be applied to P after
+// the product.  The chunk's 64 tokens form four query blocks of 16 (the
+// secondary chunking of gated linear attention): block I takes the reference
+// r_I = Lam at its first token, and its scores against every key j up to its
+// own last token are one product of scaled operands,
+//   P[I, j] = (q_i * e^{Lam_i - r_I}) . (k_j * e^{r_I - Lam_j}),
+// where both factors are <= 1 for keys of earlier blocks, and the key factor
+// of the block's own keys is at most e^{span} (span = r_I - Lam at the block's
+// last token).  So each query block needs its own scaled copy of the keys,
+// K^(I) (rows 0 .. 16 I + 15), and the scores are four MMAs
+// P^T[:, 16 I ..] = K^(I) Qh_I^T (M = 64 keys, N = 16 queries).  A block whose
+// span exceeds kDiagSpanMax in some channel (a decay stronger than e^-5 per
+// token on average) would overflow those factors: its key factors are capped,
+// and its 16 x 16 diagonal scores are recomputed exactly on the CUDA cores.
+//
+// Per chunk the MMAs are (D = d_k = d_v):
+//   P^T_I = K^(I) Qh_I^T                 M 64, N 16, K D   (x4)
+//   O     = Qt S_c,  Qt_i = q_i e^{Lam_i} M 64, N D,  K D
+//   S    += Kt^T V,  Kt_j = k_j e^{Lam_end - Lam_j}   M D, N D, K 64
+//   O    += P V                          M 64, N D,  K 64
+// and the state chain (a warpgroup) copies S_c to bf16 for O = Qt S_c and
+// multiplies row c of S by e^{Lam_end,c} in TMEM before the update adds to it.
+// One CTA carries one (b, h) sequence.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "../../include/la_gb300.h"
+#include "la_common.cuh"
+#include "la_internal.h"
+#include "la_ptx.cuh"
+#include "la_tc_sync.cuh"
+#include "la_tma_host.h"
+
+namespace la {
+namespace {
+using namespace tc;
+
+// Largest within-block decay span (in log space) whose key factors e^{span}
+// stay far from fp32 and bf16 overflow in the factored scores.
+constexpr float kDiagSpanMax = 80.f;
+
+// Warp roles: 0 TMA, 1 MMA, 2..11 PREP (320 threads), 12..15 EPI (P and O
+// epilogues), 16..19 ST (the state chain).  The two TMEM warpgroups start at a
+// multiple of four warps, so warp w reaches TMEM lanes 32 (w % 4) ..
+constexpr int kThreads = 640;
+constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_EPI = 12, W_ST = 16;
+constexpr int kPrepThreads = (W_EPI - W_PREP) * 32;
+constexpr uint32_t BAR_PREP = 1, BAR_EPI = 2, BAR_ST = 3;
+
+template <int D>
+struct CgSmem {
+  static constexpr int NST = 2;                 // q | k | v stages
+  static constexpr int NX = D == 64 ? 2 : 1;    // Qt and K^(I) buffers
+  static constexpr int NP = D == 64 ? 2 : 1;    // bf16 P tiles
+  static constexpr int NO = D == 64 ? 2 : 1;    // O staging tiles
+  static constexpr uint32_t TILE = 64 * D * 2;  // [64 tokens][D] bf16 in D/64 boxes of 8 KB
+  static constexpr uint32_t STAGE = 3 * TILE;
+  // K^(I) region: K^(3) rows 0..63, K^(2) rows 64..111, K^(1) 112..143,
+  // K^(0) 144..159; each MMA reads 64 rows from its first (rows past a copy's
+  // keys are masked out of P), so the region holds 144 + 64 rows.
+  static constexpr int KROWS = 208;
+  static constexpr uint32_t KBOX = KROWS * 128;  // one 64-channel box of the region
+  static constexpr uint32_t XBUF = TILE + (D / 64) * KBOX;  // Qt, then the K^(I) region
+  static constexpr uint32_t S_BLOCK = D * 128;              // [D][64] bf16 block of S
+  static constexpr uint32_t OFF_X = NST * STAGE;
+  static constexpr uint32_t OFF_P = OFF_X + NX * XBUF;      // [64 keys][64 queries] bf16
+  static constexpr uint32_t OFF_S = OFF_P + NP * 8192;
+  static constexpr uint32_t OFF_O = OFF_S + (D / 64) * S_BLOCK;
+  static constexpr uint32_t OFF_DEC = OFF_O + NO * TILE;    // [NST][D] e^{Lam_end,c}
+  static constexpr uint32_t OFF_TOT = OFF_DEC + NST * D * 4;  // [4][D] block sums
+  static constexpr uint32_t OFF_EX = OFF_TOT + 4 * D * 4;   // [16][16] exact diagonal scores
+  static constexpr uint32_t OFF_FLAG = OFF_EX + 256 * 4;    // [NST] span exceeded
+  static constexpr uint32_t OFF_BAR = OFF_FLAG + 16;
+  static constexpr int NBAR = 3 * NST + NX + 2 + NP + 2 + 2 + 2 + 1;
+  static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
+  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && XBUF % 1024 == 0 &&
+                    OFF_P % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+  static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
+  // TMEM columns: P^T x2 (64 each), O x2 (D each), S (D).
+  static constexpr uint32_t T_P = 0, T_O = 128, T_S = 128 + 2 * D, T_COLS = 512;
+  static_assert(T_S + D <= T_COLS, "TMEM budget");
+};
+
+// First row of K^(I) in the K^(I) region.
+__host__ __device__ constexpr int k_row0(int I) { return I == 3 ? 0 : I == 2 ? 64 : I == 1 ? 112 : 144; }
+
+struct CgParams {
+  int H, L, BH, n_chunks;
+  const float *log_alpha;  // [BH][L][D]
+  const __nv_bfloat16 *q, *k;
+  const float *S0;
+  float *S_final;
+  unsigned int *err;
+};
+
+// Byte offset of element (row, col) in a bf16 tile of 128-byte swizzled rows
+// whose 64-column boxes are `box` bytes apart.
+__device__ __forceinline__ uint32_t tile_off(int row, int col, uint32_t box) {
+  return (uint32_t)(col >> 6) * box + sw128_offset((uint32_t)row, (uint32_t)(col & 63));
+}
+
+__device__ __forceinline__ float ld_bf16(const unsigned char *p) {
+  return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
+}
+__device__ __forceinline__ void st_bf16(unsigned char *p, float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  *reinterpret_cast<__nv_bfloat16 *>(p) = b;
+}
+
+__device__ __forceinline__ float log_alpha_at(const CgParams &p, size_t bhL, int tok, int ch,
+                                              int D) {
+  return tok < p.L ? p.log_alpha[(bhL + tok) * D + ch] : 0.f;  // padding decays nothing
+}
+
+// Exact scores of the four 16 x 16 diagonal blocks of chunk c, written over
+// the factored ones in the bf16 P tile (row = key, column = query): for a
+// chunk whose within-block decay span exceeds kDiagSpanMax somewhere.  Rare:
+// one thread per channel forms its terms q_ic k_jc e^{Lam_ic - Lam_jc} and
+// adds them into a shared [16][16] table.  Called by the 128 EPI threads.
+template <int D, bool PHI>
+__device__ __noinline__ void exact_diagonal(const CgParams &p, int bh, int tok0, unsigned char *pt,
+                                            float *ex, int t) {
+  const size_t bhL = (size_t)bh * p.L;
+  for (int I = 0; I < 4; ++I) {
+    for (int x = t; x < 256; x += 128) ex[x] = 0.f;
+    named_bar_sync(BAR_EPI, 128);
+    if (t < D) {
+      float lam[16], qv[16], kv[16];
+      float run = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int tok = tok0 + 16 * I + i;
+        run += log_alpha_at(p, bhL, tok, t, D);
+        lam[i] = run;
+        float a = 0.f, b = 0.f;
+        if (tok < p.L) {
+          a = __bfloat162float(p.q[(bhL + tok) * D + t]);
+          b = __bfloat162float(p.k[(bhL + tok) * D + t]);
+        }
+        qv[i] = PHI ? elu1_fast(a) : a;
+        kv[i] = PHI ? elu1_fast(b) : b;
+      }
+      for (int i = 0; i < 16; ++i)
+        for (int j = 0; j <= i; ++j)
+          atomicAdd(&ex[i * 16 + j], qv[i] * kv[j] * __expf(lam[i] - lam[j]));
+    }
+    named_bar_sync(BAR_EPI, 128);
+    for (int x = t; x < 256; x += 128) {
+      const int i = x >> 4, j = x & 15;
+      if (j <= i)
+        st_bf16(pt + sw128_offset(16 * I + j, 16 * I + i), ex[x]);
+    }
+    named_bar_sync(BAR_EPI, 128);
+  }
+}
+
+template <int D, bool PHI>
+__global__ void __launch_bounds__(kThreads, 1)
+channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmO, CgParams p) {
+  using SM = CgSmem<D>;
+  constexpr int NST = SM::NST, NX = SM::NX, NP = SM::NP, NO = SM::NO;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *dec = reinterpret_cast<float *>(smem + SM::OFF_DEC);
+  float *tot = reinterpret_cast<float *>(smem + SM::OFF_TOT);
+  float *ex = reinterpret_cast<float *>(smem + SM::OFF_EX);
+  volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + SM::OFF_FLAG);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
+  uint64_t *empty = full + NST;
+  uint64_t *prep = empty + NST;     // [NST] scaled operands, factors and flag ready
+  uint64_t *xfree = prep + NST;     // [NX] the MMAs reading Qt and K^(I) are done
+  uint64_t *p_full = xfree + NX;    // [2] P^T in TMEM
+  uint64_t *p_ready = p_full + 2;   // [NP] bf16 P in shared memory
+  uint64_t *o_full = p_ready + NP;  // [2] O complete in TMEM
+  uint64_t *o_free = o_full + 2;    // [2] O TMEM buffer read
+  uint64_t *s_ready = o_free + 2;   // bf16 S_c in smem, TMEM S = diag(e^{Lam_end}) S_c
+  uint64_t *s_done = s_ready + 1;   // the update of chunk c (and every MMA before it) done
+  uint64_t *drain = s_done + 1;
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x;
+  const int nc = p.n_chunks;
+  const size_t bhL = (size_t)bh * p.L;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&prep[s], 1);
+      flag[s] = 0;
+    }
+    for (int i = 0; i < NX; ++i) mbar_init(&xfree[i], 1);
+    for (int i = 0; i < NP; ++i) mbar_init(&p_ready[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 1);
+    }
+    mbar_init(s_ready, 1);
+    mbar_init(s_done, 1);
+    mbar_init(drain, 1);
+    ctl->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == W_MMA) {
+    tmem_alloc(&ctl->tmem_base, SM::T_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == W_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
+      int issued = 0;
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (c >= NST && !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 1))
+          break;
+        unsigned char *stg = smem + s * SM::STAGE;
+        mbar_arrive_expect_tx(&full[s], SM::STAGE);
+        const int tok = c * CH;
+        for (int b = 0; b < D / BOX; ++b) {
+          tma_load_3d(stg + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
+          tma_load_3d(stg + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
+          tma_load_3d(stg + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
+        }
+        issued = c + 1;
+      }
+      if (*(volatile uint32_t *)&ctl->abort)
+        for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+      for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nc > 0) {
+      constexpr uint32_t id_p = idesc_bf16_f32(64, 16, false, false);
+      constexpr uint32_t id_qs = idesc_bf16_f32(64, D, false, true);
+      constexpr uint32_t id_kv = idesc_bf16_f32(D, D, true, true);
+      constexpr uint32_t id_pv = idesc_bf16_f32(64, D, true, true);
+      constexpr uint32_t HI = smem_desc_sw128_hi(1024);
+      const uint32_t sbase = smem_u32(smem);
+      const uint32_t dKM = smem_desc_sw128_lo(sbase, 16);           // K-major rows
+      const uint32_t dMN = smem_desc_sw128_lo(sbase, BOX_BYTES);    // MN-major, 8 KB blocks
+      const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::S_BLOCK);  // MN-major state blocks
+      auto at = [](uint32_t d, uint32_t off) { return d + (off >> 4); };
+      auto w = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+        return wait1(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site);
+      };
+      // P^T of chunk c: four MMAs, one per query block.
+      auto issue_p = [&](int c) {
+        const uint32_t qo = (c % NST) * SM::STAGE;
+        const uint32_t xo = SM::OFF_X + (c % NX) * SM::XBUF + SM::TILE;
+        for (int I = 0; I < 4; ++I) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_w(tmem + SM::T_P + 64 * (c & 1) + 16 * I,
+                       at(dKM, xo + (kk / 4) * SM::KBOX + k_row0(I) * 128 + 32 * (kk % 4)),
+                       at(dKM, qo + (kk / 4) * BOX_BYTES + 16 * I * 128 + 32 * (kk % 4)), HI, id_p,
+                       kk > 0);
+        }
+        mma_commit(&p_full[c & 1]);
+      };
+      bool ok = w(&prep[0], 0, 2);
+      if (ok) {
+        tc_fence_after();
+        issue_p(0);
+      }
+      for (int c = 0; ok && c < nc; ++c) {
+        const int s = c % NST, xb = c % NX, b = c & 1;
+        if (!(ok = w(s_ready, c & 1, 3))) break;
+        if (c >= 2 && !(ok = w(&o_free[b], ((c >> 1) - 1) & 1, 4))) break;
+        tc_fence_after();
+        const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
+        const uint32_t xo = SM::OFF_X + xb * SM::XBUF;
+        const uint32_t o_t = tmem + SM::T_O + D * b;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)  // O = Qt S_c
+          mma_bf16_w(o_t, at(dKM, xo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)),
+                     at(dMS, SM::OFF_S + 2048 * kk), HI, id_qs, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)  // S += Kt^T V
+          mma_bf16_w(tmem + SM::T_S, at(dMN, ko + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_kv,
+                     1u);
+        mma_commit(s_done);
+        mma_commit(&xfree[xb]);
+        if (c + 1 < nc) {
+          if (!(ok = w(&prep[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
+          tc_fence_after();
+          issue_p(c + 1);
+        }
+        if (!(ok = w(&p_ready[c % NP], (c / NP) & 1, 6))) break;
+        tc_fence_after();
+        const uint32_t po = SM::OFF_P + 8192 * (c % NP);
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)  // O += P V
+          mma_bf16_w(o_t, at(dMN, po + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_pv, 1u);
+        mma_commit(&o_full[b]);
+        mma_commit(&empty[s]);
+      }
+      // Every issued MMA finishes before TMEM is released (on the normal path
+      // the consumers have already observed them).
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else if (warp >= W_PREP && warp < W_EPI) {
+    // ------------------------------------------------------------ PREP
+    const int t = tid - W_PREP * 32;
+    auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_PREP, t);
+    };
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST, xb = c % NX;
+      const int tok0 = c * CH;
+      if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
+      // Block sums of the log decays, [4][D].
+      for (int it = t; it < 4 * D; it += kPrepThreads) {
+        const int I = it / D, ch = it % D;
+        float a[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = log_alpha_at(p, bhL, tok0 + 16 * I + i, ch, D);
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) sum += a[i];
+        tot[I * D + ch] = sum;
+      }
+      if (t == 0) flag[s] = 0;
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      if (c >= NX && !(ok = gwait(&xfree[xb], ((c / NX) - 1) & 1, 8))) break;
+      unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
+      unsigned char *xq = smem + SM::OFF_X + xb * SM::XBUF, *xk = xq + SM::TILE;
+      for (int it = t; it < 4 * D; it += kPrepThreads) {
+        const int I = it / D, ch = it % D;
+        float base = 0.f, lend = 0.f, rnext[4];
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+          const float tj = tot[J * D + ch];
+          rnext[J] = lend;  // sum of the blocks before J
+          if (J < I) base += tj;
+          lend += tj;
+        }
+        // r_{I'} for the later query blocks: the sum before them plus their
+        // first token's own log decay.
+#pragma unroll
+        for (int J = 0; J < 4; ++J)
+          if (J > I) rnext[J] += log_alpha_at(p, bhL, tok0 + 16 * J, ch, D);
+        float lam[16], qv[16], kv[16];
+        float run = base;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          run += log_alpha_at(p, bhL, tok0 + 16 * I + i, ch, D);
+          lam[i] = run;
+          const uint32_t off = tile_off(16 * I + i, ch, BOX_BYTES);
+          const float a = ld_bf16(qt + off), b = ld_bf16(kt + off);
+          qv[i] = PHI ? elu1_fast(a) : a;
+          kv[i] = PHI ? elu1_fast(b) : b;
+        }
+        const float r = lam[0];
+        if (r - lam[15] > kDiagSpanMax) flag[s] = 1u;
+        if (I == 3) dec[s * D + ch] = __expf(lend);
+        const float er = __expf(r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int row = 16 * I + i;
+          const uint32_t off = tile_off(row, ch, BOX_BYTES);
+          const float qh = qv[i] * __expf(lam[i] - r);               // <= 1 factor
+          st_bf16(qt + off, qh);                                     // Qh (in place)
+          st_bf16(xq + off, qh * er);                                // Qt = q e^{Lam}
+          st_bf16(kt + off, kv[i] * __expf(lend - lam[i]));          // Kt (in place)
+          st_bf16(xk + tile_off(k_row0(I) + row, ch, SM::KBOX),      // own block of K^(I)
+                  kv[i] * __expf(fminf(r - lam[i], kDiagSpanMax)));
+#pragma unroll
+          for (int J = 0; J < 4; ++J)                                // K^(J), J > I
+            if (J > I)
+              st_bf16(xk + tile_off(k_row0(J) + row, ch, SM::KBOX), kv[i] * __expf(rnext[J] - lam[i]));
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      if (t == 0) mbar_arrive(&prep[s]);
+    }
+  } else if (warp >= W_EPI && warp < W_ST) {
+    // ------------------------------------------------------------ EPI: P and O epilogues
+    const int t = tid - W_EPI * 32;
+    const int quarter = warp & 3;
+    const int row = acc_row<64>(quarter, lane);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto ewait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_wg(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_EPI);
+    };
+    auto p_epilogue = [&](int c) -> bool {
+      const int s = c % NST;
+      if (!ewait(&p_full[c & 1], (c >> 1) & 1, 9)) return false;
+      if (!ewait(&prep[s], (c / NST) & 1, 10)) return false;
+      if (NP == 1 && c >= 1 && !ewait(&o_full[(c - 1) & 1], ((c - 1) >> 1) & 1, 11)) return false;
+      tc_fence_after();
+      unsigned char *pt = smem + SM::OFF_P + 8192 * (c % NP);
+      uint32_t r[2][32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_off + SM::T_P + 64 * (c & 1), r[0]);
+      tmem_ld32(tmem + lane_off + SM::T_P + 64 * (c & 1) + 32, r[1]);
+      tmem_ld_wait();
+      if (row >= 0) {  // row = key j; column = query i; causal: keep i >= j
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = 32 * h + 8 * q8 + 2 * e;
+              w4[e] = pack_bf16(i >= row ? __uint_as_float(r[h][8 * q8 + 2 * e]) : 0.f,
+                                i + 1 >= row ? __uint_as_float(r[h][8 * q8 + 2 * e + 1]) : 0.f);
+            }
+            const int chunk16 = 4 * h + q8;
+            *reinterpret_cast<uint4 *>(pt + row * 128 + ((chunk16 ^ (row & 7)) << 4)) =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      if (flag[s]) {
+        named_bar_sync(BAR_EPI, 128);
+        exact_diagonal<D, PHI>(p, bh, c * CH, pt, ex, t);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_EPI, 128);
+      if (t == 0) mbar_arrive(&p_ready[c % NP]);
+      return true;
+    };
+    auto o_epilogue = [&](int c) -> bool {
+      const int b = c & 1;
+      if (!ewait(&o_full[b], (c >> 1) & 1, 12)) return false;
+      tc_fence_after();
+      if (t == 0) {
+        if (NO == 2) tma_store_wait_read<1>();
+        else tma_store_wait_read<0>();
+      }
+      __syncwarp();
+      named_bar_sync(BAR_EPI, 128);
+      unsigned char *o_sm = smem + SM::OFF_O + (c % NO) * SM::TILE;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_O + D * b + col, r);
+        tmem_ld_wait();
+        if (row >= 0) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pk[j] = pack_bf16(__uint_as_float(r[16 * h + 2 * j]), __uint_as_float(r[16 * h + 2 * j + 1]));
+            st_row16(o_sm, BOX_BYTES, row, col + 16 * h, pk);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_EPI, 128);
+      if (t == 0) {
+        mbar_arrive(&o_free[b]);
+        for (int bb = 0; bb < D / BOX; ++bb)
+          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, c * CH, bh);
+        tma_store_commit();
+      }
+      return true;
+    };
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      ok = p_epilogue(c);
+      if (ok && c >= 1) ok = o_epilogue(c - 1);
+    }
+    if (ok && nc > 0) o_epilogue(nc - 1);
+    if (t == 0) tma_store_wait_all();
+  } else if (warp >= W_ST) {
+    // ------------------------------------------------------------ ST: the state chain
+    const int t = tid - W_ST * 32;
+    const int quarter = warp & 3;
+    const int srow = acc_row<D>(quarter, lane);  // key channel
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto swait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_wg(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_ST);
+    };
+    // S0 (or zeros) into TMEM.
+#pragma unroll 1
+    for (int col = 0; col < D; col += 32) {
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+      if (srow >= 0 && p.S0) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((size_t)bh * D + srow) * D + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 f = src[j];
+          r[4 * j] = __float_as_uint(f.x);
+          r[4 * j + 1] = __float_as_uint(f.y);
+          r[4 * j + 2] = __float_as_uint(f.z);
+          r[4 * j + 3] = __float_as_uint(f.w);
+        }
+      }
+      __syncwarp();
+      tmem_st32(tmem + lane_off + SM::T_S + col, r);
+    }
+    tmem_st_wait();
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST;
+      if (!(ok = swait(&prep[s], (c / NST) & 1, 13))) break;
+      if (c >= 1 && !(ok = swait(s_done, (c - 1) & 1, 14))) break;
+      tc_fence_after();
+      const float e = srow >= 0 ? dec[s * D + srow] : 1.f;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_S + col, r);
+        tmem_ld_wait();
+        if (srow >= 0) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pk[j] = pack_bf16(__uint_as_float(r[16 * h + 2 * j]), __uint_as_float(r[16 * h + 2 * j + 1]));
+            st_row16(smem + SM::OFF_S, SM::S_BLOCK, srow, col + 16 * h, pk);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * e);
+        __syncwarp();
+        tmem_st32(tmem + lane_off + SM::T_S + col, r);
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_ST, 128);
+      if (t == 0) mbar_arrive(s_ready);
+    }
+    if (ok && nc > 0 && swait(s_done, (nc - 1) & 1, 15) && p.S_final) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_S + col, r);
+        tmem_ld_wait();
+        if (srow >= 0) {
+          float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D + col);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_MMA) {
+    __syncwarp();
+    tmem_dealloc(tmem, SM::T_COLS);
+  }
+}
+
+template <int D, bool PHI>
+cudaError_t launch_cg(const VariantArgs &a) {
+  using SM = CgSmem<D>;
+  const int BH = a.B * a.H;
+  CgParams p{};
+  p.H = a.H;
+  p.L = a.L;
+  p.BH = BH;
+  p.n_chunks = (a.L + CH - 1) / CH;
+  p.log_alpha = a.decay;
+  p.q = static_cast<const __nv_bfloat16 *>(a.q);
+  p.k = static_cast<const __nv_bfloat16 *>(a.k);
+  p.S0 = a.S0;
+  p.S_final = a.S_final;
+  p.err = device_error_word();
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tk, a.k, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX))
+    return cudaErrorInvalidValue;
+  auto kern = channel_gate_tc_kernel<D, PHI>;
+  static int smem_set[64];
+  cudaError_t e = set_smem_once(kern, SM::BYTES, smem_set);
+  if (e != cudaSuccess) return e;
+  kern<<<BH, kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool channel_gate_tc_supported(const VariantArgs &a) {
+  return a.form == VARIANT_CHANNEL_GATE && a.dtype == LA_BF16 && a.chunk == CH && a.dk == a.dv &&
+         (a.dk == 64 || a.dk == 128);
+}
+
+cudaError_t launch_channel_gate_tc(const VariantArgs &a) {
+  const bool phi = a.phi != LA_PHI_IDENTITY;
+  if (a.dk == 128) return phi ? launch_cg<128, true>(a) : launch_cg<128, false>(a);
+  return phi ? launch_cg<64, true>(a) : launch_cg<64, false>(a);
+}
+
+}  // namespace la

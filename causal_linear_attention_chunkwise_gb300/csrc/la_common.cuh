@@ -13,6 +13,7 @@ enum : unsigned int {
   KID_PREFILL_TC_OUT = 2,
   KID_SELFTEST = 3,
   KID_NONCAUSAL = 4,
+  KID_CHANNEL_GATE_TC = 5,
 };
 
 __device__ __forceinline__ void record_device_error(unsigned int *word, unsigned int kernel,

@@ -78,6 +78,11 @@ struct VariantArgs {
 };
 cudaError_t launch_variant(const VariantArgs &a);
 
+// The per-channel gate on the tensor cores: bf16, chunk 64, d_k == d_v in
+// {64, 128}; launch_variant takes this path when it applies.
+bool channel_gate_tc_supported(const VariantArgs &a);
+cudaError_t launch_channel_gate_tc(const VariantArgs &a);
+
 // Denominator of the normalised form and the division of O by it, after the
 // numerator has been written to O (d_k <= 128).
 struct NormaliserArgs {

@@ -31,7 +31,7 @@ struct Ctl {
 // ---------------------------------------------------------------- waits
 // Single-thread bounded wait; on timeout records the error and sets abort.
 // The first test is inline; the polling loop is one shared out-of-line copy.
-__device__ __noinline__ bool wait1_slow(uint64_t *bar, uint32_t parity, Ctl *ctl,
+static __device__ __noinline__ bool wait1_slow(uint64_t *bar, uint32_t parity, Ctl *ctl,
                                         unsigned int *err, uint32_t kid, uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < kSpinCap; ++i) {
@@ -55,7 +55,7 @@ __device__ __forceinline__ bool wait1(uint64_t *bar, uint32_t parity, Ctl *ctl,
 // After an abort: wait (bounded, ignoring the abort flag) for a phase that
 // in-flight asynchronous work will still complete, so that no TMA write or
 // MMA outlives the CTA's shared memory and TMEM.
-__device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+static __device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 0; i < kSpinCap; ++i) {
     if (mbar_try_wait(bar, parity)) return;

@@ -341,6 +341,7 @@ cudaError_t launch_variant(const VariantArgs &a) {
   const bool f32 = a.dtype == LA_F32;
   switch (a.form) {
     case VARIANT_CHANNEL_GATE:
+      if (channel_gate_tc_supported(a)) return launch_channel_gate_tc(a);
       return f32 ? launch_channel_gate_t<float>(a) : launch_channel_gate_t<__nv_bfloat16>(a);
     case VARIANT_DELTA:
       return f32 ? launch_delta_t<float>(a) : launch_delta_t<__nv_bfloat16>(a);

@@ -194,12 +194,51 @@ def test_channel_gate_with_equal_channels_is_the_token_gate():
     parity.check(S1.cpu(), S2.cpu(), "f32", "S")
 
 
-@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f32", 16)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("phi", ["identity", "elu1"])
+@pytest.mark.parametrize("L", [64, 65, 200, 1000])
+def test_channel_gate_tensor_core_path(d, phi, L):
+    """bf16, chunk 64, d_k = d_v in {64, 128}: the tcgen05 kernel.  One chunk,
+    one chunk and a token, ragged tails and a longer run, from a non-zero S0;
+    identity phi leaves q . k free to cancel, elu + 1 keeps it positive."""
+    B, H = 2, 2
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=21 + L,
+                                with_state=True)
+    api.la_set_feature_map(phi)
+    O, S = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]),
+                                   _d(inp["log_alpha"]), 64, _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], inp["log_alpha"], phi=phi,
+                                       S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, "bf16", "O")
+    parity.check(S.cpu(), S_ref, "bf16", "S")
+
+
+def test_channel_gate_full_workload_shape_on_sampled_sequences():
+    """The benchmarked shape (B4 H16 L4096 d64, bf16, elu + 1, S0) in one call,
+    three sequences recomputed by the oracle."""
+    B, H, L, d = 4, 16, 4096, 64
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=0, with_state=True)
+    api.la_set_feature_map("elu1")
+    O, S = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]),
+                                   _d(inp["log_alpha"]), 64, _d(inp["S0"]))
+    api.la_device_status()
+    for b, h in [(0, 0), (1, 7), (3, 15)]:
+        sl = lambda x: x[b:b + 1, h:h + 1]  # noqa: E731
+        O_ref, S_ref = oracle.channel_gate(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]),
+                                           sl(inp["log_alpha"]), phi="elu1", S0=sl(inp["S0"]))
+        parity.check(sl(O).cpu(), O_ref, "bf16", f"O[{b},{h}]")
+        parity.check(sl(S).cpu(), S_ref, "bf16", f"S[{b},{h}]")
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 64), ("bf16", 128), ("f32", 16)])
 def test_channel_gate_strong_decay_chunks(dtype, d):
     """Chunks whose cumulative log decay leaves [-80, 80] take the exact
     per-element form, the others the split form: the second and fourth chunks
     here decay ten times harder (down to e^-448 over a chunk), so the two forms
-    alternate and hand the state to each other."""
+    alternate and hand the state to each other.  On the tensor-core path (bf16)
+    those chunks have 16-token blocks whose decay span passes 80, whose
+    diagonal scores are then recomputed exactly."""
     B, H, L = 2, 2, 300
     inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, dtype, seed=13, with_state=True)
     la = inp["log_alpha"].clone()
