@@ -100,6 +100,7 @@ const char *kernel_name(unsigned int id) {
     case KID_SELFTEST: return "wait-timeout self-test kernel";
     case KID_NONCAUSAL: return "non-causal output kernel";
     case KID_CHANNEL_GATE_TC: return "per-channel gate tensor-core kernel";
+    case KID_DELTA_TC: return "delta-rule tensor-core kernel";
     default: return "unknown kernel";
   }
 }

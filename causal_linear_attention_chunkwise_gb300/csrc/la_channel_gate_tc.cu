@@ -63,7 +63,7 @@ constexpr uint32_t BAR_PREP = 1, BAR_EPI = 2, BAR_ST = 3;
 
 template <int D>
 struct CgSmem {
-  static constexpr int NST = 2;                 // q | k | v stages
+  static constexpr int NST = D == 64 ? 4 : 2;   // q | k | v stages
   static constexpr int NX = D == 64 ? 2 : 1;    // Qt and K^(I) buffers
   static constexpr int NP = D == 64 ? 2 : 1;    // bf16 P tiles
   static constexpr int NO = D == 64 ? 2 : 1;    // O staging tiles
@@ -269,9 +269,6 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       const uint32_t dMN = smem_desc_sw128_lo(sbase, BOX_BYTES);    // MN-major, 8 KB blocks
       const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::S_BLOCK);  // MN-major state blocks
       auto at = [](uint32_t d, uint32_t off) { return d + (off >> 4); };
-      auto w = [&](uint64_t *bar, uint32_t par, uint32_t site) {
-        return wait1(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site);
-      };
       // P^T of chunk c: four MMAs, one per query block.
       auto issue_p = [&](int c) {
         const uint32_t qo = (c % NST) * SM::STAGE;
@@ -286,42 +283,75 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         mma_commit(&p_full[c & 1]);
       };
-      bool ok = w(&prep[0], 0, 2);
-      if (ok) {
-        tc_fence_after();
-        issue_p(0);
-      }
-      for (int c = 0; ok && c < nc; ++c) {
-        const int s = c % NST, xb = c % NX, b = c & 1;
-        if (!(ok = w(s_ready, c & 1, 3))) break;
-        if (c >= 2 && !(ok = w(&o_free[b], ((c >> 1) - 1) & 1, 4))) break;
-        tc_fence_after();
-        const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
-        const uint32_t xo = SM::OFF_X + xb * SM::XBUF;
-        const uint32_t o_t = tmem + SM::T_O + D * b;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)  // O = Qt S_c
-          mma_bf16_w(o_t, at(dKM, xo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)),
-                     at(dMS, SM::OFF_S + 2048 * kk), HI, id_qs, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)  // S += Kt^T V
-          mma_bf16_w(tmem + SM::T_S, at(dMN, ko + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_kv,
-                     1u);
-        mma_commit(s_done);
-        mma_commit(&xfree[xb]);
-        if (c + 1 < nc) {
-          if (!(ok = w(&prep[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
+      // Three streams of MMA work, each in chunk order, issued as their inputs
+      // become ready (non-blocking tests), so that no stream waits behind
+      // another's inputs:
+      //   P^T of chunk kp: its operands prepared; its TMEM buffer was read by
+      //     the P epilogue of chunk kp - 2, whose P V has been issued;
+      //   chain step kc (O = Qt S_c, S += Kt^T V): after P^T of kc, so that
+      //     the commit freeing Qt and K^(I) covers it; O's buffer read;
+      //   P V of chunk km: after its chain step (which starts O).
+      int kp = 0, kc = 0, km = 0;
+      bool ok = true;
+      uint64_t idle_since = 0;
+      uint32_t idle = 0;
+      while (ok && km < nc) {
+        bool did = false;
+        if (kp < nc && kp <= km + 1 && mbar_test(&prep[kp % NST], (kp / NST) & 1)) {
           tc_fence_after();
-          issue_p(c + 1);
+          issue_p(kp);
+          ++kp;
+          did = true;
         }
-        if (!(ok = w(&p_ready[c % NP], (c / NP) & 1, 6))) break;
-        tc_fence_after();
-        const uint32_t po = SM::OFF_P + 8192 * (c % NP);
+        if (kc < kp && mbar_test(s_ready, kc & 1) &&
+            (kc < 2 || mbar_test(&o_free[kc & 1], ((kc >> 1) - 1) & 1))) {
+          tc_fence_after();
+          const int s = kc % NST, xb = kc % NX;
+          const uint32_t ko = s * SM::STAGE + SM::TILE, vo = ko + SM::TILE;
+          const uint32_t xo = SM::OFF_X + xb * SM::XBUF;
+          const uint32_t o_t = tmem + SM::T_O + D * (kc & 1);
 #pragma unroll
-        for (int kk = 0; kk < CH / 16; ++kk)  // O += P V
-          mma_bf16_w(o_t, at(dMN, po + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_pv, 1u);
-        mma_commit(&o_full[b]);
-        mma_commit(&empty[s]);
+          for (int kk = 0; kk < D / 16; ++kk)  // O = Qt S_c
+            mma_bf16_w(o_t, at(dKM, xo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)),
+                       at(dMS, SM::OFF_S + 2048 * kk), HI, id_qs, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < CH / 16; ++kk)  // S += Kt^T V
+            mma_bf16_w(tmem + SM::T_S, at(dMN, ko + 2048 * kk), at(dMN, vo + 2048 * kk), HI,
+                       id_kv, 1u);
+          mma_commit(s_done);
+          mma_commit(&xfree[xb]);
+          ++kc;
+          did = true;
+        }
+        if (km < kc && mbar_test(&p_ready[km % NP], (km / NP) & 1)) {
+          tc_fence_after();
+          const int s = km % NST;
+          const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * (km % NP);
+          const uint32_t o_t = tmem + SM::T_O + D * (km & 1);
+#pragma unroll
+          for (int kk = 0; kk < CH / 16; ++kk)  // O += P V
+            mma_bf16_w(o_t, at(dMN, po + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_pv, 1u);
+          mma_commit(&o_full[km & 1]);
+          mma_commit(&empty[s]);
+          ++km;
+          did = true;
+        }
+        if (did) {
+          idle = 0;
+          idle_since = 0;
+        } else if (__nanosleep(20), ++idle == 64) {  // bounded: give up after the limit
+          idle = 0;
+          const uint64_t now = global_timer_ns();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > kWaitNs || *(volatile uint32_t *)&ctl->abort) {
+            if (!*(volatile uint32_t *)&ctl->abort) {
+              atomicExch(&ctl->abort, 1u);
+              record_device_error(p.err, KID_CHANNEL_GATE_TC, 3);
+            }
+            ok = false;
+          }
+        }
       }
       // Every issued MMA finishes before TMEM is released (on the normal path
       // the consumers have already observed them).
@@ -338,8 +368,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST, xb = c % NX;
       const int tok0 = c * CH;
-      if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
-      // Block sums of the log decays, [4][D].
+      // Block sums of the log decays, [4][D]: they do not need the stage, so
+      // their loads go out while the chunk's tiles are still arriving.
       for (int it = t; it < 4 * D; it += kPrepThreads) {
         const int I = it / D, ch = it % D;
         float a[16];
@@ -350,6 +380,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         for (int i = 0; i < 16; ++i) sum += a[i];
         tot[I * D + ch] = sum;
       }
+      if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
       if (t == 0) flag[s] = 0;
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (c >= NX && !(ok = gwait(&xfree[xb], ((c / NX) - 1) & 1, 8))) break;

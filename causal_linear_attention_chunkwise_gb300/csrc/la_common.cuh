@@ -14,6 +14,7 @@ enum : unsigned int {
   KID_SELFTEST = 3,
   KID_NONCAUSAL = 4,
   KID_CHANNEL_GATE_TC = 5,
+  KID_DELTA_TC = 6,
 };
 
 __device__ __forceinline__ void record_device_error(unsigned int *word, unsigned int kernel,

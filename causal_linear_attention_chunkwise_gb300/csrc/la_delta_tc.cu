@@ -1,0 +1,717 @@
+// la_delta_tc.cu -- the (gated) delta rule on the 5th-gen tensor cores, a chunk
+// of 64 tokens at a time: bf16 q, k, v with fp32 accumulation, d_k = d_v = D in
+// {64, 128}.
+//
+// The rule ("Linear / Sparse Attention - minimal runnable implementation",
+// delta_rule_recurrent; "Linear / sparse attention tutorial" section 5 and
+// Q21, the gated form), with S kept as [d_k, d_v] like every other state here:
+//   S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+//   o_t = phi(q_t)^T S_t,   k_t = phi(k_t) as given.
+// Writing u_t = beta_t (v_t - alpha_t S_{t-1}^T k_t) turns it into
+// S_t = alpha_t S_{t-1} + k_t u_t^T, and unrolling it over a chunk (Lam the
+// inclusive prefix of log alpha from the chunk start, Gam_tj = e^{Lam_t - Lam_j})
+// gives the unit lower-triangular system (I + A) U = diag(beta) V -
+// diag(beta e^{Lam}) K S_in with A_tj = beta_t Gam_tj (k_t . k_j) for j < t.
+// So with T = (I + A)^{-1} (the WY form; the tutorial's section 5.3):
+//   W  = T diag(beta e^{Lam}) K,  U0 = T diag(beta) V,  U = U0 - W S_in,
+//   O  = diag(e^{Lam}) Q S_in + P U,       P_tj = Gam_tj (q_t . k_j), j <= t,
+//   S' = e^{Lam_end} S_in + Kt^T U,        Kt_j = e^{Lam_end - Lam_j} k_j.
+// Substituting U, everything that does not involve S_in is formed off the
+// state chain, once per chunk:
+//   M  = -Kt^T W      (d_k x d_k),   Qe = diag(e^{Lam}) Q - P W   (64 x d_k),
+// and the chain itself is
+//   S' = e^{Lam_end} S_in + Kt^T U0 + M S_in,     O = P U0 + Qe S_in.
+// The state stays fp32 in TMEM; only the products with S_in see its bf16 copy.
+//
+// Per chunk (one CTA per (b, h) sequence):
+//   PREP   phi on q, k; Lam, beta; V <- diag(beta) V; Kb = diag(beta e^Lam) K;
+//          after K K^T: K <- Kt in place
+//   MMA    G = K K^T, P' = Q K^T                     (M 64, N 64, K D)
+//   SOLVE  A and P from G, P'; T = (I + A)^{-1} by 16 x 16 blocks (CUDA cores, fp32)
+//   MMA    W = T Kb, U0 = T V                        (M 64, N D, K 64)
+//   EPI    W, U0 -> bf16
+//   MMA    Kt^T W, P W, O = P U0                     (M D / 64, N D, K 64)
+//   EPI    M = -Kt^T W -> bf16, Qe = e^Lam Q - P W -> bf16 (in place of Q)
+//   MMA    chain: S += Kt^T U0, S += M S_in, O += Qe S_in
+//   ST     S_in for the next chunk: bf16 copy, TMEM S *= e^{Lam_end}
+//   EPI    O -> bf16 -> TMA store
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "../../include/la_gb300.h"
+#include "la_common.cuh"
+#include "la_internal.h"
+#include "la_ptx.cuh"
+#include "la_tc_sync.cuh"
+#include "la_tma_host.h"
+
+namespace la {
+namespace {
+using namespace tc;
+
+// Warp roles: 0 TMA, 1 MMA, 2..7 PREP (192 threads), 8..11 SOLVE, 12..15 EPI,
+// 16..19 ST.  The TMEM warpgroups start at a multiple of four warps.
+constexpr int kThreads = 640;
+constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_SOLVE = 8, W_EPI = 12, W_ST = 16;
+constexpr int kPrepThreads = (W_SOLVE - W_PREP) * 32;
+constexpr uint32_t BAR_PREP = 1, BAR_SOLVE = 2, BAR_EPI = 3, BAR_ST = 4;
+constexpr int kAS = 65;  // fp32 row stride of the solve's A and T (conflict-free columns)
+
+template <int D>
+struct DtSmem {
+  static constexpr bool SMALL = D == 64;
+  static constexpr int NST = SMALL ? 2 : 1;   // q | k | v stages (and Kb tiles)
+  static constexpr bool GSEP = SMALL;         // G, P' in their own TMEM columns
+  static constexpr uint32_t TILE = 64 * D * 2;
+  static constexpr uint32_t STAGE = 3 * TILE;
+  static constexpr uint32_t MBOX = D * 128;   // one 64-column box of a [D][D] bf16 matrix
+  static constexpr uint32_t OFF_KB = NST * STAGE;
+  static constexpr uint32_t OFF_T = OFF_KB + NST * TILE;      // [64][64] bf16, K-major
+  static constexpr uint32_t OFF_P = OFF_T + 8192;             // [64][64] bf16, K-major
+  static constexpr uint32_t OFF_W = OFF_P + 8192;             // [64][D] bf16 (MN-major B)
+  static constexpr uint32_t OFF_U = OFF_W + TILE;             // [64][D] bf16
+  static constexpr uint32_t OFF_M = OFF_U + TILE;             // [D][D] bf16, K-major
+  static constexpr uint32_t OFF_S = OFF_M + D * D * 2;        // [D][D] bf16, MN-major
+  // O staging: its own tile at D = 64; at D = 128 it shares the W tile (W of a
+  // chunk is read before its O is stored; the next W waits for that store).
+  static constexpr uint32_t OFF_O = SMALL ? OFF_S + D * D * 2 : OFF_W;
+  static constexpr uint32_t OFF_A = SMALL ? OFF_O + TILE : OFF_S + D * D * 2;  // fp32 [64][kAS]
+  static constexpr uint32_t OFF_TF = OFF_A + 64 * kAS * 4;     // fp32 [64][kAS]
+  static constexpr uint32_t OFF_R = OFF_TF + 64 * kAS * 4;     // fp32 [3][16][17]
+  static constexpr uint32_t OFF_LAM = OFF_R + 3 * 16 * 17 * 4; // [NST][64] Lam
+  static constexpr uint32_t OFF_BETA = OFF_LAM + NST * 64 * 4; // [NST][64] beta
+  static constexpr uint32_t OFF_SCR = OFF_BETA + NST * 64 * 4; // 16 floats
+  static constexpr uint32_t OFF_BAR = OFF_SCR + 64;
+  static constexpr int NBAR = 4 * NST + 10;
+  static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
+  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static_assert(STAGE % 1024 == 0 && OFF_KB % 1024 == 0 && OFF_T % 1024 == 0 &&
+                    OFF_P % 1024 == 0 && OFF_W % 1024 == 0 && OFF_U % 1024 == 0 &&
+                    OFF_M % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
+                "swizzled tiles need 1024-byte alignment");
+  static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
+  // TMEM columns: S (D), O (D), X (W, then Kt^T W: D), Y (U0, then P W: D),
+  // and G | P' (128), which shares X's columns at D = 128.
+  static constexpr uint32_t T_S = 0, T_O = D, T_X = 2 * D, T_Y = 3 * D;
+  static constexpr uint32_t T_G = GSEP ? 4 * D : T_X;
+  static constexpr uint32_t T_COLS = 512;
+  static_assert((GSEP ? T_G + 128 : T_Y + D) <= T_COLS, "TMEM budget");
+};
+
+struct DtParams {
+  int H, L, BH, n_chunks;
+  const float *beta;       // [BH][L]
+  const float *log_alpha;  // [BH][L] or null
+  const float *S0;
+  float *S_final;
+  unsigned int *err;
+};
+
+// dst <- src * fac(row) over one [64][D] bf16 tile (same swizzled layout).
+template <int D, typename Fac>
+__device__ __forceinline__ void scaled_copy(const unsigned char *src, unsigned char *dst, Fac fac,
+                                            int t, int n) {
+  constexpr int kChunks = 64 * D * 2 / 16;
+  for (int x = t; x < kChunks; x += n) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(src + (size_t)x * 16);
+    const float f = fac((x & 511) >> 3);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = pack_bf16(__uint_as_float(w[e] << 16) * f, __uint_as_float(w[e] & 0xffff0000u) * f);
+    *reinterpret_cast<uint4 *>(dst + (size_t)x * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <int D, bool PHI, bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                DtParams p) {
+  using SM = DtSmem<D>;
+  constexpr int NST = SM::NST;
+  constexpr bool GSEP = SM::GSEP;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
+  float *bet = reinterpret_cast<float *>(smem + SM::OFF_BETA);
+  float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
+  float *As = reinterpret_cast<float *>(smem + SM::OFF_A);
+  float *Ts = reinterpret_cast<float *>(smem + SM::OFF_TF);
+  float *Rs = reinterpret_cast<float *>(smem + SM::OFF_R);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
+  uint64_t *empty = full + NST;
+  uint64_t *prep_a = empty + NST;   // [NST] phi, Lam, beta, V scaled, Kb
+  uint64_t *prep_b = prep_a + NST;  // [NST] K <- Kt in place
+  uint64_t *t_ready = prep_b + NST; // T and P tiles written
+  uint64_t *g_full = t_ready + 1;   // G, P' in TMEM
+  uint64_t *wu_full = g_full + 1;   // W, U0 in TMEM
+  uint64_t *wu_ready = wu_full + 1; // W, U0 tiles written
+  uint64_t *m_full = wu_ready + 1;  // Kt^T W, P W in TMEM; O = P U0 issued
+  uint64_t *m_ready = m_full + 1;   // M and Qe tiles written
+  uint64_t *s_ready = m_ready + 1;  // bf16 S_in copy written, TMEM S scaled
+  uint64_t *s_done = s_ready + 1;   // the chain's MMAs (and all before) done
+  uint64_t *o_free = s_done + 1;    // O read out of TMEM
+  uint64_t *drain = o_free + 1;
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int bh = blockIdx.x, nc = p.n_chunks;
+  const size_t bhL = (size_t)bh * p.L;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&prep_a[s], 1);
+      mbar_init(&prep_b[s], 1);
+    }
+    mbar_init(t_ready, 1);
+    mbar_init(g_full, 1);
+    mbar_init(wu_full, 1);
+    mbar_init(wu_ready, 1);
+    mbar_init(m_full, 1);
+    mbar_init(m_ready, 1);
+    mbar_init(s_ready, 1);
+    mbar_init(s_done, 1);
+    mbar_init(o_free, 1);
+    mbar_init(drain, 1);
+    ctl->abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == W_MMA) {
+    tmem_alloc(&ctl->tmem_base, SM::T_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == W_TMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
+      int issued = 0;
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (c >= NST && !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_DELTA_TC, 1)) break;
+        unsigned char *stg = smem + s * SM::STAGE;
+        mbar_arrive_expect_tx(&full[s], SM::STAGE);
+        for (int b = 0; b < D / BOX; ++b) {
+          tma_load_3d(stg + b * BOX_BYTES, &tmQ, &full[s], b * BOX, c * CH, bh);
+          tma_load_3d(stg + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, c * CH, bh);
+          tma_load_3d(stg + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, c * CH, bh);
+        }
+        issued = c + 1;
+      }
+      if (*(volatile uint32_t *)&ctl->abort)
+        for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+      for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nc > 0) {
+      constexpr uint32_t id_g = idesc_bf16_f32(64, 64, false, false);
+      constexpr uint32_t id_tx = idesc_bf16_f32(64, D, false, true);   // T Kb, T V, P W, P U0, Qe S
+      constexpr uint32_t id_kt = idesc_bf16_f32(D, D, true, true);     // Kt^T W, Kt^T U0
+      constexpr uint32_t id_ms = idesc_bf16_f32(D, D, false, true);    // M S
+      constexpr uint32_t HI = smem_desc_sw128_hi(1024);
+      const uint32_t sbase = smem_u32(smem);
+      const uint32_t dKM = smem_desc_sw128_lo(sbase, 16);
+      const uint32_t dMN = smem_desc_sw128_lo(sbase, BOX_BYTES);
+      const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::MBOX);
+      auto at = [](uint32_t d, uint32_t off) { return d + (off >> 4); };
+      auto w = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+        return wait1(bar, par, ctl, p.err, KID_DELTA_TC, site);
+      };
+      // G = K K^T and P' = Q K^T of chunk c.
+      auto issue_g = [&](int c) {
+        const uint32_t qo = (c % NST) * SM::STAGE, ko = qo + SM::TILE;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * BOX_BYTES + 32 * (kk % 4);
+          mma_bf16_w(tmem + SM::T_G, at(dKM, ko + off), at(dKM, ko + off), HI, id_g, kk > 0);
+          mma_bf16_w(tmem + SM::T_G + 64, at(dKM, qo + off), at(dKM, ko + off), HI, id_g, kk > 0);
+        }
+        mma_commit(g_full);
+      };
+      bool ok = w(&prep_a[0], 0, 2);
+      if (ok) {
+        tc_fence_after();
+        issue_g(0);
+      }
+      for (int c = 0; ok && c < nc; ++c) {
+        const int s = c % NST;
+        const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
+        const uint32_t kbo = SM::OFF_KB + s * SM::TILE;
+        const uint32_t to = SM::OFF_T, po = SM::OFF_P;
+        // W = T Kb, U0 = T V (X and Y are free once the previous chunk's M, Qe are out).
+        if (!(ok = w(t_ready, c & 1, 3))) break;
+        if (c >= 1 && !(ok = w(m_ready, (c - 1) & 1, 4))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk) {
+          mma_bf16_w(tmem + SM::T_X, at(dKM, to + 32 * kk), at(dMN, kbo + 2048 * kk), HI, id_tx, kk > 0);
+          mma_bf16_w(tmem + SM::T_Y, at(dKM, to + 32 * kk), at(dMN, vo + 2048 * kk), HI, id_tx, kk > 0);
+        }
+        mma_commit(wu_full);
+        if (GSEP && c + 1 < nc) {  // the next chunk's G, P' while this one goes on
+          if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
+          tc_fence_after();
+          issue_g(c + 1);
+        }
+        // Kt^T W -> X, P W -> Y, O = P U0 (O is free once the previous chunk's O is out).
+        if (!(ok = w(wu_ready, c & 1, 6))) break;
+        if (!(ok = w(&prep_b[s], (c / NST) & 1, 7))) break;
+        if (c >= 1 && !(ok = w(o_free, (c - 1) & 1, 8))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk) {
+          mma_bf16_w(tmem + SM::T_X, at(dMN, ko + 2048 * kk), at(dMN, SM::OFF_W + 2048 * kk), HI,
+                     id_kt, kk > 0);
+          mma_bf16_w(tmem + SM::T_Y, at(dKM, po + 32 * kk), at(dMN, SM::OFF_W + 2048 * kk), HI,
+                     id_tx, kk > 0);
+          mma_bf16_w(tmem + SM::T_O, at(dKM, po + 32 * kk), at(dMN, SM::OFF_U + 2048 * kk), HI,
+                     id_tx, kk > 0);
+        }
+        mma_commit(m_full);
+        // The state chain.
+        if (!(ok = w(m_ready, c & 1, 9))) break;
+        if (!(ok = w(s_ready, c & 1, 10))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)  // S += Kt^T U0
+          mma_bf16_w(tmem + SM::T_S, at(dMN, ko + 2048 * kk), at(dMN, SM::OFF_U + 2048 * kk), HI,
+                     id_kt, 1u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S += M S_in, O += Qe S_in
+          mma_bf16_w(tmem + SM::T_S, at(dKM, SM::OFF_M + (kk / 4) * SM::MBOX + 32 * (kk % 4)),
+                     at(dMS, SM::OFF_S + 2048 * kk), HI, id_ms, 1u);
+          mma_bf16_w(tmem + SM::T_O, at(dKM, qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)),
+                     at(dMS, SM::OFF_S + 2048 * kk), HI, id_tx, 1u);
+        }
+        mma_commit(s_done);
+        mma_commit(&empty[s]);
+        if (!GSEP && c + 1 < nc) {
+          if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 11))) break;
+          if (!(ok = w(m_ready, c & 1, 12))) break;
+          tc_fence_after();
+          issue_g(c + 1);
+        }
+      }
+      mma_commit(drain);
+      drain_wait(drain, 0);
+    }
+  } else if (warp >= W_PREP && warp < W_SOLVE) {
+    // ------------------------------------------------------------ PREP
+    const int t = tid - W_PREP * 32;
+    auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_DELTA_TC, site, BAR_PREP, t);
+    };
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST;
+      unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE, *vt = kt + SM::TILE;
+      unsigned char *kb = smem + SM::OFF_KB + s * SM::TILE;
+      if (!(ok = gwait(&full[s], (c / NST) & 1, 13))) break;
+      if (t < 64) {  // inclusive prefix of log alpha (warps 2, 3), beta
+        const int tok = c * CH + t;
+        float x = 0.f, b = 0.f;
+        if (tok < p.L) {
+          b = p.beta[bhL + tok];
+          if (GATED) x = p.log_alpha[bhL + tok];
+        }
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, off);
+          if (lane >= off) x += y;
+        }
+        if (t == 31) scr[0] = x;
+        lam[s * 64 + t] = x;
+        bet[s * 64 + t] = b;
+      }
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      if (t >= 32 && t < 64) lam[s * 64 + t] += scr[0];
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      const float *lm = lam + s * 64, *bt = bet + s * 64;
+      if constexpr (PHI) tile_pass<D, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
+      tile_pass<D, 1, false, true>(vt, [bt](int, int r) { return bt[r]; }, t, kPrepThreads);
+      fence_proxy_async_smem();  // phi(k) is read back below by the other threads
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      scaled_copy<D>(kt, kb, [lm, bt](int r) { return bt[r] * __expf(lm[r]); }, t, kPrepThreads);
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      if (t == 0) mbar_arrive(&prep_a[s]);
+      // Once K K^T and Q K^T have read phi(K): K <- Kt in place.
+      if (!(ok = gwait(g_full, c & 1, 14))) break;
+      const float le = lm[63];
+      tile_pass<D, 1, false, true>(kt, [lm, le](int, int r) { return __expf(le - lm[r]); }, t,
+                                   kPrepThreads);
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_PREP, kPrepThreads);
+      if (t == 0) mbar_arrive(&prep_b[s]);
+    }
+  } else if (warp >= W_SOLVE && warp < W_EPI) {
+    // ------------------------------------------------------------ SOLVE: T = (I + A)^{-1}, P
+    const int t = tid - W_SOLVE * 32;
+    const int quarter = warp & 3;
+    const int row = acc_row<64>(quarter, lane);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto swait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_wg(bar, par, ctl, p.err, KID_DELTA_TC, site, BAR_SOLVE);
+    };
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST;
+      if (!(ok = swait(&prep_a[s], (c / NST) & 1, 15))) break;
+      if (!(ok = swait(g_full, c & 1, 16))) break;
+      tc_fence_after();
+      const float *lm = lam + s * 64, *bt = bet + s * 64;
+      // A (fp32, shared) and this row's P (bf16 pairs, kept in registers until
+      // the P tile is free) from G and P'.
+      uint32_t pk[32];
+      const float lr = row >= 0 ? lm[row] : 0.f, br = row >= 0 ? bt[row] : 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t g[32], pp[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_G + 32 * h, g);
+        tmem_ld32(tmem + lane_off + SM::T_G + 64 + 32 * h, pp);
+        tmem_ld_wait();
+        if (row >= 0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = 32 * h + 2 * e;
+            const float f0 = j <= row ? __expf(lr - lm[j]) : 0.f;
+            const float f1 = j + 1 <= row ? __expf(lr - lm[j + 1]) : 0.f;
+            As[row * kAS + j] = j < row ? br * f0 * __uint_as_float(g[2 * e]) : 0.f;
+            As[row * kAS + j + 1] = j + 1 < row ? br * f1 * __uint_as_float(g[2 * e + 1]) : 0.f;
+            pk[16 * h + e] = pack_bf16(f0 * __uint_as_float(pp[2 * e]), f1 * __uint_as_float(pp[2 * e + 1]));
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(BAR_SOLVE, 128);
+      // Diagonal 16 x 16 blocks by forward substitution, one column per thread;
+      // the blocks above the diagonal are zero.
+      if (t < 64) {
+        const int I = t >> 4, col = t & 15, r0 = 16 * I;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float acc = i == col ? 1.f : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < i) acc -= As[(r0 + i) * kAS + r0 + j] * x[j];
+          x[i] = i >= col ? acc : 0.f;
+          Ts[(r0 + i) * kAS + r0 + col] = x[i];
+        }
+      } else {
+        for (int e = t - 64; e < 64 * 64; e += 64) {
+          const int i = e >> 6, j = e & 63;
+          if ((j >> 4) > (i >> 4)) Ts[i * kAS + j] = 0.f;
+        }
+      }
+      named_bar_sync(BAR_SOLVE, 128);
+      // Below the diagonal, by distance d = I - J:
+      //   R = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II R.
+      for (int d = 1; d <= 3; ++d) {
+        const int nb = 4 - d;  // blocks (I, I - d), I = d .. 3
+        for (int e = t; e < nb * 256; e += 128) {
+          const int b = e >> 8, I = d + b, J = I - d, i = (e >> 4) & 15, j = e & 15;
+          float acc = 0.f;
+          for (int m = 16 * J; m < 16 * I; ++m) acc += As[(16 * I + i) * kAS + m] * Ts[m * kAS + 16 * J + j];
+          Rs[b * 272 + i * 17 + j] = acc;
+        }
+        named_bar_sync(BAR_SOLVE, 128);
+        for (int e = t; e < nb * 256; e += 128) {
+          const int b = e >> 8, I = d + b, J = I - d, i = (e >> 4) & 15, j = e & 15;
+          float acc = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m)
+            if (m <= i) acc -= Ts[(16 * I + i) * kAS + 16 * I + m] * Rs[b * 272 + m * 17 + j];
+          Ts[(16 * I + i) * kAS + 16 * J + j] = acc;
+        }
+        named_bar_sync(BAR_SOLVE, 128);
+      }
+      // The T and P tiles were last read by the previous chunk's MMAs.
+      if (c >= 1 && !(ok = swait(m_full, (c - 1) & 1, 17))) break;
+      if (row >= 0) {
+        unsigned char *pt = smem + SM::OFF_P;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8)
+          *reinterpret_cast<uint4 *>(pt + row * 128 + ((q8 ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
+      }
+      {  // T -> bf16, K-major rows (row r holds T[r, 0..63]); two threads per row
+        unsigned char *tt = smem + SM::OFF_T;
+        const int r = t >> 1, h = t & 1;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const int j0 = 32 * h + 8 * q8;
+          uint32_t w4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w4[e] = pack_bf16(Ts[r * kAS + j0 + 2 * e], Ts[r * kAS + j0 + 2 * e + 1]);
+          const int ch = 4 * h + q8;
+          *reinterpret_cast<uint4 *>(tt + r * 128 + ((ch ^ (r & 7)) << 4)) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_SOLVE, 128);
+      if (t == 0) mbar_arrive(t_ready);
+    }
+  } else if (warp >= W_EPI && warp < W_ST) {
+    // ------------------------------------------------------------ EPI
+    const int t = tid - W_EPI * 32;
+    const int quarter = warp & 3;
+    const int row = acc_row<64>(quarter, lane);     // token row of an M = 64 product
+    const int mrow = acc_row<D>(quarter, lane);     // row of an M = D product
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto ewait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_wg(bar, par, ctl, p.err, KID_DELTA_TC, site, BAR_EPI);
+    };
+    // 32 fp32 columns of TMEM row -> 16 bf16 pairs * sc into a swizzled tile.
+    auto put32 = [&](unsigned char *base, uint32_t blk, int r, int col, const uint32_t (&v)[32],
+                     float sc) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          pk[j] = pack_bf16(__uint_as_float(v[16 * h + 2 * j]) * sc,
+                            __uint_as_float(v[16 * h + 2 * j + 1]) * sc);
+        st_row16(base, blk, r, col + 16 * h, pk);
+      }
+    };
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST;
+      // W, U0 -> bf16 tiles (U0's tile was last read by the previous chain).
+      if (!(ok = ewait(wu_full, c & 1, 18))) break;
+      if (c >= 1 && !(ok = ewait(s_done, (c - 1) & 1, 19))) break;
+      if (!SM::SMALL && t == 0) tma_store_wait_read<0>();  // O staging shares the W tile
+      __syncwarp();
+      named_bar_sync(BAR_EPI, 128);
+      tc_fence_after();
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32], u[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_X + col, r);
+        tmem_ld32(tmem + lane_off + SM::T_Y + col, u);
+        tmem_ld_wait();
+        if (row >= 0) {
+          put32(smem + SM::OFF_W, BOX_BYTES, row, col, r, 1.f);
+          put32(smem + SM::OFF_U, BOX_BYTES, row, col, u, 1.f);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_EPI, 128);
+      if (t == 0) mbar_arrive(wu_ready);
+      // M = -Kt^T W -> bf16 (K-major rows), Qe = e^{Lam} Q - P W in place of Q.
+      if (!(ok = ewait(m_full, c & 1, 20))) break;
+      tc_fence_after();
+      const float *lm = lam + s * 64;
+      unsigned char *qt = smem + s * SM::STAGE;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32], u[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_X + col, r);
+        tmem_ld32(tmem + lane_off + SM::T_Y + col, u);
+        tmem_ld_wait();
+        if (mrow >= 0) put32(smem + SM::OFF_M, SM::MBOX, mrow, col, r, -1.f);
+        if (row >= 0) {
+          const float el = __expf(lm[row]);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int cc = col + 2 * j;
+            const uint32_t qw = *reinterpret_cast<const uint32_t *>(
+                qt + (cc >> 6) * BOX_BYTES + sw128_offset(row, cc & 63));
+            pk[j] = pack_bf16(__uint_as_float(qw << 16) * el - __uint_as_float(u[2 * j]),
+                              __uint_as_float(qw & 0xffff0000u) * el - __uint_as_float(u[2 * j + 1]));
+          }
+          st_row16(qt, BOX_BYTES, row, col, pk);
+          st_row16(qt, BOX_BYTES, row, col + 16, pk + 8);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_EPI, 128);
+      if (t == 0) mbar_arrive(m_ready);
+      // O -> bf16 -> TMA store.
+      if (!(ok = ewait(s_done, c & 1, 21))) break;
+      tc_fence_after();
+      if (SM::SMALL && t == 0) tma_store_wait_read<0>();
+      __syncwarp();
+      named_bar_sync(BAR_EPI, 128);
+      unsigned char *o_sm = smem + SM::OFF_O;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_O + col, r);
+        tmem_ld_wait();
+        if (row >= 0) put32(o_sm, BOX_BYTES, row, col, r, 1.f);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_EPI, 128);
+      if (t == 0) {
+        mbar_arrive(o_free);
+        for (int bb = 0; bb < D / BOX; ++bb)
+          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, c * CH, bh);
+        tma_store_commit();
+      }
+    }
+    if (t == 0) tma_store_wait_all();
+  } else if (warp >= W_ST) {
+    // ------------------------------------------------------------ ST: the state chain
+    const int t = tid - W_ST * 32;
+    const int quarter = warp & 3;
+    const int srow = acc_row<D>(quarter, lane);
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    auto swait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
+      return wait_wg(bar, par, ctl, p.err, KID_DELTA_TC, site, BAR_ST);
+    };
+#pragma unroll 1
+    for (int col = 0; col < D; col += 32) {  // S0 (or zeros) into TMEM
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+      if (srow >= 0 && p.S0) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((size_t)bh * D + srow) * D + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 f = src[j];
+          r[4 * j] = __float_as_uint(f.x);
+          r[4 * j + 1] = __float_as_uint(f.y);
+          r[4 * j + 2] = __float_as_uint(f.z);
+          r[4 * j + 3] = __float_as_uint(f.w);
+        }
+      }
+      __syncwarp();
+      tmem_st32(tmem + lane_off + SM::T_S + col, r);
+    }
+    tmem_st_wait();
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST;
+      if (!(ok = swait(&prep_a[s], (c / NST) & 1, 22))) break;
+      if (c >= 1 && !(ok = swait(s_done, (c - 1) & 1, 23))) break;
+      tc_fence_after();
+      const float e = GATED ? __expf(lam[s * 64 + 63]) : 1.f;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_S + col, r);
+        tmem_ld_wait();
+        if (srow >= 0) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              pk[j] = pack_bf16(__uint_as_float(r[16 * h + 2 * j]), __uint_as_float(r[16 * h + 2 * j + 1]));
+            st_row16(smem + SM::OFF_S, SM::MBOX, srow, col + 16 * h, pk);
+          }
+        }
+        if (GATED) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * e);
+          __syncwarp();
+          tmem_st32(tmem + lane_off + SM::T_S + col, r);
+        }
+      }
+      if (GATED) tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(BAR_ST, 128);
+      if (t == 0) mbar_arrive(s_ready);
+    }
+    if (ok && nc > 0 && swait(s_done, (nc - 1) & 1, 24) && p.S_final) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_off + SM::T_S + col, r);
+        tmem_ld_wait();
+        if (srow >= 0) {
+          float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D + col);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == W_MMA) {
+    __syncwarp();
+    tmem_dealloc(tmem, SM::T_COLS);
+  }
+}
+
+template <int D, bool PHI, bool GATED>
+cudaError_t launch_dt(const VariantArgs &a) {
+  using SM = DtSmem<D>;
+  const int BH = a.B * a.H;
+  DtParams p{};
+  p.H = a.H;
+  p.L = a.L;
+  p.BH = BH;
+  p.n_chunks = (a.L + CH - 1) / CH;
+  p.beta = a.beta;
+  p.log_alpha = a.decay;
+  p.S0 = a.S0;
+  p.S_final = a.S_final;
+  p.err = device_error_word();
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tmap_bf16_3d(&tq, a.q, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tk, a.k, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&tv, a.v, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX))
+    return cudaErrorInvalidValue;
+  auto kern = delta_tc_kernel<D, PHI, GATED>;
+  static int smem_set[64];
+  cudaError_t e = set_smem_once(kern, SM::BYTES, smem_set);
+  if (e != cudaSuccess) return e;
+  kern<<<BH, kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// The rule as the pages state it: phi = identity on keys the caller has
+// normalised.  Under elu + 1 the keys are long (|phi(k)|^2 ~ 1.3 d_k) and O
+// cancels heavily; bf16 operands then miss the 2e-2 row tolerance by up to 3x
+// (a CPU emulation of this pipeline), so that case keeps the fp32 CUDA-core
+// kernel.
+bool delta_tc_supported(const VariantArgs &a) {
+  return a.form == VARIANT_DELTA && a.dtype == LA_BF16 && a.phi == LA_PHI_IDENTITY &&
+         a.dk == a.dv && (a.dk == 64 || a.dk == 128);
+}
+
+cudaError_t launch_delta_tc(const VariantArgs &a) {
+  const bool gated = a.decay != nullptr;
+  if (a.dk == 128) return gated ? launch_dt<128, false, true>(a) : launch_dt<128, false, false>(a);
+  return gated ? launch_dt<64, false, true>(a) : launch_dt<64, false, false>(a);
+}
+
+}  // namespace la

@@ -83,6 +83,12 @@ cudaError_t launch_variant(const VariantArgs &a);
 bool channel_gate_tc_supported(const VariantArgs &a);
 cudaError_t launch_channel_gate_tc(const VariantArgs &a);
 
+// The delta rule a chunk of 64 tokens at a time on the tensor cores (the WY
+// form): bf16, d_k == d_v in {64, 128}; launch_variant takes this path when it
+// applies.
+bool delta_tc_supported(const VariantArgs &a);
+cudaError_t launch_delta_tc(const VariantArgs &a);
+
 // Denominator of the normalised form and the division of O by it, after the
 // numerator has been written to O (d_k <= 128).
 struct NormaliserArgs {

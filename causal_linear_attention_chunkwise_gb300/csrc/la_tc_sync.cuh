@@ -158,6 +158,52 @@ __device__ __forceinline__ void st_row16(unsigned char *base, uint32_t blk, int 
       make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
+// Elementwise pass over NT consecutive bf16 tiles of 64 rows x D columns (D/64
+// swizzled 8 KB boxes per tile, 8 sixteen-byte chunks per 128-byte row):
+// x <- phi(x) * fac(k, row) in tile k.  Threads t = 0..n-1 take chunks t,
+// t + n, ...; four loads are issued before any use.
+template <int D, int NT, bool PHI, bool SCALE, typename Fac>
+__device__ __forceinline__ void tile_pass(unsigned char *tile, Fac fac, int t, int n) {
+  constexpr int kTileChunks = 64 * D * 2 / 16;
+  constexpr int kChunks = NT * kTileChunks;
+#pragma unroll 1
+  for (int base = 0; base < kChunks; base += 4 * n) {
+    uint4 u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = base + j * n + t;
+      if (x < kChunks) u[j] = *reinterpret_cast<const uint4 *>(tile + (size_t)x * 16);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = base + j * n + t;
+      if (x >= kChunks) continue;
+      float sc = 1.f;
+      if (SCALE) sc = fac(NT == 1 || x < kTileChunks ? 0 : 1, (x & 511) >> 3);
+      uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (PHI && !SCALE) {  // phi alone: packed bf16 arithmetic
+          w[e] = elu1_bf16x2(w[e]);
+          continue;
+        }
+        float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+        if (PHI) {
+          lo = elu1_fast(lo);
+          hi = elu1_fast(hi);
+        }
+        w[e] = pack_bf16(lo * sc, hi * sc);
+      }
+      u[j] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int x = base + j * n + t;
+      if (x < kChunks) *reinterpret_cast<uint4 *>(tile + (size_t)x * 16) = u[j];
+    }
+  }
+}
+
 // ---------------------------------------------------------------- host helpers
 inline int sm_count() {
   int dev = 0, n = 0;

@@ -344,6 +344,7 @@ cudaError_t launch_variant(const VariantArgs &a) {
       if (channel_gate_tc_supported(a)) return launch_channel_gate_tc(a);
       return f32 ? launch_channel_gate_t<float>(a) : launch_channel_gate_t<__nv_bfloat16>(a);
     case VARIANT_DELTA:
+      if (delta_tc_supported(a)) return launch_delta_tc(a);
       return f32 ? launch_delta_t<float>(a) : launch_delta_t<__nv_bfloat16>(a);
     default: return cudaErrorInvalidValue;
   }

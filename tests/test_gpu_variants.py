@@ -90,6 +90,61 @@ def test_delta_matches_oracle(case):
     parity.check(S.cpu(), S_ref, dtype, "S")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("phi", ["identity", "elu1"])
+@pytest.mark.parametrize("gated", [True, False])
+@pytest.mark.parametrize("L", [65, 300, 1000])
+def test_delta_tensor_core_path(d, phi, gated, L):
+    """bf16, d_k = d_v in {64, 128}: with identity phi, the chunkwise (WY)
+    tcgen05 kernel; with elu + 1 (long keys, beta shrunk to keep the erase a
+    contraction) the fp32 CUDA-core kernel.  One chunk and a token, ragged
+    tails and a longer run, from a non-zero S0, with and without the gate."""
+    beta_max = 1.0 if phi == "identity" else 1.0 / d
+    inp = W.make_variant_inputs("delta", 2, 2, L, d, d, "bf16", seed=30 + L, with_state=True,
+                                gated=gated, beta_max=beta_max)
+    api.la_set_feature_map(phi)
+    O, S = api.la_delta_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["beta"]),
+                            _d(inp["log_alpha"]), _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.delta(inp["q"], inp["k"], inp["v"], inp["beta"], inp["log_alpha"],
+                                phi=phi, S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, "bf16", "O")
+    parity.check(S.cpu(), S_ref, "bf16", "S")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_delta_tensor_core_recalls_the_key_just_written(d):
+    """beta = 1, unit keys, no gate, on the tensor-core path: every read with
+    the key just written returns its value (up to bf16), however much of the
+    chunk's solve cancels."""
+    B, H, L = 2, 2, 200
+    inp = W.make_variant_inputs("delta", B, H, L, d, d, "bf16", seed=41, with_state=True,
+                                gated=False)
+    beta = torch.ones(B, H, L)
+    api.la_set_feature_map("identity")
+    O, _ = api.la_delta_fwd(_d(inp["k"]), _d(inp["k"]), _d(inp["v"]), _d(beta), None,
+                            _d(inp["S0"]))
+    api.la_device_status()
+    parity.check(O.cpu(), inp["v"].double(), "bf16", "recall")
+
+
+def test_delta_full_workload_shape_on_sampled_sequences():
+    """The benchmarked shape (B4 H16 L4096 d64, bf16, identity, gated, S0,
+    beta ~ U(0, 1)) in one call; three sequences recomputed by the oracle."""
+    B, H, L, d = 4, 16, 4096, 64
+    inp = W.make_variant_inputs("delta", B, H, L, d, d, "bf16", seed=0, with_state=True)
+    api.la_set_feature_map("identity")
+    O, S = api.la_delta_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(inp["beta"]),
+                            _d(inp["log_alpha"]), _d(inp["S0"]))
+    api.la_device_status()
+    for b, h in [(0, 0), (2, 9), (3, 15)]:
+        sl = lambda x: x[b:b + 1, h:h + 1]  # noqa: E731
+        O_ref, S_ref = oracle.delta(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]), sl(inp["beta"]),
+                                    sl(inp["log_alpha"]), phi="identity", S0=sl(inp["S0"]))
+        parity.check(sl(O).cpu(), O_ref, "bf16", f"O[{b},{h}]")
+        parity.check(sl(S).cpu(), S_ref, "bf16", f"S[{b},{h}]")
+
+
 @pytest.mark.parametrize("L,d,dtype", [(2, 16, "f32"), (31, 128, "bf16"), (32, 64, "f32"),
                                        (33, 32, "f32"), (64, 128, "f32"), (65, 64, "bf16")])
 def test_delta_short_sequences(L, d, dtype):
