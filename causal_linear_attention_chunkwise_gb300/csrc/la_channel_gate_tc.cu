@@ -45,6 +45,17 @@
 #include "la_tc_sync.cuh"
 #include "la_tma_host.h"
 
+#ifdef LA_TRACE
+namespace la {
+namespace {
+__device__ long long g_trace[kTraceEvents][kTraceChunks];
+}
+}  // namespace la
+extern "C" int la_trace_read_cg(long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, la::g_trace, sizeof(la::g_trace));
+}
+#endif
+
 namespace la {
 namespace {
 using namespace tc;
@@ -200,6 +211,10 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   const int bh = blockIdx.x;
   const int nc = p.n_chunks;
   const size_t bhL = (size_t)bh * p.L;
+  const bool trace_on = blockIdx.x == 0;
+  const long long t0 = clock64();
+  (void)trace_on;
+  (void)t0;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -251,6 +266,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           tma_load_3d(stg + 2 * SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
         }
         issued = c + 1;
+        LA_TRACE_EVENT(trace_on, t0, 0, c);
       }
       if (*(volatile uint32_t *)&ctl->abort)
         for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
@@ -300,6 +316,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (kp < nc && kp <= km + 1 && mbar_test(&prep[kp % NST], (kp / NST) & 1)) {
           tc_fence_after();
           issue_p(kp);
+          LA_TRACE_EVENT(trace_on, t0, 3, kp);
           ++kp;
           did = true;
         }
@@ -320,6 +337,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        id_kv, 1u);
           mma_commit(s_done);
           mma_commit(&xfree[xb]);
+          LA_TRACE_EVENT(trace_on, t0, 4, kc);
           ++kc;
           did = true;
         }
@@ -333,6 +351,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             mma_bf16_w(o_t, at(dMN, po + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_pv, 1u);
           mma_commit(&o_full[km & 1]);
           mma_commit(&empty[s]);
+          LA_TRACE_EVENT(trace_on, t0, 5, km);
           ++km;
           did = true;
         }
@@ -381,6 +400,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         tot[I * D + ch] = sum;
       }
       if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);
       if (t == 0) flag[s] = 0;
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (c >= NX && !(ok = gwait(&xfree[xb], ((c / NX) - 1) & 1, 8))) break;
@@ -435,6 +455,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&prep[s]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
     }
   } else if (warp >= W_EPI && warp < W_ST) {
     // ------------------------------------------------------------ EPI: P and O epilogues
@@ -483,6 +504,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       tc_fence_before();
       named_bar_sync(BAR_EPI, 128);
       if (t == 0) mbar_arrive(&p_ready[c % NP]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 6, c);
       return true;
     };
     auto o_epilogue = [&](int c) -> bool {
@@ -516,6 +538,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(BAR_EPI, 128);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 7, c);
       if (t == 0) {
         mbar_arrive(&o_free[b]);
         for (int bb = 0; bb < D / BOX; ++bb)
@@ -594,6 +617,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       tc_fence_before();
       named_bar_sync(BAR_ST, 128);
       if (t == 0) mbar_arrive(s_ready);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 8, c);
     }
     if (ok && nc > 0 && swait(s_done, (nc - 1) & 1, 15) && p.S_final) {
       tc_fence_after();

@@ -47,15 +47,27 @@
 #include "la_tc_sync.cuh"
 #include "la_tma_host.h"
 
+#ifdef LA_TRACE
+namespace la {
+namespace {
+__device__ long long g_trace[kTraceEvents][kTraceChunks];
+}
+}  // namespace la
+extern "C" int la_trace_read_delta(long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, la::g_trace, sizeof(la::g_trace));
+}
+#endif
+
 namespace la {
 namespace {
 using namespace tc;
 
-// Warp roles: 0 TMA, 1 MMA, 2..7 PREP (192 threads), 8..11 SOLVE, 12..15 EPI,
-// 16..19 ST.  The TMEM warpgroups start at a multiple of four warps.
+// Warp roles: 0 TMA, 1 MMA, 2..3 PREP (64 threads), 4..11 SOLVE (256 threads),
+// 12..15 EPI, 16..19 ST.  The TMEM warpgroups start at a multiple of four warps.
 constexpr int kThreads = 640;
-constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_SOLVE = 8, W_EPI = 12, W_ST = 16;
+constexpr int W_TMA = 0, W_MMA = 1, W_PREP = 2, W_SOLVE = 4, W_EPI = 12, W_ST = 16;
 constexpr int kPrepThreads = (W_SOLVE - W_PREP) * 32;
+constexpr int kSolveThreads = (W_EPI - W_SOLVE) * 32;
 constexpr uint32_t BAR_PREP = 1, BAR_SOLVE = 2, BAR_EPI = 3, BAR_ST = 4;
 constexpr int kAS = 65;  // fp32 row stride of the solve's A and T (conflict-free columns)
 
@@ -160,6 +172,10 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x, nc = p.n_chunks;
   const size_t bhL = (size_t)bh * p.L;
+  const bool trace_on = blockIdx.x == 0;
+  const long long t0 = clock64();
+  (void)trace_on;
+  (void)t0;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -240,6 +256,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           mma_bf16_w(tmem + SM::T_G + 64, at(dKM, qo + off), at(dKM, ko + off), HI, id_g, kk > 0);
         }
         mma_commit(g_full);
+        LA_TRACE_EVENT(trace_on, t0, 1, c);
       };
       bool ok = w(&prep_a[0], 0, 2);
       if (ok) {
@@ -261,6 +278,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           mma_bf16_w(tmem + SM::T_Y, at(dKM, to + 32 * kk), at(dMN, vo + 2048 * kk), HI, id_tx, kk > 0);
         }
         mma_commit(wu_full);
+        LA_TRACE_EVENT(trace_on, t0, 5, c);
         if (GSEP && c + 1 < nc) {  // the next chunk's G, P' while this one goes on
           if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
           tc_fence_after();
@@ -281,6 +299,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
                      id_tx, kk > 0);
         }
         mma_commit(m_full);
+        LA_TRACE_EVENT(trace_on, t0, 7, c);
         // The state chain.
         if (!(ok = w(m_ready, c & 1, 9))) break;
         if (!(ok = w(s_ready, c & 1, 10))) break;
@@ -298,6 +317,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mma_commit(s_done);
         mma_commit(&empty[s]);
+        LA_TRACE_EVENT(trace_on, t0, 9, c);
         if (!GSEP && c + 1 < nc) {
           if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 11))) break;
           if (!(ok = w(m_ready, c & 1, 12))) break;
@@ -341,6 +361,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       named_bar_sync(BAR_PREP, kPrepThreads);
       const float *lm = lam + s * 64, *bt = bet + s * 64;
       if constexpr (PHI) tile_pass<D, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
+      if (!PHI) (void)qt;
       tile_pass<D, 1, false, true>(vt, [bt](int, int r) { return bt[r]; }, t, kPrepThreads);
       fence_proxy_async_smem();  // phi(k) is read back below by the other threads
       named_bar_sync(BAR_PREP, kPrepThreads);
@@ -348,6 +369,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&prep_a[s]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 0, c);
       // Once K K^T and Q K^T have read phi(K): K <- Kt in place.
       if (!(ok = gwait(g_full, c & 1, 14))) break;
       const float le = lm[63];
@@ -356,33 +378,37 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&prep_b[s]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 12, c);
     }
   } else if (warp >= W_SOLVE && warp < W_EPI) {
     // ------------------------------------------------------------ SOLVE: T = (I + A)^{-1}, P
+    // Warps 4..7 build A from G, warps 8..11 build P from P' (each warpgroup
+    // reaches every TMEM lane quarter); all 256 threads then invert I + A.
     const int t = tid - W_SOLVE * 32;
     const int quarter = warp & 3;
+    const bool p_side = warp >= W_SOLVE + 4;
     const int row = acc_row<64>(quarter, lane);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     auto swait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
-      return wait_wg(bar, par, ctl, p.err, KID_DELTA_TC, site, BAR_SOLVE);
+      return wait_grp<kSolveThreads>(bar, par, ctl, p.err, KID_DELTA_TC, site, BAR_SOLVE, t);
     };
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST;
       if (!(ok = swait(&prep_a[s], (c / NST) & 1, 15))) break;
       if (!(ok = swait(g_full, c & 1, 16))) break;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
       tc_fence_after();
       const float *lm = lam + s * 64, *bt = bet + s * 64;
-      // A (fp32, shared) and this row's P (bf16 pairs, kept in registers until
-      // the P tile is free) from G and P'.
+      // A (fp32, shared) from G, or this row's P (bf16 pairs, kept in
+      // registers until the P tile is free) from P'.
       uint32_t pk[32];
       const float lr = row >= 0 ? lm[row] : 0.f, br = row >= 0 ? bt[row] : 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t g[32], pp[32];
+        uint32_t g[32];
         __syncwarp();
-        tmem_ld32(tmem + lane_off + SM::T_G + 32 * h, g);
-        tmem_ld32(tmem + lane_off + SM::T_G + 64 + 32 * h, pp);
+        tmem_ld32(tmem + lane_off + SM::T_G + (p_side ? 64 : 0) + 32 * h, g);
         tmem_ld_wait();
         if (row >= 0) {
 #pragma unroll
@@ -390,16 +416,19 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
             const int j = 32 * h + 2 * e;
             const float f0 = j <= row ? __expf(lr - lm[j]) : 0.f;
             const float f1 = j + 1 <= row ? __expf(lr - lm[j + 1]) : 0.f;
-            As[row * kAS + j] = j < row ? br * f0 * __uint_as_float(g[2 * e]) : 0.f;
-            As[row * kAS + j + 1] = j + 1 < row ? br * f1 * __uint_as_float(g[2 * e + 1]) : 0.f;
-            pk[16 * h + e] = pack_bf16(f0 * __uint_as_float(pp[2 * e]), f1 * __uint_as_float(pp[2 * e + 1]));
+            if (p_side) {
+              pk[16 * h + e] = pack_bf16(f0 * __uint_as_float(g[2 * e]), f1 * __uint_as_float(g[2 * e + 1]));
+            } else {
+              As[row * kAS + j] = j < row ? br * f0 * __uint_as_float(g[2 * e]) : 0.f;
+              As[row * kAS + j + 1] = j + 1 < row ? br * f1 * __uint_as_float(g[2 * e + 1]) : 0.f;
+            }
           }
         }
       }
       tc_fence_before();
-      named_bar_sync(BAR_SOLVE, 128);
-      // Diagonal 16 x 16 blocks by forward substitution, one column per thread;
-      // the blocks above the diagonal are zero.
+      named_bar_sync(BAR_SOLVE, kSolveThreads);
+      // Diagonal 16 x 16 blocks by forward substitution, one column per thread
+      // (zero above the diagonal).
       if (t < 64) {
         const int I = t >> 4, col = t & 15, r0 = 16 * I;
         float x[16];
@@ -412,61 +441,74 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           x[i] = i >= col ? acc : 0.f;
           Ts[(r0 + i) * kAS + r0 + col] = x[i];
         }
-      } else {
-        for (int e = t - 64; e < 64 * 64; e += 64) {
-          const int i = e >> 6, j = e & 63;
-          if ((j >> 4) > (i >> 4)) Ts[i * kAS + j] = 0.f;
-        }
       }
-      named_bar_sync(BAR_SOLVE, 128);
+      named_bar_sync(BAR_SOLVE, kSolveThreads);
       // Below the diagonal, by distance d = I - J:
       //   R = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II R.
+      // 64 threads per block; each takes four rows of one column.
+#pragma unroll 1
       for (int d = 1; d <= 3; ++d) {
-        const int nb = 4 - d;  // blocks (I, I - d), I = d .. 3
-        for (int e = t; e < nb * 256; e += 128) {
-          const int b = e >> 8, I = d + b, J = I - d, i = (e >> 4) & 15, j = e & 15;
-          float acc = 0.f;
-          for (int m = 16 * J; m < 16 * I; ++m) acc += As[(16 * I + i) * kAS + m] * Ts[m * kAS + 16 * J + j];
-          Rs[b * 272 + i * 17 + j] = acc;
-        }
-        named_bar_sync(BAR_SOLVE, 128);
-        for (int e = t; e < nb * 256; e += 128) {
-          const int b = e >> 8, I = d + b, J = I - d, i = (e >> 4) & 15, j = e & 15;
-          float acc = 0.f;
+        const int b = t >> 6, tt = t & 63, ri = tt >> 4, j = tt & 15;
+        const bool act = b < 4 - d;
+        const int I = d + b, J = I - d, i0 = 16 * I + 4 * ri;
+        if (act) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int K = J; K < I; ++K) {
 #pragma unroll
-          for (int m = 0; m < 16; ++m)
-            if (m <= i) acc -= Ts[(16 * I + i) * kAS + 16 * I + m] * Rs[b * 272 + m * 17 + j];
-          Ts[(16 * I + i) * kAS + 16 * J + j] = acc;
+            for (int m = 0; m < 16; ++m) {
+              const float tv = Ts[(16 * K + m) * kAS + 16 * J + j];
+#pragma unroll
+              for (int r = 0; r < 4; ++r) acc[r] += As[(i0 + r) * kAS + 16 * K + m] * tv;
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) Rs[b * 272 + (4 * ri + r) * 17 + j] = acc[r];
         }
-        named_bar_sync(BAR_SOLVE, 128);
+        named_bar_sync(BAR_SOLVE, kSolveThreads);
+        if (act) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const float rv = Rs[b * 272 + m * 17 + j];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              if (m <= 4 * ri + r) acc[r] -= Ts[(i0 + r) * kAS + 16 * I + m] * rv;
+          }
+#pragma unroll
+          for (int r = 0; r < 4; ++r) Ts[(i0 + r) * kAS + 16 * J + j] = acc[r];
+        }
+        named_bar_sync(BAR_SOLVE, kSolveThreads);
       }
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 3, c);
       // The T and P tiles were last read by the previous chunk's MMAs.
       if (c >= 1 && !(ok = swait(m_full, (c - 1) & 1, 17))) break;
-      if (row >= 0) {
+      if (p_side && row >= 0) {
         unsigned char *pt = smem + SM::OFF_P;
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8)
           *reinterpret_cast<uint4 *>(pt + row * 128 + ((q8 ^ (row & 7)) << 4)) =
               make_uint4(pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
       }
-      {  // T -> bf16, K-major rows (row r holds T[r, 0..63]); two threads per row
+      {  // T -> bf16, K-major rows; 16-byte chunk x2 per thread; zero above the block diagonal
         unsigned char *tt = smem + SM::OFF_T;
-        const int r = t >> 1, h = t & 1;
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          const int j0 = 32 * h + 8 * q8;
-          uint32_t w4[4];
+        for (int u = 0; u < 2; ++u) {
+          const int x = t + kSolveThreads * u, r = x >> 3, ch = x & 7, j0 = 8 * ch;
+          uint32_t w4[4] = {0u, 0u, 0u, 0u};
+          if ((j0 >> 4) <= (r >> 4)) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w4[e] = pack_bf16(Ts[r * kAS + j0 + 2 * e], Ts[r * kAS + j0 + 2 * e + 1]);
-          const int ch = 4 * h + q8;
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack_bf16(Ts[r * kAS + j0 + 2 * e], Ts[r * kAS + j0 + 2 * e + 1]);
+          }
           *reinterpret_cast<uint4 *>(tt + r * 128 + ((ch ^ (r & 7)) << 4)) =
               make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(BAR_SOLVE, 128);
+      named_bar_sync(BAR_SOLVE, kSolveThreads);
       if (t == 0) mbar_arrive(t_ready);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 4, c);
     }
   } else if (warp >= W_EPI && warp < W_ST) {
     // ------------------------------------------------------------ EPI
@@ -517,6 +559,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       named_bar_sync(BAR_EPI, 128);
       if (t == 0) mbar_arrive(wu_ready);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 6, c);
       // M = -Kt^T W -> bf16 (K-major rows), Qe = e^{Lam} Q - P W in place of Q.
       if (!(ok = ewait(m_full, c & 1, 20))) break;
       tc_fence_after();
@@ -549,6 +592,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       named_bar_sync(BAR_EPI, 128);
       if (t == 0) mbar_arrive(m_ready);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 8, c);
       // O -> bf16 -> TMA store.
       if (!(ok = ewait(s_done, c & 1, 21))) break;
       tc_fence_after();
@@ -567,6 +611,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(BAR_EPI, 128);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 11, c);
       if (t == 0) {
         mbar_arrive(o_free);
         for (int bb = 0; bb < D / BOX; ++bb)
@@ -639,6 +684,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_before();
       named_bar_sync(BAR_ST, 128);
       if (t == 0) mbar_arrive(s_ready);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 10, c);
     }
     if (ok && nc > 0 && swait(s_done, (nc - 1) & 1, 24) && p.S_final) {
       tc_fence_after();
