@@ -91,7 +91,8 @@ struct DtSmem {
   static constexpr uint32_t OFF_O = SMALL ? OFF_S + D * D * 2 : OFF_W;
   static constexpr uint32_t OFF_A = SMALL ? OFF_O + TILE : OFF_S + D * D * 2;  // fp32 [64][kAS]
   static constexpr uint32_t OFF_TF = OFF_A + 64 * kAS * 4;     // fp32 [64][kAS]
-  static constexpr uint32_t OFF_R = OFF_TF + 64 * kAS * 4;     // fp32 [3][16][17]
+  static constexpr uint32_t OFF_PS = OFF_TF + 64 * kAS * 4;    // [64][64] bf16 P staging
+  static constexpr uint32_t OFF_R = OFF_PS + 8192;             // fp32 [3][16][17]
   static constexpr uint32_t OFF_LAM = OFF_R + 3 * 16 * 17 * 4; // [NST][64] Lam
   static constexpr uint32_t OFF_BETA = OFF_LAM + NST * 64 * 4; // [NST][64] beta
   static constexpr uint32_t OFF_SCR = OFF_BETA + NST * 64 * 4; // 16 floats
@@ -378,7 +379,6 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (t == 0) mbar_arrive(&prep_b[s]);
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 12, c);
     }
   } else if (warp >= W_SOLVE && warp < W_EPI) {
     // ------------------------------------------------------------ SOLVE: T = (I + A)^{-1}, P
@@ -400,52 +400,70 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
       tc_fence_after();
       const float *lm = lam + s * 64, *bt = bet + s * 64;
-      // A (fp32, shared) from G, or this row's P (bf16 pairs, kept in
-      // registers until the P tile is free) from P'.
-      uint32_t pk[32];
+      // A (fp32) from G, or P (bf16) from P' into a staging tile (the P tile
+      // itself may still be read by the previous chunk's MMAs); 16 columns
+      // per TMEM load keeps few values live.
+      unsigned char *ps = smem + SM::OFF_PS;
       const float lr = row >= 0 ? lm[row] : 0.f, br = row >= 0 ? bt[row] : 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t g[32];
+#pragma unroll 1
+      for (int j0 = 0; j0 < 64; j0 += 16) {
+        uint32_t g[16];
         __syncwarp();
-        tmem_ld32(tmem + lane_off + SM::T_G + (p_side ? 64 : 0) + 32 * h, g);
+        tmem_ld16(tmem + lane_off + SM::T_G + (p_side ? 64 : 0) + j0, g);
         tmem_ld_wait();
+        LA_TRACE_EVENT(trace_on && t == 0 && j0 < 32, t0, 11 + (j0 >> 4), c);
         if (row >= 0) {
+          float f[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = 32 * h + 2 * e;
-            const float f0 = j <= row ? __expf(lr - lm[j]) : 0.f;
-            const float f1 = j + 1 <= row ? __expf(lr - lm[j + 1]) : 0.f;
-            if (p_side) {
-              pk[16 * h + e] = pack_bf16(f0 * __uint_as_float(g[2 * e]), f1 * __uint_as_float(g[2 * e + 1]));
-            } else {
-              As[row * kAS + j] = j < row ? br * f0 * __uint_as_float(g[2 * e]) : 0.f;
-              As[row * kAS + j + 1] = j + 1 < row ? br * f1 * __uint_as_float(g[2 * e + 1]) : 0.f;
-            }
+          for (int e = 0; e < 16; ++e) f[e] = j0 + e <= row ? __expf(lr - lm[j0 + e]) : 0.f;
+          if (p_side) {
+            uint32_t w8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              w8[e] = pack_bf16(f[2 * e] * __uint_as_float(g[2 * e]), f[2 * e + 1] * __uint_as_float(g[2 * e + 1]));
+            const int ch = j0 >> 3;
+            *reinterpret_cast<uint4 *>(ps + row * 128 + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(w8[0], w8[1], w8[2], w8[3]);
+            *reinterpret_cast<uint4 *>(ps + row * 128 + (((ch + 1) ^ (row & 7)) << 4)) =
+                make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              As[row * kAS + j0 + e] = j0 + e < row ? br * f[e] * __uint_as_float(g[e]) : 0.f;
           }
         }
       }
       tc_fence_before();
       named_bar_sync(BAR_SOLVE, kSolveThreads);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 13, c);
       // Diagonal 16 x 16 blocks by forward substitution, one column per thread
-      // (zero above the diagonal).
+      // (zero above the diagonal), right-looking: once x_j is final, every
+      // later row's sum takes its term at once, so the dependent chain is the
+      // 16 steps of j, not the 120 products.
       if (t < 64) {
         const int I = t >> 4, col = t & 15, r0 = 16 * I;
         float x[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float acc = i == col ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) x[i] = i == col ? 1.f : 0.f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (j < i) acc -= As[(r0 + i) * kAS + r0 + j] * x[j];
-          x[i] = i >= col ? acc : 0.f;
-          Ts[(r0 + i) * kAS + r0 + col] = x[i];
+        for (int j = 0; j < 15; ++j) {
+          float a[16];
+#pragma unroll
+          for (int i = j + 1; i < 16; ++i) a[i] = As[(r0 + i) * kAS + r0 + j];
+          const float xj = j >= col ? x[j] : 0.f;
+#pragma unroll
+          for (int i = j + 1; i < 16; ++i) x[i] -= a[i] * xj;
         }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Ts[(r0 + i) * kAS + r0 + col] = i >= col ? x[i] : 0.f;
       }
       named_bar_sync(BAR_SOLVE, kSolveThreads);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 14, c);
       // Below the diagonal, by distance d = I - J:
       //   R = sum_{K=J}^{I-1} A_IK T_KJ,   T_IJ = -T_II R.
-      // 64 threads per block; each takes four rows of one column.
+      // 64 threads per block; each takes four rows of one column.  The column
+      // vector is loaded once per block of 16 and each row's 16 values
+      // before their products, so the loads overlap.
 #pragma unroll 1
       for (int d = 1; d <= 3; ++d) {
         const int b = t >> 6, tt = t & 63, ri = tt >> 4, j = tt & 15;
@@ -455,11 +473,21 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
           for (int K = J; K < I; ++K) {
+            float tv[16];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-              const float tv = Ts[(16 * K + m) * kAS + 16 * J + j];
+            for (int m = 0; m < 16; ++m) tv[m] = Ts[(16 * K + m) * kAS + 16 * J + j];
 #pragma unroll
-              for (int r = 0; r < 4; ++r) acc[r] += As[(i0 + r) * kAS + 16 * K + m] * tv;
+            for (int r = 0; r < 4; ++r) {
+              float av[16];
+#pragma unroll
+              for (int m = 0; m < 16; ++m) av[m] = As[(i0 + r) * kAS + 16 * K + m];
+              float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+              for (int m = 0; m < 16; m += 2) {
+                s0 += av[m] * tv[m];
+                s1 += av[m + 1] * tv[m + 1];
+              }
+              acc[r] += s0 + s1;
             }
           }
 #pragma unroll
@@ -467,28 +495,34 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         named_bar_sync(BAR_SOLVE, kSolveThreads);
         if (act) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          float rv[16];
 #pragma unroll
-          for (int m = 0; m < 16; ++m) {
-            const float rv = Rs[b * 272 + m * 17 + j];
+          for (int m = 0; m < 16; ++m) rv[m] = Rs[b * 272 + m * 17 + j];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-              if (m <= 4 * ri + r) acc[r] -= Ts[(i0 + r) * kAS + 16 * I + m] * rv;
+          for (int r = 0; r < 4; ++r) {
+            float tv[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) tv[m] = Ts[(i0 + r) * kAS + 16 * I + m];  // zero above the diagonal
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m += 2) {
+              s0 += tv[m] * rv[m];
+              s1 += tv[m + 1] * rv[m + 1];
+            }
+            Ts[(i0 + r) * kAS + 16 * J + j] = -(s0 + s1);
           }
-#pragma unroll
-          for (int r = 0; r < 4; ++r) Ts[(i0 + r) * kAS + 16 * J + j] = acc[r];
         }
         named_bar_sync(BAR_SOLVE, kSolveThreads);
       }
       LA_TRACE_EVENT(trace_on && t == 0, t0, 3, c);
       // The T and P tiles were last read by the previous chunk's MMAs.
       if (c >= 1 && !(ok = swait(m_full, (c - 1) & 1, 17))) break;
-      if (p_side && row >= 0) {
-        unsigned char *pt = smem + SM::OFF_P;
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8)
-          *reinterpret_cast<uint4 *>(pt + row * 128 + ((q8 ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 15, c);
+      {  // P staging -> P tile: the same swizzled layout, 16 bytes x2 per thread
+        const uint4 *src = reinterpret_cast<const uint4 *>(smem + SM::OFF_PS);
+        uint4 *dst = reinterpret_cast<uint4 *>(smem + SM::OFF_P);
+        dst[t] = src[t];
+        dst[t + kSolveThreads] = src[t + kSolveThreads];
       }
       {  // T -> bf16, K-major rows; 16-byte chunk x2 per thread; zero above the block diagonal
         unsigned char *tt = smem + SM::OFF_T;
@@ -611,7 +645,6 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       fence_proxy_async_smem();
       tc_fence_before();
       named_bar_sync(BAR_EPI, 128);
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 11, c);
       if (t == 0) {
         mbar_arrive(o_free);
         for (int bb = 0; bb < D / BOX; ++bb)

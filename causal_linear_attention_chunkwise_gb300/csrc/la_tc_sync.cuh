@@ -22,6 +22,7 @@ constexpr int BOX = 64;                 // TMA box: 64 rows x 64 bf16 (128 bytes
 constexpr uint32_t BOX_BYTES = 8192;
 constexpr uint64_t kWaitNs = 2000000000ull;  // a wait gives up after 2 s
 constexpr uint32_t kSpinCap = 1u << 26;       // and after this many polls regardless
+constexpr uint32_t kSleepNs = 1000;           // suspend-time hint of one poll
 
 struct Ctl {
   uint32_t abort;
@@ -35,7 +36,9 @@ static __device__ __noinline__ bool wait1_slow(uint64_t *bar, uint32_t parity, C
                                         unsigned int *err, uint32_t kid, uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1; i < kSpinCap; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // Suspend (up to kSleepNs) rather than spin: the other warps of this
+    // sub-partition keep its issue slots.
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
     if ((i & 63u) == 0) {
       if (*(volatile uint32_t *)&ctl->abort) return false;
       if (global_timer_ns() - t0 > kWaitNs) break;
@@ -158,13 +161,14 @@ __device__ __forceinline__ void st_row16(unsigned char *base, uint32_t blk, int 
       make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
-// Elementwise pass over NT consecutive bf16 tiles of 64 rows x D columns (D/64
-// swizzled 8 KB boxes per tile, 8 sixteen-byte chunks per 128-byte row):
-// x <- phi(x) * fac(k, row) in tile k.  Threads t = 0..n-1 take chunks t,
-// t + n, ...; four loads are issued before any use.
-template <int D, int NT, bool PHI, bool SCALE, typename Fac>
+// Elementwise pass over NT consecutive bf16 tiles of ROWS rows x D columns
+// (D/64 swizzled boxes of ROWS x 128 bytes per tile, 8 sixteen-byte chunks per
+// row): x <- phi(x) * fac(k, row) in tile k.  Threads t = 0..n-1 take chunks
+// t, t + n, ...; four loads are issued before any use.
+template <int D, int NT, bool PHI, bool SCALE, typename Fac, int ROWS = 64>
 __device__ __forceinline__ void tile_pass(unsigned char *tile, Fac fac, int t, int n) {
-  constexpr int kTileChunks = 64 * D * 2 / 16;
+  constexpr int kTileChunks = ROWS * D * 2 / 16;
+  constexpr int kBoxChunks = ROWS * 8;
   constexpr int kChunks = NT * kTileChunks;
 #pragma unroll 1
   for (int base = 0; base < kChunks; base += 4 * n) {
@@ -179,7 +183,7 @@ __device__ __forceinline__ void tile_pass(unsigned char *tile, Fac fac, int t, i
       const int x = base + j * n + t;
       if (x >= kChunks) continue;
       float sc = 1.f;
-      if (SCALE) sc = fac(NT == 1 || x < kTileChunks ? 0 : 1, (x & 511) >> 3);
+      if (SCALE) sc = fac(NT == 1 || x < kTileChunks ? 0 : 1, (x % kBoxChunks) >> 3);
       uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
