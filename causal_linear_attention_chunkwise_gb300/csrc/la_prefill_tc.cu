@@ -55,10 +55,24 @@
 #ifdef LA_TRACE
 namespace la {
 __device__ long long g_trace[kTraceEvents][kTraceChunks];
+// Global-timer stamps per CTA of the three prefill kernels: [kernel][cta][slot].
+__device__ unsigned long long g_cta[3][1024][3];
 }
 extern "C" int la_trace_read(long long *out) {
   return (int)cudaMemcpyFromSymbol(out, la::g_trace, sizeof(la::g_trace));
 }
+extern "C" int la_cta_read(unsigned long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, la::g_cta, sizeof(la::g_cta));
+}
+#define LA_CTA_STAMP(kern, slot)                                                             \
+  do {                                                                                     \
+    const unsigned cta_ = blockIdx.x + gridDim.x * blockIdx.y;                             \
+    if (cta_ < 1024) ::la::g_cta[(kern)][cta_][(slot)] = ::la::global_timer_ns();           \
+  } while (0)
+#else
+#define LA_CTA_STAMP(kern, slot) \
+  do {                           \
+  } while (0)
 #endif
 
 namespace la {
@@ -144,6 +158,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
   float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
   pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid
+  if (threadIdx.x == 0) LA_CTA_STAMP(0, 0);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
@@ -310,6 +325,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     __syncwarp();
     tmem_dealloc(tmem, D);
   }
+  if (threadIdx.x == 0) LA_CTA_STAMP(0, 2);
 }
 
 // ================================================================ state scan
@@ -320,7 +336,9 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
   // Launched as a programmatic dependent of the segment-state kernel: let the
   // output kernel's CTAs start, then wait until the segment states are written.
   pdl_launch_dependents();
+  if (threadIdx.x == 0) LA_CTA_STAMP(1, 0);
   pdl_wait_previous();
+  if (threadIdx.x == 0) LA_CTA_STAMP(1, 1);
   const int bh = blockIdx.y;
   const size_t n4 = (size_t)D * D / 4;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -513,6 +531,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) LA_CTA_STAMP(2, 0);
   // Grid (B*H, segment pairs or segments): blocks launch segment by segment,
   // so the shorter last segments of every sequence come last.
   const int bh = blockIdx.x, h = bh % p.H;
@@ -1104,6 +1123,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     // have been launched alongside (programmatic dependent launch): only this
     // warpgroup reads them, so only it waits for the scan grid to finish.
     if (p.n_seg > 1) pdl_wait_previous();
+    if (t == 0) LA_CTA_STAMP(2, 1);
     // Initial states, chain by chain (a chain's first chunk is virtual 0 or 1).
     for (int ch = 0; ok && ch < NCHAIN; ++ch) {
       const int sg = ch_seg(ch);
@@ -1258,6 +1278,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     __syncwarp();
     tmem_dealloc(tmem, SM::T_COLS);
   }
+  if (tid == 0) LA_CTA_STAMP(2, 2);
 }
 
 // ---------------------------------------------------------------- planning
