@@ -421,36 +421,43 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int J = 0; J < 4; ++J)
           if (J > I) rnext[J] += log_alpha_at(p, bhL, tok0 + 16 * J, ch, D);
-        float lam[16], qv[16], kv[16];
-        float run = base;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          run += log_alpha_at(p, bhL, tok0 + 16 * I + i, ch, D);
-          lam[i] = run;
-          const uint32_t off = tile_off(16 * I + i, ch, BOX_BYTES);
-          const float a = ld_bf16(qt + off), b = ld_bf16(kt + off);
-          qv[i] = PHI ? elu1_fast(a) : a;
-          kv[i] = PHI ? elu1_fast(b) : b;
-        }
-        const float r = lam[0];
-        if (r - lam[15] > kDiagSpanMax) flag[s] = 1u;
+        // The block's 16 tokens in two halves of 8, so that few values are
+        // live at once and the tokens' independent chains can overlap.
         if (I == 3) dec[s * D + ch] = __expf(lend);
-        const float er = __expf(r);
+        float run = base, r = 0.f, er = 1.f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int row = 16 * I + i;
-          const uint32_t off = tile_off(row, ch, BOX_BYTES);
-          const float qh = qv[i] * __expf(lam[i] - r);               // <= 1 factor
-          st_bf16(qt + off, qh);                                     // Qh (in place)
-          st_bf16(xq + off, qh * er);                                // Qt = q e^{Lam}
-          st_bf16(kt + off, kv[i] * __expf(lend - lam[i]));          // Kt (in place)
-          st_bf16(xk + tile_off(k_row0(I) + row, ch, SM::KBOX),      // own block of K^(I)
-                  kv[i] * __expf(fminf(r - lam[i], kDiagSpanMax)));
+        for (int hh = 0; hh < 2; ++hh) {
+          float lam[8], qv[8], kv[8];
 #pragma unroll
-          for (int J = 0; J < 4; ++J)                                // K^(J), J > I
-            if (J > I)
-              st_bf16(xk + tile_off(k_row0(J) + row, ch, SM::KBOX), kv[i] * __expf(rnext[J] - lam[i]));
+          for (int i = 0; i < 8; ++i) {
+            run += log_alpha_at(p, bhL, tok0 + 16 * I + 8 * hh + i, ch, D);
+            lam[i] = run;
+            const uint32_t off = tile_off(16 * I + 8 * hh + i, ch, BOX_BYTES);
+            const float a = ld_bf16(qt + off), b = ld_bf16(kt + off);
+            qv[i] = PHI ? elu1_fast(a) : a;
+            kv[i] = PHI ? elu1_fast(b) : b;
+          }
+          if (hh == 0) {
+            r = lam[0];
+            er = __expf(r);
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 16 * I + 8 * hh + i;
+            const uint32_t off = tile_off(row, ch, BOX_BYTES);
+            const float qh = qv[i] * __expf(lam[i] - r);               // <= 1 factor
+            st_bf16(qt + off, qh);                                     // Qh (in place)
+            st_bf16(xq + off, qh * er);                                // Qt = q e^{Lam}
+            st_bf16(kt + off, kv[i] * __expf(lend - lam[i]));          // Kt (in place)
+            st_bf16(xk + tile_off(k_row0(I) + row, ch, SM::KBOX),      // own block of K^(I)
+                    kv[i] * __expf(fminf(r - lam[i], kDiagSpanMax)));
+#pragma unroll
+            for (int J = 0; J < 4; ++J)                                // K^(J), J > I
+              if (J > I)
+                st_bf16(xk + tile_off(k_row0(J) + row, ch, SM::KBOX), kv[i] * __expf(rnext[J] - lam[i]));
+          }
         }
+        if (r - run > kDiagSpanMax) flag[s] = 1u;
       }
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
