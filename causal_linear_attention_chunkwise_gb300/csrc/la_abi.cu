@@ -286,6 +286,15 @@ la_status la_decode_step(const void *q, const void *k, const void *v, int dtype,
 size_t la_normalised_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk,
                                          int dtype) {
   if (B <= 0 || H <= 0 || L <= 0 || !supported_d(d_k) || !supported_d(d_v)) return 0;
+  PrefillArgs probe{};
+  probe.dtype = dtype;
+  probe.B = B;
+  probe.H = H;
+  probe.L = L;
+  probe.dk = d_k;
+  probe.dv = d_v;
+  probe.chunk = chunk;
+  if (prefill_tc_norm_supported(probe)) return prefill_tc_norm_workspace_bytes(B, H, L);
   return align256(la_chunk_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk, dtype)) +
          normaliser_workspace_bytes(B, H, L, d_k);
 }
@@ -305,6 +314,26 @@ la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dty
   la_status s = check_variant(fn, q, k, v, dtype, B, H, L, d_k, d_v, chunk, true, S0, z0, O,
                               S_final, z_final, st, &done);
   if (s != LA_OK || done) return s;
+  const int phi = g_phi.load();
+  const float *dec = decay_kind == LA_DECAY_NONE ? nullptr : decay;
+  {
+    // One pass on the d = 64 tensor-core kernels: the denominator and z ride
+    // with the numerator and the state as one more value column.
+    PrefillArgs a{q, k, v, dtype, B, H, L, d_k, d_v, chunk, phi, decay_kind, dec, S0, O,
+                  S_final, workspace, ws_bytes, st};
+    if (prefill_tc_norm_supported(a)) {
+      const size_t need = prefill_tc_norm_workspace_bytes(B, H, L);
+      if (need > 0 && (!workspace || ws_bytes < need))
+        return fail(LA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                    workspace ? ws_bytes : (size_t)0);
+      if (need > 0 && !aligned16(workspace))
+        return fail(LA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
+      const char *why = nullptr;
+      const cudaError_t e = launch_prefill_tc_norm(a, z0, z_final, &why);
+      if (e != cudaSuccess) return cuda_fail(e, why ? why : fn);
+      return ok();
+    }
+  }
   const size_t num_ws = la_chunk_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk, dtype);
   const size_t need = align256(num_ws) + normaliser_workspace_bytes(B, H, L, d_k);
   if (!workspace || ws_bytes < need)
@@ -312,8 +341,6 @@ la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dty
                 workspace ? ws_bytes : (size_t)0);
   if (!aligned16(workspace))
     return fail(LA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
-  const int phi = g_phi.load();
-  const float *dec = decay_kind == LA_DECAY_NONE ? nullptr : decay;
   // The numerator phi(q_t)^T S_t goes to O (and S_final) through the prefill
   // kernels; the normaliser then forms z and divides O in place.
   PrefillArgs a{q, k, v, dtype, B, H, L, d_k, d_v, chunk, phi, decay_kind, dec, S0, O,

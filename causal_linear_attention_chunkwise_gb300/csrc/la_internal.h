@@ -46,6 +46,15 @@ size_t prefill_tc_workspace_bytes(int B, int H, int L, int d);
 int prefill_tc_kernel_count(int B, int H, int L, int d);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, const char **why);
 
+// The normalised form in one pass on the d = 64 tensor-core kernels: a ones
+// column rides with V, so O carries the denominator (divided out before the
+// store) and the state carries z.  Supported when prefill_tc_supported and
+// d_k = d_v = 64; the workspace holds segment states of 64 + 16 columns.
+bool prefill_tc_norm_supported(const PrefillArgs &a);
+size_t prefill_tc_norm_workspace_bytes(int B, int H, int L);
+cudaError_t launch_prefill_tc_norm(const PrefillArgs &a, const float *z0, float *z_final,
+                                   const char **why);
+
 // Non-causal form O = phi(Q) (phi(K)^T V): bf16, d_k == d_v in {64, 128}.
 struct NoncausalArgs {
   const void *q, *k, *v;

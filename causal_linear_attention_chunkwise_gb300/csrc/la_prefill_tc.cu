@@ -108,9 +108,14 @@ struct TcParams {
   const float *decay;
   const float *S0;  // read directly only when NS == 1
   float *S_final;
-  float *ws_state;  // [BH][NS][D][D]: slot s = incoming state of segment s
+  float *ws_state;  // [BH][NS][D][srow]: slot s = incoming state of segment s
   float *ws_logdec; // [BH][NS]: total log decay of segment s (s < NS-1)
   unsigned int *err;
+  // The normalised form (d = 64): state rows carry z in column D (srow = D + 16),
+  // and the output is divided by the denominator riding in O's column D.
+  int srow;           // floats per state row in the workspace slots (D, or D + 16)
+  const float *z0;    // [BH][D] or null (= zeros)
+  float *z_final;     // [BH][D] or null
 };
 
 // ================================================================ shared pieces
@@ -118,7 +123,7 @@ struct TcParams {
 // ================================================================ segment state
 // Shared memory: NST stages of {K tile, V tile}; the segment's suffix log
 // decays; per-stage row weights; barriers.
-template <int D>
+template <int D, bool NORM = false>
 struct StateSmem {
   // The two transform groups take alternate chunks, so the stage count must be
   // even: stage s is then always used by group s % 2, and every phase of its
@@ -131,7 +136,10 @@ struct StateSmem {
   static_assert(NST % 2 == 0, "stages must alternate between the two transform groups");
   static constexpr uint32_t TILE = 64 * D * 2;
   static constexpr uint32_t STAGE = 2 * TILE;
-  static constexpr uint32_t OFF_SUF = NST * STAGE;                       // floats [G*64]
+  // NORM: one constant block of ones (column 0) after the stages, read as the
+  // second 64-column block of every V operand: the state gains column D = z.
+  static constexpr uint32_t OFF_ONES = NST * STAGE;
+  static constexpr uint32_t OFF_SUF = OFF_ONES + (NORM ? 8192 : 0);      // floats [G*64]
   static constexpr uint32_t OFF_W = OFF_SUF + kMaxSegChunks * CH * 4;     // [NST][64] floats
   static constexpr uint32_t OFF_BAR = OFF_W + NST * 64 * 4;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
@@ -142,11 +150,14 @@ struct StateSmem {
 constexpr int kThreadsState = 384;  // warps 0..11: TMA, MMA, -, -, XG0 (4..7), XG1 (8..11)
 constexpr uint32_t BAR_XG0 = 1, BAR_XG1 = 2, BAR_XG = 3;
 
-template <int D, bool PHI, bool DECAY>
+template <int D, bool PHI, bool DECAY, bool NORM = false>
 __global__ void __launch_bounds__(kThreadsState, 2)  // two CTAs per SM
 segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
-  using SM = StateSmem<D>;
+  using SM = StateSmem<D, NORM>;
+  static_assert(!NORM || D == 64, "the normalised form rides the d = 64 kernels");
+  constexpr int ZW = NORM ? 16 : 0;
+  constexpr uint32_t kTmemCols = NORM ? 128 : D;
   constexpr int NST = SM::NST;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *suf = reinterpret_cast<float *>(smem + SM::OFF_SUF);
@@ -178,8 +189,16 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     fence_mbarrier_init();
   }
   if (warp == W_MMA) {
-    tmem_alloc(&ctl->tmem_base, D);
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
+  }
+  if constexpr (NORM) {  // the ones block: column 0 = 1, columns 1..15 = 0 (of 16 read)
+    if (tid < 64) {
+      unsigned char *ob = smem + SM::OFF_ONES + tid * 128;
+      *reinterpret_cast<uint4 *>(ob + ((0 ^ (tid & 7)) << 4)) = make_uint4(pack_bf16(1.f, 0.f), 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(ob + ((1 ^ (tid & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+      fence_proxy_async_smem();
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -214,17 +233,20 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     }
   } else if (warp == W_MMA) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(D, D, true, true);
+      constexpr uint32_t idesc = idesc_bf16_f32(D, D + ZW, true, true);
       for (int c = 0; c < nc; ++c) {
         const int s = c % NST;
         if (!wait1(&ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 2)) break;
         tc_fence_after();
         const uint32_t kt = smem_u32(smem + s * SM::STAGE);
         const uint32_t vt = kt + SM::TILE;
+        // V's second 64-column block: its next box (d = 128), or the ones
+        // block (NORM), LBO bytes on.
+        const uint32_t v_lbo = NORM ? smem_u32(smem + SM::OFF_ONES) - vt : BOX_BYTES;
 #pragma unroll
         for (int kk = 0; kk < CH / 16; ++kk)
           mma_bf16(tmem, smem_desc_sw128(kt + 2048 * kk, BOX_BYTES, 1024),
-                   smem_desc_sw128(vt + 2048 * kk, BOX_BYTES, 1024), idesc, (c | kk) != 0);
+                   smem_desc_sw128(vt + 2048 * kk, v_lbo, 1024), idesc, (c | kk) != 0);
         mma_commit(&empty[s]);
       }
       mma_commit(done);
@@ -299,7 +321,20 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       const int quarter = warp & 3;
       const int row = acc_row<D>(quarter, lane);
       if (!LA_CHK(seg + 1 < p.n_seg && bh < p.BH, KID_PREFILL_TC_STATE, 4)) seg_total = 0.f;
-      float *dst = p.ws_state + (((size_t)bh * p.n_seg + min(seg + 1, p.n_seg - 1)) * D) * D;
+      float *dst = p.ws_state + (((size_t)bh * p.n_seg + min(seg + 1, p.n_seg - 1)) * D) * p.srow;
+      if constexpr (NORM) {  // z: state column D (the 15 after it are zero)
+        __syncwarp();
+        uint32_t r[16];
+        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + D, r);
+        tmem_ld_wait();
+        if (row >= 0) {
+          float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * p.srow + D);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
         __syncwarp();
@@ -307,7 +342,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, r);
         tmem_ld_wait();
         if (row >= 0) {
-          float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * D + col);
+          float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * p.srow + col);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
@@ -323,7 +358,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   tc_fence_after();
   if (warp == W_MMA) {
     __syncwarp();
-    tmem_dealloc(tmem, D);
+    tmem_dealloc(tmem, kTmemCols);
   }
   if (threadIdx.x == 0) LA_CTA_STAMP(0, 2);
 }
@@ -331,8 +366,8 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
 // ================================================================ state scan
 // slot 0 <- S0 (or 0); slot s+1 <- exp(A_s) slot s + slot s+1, for s < NS-1.
 __global__ void __launch_bounds__(256)
-state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_state,
-                  const float *__restrict__ ws_logdec) {
+state_scan_kernel(int D, int srow, int n_seg, const float *S0, const float *z0,
+                  float *__restrict__ ws_state, const float *__restrict__ ws_logdec) {
   // Launched as a programmatic dependent of the segment-state kernel: let the
   // output kernel's CTAs start, then wait until the segment states are written.
   pdl_launch_dependents();
@@ -340,13 +375,19 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
   pdl_wait_previous();
   if (threadIdx.x == 0) LA_CTA_STAMP(1, 1);
   const int bh = blockIdx.y;
-  const size_t n4 = (size_t)D * D / 4;
+  // A slot is D rows of srow floats: the state, then (srow > D) z in column D.
+  const size_t n4 = (size_t)D * srow / 4;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n4) return;
+  const int r4 = srow / 4, row = (int)(i / r4), c4 = (int)(i % r4);
   float4 *slots = reinterpret_cast<float4 *>(ws_state) + (size_t)bh * n_seg * n4;
   const float *logdec = ws_logdec + (size_t)bh * n_seg;
-  float4 cur = S0 ? reinterpret_cast<const float4 *>(S0)[(size_t)bh * n4 + i]
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c4 < D / 4) {
+    if (S0) cur = reinterpret_cast<const float4 *>(S0)[((size_t)bh * D + row) * (D / 4) + c4];
+  } else if (c4 == D / 4 && z0) {
+    cur.x = z0[(size_t)bh * D + row];
+  }
   slots[i] = cur;
   // Segments in batches of eight: every load of a batch is issued before the
   // first use, so a batch costs one memory round trip.
@@ -386,20 +427,27 @@ state_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_stat
 //   so that every product has M = 128: S^T += V^T K, O^T = S^T Q^T (A, the
 //   bf16 copy of S^T, read from TMEM) and O^T += V^T P^T.  The state hand-over
 //   then stays in TMEM.
-template <int DK>
+template <int DK, bool NORM = false>
 struct OutSmem {
   static constexpr bool PAIRS = DK == 64;                       // two segments per CTA
   static constexpr int NCHAIN = PAIRS ? 2 : 1;                  // state chains
   static constexpr int CW = PAIRS ? 64 : DK / NCHAIN;           // state columns per chain
+  // The normalised form carries one more value column (ones: the denominator
+  // in O, z in the state), as a second 16-column block of every value-side
+  // operand; ZW = 16 extra columns (one used, the rest zero).
+  static constexpr int ZW = NORM ? 16 : 0;
+  static constexpr int CWT = CW + ZW;                           // TMEM columns per chain
+  static_assert(!NORM || PAIRS, "the normalised form rides the d = 64 kernel");
   // d = 128 keeps the output and the state transposed in TMEM (see the kernel):
   // its bf16 state copy lives in TMEM, not in shared memory.
   static constexpr bool TRANS = DK == 128 && NCHAIN == 1;
-  static constexpr int NST = PAIRS ? 5 : 3;
+  static constexpr int NST = PAIRS ? (NORM ? 4 : 5) : 3;
   static constexpr uint32_t TILE = 64 * DK * 2;            // Q, K, V or O tile of one chunk
-  static constexpr uint32_t STAGE = 3 * TILE;              // Q | K | V
+  static constexpr uint32_t STAGE = (NORM ? 4 : 3) * TILE; // Q | K | V (| ones block)
   static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
   static constexpr uint32_t S_BLOCK = DK * 128;            // [DK][64] bf16, MN-major
-  static constexpr uint32_t S_BYTES = TRANS ? 0 : S_BLOCK * (CW / 64);  // one chain's bf16 state
+  static constexpr uint32_t S_BYTES =                      // one chain's bf16 state (and z)
+      TRANS ? 0 : S_BLOCK * (CW / 64 + (NORM ? 1 : 0));
   static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;
   static constexpr uint32_t OFF_O = OFF_S + NCHAIN * S_BYTES;  // 2 x O tile store staging
   static constexpr uint32_t OFF_OFR = OFF_O + 2 * TILE;    // [2][64] output token factors (TRANS)
@@ -416,12 +464,12 @@ struct OutSmem {
                     OFF_O % 1024 == 0 && S_BYTES % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
   static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
-  // TMEM columns: P and O by virtual chunk parity, S by chain (CW columns each).
+  // TMEM columns: P and O by virtual chunk parity, S by chain (CWT columns each).
   // TRANS: O^T buffers of 64 columns (lanes = value columns), S^T fp32 (128
   // columns), and two bf16 copies of S^T as MMA A operands (64 columns each).
-  static constexpr uint32_t T_P = 0, T_O = 128, T_OW = TRANS ? 64 : DK;
+  static constexpr uint32_t T_P = 0, T_O = 128, T_OW = TRANS ? 64 : DK + ZW;
   static constexpr uint32_t T_S = 128 + 2 * T_OW, T_SB = T_S + 128, T_COLS = 512;
-  static_assert(T_S + NCHAIN * CW <= T_COLS && (!TRANS || T_SB + 128 <= T_COLS), "TMEM budget");
+  static_assert(T_S + NCHAIN * CWT <= T_COLS && (!TRANS || T_SB + 128 <= T_COLS), "TMEM budget");
 };
 
 // Warps: 0 TMA, 1 MMA, 2-7 PREP (192 threads), 8-11 WG2, 12-15 WG3.
@@ -500,16 +548,16 @@ struct Streams {
   __device__ int index(int sg, int c) const { return c < m ? 2 * c + sg : 2 * m + (c - m); }
 };
 
-template <int DK, bool PHI, bool DECAY>
+template <int DK, bool PHI, bool DECAY, bool NORM = false>
 __global__ void __launch_bounds__(kThreadsOut, 1)
 chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
                     const __grid_constant__ CUtensorMap tmO, TcParams p) {
-  using SM = OutSmem<DK>;
+  using SM = OutSmem<DK, NORM>;
   constexpr int NST = SM::NST;
   constexpr bool PAIRS = SM::PAIRS;
-  constexpr int NCHAIN = SM::NCHAIN, CW = SM::CW;
+  constexpr int NCHAIN = SM::NCHAIN, CW = SM::CW, CWT = SM::CWT, ZW = SM::ZW;
   constexpr int D = DK;  // d_k = d_v: the state row length
   extern __shared__ __align__(1024) unsigned char smem[];
   float *lam = reinterpret_cast<float *>(smem + SM::OFF_LAM);
@@ -540,6 +588,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   Streams st;
   int tok0[2], seg[2];
   const float *S_seg[2];
+  int S_ld[2];  // floats per row of S_seg (a workspace slot row holds z after S when NORM)
   for (int sg = 0; sg < 2; ++sg) {
     seg[sg] = PAIRS ? 2 * (int)blockIdx.y + sg : (sg == 0 ? (int)blockIdx.y : p.n_seg);
     const int c0 = seg[sg] * p.seg_chunks;
@@ -547,8 +596,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     tok0[sg] = c0 * CH;
     S_seg[sg] = nullptr;
     if (p.n_seg > 1) {
-      if (seg[sg] > 0 || p.S0) S_seg[sg] = p.ws_state + ((size_t)bh * p.n_seg + seg[sg]) * D * D;
+      S_ld[sg] = p.srow;
+      if (seg[sg] > 0 || p.S0 || (NORM && p.z0))
+        S_seg[sg] = p.ws_state + ((size_t)bh * p.n_seg + seg[sg]) * D * p.srow;
     } else {
+      S_ld[sg] = D;
       S_seg[sg] = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
     }
   }
@@ -617,7 +669,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         int sg, c;
         st.at(k, sg, c);
         unsigned char *stg = smem + s * SM::STAGE;
-        mbar_arrive_expect_tx(&full[s], SM::STAGE);
+        mbar_arrive_expect_tx(&full[s], 3 * SM::TILE);  // Q, K, V (not the ones block)
         const int tok = tok0[sg] + c * CH;
         for (int b = 0; b < DK / BOX; ++b) {
           if (!LA_CHK(b * BOX + BOX <= DK && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 2))
@@ -647,9 +699,11 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (nk > 0) {
       constexpr uint32_t FULL = 0xffffffffu;
       constexpr uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(64, DK, false, true);
-      constexpr uint32_t id_qs = idesc_bf16_f32(64, CW, false, true);
-      constexpr uint32_t id_kv = idesc_bf16_f32(DK, CW, true, true);
+      // NORM: N includes the ones block (V) / z block (S), read as the second
+      // 64-column MN block of the operand (V's next tile / the S copy's z block).
+      constexpr uint32_t id_pv = idesc_bf16_f32(64, DK + ZW, false, true);
+      constexpr uint32_t id_qs = idesc_bf16_f32(64, CW + ZW, false, true);
+      constexpr uint32_t id_kv = idesc_bf16_f32(DK, CW + ZW, true, true);
       // Transposed forms (TRANS): S^T += V^T K, O^T = S^T Q^T (A in TMEM),
       // O^T += V^T P^T.  M = 128 value columns in every one.
       constexpr uint32_t id_kvT = idesc_bf16_f32(DK, DK, true, true);
@@ -695,7 +749,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             LA_TRACE_EVENT(trace_on && lane == 0 && cc == 0, t0, 8, kc);
             const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
             const uint32_t o_t = tmem + SM::T_O + SM::T_OW * b;
-            const bool inter = S_seg[sg] != nullptr || c > 0;
+            const bool inter = NORM || S_seg[sg] != nullptr || c > 0;
             if constexpr (SM::TRANS) {
               // The chain is S^T += V^T K alone; O^T = S^T Q^T follows it off the
               // chain (its bf16 S^T copy is double-buffered in TMEM).
@@ -722,7 +776,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
               if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < CH / 16; ++kk)  // chain state: S (TMEM) += K^T V
-                  mma_bf16_w(tmem + SM::T_S + CW * ch, at(dMN, ko + 2048 * kk),
+                  mma_bf16_w(tmem + SM::T_S + CWT * ch, at(dMN, ko + 2048 * kk),
                              at(dMN, vb + 2048 * kk), HI, id_kv, (inter || kk > 0) ? 1u : 0u);
                 if (inter) {
 #pragma unroll
@@ -750,7 +804,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             tc_fence_after();
             LA_TRACE_EVENT(trace_on && lane == 0, t0, 5, km);
             const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * b;
-            const bool inter = S_seg[sg] != nullptr || c > 0;
+            const bool inter = NORM || S_seg[sg] != nullptr || c > 0;
             if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < CH / 16; ++kk) {  // O += P V   (TRANS: O^T += V^T P^T)
@@ -861,6 +915,21 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         if (t == 0) split[s] = sp ? 1u : 0u;
         if (sp) named_bar_sync(BAR_PREP, kPrepThreads);  // factors visible to the V pass
+      }
+      if constexpr (NORM) {  // the ones block after V: column 0 = V's row factor, the rest 0
+        if (t < 64) {
+          // Rows past the sequence end hold zero-filled keys that phi may map
+          // to non-zero values (elu + 1 gives 1): their ones must be zero, as
+          // their zero-filled values are, or they would be added to z.
+          int sg, c;
+          st.at(k, sg, c);
+          const bool live = tok0[sg] + c * CH + t < p.L;
+          const float f = !live ? 0.f : (DECAY && sp) ? vfac[s * 64 + t] : 1.f;
+          unsigned char *ob = qt + 3 * SM::TILE + t * 128;
+          *reinterpret_cast<uint4 *>(ob + ((0 ^ (t & 7)) << 4)) = make_uint4(pack_bf16(f, 0.f), 0u, 0u, 0u);
+          *reinterpret_cast<uint4 *>(ob + ((1 ^ (t & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
       }
       if constexpr (PHI) {  // Q and K tiles are adjacent in the stage: one pass
         tile_pass<DK, 2, true, false>(qt, [](int, int) { return 1.f; }, t, kPrepThreads);
@@ -1010,13 +1079,23 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       } else {
         // O has M = 64 as P: 16x256b loads, the rows' output factors, stmatrix.
         const int ra = 16 * quarter + (lane >> 2);
-        const float fa = DECAY ? ofr[b * 64 + ra] : 1.f, fb = DECAY ? ofr[b * 64 + ra + 8] : 1.f;
+        float fa = DECAY ? ofr[b * 64 + ra] : 1.f, fb = DECAY ? ofr[b * 64 + ra + 8] : 1.f;
+        if constexpr (NORM) {
+          // The denominator rides in O's column DK (the ones column), with the
+          // same output row factor as the numerator: the factor cancels.
+          uint32_t dr[4];
+          __syncwarp();
+          tmem_ld_16x256b_x1(tmem + lane_off + SM::T_O + SM::T_OW * b + DK, dr);
+          tmem_ld_wait();
+          fa = 1.f / __shfl_sync(0xffffffffu, __uint_as_float(dr[0]), lane & ~3);
+          fb = 1.f / __shfl_sync(0xffffffffu, __uint_as_float(dr[2]), lane & ~3);
+        }
         const int mi = lane >> 3, srow = 16 * quarter + 8 * (mi & 1) + (lane & 7);
 #pragma unroll 1
         for (int col = 0; col < DK; col += 64) {
           __syncwarp();
           uint32_t r[32];
-          tmem_ld_16x256b_x8(tmem + lane_off + SM::T_O + DK * b + col, r);
+          tmem_ld_16x256b_x8(tmem + lane_off + SM::T_O + SM::T_OW * b + col, r);
           tmem_ld_wait();
           uint32_t pa[8], pb[8];
 #pragma unroll
@@ -1080,8 +1159,31 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * tm_scale);
         __syncwarp();
-        tmem_st32(tmem + lane_off + SM::T_S + CW * ch + col, r);
+        tmem_st32(tmem + lane_off + SM::T_S + CWT * ch + col, r);
       }
+    };
+    // NORM: the chain's z column (state column DK; the next 15 stay zero):
+    // z * sm_scale into the bf16 copy's z block, z * tm_scale back into TMEM.
+    auto putz = [&](int ch, float z, float sm_scale, float tm_scale, bool to_tmem) {
+      if (srow >= 0) {
+        const uint32_t pk[8] = {pack_bf16(z * sm_scale, 0.f), 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        st_row16(smem + SM::OFF_S + ch * SM::S_BYTES, SM::S_BLOCK, srow, CW, pk);
+      }
+      if (to_tmem) {
+        uint32_t r16[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r16[j] = 0u;
+        r16[0] = __float_as_uint(z * tm_scale);
+        __syncwarp();
+        tmem_st16(tmem + lane_off + SM::T_S + CWT * ch + CW, r16);
+      }
+    };
+    auto getz = [&](int ch) -> float {  // the chain's z from TMEM (warp-collective)
+      uint32_t r16[16];
+      __syncwarp();
+      tmem_ld16(tmem + lane_off + SM::T_S + CWT * ch + CW, r16);
+      tmem_ld_wait();
+      return __uint_as_float(r16[0]);
     };
     // TRANS: this thread's TMEM lane is value column dv = t of S^T.  32 state
     // rows (d_k = 32 cb ..) of that column: r * sm packed to bf16 pairs into
@@ -1148,13 +1250,21 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           put_trans(cb, 0, r, sm0, tm0, true);
         }
         tmem_st_wait();
-      } else if (S_seg[sg] != nullptr) {
+      } else if (NORM || S_seg[sg] != nullptr) {
         const float sm0 = __expf(m0), tm0 = __expf(t0s);
+        if constexpr (NORM) {  // z: column D of a slot row, or z0 at the sequence start
+          float z = 0.f;
+          if (srow >= 0) {
+            if (p.n_seg > 1 && S_seg[sg] != nullptr) z = S_seg[sg][(size_t)srow * S_ld[sg] + D];
+            else if (p.n_seg == 1 && p.z0) z = p.z0[(size_t)bh * D + srow];
+          }
+          putz(ch, z, sm0, tm0, true);
+        }
 #pragma unroll 1
         for (int col = 0; col < CW; col += 32) {
           uint32_t r[32];
-          if (srow >= 0) {
-            const float4 *src = reinterpret_cast<const float4 *>(S_seg[sg] + (size_t)srow * D +
+          if (srow >= 0 && S_seg[sg] != nullptr) {
+            const float4 *src = reinterpret_cast<const float4 *>(S_seg[sg] + (size_t)srow * S_ld[sg] +
                                                                  ch_col(ch) + col);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1222,12 +1332,13 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           for (int col = 0; col < CW; col += 64) {
             __syncwarp();
             uint32_t r[2][32];
-            tmem_ld32(tmem + lane_off + SM::T_S + CW * ch + col, r[0]);
-            tmem_ld32(tmem + lane_off + SM::T_S + CW * ch + col + 32, r[1]);
+            tmem_ld32(tmem + lane_off + SM::T_S + CWT * ch + col, r[0]);
+            tmem_ld32(tmem + lane_off + SM::T_S + CWT * ch + col + 32, r[1]);
             tmem_ld_wait();
             put32(ch, col, r[0], sm, tm, DECAY);
             put32(ch, col + 32, r[1], sm, tm, DECAY);
           }
+          if constexpr (NORM) putz(ch, getz(ch), sm, tm, DECAY);
           if (DECAY) tmem_st_wait();
           }
           fence_proxy_async_smem();
@@ -1247,13 +1358,17 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int j = 0; j < 32; ++j) dst[(size_t)j * D] = __uint_as_float(r[j]) * fin;
           }
-        } else if (seg[sg] == p.n_seg - 1 && p.S_final) {
+        } else if (seg[sg] == p.n_seg - 1 && (p.S_final || (NORM && p.z_final))) {
           const float fin = DECAY ? __expf(g_prev[ch]) : 1.f;
+          if constexpr (NORM) {
+            const float z = getz(ch);
+            if (srow >= 0 && p.z_final) p.z_final[(size_t)bh * D + srow] = z * fin;
+          }
 #pragma unroll 1
-          for (int col = 0; col < CW; col += 32) {
+          for (int col = 0; col < CW && p.S_final; col += 32) {
             __syncwarp();
             uint32_t r[32];
-            tmem_ld32(tmem + lane_off + SM::T_S + CW * ch + col, r);
+            tmem_ld32(tmem + lane_off + SM::T_S + CWT * ch + col, r);
             tmem_ld_wait();
             if (srow >= 0) {
               float4 *dst = reinterpret_cast<float4 *>(p.S_final + ((size_t)bh * D + srow) * D +
@@ -1326,16 +1441,18 @@ Plan make_plan(int B, int H, int L, int D) {
   return best;
 }
 
-size_t ws_bytes_for(int B, int H, int L, int D) {
+// srow: floats per state row in a slot (D, or D + 16 for the normalised form).
+size_t ws_bytes_for(int B, int H, int L, int D, int srow) {
   Plan pl = make_plan(B, H, L, D);
   if (pl.n_seg <= 1) return 0;
   const size_t bh = (size_t)B * H;
-  const size_t st = bh * pl.n_seg * (size_t)D * D * sizeof(float);
+  const size_t st = bh * pl.n_seg * (size_t)D * srow * sizeof(float);
   return st + ((bh * pl.n_seg * sizeof(float) + 255) & ~(size_t)255);
 }
 
-template <int D, bool PHI, bool DECAY>
-cudaError_t launch_d(const PrefillArgs &a, const char **why) {
+template <int D, bool PHI, bool DECAY, bool NORM = false>
+cudaError_t launch_d(const PrefillArgs &a, const char **why, const float *z0 = nullptr,
+                     float *z_final = nullptr) {
   const Plan pl = make_plan(a.B, a.H, a.L, D);
   const int BH = a.B * a.H;
   TcParams p{};
@@ -1351,9 +1468,12 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   p.S0 = a.S0;
   p.S_final = a.S_final;
   p.err = device_error_word();
+  p.srow = NORM ? D + 16 : D;
+  p.z0 = z0;
+  p.z_final = z_final;
   if (pl.n_seg > 1) {
     p.ws_state = static_cast<float *>(a.workspace);
-    p.ws_logdec = p.ws_state + (size_t)BH * pl.n_seg * D * D;
+    p.ws_logdec = p.ws_state + (size_t)BH * pl.n_seg * D * p.srow;
   }
   CUtensorMap tq, tk, tv, to;
   if (!make_tmap_bf16_3d(&tq, a.q, D, a.L, BH, BOX, BOX) ||
@@ -1365,8 +1485,8 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
   }
   cudaError_t e;
   if (pl.n_seg > 1) {
-    using SS = StateSmem<D>;
-    auto ks = segment_state_kernel<D, PHI, DECAY>;
+    using SS = StateSmem<D, NORM>;
+    auto ks = segment_state_kernel<D, PHI, DECAY, NORM>;
     static int smem_set_state[64];
     e = set_smem_once(ks, SS::BYTES, smem_set_state);
     if (e != cudaSuccess) return e;
@@ -1381,9 +1501,9 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
       return e;
     }
 #endif
-    const int n4 = D * D / 4;
-    e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, pl.n_seg,
-                   a.S0, p.ws_state, (const float *)p.ws_logdec);
+    const int n4 = D * p.srow / 4;
+    e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, p.srow,
+                   pl.n_seg, a.S0, z0, p.ws_state, (const float *)p.ws_logdec);
     if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
       if (why) *why = "la_chunk_fwd: state-scan kernel launch";
       return e;
@@ -1395,8 +1515,8 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why) {
     }
 #endif
   }
-  using OS = OutSmem<D>;
-  auto ko = chunk_output_kernel<D, PHI, DECAY>;
+  using OS = OutSmem<D, NORM>;
+  auto ko = chunk_output_kernel<D, PHI, DECAY, NORM>;
   static int smem_set_out[64];
   e = set_smem_once(ko, OS::BYTES, smem_set_out);
   if (e != cudaSuccess) return e;
@@ -1644,6 +1764,7 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
   p.phi = a.phi;
   p.decay_kind = LA_DECAY_NONE;
   p.err = device_error_word();
+  p.srow = D;
   p.ws_state = static_cast<float *>(a.workspace);
   p.ws_logdec = p.ws_state + (size_t)BH * slots * D * D;
   CUtensorMap tq, tk, tv, to;
@@ -1665,8 +1786,9 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
     return e;
   }
   const int n4 = D * D / 4;
-  e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, slots,
-                 (const float *)nullptr, p.ws_state, (const float *)p.ws_logdec);
+  e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, D, slots,
+                 (const float *)nullptr, (const float *)nullptr, p.ws_state,
+                 (const float *)p.ws_logdec);
   if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
     if (why) *why = "la_noncausal_fwd: state-scan kernel launch";
     return e;
@@ -1702,7 +1824,25 @@ bool prefill_tc_supported(const PrefillArgs &a) {
 
 size_t prefill_tc_workspace_bytes(int B, int H, int L, int d) {
   if (B <= 0 || H <= 0 || L <= 0) return 0;
-  return ws_bytes_for(B, H, L, d);
+  return ws_bytes_for(B, H, L, d, d);
+}
+
+bool prefill_tc_norm_supported(const PrefillArgs &a) {
+  return prefill_tc_supported(a) && a.dk == 64;
+}
+
+size_t prefill_tc_norm_workspace_bytes(int B, int H, int L) {
+  if (B <= 0 || H <= 0 || L <= 0) return 0;
+  return ws_bytes_for(B, H, L, 64, 64 + 16);
+}
+
+cudaError_t launch_prefill_tc_norm(const PrefillArgs &a, const float *z0, float *z_final,
+                                   const char **why) {
+  const bool phi = a.phi != LA_PHI_IDENTITY, decay = a.decay_kind != LA_DECAY_NONE;
+  if (phi && decay) return launch_d<64, true, true, true>(a, why, z0, z_final);
+  if (phi) return launch_d<64, true, false, true>(a, why, z0, z_final);
+  if (decay) return launch_d<64, false, true, true>(a, why, z0, z_final);
+  return launch_d<64, false, false, true>(a, why, z0, z_final);
 }
 
 int prefill_tc_kernel_count(int B, int H, int L, int d) {

@@ -266,6 +266,14 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)
       : "r"(taddr));
 }
 
+// 16 lanes x 8 columns (x1 of 16x256b): register e of thread t holds lane
+// t / 4 + 8 (e >= 2), column 2 (t % 4) + (e & 1).
+__device__ __forceinline__ void tmem_ld_16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
 // Four 8x8 bf16 matrices in the mma fragment layout (thread t holds row t / 4,
 // columns 2 (t % 4), +1 of each), stored untransposed: thread 8 i + j gives
 // the address of row j of matrix i, 16 bytes.

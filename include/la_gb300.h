@@ -183,19 +183,25 @@ size_t la_noncausal_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v);
  *     S_t = a_t S_{t-1} + phi(k_t) v_t^T,   z_t = a_t z_{t-1} + phi(k_t),
  *     o_t = phi(q_t)^T S_t / (phi(q_t)^T z_t).
  *
- * The numerator runs on the same kernels as la_chunk_fwd (the tensor-core
- * kernels for bf16 with d_k = d_v in {64, 128} and chunk 64), then a scan of z
- * forms the denominators and divides O in place.  There is no epsilon in the
- * denominator: choose a positive feature map (LA_PHI_ELU1), as the tutorial
- * does, or the quotient may be undefined.
+ * For bf16 with d_k = d_v = 64 and chunk 64 it is one pass of the tensor-core
+ * prefill kernels: a column of ones rides with v, so z travels as one more
+ * state column and each row's denominator comes out of the same products as
+ * its numerator, and the epilogue divides before it stores O.  Otherwise the
+ * numerator runs on the la_chunk_fwd kernels (the tensor-core ones for bf16,
+ * d_k = d_v = 128, chunk 64), then a scan of z forms the denominators and
+ * divides O in place.  There is no epsilon in the denominator: choose a
+ * positive feature map (LA_PHI_ELU1), as the tutorial does, or the quotient
+ * may be undefined.
  *
  *   q, k   [B,H,L,d_k] dtype;  v, O [B,H,L,d_v] dtype
  *   decay_kind / decay   as for la_chunk_fwd
  *   S0     [B,H,d_k,d_v] fp32 or NULL (zero);  z0 [B,H,d_k] fp32 or NULL (zero)
  *   S_final, z_final   the states after the last token, or NULL; each may be
  *          the same buffer as S0 / z0.
- *   workspace  device scratch of la_normalised_fwd_workspace_bytes(...) bytes
- *          (never 0 for a non-empty problem); ws_bytes = its size.
+ *   workspace  device scratch of la_normalised_fwd_workspace_bytes(...) bytes,
+ *          or NULL when that is 0 (the one-pass form on a sequence short
+ *          enough for one CTA); ws_bytes = its size.  Its contents need no
+ *          initialisation and are not kept.
  */
 la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dtype,
                             int B, int H, int L, int d_k, int d_v, int chunk,

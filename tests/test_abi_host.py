@@ -177,7 +177,7 @@ def test_variant_validation_before_any_device_work(lib):
     assert nf(p, p, p, 1, 1, 1, 8, 16, 16, 64, 0, None, None, odd, p, None, None) == 1
     assert b"16-byte" in lib.la_last_error()
     assert nf(p, p, p, 1, 0, 3, 8, 16, 16, 64, 0, None, None, None, p, None, None) == 0
-    # the workspace: never empty for a non-empty problem, checked before any launch
+    # the workspace, checked before any launch
     need = lib.la_normalised_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 1)
     assert need > lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 1) > 0
     assert lib.la_normalised_fwd_workspace_bytes(1, 1, 300, 16, 16, 64, 0) > 0
@@ -205,16 +205,33 @@ def test_variant_validation_before_any_device_work(lib):
     assert dl(p, p, p, 2, 1, 1, 8, 16, 16, p, None, None, p, None, None) == 1
 
 
+def _segments(num, bh, d):
+    """Segments per sequence of a prefill workspace of num bytes: per segment a
+    d x d fp32 state, then a 256-byte-rounded fp32 log decay per segment."""
+    for n in range(1, 4096):
+        if bh * n * d * d * 4 + (bh * n * 4 + 255) // 256 * 256 == num:
+            return n
+    raise AssertionError(f"no segment count gives {num} bytes")
+
+
 def test_normalised_workspace_layout(lib):
-    """la_normalised_fwd's workspace is the prefill's (rounded up to 256 bytes)
-    followed by the z scan's: per sequence and 256-token block a d_k total and a
-    log decay, and one incoming z0 per sequence, all fp32."""
+    """la_normalised_fwd's workspace.  The two-pass form (every case but bf16,
+    d_k = d_v = 64, chunk 64) is the prefill's workspace (rounded up to 256
+    bytes) followed by the z scan's: per sequence and 256-token block a d_k
+    total and a log decay, and one incoming z0 per sequence, all fp32.  The
+    one-pass d = 64 form keeps the same segments, with each segment state 16
+    columns wider (z in the first of them), and has no scan of its own."""
     for B, H, L, dk, dv, chunk, dtype in [(4, 16, 4096, 64, 64, 64, 1), (1, 16, 32768, 128, 128, 64, 1),
                                           (2, 3, 300, 32, 16, 7, 0), (1, 1, 1, 16, 16, 64, 0),
-                                          (2, 32, 8192, 128, 128, 64, 1)]:
+                                          (2, 32, 8192, 128, 128, 64, 1), (4, 16, 4096, 64, 64, 64, 0),
+                                          (1, 2, 300, 64, 64, 64, 1), (8, 16, 16384, 64, 64, 64, 1)]:
         num = lib.la_chunk_fwd_workspace_bytes(B, H, L, dk, dv, chunk, dtype)
         bh, nblk = B * H, -(-L // 256)
-        scan = 4 * (bh * nblk * dk + bh * nblk + bh * dk)
-        want = (num + 255) // 256 * 256 + scan
+        if (dk, dv, chunk, dtype) == (64, 64, 64, 1):
+            n = _segments(num, bh, 64) if num else 0
+            want = bh * n * 64 * 80 * 4 + (bh * n * 4 + 255) // 256 * 256
+        else:
+            scan = 4 * (bh * nblk * dk + bh * nblk + bh * dk)
+            want = (num + 255) // 256 * 256 + scan
         assert lib.la_normalised_fwd_workspace_bytes(B, H, L, dk, dv, chunk, dtype) == want
     assert lib.la_normalised_fwd_workspace_bytes(1, 1, 64, 48, 48, 64, 1) == 0  # unsupported d

@@ -57,6 +57,76 @@ def test_normalised_matches_oracle(case):
     parity.check(z.cpu()[..., None], z_ref[..., None], dtype, "z")
 
 
+def _normalised_check(inp, phi, dtype, tag=""):
+    api.la_set_feature_map(phi)
+    O, S, z = api.la_normalised_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), 64,
+                                    inp["decay_kind"], _d(inp["decay"]), _d(inp["S0"]),
+                                    _d(inp["z0"]))
+    api.la_device_status()
+    O_ref, S_ref, z_ref = oracle.normalised(inp["q"], inp["k"], inp["v"], phi=phi,
+                                            decay_kind=inp["decay_kind"], decay=inp["decay"],
+                                            S0=inp["S0"], z0=inp["z0"])
+    parity.check(O.cpu(), O_ref, dtype, f"O{tag}")
+    parity.check(S.cpu(), S_ref, dtype, f"S{tag}")
+    parity.check(z.cpu()[..., None], z_ref[..., None], dtype, f"z{tag}")
+
+
+@pytest.mark.parametrize("decay", ["none", "head", "logit"])
+@pytest.mark.parametrize("with_state", [False, True])
+@pytest.mark.parametrize("L", [1, 64, 65, 1000, 5000])
+def test_normalised_one_pass_path(decay, with_state, L):
+    """bf16, d_k = d_v = 64, chunk 64: z rides with the numerator through the
+    tensor-core prefill kernels as a 65th value column.  One token, one chunk,
+    a ragged tail, and sequences long enough to be split into segments whose z
+    partials go through the scan; no decay, a per-head decay and gate logits
+    (whose chunks often pass the split form's range); with and without S0, z0."""
+    inp = W.make_variant_inputs("normalised", 2, 3, L, 64, 64, "bf16", seed=40 + L,
+                                with_state=with_state, gated=decay == "logit")
+    if decay == "head":
+        inp["decay_kind"] = "head"
+        inp["decay"] = torch.log(1 - 2.0 ** (-5 - torch.arange(3, dtype=torch.float32)))
+    _normalised_check(inp, "elu1", "bf16")
+
+
+def test_normalised_full_workload_shape_on_sampled_sequences():
+    """The benchmarked shape (B4 H16 L4096 d64, bf16, elu + 1, gate logits, S0
+    and z0) in one call, three sequences recomputed by the oracle."""
+    B, H, L, d = 4, 16, 4096, 64
+    inp = W.make_variant_inputs("normalised", B, H, L, d, d, "bf16", seed=0, with_state=True)
+    api.la_set_feature_map("elu1")
+    O, S, z = api.la_normalised_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), 64,
+                                    inp["decay_kind"], _d(inp["decay"]), _d(inp["S0"]),
+                                    _d(inp["z0"]))
+    api.la_device_status()
+    for b, h in [(0, 0), (1, 7), (3, 15)]:
+        sl = lambda x: x[b:b + 1, h:h + 1]  # noqa: E731
+        O_ref, S_ref, z_ref = oracle.normalised(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]),
+                                                phi="elu1", decay_kind="logit",
+                                                decay=sl(inp["decay"]), S0=sl(inp["S0"]),
+                                                z0=sl(inp["z0"]))
+        parity.check(sl(O).cpu(), O_ref, "bf16", f"O[{b},{h}]")
+        parity.check(sl(S).cpu(), S_ref, "bf16", f"S[{b},{h}]")
+        parity.check(sl(z).cpu()[..., None], z_ref[..., None], "bf16", f"z[{b},{h}]")
+
+
+def test_normalised_one_pass_outputs_may_alias_the_initial_states():
+    """S_final and z_final may be the S0 and z0 buffers (one-pass path, split
+    into segments so the scan reads S0 and z0 while the outputs are written)."""
+    inp = W.make_variant_inputs("normalised", 2, 2, 3000, 64, 64, "bf16", seed=47, with_state=True)
+    api.la_set_feature_map("elu1")
+    S, z = _d(inp["S0"]).clone(), _d(inp["z0"]).clone()
+    O, S_out, z_out = api.la_normalised_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), 64, "logit",
+                                            _d(inp["decay"]), S, z, S_final=S, z_final=z)
+    api.la_device_status()
+    assert S_out.data_ptr() == S.data_ptr() and z_out.data_ptr() == z.data_ptr()
+    O_ref, S_ref, z_ref = oracle.normalised(inp["q"], inp["k"], inp["v"], phi="elu1",
+                                            decay_kind="logit", decay=inp["decay"], S0=inp["S0"],
+                                            z0=inp["z0"])
+    parity.check(O.cpu(), O_ref, "bf16", "O")
+    parity.check(S.cpu(), S_ref, "bf16", "S")
+    parity.check(z.cpu()[..., None], z_ref[..., None], "bf16", "z")
+
+
 @pytest.mark.parametrize("case", CASES, ids=IDS)
 def test_channel_gate_matches_oracle(case):
     B, H, L, dk, dv, dtype, chunk, phi, _, with_state = case
