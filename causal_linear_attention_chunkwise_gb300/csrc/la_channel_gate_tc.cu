@@ -358,7 +358,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (did) {
           idle = 0;
           idle_since = 0;
-        } else if (__nanosleep(20), ++idle == 64) {  // bounded: give up after the limit
+        } else if (++idle == 256) {  // spin (a sleep delays the reaction to a barrier
+                                        // by far more than asked); bounded: give up after the limit
           idle = 0;
           const uint64_t now = global_timer_ns();
           if (idle_since == 0) {

@@ -441,20 +441,25 @@ struct OutSmem {
   // d = 128 keeps the output and the state transposed in TMEM (see the kernel):
   // its bf16 state copy lives in TMEM, not in shared memory.
   static constexpr bool TRANS = DK == 128 && NCHAIN == 1;
-  static constexpr int NST = PAIRS ? (NORM ? 4 : 5) : 3;
+  // d = 128 takes a fourth input stage in the room of a second P tile and a
+  // second O staging tile: the deeper prefetch is worth more than either.
+  static constexpr int NST = PAIRS ? (NORM ? 4 : 5) : 4;
+  static constexpr int NPB = TRANS ? 1 : 2;                // P tiles in shared memory
+  static constexpr int NOB = TRANS ? 1 : 2;                // O store staging tiles
   static constexpr uint32_t TILE = 64 * DK * 2;            // Q, K, V or O tile of one chunk
   static constexpr uint32_t STAGE = (NORM ? 4 : 3) * TILE; // Q | K | V (| ones block)
-  static constexpr uint32_t OFF_P = NST * STAGE;           // 2 x [64][64] bf16
+  static constexpr uint32_t OFF_P = NST * STAGE;           // NPB x [64][64] bf16
   static constexpr uint32_t S_BLOCK = DK * 128;            // [DK][64] bf16, MN-major
   static constexpr uint32_t S_BYTES =                      // one chain's bf16 state (and z)
       TRANS ? 0 : S_BLOCK * (CW / 64 + (NORM ? 1 : 0));
-  static constexpr uint32_t OFF_S = OFF_P + 2 * 8192;
-  static constexpr uint32_t OFF_O = OFF_S + NCHAIN * S_BYTES;  // 2 x O tile store staging
-  static constexpr uint32_t OFF_OFR = OFF_O + 2 * TILE;    // [2][64] output token factors (TRANS)
+  static constexpr uint32_t OFF_S = OFF_P + NPB * 8192;
+  static constexpr uint32_t OFF_O = OFF_S + NCHAIN * S_BYTES;  // NOB x O tile store staging
+  static constexpr uint32_t OFF_OFR = OFF_O + NOB * TILE;  // [2][64] output token factors (TRANS)
   static constexpr uint32_t OFF_LAM = OFF_OFR + 2 * 64 * 4;  // [NST][64] inclusive prefix
   static constexpr uint32_t OFF_VF = OFF_LAM + NST * 64 * 4;   // [NST][64] exp(A/2 - Lam_j)
   static constexpr uint32_t OFF_OF = OFF_VF + NST * 64 * 4;    // [NST][64] exp(Lam_i - A/2)
-  static constexpr uint32_t OFF_SPLIT = OFF_OF + NST * 64 * 4; // [NST] split decay used
+  static constexpr uint32_t OFF_RAW = OFF_OF + NST * 64 * 4;  // [4][64] decay inputs
+  static constexpr uint32_t OFF_SPLIT = OFF_RAW + 4 * 64 * 4;  // [NST] split decay used
   static constexpr uint32_t OFF_SCR = OFF_SPLIT + 16 * 4;      // 16 floats
   static constexpr uint32_t OFF_BAR = OFF_SCR + 16 * 4;
   static constexpr int NBAR = 4 * NST + 4 * 2 + 2 * 2 + 1;
@@ -724,8 +729,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       //   chain step kc: per chain, S += K^T V and O = Q S_c (needs the
       //     chain's state, Q/K/V rows in final form, O buffer kc & 1 free);
       //   P V of chunk km (needs P in smem; after its chain step);
-      //   QK^T of chunk kq (needs its tiles; P buffer kq & 1 free once
-      //     P V of chunk kq - 2 is issued: kq <= km + 1).
+      //   QK^T of chunk kq (needs its tiles; the shared-memory P tile it
+      //     leads to is free once P V of chunk kq - NPB is issued:
+      //     kq <= km + NPB - 1; MMAs complete in issue order).
       // In each stream the chunks go in order, and every test is of a phase
       // that cannot yet be overtaken by the next one on the same barrier.
       int kq = 0, kc = 0, cc = 0, km = 0;  // cc: next chain within step kc
@@ -803,7 +809,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           if (ready(&p_ready[b], (km >> 1) & 1)) {
             tc_fence_after();
             LA_TRACE_EVENT(trace_on && lane == 0, t0, 5, km);
-            const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * b;
+            const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * (b % SM::NPB);
             const bool inter = NORM || S_seg[sg] != nullptr || c > 0;
             if (elect_one()) {
 #pragma unroll
@@ -824,7 +830,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
             did = true;
           }
         }
-        if (kq < nk && kq <= km + 1) {  // ---- QK^T
+        if (kq < nk && kq <= km + SM::NPB - 1) {  // ---- QK^T
           const int s = kq % NST;
           if (ready(&xdone[s], (kq / NST) & 1)) {
             tc_fence_after();
@@ -847,7 +853,8 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (did) {
           idle_polls = 0;
           idle_since = 0;
-        } else if (__nanosleep(20), ++idle_polls == 64) {  // bounded: give up after the limit
+        } else if (++idle_polls == 256) {  // spin (a sleep delays the reaction to a barrier
+                                        // by far more than asked); bounded: give up after the limit
           idle_polls = 0;
           const uint64_t now = __shfl_sync(FULL, global_timer_ns(), 0);
           if (idle_since == 0) {
@@ -876,15 +883,30 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_PREFILL_TC_OUT, site, BAR_PREP, t);
     };
-    // Threads t < 64 load their token's decay input one chunk ahead, so the
-    // global load is in flight while the previous chunk is prepared.
-    auto decay_raw = [&](int k) -> float {
-      int sg, c;
-      st.at(k, sg, c);
-      return token_decay_raw(p.decay_kind, p.decay, h, bhL, tok0[sg] + c * CH + t, p.L);
+    // Threads t < 64 fetch their token's decay input three chunks ahead, as an
+    // asynchronous copy into a ring of four chunk slots: a DRAM round trip under
+    // full load can take longer than a chunk, and no register waits on it.
+    // Each fetch is one copy group of the thread (empty past the last chunk),
+    // so at prep(k) the groups of chunks k, k + 1, k + 2 are the pending ones.
+    float *rawbuf = reinterpret_cast<float *>(smem + SM::OFF_RAW);
+    auto fetch = [&](int k) {
+      if (k < nk) {
+        int sg, c;
+        st.at(k, sg, c);
+        const int tok = tok0[sg] + c * CH + t;
+        float *dst = rawbuf + (k & 3) * 64 + t;
+        if (tok < p.L)
+          cp_async_4(dst, p.decay_kind == LA_DECAY_HEAD ? p.decay + h : p.decay + bhL + tok);
+        else
+          *dst = token_decay_raw(p.decay_kind, p.decay, h, bhL, tok, p.L);
+      }
+      cp_async_commit();
     };
-    float raw_next = 0.f;
-    if (DECAY && t < 64 && nk > 0) raw_next = decay_raw(0);
+    if (DECAY && t < 64) {
+      fetch(0);
+      fetch(1);
+      fetch(2);
+    }
     auto prep = [&](int k) -> bool {
       const int s = k % NST;
       if (!gwait(&full[s], (k / NST) & 1, 7)) return false;
@@ -893,8 +915,9 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       bool sp = false;  // uniform over the group
       if constexpr (DECAY) {
         if (t < 64) {  // inclusive prefix of the chunk's log decays (warps 2, 3)
-          float x = token_log_decay(p.decay_kind, raw_next);
-          if (k + 1 < nk) raw_next = decay_raw(k + 1);
+          cp_async_wait<2>();  // chunk k's group is complete
+          float x = token_log_decay(p.decay_kind, rawbuf[(k & 3) * 64 + t]);
+          fetch(k + 3);  // into chunk k - 1's slot, read by this thread at prep(k - 1)
 #pragma unroll
           for (int off = 1; off < 32; off <<= 1) {
             float y = __shfl_up_sync(0xffffffffu, x, off);
@@ -963,11 +986,13 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       LA_TRACE_EVENT(trace_on && t == 0, t0, 14, k);
       return true;
     };
-    bool ok = nk > 0 && prep(0);
-    for (int k = 0; ok && k < nk; ++k) {
-      if (k + 1 < nk && !(ok = prep(k + 1))) break;
+    // prep(0), then prep(k + 1) before rescale(k): each lambda has one call
+    // site, so it is inlined and its captures (the decay ring) stay in registers.
+    bool ok = true;
+    for (int k = 0; ok && k <= nk; ++k) {
+      if (k < nk && !(ok = prep(k))) break;
       if constexpr (DECAY) {
-        if (!split[k % NST] && !(ok = rescale(k))) break;
+        if (k > 0 && !split[(k - 1) % NST] && !(ok = rescale(k - 1))) break;
       }
     }
   } else if (warp >= WG2 && warp < WG3) {
@@ -985,7 +1010,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         return false;
       tc_fence_after();
       LA_TRACE_EVENT(trace_on && t == 0, t0, 3, k);
-      unsigned char *ps = smem + SM::OFF_P + 8192 * b;
+      unsigned char *ps = smem + SM::OFF_P + 8192 * (b % SM::NPB);
       // Causal mask.  Split-form chunks need nothing more here (their row
       // factor is applied by the O epilogue); others take their decay per
       // element, out of line.
@@ -1033,10 +1058,10 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (!wait_wg(&o_full[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
         return false;
       tc_fence_after();
-      if (t == 0) tma_store_wait_read<1>();  // the store that used this buffer is done
+      if (t == 0) tma_store_wait_read<SM::NOB - 1>();  // the store that used this buffer is done
       __syncwarp();
       named_bar_sync(BAR_WG2, 128);
-      unsigned char *o_sm = smem + SM::OFF_O + b * SM::TILE;
+      unsigned char *o_sm = smem + SM::OFF_O + (b % SM::NOB) * SM::TILE;
       if constexpr (SM::TRANS) {
         // O^T: TMEM lanes are value columns, columns the chunk's 64 tokens.
         // Per 16 lanes (16x256b loads), each 8x8 block (8 value columns x 8

@@ -367,6 +367,22 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t row, uint32_t col) 
 
 namespace la {
 
+// Ampere-style asynchronous 4-byte copy global -> shared (no register is
+// written, so the issuing thread does not wait for it), grouped per thread.
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's most recent groups are still pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // 32 lanes x 32 bit, 32 consecutive columns per thread (see tmem_ld16).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
