@@ -64,6 +64,17 @@ extern "C" int la_trace_read(long long *out) {
 extern "C" int la_cta_read(unsigned long long *out) {
   return (int)cudaMemcpyFromSymbol(out, la::g_cta, sizeof(la::g_cta));
 }
+// Per-chunk events of the segment-state kernel's CTA (0, 0): [event][chunk].
+namespace la {
+__device__ long long g_strace[8][64];
+}
+extern "C" int la_strace_read(long long *out) {
+  return (int)cudaMemcpyFromSymbol(out, la::g_strace, sizeof(la::g_strace));
+}
+#define LA_STRACE(on, t0, ev, c)                                                             \
+  do {                                                                                     \
+    if ((on) && (c) < 64) ::la::g_strace[(ev)][(c)] = clock64() - (t0);                    \
+  } while (0)
 #define LA_CTA_STAMP(kern, slot)                                                             \
   do {                                                                                     \
     const unsigned cta_ = blockIdx.x + gridDim.x * blockIdx.y;                             \
@@ -71,6 +82,9 @@ extern "C" int la_cta_read(unsigned long long *out) {
   } while (0)
 #else
 #define LA_CTA_STAMP(kern, slot) \
+  do {                           \
+  } while (0)
+#define LA_STRACE(on, t0, ev, c) \
   do {                           \
   } while (0)
 #endif
@@ -140,8 +154,7 @@ struct StateSmem {
   // second 64-column block of every V operand: the state gains column D = z.
   static constexpr uint32_t OFF_ONES = NST * STAGE;
   static constexpr uint32_t OFF_SUF = OFF_ONES + (NORM ? 8192 : 0);      // floats [G*64]
-  static constexpr uint32_t OFF_W = OFF_SUF + kMaxSegChunks * CH * 4;     // [NST][64] floats
-  static constexpr uint32_t OFF_BAR = OFF_W + NST * 64 * 4;
+  static constexpr uint32_t OFF_BAR = OFF_SUF + kMaxSegChunks * CH * 4;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
   static constexpr uint32_t OFF_SCR = OFF_CTL + 64;                       // 8 floats
   static constexpr uint32_t BYTES = OFF_SCR + 64;
@@ -161,7 +174,6 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   constexpr int NST = SM::NST;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *suf = reinterpret_cast<float *>(smem + SM::OFF_SUF);
-  float *wrow = reinterpret_cast<float *>(smem + SM::OFF_W);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
   uint64_t *ready = empty + NST;   // K tile transformed
@@ -170,6 +182,10 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   float *scr = reinterpret_cast<float *>(smem + SM::OFF_SCR);
   pdl_launch_dependents();  // the scan may be scheduled now; it waits for this grid
   if (threadIdx.x == 0) LA_CTA_STAMP(0, 0);
+  const bool st_on = blockIdx.x == 0 && blockIdx.y == 0;
+  const long long st_t0 = clock64();
+  (void)st_on;
+  (void)st_t0;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
@@ -215,6 +231,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         if (c >= NST &&
             !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 1))
           break;
+        if (c >= NST) LA_STRACE(st_on, st_t0, 4, c - NST);
         unsigned char *st = smem + s * SM::STAGE;
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
         const int tok = tok0 + c * CH;
@@ -224,6 +241,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
           tma_load_3d(st + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
           tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
         }
+        LA_STRACE(st_on, st_t0, 0, c);
         issued = c + 1;
       }
       if (*(volatile uint32_t *)&ctl->abort)
@@ -238,6 +256,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         const int s = c % NST;
         if (!wait1(&ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 2)) break;
         tc_fence_after();
+        LA_STRACE(st_on, st_t0, 3, c);
         const uint32_t kt = smem_u32(smem + s * SM::STAGE);
         const uint32_t vt = kt + SM::TILE;
         // V's second 64-column block: its next box (d = 128), or the ones
@@ -256,8 +275,8 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     const int g = (warp - WG1) >> 2;           // transform group 0 or 1
     const int t = tid - WG1 * 32 - 128 * g;    // 0..127 within the group
     const uint32_t gbar = g ? BAR_XG1 : BAR_XG0;
-    // Suffix sums of the segment's log decays: suf[i] = sum_{r > i} lambda_r,
-    // so token i's weight is exp(suf[i]); A_s = sum of all lambda.  Both
+    // Token weights of the segment: suf[i] = exp(sum_{r > i} lambda_r), the
+    // decay from token i to the segment end; A_s = sum of all lambda.  Both
     // groups (256 threads) take PER consecutive tokens each: all of a
     // thread's decay inputs are loaded before any is used, so the prologue
     // costs one memory round trip, then a suffix scan over threads.
@@ -294,8 +313,8 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         if (w2 > wid) later += scr[w2];
       }
 #pragma unroll
-      for (int j = 0; j < PER; ++j)
-        if (t2 * PER + j < ntok) suf[t2 * PER + j] = sfx[j] + later;
+      for (int j = 0; j < PER; ++j)  // the token's weight itself (<= 1)
+        if (t2 * PER + j < ntok) suf[t2 * PER + j] = __expf(sfx[j] + later);
       seg_total = total;
     }
     named_bar_sync(BAR_XG, 256);  // suffix sums visible to both groups
@@ -303,17 +322,17 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     for (int c = g; c < nc; c += 2) {
       const int s = c % NST;
       if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, gbar)) break;
+      LA_STRACE(st_on && t == 0, st_t0, 1, c);
       unsigned char *kt = smem + s * SM::STAGE;
-      if (scale) {
-        if (t < 64) wrow[s * 64 + t] = __expf(suf[c * CH + t]);
-        named_bar_sync(gbar, 128);
-      }
-      const float *w = wrow + s * 64;
+      LA_STRACE(st_on && t == 0, st_t0, 5, c);
+      const float *w = suf + c * CH;
       if constexpr (phi || scale)
         tile_pass<D, 1, phi, scale>(kt, [w](int, int r) { return w[r]; }, t, 128);
+      LA_STRACE(st_on && t == 0, st_t0, 6, c);
       fence_proxy_async_smem();
       named_bar_sync(gbar, 128);
       if (t == 0) mbar_arrive(&ready[s]);
+      LA_STRACE(st_on && t == 0, st_t0, 2, c);
     }
     // Read the accumulated state out of TMEM (group 0) into segment slot s+1.
     if (g == 0 && wait_wg(done, 0, ctl, p.err, KID_PREFILL_TC_STATE, 4, BAR_XG0)) {

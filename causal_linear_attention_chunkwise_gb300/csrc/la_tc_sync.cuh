@@ -86,7 +86,6 @@ __device__ __forceinline__ bool wait_grp(uint64_t *bar, uint32_t parity, Ctl *ct
       : "r"(ok ? 1u : 0u), "r"(bar_id), "n"(NT)
       : "memory");
   if (any_fail) return false;
-  if (t != 0) mbar_try_wait(bar, parity);  // completed: own acquire
   __syncwarp();
   return true;
 }
