@@ -98,7 +98,9 @@ struct CgSmem {
   static constexpr uint32_t OFF_BAR = OFF_FLAG + 16;
   static constexpr int NBAR = 3 * NST + NX + 2 + NP + 2 + 2 + 2 + 1;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
-  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static constexpr int kTraceShrink = D == 64 ? 1 : 4;  // trace builds: chunks kept
+  static constexpr uint32_t OFF_TRC = OFF_CTL + 64;
+  static constexpr uint32_t BYTES = OFF_TRC + trace_smem_bytes(kTraceShrink);
   static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && XBUF % 1024 == 0 &&
                     OFF_P % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
@@ -240,6 +242,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     tmem_alloc(&ctl->tmem_base, SM::T_COLS);
     tmem_relinquish();
   }
+  LA_TRACE_TABLE(smem + SM::OFF_TRC, SM::kTraceShrink);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -653,6 +656,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     __syncwarp();
     tmem_dealloc(tmem, SM::T_COLS);
   }
+  LA_TRACE_FLUSH(trace_on, &g_trace[0][0]);
 }
 
 template <int D, bool PHI>

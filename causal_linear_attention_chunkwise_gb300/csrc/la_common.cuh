@@ -113,20 +113,52 @@ __device__ __forceinline__ void stage_slab(const T *__restrict__ src, size_t src
 }  // namespace la
 
 // Opt-in event trace for kernel development.  Built with -DLA_TRACE, kernels
-// record clock64() stamps of pipeline events for one chosen CTA into
-// la::g_trace[event][chunk] (relative to the CTA's start), which the using
-// translation unit defines; otherwise every LA_TRACE_EVENT compiles to nothing.
+// record clock64() stamps of pipeline events for one chosen CTA (relative to
+// the CTA's start) into a shared-memory table [event][chunk], which the CTA
+// copies to global memory as it exits: a global store per event would hold up
+// the next barrier its thread reaches (a barrier waits for the participating
+// threads' earlier memory accesses), and so distort the timeline it records.
+// Otherwise every trace macro compiles to nothing and the table takes no room.
+// A kernel short of shared memory keeps fewer chunks (kTraceChunks / shrink).
 namespace la {
 constexpr int kTraceEvents = 16, kTraceChunks = 64;
+#ifdef LA_TRACE
+constexpr uint32_t trace_smem_bytes(int shrink = 1) {
+  return kTraceEvents * (kTraceChunks / shrink) * 4;
+}
+#else
+constexpr uint32_t trace_smem_bytes(int = 1) { return 0; }
+#endif
 }  // namespace la
 #ifdef LA_TRACE
-#define LA_TRACE_EVENT(on, t0, ev, c)                                          \
-  do {                                                                         \
-    if ((on) && (c) < ::la::kTraceChunks)                                      \
-      ::la::g_trace[(ev)][(c)] = clock64() - (t0);                             \
+// Declares the kernel's table of kTraceChunks / shrink chunks at smem_ptr and
+// clears it (before a block barrier).
+#define LA_TRACE_TABLE(smem_ptr, shrink)                                           \
+  constexpr int la_trc_n = ::la::kTraceChunks / (shrink);                          \
+  uint32_t *la_trc = reinterpret_cast<uint32_t *>(smem_ptr);                       \
+  for (int i_ = threadIdx.x; i_ < ::la::kTraceEvents * la_trc_n; i_ += blockDim.x) \
+    la_trc[i_] = 0u
+#define LA_TRACE_EVENT(on, t0, ev, c)                                              \
+  do {                                                                             \
+    if ((on) && (c) < la_trc_n)                                                    \
+      la_trc[(ev) * la_trc_n + (c)] = (uint32_t)(clock64() - (t0));                \
+  } while (0)
+// Copies the table to long long dst[kTraceEvents][kTraceChunks] (after a block
+// barrier); chunks past the table's stay as they were.
+#define LA_TRACE_FLUSH(on, dst)                                                    \
+  do {                                                                             \
+    if (on)                                                                        \
+      for (int i_ = threadIdx.x; i_ < ::la::kTraceEvents * la_trc_n; i_ += blockDim.x) \
+        (dst)[(i_ / la_trc_n) * ::la::kTraceChunks + i_ % la_trc_n] = (long long)la_trc[i_]; \
   } while (0)
 #else
+#define LA_TRACE_TABLE(smem_ptr, shrink) \
+  do {                                   \
+  } while (0)
 #define LA_TRACE_EVENT(on, t0, ev, c) \
   do {                                \
+  } while (0)
+#define LA_TRACE_FLUSH(on, dst) \
+  do {                          \
   } while (0)
 #endif

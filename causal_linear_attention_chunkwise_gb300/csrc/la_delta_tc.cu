@@ -99,7 +99,8 @@ struct DtSmem {
   static constexpr uint32_t OFF_BAR = OFF_SCR + 64;
   static constexpr int NBAR = 4 * NST + 10;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
-  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static constexpr uint32_t OFF_TRC = OFF_CTL + 64;  // trace builds
+  static constexpr uint32_t BYTES = OFF_TRC + trace_smem_bytes();
   static_assert(STAGE % 1024 == 0 && OFF_KB % 1024 == 0 && OFF_T % 1024 == 0 &&
                     OFF_P % 1024 == 0 && OFF_W % 1024 == 0 && OFF_U % 1024 == 0 &&
                     OFF_M % 1024 == 0 && OFF_S % 1024 == 0 && OFF_O % 1024 == 0,
@@ -202,6 +203,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     tmem_alloc(&ctl->tmem_base, SM::T_COLS);
     tmem_relinquish();
   }
+  LA_TRACE_TABLE(smem + SM::OFF_TRC, 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -745,6 +747,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     __syncwarp();
     tmem_dealloc(tmem, SM::T_COLS);
   }
+  LA_TRACE_FLUSH(trace_on, &g_trace[0][0]);
 }
 
 template <int D, bool PHI, bool GATED>

@@ -66,15 +66,11 @@ extern "C" int la_cta_read(unsigned long long *out) {
 }
 // Per-chunk events of the segment-state kernel's CTA (0, 0): [event][chunk].
 namespace la {
-__device__ long long g_strace[8][64];
+__device__ long long g_strace[kTraceEvents][kTraceChunks];
 }
 extern "C" int la_strace_read(long long *out) {
   return (int)cudaMemcpyFromSymbol(out, la::g_strace, sizeof(la::g_strace));
 }
-#define LA_STRACE(on, t0, ev, c)                                                             \
-  do {                                                                                     \
-    if ((on) && (c) < 64) ::la::g_strace[(ev)][(c)] = clock64() - (t0);                    \
-  } while (0)
 #define LA_CTA_STAMP(kern, slot)                                                             \
   do {                                                                                     \
     const unsigned cta_ = blockIdx.x + gridDim.x * blockIdx.y;                             \
@@ -82,9 +78,6 @@ extern "C" int la_strace_read(long long *out) {
   } while (0)
 #else
 #define LA_CTA_STAMP(kern, slot) \
-  do {                           \
-  } while (0)
-#define LA_STRACE(on, t0, ev, c) \
   do {                           \
   } while (0)
 #endif
@@ -157,7 +150,8 @@ struct StateSmem {
   static constexpr uint32_t OFF_BAR = OFF_SUF + kMaxSegChunks * CH * 4;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
   static constexpr uint32_t OFF_SCR = OFF_CTL + 64;                       // 8 floats
-  static constexpr uint32_t BYTES = OFF_SCR + 64;
+  static constexpr uint32_t OFF_TRC = OFF_SCR + 64;                       // trace builds
+  static constexpr uint32_t BYTES = OFF_TRC + trace_smem_bytes();
 };
 
 constexpr int kThreadsState = 384;  // warps 0..11: TMA, MMA, -, -, XG0 (4..7), XG1 (8..11)
@@ -186,6 +180,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   const long long st_t0 = clock64();
   (void)st_on;
   (void)st_t0;
+  LA_TRACE_TABLE(smem + SM::OFF_TRC, 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, bh = blockIdx.y, h = bh % p.H;
@@ -231,7 +226,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         if (c >= NST &&
             !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 1))
           break;
-        if (c >= NST) LA_STRACE(st_on, st_t0, 4, c - NST);
+        if (c >= NST) LA_TRACE_EVENT(st_on, st_t0, 4, c - NST);
         unsigned char *st = smem + s * SM::STAGE;
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
         const int tok = tok0 + c * CH;
@@ -241,7 +236,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
           tma_load_3d(st + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
           tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
         }
-        LA_STRACE(st_on, st_t0, 0, c);
+        LA_TRACE_EVENT(st_on, st_t0, 0, c);
         issued = c + 1;
       }
       if (*(volatile uint32_t *)&ctl->abort)
@@ -256,7 +251,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         const int s = c % NST;
         if (!wait1(&ready[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 2)) break;
         tc_fence_after();
-        LA_STRACE(st_on, st_t0, 3, c);
+        LA_TRACE_EVENT(st_on, st_t0, 3, c);
         const uint32_t kt = smem_u32(smem + s * SM::STAGE);
         const uint32_t vt = kt + SM::TILE;
         // V's second 64-column block: its next box (d = 128), or the ones
@@ -322,17 +317,18 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     for (int c = g; c < nc; c += 2) {
       const int s = c % NST;
       if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, gbar)) break;
-      LA_STRACE(st_on && t == 0, st_t0, 1, c);
+      LA_TRACE_EVENT(st_on && t == 0, st_t0, 1, c);
       unsigned char *kt = smem + s * SM::STAGE;
-      LA_STRACE(st_on && t == 0, st_t0, 5, c);
+      LA_TRACE_EVENT(st_on && t == 0, st_t0, 5, c);
       const float *w = suf + c * CH;
       if constexpr (phi || scale)
         tile_pass<D, 1, phi, scale>(kt, [w](int, int r) { return w[r]; }, t, 128);
-      LA_STRACE(st_on && t == 0, st_t0, 6, c);
+      LA_TRACE_EVENT(st_on && t == 0, st_t0, 6, c);
       fence_proxy_async_smem();
+      LA_TRACE_EVENT(st_on && (t & 31) == 0, st_t0, 8 + (t >> 5), c);
       named_bar_sync(gbar, 128);
       if (t == 0) mbar_arrive(&ready[s]);
-      LA_STRACE(st_on && t == 0, st_t0, 2, c);
+      LA_TRACE_EVENT(st_on && t == 0, st_t0, 2, c);
     }
     // Read the accumulated state out of TMEM (group 0) into segment slot s+1.
     if (g == 0 && wait_wg(done, 0, ctl, p.err, KID_PREFILL_TC_STATE, 4, BAR_XG0)) {
@@ -379,6 +375,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
+  LA_TRACE_FLUSH(st_on, &g_strace[0][0]);
   if (threadIdx.x == 0) LA_CTA_STAMP(0, 2);
 }
 
@@ -483,7 +480,8 @@ struct OutSmem {
   static constexpr uint32_t OFF_BAR = OFF_SCR + 16 * 4;
   static constexpr int NBAR = 4 * NST + 4 * 2 + 2 * 2 + 1;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
-  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static constexpr uint32_t OFF_TRC = OFF_CTL + 64;  // trace builds
+  static constexpr uint32_t BYTES = OFF_TRC + trace_smem_bytes();
   static_assert(STAGE % 1024 == 0 && OFF_P % 1024 == 0 && OFF_S % 1024 == 0 &&
                     OFF_O % 1024 == 0 && S_BYTES % 1024 == 0,
                 "swizzled tiles need 1024-byte alignment");
@@ -668,6 +666,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     tmem_alloc(&ctl->tmem_base, SM::T_COLS);
     tmem_relinquish();
   }
+  LA_TRACE_TABLE(smem + SM::OFF_TRC, 1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1437,6 +1436,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     __syncwarp();
     tmem_dealloc(tmem, SM::T_COLS);
   }
+  LA_TRACE_FLUSH(trace_on, &g_trace[0][0]);
   if (tid == 0) LA_CTA_STAMP(2, 2);
 }
 

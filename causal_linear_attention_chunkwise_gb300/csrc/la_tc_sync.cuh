@@ -66,11 +66,11 @@ static __device__ __noinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   }
 }
 
-// Group-wide bounded wait for NT threads (t = index within the group): the
-// group's first thread polls while the others sleep in a reducing named
-// barrier that also hands them the outcome, so all leave together.  The
-// barrier orders the group's later accesses after the leader's acquire of the
-// mbarrier phase.
+// Group-wide bounded wait for NT threads (t = index within the group, whole
+// warps): the group's first thread polls while the others sleep in a reducing
+// named barrier (the .aligned form, entered converged after a __syncwarp) that
+// also hands them the outcome, so all leave together.  The barrier orders the
+// group's later accesses after the leader's acquire of the mbarrier phase.
 template <int NT>
 __device__ __forceinline__ bool wait_grp(uint64_t *bar, uint32_t parity, Ctl *ctl,
                                          unsigned int *err, uint32_t kid, uint32_t site,
@@ -81,7 +81,7 @@ __device__ __forceinline__ bool wait_grp(uint64_t *bar, uint32_t parity, Ctl *ct
   uint32_t any_fail;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
-      "barrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(any_fail)
       : "r"(ok ? 1u : 0u), "r"(bar_id), "n"(NT)
       : "memory");
