@@ -381,7 +381,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
 
 // ================================================================ state scan
 // slot 0 <- S0 (or 0); slot s+1 <- exp(A_s) slot s + slot s+1, for s < NS-1.
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 state_scan_kernel(int D, int srow, int n_seg, const float *S0, const float *z0,
                   float *__restrict__ ws_state, const float *__restrict__ ws_logdec) {
   // Launched as a programmatic dependent of the segment-state kernel: let the
@@ -405,9 +405,10 @@ state_scan_kernel(int D, int srow, int n_seg, const float *S0, const float *z0,
     cur.x = z0[(size_t)bh * D + row];
   }
   slots[i] = cur;
-  // Segments in batches of eight: every load of a batch is issued before the
-  // first use, so a batch costs one memory round trip.
-  constexpr int kB = 8;
+  // Segments in batches of 20: every load of a batch is issued before the
+  // first use, so a batch costs one memory round trip (one batch for up to 21
+  // segments).
+  constexpr int kB = 20;
   for (int s0 = 0; s0 + 1 < n_seg; s0 += kB) {
     float4 d[kB];
     float a[kB];
