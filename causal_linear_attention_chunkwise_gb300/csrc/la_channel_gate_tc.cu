@@ -93,12 +93,13 @@ struct CgSmem {
   static constexpr uint32_t OFF_O = OFF_S + (D / 64) * S_BLOCK;
   static constexpr uint32_t OFF_DEC = OFF_O + NO * TILE;    // [NST][D] e^{Lam_end,c}
   static constexpr uint32_t OFF_TOT = OFF_DEC + NST * D * 4;  // [4][D] block sums
-  static constexpr uint32_t OFF_EX = OFF_TOT + 4 * D * 4;   // [16][16] exact diagonal scores
+  static constexpr uint32_t OFF_FIRST = OFF_TOT + 4 * D * 4;  // [4][D] blocks' first log decays
+  static constexpr uint32_t OFF_EX = OFF_FIRST + 4 * D * 4; // [16][16] exact diagonal scores
   static constexpr uint32_t OFF_FLAG = OFF_EX + 256 * 4;    // [NST] span exceeded
   static constexpr uint32_t OFF_BAR = OFF_FLAG + 16;
   static constexpr int NBAR = 3 * NST + NX + 2 + NP + 2 + 2 + 2 + 1;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
-  static constexpr int kTraceShrink = D == 64 ? 1 : 4;  // trace builds: chunks kept
+  static constexpr int kTraceShrink = D == 64 ? 1 : 16;  // trace builds: chunks kept
   static constexpr uint32_t OFF_TRC = OFF_CTL + 64;
   static constexpr uint32_t BYTES = OFF_TRC + trace_smem_bytes(kTraceShrink);
   static_assert(STAGE % 1024 == 0 && OFF_X % 1024 == 0 && XBUF % 1024 == 0 &&
@@ -194,6 +195,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   extern __shared__ __align__(1024) unsigned char smem[];
   float *dec = reinterpret_cast<float *>(smem + SM::OFF_DEC);
   float *tot = reinterpret_cast<float *>(smem + SM::OFF_TOT);
+  float *first = reinterpret_cast<float *>(smem + SM::OFF_FIRST);
   float *ex = reinterpret_cast<float *>(smem + SM::OFF_EX);
   volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + SM::OFF_FLAG);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
@@ -387,12 +389,18 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_PREP, t);
     };
+    // One (block, channel) item per thread when 4 D <= the PREP threads
+    // (d = 64): the item's 16 log decays, loaded for the block sums, stay in
+    // registers for the block's own pass.  Otherwise (two items for some
+    // threads) that pass loads them again, all 16 at once.
+    constexpr bool KEEP = 4 * D <= kPrepThreads;
+    float av[16];
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST, xb = c % NX;
       const int tok0 = c * CH;
-      // Block sums of the log decays, [4][D]: they do not need the stage, so
-      // their loads go out while the chunk's tiles are still arriving.
+      // Block sums and first log decays, [4][D]: they do not need the stage,
+      // so their loads go out while the chunk's tiles are still arriving.
       for (int it = t; it < 4 * D; it += kPrepThreads) {
         const int I = it / D, ch = it % D;
         float a[16];
@@ -402,6 +410,11 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int i = 0; i < 16; ++i) sum += a[i];
         tot[I * D + ch] = sum;
+        first[I * D + ch] = a[0];
+        if constexpr (KEEP) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) av[i] = a[i];
+        }
       }
       if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
       LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);
@@ -424,7 +437,15 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         // first token's own log decay.
 #pragma unroll
         for (int J = 0; J < 4; ++J)
-          if (J > I) rnext[J] += log_alpha_at(p, bhL, tok0 + 16 * J, ch, D);
+          if (J > I) rnext[J] += first[J * D + ch];
+        float ai[16];  // the block's log decays
+        if constexpr (KEEP) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ai[i] = av[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ai[i] = log_alpha_at(p, bhL, tok0 + 16 * I + i, ch, D);
+        }
         // The block's 16 tokens in two halves of 8, so that few values are
         // live at once and the tokens' independent chains can overlap.
         if (I == 3) dec[s * D + ch] = __expf(lend);
@@ -434,7 +455,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           float lam[8], qv[8], kv[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            run += log_alpha_at(p, bhL, tok0 + 16 * I + 8 * hh + i, ch, D);
+            run += ai[8 * hh + i];
             lam[i] = run;
             const uint32_t off = tile_off(16 * I + 8 * hh + i, ch, BOX_BYTES);
             const float a = ld_bf16(qt + off), b = ld_bf16(kt + off);
