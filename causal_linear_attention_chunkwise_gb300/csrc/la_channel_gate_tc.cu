@@ -92,8 +92,11 @@ struct CgSmem {
   static constexpr uint32_t OFF_S = OFF_P + NP * 8192;
   static constexpr uint32_t OFF_O = OFF_S + (D / 64) * S_BLOCK;
   static constexpr uint32_t OFF_DEC = OFF_O + NO * TILE;    // [NST][D] e^{Lam_end,c}
-  static constexpr uint32_t OFF_TOT = OFF_DEC + NST * D * 4;  // [4][D] block sums
-  static constexpr uint32_t OFF_FIRST = OFF_TOT + 4 * D * 4;  // [4][D] blocks' first log decays
+  // PREP items are (block, channel pair, part): parts of 8 tokens at d = 64, whole
+  // 16-token blocks at d = 128, so that either has 256 items.
+  static constexpr int PARTS = D == 64 ? 2 : 1;
+  static constexpr uint32_t OFF_TOT = OFF_DEC + NST * D * 4;  // [4 PARTS][D] part sums
+  static constexpr uint32_t OFF_FIRST = OFF_TOT + 4 * PARTS * D * 4;  // [4][D] first log decays
   static constexpr uint32_t OFF_EX = OFF_FIRST + 4 * D * 4; // [16][16] exact diagonal scores
   static constexpr uint32_t OFF_FLAG = OFF_EX + 256 * 4;    // [NST] span exceeded
   static constexpr uint32_t OFF_BAR = OFF_FLAG + 16;
@@ -129,9 +132,6 @@ __device__ __forceinline__ uint32_t tile_off(int row, int col, uint32_t box) {
   return (uint32_t)(col >> 6) * box + sw128_offset((uint32_t)row, (uint32_t)(col & 63));
 }
 
-__device__ __forceinline__ float ld_bf16(const unsigned char *p) {
-  return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t *>(p)) << 16);
-}
 __device__ __forceinline__ void st_bf16(unsigned char *p, float x) {
   __nv_bfloat16 b = __float2bfloat16_rn(x);
   *reinterpret_cast<__nv_bfloat16 *>(p) = b;
@@ -194,7 +194,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   constexpr int NST = SM::NST, NX = SM::NX, NP = SM::NP, NO = SM::NO;
   extern __shared__ __align__(1024) unsigned char smem[];
   float *dec = reinterpret_cast<float *>(smem + SM::OFF_DEC);
-  float *tot = reinterpret_cast<float *>(smem + SM::OFF_TOT);
+  float *hsum = reinterpret_cast<float *>(smem + SM::OFF_TOT);
   float *first = reinterpret_cast<float *>(smem + SM::OFF_FIRST);
   float *ex = reinterpret_cast<float *>(smem + SM::OFF_EX);
   volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + SM::OFF_FLAG);
@@ -389,31 +389,52 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_PREP, t);
     };
-    // One (block, channel) item per thread when 4 D <= the PREP threads
-    // (d = 64): the item's 16 log decays, loaded for the block sums, stay in
-    // registers for the block's own pass.  Otherwise (two items for some
-    // threads) that pass loads them again, all 16 at once.
-    constexpr bool KEEP = 4 * D <= kPrepThreads;
-    float av[16];
+    // Items (block I, channel pair cp, part hh): TPI tokens of two adjacent
+    // channels, so that every shared-memory access moves a bf16 pair and the
+    // swizzled address is formed once per row for both.  Consecutive threads
+    // take consecutive pairs (coalesced log decay loads, one tile row per
+    // warp).  When the items fit the PREP threads one each, an item's log
+    // decays, loaded for the part sums, stay in registers for its pass;
+    // otherwise the pass loads them again, all at once.
+    constexpr int PARTS = SM::PARTS, TPI = 16 / PARTS;
+    constexpr int NPAIR = D / 2, NITEM = 4 * PARTS * NPAIR;
+    constexpr bool KEEP = NITEM <= kPrepThreads;
+    auto item_of = [](int it, int &I, int &cp, int &hh) {
+      cp = it % NPAIR;
+      hh = (it / NPAIR) % PARTS;
+      I = it / (PARTS * NPAIR);
+    };
+    auto load_item = [&](int tok0, int I, int cp, int hh, float2 (&a)[TPI]) {
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+        const int tok = tok0 + 16 * I + TPI * hh + i;
+        a[i] = tok < p.L ? *reinterpret_cast<const float2 *>(p.log_alpha + (bhL + tok) * D + 2 * cp)
+                         : make_float2(0.f, 0.f);  // padding decays nothing
+      }
+    };
+    float2 av[TPI];
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST, xb = c % NX;
       const int tok0 = c * CH;
-      // Block sums and first log decays, [4][D]: they do not need the stage,
-      // so their loads go out while the chunk's tiles are still arriving.
-      for (int it = t; it < 4 * D; it += kPrepThreads) {
-        const int I = it / D, ch = it % D;
-        float a[16];
+      // Half-block sums and blocks' first log decays: they do not need the
+      // stage, so their loads go out while the chunk's tiles are arriving.
+      for (int it = t; it < NITEM; it += kPrepThreads) {
+        int I, cp, hh;
+        item_of(it, I, cp, hh);
+        float2 a[TPI];
+        load_item(tok0, I, cp, hh, a);
+        float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) a[i] = log_alpha_at(p, bhL, tok0 + 16 * I + i, ch, D);
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) sum += a[i];
-        tot[I * D + ch] = sum;
-        first[I * D + ch] = a[0];
+        for (int i = 0; i < TPI; ++i) {
+          sum.x += a[i].x;
+          sum.y += a[i].y;
+        }
+        *reinterpret_cast<float2 *>(hsum + (PARTS * I + hh) * D + 2 * cp) = sum;
+        if (hh == 0) *reinterpret_cast<float2 *>(first + I * D + 2 * cp) = a[0];
         if constexpr (KEEP) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) av[i] = a[i];
+          for (int i = 0; i < TPI; ++i) av[i] = a[i];
         }
       }
       if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
@@ -423,66 +444,89 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (c >= NX && !(ok = gwait(&xfree[xb], ((c / NX) - 1) & 1, 8))) break;
       unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
       unsigned char *xq = smem + SM::OFF_X + xb * SM::XBUF, *xk = xq + SM::TILE;
-      for (int it = t; it < 4 * D; it += kPrepThreads) {
-        const int I = it / D, ch = it % D;
-        float base = 0.f, lend = 0.f, rnext[4];
+      for (int it = t; it < NITEM; it += kPrepThreads) {
+        int I, cp, hh;
+        item_of(it, I, cp, hh);
+        const int c0 = 2 * cp;
+        // Per channel of the pair: base = the blocks before I, lend = the
+        // whole chunk, rnext[J] = r of a later query block J (the blocks
+        // before it plus its first token's own log decay).
+        float2 base = make_float2(0.f, 0.f), lend = base, rnext[4];
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
-          const float tj = tot[J * D + ch];
-          rnext[J] = lend;  // sum of the blocks before J
-          if (J < I) base += tj;
-          lend += tj;
-        }
-        // r_{I'} for the later query blocks: the sum before them plus their
-        // first token's own log decay.
+          float2 tj = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int J = 0; J < 4; ++J)
-          if (J > I) rnext[J] += first[J * D + ch];
-        float ai[16];  // the block's log decays
+          for (int h = 0; h < PARTS; ++h) {
+            const float2 x = *reinterpret_cast<const float2 *>(hsum + (PARTS * J + h) * D + c0);
+            tj.x += x.x;
+            tj.y += x.y;
+          }
+          rnext[J] = lend;
+          if (J < I) {
+            base.x += tj.x;
+            base.y += tj.y;
+          }
+          lend.x += tj.x;
+          lend.y += tj.y;
+        }
+#pragma unroll
+        for (int J = 0; J < 4; ++J) {
+          if (J > I) {
+            const float2 f = *reinterpret_cast<const float2 *>(first + J * D + c0);
+            rnext[J].x += f.x;
+            rnext[J].y += f.y;
+          }
+        }
+        const float2 fI = *reinterpret_cast<const float2 *>(first + I * D + c0);
+        const float2 r = make_float2(base.x + fI.x, base.y + fI.y);  // the block's first Lam
+        float2 run = base;
+        if (hh) {  // the block's first part
+          const float2 h0 = *reinterpret_cast<const float2 *>(hsum + (PARTS * I) * D + c0);
+          run.x += h0.x;
+          run.y += h0.y;
+        }
+        if (I == 3 && hh == 0)
+          *reinterpret_cast<float2 *>(dec + s * D + c0) = make_float2(__expf(lend.x), __expf(lend.y));
+        float2 ai[TPI];
         if constexpr (KEEP) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ai[i] = av[i];
+          for (int i = 0; i < TPI; ++i) ai[i] = av[i];
         } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ai[i] = log_alpha_at(p, bhL, tok0 + 16 * I + i, ch, D);
+          load_item(tok0, I, cp, hh, ai);
         }
-        // The block's 16 tokens in two halves of 8, so that few values are
-        // live at once and the tokens' independent chains can overlap.
-        if (I == 3) dec[s * D + ch] = __expf(lend);
-        float run = base, r = 0.f, er = 1.f;
+        const float erx = __expf(r.x), ery = __expf(r.y);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float lam[8], qv[8], kv[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            run += ai[8 * hh + i];
-            lam[i] = run;
-            const uint32_t off = tile_off(16 * I + 8 * hh + i, ch, BOX_BYTES);
-            const float a = ld_bf16(qt + off), b = ld_bf16(kt + off);
-            qv[i] = PHI ? elu1_fast(a) : a;
-            kv[i] = PHI ? elu1_fast(b) : b;
+        for (int i = 0; i < TPI; ++i) {
+          run.x += ai[i].x;
+          run.y += ai[i].y;
+          const int row = 16 * I + TPI * hh + i;
+          const uint32_t off = tile_off(row, c0, BOX_BYTES);
+          const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
+          const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
+          float qx = __uint_as_float(qw << 16), qy = __uint_as_float(qw & 0xffff0000u);
+          float kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
+          if (PHI) {
+            qx = elu1_fast(qx);
+            qy = elu1_fast(qy);
+            kx = elu1_fast(kx);
+            ky = elu1_fast(ky);
           }
-          if (hh == 0) {
-            r = lam[0];
-            er = __expf(r);
-          }
+          const float qhx = qx * __expf(run.x - r.x), qhy = qy * __expf(run.y - r.y);  // <= 1
+          *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qhx, qhy);              // Qh
+          *reinterpret_cast<uint32_t *>(xq + off) = pack_bf16(qhx * erx, qhy * ery);  // Qt
+          *reinterpret_cast<uint32_t *>(kt + off) =                                   // Kt
+              pack_bf16(kx * __expf(lend.x - run.x), ky * __expf(lend.y - run.y));
+          *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(I) + row, c0, SM::KBOX)) =  // K^(I)
+              pack_bf16(kx * __expf(fminf(r.x - run.x, kDiagSpanMax)),
+                        ky * __expf(fminf(r.y - run.y, kDiagSpanMax)));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = 16 * I + 8 * hh + i;
-            const uint32_t off = tile_off(row, ch, BOX_BYTES);
-            const float qh = qv[i] * __expf(lam[i] - r);               // <= 1 factor
-            st_bf16(qt + off, qh);                                     // Qh (in place)
-            st_bf16(xq + off, qh * er);                                // Qt = q e^{Lam}
-            st_bf16(kt + off, kv[i] * __expf(lend - lam[i]));          // Kt (in place)
-            st_bf16(xk + tile_off(k_row0(I) + row, ch, SM::KBOX),      // own block of K^(I)
-                    kv[i] * __expf(fminf(r - lam[i], kDiagSpanMax)));
-#pragma unroll
-            for (int J = 0; J < 4; ++J)                                // K^(J), J > I
-              if (J > I)
-                st_bf16(xk + tile_off(k_row0(J) + row, ch, SM::KBOX), kv[i] * __expf(rnext[J] - lam[i]));
-          }
+          for (int J = 0; J < 4; ++J)                                                  // K^(J), J > I
+            if (J > I)
+              *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(J) + row, c0, SM::KBOX)) =
+                  pack_bf16(kx * __expf(rnext[J].x - run.x), ky * __expf(rnext[J].y - run.y));
         }
-        if (r - run > kDiagSpanMax) flag[s] = 1u;
+        // The block's largest span sits at its last token (its last part).
+        if (hh == PARTS - 1 && fmaxf(r.x - run.x, r.y - run.y) > kDiagSpanMax) flag[s] = 1u;
       }
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
