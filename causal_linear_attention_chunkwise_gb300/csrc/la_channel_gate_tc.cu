@@ -74,7 +74,9 @@ constexpr uint32_t BAR_PREP = 1, BAR_EPI = 2, BAR_ST = 3;
 
 template <int D>
 struct CgSmem {
-  static constexpr int NST = D == 64 ? 4 : 2;   // q | k | v stages
+  // d = 64 gives a fourth stage's room to the next chunk's log decays (LAPF).
+  static constexpr int NST = D == 64 ? 3 : 2;   // q | k | v stages
+  static constexpr bool LAPF = D == 64;
   static constexpr int NX = D == 64 ? 2 : 1;    // Qt and K^(I) buffers
   static constexpr int NP = D == 64 ? 2 : 1;    // bf16 P tiles
   static constexpr int NO = D == 64 ? 2 : 1;    // O staging tiles
@@ -97,7 +99,8 @@ struct CgSmem {
   static constexpr int PARTS = D == 64 ? 2 : 1;
   static constexpr uint32_t OFF_TOT = OFF_DEC + NST * D * 4;  // [4 PARTS][D] part sums
   static constexpr uint32_t OFF_FIRST = OFF_TOT + 4 * PARTS * D * 4;  // [4][D] first log decays
-  static constexpr uint32_t OFF_EX = OFF_FIRST + 4 * D * 4; // [16][16] exact diagonal scores
+  static constexpr uint32_t OFF_LA = OFF_FIRST + 4 * D * 4;  // LAPF: [64][D] fp32, next chunk
+  static constexpr uint32_t OFF_EX = OFF_LA + (LAPF ? 64 * D * 4 : 0);  // [16][16] exact diagonal scores
   static constexpr uint32_t OFF_FLAG = OFF_EX + 256 * 4;    // [NST] span exceeded
   static constexpr uint32_t OFF_BAR = OFF_FLAG + 16;
   static constexpr int NBAR = 3 * NST + NX + 2 + NP + 2 + 2 + 2 + 1;
@@ -412,6 +415,34 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                          : make_float2(0.f, 0.f);  // padding decays nothing
       }
     };
+    // LAPF: each thread copies its own items' log decays of a chunk into the
+    // [64][D] buffer asynchronously, one chunk ahead, and reads back only what
+    // it copied (after cp.async.wait_group): no barrier is involved.
+    float *labuf = reinterpret_cast<float *>(smem + SM::OFF_LA);
+    auto prefetch = [&](int tok0) {
+      for (int it = t; it < NITEM; it += kPrepThreads) {
+        int I, cp, hh;
+        item_of(it, I, cp, hh);
+#pragma unroll
+        for (int i = 0; i < TPI; ++i) {
+          const int row = 16 * I + TPI * hh + i, tok = tok0 + row;
+          float *dst = labuf + row * D + 2 * cp;
+          if (tok < p.L)
+            cp_async_8(dst, p.log_alpha + (bhL + tok) * D + 2 * cp);
+          else
+            *reinterpret_cast<float2 *>(dst) = make_float2(0.f, 0.f);  // padding decays nothing
+        }
+      }
+      cp_async_commit();
+    };
+    auto read_item = [&](int I, int cp, int hh, float2 (&a)[TPI]) {
+#pragma unroll
+      for (int i = 0; i < TPI; ++i)
+        a[i] = *reinterpret_cast<const float2 *>(labuf + (16 * I + TPI * hh + i) * D + 2 * cp);
+    };
+    if constexpr (SM::LAPF) {
+      if (nc > 0) prefetch(0);
+    }
     float2 av[TPI];
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
@@ -419,11 +450,15 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       const int tok0 = c * CH;
       // Half-block sums and blocks' first log decays: they do not need the
       // stage, so their loads go out while the chunk's tiles are arriving.
+      if constexpr (SM::LAPF) cp_async_wait<0>();  // this chunk's copies, issued a chunk ago
       for (int it = t; it < NITEM; it += kPrepThreads) {
         int I, cp, hh;
         item_of(it, I, cp, hh);
         float2 a[TPI];
-        load_item(tok0, I, cp, hh, a);
+        if constexpr (SM::LAPF)
+          read_item(I, cp, hh, a);
+        else
+          load_item(tok0, I, cp, hh, a);
         float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < TPI; ++i) {
@@ -436,6 +471,11 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
           for (int i = 0; i < TPI; ++i) av[i] = a[i];
         }
+      }
+      // The next chunk's copies overwrite what this thread has just read (its
+      // values are consumed above, so those reads have completed).
+      if constexpr (SM::LAPF) {
+        if (c + 1 < nc) prefetch(tok0 + CH);
       }
       if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
       LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);

@@ -377,6 +377,10 @@ __device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src)
                "l"(gmem_src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async_8(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
