@@ -482,6 +482,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (t == 0) flag[s] = 0;
       named_bar_sync(BAR_PREP, kPrepThreads);
       if (c >= NX && !(ok = gwait(&xfree[xb], ((c / NX) - 1) & 1, 8))) break;
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 9, c);
       unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
       unsigned char *xq = smem + SM::OFF_X + xb * SM::XBUF, *xk = xq + SM::TILE;
       for (int it = t; it < NITEM; it += kPrepThreads) {

@@ -229,7 +229,10 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         if (c >= NST) LA_TRACE_EVENT(st_on, st_t0, 4, c - NST);
         unsigned char *st = smem + s * SM::STAGE;
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
-        const int tok = tok0 + c * CH;
+        // The segment's chunks last first: when the pass ends, the K and V
+        // tiles still in L2 are those of the segments' first chunks, which
+        // the output kernel's first blocks read first.
+        const int tok = tok0 + (nc - 1 - c) * CH;
         for (int b = 0; b < D / BOX; ++b) {
           if (!LA_CHK(b * BOX + BOX <= D && tok < p.L && bh < p.BH, KID_PREFILL_TC_STATE, 1))
             continue;
@@ -320,7 +323,7 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       LA_TRACE_EVENT(st_on && t == 0, st_t0, 1, c);
       unsigned char *kt = smem + s * SM::STAGE;
       LA_TRACE_EVENT(st_on && t == 0, st_t0, 5, c);
-      const float *w = suf + c * CH;
+      const float *w = suf + (nc - 1 - c) * CH;  // the chunk's tokens (chunks last first)
       if constexpr (phi || scale)
         tile_pass<D, 1, phi, scale>(kt, [w](int, int r) { return w[r]; }, t, 128);
       LA_TRACE_EVENT(st_on && t == 0, st_t0, 6, c);
