@@ -499,10 +499,18 @@ struct OutSmem {
 };
 
 // Warps: 0 TMA, 1 MMA, 2-7 PREP (192 threads), 8-11 WG2, 12-15 WG3.
-constexpr int kThreadsOut = 512;
 constexpr int W_PREP = 2, kPrepThreads = 192;
 constexpr int WG3 = 12;
 constexpr uint32_t BAR_PREP = 1, BAR_WG3 = 3;
+// d = 64 without decay or z: a fifth warpgroup (warps 16-19, WG4) takes the O
+// epilogue from WG2, whose two epilogues otherwise set the chunk period.  The
+// other forms use more registers than 640 threads leave (at most 102 each).
+template <int DK, bool DECAY, bool NORM>
+constexpr bool kOutWG4 = DK == 64 && !DECAY && !NORM;
+template <int DK, bool DECAY, bool NORM>
+constexpr int kThreadsOut = kOutWG4<DK, DECAY, NORM> ? 640 : 512;
+constexpr int WG4 = 16;
+constexpr uint32_t BAR_WG4 = 4;
 
 // Decay of a chunk with total log decay A, reference r = A/2.  Split form:
 // the decay between tokens i >= j, exp(Lam_i - Lam_j) = exp(Lam_i - r) *
@@ -575,7 +583,7 @@ struct Streams {
 };
 
 template <int DK, bool PHI, bool DECAY, bool NORM = false>
-__global__ void __launch_bounds__(kThreadsOut, 1)
+__global__ void __launch_bounds__((kThreadsOut<DK, DECAY, NORM>), 1)
 chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV,
@@ -680,6 +688,109 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   (void)trace_on;
   (void)t0;
 
+  float *ofr = reinterpret_cast<float *>(smem + SM::OFF_OFR);  // [2][64] (TRANS)
+  // The O epilogue of virtual chunk k, run by one warpgroup (t = 0..127 within
+  // it, its lane quarter, its named barrier): WG2, or WG4 where there is one.
+  auto o_epilogue_by = [&](int k, int t, int quarter, uint32_t bar) -> bool {
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int b = k & 1;
+    if (!wait_wg(&o_full[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, bar))
+      return false;
+    tc_fence_after();
+    if (t == 0) tma_store_wait_read<SM::NOB - 1>();  // the store that used this buffer is done
+    __syncwarp();
+    named_bar_sync(bar, 128);
+    unsigned char *o_sm = smem + SM::OFF_O + (b % SM::NOB) * SM::TILE;
+    if constexpr (SM::TRANS) {
+      // O^T: TMEM lanes are value columns, columns the chunk's 64 tokens.
+      // Per 16 lanes (16x256b loads), each 8x8 block (8 value columns x 8
+      // tokens) is scaled by its tokens' factors, packed to bf16 and stored
+      // transposed (stmatrix .trans): one 16-byte chunk of a token's row of
+      // the swizzled staging tile per stored row.
+      const int tq = lane & 3;
+      float2 fq[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        fq[q] = DECAY ? *reinterpret_cast<const float2 *>(ofr + b * 64 + 8 * q + 2 * tq)
+                      : make_float2(1.f, 1.f);
+      const uint32_t o_base = smem_u32(o_sm);
+#pragma unroll 1
+      for (int g = 0; g < 2; ++g) {
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld_16x256b_x8(tmem + ((uint32_t)(quarter * 32 + 16 * g) << 16) + SM::T_O +
+                               SM::T_OW * b,
+                           r);
+        tmem_ld_wait();
+        uint32_t pa[8], pb[8];  // value rows 0-7 and 8-15 of the 16, per token chunk
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          pa[q] = pack_bf16(__uint_as_float(r[4 * q]) * fq[q].x,
+                            __uint_as_float(r[4 * q + 1]) * fq[q].y);
+          pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]) * fq[q].x,
+                            __uint_as_float(r[4 * q + 3]) * fq[q].y);
+        }
+#pragma unroll
+        for (int qq = 0; qq < 8; qq += 2) {
+          // matrices (qq, rows 0-7), (qq, 8-15), (qq+1, 0-7), (qq+1, 8-15)
+          const int mi = lane >> 3, tok = 8 * (qq + (mi >> 1)) + (lane & 7);
+          const int dv0 = quarter * 32 + 16 * g + 8 * (mi & 1);
+          const uint32_t addr = o_base + (dv0 >> 6) * BOX_BYTES + tok * 128 +
+                                ((((dv0 & 63) >> 3) ^ (tok & 7)) << 4);
+          stmatrix_x4_trans(addr, pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
+        }
+      }
+    } else {
+      // O has M = 64 as P: 16x256b loads, the rows' output factors, stmatrix.
+      const int ra = 16 * quarter + (lane >> 2);
+      float fa = DECAY ? ofr[b * 64 + ra] : 1.f, fb = DECAY ? ofr[b * 64 + ra + 8] : 1.f;
+      if constexpr (NORM) {
+        // The denominator rides in O's column DK (the ones column), with the
+        // same output row factor as the numerator: the factor cancels.
+        uint32_t dr[4];
+        __syncwarp();
+        tmem_ld_16x256b_x1(tmem + lane_off + SM::T_O + SM::T_OW * b + DK, dr);
+        tmem_ld_wait();
+        fa = 1.f / __shfl_sync(0xffffffffu, __uint_as_float(dr[0]), lane & ~3);
+        fb = 1.f / __shfl_sync(0xffffffffu, __uint_as_float(dr[2]), lane & ~3);
+      }
+      const int mi = lane >> 3, srow = 16 * quarter + 8 * (mi & 1) + (lane & 7);
+#pragma unroll 1
+      for (int col = 0; col < DK; col += 64) {
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld_16x256b_x8(tmem + lane_off + SM::T_O + SM::T_OW * b + col, r);
+        tmem_ld_wait();
+        uint32_t pa[8], pb[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          pa[q] = pack_bf16(__uint_as_float(r[4 * q]) * fa, __uint_as_float(r[4 * q + 1]) * fa);
+          pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]) * fb, __uint_as_float(r[4 * q + 3]) * fb);
+        }
+        const uint32_t rbase = smem_u32(o_sm) + (col / 64) * BOX_BYTES + srow * 128;
+#pragma unroll
+        for (int qq = 0; qq < 8; qq += 2) {
+          const int q = qq + (mi >> 1);
+          stmatrix_x4(rbase + ((q ^ (srow & 7)) << 4), pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(bar, 128);
+    if (t == 0) {
+      mbar_arrive(&o_free[b]);
+      int sg, c;
+      st.at(k, sg, c);
+      const int tok = tok0[sg] + c * CH;
+      for (int bb = 0; bb < DK / BOX; ++bb)
+        if (LA_CHK(bb * BOX + BOX <= DK && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 3))
+          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok, bh);
+      tma_store_commit();
+      LA_TRACE_EVENT(trace_on, t0, 12, k);
+    }
+    return true;
+  };
   if (warp == W_TMA) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -1022,7 +1133,6 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int t = tid - WG2 * 32;
     const int quarter = warp & 3;
     const int row = acc_row<64>(quarter, lane);   // row within the chunk
-    float *ofr = reinterpret_cast<float *>(smem + SM::OFF_OFR);  // [2][64] (TRANS)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     auto p_epilogue = [&](int k) -> bool {
       const int s = k % NST, b = k & 1;
@@ -1075,111 +1185,20 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
       LA_TRACE_EVENT(trace_on && t == 0, t0, 4, k);
       return true;
     };
-    auto o_epilogue = [&](int k) -> bool {
-      const int b = k & 1;
-      if (!wait_wg(&o_full[b], (k >> 1) & 1, ctl, p.err, KID_PREFILL_TC_OUT, 11, BAR_WG2))
-        return false;
-      tc_fence_after();
-      if (t == 0) tma_store_wait_read<SM::NOB - 1>();  // the store that used this buffer is done
-      __syncwarp();
-      named_bar_sync(BAR_WG2, 128);
-      unsigned char *o_sm = smem + SM::OFF_O + (b % SM::NOB) * SM::TILE;
-      if constexpr (SM::TRANS) {
-        // O^T: TMEM lanes are value columns, columns the chunk's 64 tokens.
-        // Per 16 lanes (16x256b loads), each 8x8 block (8 value columns x 8
-        // tokens) is scaled by its tokens' factors, packed to bf16 and stored
-        // transposed (stmatrix .trans): one 16-byte chunk of a token's row of
-        // the swizzled staging tile per stored row.
-        const int tq = lane & 3;
-        float2 fq[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          fq[q] = DECAY ? *reinterpret_cast<const float2 *>(ofr + b * 64 + 8 * q + 2 * tq)
-                        : make_float2(1.f, 1.f);
-        const uint32_t o_base = smem_u32(o_sm);
-#pragma unroll 1
-        for (int g = 0; g < 2; ++g) {
-          __syncwarp();
-          uint32_t r[32];
-          tmem_ld_16x256b_x8(tmem + ((uint32_t)(quarter * 32 + 16 * g) << 16) + SM::T_O +
-                                 SM::T_OW * b,
-                             r);
-          tmem_ld_wait();
-          uint32_t pa[8], pb[8];  // value rows 0-7 and 8-15 of the 16, per token chunk
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            pa[q] = pack_bf16(__uint_as_float(r[4 * q]) * fq[q].x,
-                              __uint_as_float(r[4 * q + 1]) * fq[q].y);
-            pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]) * fq[q].x,
-                              __uint_as_float(r[4 * q + 3]) * fq[q].y);
-          }
-#pragma unroll
-          for (int qq = 0; qq < 8; qq += 2) {
-            // matrices (qq, rows 0-7), (qq, 8-15), (qq+1, 0-7), (qq+1, 8-15)
-            const int mi = lane >> 3, tok = 8 * (qq + (mi >> 1)) + (lane & 7);
-            const int dv0 = quarter * 32 + 16 * g + 8 * (mi & 1);
-            const uint32_t addr = o_base + (dv0 >> 6) * BOX_BYTES + tok * 128 +
-                                  ((((dv0 & 63) >> 3) ^ (tok & 7)) << 4);
-            stmatrix_x4_trans(addr, pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
-          }
-        }
-      } else {
-        // O has M = 64 as P: 16x256b loads, the rows' output factors, stmatrix.
-        const int ra = 16 * quarter + (lane >> 2);
-        float fa = DECAY ? ofr[b * 64 + ra] : 1.f, fb = DECAY ? ofr[b * 64 + ra + 8] : 1.f;
-        if constexpr (NORM) {
-          // The denominator rides in O's column DK (the ones column), with the
-          // same output row factor as the numerator: the factor cancels.
-          uint32_t dr[4];
-          __syncwarp();
-          tmem_ld_16x256b_x1(tmem + lane_off + SM::T_O + SM::T_OW * b + DK, dr);
-          tmem_ld_wait();
-          fa = 1.f / __shfl_sync(0xffffffffu, __uint_as_float(dr[0]), lane & ~3);
-          fb = 1.f / __shfl_sync(0xffffffffu, __uint_as_float(dr[2]), lane & ~3);
-        }
-        const int mi = lane >> 3, srow = 16 * quarter + 8 * (mi & 1) + (lane & 7);
-#pragma unroll 1
-        for (int col = 0; col < DK; col += 64) {
-          __syncwarp();
-          uint32_t r[32];
-          tmem_ld_16x256b_x8(tmem + lane_off + SM::T_O + SM::T_OW * b + col, r);
-          tmem_ld_wait();
-          uint32_t pa[8], pb[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            pa[q] = pack_bf16(__uint_as_float(r[4 * q]) * fa, __uint_as_float(r[4 * q + 1]) * fa);
-            pb[q] = pack_bf16(__uint_as_float(r[4 * q + 2]) * fb, __uint_as_float(r[4 * q + 3]) * fb);
-          }
-          const uint32_t rbase = smem_u32(o_sm) + (col / 64) * BOX_BYTES + srow * 128;
-#pragma unroll
-          for (int qq = 0; qq < 8; qq += 2) {
-            const int q = qq + (mi >> 1);
-            stmatrix_x4(rbase + ((q ^ (srow & 7)) << 4), pa[qq], pb[qq], pa[qq + 1], pb[qq + 1]);
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar_sync(BAR_WG2, 128);
-      if (t == 0) {
-        mbar_arrive(&o_free[b]);
-        int sg, c;
-        st.at(k, sg, c);
-        const int tok = tok0[sg] + c * CH;
-        for (int bb = 0; bb < DK / BOX; ++bb)
-          if (LA_CHK(bb * BOX + BOX <= DK && tok < p.L && bh < p.BH, KID_PREFILL_TC_OUT, 3))
-            tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, tok, bh);
-        tma_store_commit();
-        LA_TRACE_EVENT(trace_on, t0, 12, k);
-      }
-      return true;
-    };
+    auto o_epilogue = [&](int k) { return o_epilogue_by(k, t, quarter, BAR_WG2); };
     bool ok = true;
+    constexpr bool own_o = !kOutWG4<DK, DECAY, NORM>;
     for (int k = 0; ok && k < nk; ++k) {
       ok = p_epilogue(k);
-      if (ok && k >= 1) ok = o_epilogue(k - 1);
+      if (own_o && ok && k >= 1) ok = o_epilogue(k - 1);
     }
-    if (ok && nk > 0) o_epilogue(nk - 1);
+    if (own_o && ok && nk > 0) o_epilogue(nk - 1);
+    if (own_o && t == 0) tma_store_wait_all();
+  } else if (kOutWG4<DK, DECAY, NORM> && warp >= WG4) {
+    // ------------------------------------------------------------ WG4: O epilogues
+    const int t = tid - WG4 * 32;
+    bool ok = true;
+    for (int k = 0; ok && k < nk; ++k) ok = o_epilogue_by(k, t, warp & 3, BAR_WG4);
     if (t == 0) tma_store_wait_all();
   } else if (warp >= WG3) {
     // ------------------------------------------------------------ WG3: the state chains
@@ -1573,9 +1592,9 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why, const float *z0 = n
   // (its inputs were complete before the segment-state kernel started).  A
   // single segment has no predecessor of its own: ordinary stream order.
   if (pl.n_seg > 1)
-    e = launch_pdl(ko, dim3(BH, out_x), kThreadsOut, OS::BYTES, a.stream, tq, tk, tv, to, p);
+    e = launch_pdl(ko, dim3(BH, out_x), kThreadsOut<D, DECAY, NORM>, OS::BYTES, a.stream, tq, tk, tv, to, p);
   else
-    ko<<<dim3(BH, out_x), kThreadsOut, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
+    ko<<<dim3(BH, out_x), kThreadsOut<D, DECAY, NORM>, OS::BYTES, a.stream>>>(tq, tk, tv, to, p);
   if ((e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) && why)
     *why = "la_chunk_fwd: chunk-output kernel launch";
 #ifdef LA_CHECKED
