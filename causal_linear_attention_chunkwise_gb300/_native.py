@@ -30,7 +30,8 @@ SIGNATURES = {
                                _vp, _vp, _vp, _vp, _sz, _vp]),
     "la_normalised_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "la_channel_gate_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
-                                 _vp]),
+                                 _vp, _sz, _vp]),
+    "la_channel_gate_fwd_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "la_delta_fwd": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "la_device_status": (_i, [_vp]),
     "la_selftest_wait_timeout": (_i, [_u, _vp]),

@@ -258,19 +258,33 @@ def la_normalised_fwd(q, k, v, chunk=64, decay_kind="none", decay=None, S0=None,
     return O, S_final, z_final
 
 
+def la_channel_gate_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk=64, dtype=torch.bfloat16) -> int:
+    return int(_native.load().la_channel_gate_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk,
+                                                                  DTYPE[dtype]))
+
+
 def la_channel_gate_fwd(q, k, v, log_alpha, chunk=64, S0=None, O=None, S_final=None,
-                        want_final_state=True, stream=None):
+                        want_final_state=True, workspace=None, segments=True, stream=None):
     """Per-channel gate S_t = diag(alpha_t) S_{t-1} + phi(k_t) v_t^T with
-    ``log_alpha`` fp32 [B,H,L,d_k].  Returns ``(O, S_final)``."""
+    ``log_alpha`` fp32 [B,H,L,d_k].  Returns ``(O, S_final)``.  With
+    ``segments`` (the default) a cached workspace lets the library run each
+    sequence as several segments side by side; ``segments=False`` runs each
+    sequence in one piece."""
     O = _qkv(q, k, v, O)
     S_final, _ = _state_bufs(q, v, want_final_state, S_final)
     _need_cuda(q, k, v, log_alpha, S0, O, S_final)
     B, H, L, dk = q.shape
+    dv = v.shape[-1]
     if log_alpha.shape != (B, H, L, dk) or log_alpha.dtype != torch.float32:
         raise ValueError("log_alpha must be fp32 [B,H,L,d_k]")
+    if workspace is None and segments:
+        workspace = _workspace(la_channel_gate_fwd_workspace_bytes(B, H, L, dk, dv, chunk, q.dtype),
+                               q.device, stream)
     _check(_native.load().la_channel_gate_fwd(
-        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, v.shape[-1], chunk,
-        _ptr(log_alpha), _ptr(S0), _ptr(O), _ptr(S_final), _stream(stream)))
+        _ptr(q), _ptr(k), _ptr(v), DTYPE[q.dtype], B, H, L, dk, dv, chunk,
+        _ptr(log_alpha), _ptr(S0), _ptr(O), _ptr(S_final), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return O, S_final
 
 

@@ -360,9 +360,16 @@ la_status la_normalised_fwd(const void *q, const void *k, const void *v, int dty
   return ok();
 }
 
+size_t la_channel_gate_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk,
+                                           int dtype) {
+  if (dtype != LA_BF16 || chunk != 64 || d_k != d_v) return 0;
+  return channel_gate_tc_workspace_bytes(B, H, L, d_k);
+}
+
 la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int dtype, int B,
                               int H, int L, int d_k, int d_v, int chunk, const float *log_alpha,
-                              const float *S0, void *O, float *S_final, void *cuda_stream) {
+                              const float *S0, void *O, float *S_final, void *workspace,
+                              size_t ws_bytes, void *cuda_stream) {
   const char *fn = "la_channel_gate_fwd";
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   bool done = false;
@@ -372,8 +379,18 @@ la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int d
   if (!log_alpha) return fail(LA_ERR_INVALID_ARG, "%s: log_alpha must be non-null", fn);
   if (!aligned16(log_alpha))
     return fail(LA_ERR_INVALID_ARG, "%s: log_alpha must start on a 16-byte boundary", fn);
+  if (workspace) {
+    const size_t need = la_channel_gate_fwd_workspace_bytes(B, H, L, d_k, d_v, chunk, dtype);
+    if (ws_bytes < need)
+      return fail(LA_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                  ws_bytes);
+    if (!aligned16(workspace))
+      return fail(LA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
+  }
   VariantArgs a{VARIANT_CHANNEL_GATE, q, k, v, dtype, B, H, L, d_k, d_v, chunk, g_phi.load(),
                 log_alpha, nullptr, S0, O, S_final, st};
+  a.workspace = workspace;
+  a.ws_bytes = workspace ? ws_bytes : 0;
   return run_variant(fn, a);
 }
 

@@ -36,6 +36,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "../../include/la_gb300.h"
@@ -122,10 +123,13 @@ __host__ __device__ constexpr int k_row0(int I) { return I == 3 ? 0 : I == 2 ? 6
 
 struct CgParams {
   int H, L, BH, n_chunks;
+  int seg_chunks, n_seg;   // segments of a sequence (one without a workspace)
   const float *log_alpha;  // [BH][L][D]
   const __nv_bfloat16 *q, *k;
   const float *S0;
   float *S_final;
+  float *ws_state;         // [BH][NS][D][D]: slot s = incoming state of segment s
+  float *ws_logdec;        // [BH][NS][D]: segment s's total log decay per key channel
   unsigned int *err;
 };
 
@@ -215,10 +219,18 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x;
-  const int nc = p.n_chunks;
+  // Grid (B*H, segments): a CTA runs one segment of a sequence from its
+  // incoming state (S0, or the scanned workspace slot).
+  const int bh = blockIdx.x, seg = blockIdx.y;
+  const int cbase = seg * p.seg_chunks;
+  const int nc = min(p.seg_chunks, p.n_chunks - cbase);
   const size_t bhL = (size_t)bh * p.L;
-  const bool trace_on = blockIdx.x == 0;
+  const float *S_in = p.n_seg > 1
+                          ? (seg > 0 || p.S0 ? p.ws_state + ((size_t)bh * p.n_seg + seg) * D * D
+                                             : nullptr)
+                          : (p.S0 ? p.S0 + (size_t)bh * D * D : nullptr);
+  const bool last_seg = seg == p.n_seg - 1;
+  const bool trace_on = blockIdx.x == 0 && blockIdx.y == 0;
   const long long t0 = clock64();
   (void)trace_on;
   (void)t0;
@@ -267,7 +279,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           break;
         unsigned char *stg = smem + s * SM::STAGE;
         mbar_arrive_expect_tx(&full[s], SM::STAGE);
-        const int tok = c * CH;
+        const int tok = (cbase + c) * CH;
         for (int b = 0; b < D / BOX; ++b) {
           tma_load_3d(stg + b * BOX_BYTES, &tmQ, &full[s], b * BOX, tok, bh);
           tma_load_3d(stg + SM::TILE + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
@@ -441,13 +453,13 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         a[i] = *reinterpret_cast<const float2 *>(labuf + (16 * I + TPI * hh + i) * D + 2 * cp);
     };
     if constexpr (SM::LAPF) {
-      if (nc > 0) prefetch(0);
+      if (nc > 0) prefetch(cbase * CH);
     }
     float2 av[TPI];
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST, xb = c % NX;
-      const int tok0 = c * CH;
+      const int tok0 = (cbase + c) * CH;
       // Half-block sums and blocks' first log decays: they do not need the
       // stage, so their loads go out while the chunk's tiles are arriving.
       if constexpr (SM::LAPF) cp_async_wait<0>();  // this chunk's copies, issued a chunk ago
@@ -615,7 +627,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       if (flag[s]) {
         named_bar_sync(BAR_EPI, 128);
-        exact_diagonal<D, PHI>(p, bh, c * CH, pt, ex, t);
+        exact_diagonal<D, PHI>(p, bh, (cbase + c) * CH, pt, ex, t);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -659,7 +671,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (t == 0) {
         mbar_arrive(&o_free[b]);
         for (int bb = 0; bb < D / BOX; ++bb)
-          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, c * CH, bh);
+          tma_store_3d(&tmO, o_sm + bb * BOX_BYTES, bb * BOX, (cbase + c) * CH, bh);
         tma_store_commit();
       }
       return true;
@@ -680,14 +692,14 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto swait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_wg(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_ST);
     };
-    // S0 (or zeros) into TMEM.
+    // The incoming state (or zeros) into TMEM.
 #pragma unroll 1
     for (int col = 0; col < D; col += 32) {
       uint32_t r[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) r[j] = 0u;
-      if (srow >= 0 && p.S0) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.S0 + ((size_t)bh * D + srow) * D + col);
+      if (srow >= 0 && S_in) {
+        const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float4 f = src[j];
@@ -736,7 +748,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (t == 0) mbar_arrive(s_ready);
       LA_TRACE_EVENT(trace_on && t == 0, t0, 8, c);
     }
-    if (ok && nc > 0 && swait(s_done, (nc - 1) & 1, 15) && p.S_final) {
+    if (ok && nc > 0 && last_seg && swait(s_done, (nc - 1) & 1, 15) && p.S_final) {
       tc_fence_after();
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
@@ -765,6 +777,272 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   LA_TRACE_FLUSH(trace_on, &g_trace[0][0]);
 }
 
+// ================================================================ segment states
+// Per (b,h, segment s < NS-1): the segment's own state
+//   dS_s = sum_t diag(w_t) phi(k_t) v_t^T,   w_t[i] = exp(sum_{r > t in s} log alpha_r[i]),
+// the decay from each token to the segment end per key channel, and the
+// segment's total log decay per channel.  The chunks go last first, so each
+// chunk's weights are its in-chunk suffix sums plus a carry (the log decay of
+// the later chunks): no state chain, every MMA accumulates into TMEM.
+template <int D>
+struct CgStateSmem {
+  static constexpr int NST = 2;
+  static constexpr uint32_t TILE = 64 * D * 2;           // K or V, bf16, swizzled boxes
+  static constexpr uint32_t LAT = 64 * D * 4;            // log alpha, fp32 [64][D]
+  static constexpr uint32_t STAGE = 2 * TILE + LAT;      // K | V | log alpha
+  static constexpr uint32_t OFF_OCT = NST * STAGE;       // [8][D] octet sums of the chunk
+  static constexpr uint32_t OFF_CARRY = OFF_OCT + 8 * D * 4;  // [2][D] log decay after the chunk
+  static constexpr uint32_t OFF_BAR = OFF_CARRY + 2 * D * 4;
+  static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
+  static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static_assert(STAGE % 1024 == 0 && TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+};
+
+constexpr int kThreadsCgState = 384;  // warps 0 TMA, 1 MMA, 2-3 idle, 4-11 transform (256)
+constexpr int W_XF = 4, kXfThreads = 256;
+constexpr uint32_t BAR_XF = 5;
+
+template <int D, bool PHI>
+__global__ void __launch_bounds__(kThreadsCgState, 1)
+cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmA, CgParams p) {
+  using SM = CgStateSmem<D>;
+  constexpr int NST = SM::NST;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  float *oct = reinterpret_cast<float *>(smem + SM::OFF_OCT);
+  float *carry = reinterpret_cast<float *>(smem + SM::OFF_CARRY);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
+  uint64_t *empty = full + NST;
+  uint64_t *ready = empty + NST;  // K rows weighted
+  uint64_t *done = ready + NST;   // every MMA finished
+  Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int seg = blockIdx.x, bh = blockIdx.y;
+  const int cbase = seg * p.seg_chunks;
+  const int nc = min(p.seg_chunks, p.n_chunks - cbase);  // full chunks: s < NS-1
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&ready[s], 1);
+    }
+    mbar_init(done, 1);
+    ctl->abort = 0;
+    fence_mbarrier_init();
+  }
+  for (int i = tid; i < D; i += blockDim.x) carry[i] = 0.f;
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, D);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmA);
+      int issued = 0;
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (c >= NST && !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 30))
+          break;
+        unsigned char *st = smem + s * SM::STAGE;
+        mbar_arrive_expect_tx(&full[s], SM::STAGE);
+        const int tok = (cbase + nc - 1 - c) * CH;  // chunks last first
+        for (int b = 0; b < D / BOX; ++b) {
+          tma_load_3d(st + b * BOX_BYTES, &tmK, &full[s], b * BOX, tok, bh);
+          tma_load_3d(st + SM::TILE + b * BOX_BYTES, &tmV, &full[s], b * BOX, tok, bh);
+        }
+        tma_load_3d(st + 2 * SM::TILE, &tmA, &full[s], 0, tok, bh);
+        issued = c + 1;
+      }
+      if (*(volatile uint32_t *)&ctl->abort)
+        for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+      for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(D, D, true, true);
+      for (int c = 0; c < nc; ++c) {
+        const int s = c % NST;
+        if (!wait1(&ready[s], (c / NST) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 31)) break;
+        tc_fence_after();
+        const uint32_t kt = smem_u32(smem + s * SM::STAGE), vt = kt + SM::TILE;
+#pragma unroll
+        for (int kk = 0; kk < CH / 16; ++kk)  // S += K~^T V over the chunk's 64 tokens
+          mma_bf16(tmem, smem_desc_sw128(kt + 2048 * kk, BOX_BYTES, 1024),
+                   smem_desc_sw128(vt + 2048 * kk, BOX_BYTES, 1024), idesc, (c | kk) != 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(done);
+      drain_wait(done, 0);
+    }
+  } else if (warp >= W_XF) {
+    const int t = tid - W_XF * 32;  // 0..255
+    // Items (channel pair cp, octet q of 8 tokens): D/2 x 8 of them.
+    constexpr int NPAIR = D / 2, NITEM = NPAIR * 8;
+    bool ok = true;
+    for (int c = 0; ok && c < nc; ++c) {
+      const int s = c % NST;
+      if (!(ok = wait_grp<kXfThreads>(&full[s], (c / NST) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 32,
+                                      BAR_XF, t)))
+        break;
+      unsigned char *kt = smem + s * SM::STAGE;
+      const float *la = reinterpret_cast<const float *>(kt + 2 * SM::TILE);
+      const float *cin = carry + (c & 1) * D;
+      float *cout = carry + ((c + 1) & 1) * D;
+      for (int it = t; it < NITEM; it += kXfThreads) {  // octet sums
+        const int cp = it % NPAIR, q = it / NPAIR;
+        float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 a = *reinterpret_cast<const float2 *>(la + (8 * q + i) * D + 2 * cp);
+          sum.x += a.x;
+          sum.y += a.y;
+        }
+        *reinterpret_cast<float2 *>(oct + q * D + 2 * cp) = sum;
+      }
+      named_bar_sync(BAR_XF, kXfThreads);
+      for (int it = t; it < NITEM; it += kXfThreads) {  // weights, K rows in place
+        const int cp = it % NPAIR, q = it / NPAIR, c0 = 2 * cp;
+        float2 run = *reinterpret_cast<const float2 *>(cin + c0);  // decay after the chunk
+        float2 tot = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q2 = 0; q2 < 8; ++q2) {
+          const float2 o = *reinterpret_cast<const float2 *>(oct + q2 * D + c0);
+          tot.x += o.x;
+          tot.y += o.y;
+          if (q2 > q) {
+            run.x += o.x;
+            run.y += o.y;
+          }
+        }
+        if (q == 0) {
+          const float2 cc = *reinterpret_cast<const float2 *>(cin + c0);
+          *reinterpret_cast<float2 *>(cout + c0) = make_float2(cc.x + tot.x, cc.y + tot.y);
+        }
+        const uint32_t cbox = (uint32_t)c0 >> 6, cin64 = (uint32_t)c0 & 63u;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {  // token 8 q + i: the decay of the tokens after it
+          const int row = 8 * q + i;
+          const uint32_t off = cbox * BOX_BYTES + sw128_offset((uint32_t)row, cin64);
+          const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
+          float kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
+          if (PHI) {
+            kx = elu1_fast(kx);
+            ky = elu1_fast(ky);
+          }
+          *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kx * __expf(run.x), ky * __expf(run.y));
+          const float2 a = *reinterpret_cast<const float2 *>(la + row * D + c0);
+          run.x += a.x;
+          run.y += a.y;
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_XF, kXfThreads);
+      if (t == 0) mbar_arrive(&ready[s]);
+    }
+    // The accumulated state (warps 4-7: lane quarters 0-3) into slot s+1, and
+    // the segment's total log decay per key channel.
+    if (t < 128 && wait_wg(done, 0, ctl, p.err, KID_CHANNEL_GATE_TC, 33, BAR_XF + 1)) {
+      tc_fence_after();
+      const int quarter = warp & 3;
+      const int row = acc_row<D>(quarter, lane);
+      const size_t slot = (size_t)bh * p.n_seg + seg + 1;
+      float *dst = p.ws_state + slot * D * D;
+#pragma unroll 1
+      for (int col = 0; col < D; col += 32) {
+        __syncwarp();
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, r);
+        tmem_ld_wait();
+        if (row >= 0) {
+          float4 *o = reinterpret_cast<float4 *>(dst + (size_t)row * D + col);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            o[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+      }
+      if (ok)
+        for (int i = t; i < D; i += 128)
+          p.ws_logdec[((size_t)bh * p.n_seg + seg) * D + i] = carry[(nc & 1) * D + i];
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, D);
+  }
+}
+
+// slot 0 <- S0 (or 0); slot s+1 <- diag(exp(A_s)) slot s + slot s+1 (slot s+1
+// holds dS_s on entry), for s < NS-1: a per-row decay.
+__global__ void __launch_bounds__(256)
+cg_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_state,
+               const float *__restrict__ ws_logdec) {
+  const int bh = blockIdx.y;
+  const size_t n4 = (size_t)D * D / 4;
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const int row = (int)(i / (D / 4));
+  float4 *slots = reinterpret_cast<float4 *>(ws_state) + (size_t)bh * n_seg * n4;
+  const float *ld = ws_logdec + (size_t)bh * n_seg * D;
+  float4 cur = S0 ? reinterpret_cast<const float4 *>(S0)[(size_t)bh * n4 + i]
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+  slots[i] = cur;
+  constexpr int kB = 8;
+  for (int s0 = 0; s0 + 1 < n_seg; s0 += kB) {
+    float4 d[kB];
+    float a[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      if (s0 + j + 1 < n_seg) {
+        d[j] = slots[(size_t)(s0 + j + 1) * n4 + i];
+        a[j] = ld[(size_t)(s0 + j) * D + row];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      if (s0 + j + 1 < n_seg) {
+        const float e = __expf(a[j]);
+        cur.x = fmaf(e, cur.x, d[j].x);
+        cur.y = fmaf(e, cur.y, d[j].y);
+        cur.z = fmaf(e, cur.z, d[j].z);
+        cur.w = fmaf(e, cur.w, d[j].w);
+        slots[(size_t)(s0 + j + 1) * n4 + i] = cur;
+      }
+    }
+  }
+}
+
+// Segments per sequence: enough (sequence, segment) blocks to fill the SMs
+// once, at least 8 chunks per segment, and only with a workspace.
+struct CgPlan {
+  int n_chunks, seg_chunks, n_seg;
+};
+CgPlan cg_plan(int B, int H, int L) {
+  const int nc = (L + CH - 1) / CH, BH = B * H;
+  int ns = std::max(1, std::min(sm_count() / std::max(1, BH), nc / 8));
+  const int g = (nc + ns - 1) / ns;
+  ns = (nc + g - 1) / g;
+  return CgPlan{nc, g, ns};
+}
+
+size_t cg_ws_bytes(int B, int H, int L, int D) {
+  const CgPlan pl = cg_plan(B, H, L);
+  if (pl.n_seg <= 1) return 0;
+  const size_t bh = (size_t)B * H, slots = bh * pl.n_seg;
+  return slots * D * D * sizeof(float) + slots * D * sizeof(float);
+}
+
 template <int D, bool PHI>
 cudaError_t launch_cg(const VariantArgs &a) {
   using SM = CgSmem<D>;
@@ -773,7 +1051,15 @@ cudaError_t launch_cg(const VariantArgs &a) {
   p.H = a.H;
   p.L = a.L;
   p.BH = BH;
-  p.n_chunks = (a.L + CH - 1) / CH;
+  const CgPlan pl = cg_plan(a.B, a.H, a.L);
+  const bool segs = pl.n_seg > 1 && a.workspace && a.ws_bytes >= cg_ws_bytes(a.B, a.H, a.L, D);
+  p.n_chunks = pl.n_chunks;
+  p.seg_chunks = segs ? pl.seg_chunks : pl.n_chunks;
+  p.n_seg = segs ? pl.n_seg : 1;
+  if (segs) {
+    p.ws_state = static_cast<float *>(a.workspace);
+    p.ws_logdec = p.ws_state + (size_t)BH * pl.n_seg * D * D;
+  }
   p.log_alpha = a.decay;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.k = static_cast<const __nv_bfloat16 *>(a.k);
@@ -786,11 +1072,25 @@ cudaError_t launch_cg(const VariantArgs &a) {
       !make_tmap_bf16_3d(&tv, a.v, D, a.L, BH, BOX, BOX) ||
       !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX))
     return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (segs) {  // segment states, then their scan (stream order)
+    CUtensorMap ta;
+    if (!make_tmap_f32_3d(&ta, a.decay, D, a.L, BH, D, CH)) return cudaErrorInvalidValue;
+    using SS = CgStateSmem<D>;
+    auto ks = cg_segment_state_kernel<D, PHI>;
+    static int smem_set_state[64];
+    if ((e = set_smem_once(ks, SS::BYTES, smem_set_state)) != cudaSuccess) return e;
+    ks<<<dim3(pl.n_seg - 1, BH), kThreadsCgState, SS::BYTES, a.stream>>>(tk, tv, ta, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int n4 = D * D / 4;
+    cg_scan_kernel<<<dim3((n4 + 255) / 256, BH), 256, 0, a.stream>>>(D, pl.n_seg, a.S0, p.ws_state,
+                                                                   p.ws_logdec);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   auto kern = channel_gate_tc_kernel<D, PHI>;
   static int smem_set[64];
-  cudaError_t e = set_smem_once(kern, SM::BYTES, smem_set);
-  if (e != cudaSuccess) return e;
-  kern<<<BH, kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  if ((e = set_smem_once(kern, SM::BYTES, smem_set)) != cudaSuccess) return e;
+  kern<<<dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -799,6 +1099,11 @@ cudaError_t launch_cg(const VariantArgs &a) {
 bool channel_gate_tc_supported(const VariantArgs &a) {
   return a.form == VARIANT_CHANNEL_GATE && a.dtype == LA_BF16 && a.chunk == CH && a.dk == a.dv &&
          (a.dk == 64 || a.dk == 128);
+}
+
+size_t channel_gate_tc_workspace_bytes(int B, int H, int L, int d) {
+  if (B <= 0 || H <= 0 || L <= 0 || (d != 64 && d != 128)) return 0;
+  return cg_ws_bytes(B, H, L, d);
 }
 
 cudaError_t launch_channel_gate_tc(const VariantArgs &a) {

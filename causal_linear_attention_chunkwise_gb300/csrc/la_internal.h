@@ -84,6 +84,8 @@ struct VariantArgs {
   void *O;
   float *S_final;
   cudaStream_t stream;
+  void *workspace = nullptr;  // channel gate: segment states (optional)
+  size_t ws_bytes = 0;
 };
 cudaError_t launch_variant(const VariantArgs &a);
 
@@ -91,6 +93,8 @@ cudaError_t launch_variant(const VariantArgs &a);
 // {64, 128}; launch_variant takes this path when it applies.
 bool channel_gate_tc_supported(const VariantArgs &a);
 cudaError_t launch_channel_gate_tc(const VariantArgs &a);
+// Workspace for running each sequence as several segments (0: one per sequence).
+size_t channel_gate_tc_workspace_bytes(int B, int H, int L, int d);
 
 // The delta rule a chunk of 64 tokens at a time on the tensor cores (the WY
 // form): bf16, d_k == d_v in {64, 128}; launch_variant takes this path when it

@@ -44,4 +44,21 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
   return r == CUDA_SUCCESS;
 }
 
+// A rank-3 fp32 tensor [d2][d1][d0] (d0 contiguous) read in boxes of box1 rows
+// x box0 columns of one d2 slice, without swizzle (box0 * 4 bytes a multiple of
+// 16, box0 and box1 <= 256): the box lands as dense rows of box0 floats.
+inline bool make_tmap_f32_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
+                             uint64_t d2, uint32_t box0, uint32_t box1) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace la

@@ -223,11 +223,23 @@ size_t la_normalised_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, 
  *   log_alpha  [B,H,L,d_k] fp32, log alpha_t[i] (expected <= 0), 16-byte
  *              aligned like the other tensors                      (read)
  *   S0         [B,H,d_k,d_v] fp32 or NULL;  S_final may alias S0.
+ *   workspace  device scratch of la_channel_gate_fwd_workspace_bytes(...)
+ *              bytes (16-byte aligned), or NULL; ws_bytes = its size.  With it
+ *              (bf16, d_k = d_v in {64, 128}, chunk 64, when the query is not
+ *              0) each sequence is cut into segments that run side by side: a
+ *              state pass per segment, a scan of the segment states, then the
+ *              segments' outputs.  With NULL each sequence runs in one piece.
+ *              A non-NULL workspace smaller than the query or misaligned is
+ *              LA_ERR_INVALID_ARG.  Its contents need no initialisation and are
+ *              not kept.
  */
 la_status la_channel_gate_fwd(const void *q, const void *k, const void *v, int dtype,
                               int B, int H, int L, int d_k, int d_v, int chunk,
                               const float *log_alpha, const float *S0, void *O,
-                              float *S_final, void *cuda_stream);
+                              float *S_final, void *workspace, size_t ws_bytes,
+                              void *cuda_stream);
+size_t la_channel_gate_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, int chunk,
+                                           int dtype);
 
 /*
  * The (gated) delta rule ("Linear / Sparse Attention - minimal runnable

@@ -187,15 +187,28 @@ def test_variant_validation_before_any_device_work(lib):
     assert b"workspace" in lib.la_last_error()
     assert lib.la_normalised_fwd(p, p, p, 1, 4, 16, 4096, 64, 64, 64, 0, None, None, None, p,
                                  None, None, None, 0, None) == 1
-    cg = lambda *a: lib.la_channel_gate_fwd(*a)  # noqa: E731
-    # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, log_alpha, S0, O, S_final, stream)
-    assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, None, None, p, None, None) == 1
+    cg = lambda *a: lib.la_channel_gate_fwd(*a, None, 0, None)  # noqa: E731
+    # (q, k, v, dtype, B, H, L, d_k, d_v, chunk, log_alpha, S0, O, S_final[, workspace,
+    #  ws_bytes, stream])
+    assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, None, None, p, None) == 1
     assert b"log_alpha" in lib.la_last_error()
-    assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, odd, None, p, None, None) == 1
+    assert cg(p, p, p, 1, 1, 1, 8, 16, 16, 64, odd, None, p, None) == 1
     assert b"log_alpha" in lib.la_last_error()
-    assert cg(p, p, p, 1, 1, 1, 8, 16, 256, 64, p, None, p, None, None) == 2
-    assert cg(p, p, p, 1, 1, -1, 8, 16, 16, 64, p, None, p, None, None) == 1
-    assert cg(p, odd, p, 1, 1, 1, 8, 16, 16, 64, p, None, p, None, None) == 1
+    assert cg(p, p, p, 1, 1, 1, 8, 16, 256, 64, p, None, p, None) == 2
+    assert cg(p, p, p, 1, 1, -1, 8, 16, 16, 64, p, None, p, None) == 1
+    assert cg(p, odd, p, 1, 1, 1, 8, 16, 16, 64, p, None, p, None) == 1
+    # the segment workspace: none needed for a short or an unsupported problem; a
+    # given one that is too small or misaligned is refused before any launch
+    need = lib.la_channel_gate_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 1)
+    assert need > 0
+    assert lib.la_channel_gate_fwd_workspace_bytes(1, 1, 300, 64, 64, 64, 1) == 0
+    assert lib.la_channel_gate_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 0) == 0
+    assert lib.la_channel_gate_fwd_workspace_bytes(4, 16, 4096, 64, 64, 32, 1) == 0
+    full = lambda *a: lib.la_channel_gate_fwd(*a)  # noqa: E731
+    assert full(p, p, p, 1, 4, 16, 4096, 64, 64, 64, p, None, p, None, p, need - 1, None) == 1
+    assert b"workspace" in lib.la_last_error()
+    assert full(p, p, p, 1, 4, 16, 4096, 64, 64, 64, p, None, p, None, odd, need, None) == 1
+    assert b"16-byte" in lib.la_last_error()
     dl = lambda *a: lib.la_delta_fwd(*a)  # noqa: E731
     # (q, k, v, dtype, B, H, L, d_k, d_v, beta, log_alpha, S0, O, S_final, stream)
     assert dl(p, p, p, 1, 1, 1, 8, 16, 16, None, None, None, p, None, None) == 1
