@@ -123,15 +123,24 @@ __host__ __device__ constexpr int k_row0(int I) { return I == 3 ? 0 : I == 2 ? 6
 
 struct CgParams {
   int H, L, BH, n_chunks;
-  int seg_chunks, n_seg;   // segments of a sequence (one without a workspace)
+  // Segments of a sequence (one without a workspace): the first has
+  // first_chunks chunks, the others seg_chunks each (the last may have fewer).
+  int first_chunks, seg_chunks, n_seg;
   const float *log_alpha;  // [BH][L][D]
   const __nv_bfloat16 *q, *k;
   const float *S0;
   float *S_final;
-  float *ws_state;         // [BH][NS][D][D]: slot s = incoming state of segment s
+  float *ws_state;         // [BH][NS][D][D]: slot s < NS-1 = segment s's own state;
+                           // slot NS-1 = a copy of S0 when S_final is S0
   float *ws_logdec;        // [BH][NS][D]: segment s's total log decay per key channel
   unsigned int *err;
 };
+
+// First chunk and chunk count of segment seg.
+__device__ __forceinline__ void seg_range(const CgParams &p, int seg, int &c0, int &n) {
+  c0 = seg == 0 ? 0 : p.first_chunks + (seg - 1) * p.seg_chunks;
+  n = min(seg == 0 ? p.first_chunks : p.seg_chunks, p.n_chunks - c0);
+}
 
 // Byte offset of element (row, col) in a bf16 tile of 128-byte swizzled rows
 // whose 64-column boxes are `box` bytes apart.
@@ -220,15 +229,20 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Grid (B*H, segments): a CTA runs one segment of a sequence from its
-  // incoming state (S0, or the scanned workspace slot).
+  // incoming state.
   const int bh = blockIdx.x, seg = blockIdx.y;
-  const int cbase = seg * p.seg_chunks;
-  const int nc = min(p.seg_chunks, p.n_chunks - cbase);
+  int cbase, nc;
+  seg_range(p, seg, cbase, nc);
   const size_t bhL = (size_t)bh * p.L;
-  const float *S_in = p.n_seg > 1
-                          ? (seg > 0 || p.S0 ? p.ws_state + ((size_t)bh * p.n_seg + seg) * D * D
-                                             : nullptr)
-                          : (p.S0 ? p.S0 + (size_t)bh * D * D : nullptr);
+  // The incoming state: S0 folded with the earlier segments' own states (their
+  // per-channel decays applied), for a segment after the first.  S0 is read
+  // from the state pass's copy of it when S_final is the same buffer, so that
+  // the last segment cannot overwrite it before another reads it.
+  const bool alias0 = p.n_seg > 1 && p.S0 && p.S0 == p.S_final;
+  const float *slots = p.n_seg > 1 ? p.ws_state + (size_t)bh * p.n_seg * D * D : nullptr;
+  const float *S_base = alias0 ? slots + (size_t)(p.n_seg - 1) * D * D
+                               : (p.S0 ? p.S0 + (size_t)bh * D * D : nullptr);
+  const bool needs_pass = p.n_seg > 1 && (seg > 0 || alias0);
   const bool last_seg = seg == p.n_seg - 1;
   const bool trace_on = blockIdx.x == 0 && blockIdx.y == 0;
   const long long t0 = clock64();
@@ -692,23 +706,46 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto swait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
       return wait_wg(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_ST);
     };
-    // The incoming state (or zeros) into TMEM.
+    // The incoming state (or zeros) into TMEM.  With segments this kernel is a
+    // programmatic dependent of the state pass, and only this warpgroup reads
+    // its results, so only it waits, and only where it needs them: first
+    // segments run alongside the state pass.
+    if (needs_pass) pdl_wait_previous();
+    const float *ld_row = p.n_seg > 1 ? p.ws_logdec + (size_t)bh * p.n_seg * D + srow : nullptr;
 #pragma unroll 1
     for (int col = 0; col < D; col += 32) {
-      uint32_t r[32];
+      float acc[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) r[j] = 0u;
-      if (srow >= 0 && S_in) {
-        const float4 *src = reinterpret_cast<const float4 *>(S_in + (size_t)srow * D + col);
+      for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+      if (srow >= 0 && S_base) {
+        const float4 *src = reinterpret_cast<const float4 *>(S_base + (size_t)srow * D + col);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const float4 f = src[j];
-          r[4 * j] = __float_as_uint(f.x);
-          r[4 * j + 1] = __float_as_uint(f.y);
-          r[4 * j + 2] = __float_as_uint(f.z);
-          r[4 * j + 3] = __float_as_uint(f.w);
+          acc[4 * j] = f.x;
+          acc[4 * j + 1] = f.y;
+          acc[4 * j + 2] = f.z;
+          acc[4 * j + 3] = f.w;
         }
       }
+      if (srow >= 0) {
+        for (int j2 = 0; j2 < seg; ++j2) {  // S <- diag(e^{A_j}) S + dS_j
+          const float e = __expf(ld_row[(size_t)j2 * D]);
+          const float4 *src =
+              reinterpret_cast<const float4 *>(slots + ((size_t)j2 * D + srow) * D + col);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = src[j];
+            acc[4 * j] = fmaf(e, acc[4 * j], f.x);
+            acc[4 * j + 1] = fmaf(e, acc[4 * j + 1], f.y);
+            acc[4 * j + 2] = fmaf(e, acc[4 * j + 2], f.z);
+            acc[4 * j + 3] = fmaf(e, acc[4 * j + 3], f.w);
+          }
+        }
+      }
+      uint32_t r[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(acc[j]);
       __syncwarp();
       tmem_st32(tmem + lane_off + SM::T_S + col, r);
     }
@@ -818,9 +855,15 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   uint64_t *done = ready + NST;   // every MMA finished
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_launch_dependents();  // the output kernel may start; its later segments wait
   const int seg = blockIdx.x, bh = blockIdx.y;
-  const int cbase = seg * p.seg_chunks;
-  const int nc = min(p.seg_chunks, p.n_chunks - cbase);  // full chunks: s < NS-1
+  if (seg == 0 && p.S0 && p.S0 == p.S_final) {  // S0 aside, for when S_final overwrites it
+    const float4 *src = reinterpret_cast<const float4 *>(p.S0 + (size_t)bh * D * D);
+    float4 *dst = reinterpret_cast<float4 *>(p.ws_state + ((size_t)bh * p.n_seg + p.n_seg - 1) * D * D);
+    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) dst[i] = src[i];
+  }
+  int cbase, nc;  // full chunks: s < NS-1
+  seg_range(p, seg, cbase, nc);
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
@@ -952,7 +995,7 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       tc_fence_after();
       const int quarter = warp & 3;
       const int row = acc_row<D>(quarter, lane);
-      const size_t slot = (size_t)bh * p.n_seg + seg + 1;
+      const size_t slot = (size_t)bh * p.n_seg + seg;  // the segment's own state
       float *dst = p.ws_state + slot * D * D;
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
@@ -983,57 +1026,26 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   }
 }
 
-// slot 0 <- S0 (or 0); slot s+1 <- diag(exp(A_s)) slot s + slot s+1 (slot s+1
-// holds dS_s on entry), for s < NS-1: a per-row decay.
-__global__ void __launch_bounds__(256)
-cg_scan_kernel(int D, int n_seg, const float *S0, float *__restrict__ ws_state,
-               const float *__restrict__ ws_logdec) {
-  const int bh = blockIdx.y;
-  const size_t n4 = (size_t)D * D / 4;
-  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n4) return;
-  const int row = (int)(i / (D / 4));
-  float4 *slots = reinterpret_cast<float4 *>(ws_state) + (size_t)bh * n_seg * n4;
-  const float *ld = ws_logdec + (size_t)bh * n_seg * D;
-  float4 cur = S0 ? reinterpret_cast<const float4 *>(S0)[(size_t)bh * n4 + i]
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-  slots[i] = cur;
-  constexpr int kB = 8;
-  for (int s0 = 0; s0 + 1 < n_seg; s0 += kB) {
-    float4 d[kB];
-    float a[kB];
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      if (s0 + j + 1 < n_seg) {
-        d[j] = slots[(size_t)(s0 + j + 1) * n4 + i];
-        a[j] = ld[(size_t)(s0 + j) * D + row];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      if (s0 + j + 1 < n_seg) {
-        const float e = __expf(a[j]);
-        cur.x = fmaf(e, cur.x, d[j].x);
-        cur.y = fmaf(e, cur.y, d[j].y);
-        cur.z = fmaf(e, cur.z, d[j].z);
-        cur.w = fmaf(e, cur.w, d[j].w);
-        slots[(size_t)(s0 + j + 1) * n4 + i] = cur;
-      }
-    }
-  }
-}
-
 // Segments per sequence: enough (sequence, segment) blocks to fill the SMs
-// once, at least 8 chunks per segment, and only with a workspace.
+// once, at least 8 chunks per segment, and only with a workspace.  The first
+// segments start at once, alongside the state pass; the others wait for the
+// state pass and the scan.  So the first segment is the longer one, by the
+// state pass's cost per chunk relative to the output pass's (kStateShare,
+// measured): f chunks of output take as long as f chunks of state pass plus a
+// later segment's g, i.e. g = (1 - kStateShare) f.
+constexpr double kStateShare = 0.3;
 struct CgPlan {
-  int n_chunks, seg_chunks, n_seg;
+  int n_chunks, first_chunks, seg_chunks, n_seg;
 };
 CgPlan cg_plan(int B, int H, int L) {
   const int nc = (L + CH - 1) / CH, BH = B * H;
-  int ns = std::max(1, std::min(sm_count() / std::max(1, BH), nc / 8));
-  const int g = (nc + ns - 1) / ns;
-  ns = (nc + g - 1) / g;
-  return CgPlan{nc, g, ns};
+  const int ns = std::max(1, std::min(sm_count() / std::max(1, BH), nc / 8));
+  if (ns <= 1) return CgPlan{nc, nc, nc, 1};
+  const double f = nc / (1.0 + (1.0 - kStateShare) * (ns - 1));
+  const int first = std::max(1, std::min(nc - 1, (int)std::lround(f)));
+  const int g = (nc - first + ns - 2) / (ns - 1);
+  const int n_seg = 1 + (nc - first + g - 1) / g;
+  return CgPlan{nc, first, g, n_seg};
 }
 
 size_t cg_ws_bytes(int B, int H, int L, int D) {
@@ -1054,6 +1066,7 @@ cudaError_t launch_cg(const VariantArgs &a) {
   const CgPlan pl = cg_plan(a.B, a.H, a.L);
   const bool segs = pl.n_seg > 1 && a.workspace && a.ws_bytes >= cg_ws_bytes(a.B, a.H, a.L, D);
   p.n_chunks = pl.n_chunks;
+  p.first_chunks = segs ? pl.first_chunks : pl.n_chunks;
   p.seg_chunks = segs ? pl.seg_chunks : pl.n_chunks;
   p.n_seg = segs ? pl.n_seg : 1;
   if (segs) {
@@ -1073,7 +1086,7 @@ cudaError_t launch_cg(const VariantArgs &a) {
       !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX))
     return cudaErrorInvalidValue;
   cudaError_t e;
-  if (segs) {  // segment states, then their scan (stream order)
+  if (segs) {  // the segments' own states first
     CUtensorMap ta;
     if (!make_tmap_f32_3d(&ta, a.decay, D, a.L, BH, D, CH)) return cudaErrorInvalidValue;
     using SS = CgStateSmem<D>;
@@ -1082,15 +1095,15 @@ cudaError_t launch_cg(const VariantArgs &a) {
     if ((e = set_smem_once(ks, SS::BYTES, smem_set_state)) != cudaSuccess) return e;
     ks<<<dim3(pl.n_seg - 1, BH), kThreadsCgState, SS::BYTES, a.stream>>>(tk, tv, ta, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int n4 = D * D / 4;
-    cg_scan_kernel<<<dim3((n4 + 255) / 256, BH), 256, 0, a.stream>>>(D, pl.n_seg, a.S0, p.ws_state,
-                                                                   p.ws_logdec);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   auto kern = channel_gate_tc_kernel<D, PHI>;
   static int smem_set[64];
   if ((e = set_smem_once(kern, SM::BYTES, smem_set)) != cudaSuccess) return e;
-  kern<<<dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  if (segs)
+    e = launch_pdl(kern, dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream, tq, tk, tv, to, p);
+  else
+    kern<<<dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -394,6 +394,24 @@ def test_channel_gate_segments(d, phi, strong):
         parity.check(O.cpu(), O_ref, "bf16", "O")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_channel_gate_segments_final_state_may_alias_initial_state(d):
+    """S_final given as the S0 buffer while the sequence runs as five segments:
+    the first segment and the scan read S0 before the last segment writes it."""
+    B, H, L = 1, 2, 3000
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=60 + d, with_state=True)
+    api.la_set_feature_map("elu1")
+    S = _d(inp["S0"]).clone()
+    O, S_out = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]),
+                                       _d(inp["log_alpha"]), 64, S, S_final=S)
+    api.la_device_status()
+    assert S_out.data_ptr() == S.data_ptr()
+    O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], inp["log_alpha"], phi="elu1",
+                                       S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, "bf16", "O")
+    parity.check(S.cpu(), S_ref, "bf16", "S")
+
+
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 64), ("bf16", 128), ("f32", 16)])
 def test_channel_gate_strong_decay_chunks(dtype, d):
     """Chunks whose cumulative log decay leaves [-80, 80] take the exact
