@@ -403,35 +403,39 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       tc_fence_after();
       const float *lm = lam + s * 64, *bt = bet + s * 64;
       // A (fp32) from G, or P (bf16) from P' into a staging tile (the P tile
-      // itself may still be read by the previous chunk's MMAs); 16 columns
-      // per TMEM load keeps few values live.
+      // itself may still be read by the previous chunk's MMAs).  The M = 64
+      // accumulators keep their rows in 16 lanes of each warp quarter; a
+      // 16x256b load spreads them over all 32 threads: rows ra and ra + 8,
+      // columns 8 q + c2 and + 1 for q = 0..7.
       unsigned char *ps = smem + SM::OFF_PS;
-      const float lr = row >= 0 ? lm[row] : 0.f, br = row >= 0 ? bt[row] : 0.f;
-#pragma unroll 1
-      for (int j0 = 0; j0 < 64; j0 += 16) {
-        uint32_t g[16];
+      {
+        const int ra = 16 * quarter + (lane >> 2), c2 = 2 * (lane & 3);
+        uint32_t g[32];
         __syncwarp();
-        tmem_ld16(tmem + lane_off + SM::T_G + (p_side ? 64 : 0) + j0, g);
+        tmem_ld_16x256b_x8(tmem + lane_off + SM::T_G + (p_side ? 64 : 0), g);
         tmem_ld_wait();
-        LA_TRACE_EVENT(trace_on && t == 0 && j0 < 32, t0, 11 + (j0 >> 4), c);
-        if (row >= 0) {
-          float f[16];
+        const float la = lm[ra], lb = lm[ra + 8], ba = bt[ra], bb = bt[ra + 8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) f[e] = j0 + e <= row ? __expf(lr - lm[j0 + e]) : 0.f;
+        for (int q = 0; q < 8; ++q) {
+          const int j = 8 * q + c2;
+          const float l0 = lm[j], l1 = lm[j + 1];
+          // decay between the rows' tokens and keys j, j + 1 (keys up to the row)
+          const float fa0 = j <= ra ? __expf(la - l0) : 0.f;
+          const float fa1 = j + 1 <= ra ? __expf(la - l1) : 0.f;
+          const float fb0 = j <= ra + 8 ? __expf(lb - l0) : 0.f;
+          const float fb1 = j + 1 <= ra + 8 ? __expf(lb - l1) : 0.f;
+          const float ga0 = __uint_as_float(g[4 * q]), ga1 = __uint_as_float(g[4 * q + 1]);
+          const float gb0 = __uint_as_float(g[4 * q + 2]), gb1 = __uint_as_float(g[4 * q + 3]);
           if (p_side) {
-            uint32_t w8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              w8[e] = pack_bf16(f[2 * e] * __uint_as_float(g[2 * e]), f[2 * e + 1] * __uint_as_float(g[2 * e + 1]));
-            const int ch = j0 >> 3;
-            *reinterpret_cast<uint4 *>(ps + row * 128 + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(w8[0], w8[1], w8[2], w8[3]);
-            *reinterpret_cast<uint4 *>(ps + row * 128 + (((ch + 1) ^ (row & 7)) << 4)) =
-                make_uint4(w8[4], w8[5], w8[6], w8[7]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              As[row * kAS + j0 + e] = j0 + e < row ? br * f[e] * __uint_as_float(g[e]) : 0.f;
+            const uint32_t sw = (uint32_t)((q ^ (ra & 7)) << 4) + (uint32_t)(c2 << 1);
+            // rows ra and ra + 8 share (row & 7), so one swizzle serves both
+            *reinterpret_cast<uint32_t *>(ps + ra * 128 + sw) = pack_bf16(fa0 * ga0, fa1 * ga1);
+            *reinterpret_cast<uint32_t *>(ps + (ra + 8) * 128 + sw) = pack_bf16(fb0 * gb0, fb1 * gb1);
+          } else {  // strictly below the diagonal
+            As[ra * kAS + j] = j < ra ? ba * fa0 * ga0 : 0.f;
+            As[ra * kAS + j + 1] = j + 1 < ra ? ba * fa1 * ga1 : 0.f;
+            As[(ra + 8) * kAS + j] = j < ra + 8 ? bb * fb0 * gb0 : 0.f;
+            As[(ra + 8) * kAS + j + 1] = j + 1 < ra + 8 ? bb * fb1 * gb1 : 0.f;
           }
         }
       }
