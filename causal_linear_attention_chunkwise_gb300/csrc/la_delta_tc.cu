@@ -74,7 +74,7 @@ constexpr int kAS = 65;  // fp32 row stride of the solve's A and T (conflict-fre
 template <int D>
 struct DtSmem {
   static constexpr bool SMALL = D == 64;
-  static constexpr int NST = SMALL ? 2 : 1;   // q | k | v stages (and Kb tiles)
+  static constexpr int NST = SMALL ? 3 : 1;   // q | k | v stages (and Kb tiles)
   static constexpr bool GSEP = SMALL;         // G, P' in their own TMEM columns
   static constexpr uint32_t TILE = 64 * D * 2;
   static constexpr uint32_t STAGE = 3 * TILE;
