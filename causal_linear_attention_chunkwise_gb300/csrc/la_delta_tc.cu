@@ -97,7 +97,7 @@ struct DtSmem {
   static constexpr uint32_t OFF_BETA = OFF_LAM + NST * 64 * 4; // [NST][64] beta
   static constexpr uint32_t OFF_SCR = OFF_BETA + NST * 64 * 4; // 16 floats
   static constexpr uint32_t OFF_BAR = OFF_SCR + 64;
-  static constexpr int NBAR = 4 * NST + 10;
+  static constexpr int NBAR = 4 * NST + 11;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
   static constexpr uint32_t OFF_TRC = OFF_CTL + 64;  // trace builds
   static constexpr uint32_t BYTES = OFF_TRC + trace_smem_bytes();
@@ -169,6 +169,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
   uint64_t *s_done = s_ready + 1;   // the chain's MMAs (and all before) done
   uint64_t *o_free = s_done + 1;    // O read out of TMEM
   uint64_t *drain = o_free + 1;
+  uint64_t *g_free = drain + 1;     // (GSEP) A and P built: G, P' TMEM may be overwritten
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -196,6 +197,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
     mbar_init(s_done, 1);
     mbar_init(o_free, 1);
     mbar_init(drain, 1);
+    mbar_init(g_free, 1);
     ctl->abort = 0;
     fence_mbarrier_init();
   }
@@ -271,6 +273,14 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
         const uint32_t kbo = SM::OFF_KB + s * SM::TILE;
         const uint32_t to = SM::OFF_T, po = SM::OFF_P;
+        // GSEP: the next chunk's G, P' as soon as the solve has read this
+        // chunk's out of TMEM, so that the solve can start it right after this one.
+        if (GSEP && c + 1 < nc) {
+          if (!(ok = w(g_free, c & 1, 5))) break;
+          if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
+          tc_fence_after();
+          issue_g(c + 1);
+        }
         // W = T Kb, U0 = T V (X and Y are free once the previous chunk's M, Qe are out).
         if (!(ok = w(t_ready, c & 1, 3))) break;
         if (c >= 1 && !(ok = w(m_ready, (c - 1) & 1, 4))) break;
@@ -282,11 +292,6 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mma_commit(wu_full);
         LA_TRACE_EVENT(trace_on, t0, 5, c);
-        if (GSEP && c + 1 < nc) {  // the next chunk's G, P' while this one goes on
-          if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
-          tc_fence_after();
-          issue_g(c + 1);
-        }
         // Kt^T W -> X, P W -> Y, O = P U0 (O is free once the previous chunk's O is out).
         if (!(ok = w(wu_ready, c & 1, 6))) break;
         if (!(ok = w(&prep_b[s], (c / NST) & 1, 7))) break;
@@ -441,6 +446,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       }
       tc_fence_before();
       named_bar_sync(BAR_SOLVE, kSolveThreads);
+      if (SM::GSEP && t == 0) mbar_arrive(g_free);  // G, P' read out of TMEM
       LA_TRACE_EVENT(trace_on && t == 0, t0, 13, c);
       // Diagonal 16 x 16 blocks by forward substitution, one column per thread
       // (zero above the diagonal), right-looking: once x_j is final, every
