@@ -268,6 +268,26 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         tc_fence_after();
         issue_g(0);
       }
+      // GSEP: G, P' of chunk g_next may go once the solve has read chunk
+      // g_next - 1's out of TMEM and chunk g_next's prep is done.  The issue is
+      // tried without blocking once this chunk's M, Qe MMAs are out (the solve
+      // of the next chunk has usually built by then), and otherwise made with
+      // blocking waits before this chunk's W, U0.
+      int g_next = 1;
+      auto try_g = [&](bool block) -> bool {
+        if (!GSEP || g_next >= nc) return true;
+        const int k = g_next;
+        if (block) {
+          if (!w(g_free, (k - 1) & 1, 5)) return false;
+          if (!w(&prep_a[k % NST], (k / NST) & 1, 5)) return false;
+        } else if (!mbar_test(g_free, (k - 1) & 1) || !mbar_test(&prep_a[k % NST], (k / NST) & 1)) {
+          return true;
+        }
+        tc_fence_after();
+        issue_g(k);
+        ++g_next;
+        return true;
+      };
       for (int c = 0; ok && c < nc; ++c) {
         const int s = c % NST;
         const uint32_t qo = s * SM::STAGE, ko = qo + SM::TILE, vo = qo + 2 * SM::TILE;
@@ -275,12 +295,8 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         const uint32_t to = SM::OFF_T, po = SM::OFF_P;
         // GSEP: the next chunk's G, P' as soon as the solve has read this
         // chunk's out of TMEM, so that the solve can start it right after this one.
-        if (GSEP && c + 1 < nc) {
-          if (!(ok = w(g_free, c & 1, 5))) break;
-          if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 5))) break;
-          tc_fence_after();
-          issue_g(c + 1);
-        }
+        while (ok && GSEP && g_next <= c + 1 && g_next < nc) ok = try_g(true);
+        if (!ok) break;
         // W = T Kb, U0 = T V (X and Y are free once the previous chunk's M, Qe are out).
         if (!(ok = w(t_ready, c & 1, 3))) break;
         if (c >= 1 && !(ok = w(m_ready, (c - 1) & 1, 4))) break;
@@ -308,9 +324,11 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         }
         mma_commit(m_full);
         LA_TRACE_EVENT(trace_on, t0, 7, c);
+        try_g(false);
         // The state chain.
         if (!(ok = w(m_ready, c & 1, 9))) break;
         if (!(ok = w(s_ready, c & 1, 10))) break;
+        try_g(false);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < CH / 16; ++kk)  // S += Kt^T U0
@@ -326,6 +344,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
         mma_commit(s_done);
         mma_commit(&empty[s]);
         LA_TRACE_EVENT(trace_on, t0, 9, c);
+        try_g(false);
         if (!GSEP && c + 1 < nc) {
           if (!(ok = w(&prep_a[(c + 1) % NST], ((c + 1) / NST) & 1, 11))) break;
           if (!(ok = w(m_ready, c & 1, 12))) break;
