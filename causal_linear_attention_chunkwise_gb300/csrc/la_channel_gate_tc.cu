@@ -428,10 +428,13 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     constexpr int PARTS = SM::PARTS, TPI = 16 / PARTS;
     constexpr int NPAIR = D / 2, NITEM = 4 * PARTS * NPAIR;
     constexpr bool KEEP = NITEM <= kPrepThreads;
+    // Blocks in the order 0, 1, 3, 2: the warps of blocks 0 and 3 (and of 1
+    // and 2) share a scheduler, which evens out the K^(J) copies (3 - I a token).
     auto item_of = [](int it, int &I, int &cp, int &hh) {
       cp = it % NPAIR;
       hh = (it / NPAIR) % PARTS;
       I = it / (PARTS * NPAIR);
+      I ^= I >> 1;
     };
     auto load_item = [&](int tok0, int I, int cp, int hh, float2 (&a)[TPI]) {
 #pragma unroll
@@ -562,35 +565,95 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           load_item(tok0, I, cp, hh, ai);
         }
         const float erx = __expf(r.x), ery = __expf(r.y);
+        // Every key factor e^{x - Lam_t} (x = lend or a later block's r) is
+        // e^{x - r} e^{r - Lam_t}: the first factor is the item's, so a token
+        // takes one exponential for all its key copies and one for its query,
+        // as long as |r - Lam_t| and x - r stay within kDiagSpanMax (always,
+        // for log decays <= 0 and blocks whose span is within it).  An item
+        // past that takes every factor directly, in a loop kept short so that
+        // the rare case adds little code.
+        const float2 eL = make_float2(__expf(lend.x - r.x), __expf(lend.y - r.y));
+        float2 eJ[4];
+        bool item_fast = fmaxf(lend.x - r.x, lend.y - r.y) <= kDiagSpanMax;
 #pragma unroll
-        for (int i = 0; i < TPI; ++i) {
-          run.x += ai[i].x;
-          run.y += ai[i].y;
-          const int row = 16 * I + TPI * hh + i;
-          const uint32_t off = tile_off(row, c0, BOX_BYTES);
+        for (int J = 0; J < 4; ++J) {
+          if (J > I) {
+            eJ[J] = make_float2(__expf(rnext[J].x - r.x), __expf(rnext[J].y - r.y));
+            item_fast = item_fast && fmaxf(rnext[J].x - r.x, rnext[J].y - r.y) <= kDiagSpanMax;
+          }
+        }
+        {
+          float2 rr = run;
+          float m = 0.f;
+#pragma unroll
+          for (int i = 0; i < TPI; ++i) {
+            rr.x += ai[i].x;
+            rr.y += ai[i].y;
+            m = fmaxf(m, fmaxf(fabsf(r.x - rr.x), fabsf(r.y - rr.y)));
+          }
+          item_fast = item_fast && m <= kDiagSpanMax;
+        }
+        auto load_qk = [&](int row, uint32_t off, float &qx, float &qy, float &kx, float &ky) {
           const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
           const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
-          float qx = __uint_as_float(qw << 16), qy = __uint_as_float(qw & 0xffff0000u);
-          float kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
+          qx = __uint_as_float(qw << 16), qy = __uint_as_float(qw & 0xffff0000u);
+          kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
           if (PHI) {
             qx = elu1_fast(qx);
             qy = elu1_fast(qy);
             kx = elu1_fast(kx);
             ky = elu1_fast(ky);
           }
-          const float qhx = qx * __expf(run.x - r.x), qhy = qy * __expf(run.y - r.y);  // <= 1
-          *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qhx, qhy);              // Qh
-          *reinterpret_cast<uint32_t *>(xq + off) = pack_bf16(qhx * erx, qhy * ery);  // Qt
-          *reinterpret_cast<uint32_t *>(kt + off) =                                   // Kt
-              pack_bf16(kx * __expf(lend.x - run.x), ky * __expf(lend.y - run.y));
-          *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(I) + row, c0, SM::KBOX)) =  // K^(I)
-              pack_bf16(kx * __expf(fminf(r.x - run.x, kDiagSpanMax)),
-                        ky * __expf(fminf(r.y - run.y, kDiagSpanMax)));
+        };
+        if (item_fast) {
 #pragma unroll
-          for (int J = 0; J < 4; ++J)                                                  // K^(J), J > I
-            if (J > I)
-              *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(J) + row, c0, SM::KBOX)) =
-                  pack_bf16(kx * __expf(rnext[J].x - run.x), ky * __expf(rnext[J].y - run.y));
+          for (int i = 0; i < TPI; ++i) {
+            run.x += ai[i].x;
+            run.y += ai[i].y;
+            const int row = 16 * I + TPI * hh + i;
+            const uint32_t off = tile_off(row, c0, BOX_BYTES);
+            float qx, qy, kx, ky;
+            load_qk(row, off, qx, qy, kx, ky);
+            const float dx = r.x - run.x, dy = r.y - run.y;  // the block's span so far
+            const float qhx = qx * __expf(-dx), qhy = qy * __expf(-dy);                 // <= 1
+            *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qhx, qhy);              // Qh
+            *reinterpret_cast<uint32_t *>(xq + off) = pack_bf16(qhx * erx, qhy * ery);  // Qt
+            const float kux = kx * __expf(dx), kuy = ky * __expf(dy);
+            *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(I) + row, c0, SM::KBOX)) =  // K^(I)
+                pack_bf16(kux, kuy);
+            *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kux * eL.x, kuy * eL.y);    // Kt
+#pragma unroll
+            for (int J = 0; J < 4; ++J)                                                  // K^(J), J > I
+              if (J > I)
+                *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(J) + row, c0, SM::KBOX)) =
+                    pack_bf16(kux * eJ[J].x, kuy * eJ[J].y);
+          }
+        } else {
+#pragma unroll 1
+          for (int i = 0; i < TPI; ++i) {
+            const int row = 16 * I + TPI * hh + i, tok = tok0 + row;
+            const float2 a = tok < p.L
+                                 ? *reinterpret_cast<const float2 *>(p.log_alpha + (bhL + tok) * D + c0)
+                                 : make_float2(0.f, 0.f);
+            run.x += a.x;
+            run.y += a.y;
+            const uint32_t off = tile_off(row, c0, BOX_BYTES);
+            float qx, qy, kx, ky;
+            load_qk(row, off, qx, qy, kx, ky);
+            const float qhx = qx * __expf(run.x - r.x), qhy = qy * __expf(run.y - r.y);
+            *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qhx, qhy);              // Qh
+            *reinterpret_cast<uint32_t *>(xq + off) = pack_bf16(qhx * erx, qhy * ery);  // Qt
+            *reinterpret_cast<uint32_t *>(kt + off) =                                   // Kt
+                pack_bf16(kx * __expf(lend.x - run.x), ky * __expf(lend.y - run.y));
+            *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(I) + row, c0, SM::KBOX)) =  // K^(I)
+                pack_bf16(kx * __expf(fminf(r.x - run.x, kDiagSpanMax)),
+                          ky * __expf(fminf(r.y - run.y, kDiagSpanMax)));
+#pragma unroll
+            for (int J = 0; J < 4; ++J)                                                // K^(J), J > I
+              if (J > I)
+                *reinterpret_cast<uint32_t *>(xk + tile_off(k_row0(J) + row, c0, SM::KBOX)) =
+                    pack_bf16(kx * __expf(rnext[J].x - run.x), ky * __expf(rnext[J].y - run.y));
+          }
         }
         // The block's largest span sits at its last token (its last part).
         if (hh == PARTS - 1 && fmaxf(r.x - run.x, r.y - run.y) > kDiagSpanMax) flag[s] = 1u;
