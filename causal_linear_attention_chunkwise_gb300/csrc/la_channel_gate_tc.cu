@@ -64,6 +64,10 @@ using namespace tc;
 // Largest within-block decay span (in log space) whose key factors e^{span}
 // stay far from fp32 and bf16 overflow in the factored scores.
 constexpr float kDiagSpanMax = 80.f;
+// Largest fall of Lam through a chunk (per key channel) for which the chunk
+// takes one reference point per channel instead of one per 16-token block:
+// its query and key factors then stay within e^{40}.
+constexpr float kChunkSpanMax = 80.f;
 
 // Warp roles: 0 TMA, 1 MMA, 2..11 PREP (320 threads), 12..15 EPI (P and O
 // epilogues), 16..19 ST (the state chain).  The two TMEM warpgroups start at a
@@ -75,7 +79,7 @@ constexpr uint32_t BAR_PREP = 1, BAR_EPI = 2, BAR_ST = 3;
 
 template <int D>
 struct CgSmem {
-  // d = 64 gives a fourth stage's room to the next chunk's log decays (LAPF).
+  // d = 64 has room for two log decay tiles, loaded by TMA ahead of PREP (LAPF).
   static constexpr int NST = D == 64 ? 3 : 2;   // q | k | v stages
   static constexpr bool LAPF = D == 64;
   static constexpr int NX = D == 64 ? 2 : 1;    // Qt and K^(I) buffers
@@ -83,10 +87,11 @@ struct CgSmem {
   static constexpr int NO = D == 64 ? 2 : 1;    // O staging tiles
   static constexpr uint32_t TILE = 64 * D * 2;  // [64 tokens][D] bf16 in D/64 boxes of 8 KB
   static constexpr uint32_t STAGE = 3 * TILE;
-  // K^(I) region: K^(3) rows 0..63, K^(2) rows 64..111, K^(1) 112..143,
-  // K^(0) 144..159; each MMA reads 64 rows from its first (rows past a copy's
-  // keys are masked out of P), so the region holds 144 + 64 rows.
-  static constexpr int KROWS = 208;
+  // K^(I) region: K^(0) rows 0..15, K^(1) 16..47, K^(2) 48..95, K^(3)
+  // 96..159; each MMA reads 64 rows from its copy's first (rows past a copy's
+  // keys are masked out of P), the last copy's exactly.  The one-reference
+  // form keeps its Ko in rows 0..63.
+  static constexpr int KROWS = 160;
   static constexpr uint32_t KBOX = KROWS * 128;  // one 64-channel box of the region
   static constexpr uint32_t XBUF = TILE + (D / 64) * KBOX;  // Qt, then the K^(I) region
   static constexpr uint32_t S_BLOCK = D * 128;              // [D][64] bf16 block of S
@@ -100,11 +105,14 @@ struct CgSmem {
   static constexpr int PARTS = D == 64 ? 2 : 1;
   static constexpr uint32_t OFF_TOT = OFF_DEC + NST * D * 4;  // [4 PARTS][D] part sums
   static constexpr uint32_t OFF_FIRST = OFF_TOT + 4 * PARTS * D * 4;  // [4][D] first log decays
-  static constexpr uint32_t OFF_LA = OFF_FIRST + 4 * D * 4;  // LAPF: [64][D] fp32, next chunk
-  static constexpr uint32_t OFF_EX = OFF_LA + (LAPF ? 64 * D * 4 : 0);  // [16][16] exact diagonal scores
+  static constexpr uint32_t LA_TILE = 64 * D * 4;          // [64 tokens][D] fp32 log decays
+  static constexpr uint32_t OFF_LA = OFF_FIRST + 4 * D * 4;  // LAPF: [2] log decay tiles
+  static constexpr uint32_t OFF_EX = OFF_LA + (LAPF ? 2 * LA_TILE : 0);  // [16][16] exact diagonal scores
   static constexpr uint32_t OFF_FLAG = OFF_EX + 256 * 4;    // [NST] span exceeded
-  static constexpr uint32_t OFF_BAR = OFF_FLAG + 16;
-  static constexpr int NBAR = 3 * NST + NX + 2 + NP + 2 + 2 + 2 + 1;
+  static constexpr uint32_t OFF_MODE = OFF_FLAG + 16;       // [NST] one reference (1) or blocks (0)
+  static constexpr uint32_t OFF_EM = OFF_MODE + 16;         // [NST][D] e^{m}: the state's row scale
+  static constexpr uint32_t OFF_BAR = OFF_EM + NST * D * 4;
+  static constexpr int NBAR = 3 * NST + NX + 2 + NP + 2 + 2 + 2 + 1 + 4;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * NBAR;
   static constexpr int kTraceShrink = D == 64 ? 1 : 16;  // trace builds: chunks kept
   static constexpr uint32_t OFF_TRC = OFF_CTL + 64;
@@ -119,7 +127,7 @@ struct CgSmem {
 };
 
 // First row of K^(I) in the K^(I) region.
-__host__ __device__ constexpr int k_row0(int I) { return I == 3 ? 0 : I == 2 ? 64 : I == 1 ? 112 : 144; }
+__host__ __device__ constexpr int k_row0(int I) { return I == 0 ? 0 : I == 1 ? 16 : I == 2 ? 48 : 96; }
 
 struct CgParams {
   int H, L, BH, n_chunks;
@@ -205,7 +213,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmO, CgParams p) {
+                       const __grid_constant__ CUtensorMap tmO,
+                       const __grid_constant__ CUtensorMap tmA, CgParams p) {
   using SM = CgSmem<D>;
   constexpr int NST = SM::NST, NX = SM::NX, NP = SM::NP, NO = SM::NO;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -214,6 +223,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   float *first = reinterpret_cast<float *>(smem + SM::OFF_FIRST);
   float *ex = reinterpret_cast<float *>(smem + SM::OFF_EX);
   volatile uint32_t *flag = reinterpret_cast<volatile uint32_t *>(smem + SM::OFF_FLAG);
+  volatile uint32_t *mode = reinterpret_cast<volatile uint32_t *>(smem + SM::OFF_MODE);
+  float *emv = reinterpret_cast<float *>(smem + SM::OFF_EM);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
   uint64_t *prep = empty + NST;     // [NST] scaled operands, factors and flag ready
@@ -225,6 +236,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   uint64_t *s_ready = o_free + 2;   // bf16 S_c in smem, TMEM S = diag(e^{Lam_end}) S_c
   uint64_t *s_done = s_ready + 1;   // the update of chunk c (and every MMA before it) done
   uint64_t *drain = s_done + 1;
+  uint64_t *la_full = drain + 1;    // LAPF: [2] log decay tile landed
+  uint64_t *la_empty = la_full + 2; // LAPF: [2] log decay tile read by PREP
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -266,6 +279,10 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     mbar_init(s_ready, 1);
     mbar_init(s_done, 1);
     mbar_init(drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&la_full[i], 1);
+      mbar_init(&la_empty[i], 1);
+    }
     ctl->abort = 0;
     fence_mbarrier_init();
   }
@@ -286,9 +303,18 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmO);
-      int issued = 0;
+      if constexpr (SM::LAPF) tma_prefetch_desc(&tmA);
+      int issued = 0, la_issued = 0;
       for (int c = 0; c < nc; ++c) {
         const int s = c % NST;
+        if constexpr (SM::LAPF) {  // the chunk's log decays, once PREP has read the buffer's last
+          const int lb = c & 1;
+          if (c >= 2 && !wait1(&la_empty[lb], ((c >> 1) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 2))
+            break;
+          mbar_arrive_expect_tx(&la_full[lb], SM::LA_TILE);
+          tma_load_3d(smem + SM::OFF_LA + lb * SM::LA_TILE, &tmA, &la_full[lb], 0, (cbase + c) * CH, bh);
+          la_issued = c + 1;
+        }
         if (c >= NST && !wait1(&empty[s], ((c / NST) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 1))
           break;
         unsigned char *stg = smem + s * SM::STAGE;
@@ -302,14 +328,17 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         issued = c + 1;
         LA_TRACE_EVENT(trace_on, t0, 0, c);
       }
-      if (*(volatile uint32_t *)&ctl->abort)
+      if (*(volatile uint32_t *)&ctl->abort) {
         for (int c = max(0, issued - NST); c < issued; ++c) drain_wait(&full[c % NST], (c / NST) & 1);
+        for (int c = max(0, la_issued - 2); c < la_issued; ++c) drain_wait(&la_full[c & 1], (c >> 1) & 1);
+      }
       for (int c = max(0, nc - NST); c < nc; ++c) drain_wait(&empty[c % NST], (c / NST) & 1);
     }
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nc > 0) {
       constexpr uint32_t id_p = idesc_bf16_f32(64, 16, false, false);
+      constexpr uint32_t id_p64 = idesc_bf16_f32(64, 64, false, false);
       constexpr uint32_t id_qs = idesc_bf16_f32(64, D, false, true);
       constexpr uint32_t id_kv = idesc_bf16_f32(D, D, true, true);
       constexpr uint32_t id_pv = idesc_bf16_f32(64, D, true, true);
@@ -319,10 +348,24 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       const uint32_t dMN = smem_desc_sw128_lo(sbase, BOX_BYTES);    // MN-major, 8 KB blocks
       const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::S_BLOCK);  // MN-major state blocks
       auto at = [](uint32_t d, uint32_t off) { return d + (off >> 4); };
-      // P^T of chunk c: four MMAs, one per query block.
+      // P^T of chunk c: one MMA over the one-reference operands, or four, one
+      // per query block.  one_ref keeps each chunk's form (bit c % 32) for its
+      // chain step, which reads Qo from the stage in the one-reference form.
+      uint32_t one_ref = 0;
       auto issue_p = [&](int c) {
         const uint32_t qo = (c % NST) * SM::STAGE;
         const uint32_t xo = SM::OFF_X + (c % NX) * SM::XBUF + SM::TILE;
+        if (mode[c % NST]) {
+          one_ref |= 1u << (c & 31);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_w(tmem + SM::T_P + 64 * (c & 1),
+                       at(dKM, xo + (kk / 4) * SM::KBOX + 32 * (kk % 4)),
+                       at(dKM, qo + (kk / 4) * BOX_BYTES + 32 * (kk % 4)), HI, id_p64, kk > 0);
+          mma_commit(&p_full[c & 1]);
+          return;
+        }
+        one_ref &= ~(1u << (c & 31));
         for (int I = 0; I < 4; ++I) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
@@ -359,7 +402,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           tc_fence_after();
           const int s = kc % NST, xb = kc % NX;
           const uint32_t ko = s * SM::STAGE + SM::TILE, vo = ko + SM::TILE;
-          const uint32_t xo = SM::OFF_X + xb * SM::XBUF;
+          const uint32_t xo = (one_ref >> (kc & 31)) & 1u ? s * SM::STAGE : SM::OFF_X + xb * SM::XBUF;
           const uint32_t o_t = tmem + SM::T_O + D * (kc & 1);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)  // O = Qt S_c
@@ -415,113 +458,83 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   } else if (warp >= W_PREP && warp < W_EPI) {
     // ------------------------------------------------------------ PREP
     const int t = tid - W_PREP * 32;
-    auto gwait = [&](uint64_t *bar, uint32_t par, uint32_t site) {
-      return wait_grp<kPrepThreads>(bar, par, ctl, p.err, KID_CHANNEL_GATE_TC, site, BAR_PREP, t);
-    };
     // Items (block I, channel pair cp, part hh): TPI tokens of two adjacent
     // channels, so that every shared-memory access moves a bf16 pair and the
-    // swizzled address is formed once per row for both.  Consecutive threads
-    // take consecutive pairs (coalesced log decay loads, one tile row per
-    // warp).  When the items fit the PREP threads one each, an item's log
-    // decays, loaded for the part sums, stay in registers for its pass;
-    // otherwise the pass loads them again, all at once.
+    // swizzled address is formed once per row for both; one item per thread,
+    // the same in every chunk.  Consecutive threads take consecutive pairs
+    // (coalesced log decay loads, one tile row per warp).  An item's log
+    // decays, loaded for the part sums, stay in registers for its pass.
     constexpr int PARTS = SM::PARTS, TPI = 16 / PARTS;
     constexpr int NPAIR = D / 2, NITEM = 4 * PARTS * NPAIR;
-    constexpr bool KEEP = NITEM <= kPrepThreads;
+    static_assert(NITEM <= kPrepThreads, "one item per PREP thread");
+    const bool has_item = t < NITEM;
+    const int cp = t % NPAIR, hh = (t / NPAIR) % PARTS, c0 = 2 * cp;
     // Blocks in the order 0, 1, 3, 2: the warps of blocks 0 and 3 (and of 1
-    // and 2) share a scheduler, which evens out the K^(J) copies (3 - I a token).
-    auto item_of = [](int it, int &I, int &cp, int &hh) {
-      cp = it % NPAIR;
-      hh = (it / NPAIR) % PARTS;
-      I = it / (PARTS * NPAIR);
-      I ^= I >> 1;
-    };
-    auto load_item = [&](int tok0, int I, int cp, int hh, float2 (&a)[TPI]) {
+    // and 2) share a scheduler, which evens out the K^(J) copies (3 - I a
+    // token).  Threads without an item keep an unused I in range.
+    int I = (t / (PARTS * NPAIR)) & 3;
+    I ^= I >> 1;
+    auto load_item = [&](int tok0, float2 (&a)[TPI]) {
 #pragma unroll
       for (int i = 0; i < TPI; ++i) {
         const int tok = tok0 + 16 * I + TPI * hh + i;
-        a[i] = tok < p.L ? *reinterpret_cast<const float2 *>(p.log_alpha + (bhL + tok) * D + 2 * cp)
+        a[i] = tok < p.L ? *reinterpret_cast<const float2 *>(p.log_alpha + (bhL + tok) * D + c0)
                          : make_float2(0.f, 0.f);  // padding decays nothing
       }
     };
-    // LAPF: each thread copies its own items' log decays of a chunk into the
-    // [64][D] buffer asynchronously, one chunk ahead, and reads back only what
-    // it copied (after cp.async.wait_group): no barrier is involved.
-    float *labuf = reinterpret_cast<float *>(smem + SM::OFF_LA);
-    auto prefetch = [&](int tok0) {
-      for (int it = t; it < NITEM; it += kPrepThreads) {
-        int I, cp, hh;
-        item_of(it, I, cp, hh);
-#pragma unroll
-        for (int i = 0; i < TPI; ++i) {
-          const int row = 16 * I + TPI * hh + i, tok = tok0 + row;
-          float *dst = labuf + row * D + 2 * cp;
-          if (tok < p.L)
-            cp_async_8(dst, p.log_alpha + (bhL + tok) * D + 2 * cp);
-          else
-            *reinterpret_cast<float2 *>(dst) = make_float2(0.f, 0.f);  // padding decays nothing
-        }
-      }
-      cp_async_commit();
-    };
-    auto read_item = [&](int I, int cp, int hh, float2 (&a)[TPI]) {
+    // LAPF: the chunk's log decays come as a TMA tile (zero past L: padding
+    // decays nothing), which every thread waits for itself.
+    auto read_item = [&](const float *labuf, float2 (&a)[TPI]) {
 #pragma unroll
       for (int i = 0; i < TPI; ++i)
-        a[i] = *reinterpret_cast<const float2 *>(labuf + (16 * I + TPI * hh + i) * D + 2 * cp);
+        a[i] = *reinterpret_cast<const float2 *>(labuf + (16 * I + TPI * hh + i) * D + c0);
     };
-    if constexpr (SM::LAPF) {
-      if (nc > 0) prefetch(cbase * CH);
-    }
-    float2 av[TPI];
+    float2 ai[TPI];
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST, xb = c % NX;
       const int tok0 = (cbase + c) * CH;
-      // Half-block sums and blocks' first log decays: they do not need the
-      // stage, so their loads go out while the chunk's tiles are arriving.
-      if constexpr (SM::LAPF) cp_async_wait<0>();  // this chunk's copies, issued a chunk ago
-      for (int it = t; it < NITEM; it += kPrepThreads) {
-        int I, cp, hh;
-        item_of(it, I, cp, hh);
-        float2 a[TPI];
+      // Part sums and blocks' first log decays: they do not need the stage, so
+      // their loads go out while the chunk's tiles are arriving.
+      bool la_ok = true;
+      if constexpr (SM::LAPF)
+        la_ok = wait1(&la_full[c & 1], (c >> 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 6);
+      bool rising = false;  // a log decay above zero in the item
+      if (has_item && la_ok) {
         if constexpr (SM::LAPF)
-          read_item(I, cp, hh, a);
+          read_item(reinterpret_cast<const float *>(smem + SM::OFF_LA + (c & 1) * SM::LA_TILE), ai);
         else
-          load_item(tok0, I, cp, hh, a);
+          load_item(tok0, ai);
         float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < TPI; ++i) {
-          sum.x += a[i].x;
-          sum.y += a[i].y;
+          sum.x += ai[i].x;
+          sum.y += ai[i].y;
+          rising = rising || fmaxf(ai[i].x, ai[i].y) > 0.f;
         }
-        *reinterpret_cast<float2 *>(hsum + (PARTS * I + hh) * D + 2 * cp) = sum;
-        if (hh == 0) *reinterpret_cast<float2 *>(first + I * D + 2 * cp) = a[0];
-        if constexpr (KEEP) {
-#pragma unroll
-          for (int i = 0; i < TPI; ++i) av[i] = a[i];
-        }
+        *reinterpret_cast<float2 *>(hsum + (PARTS * I + hh) * D + c0) = sum;
+        if (hh == 0) *reinterpret_cast<float2 *>(first + I * D + c0) = ai[0];
       }
-      // The next chunk's copies overwrite what this thread has just read (its
-      // values are consumed above, so those reads have completed).
-      if constexpr (SM::LAPF) {
-        if (c + 1 < nc) prefetch(tok0 + CH);
+      // One barrier publishes the part sums, the stage's arrival (its flag
+      // reset: the P epilogue of the stage's last chunk is past) and every
+      // thread's wait for its log decays; after it the tile may be refilled.
+      bool fok = true;
+      if (t == 0) {
+        fok = wait1(&full[s], (c / NST) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 7);
+        if (fok) flag[s] = 0;
       }
-      if (!(ok = gwait(&full[s], (c / NST) & 1, 7))) break;
+      __syncwarp();
+      if (bar_red_or(BAR_PREP, kPrepThreads, !(fok && la_ok))) {
+        ok = false;
+        break;
+      }
       LA_TRACE_EVENT(trace_on && t == 0, t0, 1, c);
-      if (t == 0) flag[s] = 0;
-      named_bar_sync(BAR_PREP, kPrepThreads);
-      if (c >= NX && !(ok = gwait(&xfree[xb], ((c / NX) - 1) & 1, 8))) break;
-      LA_TRACE_EVENT(trace_on && t == 0, t0, 9, c);
-      unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
-      unsigned char *xq = smem + SM::OFF_X + xb * SM::XBUF, *xk = xq + SM::TILE;
-      for (int it = t; it < NITEM; it += kPrepThreads) {
-        int I, cp, hh;
-        item_of(it, I, cp, hh);
-        const int c0 = 2 * cp;
-        // Per channel of the pair: base = the blocks before I, lend = the
-        // whole chunk, rnext[J] = r of a later query block J (the blocks
-        // before it plus its first token's own log decay).
-        float2 base = make_float2(0.f, 0.f), lend = base, rnext[4];
+      // Per channel of the pair: base = the blocks before I, lend = the whole
+      // chunk, rnext[J] = r of a later query block J (the blocks before it
+      // plus its first token's own log decay), r = the block's first Lam.
+      auto block_sums = [&](float2 &base, float2 &lend, float2 (&rnext)[4]) {
+        base = make_float2(0.f, 0.f);
+        lend = base;
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
           float2 tj = make_float2(0.f, 0.f);
@@ -539,6 +552,85 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           lend.x += tj.x;
           lend.y += tj.y;
         }
+      };
+      bool need_blocks = false;
+      if (has_item) {
+        // The one-reference form needs Lam falling through the chunk (log
+        // decays <= 0) by at most kChunkSpanMax: Lam_0 - lend is its span.
+        float2 base, lend, rnext[4];
+        block_sums(base, lend, rnext);
+        const float2 l0 = *reinterpret_cast<const float2 *>(first + c0);
+        need_blocks = rising || fmaxf(l0.x - lend.x, l0.y - lend.y) > kChunkSpanMax;
+      }
+      // One barrier publishes both the wait for this chunk's X buffer and
+      // whether any channel of the chunk needs the blocked form.
+      bool wok = true;
+      if (t == 0 && c >= NX)
+        wok = wait1(&xfree[xb], ((c / NX) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 8);
+      __syncwarp();
+      const bool blocked = bar_red_or(BAR_PREP, kPrepThreads, need_blocks || !wok);
+      if (blocked && *(volatile uint32_t *)&ctl->abort) {
+        ok = false;
+        break;
+      }
+      LA_TRACE_EVENT(trace_on && t == 0, t0, 9, c);
+      if (t == 0) mode[s] = blocked ? 0u : 1u;
+      unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
+      unsigned char *xq = smem + SM::OFF_X + xb * SM::XBUF, *xk = xq + SM::TILE;
+      auto load_qk = [&](uint32_t off, float &qx, float &qy, float &kx, float &ky) {
+        const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
+        const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
+        qx = __uint_as_float(qw << 16), qy = __uint_as_float(qw & 0xffff0000u);
+        kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
+        if (PHI) {
+          qx = elu1_fast(qx);
+          qy = elu1_fast(qy);
+          kx = elu1_fast(kx);
+          ky = elu1_fast(ky);
+        }
+      };
+      float2 base, lend, rnext[4];
+      block_sums(base, lend, rnext);
+      float2 run = base;
+      if (hh) {  // the block's first part
+        const float2 h0 = *reinterpret_cast<const float2 *>(hsum + (PARTS * I) * D + c0);
+        run.x += h0.x;
+        run.y += h0.y;
+      }
+      if (has_item && I == 3 && hh == 0)
+        *reinterpret_cast<float2 *>(dec + s * D + c0) = make_float2(__expf(lend.x), __expf(lend.y));
+      if (has_item && !blocked) {
+        // One reference per channel for the whole chunk, m = the middle of its
+        // Lam range: Qo = q e^{Lam_t - m} (it also stands for Qt, the state
+        // being stored as diag(e^m) S_c), Ko = k e^{m - Lam_t}, both within
+        // e^{kChunkSpanMax / 2}, P^T = Ko Qo^T in one MMA, Kt = Ko e^{lend - m}.
+        const float2 l0 = *reinterpret_cast<const float2 *>(first + c0);
+        const float2 m = make_float2(0.5f * (l0.x + lend.x), 0.5f * (l0.y + lend.y));
+        const float2 eK = make_float2(__expf(lend.x - m.x), __expf(lend.y - m.y));
+        if (I == 0 && hh == 0)
+          *reinterpret_cast<float2 *>(emv + s * D + c0) = make_float2(__expf(m.x), __expf(m.y));
+        // LAPF: the log decays are read again from the tile (kept until the
+        // pass ends), so that the loop need not be unrolled to index
+        // registers: short code keeps the instruction cache warm.
+        const float *la_it = reinterpret_cast<const float *>(smem + SM::OFF_LA + (c & 1) * SM::LA_TILE) +
+                             (16 * I + TPI * hh) * D + c0;
+#pragma unroll(SM::LAPF ? 2 : TPI)
+        for (int i = 0; i < TPI; ++i) {
+          const float2 a = SM::LAPF ? *reinterpret_cast<const float2 *>(la_it + i * D) : ai[i];
+          run.x += a.x;
+          run.y += a.y;
+          const int row = 16 * I + TPI * hh + i;
+          const uint32_t off = tile_off(row, c0, BOX_BYTES);
+          float qx, qy, kx, ky;
+          load_qk(off, qx, qy, kx, ky);
+          const float dx = run.x - m.x, dy = run.y - m.y;
+          const float kox = kx * __expf(-dx), koy = ky * __expf(-dy);
+          *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qx * __expf(dx), qy * __expf(dy));  // Qo
+          *reinterpret_cast<uint32_t *>(xk + tile_off(row, c0, SM::KBOX)) = pack_bf16(kox, koy);  // Ko
+          *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kox * eK.x, koy * eK.y);            // Kt
+        }
+      } else if (has_item) {
+        if (I == 0 && hh == 0) *reinterpret_cast<float2 *>(emv + s * D + c0) = make_float2(1.f, 1.f);
 #pragma unroll
         for (int J = 0; J < 4; ++J) {
           if (J > I) {
@@ -548,22 +640,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
         }
         const float2 fI = *reinterpret_cast<const float2 *>(first + I * D + c0);
-        const float2 r = make_float2(base.x + fI.x, base.y + fI.y);  // the block's first Lam
-        float2 run = base;
-        if (hh) {  // the block's first part
-          const float2 h0 = *reinterpret_cast<const float2 *>(hsum + (PARTS * I) * D + c0);
-          run.x += h0.x;
-          run.y += h0.y;
-        }
-        if (I == 3 && hh == 0)
-          *reinterpret_cast<float2 *>(dec + s * D + c0) = make_float2(__expf(lend.x), __expf(lend.y));
-        float2 ai[TPI];
-        if constexpr (KEEP) {
-#pragma unroll
-          for (int i = 0; i < TPI; ++i) ai[i] = av[i];
-        } else {
-          load_item(tok0, I, cp, hh, ai);
-        }
+        const float2 r = make_float2(base.x + fI.x, base.y + fI.y);
         const float erx = __expf(r.x), ery = __expf(r.y);
         // Every key factor e^{x - Lam_t} (x = lend or a later block's r) is
         // e^{x - r} e^{r - Lam_t}: the first factor is the item's, so a token
@@ -584,27 +661,15 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         {
           float2 rr = run;
-          float m = 0.f;
+          float mx = 0.f;
 #pragma unroll
           for (int i = 0; i < TPI; ++i) {
             rr.x += ai[i].x;
             rr.y += ai[i].y;
-            m = fmaxf(m, fmaxf(fabsf(r.x - rr.x), fabsf(r.y - rr.y)));
+            mx = fmaxf(mx, fmaxf(fabsf(r.x - rr.x), fabsf(r.y - rr.y)));
           }
-          item_fast = item_fast && m <= kDiagSpanMax;
+          item_fast = item_fast && mx <= kDiagSpanMax;
         }
-        auto load_qk = [&](int row, uint32_t off, float &qx, float &qy, float &kx, float &ky) {
-          const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
-          const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
-          qx = __uint_as_float(qw << 16), qy = __uint_as_float(qw & 0xffff0000u);
-          kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
-          if (PHI) {
-            qx = elu1_fast(qx);
-            qy = elu1_fast(qy);
-            kx = elu1_fast(kx);
-            ky = elu1_fast(ky);
-          }
-        };
         if (item_fast) {
 #pragma unroll
           for (int i = 0; i < TPI; ++i) {
@@ -613,7 +678,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             const int row = 16 * I + TPI * hh + i;
             const uint32_t off = tile_off(row, c0, BOX_BYTES);
             float qx, qy, kx, ky;
-            load_qk(row, off, qx, qy, kx, ky);
+            load_qk(off, qx, qy, kx, ky);
             const float dx = r.x - run.x, dy = r.y - run.y;  // the block's span so far
             const float qhx = qx * __expf(-dx), qhy = qy * __expf(-dy);                 // <= 1
             *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qhx, qhy);              // Qh
@@ -639,7 +704,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             run.y += a.y;
             const uint32_t off = tile_off(row, c0, BOX_BYTES);
             float qx, qy, kx, ky;
-            load_qk(row, off, qx, qy, kx, ky);
+            load_qk(off, qx, qy, kx, ky);
             const float qhx = qx * __expf(run.x - r.x), qhy = qy * __expf(run.y - r.y);
             *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qhx, qhy);              // Qh
             *reinterpret_cast<uint32_t *>(xq + off) = pack_bf16(qhx * erx, qhy * ery);  // Qt
@@ -660,7 +725,10 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       }
       fence_proxy_async_smem();
       named_bar_sync(BAR_PREP, kPrepThreads);
-      if (t == 0) mbar_arrive(&prep[s]);
+      if (t == 0) {
+        mbar_arrive(&prep[s]);
+        if constexpr (SM::LAPF) mbar_arrive(&la_empty[c & 1]);  // the tile may be refilled
+      }
       LA_TRACE_EVENT(trace_on && t == 0, t0, 2, c);
     }
   } else if (warp >= W_EPI && warp < W_ST) {
@@ -820,6 +888,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (c >= 1 && !(ok = swait(s_done, (c - 1) & 1, 14))) break;
       tc_fence_after();
       const float e = srow >= 0 ? dec[s * D + srow] : 1.f;
+      const float em = srow >= 0 ? emv[s * D + srow] : 1.f;  // diag(e^m) S_c for Qo
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
         uint32_t r[32];
@@ -832,7 +901,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             uint32_t pk[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              pk[j] = pack_bf16(__uint_as_float(r[16 * h + 2 * j]), __uint_as_float(r[16 * h + 2 * j + 1]));
+              pk[j] = pack_bf16(em * __uint_as_float(r[16 * h + 2 * j]),
+                                em * __uint_as_float(r[16 * h + 2 * j + 1]));
             st_row16(smem + SM::OFF_S, SM::S_BLOCK, srow, col + 16 * h, pk);
           }
         }
@@ -886,7 +956,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 // the later chunks): no state chain, every MMA accumulates into TMEM.
 template <int D>
 struct CgStateSmem {
-  static constexpr int NST = 2;
+  // Stages to cover the loads' latency: the pass's own work per chunk is short.
+  static constexpr int NST = D == 64 ? 4 : 3;
   static constexpr uint32_t TILE = 64 * D * 2;           // K or V, bf16, swizzled boxes
   static constexpr uint32_t LAT = 64 * D * 4;            // log alpha, fp32 [64][D]
   static constexpr uint32_t STAGE = 2 * TILE + LAT;      // K | V | log alpha
@@ -896,6 +967,7 @@ struct CgStateSmem {
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
   static constexpr uint32_t BYTES = OFF_CTL + 64;
   static_assert(STAGE % 1024 == 0 && TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
 };
 
 constexpr int kThreadsCgState = 384;  // warps 0 TMA, 1 MMA, 2-3 idle, 4-11 transform (256)
@@ -1142,16 +1214,15 @@ cudaError_t launch_cg(const VariantArgs &a) {
   p.S0 = a.S0;
   p.S_final = a.S_final;
   p.err = device_error_word();
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv, to, ta;
   if (!make_tmap_bf16_3d(&tq, a.q, D, a.L, BH, BOX, BOX) ||
       !make_tmap_bf16_3d(&tk, a.k, D, a.L, BH, BOX, BOX) ||
       !make_tmap_bf16_3d(&tv, a.v, D, a.L, BH, BOX, BOX) ||
-      !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX))
+      !make_tmap_bf16_3d(&to, a.O, D, a.L, BH, BOX, BOX) ||
+      !make_tmap_f32_3d(&ta, a.decay, D, a.L, BH, D, CH))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (segs) {  // the segments' own states first
-    CUtensorMap ta;
-    if (!make_tmap_f32_3d(&ta, a.decay, D, a.L, BH, D, CH)) return cudaErrorInvalidValue;
     using SS = CgStateSmem<D>;
     auto ks = cg_segment_state_kernel<D, PHI>;
     static int smem_set_state[64];
@@ -1163,9 +1234,9 @@ cudaError_t launch_cg(const VariantArgs &a) {
   static int smem_set[64];
   if ((e = set_smem_once(kern, SM::BYTES, smem_set)) != cudaSuccess) return e;
   if (segs)
-    e = launch_pdl(kern, dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream, tq, tk, tv, to, p);
+    e = launch_pdl(kern, dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream, tq, tk, tv, to, ta, p);
   else
-    kern<<<dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, p);
+    kern<<<dim3(BH, p.n_seg), kThreads, SM::BYTES, a.stream>>>(tq, tk, tv, to, ta, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -91,6 +91,18 @@ __device__ __forceinline__ bool wait_grp(uint64_t *bar, uint32_t parity, Ctl *ct
 }
 
 // The same for a warpgroup (four consecutive warps starting at a multiple of 4).
+// Barrier bar_id over n threads that ORs a predicate across them.
+__device__ __forceinline__ bool bar_red_or(uint32_t bar_id, uint32_t n, bool pred) {
+  uint32_t any;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(any)
+      : "r"(pred ? 1u : 0u), "r"(bar_id), "r"(n)
+      : "memory");
+  return any != 0;
+}
+
 __device__ __forceinline__ bool wait_wg(uint64_t *bar, uint32_t parity, Ctl *ctl,
                                         unsigned int *err, uint32_t kid, uint32_t site,
                                         uint32_t bar_id) {

@@ -371,7 +371,10 @@ def test_channel_gate_segments(d, phi, strong):
     decayed away); the bf16 rounding of the rescaled operands then shows as up
     to ~0.4 relative error in those rows, identically in one piece, so there
     the oracle checks the final state and the outputs are held to the one-piece
-    run."""
+    run.  Identity phi without strong decay has such rows too (one at 0.17 of
+    the median row norm here, 2.7e-2 off): its outputs are held to the oracle
+    with each row's norm floored at half the RMS row norm, the scale of the
+    terms whose rounding the row carries."""
     B, H, L = 1, 2, 3000
     assert api.la_channel_gate_fwd_workspace_bytes(B, H, L, d, d) > 0
     inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=50 + d, with_state=True)
@@ -391,7 +394,7 @@ def test_channel_gate_segments(d, phi, strong):
     O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], la, phi=phi, S0=inp["S0"])
     parity.check(S.cpu(), S_ref, "bf16", "S")
     if not (strong and phi == "identity"):
-        parity.check(O.cpu(), O_ref, "bf16", "O")
+        parity.check(O.cpu(), O_ref, "bf16", "O", row_floor=0.5 if phi == "identity" else 1e-6)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -407,6 +410,31 @@ def test_channel_gate_segments_final_state_may_alias_initial_state(d):
     api.la_device_status()
     assert S_out.data_ptr() == S.data_ptr()
     O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], inp["log_alpha"], phi="elu1",
+                                       S0=inp["S0"])
+    parity.check(O.cpu(), O_ref, "bf16", "O")
+    parity.check(S.cpu(), S_ref, "bf16", "S")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_channel_gate_chunk_forms_alternate(d):
+    """The tensor-core kernel picks a form per chunk: one reference point per
+    key channel when the chunk's cumulative log decay falls by at most 80 and
+    never rises, 16-token blocks otherwise.  Here chunk 1 falls by ~70 (one
+    reference, factors up to e^35), chunk 2 by ~140 (blocks), chunk 3 has log
+    decays above zero in a few channels (blocks), chunks 0 and 4 are plain;
+    each hands its state to the next."""
+    B, H, L = 1, 2, 320
+    inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=70 + d, with_state=True)
+    la = inp["log_alpha"].clone()
+    la[:, :, 64:128] *= 2.6
+    la[:, :, 128:192] *= 5.0
+    la[:, :, 200:204, : d // 8] = 0.05
+    assert float((-la[:, :, 65:128].sum(2)).max()) < 80 < float((-la[:, :, 129:192].sum(2)).max())
+    api.la_set_feature_map("elu1")
+    O, S = api.la_channel_gate_fwd(_d(inp["q"]), _d(inp["k"]), _d(inp["v"]), _d(la), 64,
+                                   _d(inp["S0"]))
+    api.la_device_status()
+    O_ref, S_ref = oracle.channel_gate(inp["q"], inp["k"], inp["v"], la, phi="elu1",
                                        S0=inp["S0"])
     parity.check(O.cpu(), O_ref, "bf16", "O")
     parity.check(S.cpu(), S_ref, "bf16", "S")
