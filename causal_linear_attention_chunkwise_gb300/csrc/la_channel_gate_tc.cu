@@ -577,17 +577,17 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (t == 0) mode[s] = blocked ? 0u : 1u;
       unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
       unsigned char *xq = smem + SM::OFF_X + xb * SM::XBUF, *xk = xq + SM::TILE;
+      // q and k of two channels as bf16 pairs; phi = elu + 1 in packed bf16
+      // arithmetic (half the instructions of fp32, one more rounding).
       auto load_qk = [&](uint32_t off, float &qx, float &qy, float &kx, float &ky) {
-        const uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
-        const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
+        uint32_t qw = *reinterpret_cast<const uint32_t *>(qt + off);
+        uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
+        if (PHI) {
+          qw = elu1_bf16x2(qw);
+          kw = elu1_bf16x2(kw);
+        }
         qx = __uint_as_float(qw << 16), qy = __uint_as_float(qw & 0xffff0000u);
         kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
-        if (PHI) {
-          qx = elu1_fast(qx);
-          qy = elu1_fast(qy);
-          kx = elu1_fast(kx);
-          ky = elu1_fast(ky);
-        }
       };
       float2 base, lend, rnext[4];
       block_sums(base, lend, rnext);
@@ -1061,8 +1061,12 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     }
   } else if (warp >= W_XF) {
     const int t = tid - W_XF * 32;  // 0..255
-    // Items (channel pair cp, octet q of 8 tokens): D/2 x 8 of them.
-    constexpr int NPAIR = D / 2, NITEM = NPAIR * 8;
+    // Items (channel pair cp, octet q of 8 tokens): D/2 x 8 of them, NIT a
+    // thread.  An item's log decays, read for the octet sums, stay in
+    // registers for its weights.
+    constexpr int NPAIR = D / 2, NITEM = NPAIR * 8, NIT = NITEM / kXfThreads;
+    static_assert(NITEM % kXfThreads == 0, "whole items per thread");
+    float2 av[NIT][8];
     bool ok = true;
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST;
@@ -1073,20 +1077,22 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       const float *la = reinterpret_cast<const float *>(kt + 2 * SM::TILE);
       const float *cin = carry + (c & 1) * D;
       float *cout = carry + ((c + 1) & 1) * D;
-      for (int it = t; it < NITEM; it += kXfThreads) {  // octet sums
-        const int cp = it % NPAIR, q = it / NPAIR;
+#pragma unroll
+      for (int j = 0; j < NIT; ++j) {  // octet sums
+        const int it = t + j * kXfThreads, cp = it % NPAIR, q = it / NPAIR;
         float2 sum = make_float2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 a = *reinterpret_cast<const float2 *>(la + (8 * q + i) * D + 2 * cp);
-          sum.x += a.x;
-          sum.y += a.y;
+          av[j][i] = *reinterpret_cast<const float2 *>(la + (8 * q + i) * D + 2 * cp);
+          sum.x += av[j][i].x;
+          sum.y += av[j][i].y;
         }
         *reinterpret_cast<float2 *>(oct + q * D + 2 * cp) = sum;
       }
       named_bar_sync(BAR_XF, kXfThreads);
-      for (int it = t; it < NITEM; it += kXfThreads) {  // weights, K rows in place
-        const int cp = it % NPAIR, q = it / NPAIR, c0 = 2 * cp;
+#pragma unroll
+      for (int j = 0; j < NIT; ++j) {  // weights, K rows in place
+        const int it = t + j * kXfThreads, cp = it % NPAIR, q = it / NPAIR, c0 = 2 * cp;
         float2 run = *reinterpret_cast<const float2 *>(cin + c0);  // decay after the chunk
         float2 tot = make_float2(0.f, 0.f);
 #pragma unroll
@@ -1104,20 +1110,19 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
           *reinterpret_cast<float2 *>(cout + c0) = make_float2(cc.x + tot.x, cc.y + tot.y);
         }
         const uint32_t cbox = (uint32_t)c0 >> 6, cin64 = (uint32_t)c0 & 63u;
+        uint32_t kw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          kw[i] = *reinterpret_cast<const uint32_t *>(kt + cbox * BOX_BYTES +
+                                                      sw128_offset((uint32_t)(8 * q + i), cin64));
 #pragma unroll
         for (int i = 7; i >= 0; --i) {  // token 8 q + i: the decay of the tokens after it
-          const int row = 8 * q + i;
-          const uint32_t off = cbox * BOX_BYTES + sw128_offset((uint32_t)row, cin64);
-          const uint32_t kw = *reinterpret_cast<const uint32_t *>(kt + off);
-          float kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
-          if (PHI) {
-            kx = elu1_fast(kx);
-            ky = elu1_fast(ky);
-          }
+          const uint32_t off = cbox * BOX_BYTES + sw128_offset((uint32_t)(8 * q + i), cin64);
+          const uint32_t w = PHI ? elu1_bf16x2(kw[i]) : kw[i];  // as the output pass forms its keys
+          const float kx = __uint_as_float(w << 16), ky = __uint_as_float(w & 0xffff0000u);
           *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kx * __expf(run.x), ky * __expf(run.y));
-          const float2 a = *reinterpret_cast<const float2 *>(la + row * D + c0);
-          run.x += a.x;
-          run.y += a.y;
+          run.x += av[j][i].x;
+          run.y += av[j][i].y;
         }
       }
       fence_proxy_async_smem();
@@ -1164,7 +1169,7 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
 // Segments per sequence: enough (sequence, segment) blocks to fill the SMs
 // once, at least 8 chunks per segment, and only with a workspace.  The first
 // segments start at once, alongside the state pass; the others wait for the
-// state pass and the scan.  So the first segment is the longer one, by the
+// state pass.  So the first segment is the longer one, by the
 // state pass's cost per chunk relative to the output pass's (kStateShare,
 // measured): f chunks of output take as long as f chunks of state pass plus a
 // later segment's g, i.e. g = (1 - kStateShare) f.
