@@ -614,20 +614,39 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         // registers: short code keeps the instruction cache warm.
         const float *la_it = reinterpret_cast<const float *>(smem + SM::OFF_LA + (c & 1) * SM::LA_TILE) +
                              (16 * I + TPI * hh) * D + c0;
-#pragma unroll(SM::LAPF ? 2 : TPI)
-        for (int i = 0; i < TPI; ++i) {
-          const float2 a = SM::LAPF ? *reinterpret_cast<const float2 *>(la_it + i * D) : ai[i];
-          run.x += a.x;
-          run.y += a.y;
-          const int row = 16 * I + TPI * hh + i;
-          const uint32_t off = tile_off(row, c0, BOX_BYTES);
-          float qx, qy, kx, ky;
-          load_qk(off, qx, qy, kx, ky);
-          const float dx = run.x - m.x, dy = run.y - m.y;
-          const float kox = kx * __expf(-dx), koy = ky * __expf(-dy);
-          *reinterpret_cast<uint32_t *>(qt + off) = pack_bf16(qx * __expf(dx), qy * __expf(dy));  // Qo
-          *reinterpret_cast<uint32_t *>(xk + tile_off(row, c0, SM::KBOX)) = pack_bf16(kox, koy);  // Ko
-          *reinterpret_cast<uint32_t *>(kt + off) = pack_bf16(kox * eK.x, koy * eK.y);            // Kt
+        // Two tokens a step, their loads ahead of their stores (a load after
+        // a shared-memory store waits for it: the addresses may alias).
+#pragma unroll(SM::LAPF ? 1 : TPI / 2)
+        for (int i = 0; i < TPI; i += 2) {
+          float2 a[2];
+          uint32_t qw[2], kw[2], off[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if constexpr (SM::LAPF)
+              a[u] = *reinterpret_cast<const float2 *>(la_it + (i + u) * D);
+            else
+              a[u] = ai[i + u];
+            off[u] = tile_off(16 * I + TPI * hh + i + u, c0, BOX_BYTES);
+            qw[u] = *reinterpret_cast<const uint32_t *>(qt + off[u]);
+            kw[u] = *reinterpret_cast<const uint32_t *>(kt + off[u]);
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            run.x += a[u].x;
+            run.y += a[u].y;
+            if (PHI) {
+              qw[u] = elu1_bf16x2(qw[u]);
+              kw[u] = elu1_bf16x2(kw[u]);
+            }
+            const float qx = __uint_as_float(qw[u] << 16), qy = __uint_as_float(qw[u] & 0xffff0000u);
+            const float kx = __uint_as_float(kw[u] << 16), ky = __uint_as_float(kw[u] & 0xffff0000u);
+            const float dx = run.x - m.x, dy = run.y - m.y;
+            const float kox = kx * __expf(-dx), koy = ky * __expf(-dy);
+            *reinterpret_cast<uint32_t *>(qt + off[u]) = pack_bf16(qx * __expf(dx), qy * __expf(dy));  // Qo
+            *reinterpret_cast<uint32_t *>(xk + tile_off(16 * I + TPI * hh + i + u, c0, SM::KBOX)) =
+                pack_bf16(kox, koy);                                                                // Ko
+            *reinterpret_cast<uint32_t *>(kt + off[u]) = pack_bf16(kox * eK.x, koy * eK.y);         // Kt
+          }
         }
       } else if (has_item) {
         if (I == 0 && hh == 0) *reinterpret_cast<float2 *>(emv + s * D + c0) = make_float2(1.f, 1.f);
