@@ -564,10 +564,25 @@ __device__ __noinline__ void rescale_qk_rows(unsigned char *stage, const float *
       stage, [lm, A](int kt, int r) { return __expf(kt == 0 ? lm[r] : A - lm[r]); }, t, n);
 }
 
+// Two values picked by a 0/1 index known only at run time: a select between
+// two registers (an array indexed at run time would sit in local memory,
+// and these are read on every chunk).
+template <typename T>
+struct Pair2 {
+  T v0, v1;
+  __device__ __forceinline__ T operator[](int i) const { return i ? v1 : v0; }
+  __device__ __forceinline__ void set(int i, T x) {
+    if (i)
+      v1 = x;
+    else
+      v0 = x;
+  }
+};
+
 // The virtual-chunk order of a CTA's two segments (d = 64), or of its one
 // segment (d = 128: nc[1] = 0).
 struct Streams {
-  int nc[2];   // chunks per segment (the second may have none)
+  Pair2<int> nc;  // chunks per segment (the second may have none)
   int m;       // chunks both have: virtual 0 .. 2m-1 alternate
   int longer;  // the segment whose chunks follow alone
   __device__ void at(int k, int &sg, int &c) const {
@@ -620,23 +635,26 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
   const size_t bhL = (size_t)bh * p.L;
   // Segments of this CTA (one for d = 128).
   Streams st;
-  int tok0[2], seg[2];
-  const float *S_seg[2];
-  int S_ld[2];  // floats per row of S_seg (a workspace slot row holds z after S when NORM)
+  Pair2<int> tok0, seg;
+  Pair2<const float *> S_seg;
+  Pair2<int> S_ld;  // floats per row of S_seg (a workspace slot row holds z after S when NORM)
+#pragma unroll
   for (int sg = 0; sg < 2; ++sg) {
-    seg[sg] = PAIRS ? 2 * (int)blockIdx.y + sg : (sg == 0 ? (int)blockIdx.y : p.n_seg);
-    const int c0 = seg[sg] * p.seg_chunks;
-    st.nc[sg] = seg[sg] < p.n_seg ? min(p.seg_chunks, p.n_chunks - c0) : 0;
-    tok0[sg] = c0 * CH;
-    S_seg[sg] = nullptr;
+    const int sgi = PAIRS ? 2 * (int)blockIdx.y + sg : (sg == 0 ? (int)blockIdx.y : p.n_seg);
+    seg.set(sg, sgi);
+    const int c0 = sgi * p.seg_chunks;
+    st.nc.set(sg, sgi < p.n_seg ? min(p.seg_chunks, p.n_chunks - c0) : 0);
+    tok0.set(sg, c0 * CH);
+    const float *src = nullptr;
     if (p.n_seg > 1) {
-      S_ld[sg] = p.srow;
-      if (seg[sg] > 0 || p.S0 || (NORM && p.z0))
-        S_seg[sg] = p.ws_state + ((size_t)bh * p.n_seg + seg[sg]) * D * p.srow;
+      S_ld.set(sg, p.srow);
+      if (sgi > 0 || p.S0 || (NORM && p.z0))
+        src = p.ws_state + ((size_t)bh * p.n_seg + sgi) * D * p.srow;
     } else {
-      S_ld[sg] = D;
-      S_seg[sg] = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
+      S_ld.set(sg, D);
+      src = p.S0 ? p.S0 + (size_t)bh * D * D : nullptr;
     }
+    S_seg.set(sg, src);
   }
   st.m = min(st.nc[0], st.nc[1]);
   st.longer = st.nc[0] >= st.nc[1] ? 0 : 1;
