@@ -1303,7 +1303,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         tt = A;
       }
     };
-    float g_prev[2] = {0.f, 0.f};  // per chain: g of its chunk whose MMA4 is next awaited
+    Pair2<float> g_prev{0.f, 0.f};  // per chain: g of its chunk whose MMA4 is next awaited
     bool ok = true;
     // The incoming segment states come from the scan, which this kernel may
     // have been launched alongside (programmatic dependent launch): only this
@@ -1321,7 +1321,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (!ok) break;
         float g0;
         log_scales(k, m0, t0s, g0);
-        g_prev[ch] = g0;
+        g_prev.set(ch, g0);
       }
       if (SM::TRANS && S_seg[sg] != nullptr) {
         const float sm0 = __expf(m0), tm0 = __expf(t0s);
@@ -1396,7 +1396,7 @@ chunk_output_kernel(const __grid_constant__ CUtensorMap tmQ,
           if constexpr (DECAY) {
             sm = __expf(g_prev[ch] + lm1);
             tm = __expf(g_prev[ch] + lt1);
-            g_prev[ch] = lg1;
+            g_prev.set(ch, lg1);
           }
           if constexpr (SM::TRANS) {
             // TMEM to TMEM: the copy for chunk c+1 goes to buffer (c+1) & 1;
