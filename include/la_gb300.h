@@ -227,8 +227,9 @@ size_t la_normalised_fwd_workspace_bytes(int B, int H, int L, int d_k, int d_v, 
  *              bytes (16-byte aligned), or NULL; ws_bytes = its size.  With it
  *              (bf16, d_k = d_v in {64, 128}, chunk 64, when the query is not
  *              0) each sequence is cut into segments that run side by side: a
- *              state pass per segment, a scan of the segment states, then the
- *              segments' outputs.  With NULL each sequence runs in one piece.
+ *              state pass over every segment but the last, then the segments'
+ *              outputs, each folding in the states of the segments before it.
+ *              With NULL each sequence runs in one piece.
  *              A non-NULL workspace smaller than the query or misaligned is
  *              LA_ERR_INVALID_ARG.  Its contents need no initialisation and are
  *              not kept.
