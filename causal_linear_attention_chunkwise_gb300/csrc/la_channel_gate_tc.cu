@@ -66,7 +66,8 @@ using namespace tc;
 constexpr float kDiagSpanMax = 80.f;
 // Largest fall of Lam through a chunk (per key channel) for which the chunk
 // takes one reference point per channel instead of one per 16-token block:
-// its query and key factors then stay within e^{40}.
+// its query and key factors then stay within e^{40}.  A chunk takes it when
+// every part of it (8 or 16 tokens) falls by at most its share of that.
 constexpr float kChunkSpanMax = 80.f;
 
 // Warp roles: 0 TMA, 1 MMA, 2..11 PREP (320 threads), 12..15 EPI (P and O
@@ -134,13 +135,17 @@ struct CgParams {
   // Segments of a sequence (one without a workspace): the first has
   // first_chunks chunks, the others seg_chunks each (the last may have fewer).
   int first_chunks, seg_chunks, n_seg;
+  // The state pass cuts every segment but the last into state_parts pieces,
+  // one block each; a sequence has n_slot = (n_seg - 1) state_parts + 1
+  // workspace slots (the last for a copy of S0).
+  int state_parts, n_slot;
   const float *log_alpha;  // [BH][L][D]
   const __nv_bfloat16 *q, *k;
   const float *S0;
   float *S_final;
-  float *ws_state;         // [BH][NS][D][D]: slot s < NS-1 = segment s's own state;
-                           // slot NS-1 = a copy of S0 when S_final is S0
-  float *ws_logdec;        // [BH][NS][D]: segment s's total log decay per key channel
+  float *ws_state;         // [BH][n_slot][D][D]: slot j < n_slot-1 = piece j's own state;
+                           // slot n_slot-1 = a copy of S0 when S_final is S0
+  float *ws_logdec;        // [BH][n_slot][D]: piece j's total log decay per key channel
   unsigned int *err;
 };
 
@@ -148,6 +153,16 @@ struct CgParams {
 __device__ __forceinline__ void seg_range(const CgParams &p, int seg, int &c0, int &n) {
   c0 = seg == 0 ? 0 : p.first_chunks + (seg - 1) * p.seg_chunks;
   n = min(seg == 0 ? p.first_chunks : p.seg_chunks, p.n_chunks - c0);
+}
+
+// First chunk and chunk count of state-pass piece j (part j % state_parts of
+// segment j / state_parts, the parts as even as whole chunks allow).
+__device__ __forceinline__ void piece_range(const CgParams &p, int j, int &c0, int &n) {
+  int s0, sn;
+  seg_range(p, j / p.state_parts, s0, sn);
+  const int part = j % p.state_parts, base = sn / p.state_parts, rem = sn % p.state_parts;
+  c0 = s0 + part * base + min(part, rem);
+  n = base + (part < rem ? 1 : 0);
 }
 
 // Byte offset of element (row, col) in a bf16 tile of 128-byte swizzled rows
@@ -252,8 +267,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   // from the state pass's copy of it when S_final is the same buffer, so that
   // the last segment cannot overwrite it before another reads it.
   const bool alias0 = p.n_seg > 1 && p.S0 && p.S0 == p.S_final;
-  const float *slots = p.n_seg > 1 ? p.ws_state + (size_t)bh * p.n_seg * D * D : nullptr;
-  const float *S_base = alias0 ? slots + (size_t)(p.n_seg - 1) * D * D
+  const float *slots = p.n_seg > 1 ? p.ws_state + (size_t)bh * p.n_slot * D * D : nullptr;
+  const float *S_base = alias0 ? slots + (size_t)(p.n_slot - 1) * D * D
                                : (p.S0 ? p.S0 + (size_t)bh * D * D : nullptr);
   const bool needs_pass = p.n_seg > 1 && (seg > 0 || alias0);
   const bool last_seg = seg == p.n_seg - 1;
@@ -499,32 +514,40 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       bool la_ok = true;
       if constexpr (SM::LAPF)
         la_ok = wait1(&la_full[c & 1], (c >> 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 6);
-      bool rising = false;  // a log decay above zero in the item
+      // The one-reference form needs Lam falling through the chunk (log decays
+      // <= 0) by at most kChunkSpanMax; each thread tests its own part against
+      // its share, so the choice rides on the barrier that publishes the sums.
+      bool need_blocks = false;
       if (has_item && la_ok) {
         if constexpr (SM::LAPF)
           read_item(reinterpret_cast<const float *>(smem + SM::OFF_LA + (c & 1) * SM::LA_TILE), ai);
         else
           load_item(tok0, ai);
         float2 sum = make_float2(0.f, 0.f);
+        bool rising = false;  // a log decay above zero in the item
 #pragma unroll
         for (int i = 0; i < TPI; ++i) {
           sum.x += ai[i].x;
           sum.y += ai[i].y;
           rising = rising || fmaxf(ai[i].x, ai[i].y) > 0.f;
         }
+        need_blocks = rising || fmaxf(-sum.x, -sum.y) > kChunkSpanMax / (4 * PARTS);
         *reinterpret_cast<float2 *>(hsum + (PARTS * I + hh) * D + c0) = sum;
         if (hh == 0) *reinterpret_cast<float2 *>(first + I * D + c0) = ai[0];
       }
       // One barrier publishes the part sums, the stage's arrival (its flag
-      // reset: the P epilogue of the stage's last chunk is past) and every
-      // thread's wait for its log decays; after it the tile may be refilled.
+      // reset: the P epilogue of the stage's last chunk is past), the wait for
+      // this chunk's X buffer, every thread's wait for its log decays and
+      // whether any part needs the blocked form.
       bool fok = true;
       if (t == 0) {
         fok = wait1(&full[s], (c / NST) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 7);
         if (fok) flag[s] = 0;
+        if (fok && c >= NX) fok = wait1(&xfree[xb], ((c / NX) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 8);
       }
       __syncwarp();
-      if (bar_red_or(BAR_PREP, kPrepThreads, !(fok && la_ok))) {
+      const bool blocked = bar_red_or(BAR_PREP, kPrepThreads, need_blocks || !(fok && la_ok));
+      if (blocked && *(volatile uint32_t *)&ctl->abort) {  // a wait gave up (it set abort)
         ok = false;
         break;
       }
@@ -553,26 +576,6 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           lend.y += tj.y;
         }
       };
-      bool need_blocks = false;
-      if (has_item) {
-        // The one-reference form needs Lam falling through the chunk (log
-        // decays <= 0) by at most kChunkSpanMax: Lam_0 - lend is its span.
-        float2 base, lend, rnext[4];
-        block_sums(base, lend, rnext);
-        const float2 l0 = *reinterpret_cast<const float2 *>(first + c0);
-        need_blocks = rising || fmaxf(l0.x - lend.x, l0.y - lend.y) > kChunkSpanMax;
-      }
-      // One barrier publishes both the wait for this chunk's X buffer and
-      // whether any channel of the chunk needs the blocked form.
-      bool wok = true;
-      if (t == 0 && c >= NX)
-        wok = wait1(&xfree[xb], ((c / NX) - 1) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 8);
-      __syncwarp();
-      const bool blocked = bar_red_or(BAR_PREP, kPrepThreads, need_blocks || !wok);
-      if (blocked && *(volatile uint32_t *)&ctl->abort) {
-        ok = false;
-        break;
-      }
       LA_TRACE_EVENT(trace_on && t == 0, t0, 9, c);
       if (t == 0) mode[s] = blocked ? 0u : 1u;
       unsigned char *qt = smem + s * SM::STAGE, *kt = qt + SM::TILE;
@@ -861,7 +864,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     // its results, so only it waits, and only where it needs them: first
     // segments run alongside the state pass.
     if (needs_pass) pdl_wait_previous();
-    const float *ld_row = p.n_seg > 1 ? p.ws_logdec + (size_t)bh * p.n_seg * D + srow : nullptr;
+    const float *ld_row = p.n_seg > 1 ? p.ws_logdec + (size_t)bh * p.n_slot * D + srow : nullptr;
 #pragma unroll 1
     for (int col = 0; col < D; col += 32) {
       float acc[32];
@@ -879,7 +882,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
       }
       if (srow >= 0) {
-        for (int j2 = 0; j2 < seg; ++j2) {  // S <- diag(e^{A_j}) S + dS_j
+        for (int j2 = 0; j2 < seg * p.state_parts; ++j2) {  // S <- diag(e^{A_j}) S + dS_j, pieces in order
           const float e = __expf(ld_row[(size_t)j2 * D]);
           const float4 *src =
               reinterpret_cast<const float4 *>(slots + ((size_t)j2 * D + srow) * D + col);
@@ -975,8 +978,9 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 // the later chunks): no state chain, every MMA accumulates into TMEM.
 template <int D>
 struct CgStateSmem {
-  // Stages to cover the loads' latency: the pass's own work per chunk is short.
-  static constexpr int NST = D == 64 ? 4 : 3;
+  // Stages to cover the loads' latency (the pass's own work per chunk is
+  // short); at d = 64 a block runs two pieces of a segment.
+  static constexpr int NST = 3;
   static constexpr uint32_t TILE = 64 * D * 2;           // K or V, bf16, swizzled boxes
   static constexpr uint32_t LAT = 64 * D * 4;            // log alpha, fp32 [64][D]
   static constexpr uint32_t STAGE = 2 * TILE + LAT;      // K | V | log alpha
@@ -985,22 +989,30 @@ struct CgStateSmem {
   static constexpr uint32_t OFF_BAR = OFF_CARRY + 2 * D * 4;
   static constexpr uint32_t OFF_CTL = OFF_BAR + 8 * (3 * NST + 1);
   static constexpr uint32_t BYTES = OFF_CTL + 64;
+  static constexpr uint32_t PIECE = (BYTES + 1023) / 1024 * 1024;  // one piece's region
   static_assert(STAGE % 1024 == 0 && TILE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-  static_assert(BYTES <= 232448, "exceeds the per-block shared memory limit");
+  static_assert((D == 64 ? 2 : 1) * PIECE <= 232448, "exceeds the per-block shared memory limit");
 };
 
 constexpr int kThreadsCgState = 384;  // warps 0 TMA, 1 MMA, 2-3 idle, 4-11 transform (256)
 constexpr int W_XF = 4, kXfThreads = 256;
 constexpr uint32_t BAR_XF = 5;
 
-template <int D, bool PHI>
-__global__ void __launch_bounds__(kThreadsCgState, 1)
+// PB pieces per block, each with its own copy of the pipeline (warps 12 pc ..
+// 12 pc + 11), shared memory region and TMEM columns: the pieces of one
+// segment then share an SM for certain.
+template <int D, bool PHI, int PB>
+__global__ void __launch_bounds__(kThreadsCgState * PB, 1)
 cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmA, CgParams p) {
   using SM = CgStateSmem<D>;
   constexpr int NST = SM::NST;
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_all[];
+  const int pc = (int)threadIdx.x / kThreadsCgState;  // this thread's piece in the block
+  unsigned char *smem = smem_all + pc * SM::PIECE;
+  Ctl *ctl0 = reinterpret_cast<Ctl *>(smem_all + SM::OFF_CTL);  // holds the TMEM base
+  const uint32_t bar_xf = BAR_XF + 2 * pc;
   float *oct = reinterpret_cast<float *>(smem + SM::OFF_OCT);
   float *carry = reinterpret_cast<float *>(smem + SM::OFF_CARRY);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
@@ -1008,16 +1020,16 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
   uint64_t *ready = empty + NST;  // K rows weighted
   uint64_t *done = ready + NST;   // every MMA finished
   Ctl *ctl = reinterpret_cast<Ctl *>(smem + SM::OFF_CTL);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = (int)threadIdx.x - pc * kThreadsCgState, warp = tid >> 5, lane = tid & 31;
   pdl_launch_dependents();  // the output kernel may start; its later segments wait
-  const int seg = blockIdx.x, bh = blockIdx.y;
-  if (seg == 0 && p.S0 && p.S0 == p.S_final) {  // S0 aside, for when S_final overwrites it
+  const int piece = blockIdx.x * PB + pc, bh = blockIdx.y;
+  if (piece == 0 && p.S0 && p.S0 == p.S_final) {  // S0 aside, for when S_final overwrites it
     const float4 *src = reinterpret_cast<const float4 *>(p.S0 + (size_t)bh * D * D);
-    float4 *dst = reinterpret_cast<float4 *>(p.ws_state + ((size_t)bh * p.n_seg + p.n_seg - 1) * D * D);
-    for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) dst[i] = src[i];
+    float4 *dst = reinterpret_cast<float4 *>(p.ws_state + ((size_t)bh * p.n_slot + p.n_slot - 1) * D * D);
+    for (int i = tid; i < D * D / 4; i += kThreadsCgState) dst[i] = src[i];
   }
-  int cbase, nc;  // full chunks: s < NS-1
-  seg_range(p, seg, cbase, nc);
+  int cbase, nc;  // at least one chunk (the plan's parts are never empty)
+  piece_range(p, piece, cbase, nc);
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
@@ -1028,15 +1040,15 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     ctl->abort = 0;
     fence_mbarrier_init();
   }
-  for (int i = tid; i < D; i += blockDim.x) carry[i] = 0.f;
-  if (warp == 1) {
-    tmem_alloc(&ctl->tmem_base, D);
+  for (int i = tid; i < D; i += kThreadsCgState) carry[i] = 0.f;
+  if (pc == 0 && warp == 1) {
+    tmem_alloc(&ctl0->tmem_base, PB * D);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = ctl->tmem_base;
+  const uint32_t tmem = ctl0->tmem_base + pc * D;
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
@@ -1090,7 +1102,7 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     for (int c = 0; ok && c < nc; ++c) {
       const int s = c % NST;
       if (!(ok = wait_grp<kXfThreads>(&full[s], (c / NST) & 1, ctl, p.err, KID_CHANNEL_GATE_TC, 32,
-                                      BAR_XF, t)))
+                                      bar_xf, t)))
         break;
       unsigned char *kt = smem + s * SM::STAGE;
       const float *la = reinterpret_cast<const float *>(kt + 2 * SM::TILE);
@@ -1108,7 +1120,7 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         }
         *reinterpret_cast<float2 *>(oct + q * D + 2 * cp) = sum;
       }
-      named_bar_sync(BAR_XF, kXfThreads);
+      named_bar_sync(bar_xf, kXfThreads);
 #pragma unroll
       for (int j = 0; j < NIT; ++j) {  // weights, K rows in place
         const int it = t + j * kXfThreads, cp = it % NPAIR, q = it / NPAIR, c0 = 2 * cp;
@@ -1145,16 +1157,16 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
         }
       }
       fence_proxy_async_smem();
-      named_bar_sync(BAR_XF, kXfThreads);
+      named_bar_sync(bar_xf, kXfThreads);
       if (t == 0) mbar_arrive(&ready[s]);
     }
     // The accumulated state (warps 4-7: lane quarters 0-3) into slot s+1, and
     // the segment's total log decay per key channel.
-    if (t < 128 && wait_wg(done, 0, ctl, p.err, KID_CHANNEL_GATE_TC, 33, BAR_XF + 1)) {
+    if (t < 128 && wait_wg(done, 0, ctl, p.err, KID_CHANNEL_GATE_TC, 33, bar_xf + 1)) {
       tc_fence_after();
       const int quarter = warp & 3;
       const int row = acc_row<D>(quarter, lane);
-      const size_t slot = (size_t)bh * p.n_seg + seg;  // the segment's own state
+      const size_t slot = (size_t)bh * p.n_slot + piece;  // the piece's own state
       float *dst = p.ws_state + slot * D * D;
 #pragma unroll 1
       for (int col = 0; col < D; col += 32) {
@@ -1172,45 +1184,49 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
       }
       if (ok)
         for (int i = t; i < D; i += 128)
-          p.ws_logdec[((size_t)bh * p.n_seg + seg) * D + i] = carry[(nc & 1) * D + i];
+          p.ws_logdec[((size_t)bh * p.n_slot + piece) * D + i] = carry[(nc & 1) * D + i];
     }
   }
   __syncwarp();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) {
+  if (pc == 0 && warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem, D);
+    tmem_dealloc(ctl0->tmem_base, PB * D);
   }
 }
 
 // Segments per sequence: enough (sequence, segment) blocks to fill the SMs
 // once, at least 8 chunks per segment, and only with a workspace.  The first
 // segments start at once, alongside the state pass; the others wait for the
-// state pass.  So the first segment is the longer one, by the
-// state pass's cost per chunk relative to the output pass's (kStateShare,
-// measured): f chunks of output take as long as f chunks of state pass plus a
-// later segment's g, i.e. g = (1 - kStateShare) f.
-constexpr double kStateShare = 0.3;
+// state pass.  So the first segment is the longer one, by the state pass's
+// cost per chunk relative to the output pass's (share, measured): f chunks of
+// output take as long as f chunks of state pass plus a later segment's g,
+// i.e. g = (1 - share) f.  At d = 64 the state pass cuts each segment into
+// two pieces, two blocks per SM, which halves its share.
+constexpr double kStateShare64 = 0.25, kStateShare128 = 0.3;
 struct CgPlan {
-  int n_chunks, first_chunks, seg_chunks, n_seg;
+  int n_chunks, first_chunks, seg_chunks, n_seg, state_parts, n_slot;
 };
-CgPlan cg_plan(int B, int H, int L) {
+CgPlan cg_plan(int B, int H, int L, int D) {
   const int nc = (L + CH - 1) / CH, BH = B * H;
   const int ns = std::max(1, std::min(sm_count() / std::max(1, BH), nc / 8));
-  if (ns <= 1) return CgPlan{nc, nc, nc, 1};
-  const double f = nc / (1.0 + (1.0 - kStateShare) * (ns - 1));
+  if (ns <= 1) return CgPlan{nc, nc, nc, 1, 1, 1};
+  const double share = D == 64 ? kStateShare64 : kStateShare128;
+  const double f = nc / (1.0 + (1.0 - share) * (ns - 1));
   const int first = std::max(1, std::min(nc - 1, (int)std::lround(f)));
   const int g = (nc - first + ns - 2) / (ns - 1);
   const int n_seg = 1 + (nc - first + g - 1) / g;
-  return CgPlan{nc, first, g, n_seg};
+  // Every state-passed segment (all but the last) has first or g chunks.
+  const int parts = D == 64 && first >= 2 && (n_seg <= 2 || g >= 2) ? 2 : 1;
+  return CgPlan{nc, first, g, n_seg, parts, (n_seg - 1) * parts + 1};
 }
 
 size_t cg_ws_bytes(int B, int H, int L, int D) {
-  const CgPlan pl = cg_plan(B, H, L);
+  const CgPlan pl = cg_plan(B, H, L, D);
   if (pl.n_seg <= 1) return 0;
-  const size_t bh = (size_t)B * H, slots = bh * pl.n_seg;
+  const size_t bh = (size_t)B * H, slots = bh * pl.n_slot;
   return slots * D * D * sizeof(float) + slots * D * sizeof(float);
 }
 
@@ -1222,15 +1238,17 @@ cudaError_t launch_cg(const VariantArgs &a) {
   p.H = a.H;
   p.L = a.L;
   p.BH = BH;
-  const CgPlan pl = cg_plan(a.B, a.H, a.L);
+  const CgPlan pl = cg_plan(a.B, a.H, a.L, D);
   const bool segs = pl.n_seg > 1 && a.workspace && a.ws_bytes >= cg_ws_bytes(a.B, a.H, a.L, D);
   p.n_chunks = pl.n_chunks;
   p.first_chunks = segs ? pl.first_chunks : pl.n_chunks;
   p.seg_chunks = segs ? pl.seg_chunks : pl.n_chunks;
   p.n_seg = segs ? pl.n_seg : 1;
+  p.state_parts = segs ? pl.state_parts : 1;
+  p.n_slot = segs ? pl.n_slot : 1;
   if (segs) {
     p.ws_state = static_cast<float *>(a.workspace);
-    p.ws_logdec = p.ws_state + (size_t)BH * pl.n_seg * D * D;
+    p.ws_logdec = p.ws_state + (size_t)BH * pl.n_slot * D * D;
   }
   p.log_alpha = a.decay;
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -1246,13 +1264,24 @@ cudaError_t launch_cg(const VariantArgs &a) {
       !make_tmap_f32_3d(&ta, a.decay, D, a.L, BH, D, CH))
     return cudaErrorInvalidValue;
   cudaError_t e;
-  if (segs) {  // the segments' own states first
+  if (segs) {  // the segments' own states first, a block per segment
     using SS = CgStateSmem<D>;
-    auto ks = cg_segment_state_kernel<D, PHI>;
-    static int smem_set_state[64];
-    if ((e = set_smem_once(ks, SS::BYTES, smem_set_state)) != cudaSuccess) return e;
-    ks<<<dim3(pl.n_seg - 1, BH), kThreadsCgState, SS::BYTES, a.stream>>>(tk, tv, ta, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if constexpr (D == 64) {
+      if (pl.state_parts == 2) {
+        auto ks = cg_segment_state_kernel<D, PHI, 2>;
+        static int smem_set_state2[64];
+        if ((e = set_smem_once(ks, 2 * SS::PIECE, smem_set_state2)) != cudaSuccess) return e;
+        ks<<<dim3(pl.n_seg - 1, BH), 2 * kThreadsCgState, 2 * SS::PIECE, a.stream>>>(tk, tv, ta, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      }
+    }
+    if (pl.state_parts == 1) {
+      auto ks = cg_segment_state_kernel<D, PHI, 1>;
+      static int smem_set_state[64];
+      if ((e = set_smem_once(ks, SS::PIECE, smem_set_state)) != cudaSuccess) return e;
+      ks<<<dim3(pl.n_seg - 1, BH), kThreadsCgState, SS::PIECE, a.stream>>>(tk, tv, ta, p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
   auto kern = channel_gate_tc_kernel<D, PHI>;
   static int smem_set[64];

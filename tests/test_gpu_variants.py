@@ -418,15 +418,15 @@ def test_channel_gate_segments_final_state_may_alias_initial_state(d):
 @pytest.mark.parametrize("d", [64, 128])
 def test_channel_gate_chunk_forms_alternate(d):
     """The tensor-core kernel picks a form per chunk: one reference point per
-    key channel when the chunk's cumulative log decay falls by at most 80 and
-    never rises, 16-token blocks otherwise.  Here chunk 1 falls by ~70 (one
-    reference, factors up to e^35), chunk 2 by ~140 (blocks), chunk 3 has log
-    decays above zero in a few channels (blocks), chunks 0 and 4 are plain;
-    each hands its state to the next."""
+    key channel when every part of the chunk (8 or 16 tokens) falls by at
+    most its share of 80 and none rises, 16-token blocks otherwise.  Here
+    chunk 1 falls evenly by 69 (one reference, factors up to e^35), chunk 2
+    by ~140 (blocks), chunk 3 has log decays above zero in a few channels
+    (blocks), chunks 0 and 4 are plain; each hands its state to the next."""
     B, H, L = 1, 2, 320
     inp = W.make_variant_inputs("channel_gate", B, H, L, d, d, "bf16", seed=70 + d, with_state=True)
     la = inp["log_alpha"].clone()
-    la[:, :, 64:128] *= 2.6
+    la[:, :, 64:128] = -1.1
     la[:, :, 128:192] *= 5.0
     la[:, :, 200:204, : d // 8] = 0.05
     assert float((-la[:, :, 65:128].sum(2)).max()) < 80 < float((-la[:, :, 129:192].sum(2)).max())
