@@ -393,7 +393,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       };
       // Three streams of MMA work, each in chunk order, issued as their inputs
       // become ready (non-blocking tests), so that no stream waits behind
-      // another's inputs:
+      // another's inputs; the oldest work is tested first (P V releases a
+      // stage for the next loads):
       //   P^T of chunk kp: its operands prepared; its TMEM buffer was read by
       //     the P epilogue of chunk kp - 2, whose P V has been issued;
       //   chain step kc (O = Qt S_c, S += Kt^T V): after P^T of kc, so that
@@ -405,11 +406,18 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       uint32_t idle = 0;
       while (ok && km < nc) {
         bool did = false;
-        if (kp < nc && kp <= km + 1 && mbar_test(&prep[kp % NST], (kp / NST) & 1)) {
+        if (km < kc && mbar_test(&p_ready[km % NP], (km / NP) & 1)) {
           tc_fence_after();
-          issue_p(kp);
-          LA_TRACE_EVENT(trace_on, t0, 3, kp);
-          ++kp;
+          const int s = km % NST;
+          const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * (km % NP);
+          const uint32_t o_t = tmem + SM::T_O + D * (km & 1);
+#pragma unroll
+          for (int kk = 0; kk < CH / 16; ++kk)  // O += P V
+            mma_bf16_w(o_t, at(dMN, po + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_pv, 1u);
+          mma_commit(&o_full[km & 1]);
+          mma_commit(&empty[s]);
+          LA_TRACE_EVENT(trace_on, t0, 5, km);
+          ++km;
           did = true;
         }
         if (kc < kp && mbar_test(s_ready, kc & 1) &&
@@ -433,18 +441,11 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           ++kc;
           did = true;
         }
-        if (km < kc && mbar_test(&p_ready[km % NP], (km / NP) & 1)) {
+        if (kp < nc && kp <= km + 1 && mbar_test(&prep[kp % NST], (kp / NST) & 1)) {
           tc_fence_after();
-          const int s = km % NST;
-          const uint32_t vo = s * SM::STAGE + 2 * SM::TILE, po = SM::OFF_P + 8192 * (km % NP);
-          const uint32_t o_t = tmem + SM::T_O + D * (km & 1);
-#pragma unroll
-          for (int kk = 0; kk < CH / 16; ++kk)  // O += P V
-            mma_bf16_w(o_t, at(dMN, po + 2048 * kk), at(dMN, vo + 2048 * kk), HI, id_pv, 1u);
-          mma_commit(&o_full[km & 1]);
-          mma_commit(&empty[s]);
-          LA_TRACE_EVENT(trace_on, t0, 5, km);
-          ++km;
+          issue_p(kp);
+          LA_TRACE_EVENT(trace_on, t0, 3, kp);
+          ++kp;
           did = true;
         }
         if (did) {
