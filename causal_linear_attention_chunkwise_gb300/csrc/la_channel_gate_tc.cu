@@ -81,11 +81,11 @@ constexpr uint32_t BAR_PREP = 1, BAR_EPI = 2, BAR_ST = 3;
 template <int D>
 struct CgSmem {
   // d = 64 has room for two log decay tiles, loaded by TMA ahead of PREP (LAPF).
-  static constexpr int NST = D == 64 ? 3 : 2;   // q | k | v stages
+  static constexpr int NST = D == 64 ? 4 : 2;   // q | k | v stages
   static constexpr bool LAPF = D == 64;
   static constexpr int NX = D == 64 ? 2 : 1;    // Qt and K^(I) buffers
   static constexpr int NP = D == 64 ? 2 : 1;    // bf16 P tiles
-  static constexpr int NO = D == 64 ? 2 : 1;    // O staging tiles
+  static constexpr int NO = 1;                  // O staging tile (d = 64: room for a fourth stage)
   static constexpr uint32_t TILE = 64 * D * 2;  // [64 tokens][D] bf16 in D/64 boxes of 8 KB
   static constexpr uint32_t STAGE = 3 * TILE;
   // K^(I) region: K^(0) rows 0..15, K^(1) 16..47, K^(2) 48..95, K^(3)
