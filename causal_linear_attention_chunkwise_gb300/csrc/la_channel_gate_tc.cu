@@ -1205,8 +1205,10 @@ cg_segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
 // cost per chunk relative to the output pass's (share, measured): f chunks of
 // output take as long as f chunks of state pass plus a later segment's g,
 // i.e. g = (1 - share) f.  At d = 64 the state pass cuts each segment into
-// two pieces, two blocks per SM, which halves its share.
-constexpr double kStateShare64 = 0.25, kStateShare128 = 0.3;
+// two pieces run side by side, which lowers its share.  Measured best: 0.4 at
+// d = 64 with two segments, 0.25 with more (the later segments also fold
+// more states), 0.3 at d = 128.
+constexpr double kStateShare64Two = 0.4, kStateShare64 = 0.25, kStateShare128 = 0.3;
 struct CgPlan {
   int n_chunks, first_chunks, seg_chunks, n_seg, state_parts, n_slot;
 };
@@ -1214,7 +1216,7 @@ CgPlan cg_plan(int B, int H, int L, int D) {
   const int nc = (L + CH - 1) / CH, BH = B * H;
   const int ns = std::max(1, std::min(sm_count() / std::max(1, BH), nc / 8));
   if (ns <= 1) return CgPlan{nc, nc, nc, 1, 1, 1};
-  const double share = D == 64 ? kStateShare64 : kStateShare128;
+  const double share = D == 64 ? (ns == 2 ? kStateShare64Two : kStateShare64) : kStateShare128;
   const double f = nc / (1.0 + (1.0 - share) * (ns - 1));
   const int first = std::max(1, std::min(nc - 1, (int)std::lround(f)));
   const int g = (nc - first + ns - 2) / (ns - 1);
