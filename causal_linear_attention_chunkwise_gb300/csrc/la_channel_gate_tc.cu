@@ -83,7 +83,7 @@ struct CgSmem {
   // d = 64 has room for two log decay tiles, loaded by TMA ahead of PREP (LAPF).
   static constexpr int NST = D == 64 ? 4 : 2;   // q | k | v stages
   static constexpr bool LAPF = D == 64;
-  static constexpr int NX = D == 64 ? 2 : 1;    // Qt and K^(I) buffers
+  static constexpr int NX = D == 64 ? 2 : 1;    // X buffers: Qt and K^(I) (blocks), or Ko
   static constexpr int NP = D == 64 ? 2 : 1;    // bf16 P tiles
   static constexpr int NO = 1;                  // O staging tile (d = 64: room for a fourth stage)
   static constexpr uint32_t TILE = 64 * D * 2;  // [64 tokens][D] bf16 in D/64 boxes of 8 KB
@@ -94,7 +94,7 @@ struct CgSmem {
   // form keeps its Ko in rows 0..63.
   static constexpr int KROWS = 160;
   static constexpr uint32_t KBOX = KROWS * 128;  // one 64-channel box of the region
-  static constexpr uint32_t XBUF = TILE + (D / 64) * KBOX;  // Qt, then the K^(I) region
+  static constexpr uint32_t XBUF = TILE + (D / 64) * KBOX;  // Qt, then the K^(I) region (Ko: rows 0..63)
   static constexpr uint32_t S_BLOCK = D * 128;              // [D][64] bf16 block of S
   static constexpr uint32_t OFF_X = NST * STAGE;
   static constexpr uint32_t OFF_P = OFF_X + NX * XBUF;      // [64 keys][64 queries] bf16
@@ -243,7 +243,7 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM::OFF_BAR);
   uint64_t *empty = full + NST;
   uint64_t *prep = empty + NST;     // [NST] scaled operands, factors and flag ready
-  uint64_t *xfree = prep + NST;     // [NX] the MMAs reading Qt and K^(I) are done
+  uint64_t *xfree = prep + NST;     // [NX] the MMAs reading an X buffer are done
   uint64_t *p_full = xfree + NX;    // [2] P^T in TMEM
   uint64_t *p_ready = p_full + 2;   // [NP] bf16 P in shared memory
   uint64_t *o_full = p_ready + NP;  // [2] O complete in TMEM
@@ -397,8 +397,8 @@ channel_gate_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // stage for the next loads):
       //   P^T of chunk kp: its operands prepared; its TMEM buffer was read by
       //     the P epilogue of chunk kp - 2, whose P V has been issued;
-      //   chain step kc (O = Qt S_c, S += Kt^T V): after P^T of kc, so that
-      //     the commit freeing Qt and K^(I) covers it; O's buffer read;
+      //   chain step kc (O = Qt S_c, or Qo diag(e^m) S_c, S += Kt^T V): after P^T of kc, so that
+      //     the commit freeing the X buffer covers it; O's buffer read;
       //   P V of chunk km: after its chain step (which starts O).
       int kp = 0, kc = 0, km = 0;
       bool ok = true;
