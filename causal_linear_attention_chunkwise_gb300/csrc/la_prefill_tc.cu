@@ -35,9 +35,10 @@
 // runs, and waits for it (griddepcontrol.wait) before reading what it wrote.
 //
 // The non-causal form O = phi(Q) (phi(K)^T V) ("adv13 - Linear Attention /
-// SSM" section 4.3) reuses the segment-state kernel over every chunk and the
-// scan, which sums the segments into one extra slot, then runs
-// noncausal_output_kernel.
+// SSM" section 4.3) reuses the segment-state kernel over every chunk, then
+// runs noncausal_output_kernel.  At d = 64 its blocks sum a sequence's
+// segment states themselves; at d = 128 (four times the bytes per state) the
+// scan sums them into one extra slot first.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
@@ -1696,19 +1697,41 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     tma_prefetch_desc(&tmO);
     for (int i = 0; i < min(n, NQ); ++i) load_q(i);  // Q does not depend on S
   }
-  // S, the scan's last slot of a sequence, is written by the kernel before
-  // this one (a programmatic dependent launch): wait for it once.  load_s
-  // converts sequence bh's S to the bf16 B operand, MN-major with the
-  // 128-byte swizzle; every thread calls it, after every MMA that read the
-  // previous S has completed.
+  // The segments' own states (slots 1 .. n_seg - 1 of a sequence) or, at
+  // d = 128, their sum (the scan's last slot) are written by the kernel
+  // before this one (a programmatic dependent launch): wait for them once.
+  // load_s forms sequence bh's S and converts it to the bf16 B operand,
+  // MN-major with the 128-byte swizzle; every thread calls it, after every
+  // MMA that read the previous S has completed.  At d = 64 the block that
+  // holds the sequence's first chunk also writes S, fp32, to S_final.
   pdl_wait_previous();
-  auto load_s = [&](int bh) {
-    const float *S = p.ws_state + ((size_t)bh * p.n_seg + (p.n_seg - 1)) * D * D;
+  constexpr bool FOLD = D == 64;
+  auto load_s = [&](int bh, bool write_final) {
+    const float *slots = p.ws_state + (size_t)bh * p.n_seg * D * D;
+    float *fin = FOLD && write_final && p.S_final ? p.S_final + (size_t)bh * D * D : nullptr;
     unsigned char *sb = smem + SM::OFF_S;
     for (int idx = tid; idx < D * D / 8; idx += kNcThreads) {
       const int i = idx / (D / 8), j0 = (idx % (D / 8)) * 8;
-      const float4 x = *reinterpret_cast<const float4 *>(S + (size_t)i * D + j0);
-      const float4 y = *reinterpret_cast<const float4 *>(S + (size_t)i * D + j0 + 4);
+      float4 x, y;
+      if constexpr (FOLD) {
+        x = make_float4(0.f, 0.f, 0.f, 0.f);
+        y = x;
+        for (int sg = 1; sg < p.n_seg; ++sg) {
+          const float *S = slots + (size_t)sg * D * D + (size_t)i * D + j0;
+          const float4 a = *reinterpret_cast<const float4 *>(S);
+          const float4 b = *reinterpret_cast<const float4 *>(S + 4);
+          x = make_float4(x.x + a.x, x.y + a.y, x.z + a.z, x.w + a.w);
+          y = make_float4(y.x + b.x, y.y + b.y, y.z + b.z, y.w + b.w);
+        }
+      } else {
+        const float *S = slots + (size_t)(p.n_seg - 1) * D * D + (size_t)i * D + j0;
+        x = *reinterpret_cast<const float4 *>(S);
+        y = *reinterpret_cast<const float4 *>(S + 4);
+      }
+      if (fin) {
+        *reinterpret_cast<float4 *>(fin + (size_t)i * D + j0) = x;
+        *reinterpret_cast<float4 *>(fin + (size_t)i * D + j0 + 4) = y;
+      }
       *reinterpret_cast<uint4 *>(sb + (j0 / 64) * SM::S_BLOCK + i * 128 +
                                  ((((j0 % 64) >> 3) ^ (i & 7)) << 4)) =
           make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y),
@@ -1739,7 +1762,7 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
     consumed = i + 1;
     if (item_bh(i) != s_bh) {
       s_bh = item_bh(i);
-      load_s(s_bh);
+      load_s(s_bh, item_c(i) == 0);
     }
     if constexpr (PHI) {
       tile_pass<D, 1, true, false>(smem + s * SM::TILE, [](int, int) { return 1.f; }, tid,
@@ -1818,7 +1841,9 @@ noncausal_output_kernel(const __grid_constant__ CUtensorMap tmQ,
 }
 
 // Segments of the non-causal state pass: G <= 32 chunks, and about two
-// segment-state blocks per SM.  The scan adds one slot, the sum of all.
+// segment-state blocks per SM.  Slot s + 1 takes segment s's state; at
+// d = 128 the scan turns the slots into prefix sums (slot 0 = 0), the last
+// one the sum of all.
 Plan make_noncausal_plan(int B, int H, int L) {
   const int nc = (L + CH - 1) / CH;
   const int bh = std::max(1, B * H);
@@ -1845,7 +1870,8 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
   p.BH = BH;
   p.n_chunks = pl.n_chunks;
   p.seg_chunks = pl.seg_chunks;
-  p.n_seg = slots;  // segments 0..NS-1 cover every chunk; slot NS receives the sum
+  p.n_seg = slots;  // segments 0..NS-1 cover every chunk; segment s writes slot s + 1
+  p.S_final = a.S;  // d = 64: the sum, written by the output kernel
   p.phi = a.phi;
   p.decay_kind = LA_DECAY_NONE;
   p.err = device_error_word();
@@ -1870,13 +1896,15 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
     if (why) *why = "la_noncausal_fwd: segment-state kernel launch";
     return e;
   }
-  const int n4 = D * D / 4;
-  e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, D, slots,
-                 (const float *)nullptr, (const float *)nullptr, p.ws_state,
-                 (const float *)p.ws_logdec);
-  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
-    if (why) *why = "la_noncausal_fwd: state-scan kernel launch";
-    return e;
+  if constexpr (D != 64) {  // the scan sums the segments into the last slot
+    const int n4 = D * D / 4;
+    e = launch_pdl(state_scan_kernel, dim3((n4 + 255) / 256, BH), 256, 0, a.stream, D, D, slots,
+                   (const float *)nullptr, (const float *)nullptr, p.ws_state,
+                   (const float *)p.ws_logdec);
+    if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) {
+      if (why) *why = "la_noncausal_fwd: state-scan kernel launch";
+      return e;
+    }
   }
   using NS_ = NcSmem<D>;
   auto kn = noncausal_output_kernel<D, PHI>;
@@ -1891,7 +1919,7 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
     if (why) *why = "la_noncausal_fwd: output kernel launch";
     return e;
   }
-  if (a.S) {  // the sum slot of every sequence
+  if (D != 64 && a.S) {  // the sum slot of every sequence
     e = cudaMemcpy2DAsync(a.S, (size_t)D * D * sizeof(float),
                           p.ws_state + (size_t)pl.n_seg * D * D,
                           (size_t)slots * D * D * sizeof(float), (size_t)D * D * sizeof(float),
