@@ -11,8 +11,13 @@
 //   P_ij  = sum_c q_ic k_jc e^{Lam_ic - Lam_jc},
 //   S_c+1 = diag(e^{Lam_end}) S_c + sum_j (k_j * e^{Lam_end - Lam_j}) v_j^T.
 // The decay sits inside P's channel sum, so it cannot be applied to P after
-// the product.  The chunk's 64 tokens form four query blocks of 16 (the
-// secondary chunking of gated linear attention): block I takes the reference
+// the product.  A chunk each of whose parts (8 or 16 tokens) falls by at most
+// its share of kChunkSpanMax takes one reference m_c per channel (the middle
+// of Lam_c's range):  P_ij = (q_i e^{Lam_i - m}) . (k_j e^{m - Lam_j}), every
+// factor within e^{40}, one MMA P^T = Ko Qo^T (M 64 keys, N 64 queries), and
+// Qo doubles as the inter term's operand against diag(e^m) S_c.  Other chunks
+// form four query blocks of 16 (the secondary chunking of gated linear
+// attention): block I takes the reference
 // r_I = Lam at its first token, and its scores against every key j up to its
 // own last token are one product of scaled operands,
 //   P[I, j] = (q_i * e^{Lam_i - r_I}) . (k_j * e^{r_I - Lam_j}),
@@ -25,14 +30,18 @@
 // token on average) would overflow those factors: its key factors are capped,
 // and its 16 x 16 diagonal scores are recomputed exactly on the CUDA cores.
 //
-// Per chunk the MMAs are (D = d_k = d_v):
-//   P^T_I = K^(I) Qh_I^T                 M 64, N 16, K D   (x4)
-//   O     = Qt S_c,  Qt_i = q_i e^{Lam_i} M 64, N D,  K D
+// Per chunk the MMAs are (D = d_k = d_v; blocked form, the one-reference
+// form in brackets):
+//   P^T_I = K^(I) Qh_I^T                 M 64, N 16, K D   (x4)  [Ko Qo^T, N 64]
+//   O     = Qt S_c,  Qt_i = q_i e^{Lam_i} M 64, N D,  K D   [Qo diag(e^m) S_c]
 //   S    += Kt^T V,  Kt_j = k_j e^{Lam_end - Lam_j}   M D, N D, K 64
 //   O    += P V                          M 64, N D,  K 64
-// and the state chain (a warpgroup) copies S_c to bf16 for O = Qt S_c and
-// multiplies row c of S by e^{Lam_end,c} in TMEM before the update adds to it.
-// One CTA carries one (b, h) sequence.
+// and the state chain (a warpgroup) copies S_c (row c scaled by e^{m_c} in
+// the one-reference form) to bf16 for the inter term and multiplies row c of
+// S by e^{Lam_end,c} in TMEM before the update adds to it.  One CTA carries
+// one segment of a (b, h) sequence; with a workspace, a state pass first forms
+// the earlier segments' own states, which each segment folds into its
+// incoming state.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
