@@ -1638,7 +1638,7 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why, const float *z0 = n
 // apply phi and run the epilogue.
 template <int D>
 struct NcSmem {
-  static constexpr int NQ = 3;                    // Q stages
+  static constexpr int NQ = D == 64 ? 2 : 3;      // Q stages (d = 64: five blocks per SM)
   static constexpr uint32_t TILE = 64 * D * 2;    // [64][D] bf16 in D/64 boxes
   static constexpr uint32_t S_BLOCK = D * 128;    // [D][64] bf16 block of S, MN-major
   static constexpr uint32_t OFF_S = NQ * TILE;
@@ -1910,7 +1910,7 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
   auto kn = noncausal_output_kernel<D, PHI>;
   static int smem_set_nc[64];
   if ((e = set_smem_once(kn, NS_::BYTES, smem_set_nc)) != cudaSuccess) return e;
-  const int per_sm = D == 64 ? 4 : 2;  // blocks per SM that fit in shared memory
+  const int per_sm = D == 64 ? 5 : 2;  // blocks per SM that fit in shared memory
   const long total = (long)pl.n_chunks * BH, slots_all = (long)per_sm * sm_count();
   const int cpc = (int)std::max(1L, (total + slots_all - 1) / slots_all);
   const int nx = (int)((total + cpc - 1) / cpc);
