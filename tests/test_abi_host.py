@@ -157,6 +157,33 @@ def test_prefill_plan_invariants(lib):
     assert lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 32, 32, 64, 1) == 0
 
 
+def test_channel_gate_plan_invariants(lib):
+    """The per-channel gate's segment plan, seen through its workspace query: with segments,
+    one fp32 state and one log-decay row per slot, and the slots are the state pass's pieces
+    plus a copy of S0 -- at d = 64 each segment but the last in two pieces (2 (NS - 1) + 1
+    slots; the chunks / 8 cap on NS leaves every segment two chunks or more), at d = 128 in
+    one (NS slots) -- for 2 <= NS <= chunks / 8."""
+    for B, H, L in [(4, 16, 4096), (2, 32, 8192), (1, 16, 32768), (2, 16, 4096), (1, 2, 3000),
+                    (8, 16, 2048), (1, 1, 1 << 16), (64, 64, 512)]:
+        for d in (64, 128):
+            ws = lib.la_channel_gate_fwd_workspace_bytes(B, H, L, d, d, 64, 1)
+            if ws == 0:
+                continue
+            bh, nc = B * H, (L + 63) // 64
+            per_slot = bh * (d * d + d) * 4
+            assert ws % per_slot == 0, (B, H, L, d, ws)
+            slots = ws // per_slot
+            if d == 64:
+                assert slots % 2 == 1, (B, H, L, d, slots)
+                n_seg = (slots - 1) // 2 + 1
+            else:
+                n_seg = slots
+            assert 2 <= n_seg <= nc // 8, (B, H, L, d, n_seg)
+    # the tensor-core gate takes bf16, chunk 64, d in {64, 128}: no workspace otherwise
+    assert lib.la_channel_gate_fwd_workspace_bytes(4, 16, 4096, 64, 64, 64, 0) == 0
+    assert lib.la_channel_gate_fwd_workspace_bytes(4, 16, 4096, 32, 32, 64, 1) == 0
+
+
 def test_variant_validation_before_any_device_work(lib):
     """la_normalised_fwd, la_channel_gate_fwd and la_delta_fwd reject bad
     arguments before any device work."""
