@@ -71,6 +71,24 @@ constexpr int kSolveThreads = (W_EPI - W_SOLVE) * 32;
 constexpr uint32_t BAR_PREP = 1, BAR_SOLVE = 2, BAR_EPI = 3, BAR_ST = 4;
 constexpr int kAS = 65;  // fp32 row stride of the solve's A and T (conflict-free columns)
 
+// The MMA issuer's bounded wait.  It polls the phase without a suspend-time
+// hint: a suspended issuer resumed up to ~1 us after the phase it waited for
+// had completed, and each of its waits is on the chunk's critical path.
+static __device__ __noinline__ bool issuer_wait_slow(uint64_t *bar, uint32_t parity, Ctl *ctl,
+                                                     unsigned int *err, uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1; i < kSpinCap; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 0) {
+      if (*(volatile uint32_t *)&ctl->abort) return false;
+      if (global_timer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  atomicExch(&ctl->abort, 1u);
+  record_device_error(err, KID_DELTA_TC, site);
+  return false;
+}
+
 template <int D>
 struct DtSmem {
   static constexpr bool SMALL = D == 64;
@@ -249,7 +267,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
       const uint32_t dMS = smem_desc_sw128_lo(sbase, SM::MBOX);
       auto at = [](uint32_t d, uint32_t off) { return d + (off >> 4); };
       auto w = [&](uint64_t *bar, uint32_t par, uint32_t site) {
-        return wait1(bar, par, ctl, p.err, KID_DELTA_TC, site);
+        return mbar_test(bar, par) || issuer_wait_slow(bar, par, ctl, p.err, site);
       };
       // G = K K^T and P' = Q K^T of chunk c.
       auto issue_g = [&](int c) {
@@ -544,6 +562,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__
           }
         }
         named_bar_sync(BAR_SOLVE, kSolveThreads);
+        if (d < 3) LA_TRACE_EVENT(trace_on && t == 0, t0, 10 + d, c);
       }
       LA_TRACE_EVENT(trace_on && t == 0, t0, 3, c);
       // The T and P tiles were last read by the previous chunk's MMAs.
