@@ -131,17 +131,23 @@ struct TcParams {
 // ================================================================ segment state
 // Shared memory: NST stages of {K tile, V tile}; the segment's suffix log
 // decays; per-stage row weights; barriers.
-template <int D, bool NORM = false>
+template <int D, bool NORM = false, bool DEEP = false>
 struct StateSmem {
-  // The two transform groups take alternate chunks, so the stage count must be
-  // even: stage s is then always used by group s % 2, and every phase of its
-  // barriers is waited on, in order, by that one group.  (With an odd count a
-  // group could wait on a stage whose previous phase belongs to the other
-  // group and has not completed yet; the parity test would then pass early.)
-  // Two stages for D = 128 and six for D = 64 keep the block small enough
-  // for two per SM.
-  static constexpr int NST = D == 128 ? 2 : 6;
-  static_assert(NST % 2 == 0, "stages must alternate between the two transform groups");
+  // The two transform groups take alternate chunks, so the stage count must
+  // be even: stage s is then always used by group s % 2, and every phase of
+  // its barriers is waited on, in order, by that one group.  (With an odd
+  // count a group could wait on a stage whose previous phase belongs to the
+  // other group and has not completed yet; the parity test would then pass
+  // early.)  Two stages for D = 128 (three blocks fit on an SM) and six for
+  // D = 64 (two blocks).
+  // DEEP (D = 128): both groups transform every chunk together, so any count
+  // works, and three stages put 96 KB of K and V in flight per block, at two
+  // blocks per SM: more of the load latency hidden, when the pass fits in one
+  // wave of two blocks per SM.
+  static_assert(!DEEP || D == 128, "the deep form is the d = 128 one");
+  static constexpr bool ALT = !DEEP;
+  static constexpr int NST = DEEP ? 3 : D == 128 ? 2 : 6;
+  static_assert(!ALT || NST % 2 == 0, "stages must alternate between the two transform groups");
   static constexpr uint32_t TILE = 64 * D * 2;
   static constexpr uint32_t STAGE = 2 * TILE;
   // NORM: one constant block of ones (column 0) after the stages, read as the
@@ -158,11 +164,11 @@ struct StateSmem {
 constexpr int kThreadsState = 384;  // warps 0..11: TMA, MMA, -, -, XG0 (4..7), XG1 (8..11)
 constexpr uint32_t BAR_XG0 = 1, BAR_XG1 = 2, BAR_XG = 3;
 
-template <int D, bool PHI, bool DECAY, bool NORM = false>
+template <int D, bool PHI, bool DECAY, bool NORM = false, bool DEEP = false>
 __global__ void __launch_bounds__(kThreadsState, 2)  // two CTAs per SM
 segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, TcParams p) {
-  using SM = StateSmem<D, NORM>;
+  using SM = StateSmem<D, NORM, DEEP>;
   static_assert(!NORM || D == 64, "the normalised form rides the d = 64 kernels");
   constexpr int ZW = NORM ? 16 : 0;
   constexpr uint32_t kTmemCols = NORM ? 128 : D;
@@ -318,21 +324,26 @@ segment_state_kernel(const __grid_constant__ CUtensorMap tmK,
     }
     named_bar_sync(BAR_XG, 256);  // suffix sums visible to both groups
     constexpr bool phi = PHI;
-    for (int c = g; c < nc; c += 2) {
+    // ALT: group g takes chunks g, g + 2, ...; otherwise both groups (256
+    // threads, one barrier) take every chunk.
+    constexpr int NT = SM::ALT ? 128 : 256;
+    const int tx = SM::ALT ? t : tid - WG1 * 32;
+    const uint32_t xbar = SM::ALT ? gbar : BAR_XG;
+    for (int c = SM::ALT ? g : 0; c < nc; c += SM::ALT ? 2 : 1) {
       const int s = c % NST;
-      if (!wait_wg(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, gbar)) break;
-      LA_TRACE_EVENT(st_on && t == 0, st_t0, 1, c);
+      if (!wait_grp<NT>(&full[s], (c / NST) & 1, ctl, p.err, KID_PREFILL_TC_STATE, 3, xbar, tx)) break;
+      LA_TRACE_EVENT(st_on && tx == 0, st_t0, 1, c);
       unsigned char *kt = smem + s * SM::STAGE;
-      LA_TRACE_EVENT(st_on && t == 0, st_t0, 5, c);
+      LA_TRACE_EVENT(st_on && tx == 0, st_t0, 5, c);
       const float *w = suf + (nc - 1 - c) * CH;  // the chunk's tokens (chunks last first)
       if constexpr (phi || scale)
-        tile_pass<D, 1, phi, scale>(kt, [w](int, int r) { return w[r]; }, t, 128);
-      LA_TRACE_EVENT(st_on && t == 0, st_t0, 6, c);
+        tile_pass<D, 1, phi, scale>(kt, [w](int, int r) { return w[r]; }, tx, NT);
+      LA_TRACE_EVENT(st_on && tx == 0, st_t0, 6, c);
       fence_proxy_async_smem();
-      LA_TRACE_EVENT(st_on && (t & 31) == 0, st_t0, 8 + (t >> 5), c);
-      named_bar_sync(gbar, 128);
-      if (t == 0) mbar_arrive(&ready[s]);
-      LA_TRACE_EVENT(st_on && t == 0, st_t0, 2, c);
+      LA_TRACE_EVENT(st_on && (tx & 31) == 0 && tx < 128, st_t0, 8 + (tx >> 5), c);
+      named_bar_sync(xbar, NT);
+      if (tx == 0) mbar_arrive(&ready[s]);
+      LA_TRACE_EVENT(st_on && tx == 0, st_t0, 2, c);
     }
     // Read the accumulated state out of TMEM (group 0) into segment slot s+1.
     if (g == 0 && wait_wg(done, 0, ctl, p.err, KID_PREFILL_TC_STATE, 4, BAR_XG0)) {
@@ -1536,6 +1547,34 @@ size_t ws_bytes_for(int B, int H, int L, int D, int srow) {
   return st + ((bh * pl.n_seg * sizeof(float) + 255) & ~(size_t)255);
 }
 
+// The segment-state pass over grid = (segments, sequences).  At d = 128, when
+// K is transformed (phi or decay weights) and the grid fits in one wave of two
+// blocks per SM, the deep three-stage form, whose two groups share each
+// chunk's transform; else the two-stage form, of which three blocks fit on an
+// SM.  (Measured on B1 H16 L32768: 3.4 us less per call with decay, none
+// without a transform.)
+template <int D, bool PHI, bool DECAY, bool NORM>
+cudaError_t launch_state(dim3 grid, const CUtensorMap &tk, const CUtensorMap &tv,
+                         const TcParams &p, cudaStream_t stream) {
+  cudaError_t e;
+  if constexpr (D == 128 && !NORM && (PHI || DECAY)) {
+    if ((long)grid.x * grid.y <= 2L * sm_count()) {
+      using SS = StateSmem<D, NORM, true>;
+      auto ks = segment_state_kernel<D, PHI, DECAY, NORM, true>;
+      static int smem_set_deep[64];
+      if ((e = set_smem_once(ks, SS::BYTES, smem_set_deep)) != cudaSuccess) return e;
+      ks<<<grid, kThreadsState, SS::BYTES, stream>>>(tk, tv, p);
+      return cudaGetLastError();
+    }
+  }
+  using SS = StateSmem<D, NORM>;
+  auto ks = segment_state_kernel<D, PHI, DECAY, NORM>;
+  static int smem_set_state[64];
+  if ((e = set_smem_once(ks, SS::BYTES, smem_set_state)) != cudaSuccess) return e;
+  ks<<<grid, kThreadsState, SS::BYTES, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
 template <int D, bool PHI, bool DECAY, bool NORM = false>
 cudaError_t launch_d(const PrefillArgs &a, const char **why, const float *z0 = nullptr,
                      float *z_final = nullptr) {
@@ -1571,13 +1610,8 @@ cudaError_t launch_d(const PrefillArgs &a, const char **why, const float *z0 = n
   }
   cudaError_t e;
   if (pl.n_seg > 1) {
-    using SS = StateSmem<D, NORM>;
-    auto ks = segment_state_kernel<D, PHI, DECAY, NORM>;
-    static int smem_set_state[64];
-    e = set_smem_once(ks, SS::BYTES, smem_set_state);
-    if (e != cudaSuccess) return e;
-    ks<<<dim3(pl.n_seg - 1, BH), kThreadsState, SS::BYTES, a.stream>>>(tk, tv, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) {
+    if ((e = launch_state<D, PHI, DECAY, NORM>(dim3(pl.n_seg - 1, BH), tk, tv, p, a.stream)) !=
+        cudaSuccess) {
       if (why) *why = "la_chunk_fwd: segment-state kernel launch";
       return e;
     }
@@ -1887,12 +1921,8 @@ cudaError_t launch_noncausal_d(const NoncausalArgs &a, const char **why) {
     return cudaErrorInvalidValue;
   }
   cudaError_t e;
-  using SS = StateSmem<D>;
-  auto ks = segment_state_kernel<D, PHI, false>;
-  static int smem_set_state[64];
-  if ((e = set_smem_once(ks, SS::BYTES, smem_set_state)) != cudaSuccess) return e;
-  ks<<<dim3(pl.n_seg, BH), kThreadsState, SS::BYTES, a.stream>>>(tk, tv, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) {
+  if ((e = launch_state<D, PHI, false, false>(dim3(pl.n_seg, BH), tk, tv, p, a.stream)) !=
+      cudaSuccess) {
     if (why) *why = "la_noncausal_fwd: segment-state kernel launch";
     return e;
   }
