@@ -1504,13 +1504,14 @@ struct Plan {
 // but the last segment once more; the scan moves the segment states.  The estimate of each
 // kernel is the larger of its wave time -- waves x (fixed CTA cost + chunk
 // steps x step time) -- and its bytes over the HBM bandwidth; step times and
-// fixed costs are measured ones for these kernels on GB300 (microseconds).
+// fixed costs are measured ones for these kernels on GB300 (microseconds; the
+// d = 128 output step is the ~1.45 us per chunk of the traced steady state).
 // G <= 32 bounds the segment-state kernel's suffix table.
 Plan make_plan(int B, int H, int L, int D) {
   const int nc = (L + CH - 1) / CH;
   const bool halves = D == 128;  // one segment per output CTA
   const double bh = (double)B * H, sms = sm_count();
-  const double t_out = halves ? 3.5 : 1.5, t_state = halves ? 0.7 : 0.4;
+  const double t_out = 1.5, t_state = halves ? 0.7 : 0.4;
   const double fill_out = 3.0, fill_state = 2.0, t_launch = 3.0, bw = 6.5e3;  // bytes per us / 1e3
   const double tile = 64.0 * D * 2, state = (double)D * D * 4;
   Plan best{nc, nc, 1};
