@@ -157,6 +157,34 @@ def test_prefill_plan_invariants(lib):
     assert lib.la_chunk_fwd_workspace_bytes(4, 16, 4096, 32, 32, 64, 1) == 0
 
 
+def _prefill_segments(lib, B, H, L, d):
+    ws = lib.la_chunk_fwd_workspace_bytes(B, H, L, d, d, 64, 1)
+    if ws == 0:
+        return 1
+    bh, nc = B * H, (L + 63) // 64
+    ns = [n for n in range(2, nc + 1) if bh * n * d * d * 4 + (bh * n * 4 + 255) // 256 * 256 == ws]
+    assert len(ns) == 1, (B, H, L, d, ws)
+    return ns[0]
+
+
+def test_prefill_plan_picks_the_measured_segment_counts(lib):
+    """The cost model's picks on 152 SMs, at the segment counts that measured fastest on a
+    GB300 when every count within the 32-chunk bound was timed: 19 for B1 H16 L32768 d128
+    (160.6 us against 166.4 at 18 and 191.3 at 20), 4 for B2 H32 L8192 d128 (171.3 us
+    against 175.4 at 7), 4 for B4 H32 L8192 d128, 2 for B8 H32 L4096 d128 and 4 for B1 H64
+    L8192 d128; the d64 workload B4 H16 L4096 keeps 4."""
+    try:
+        import torch
+        if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 152:
+            pytest.skip("the plan depends on the SM count; these picks are for 152 SMs")
+    except ImportError:
+        pass
+    for (B, H, L, d), ns in [((1, 16, 32768, 128), 19), ((2, 32, 8192, 128), 4),
+                             ((4, 32, 8192, 128), 4), ((8, 32, 4096, 128), 2),
+                             ((1, 64, 8192, 128), 4), ((4, 16, 4096, 64), 4)]:
+        assert _prefill_segments(lib, B, H, L, d) == ns, (B, H, L, d)
+
+
 def test_channel_gate_plan_invariants(lib):
     """The per-channel gate's segment plan, seen through its workspace query: with segments,
     one fp32 state and one log-decay row per slot, and the slots are the state pass's pieces
