@@ -108,8 +108,8 @@ def test_multi_chunk_segments_match_oracle(case):
 # Sequences the launcher cuts into segments: a segment-state pass and a scan
 # give each segment its incoming state, and each output CTA interleaves two
 # segments (d = 64).  The shapes cover one-chunk segments, odd segment counts
-# (the last d = 64 CTA has one segment), a short last segment, and both head
-# sizes.
+# (the last d = 64 CTA has one segment), a short last segment, both head
+# sizes, and both forms of the d = 128 state pass with decay.
 SEGMENTED = [
     # (B, H, L, d, phi, decay, s0, sampled pairs or None for all)
     (1, 2, 1000, 64, "elu1", "none", None, None),
@@ -120,6 +120,10 @@ SEGMENTED = [
     (2, 4, 2800, 64, "identity", "logit", 0.1, None),
     (2, 4, 1500, 128, "elu1", "none", 0.1, None),
     (2, 4, 6000, 128, "identity", "logit", 0.1, [(0, 0), (1, 3), (0, 2)]),
+    # 4 segments of 32 chunks x 128 sequences: 384 segment-state blocks, more
+    # than one wave of two per SM, so the d = 128 pass with decay runs in its
+    # two-stage form (three blocks per SM)
+    (4, 32, 8192, 128, "identity", "head", None, [(0, 0), (3, 31), (2, 17)]),
 ]
 
 
